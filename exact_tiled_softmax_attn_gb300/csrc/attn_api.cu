@@ -1,0 +1,371 @@
+// C-ABI layer: argument validation, tensor-map construction, workspace
+// layout, dispatch to the kernels, and the device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "common.cuh"
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+// Device status word shared by every kernel launched through this library.
+__device__ uint32_t g_device_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  int num_sms = 0;
+  uint32_t* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+thread_local int t_last_cuda_error = 0;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+attn_status_t cuda_fail(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return ATTN_ERR_CUDA;
+}
+
+// Per-device facts, resolved once per device with that device current.
+attn_status_t device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  DeviceInfo& di = g_dev[dev];
+  std::call_once(di.once, [&] {
+    di.err = cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (di.err == cudaSuccess) di.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&di.status), g_device_status);
+  });
+  if (di.err != cudaSuccess) return cuda_fail(di.err);
+  *out = &di;
+  return ATTN_OK;
+}
+
+attn_status_t encoder(EncodeTiledFn* fn) {
+  std::call_once(g_encode_once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (!g_encode) return ATTN_ERR_CUDA;
+  *fn = g_encode;
+  return ATTN_OK;
+}
+
+// 3-D bf16 map over a [planes, rows, inner] array, 128-byte swizzled boxes of
+// 128 rows x 64 elements. Rows past `rows` read as zero within each plane.
+attn_status_t make_map(CUtensorMap* m, const void* base, int inner, int rows, int planes) {
+  EncodeTiledFn enc;
+  attn_status_t s = encoder(&enc);
+  if (s != ATTN_OK) return s;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(planes)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 2,
+                                 static_cast<cuuint64_t>(inner) * 2 * static_cast<cuuint64_t>(rows)};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    t_last_cuda_error = static_cast<int>(r);
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+size_t elem_size(attn_dtype_t dt) { return dt == ATTN_BF16 ? 2 : 4; }
+
+struct Range {
+  uintptr_t lo, hi;
+};
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+Range range(const void* p, size_t bytes) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return {lo, lo + bytes};
+}
+
+attn_status_t check_common(int B, int H, int Tq, int Tk, int d, int dv, float scale, int causal, attn_dtype_t dt) {
+  if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || d <= 0 || dv <= 0) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (dt != ATTN_F32 && dt != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (dt == ATTN_F32) {
+    if (d > 128 || dv > 128) return ATTN_ERR_UNSUPPORTED;
+  } else {
+    if (d != dv || (d != 64 && d != 128)) return ATTN_ERR_UNSUPPORTED;
+  }
+  // every index of every tensor must fit the kernels' 64-bit arithmetic and
+  // the per-head row counts must fit int (TMA coordinates are int32)
+  const double elems = static_cast<double>(B) * H * (Tq > Tk ? Tq : Tk) * (d > dv ? d : dv);
+  if (elems > 9.0e15) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+attn_status_t check_ptr(const void* p, size_t bytes, size_t align) {
+  if (bytes == 0) return ATTN_OK;  // empty tensors may be NULL
+  if (p == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(p) % align) return ATTN_ERR_MISALIGNED;
+  return ATTN_OK;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct BwdLayout {
+  size_t d_off, d_bytes, acc_off, acc_bytes, total;
+};
+BwdLayout bwd_layout(int B, int H, int Tq, int d, attn_dtype_t dt, int deterministic) {
+  BwdLayout L{};
+  const size_t rows = static_cast<size_t>(B) * H * Tq;
+  L.d_off = 0;
+  L.d_bytes = rows * sizeof(float);
+  L.acc_off = round_up(L.d_bytes, 256);
+  L.acc_bytes = (dt == ATTN_BF16 && !deterministic) ? rows * d * sizeof(float) : 0;
+  L.total = L.acc_bytes ? L.acc_off + L.acc_bytes : L.d_bytes;
+  return L;
+}
+
+attn_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Tq,
+                       int Tk, int d, int dv, float scale, int causal, attn_dtype_t dtype, int block_n,
+                       void* stream) {
+  attn_status_t s = check_common(B, H, Tq, Tk, d, dv, scale, causal, dtype);
+  if (s != ATTN_OK) return s;
+  const size_t es = elem_size(dtype);
+  const size_t bh = static_cast<size_t>(B) * H;
+  const size_t align = dtype == ATTN_BF16 ? 16 : 4;
+  const size_t bq = bh * Tq * d * es, bk = bh * Tk * d * es, bv = bh * Tk * dv * es, bo = bh * Tq * dv * es,
+               bl = bh * Tq * 4;
+  if ((s = check_ptr(Q, bq, align)) != ATTN_OK) return s;
+  if ((s = check_ptr(K, bk, align)) != ATTN_OK) return s;
+  if ((s = check_ptr(V, bv, align)) != ATTN_OK) return s;
+  if ((s = check_ptr(O, bo, align)) != ATTN_OK) return s;
+  if ((s = check_ptr(LSE, bl, 4)) != ATTN_OK) return s;
+  const Range ro = range(O, bo), rl = range(LSE, bl);
+  for (Range in : {range(Q, bq), range(K, bk), range(V, bv)})
+    if (overlap(ro, in) || overlap(rl, in)) return ATTN_ERR_INVALID_ARG;
+  if (overlap(ro, rl)) return ATTN_ERR_INVALID_ARG;
+  if (bh == 0 || Tq == 0) return ATTN_OK;
+
+  DeviceInfo* di;
+  if ((s = device_info(&di)) != ATTN_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Problem p{B, H, Tq, Tk, d, dv, scale, causal};
+  if (Tk == 0) {
+    cudaError_t e = launch_fill_empty_fwd(p, O, LSE, static_cast<int>(es), st);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+  }
+  LaunchFwd a{};
+  a.p = p;
+  a.Q = Q;
+  a.K = K;
+  a.V = V;
+  a.O = O;
+  a.LSE = LSE;
+  a.status = di->status;
+  a.num_sms = di->num_sms;
+  a.block_n = block_n;
+  a.stream = st;
+  cudaError_t e;
+  if (dtype == ATTN_F32) {
+    e = launch_fwd_f32(a);
+  } else {
+    CUtensorMap mq, mk, mv;
+    if ((s = make_map(&mq, Q, d, Tq, static_cast<int>(bh))) != ATTN_OK) return s;
+    if ((s = make_map(&mk, K, d, Tk, static_cast<int>(bh))) != ATTN_OK) return s;
+    if ((s = make_map(&mv, V, dv, Tk, static_cast<int>(bh))) != ATTN_OK) return s;
+    a.tmQ = &mq;
+    a.tmK = &mk;
+    a.tmV = &mv;
+    e = launch_fwd_bf16(a);
+  }
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+// ---------------------------------------------------------------- self-test
+
+__global__ void wait_timeout_kernel(uint32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_word;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    abort_word = 0u;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    ptx::WaitCtx w{&abort_word, status, 15u};
+    ptx::mbar_wait(&bar, 0u, w, limit_ns);  // nobody arrives: gives up after limit_ns
+  }
+  __syncthreads();
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+attn_status_t attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Tq,
+                       int Tk, int d, int dv, float scale, int causal, attn_dtype_t dtype, void* stream) {
+  return fwd_impl(Q, K, V, O, LSE, B, H, Tq, Tk, d, dv, scale, causal, dtype, 64, stream);
+}
+
+attn_status_t attn_fwd_f32_blocked(const float* Q, const float* K, const float* V, float* O, float* LSE, int B,
+                                   int H, int Tq, int Tk, int d, int dv, float scale, int causal, int block_n,
+                                   void* stream) {
+  if (block_n != 32 && block_n != 64 && block_n != 128) return ATTN_ERR_UNSUPPORTED;
+  return fwd_impl(Q, K, V, O, LSE, B, H, Tq, Tk, d, dv, scale, causal, ATTN_F32, block_n, stream);
+}
+
+size_t attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype,
+                               int deterministic) {
+  if (check_common(B, H, Tq, Tk, d, dv, 1.0f, 0, dtype) != ATTN_OK) return 0;
+  return bwd_layout(B, H, Tq, d, dtype, deterministic).total;
+}
+
+attn_status_t attn_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+                       const void* dO, void* dQ, void* dK, void* dV, int B, int H, int Tq, int Tk, int d, int dv,
+                       float scale, int causal, attn_dtype_t dtype, int deterministic, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  attn_status_t s = check_common(B, H, Tq, Tk, d, dv, scale, causal, dtype);
+  if (s != ATTN_OK) return s;
+  if (deterministic != 0 && deterministic != 1) return ATTN_ERR_INVALID_ARG;
+  const size_t es = elem_size(dtype);
+  const size_t bh = static_cast<size_t>(B) * H;
+  const size_t align = dtype == ATTN_BF16 ? 16 : 4;
+  const size_t bq = bh * Tq * d * es, bk = bh * Tk * d * es, bv = bh * Tk * dv * es, bo = bh * Tq * dv * es,
+               bl = bh * Tq * 4;
+  const void* ins[6] = {Q, K, V, O, LSE, dO};
+  const size_t in_bytes[6] = {bq, bk, bv, bo, bl, bo};
+  for (int i = 0; i < 6; ++i)
+    if ((s = check_ptr(ins[i], in_bytes[i], i == 4 ? 4 : align)) != ATTN_OK) return s;
+  void* outs[3] = {dQ, dK, dV};
+  const size_t out_bytes[3] = {bq, bk, bv};
+  for (int i = 0; i < 3; ++i)
+    if ((s = check_ptr(outs[i], out_bytes[i], align)) != ATTN_OK) return s;
+  const BwdLayout L = bwd_layout(B, H, Tq, d, dtype, deterministic);
+  if (L.total > 0) {
+    if (workspace == nullptr || workspace_bytes < L.total || reinterpret_cast<uintptr_t>(workspace) % 256)
+      return ATTN_ERR_WORKSPACE;
+  }
+  // outputs must not overlap inputs, each other, or the workspace
+  Range ro[4] = {range(dQ, bq), range(dK, bk), range(dV, bv), range(workspace, L.total)};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = 0; j < 6; ++j)
+      if (overlap(ro[i], range(ins[j], in_bytes[j]))) return i == 3 ? ATTN_ERR_WORKSPACE : ATTN_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 4; ++j)
+      if (overlap(ro[i], ro[j])) return ATTN_ERR_INVALID_ARG;
+  }
+  if (bh == 0) return ATTN_OK;
+
+  DeviceInfo* di;
+  if ((s = device_info(&di)) != ATTN_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (Tq == 0 || Tk == 0) {
+    // no (query, key) pair: every gradient is zero
+    if ((e = launch_zero(dQ, bq, st)) == cudaSuccess && (e = launch_zero(dK, bk, st)) == cudaSuccess)
+      e = launch_zero(dV, bv, st);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+  }
+  LaunchBwd a{};
+  a.p = Problem{B, H, Tq, Tk, d, dv, scale, causal};
+  a.Q = Q;
+  a.K = K;
+  a.V = V;
+  a.O = O;
+  a.LSE = LSE;
+  a.dO = dO;
+  a.dQ = dQ;
+  a.dK = dK;
+  a.dV = dV;
+  a.D = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.d_off);
+  a.dQacc = L.acc_bytes ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.acc_off) : nullptr;
+  a.deterministic = deterministic;
+  a.status = di->status;
+  a.num_sms = di->num_sms;
+  a.stream = st;
+  if (dtype == ATTN_F32) {
+    e = launch_bwd_f32(a);
+  } else {
+    CUtensorMap mq, mk, mv, mdo;
+    if ((s = make_map(&mq, Q, d, Tq, static_cast<int>(bh))) != ATTN_OK) return s;
+    if ((s = make_map(&mk, K, d, Tk, static_cast<int>(bh))) != ATTN_OK) return s;
+    if ((s = make_map(&mv, V, dv, Tk, static_cast<int>(bh))) != ATTN_OK) return s;
+    if ((s = make_map(&mdo, dO, dv, Tq, static_cast<int>(bh))) != ATTN_OK) return s;
+    a.tmQ = &mq;
+    a.tmK = &mk;
+    a.tmV = &mv;
+    a.tmdO = &mdo;
+    e = launch_bwd_bf16(a);
+  }
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+attn_status_t attn_device_status(void* stream) {
+  DeviceInfo* di;
+  attn_status_t s = device_info(&di);
+  if (s != ATTN_OK) return s;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  uint32_t v = 0;
+  e = cudaMemcpy(&v, di->status, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const uint32_t zero = 0;
+  e = cudaMemcpy(di->status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (v & ATTN_DEV_TIMEOUT) return ATTN_ERR_TIMEOUT;
+  if (v) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+attn_status_t attn_selftest_wait_timeout(int limit_ms, void* stream) {
+  if (limit_ms < 1 || limit_ms > 5000) return ATTN_ERR_INVALID_ARG;
+  DeviceInfo* di;
+  attn_status_t s = device_info(&di);
+  if (s != ATTN_OK) return s;
+  wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      di->status, static_cast<uint64_t>(limit_ms) * 1000000ull);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+const char* attn_strerror(attn_status_t status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case ATTN_ERR_MISALIGNED: return "misaligned pointer";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case ATTN_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+  }
+  return "unknown status";
+}
+
+int attn_last_cuda_error(void) { return t_last_cuda_error; }
+
+int attn_version(void) { return (1 << 16) | 0; }
+
+}  // extern "C"

@@ -1,0 +1,432 @@
+// bf16 attention forward on tcgen05 tensor cores (sm_103a).
+//
+// Computes, per head, O = softmax(scale * Q K^T) V and LSE = log sum exp(scale
+// * Q K^T) one 128-key tile at a time with an online softmax, never forming
+// the Tq x Tk score matrix ("Tiled attention with an online softmax",
+// section "Task"; "The Hidden Recurrence in Softmax Attention", section
+// "Chunk-wise Mode with Online Softmax Re-scale"). Query tiles are the outer,
+// parallel loop and key tiles the inner, sequential loop (the same page's
+// "inner-outer loop exchange").
+//
+// One persistent CTA per SM walks a causal-aware list of work units. A unit is
+// two 128-row query tiles (256 rows) of one head; both tiles share every K/V
+// tile that TMA brings in. Warp roles (10 warps):
+//   warp 0      TMA producer: lane 0 loads Q and K, lane 1 loads V
+//   warp 1      MMA issuer (lane 0); also allocates and frees TMEM
+//   warps 2-5   softmax group for query tile 0 (one thread per query row)
+//   warps 6-9   softmax group for query tile 1
+// TMEM (512 columns): tile t keeps its score tile S_t at columns [256t, 256t+128)
+// and its accumulator O_t at [256t+128, 256t+128+dv). The softmax threads write
+// P_t (bf16) over the first 64 columns of S_t, and the PV product reads it from
+// there as the A operand. MMAs issued by one thread execute in order, so the
+// next S_t product (which overwrites P_t) starts after the PV that reads it.
+//
+// Online softmax per query row, in log2 units s2 = s * scale * log2(e):
+//   m_tile = max_j s2_j
+//   if m_tile > m_used + TAU: rescale l and O by 2^(m_used - m_new), m_used = m_new
+//   p_j = 2^(s2_j - m_used), l += sum p_j, O += P V
+// Skipping the rescale while the running max grows by less than TAU keeps
+// every p_j <= 2^TAU and leaves O/l and m_used + log2 l exact. A row with no
+// allowed key yet uses 0 in place of m_used inside the exponentials (the
+// page's -inf rule), so its p, l and O stay 0.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace fwd {
+
+constexpr int BM = 128;          // query rows per tile
+constexpr int BN = 128;          // keys per tile
+constexpr int BOX_BYTES = 128 * 64 * 2;   // one TMA box: 128 rows x 64 bf16 (128-byte swizzle span)
+constexpr float TAU = 8.0f;      // lazy-rescale threshold in log2 units
+constexpr int NUM_THREADS = 320;
+
+template <int HD>
+struct Cfg {
+  static constexpr int KB = HD / 64;                   // 64-column swizzle blocks per row
+  static constexpr int TILE = BM * HD * 2;             // bytes of one 128-row tile
+  static constexpr int NS = (HD == 128) ? 2 : 4;       // K/V pipeline stages
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + 2 * TILE;
+  static constexpr int OFF_V = OFF_K + NS * TILE;
+  static constexpr int OFF_BAR = OFF_V + NS * TILE;
+  // barriers: q_full, q_empty, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS],
+  //           s_full[2], p_full[2], o_full[2], drain
+  static constexpr int NBAR = 2 + 4 * NS + 7;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16;
+  static constexpr uint32_t IDESC_S = ptx::idesc_bf16(BM, BN, false, false);
+  static constexpr uint32_t IDESC_PV = ptx::idesc_bf16(BM, HD, false, true);
+};
+
+struct Params {
+  Problem p;
+  __nv_bfloat16* O;
+  float* LSE;
+  uint32_t* status;
+  UnitOrder order;
+  int n_kv_tiles;
+  float sc2;   // scale * log2(e)
+};
+
+__device__ __forceinline__ void tile_counts(const Params& P, int qb, int* n0, int* n1) {
+  const int nkb = P.n_kv_tiles;
+  if (P.p.causal) {
+    *n0 = min(2 * qb + 1, nkb);
+    *n1 = min(2 * qb + 2, nkb);
+  } else {
+    *n0 = nkb;
+    *n1 = nkb;
+  }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const Params P) {
+  using C = Cfg<HD>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if ((ptx::smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicOr(P.status, ATTN_DEV_BAD_SMEM);
+    return;
+  }
+
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;
+  uint64_t* k_empty = k_full + C::NS;
+  uint64_t* v_full = k_empty + C::NS;
+  uint64_t* v_empty = v_full + C::NS;
+  uint64_t* s_full = v_empty + C::NS;   // [2]
+  uint64_t* p_full = s_full + 2;        // [2]
+  uint64_t* o_full = p_full + 2;        // [2]
+  uint64_t* drain = o_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(q_full, 1);
+    ptx::mbar_init(q_empty, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      ptx::mbar_init(k_full + s, 1);
+      ptx::mbar_init(k_empty + s, 1);
+      ptx::mbar_init(v_full + s, 1);
+      ptx::mbar_init(v_empty + s, 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(s_full + t, 1);
+      ptx::mbar_init(p_full + t, 128);
+      ptx::mbar_init(o_full + t, 1);
+    }
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int grid = gridDim.x;
+  const int cta = blockIdx.x;
+
+  if (warp == 0 && lane < 2) {
+    // ------------------------------------------------------------ producer
+    ptx::WaitCtx w{abort_flag, P.status, 1u + lane};
+    const bool is_qk = (lane == 0);
+    if (is_qk) {
+      ptx::tma_prefetch_desc(&tmQ);
+      ptx::tma_prefetch_desc(&tmK);
+    } else {
+      ptx::tma_prefetch_desc(&tmV);
+    }
+    uint32_t kv_it = 0, u_it = 0;
+    bool ok = true;
+    int bh, qb;
+    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qb); ++round) {
+      int n0, n1;
+      tile_counts(P, qb, &n0, &n1);
+      if (is_qk) {
+        if (!(ok = ptx::mbar_wait(q_empty, (u_it & 1u) ^ 1u, w))) break;
+        ptx::mbar_arrive_expect_tx(q_full, 2 * C::TILE);
+        for (int t = 0; t < 2; ++t)
+          for (int b = 0; b < C::KB; ++b)
+            ptx::tma_load_3d(sQ + t * C::TILE + b * BOX_BYTES, &tmQ, q_full, b * 64, (2 * qb + t) * BM, bh);
+      }
+      for (int j = 0; j < n1; ++j, ++kv_it) {
+        const int st = kv_it % C::NS;
+        const uint32_t ph = (kv_it / C::NS) & 1u;
+        uint64_t* empty = is_qk ? k_empty + st : v_empty + st;
+        uint64_t* full = is_qk ? k_full + st : v_full + st;
+        uint8_t* dst = is_qk ? sK + st * C::TILE : sV + st * C::TILE;
+        const CUtensorMap* map = is_qk ? &tmK : &tmV;
+        if (!(ok = ptx::mbar_wait(empty, ph ^ 1u, w))) break;
+        ptx::mbar_arrive_expect_tx(full, C::TILE);
+        for (int b = 0; b < C::KB; ++b) ptx::tma_load_3d(dst + b * BOX_BYTES, map, full, b * 64, j * BN, bh);
+      }
+      ++u_it;
+    }
+    if (!ok) {
+      // Let the copies already in flight land before the CTA exits.
+      for (uint32_t n = (kv_it > (uint32_t)C::NS ? kv_it - C::NS : 0u); n < kv_it; ++n)
+        ptx::mbar_wait_drain((is_qk ? k_full : v_full) + n % C::NS, (n / C::NS) & 1u);
+      if (is_qk && u_it > 0) ptx::mbar_wait_drain(q_full, (u_it - 1) & 1u);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    ptx::WaitCtx w{abort_flag, P.status, 3u};
+    const uint32_t sQa = ptx::smem_u32(sQ), sKa = ptx::smem_u32(sK), sVa = ptx::smem_u32(sV);
+    auto mma_S = [&](int t, int st) {
+      const uint32_t d = tmem + t * 256;
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
+        const uint64_t a = ptx::sdesc_sw128(sQa + t * C::TILE + off, 16, 1024);
+        const uint64_t b = ptx::sdesc_sw128(sKa + st * C::TILE + off, 16, 1024);
+        ptx::mma_ss(d, a, b, C::IDESC_S, kk > 0 ? 1u : 0u);
+      }
+    };
+    auto mma_PV = [&](int t, int st, bool acc) {
+      const uint32_t d = tmem + t * 256 + 128;
+      const uint32_t a = tmem + t * 256;  // P_t, bf16 pairs in the first 64 columns of S_t
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk) {
+        const uint64_t b = ptx::sdesc_sw128(sVa + st * C::TILE + kk * 2048, BOX_BYTES, 1024);
+        ptx::mma_ts(d, a + kk * 8, b, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+      }
+    };
+    uint32_t kv_it = 0, u_it = 0, pp[2] = {0u, 0u};
+    bool ok = true;
+    int bh, qb;
+    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qb); ++round) {
+      int n0, n1;
+      tile_counts(P, qb, &n0, &n1);
+      if (!(ok = ptx::mbar_wait(q_full, u_it & 1u, w))) break;
+      {
+        const int st = kv_it % C::NS;
+        if (!(ok = ptx::mbar_wait(k_full + st, (kv_it / C::NS) & 1u, w))) break;
+        ptx::tc_fence_after();
+        mma_S(0, st);
+        ptx::mma_commit(s_full + 0);
+        mma_S(1, st);
+        ptx::mma_commit(s_full + 1);
+        ptx::mma_commit(k_empty + st);
+      }
+      for (int j = 0; j < n1; ++j) {
+        const uint32_t it = kv_it + j, itn = it + 1;
+        const int st = it % C::NS, stn = itn % C::NS;
+        const uint32_t phn = (itn / C::NS) & 1u;
+        if (!(ok = ptx::mbar_wait(v_full + st, (it / C::NS) & 1u, w))) break;
+        if (j < n0) {
+          if (!(ok = ptx::mbar_wait(p_full + 0, pp[0] & 1u, w))) break;
+          ++pp[0];
+          ptx::tc_fence_after();
+          mma_PV(0, st, j > 0);
+          if (j == n0 - 1) {
+            ptx::mma_commit(o_full + 0);
+          } else {
+            if (!(ok = ptx::mbar_wait(k_full + stn, phn, w))) break;
+            ptx::tc_fence_after();
+            mma_S(0, stn);
+            ptx::mma_commit(s_full + 0);
+          }
+        }
+        if (!(ok = ptx::mbar_wait(p_full + 1, pp[1] & 1u, w))) break;
+        ++pp[1];
+        ptx::tc_fence_after();
+        mma_PV(1, st, j > 0);
+        if (j == n1 - 1) ptx::mma_commit(o_full + 1);
+        ptx::mma_commit(v_empty + st);
+        if (j + 1 < n1) {
+          if (!(ok = ptx::mbar_wait(k_full + stn, phn, w))) break;
+          ptx::tc_fence_after();
+          mma_S(1, stn);
+          ptx::mma_commit(s_full + 1);
+          ptx::mma_commit(k_empty + stn);
+        }
+      }
+      if (!ok) break;
+      ptx::mma_commit(q_empty);
+      kv_it += n1;
+      ++u_it;
+    }
+    if (!ok) {
+      ptx::mma_commit(drain);
+      ptx::mbar_wait_drain(drain, 0u);
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ softmax
+    const int t = (warp - 2) >> 2;          // query tile of this group
+    const int quad = warp & 3;              // TMEM lane quadrant of this warp
+    const int r = quad * 32 + lane;         // row within the tile
+    const uint32_t tS = tmem + (static_cast<uint32_t>(quad * 32) << 16) + t * 256;
+    const uint32_t tO = tS + 128;
+    ptx::WaitCtx w{abort_flag, P.status, 4u + t};
+    const float sc2 = P.sc2;
+    const int Tq = P.p.Tq, Tk = P.p.Tk;
+    uint32_t sp = 0, op = 0;
+    bool ok = true;
+    int bh, qb;
+    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qb); ++round) {
+      int n0, n1;
+      tile_counts(P, qb, &n0, &n1);
+      const int nt = t ? n1 : n0;
+      const int qt = 2 * qb + t;
+      const int q_row = qt * BM + r;
+      float m_used = -CUDART_INF_F, l = 0.f;
+      for (int j = 0; j < nt; ++j) {
+        // every lane must agree before the warp-wide tcgen05 loads
+        if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(s_full + t, sp & 1u, w)))) break;
+        ++sp;
+        ptx::tc_fence_after();
+        uint32_t raw[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, raw[c]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld_wait(raw[c]);
+        float* s = reinterpret_cast<float*>(&raw[0][0]);
+        const int kv0 = j * BN;
+        const bool diag = P.p.causal && (kv0 + BN - 1 > qt * BM);
+        if (diag || kv0 + BN > Tk) {
+          const int lim = min(Tk - kv0, P.p.causal ? q_row - kv0 + 1 : BN);  // keys [0, lim) allowed
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (i >= lim) s[i] = -CUDART_INF_F;
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+        mx *= sc2;
+        const float m_new = fmaxf(m_used, mx);
+        // Lazy rescale: move the reference max only when it grows by > TAU.
+        bool need = false;
+        float corr = 1.0f;
+        if (j == 0) {
+          m_used = m_new;
+        } else if (m_new > m_used + TAU) {
+          need = true;
+          corr = ptx::ex2(m_used - m_new);   // 0 when m_used = -inf
+          l *= corr;
+          m_used = m_new;
+        }
+        const float ref = (m_used == -CUDART_INF_F) ? 0.f : m_used;   // the -inf rule
+        float lsum = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float p0 = ptx::ex2(fmaf(s[64 * h + 2 * i], sc2, -ref));
+            const float p1 = ptx::ex2(fmaf(s[64 * h + 2 * i + 1], sc2, -ref));
+            lsum += p0 + p1;
+            pk[i] = ptx::pack_bf16(p0, p1);
+          }
+          ptx::tmem_st32(tS + 32 * h, pk);
+        }
+        l += lsum;
+        if (__any_sync(0xffffffffu, need)) {
+          // O_t *= corr before the next PV product accumulates into it. The
+          // previous PV into O_t is complete: it was issued before the S
+          // product whose completion s_full reported.
+#pragma unroll 1
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tO + c * 32, o);
+            ptx::tmem_ld_wait(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+            ptx::tmem_st32(tO + c * 32, o);
+          }
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(p_full + t);
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(o_full + t, op & 1u, w)))) break;
+      ++op;
+      ptx::tc_fence_after();
+      const float inv_l = (l > 0.f) ? 1.0f / l : 0.f;
+      const bool row_ok = q_row < Tq;
+      __nv_bfloat16* orow = P.O + (static_cast<size_t>(bh) * Tq + (row_ok ? q_row : 0)) * HD;
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t o[32];
+        ptx::tmem_ld32(tO + c * 32, o);
+        ptx::tmem_ld_wait(o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = ptx::pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+      if (row_ok) {
+        P.LSE[static_cast<size_t>(bh) * Tq + q_row] =
+            (l > 0.f) ? (m_used + log2f(l)) * 0.69314718055994530942f : -CUDART_INF_F;
+      }
+      ptx::tc_fence_before();
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int HD>
+cudaError_t launch(const LaunchFwd& a) {
+  using C = Cfg<HD>;
+  Params P;
+  P.p = a.p;
+  P.O = reinterpret_cast<__nv_bfloat16*>(a.O);
+  P.LSE = a.LSE;
+  P.status = a.status;
+  P.n_kv_tiles = (a.p.Tk + BN - 1) / BN;
+  P.order.n_blocks = (a.p.Tq + 2 * BM - 1) / (2 * BM);
+  P.order.n_heads = a.p.B * a.p.H;
+  P.order.heavy_last = a.p.causal ? 1 : 0;
+  P.sc2 = a.p.scale * 1.4426950408889634f;
+  const int units = P.order.count();
+  const int grid = units < a.num_sms ? units : a.num_sms;
+  auto kern = attn_fwd_bf16_kernel<HD>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, NUM_THREADS, C::SMEM, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, P);
+  return cudaGetLastError();
+}
+
+}  // namespace fwd
+
+cudaError_t launch_fwd_bf16(const LaunchFwd& a) {
+  if (a.p.d == 128) return fwd::launch<128>(a);
+  return fwd::launch<64>(a);
+}
+
+size_t fwd_bf16_smem_bytes(int d) { return d == 128 ? fwd::Cfg<128>::SMEM : fwd::Cfg<64>::SMEM; }
+
+}  // namespace attn

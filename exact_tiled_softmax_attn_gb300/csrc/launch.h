@@ -1,0 +1,68 @@
+// Internal launch interface between the C-ABI layer (attn_api.cu) and the
+// kernel translation units. Not installed; the public header is include/attn.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace attn {
+
+struct LaunchFwd {
+  Problem p;
+  const CUtensorMap* tmQ;   // bf16 path only
+  const CUtensorMap* tmK;
+  const CUtensorMap* tmV;
+  const void* Q;
+  const void* K;
+  const void* V;
+  void* O;
+  float* LSE;
+  uint32_t* status;
+  int num_sms;
+  int block_n;              // fp32 path: keys per tile (32, 64 or 128)
+  cudaStream_t stream;
+};
+
+struct LaunchBwd {
+  Problem p;
+  const CUtensorMap* tmQ;   // bf16 path only
+  const CUtensorMap* tmK;
+  const CUtensorMap* tmV;
+  const CUtensorMap* tmdO;
+  const void* Q;
+  const void* K;
+  const void* V;
+  const void* O;
+  const float* LSE;
+  const void* dO;
+  void* dQ;
+  void* dK;
+  void* dV;
+  float* D;                 // [B,H,Tq] workspace
+  float* dQacc;             // [B,H,Tq,d] fp32 workspace (bf16 atomic path), else null
+  int deterministic;
+  uint32_t* status;
+  int num_sms;
+  cudaStream_t stream;
+};
+
+// fp32 (SIMT, fp64 score accumulation)
+cudaError_t launch_fwd_f32(const LaunchFwd& a);
+cudaError_t launch_bwd_f32(const LaunchBwd& a);
+
+// bf16 (tcgen05 / TMA)
+cudaError_t launch_fwd_bf16(const LaunchFwd& a);
+cudaError_t launch_bwd_bf16(const LaunchBwd& a);
+size_t fwd_bf16_smem_bytes(int d);
+
+// shared small kernels
+cudaError_t launch_fill_empty_fwd(const Problem& p, void* O, float* LSE, int elem_bytes, cudaStream_t s);
+cudaError_t launch_zero(void* ptr, size_t bytes, cudaStream_t s);
+// D = rowsum(dO o O) (fp32), optionally zeroing `zero_rows` (rows of `zero_cols` floats).
+cudaError_t launch_bwd_preprocess(const Problem& p, const void* O, const void* dO, int elem_bytes, float* D,
+                                  float* zero_rows, int zero_cols, int num_sms, cudaStream_t s);
+
+}  // namespace attn

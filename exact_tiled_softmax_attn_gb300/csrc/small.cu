@@ -1,0 +1,141 @@
+// Memory-bound helper kernels: the backward preprocess D = rowsum(dO o O),
+// the empty-key forward fill, and a zero fill.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace attn {
+namespace small {
+
+constexpr int NT = 256;
+
+__device__ __forceinline__ float dot16(const uint4& a, const uint4& b, const __nv_bfloat16*) {
+  const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&a);
+  const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&b);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 fx = __bfloat1622float2(x[i]);
+    const float2 fy = __bfloat1622float2(y[i]);
+    s = fmaf(fx.x, fy.x, s);
+    s = fmaf(fx.y, fy.y, s);
+  }
+  return s;
+}
+__device__ __forceinline__ float dot16(const uint4& a, const uint4& b, const float*) {
+  const float* x = reinterpret_cast<const float*>(&a);
+  const float* y = reinterpret_cast<const float*>(&b);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) s = fmaf(x[i], y[i], s);
+  return s;
+}
+
+// D_i = sum_c dO_ic * O_ic ("attention_backprop", section "Gradient of S":
+// ROW_SUM(dL/dO o O); the delta-l term of "The Hidden Recurrence in Softmax
+// Attention", section "Flash Attention Backward Pass"). Each group of LPR
+// lanes reads one row with 16-byte loads; rows are walked grid-stride.
+// Optionally zeroes the matching row of an fp32 accumulator.
+template <typename T>
+__global__ void __launch_bounds__(NT) preprocess_vec(const T* __restrict__ O, const T* __restrict__ dO,
+                                                      float* __restrict__ D, float* __restrict__ zero_rows,
+                                                      int zero_cols, long long rows, int dv) {
+  const int chunks = dv * static_cast<int>(sizeof(T)) / 16;   // 16-byte chunks per row (<= 32)
+  const int lpr = chunks;                                      // lanes per row
+  const int rows_per_warp = 32 / lpr;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / lpr, c = lane - sub * lpr;
+  const long long warp_id = (static_cast<long long>(blockIdx.x) * NT + threadIdx.x) >> 5;
+  const long long n_warps = (static_cast<long long>(gridDim.x) * NT) >> 5;
+  for (long long r0 = warp_id * rows_per_warp; r0 < rows; r0 += n_warps * rows_per_warp) {
+    const long long r = r0 + sub;
+    float s = 0.f;
+    const bool ok = (sub < rows_per_warp) && (r < rows);
+    if (ok) {
+      const uint4 a = reinterpret_cast<const uint4*>(O + r * dv)[c];
+      const uint4 b = reinterpret_cast<const uint4*>(dO + r * dv)[c];
+      s = dot16(a, b, static_cast<const T*>(nullptr));
+    }
+    for (int o = lpr >> 1; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (ok && c == 0) D[r] = s;
+    if (ok && zero_rows) {
+      float4* z = reinterpret_cast<float4*>(zero_rows + r * zero_cols);
+      for (int k = c; k < zero_cols / 4; k += lpr) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+}
+
+// Generic fp32 version (any dv): one warp per row.
+__global__ void __launch_bounds__(NT) preprocess_f32(const float* __restrict__ O, const float* __restrict__ dO,
+                                                      float* __restrict__ D, float* __restrict__ zero_rows,
+                                                      int zero_cols, long long rows, int dv) {
+  const int lane = threadIdx.x & 31;
+  const long long warp_id = (static_cast<long long>(blockIdx.x) * NT + threadIdx.x) >> 5;
+  const long long n_warps = (static_cast<long long>(gridDim.x) * NT) >> 5;
+  for (long long r = warp_id; r < rows; r += n_warps) {
+    float s = 0.f;
+    for (int c = lane; c < dv; c += 32) s = fmaf(O[r * dv + c], dO[r * dv + c], s);
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) D[r] = s;
+    if (zero_rows)
+      for (int c = lane; c < zero_cols; c += 32) zero_rows[r * zero_cols + c] = 0.f;
+  }
+}
+
+__global__ void fill_empty_kernel(uint8_t* O, size_t o_bytes, float* LSE, size_t n_lse) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < o_bytes; i += stride) O[i] = 0;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_lse; i += stride)
+    LSE[i] = -CUDART_INF_F;
+}
+
+__global__ void zero_kernel(uint8_t* p, size_t bytes) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < bytes; i += stride) p[i] = 0;
+}
+
+}  // namespace small
+
+cudaError_t launch_bwd_preprocess(const Problem& p, const void* O, const void* dO, int elem_bytes, float* D,
+                                  float* zero_rows, int zero_cols, int num_sms, cudaStream_t s) {
+  const long long rows = static_cast<long long>(p.B) * p.H * p.Tq;
+  if (rows == 0) return cudaSuccess;
+  const int grid = num_sms * 8;
+  const bool vec = (p.dv * elem_bytes) % 16 == 0 && (p.dv * elem_bytes) / 16 <= 32 &&
+                   ((p.dv * elem_bytes) / 16 & ((p.dv * elem_bytes) / 16 - 1)) == 0 &&
+                   (reinterpret_cast<uintptr_t>(O) % 16 == 0) && (reinterpret_cast<uintptr_t>(dO) % 16 == 0) &&
+                   (zero_rows == nullptr || (zero_cols % 4 == 0 && reinterpret_cast<uintptr_t>(zero_rows) % 16 == 0));
+  if (elem_bytes == 2) {
+    small::preprocess_vec<__nv_bfloat16><<<grid, small::NT, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), D, zero_rows, zero_cols, rows,
+        p.dv);
+  } else if (vec) {
+    small::preprocess_vec<float><<<grid, small::NT, 0, s>>>(static_cast<const float*>(O),
+                                                             static_cast<const float*>(dO), D, zero_rows,
+                                                             zero_cols, rows, p.dv);
+  } else {
+    small::preprocess_f32<<<grid, small::NT, 0, s>>>(static_cast<const float*>(O), static_cast<const float*>(dO),
+                                                      D, zero_rows, zero_cols, rows, p.dv);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_empty_fwd(const Problem& p, void* O, float* LSE, int elem_bytes, cudaStream_t s) {
+  const size_t n_lse = static_cast<size_t>(p.B) * p.H * p.Tq;
+  const size_t o_bytes = n_lse * p.dv * elem_bytes;
+  if (n_lse == 0) return cudaSuccess;
+  small::fill_empty_kernel<<<1024, 256, 0, s>>>(static_cast<uint8_t*>(O), o_bytes, LSE, n_lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero(void* ptr, size_t bytes, cudaStream_t s) {
+  if (bytes == 0) return cudaSuccess;
+  small::zero_kernel<<<1024, 256, 0, s>>>(static_cast<uint8_t*>(ptr), bytes);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,151 @@
+/*
+ * attn.h -- C ABI of the exact tiled softmax attention library (libattn.so).
+ *
+ * Exact scaled-dot-product softmax attention, forward and backward, computed
+ * one key tile at a time with an online softmax, so the Tq x Tk score matrix
+ * is never stored. Kernels are written for NVIDIA sm_103a (GB300).
+ *
+ * Definitions (sources are the pages this library restates):
+ *   S   = scale * Q K^T, with S_ij = -inf where the mask blocks key j for
+ *         query i. causal = 1 blocks j > i with global row indices
+ *         ("Tiled attention with an online softmax", section "Task").
+ *   O   = softmax(S) V                ("The Hidden Recurrence in Softmax
+ *         Attention", section "Standard Attention / Forward Pass";
+ *         "attention_backprop", section "Forward Pass")
+ *   LSE = log sum_j exp(S_ij)         (natural log; the page's m_i + log l_i)
+ *   D   = rowsum(dO o O)
+ *   dV  = P^T dO,  dS = P o (dO V^T - D),  dQ = scale * dS K,
+ *   dK  = scale * dS^T Q              ("attention_backprop", sections
+ *         "Gradient of V and P", "Gradient of S", "Gradient of Q and K";
+ *         the factor scale comes from S = scale * Q K^T)
+ *
+ * Layout: every tensor is a contiguous row-major device array.
+ *   Q [B,H,Tq,d]  K [B,H,Tk,d]  V [B,H,Tk,dv]  O, dO [B,H,Tq,dv]
+ *   dQ [B,H,Tq,d] dK [B,H,Tk,d] dV [B,H,Tk,dv] LSE, D [B,H,Tq] (fp32)
+ * Q, K, V, O, dO, dQ, dK, dV use the element type `dtype`; LSE is always fp32.
+ *
+ * Ownership: the caller allocates and owns every buffer, including the
+ * backward workspace. The library never allocates device memory in these
+ * calls and never writes its inputs. Outputs must not overlap inputs.
+ *
+ * Asynchrony: every call validates its arguments on the host, then enqueues
+ * kernels on `stream` (a cudaStream_t passed as void*; NULL = legacy default
+ * stream) and returns without synchronising. A nonzero status from the host
+ * checks means nothing was enqueued.
+ *
+ * Supported shapes:
+ *   ATTN_F32 : 1 <= d, dv <= 128, any B, H, Tq, Tk >= 0
+ *   ATTN_BF16: d == dv, d in {64, 128}, any B, H, Tq, Tk >= 0
+ * Zero-sized problems are valid: Tk == 0 gives O = 0 and LSE = -inf (a row
+ * with no allowed key), and empty gradients are written as zeros.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,  /* null pointer, negative size, non-finite or non-positive scale, overlap */
+  ATTN_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement (e.g. bf16 with d = 96) */
+  ATTN_ERR_MISALIGNED = 3,   /* a pointer breaks the alignment rule of its dtype (bf16: 16 B, f32: 4 B) */
+  ATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed; see attn_last_cuda_error() */
+  ATTN_ERR_TIMEOUT = 5,      /* a kernel's bounded pipeline wait gave up (reported by attn_device_status) */
+  ATTN_ERR_WORKSPACE = 6     /* workspace missing, too small or not 256-byte aligned */
+} attn_status_t;
+
+typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype_t;
+
+/*
+ * Forward pass: O and LSE from Q, K, V.
+ * Restates flash_attention of "Tiled attention with an online softmax"
+ * (sections "Task", "Input and output") for a batch of heads: returns the
+ * attention output and the log-sum-exp of each query row. `scale` multiplies
+ * Q K^T (the page uses 1/sqrt(d); pass that for the same result) and must be
+ * finite and > 0. `causal` is 0 (no mask) or 1.
+ * Errors: ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_MISALIGNED,
+ * ATTN_ERR_CUDA (launch failure).
+ */
+ATTN_API attn_status_t attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Tq,
+                       int Tk, int d, int dv, float scale, int causal, attn_dtype_t dtype, void* stream);
+
+/*
+ * Forward pass of the fp32 path with an explicit key-tile size (keys per
+ * online-softmax step): block_n in {32, 64, 128}. The result must not depend
+ * on it ("Tiled attention with an online softmax", section "Constraints":
+ * equal to standard attention for every block size). attn_fwd uses 64.
+ * Same arguments and errors as attn_fwd with dtype ATTN_F32.
+ */
+ATTN_API attn_status_t attn_fwd_f32_blocked(const float* Q, const float* K, const float* V, float* O, float* LSE, int B,
+                                   int H, int Tq, int Tk, int d, int dv, float scale, int causal, int block_n,
+                                   void* stream);
+
+/*
+ * Bytes of device workspace attn_bwd needs for this problem (0 is possible).
+ * Holds D [B,H,Tq] fp32 and, for bf16 with deterministic == 0, the fp32 dQ
+ * accumulator [B,H,Tq,d]. Returns 0 for invalid arguments as well.
+ */
+ATTN_API size_t attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype,
+                               int deterministic);
+
+/*
+ * Backward pass: dQ, dK, dV from Q, K, V, the forward's O and LSE, and dO.
+ * Recomputes P tile by tile from LSE instead of storing it ("The Hidden
+ * Recurrence in Softmax Attention", section "Flash Attention Backward Pass":
+ * store the row statistics, recompute the attention matrix per tile), forms
+ * D = rowsum(dO o O), and accumulates the per-tile gradient terms of
+ * "attention_backprop" (sections "Gradient of V and P" through "Gradient of
+ * Q and K"). `O` and `LSE` must be the outputs of attn_fwd on the same
+ * inputs, scale and mask. deterministic = 1 computes dQ in a separate pass
+ * that sums key tiles in a fixed order (bitwise reproducible); 0 adds each
+ * key tile's share with fp32 atomics. `workspace` (256-byte aligned, at least
+ * attn_bwd_workspace_size bytes; may be NULL when that is 0) is scratch
+ * owned by the caller and overwritten.
+ * Errors: as attn_fwd, plus ATTN_ERR_WORKSPACE.
+ */
+ATTN_API attn_status_t attn_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+                       const void* dO, void* dQ, void* dK, void* dV, int B, int H, int Tq, int Tk, int d, int dv,
+                       float scale, int causal, attn_dtype_t dtype, int deterministic, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word that
+ * the kernels set when a bounded wait gives up (ATTN_ERR_TIMEOUT) or a launch
+ * precondition fails on the device (ATTN_ERR_CUDA). ATTN_OK otherwise.
+ * Intended for tests and debugging; it blocks the host.
+ */
+ATTN_API attn_status_t attn_device_status(void* stream);
+
+/*
+ * Test hook for the bounded wait itself: launches one CTA that waits on an
+ * mbarrier nobody arrives at, with a limit of `limit_ms` milliseconds
+ * (1..5000). The kernel gives up, records ATTN_ERR_TIMEOUT in the device
+ * status word and exits normally; the context stays usable. Returns the
+ * launch status; read the outcome with attn_device_status().
+ */
+ATTN_API attn_status_t attn_selftest_wait_timeout(int limit_ms, void* stream);
+
+/* Human-readable text for a status code (static storage). */
+ATTN_API const char* attn_strerror(attn_status_t status);
+
+/* The cudaError_t (as int) of the last ATTN_ERR_CUDA on this thread, else 0. */
+ATTN_API int attn_last_cuda_error(void);
+
+/* Library ABI version: (major << 16) | minor. */
+ATTN_API int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

@@ -1,0 +1,135 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+declared in include/attn.h, and rejects bad arguments on the host before
+touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+import exact_tiled_softmax_attn_gb300 as pkg
+from exact_tiled_softmax_attn_gb300 import binding as B
+from exact_tiled_softmax_attn_gb300 import build as build_mod
+
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return pkg.load_library()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    return set(re.findall(r"ATTN_API\s+[\w\s\*]*?\b(attn_\w+)\s*\(", text))
+
+
+def test_header_declares_the_binding_functions():
+    assert header_functions() == set(B.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+    # nothing but the C ABI is visible
+    out = os.popen(f"nm -D --defined-only {B.LIB_PATH}").read()
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert header_functions() <= exported
+    assert {s for s in exported if s.startswith("attn_")} == header_functions()
+
+
+def test_version_and_strerror(lib):
+    assert pkg.attn_version() >> 16 == 1
+    for s in range(7):
+        assert pkg.attn_strerror(s)
+    assert pkg.attn_strerror(99) == "unknown status"
+
+
+def _fwd(**kw):
+    a = dict(Q=0x10000, K=0x20000, V=0x30000, O=0x40000, LSE=0x50000, B=1, H=1, Tq=8, Tk=8, d=64, dv=64,
+             scale=0.125, causal=0, dtype=B.ATTN_BF16, stream=0, check=False)
+    a.update(kw)
+    return B.attn_fwd(**a)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=-1), B.ATTN_ERR_INVALID_ARG),
+    (dict(Tq=-3), B.ATTN_ERR_INVALID_ARG),
+    (dict(d=0), B.ATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), B.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), B.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), B.ATTN_ERR_INVALID_ARG),
+    (dict(scale=-1.0), B.ATTN_ERR_INVALID_ARG),
+    (dict(causal=2), B.ATTN_ERR_INVALID_ARG),
+    (dict(dtype=7), B.ATTN_ERR_INVALID_ARG),
+    (dict(d=96, dv=96), B.ATTN_ERR_UNSUPPORTED),
+    (dict(d=64, dv=128), B.ATTN_ERR_UNSUPPORTED),
+    (dict(dtype=B.ATTN_F32, d=129), B.ATTN_ERR_UNSUPPORTED),
+    (dict(Q=None), B.ATTN_ERR_INVALID_ARG),
+    (dict(LSE=None), B.ATTN_ERR_INVALID_ARG),
+    (dict(Q=0x10008), B.ATTN_ERR_MISALIGNED),
+    (dict(dtype=B.ATTN_F32, V=0x30002), B.ATTN_ERR_MISALIGNED),
+    (dict(O=0x10000), B.ATTN_ERR_INVALID_ARG),             # output overlaps Q
+    (dict(LSE=0x40010), B.ATTN_ERR_INVALID_ARG),           # LSE overlaps O
+])
+def test_forward_host_validation(lib, kw, status):
+    assert _fwd(**kw) == status
+
+
+def test_empty_problems_need_no_device(lib):
+    # nothing to compute: accepted without any CUDA call (no GPU here)
+    assert _fwd(B=0) == B.ATTN_OK
+    assert _fwd(Tq=0) == B.ATTN_OK
+    assert _fwd(B=0, Q=None, K=None, V=None, O=None, LSE=None) == B.ATTN_OK
+
+
+def test_blocked_forward_validates_block(lib):
+    st = B.attn_fwd_f32_blocked(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 1, 1, 8, 8, 64, 64, 0.1, 0, 48,
+                                stream=0, check=False)
+    assert st == B.ATTN_ERR_UNSUPPORTED
+
+
+def test_workspace_size(lib):
+    f32 = B.attn_bwd_workspace_size(2, 3, 100, 50, 64, 64, B.ATTN_F32, 0)
+    assert f32 == 2 * 3 * 100 * 4
+    bf_det = B.attn_bwd_workspace_size(2, 3, 100, 50, 64, 64, B.ATTN_BF16, 1)
+    assert bf_det == 2 * 3 * 100 * 4
+    bf_atomic = B.attn_bwd_workspace_size(2, 3, 100, 50, 64, 64, B.ATTN_BF16, 0)
+    d_bytes = 2 * 3 * 100 * 4
+    assert bf_atomic == (d_bytes + 255) // 256 * 256 + 2 * 3 * 100 * 64 * 4
+    assert B.attn_bwd_workspace_size(-1, 3, 100, 50, 64, 64, B.ATTN_BF16, 0) == 0
+
+
+def _bwd(**kw):
+    a = dict(Q=0x100000, K=0x200000, V=0x300000, O=0x400000, LSE=0x500000, dO=0x600000, dQ=0x700000,
+             dK=0x800000, dV=0x900000, B=1, H=1, Tq=8, Tk=8, d=64, dv=64, scale=0.125, causal=0,
+             dtype=B.ATTN_BF16, deterministic=0, workspace=0xA00000, workspace_bytes=1 << 20, stream=0,
+             check=False)
+    a.update(kw)
+    return B.attn_bwd(**a)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(deterministic=3), B.ATTN_ERR_INVALID_ARG),
+    (dict(workspace=None), B.ATTN_ERR_WORKSPACE),
+    (dict(workspace_bytes=16), B.ATTN_ERR_WORKSPACE),
+    (dict(workspace=0xA00010), B.ATTN_ERR_WORKSPACE),
+    (dict(workspace=0x100000), B.ATTN_ERR_WORKSPACE),     # workspace overlaps Q
+    (dict(dK=0x700000), B.ATTN_ERR_INVALID_ARG),          # two outputs overlap
+    (dict(dQ=0x600000), B.ATTN_ERR_INVALID_ARG),          # output overlaps dO
+    (dict(dO=None), B.ATTN_ERR_INVALID_ARG),
+    (dict(dV=0x900008), B.ATTN_ERR_MISALIGNED),
+    (dict(d=80, dv=80), B.ATTN_ERR_UNSUPPORTED),
+])
+def test_backward_host_validation(lib, kw, status):
+    assert _bwd(**kw) == status
+
+
+def test_error_text_carries_status(lib):
+    with pytest.raises(B.AttnError) as e:
+        B.attn_fwd(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 1, 1, 8, 8, 96, 96, 0.1, 0, B.ATTN_BF16,
+                   stream=0)
+    assert "unsupported" in str(e.value)

@@ -1,0 +1,93 @@
+"""GPU backward vs the CPU float64 oracle, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_tiled_softmax_attn_gb300 as pkg
+from exact_tiled_softmax_attn_gb300.workloads import WORKLOADS, make_inputs, make_random
+from oracle import attention as ref
+
+from parity import check_grad, check_lse, check_o
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    pkg.load_library()
+    yield
+    assert pkg.attn_device_status() == pkg.ATTN_OK
+
+
+def run(x, causal, scale, deterministic):
+    o, lse = pkg.forward(x["Q"], x["K"], x["V"], causal=causal, scale=scale)
+    dq, dk, dv = pkg.backward(x["Q"], x["K"], x["V"], o, lse, x["dO"], causal=causal, scale=scale,
+                              deterministic=deterministic)
+    torch.cuda.synchronize()
+    return o, lse, dq, dk, dv
+
+
+def check_all(x, causal, scale, dt, deterministic, heads=None):
+    o, lse, dq, dk, dv = run(x, causal, scale, deterministic)
+    r = ref.backward(x["Q"], x["K"], x["V"], x["dO"], scale, causal, heads=heads)
+    sel = (lambda t: t) if heads is None else (lambda t: np.stack([np.asarray(t)[b, h] for b, h in heads]))
+    tsel = (lambda t: t) if heads is None else (lambda t: torch.stack([t[b, h] for b, h in heads]))
+    check_o(tsel(o), sel(r["O"]), dt)
+    check_lse(tsel(lse), sel(r["LSE"]), dt)
+    check_grad(tsel(dq), sel(r["dQ"]), dt, "dQ")
+    check_grad(tsel(dk), sel(r["dK"]), dt, "dK")
+    check_grad(tsel(dv), sel(r["dV"]), dt, "dV")
+
+
+# ------------------------------------------------------------------ fp32
+
+@pytest.mark.parametrize("deterministic", [0, 1])
+@pytest.mark.parametrize("name", ["c1", "c1_causal"])
+def test_f32_c1(name, deterministic):
+    w = WORKLOADS[name]
+    check_all(make_inputs(w, DEV), w.causal, w.softmax_scale, torch.float32, deterministic)
+
+
+F32_SHAPES = [(1, 1, 1, 1, 1, 1), (2, 3, 77, 133, 40, 24), (1, 2, 200, 65, 128, 128), (1, 1, 33, 300, 7, 128)]
+
+
+@pytest.mark.parametrize("deterministic", [0, 1])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", F32_SHAPES)
+def test_f32_ragged(shape, causal, deterministic):
+    B, H, Tq, Tk, d, dv = shape
+    x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, dv), seed=Tq + 2 * Tk, device=DEV)
+    check_all(x, causal, 1 / math.sqrt(d), torch.float32, deterministic)
+
+
+@pytest.mark.parametrize("deterministic", [0, 1])
+@pytest.mark.parametrize("name", ["c4", "c4_scale1"])
+def test_f32_c4_full_size(name, deterministic):
+    w = WORKLOADS[name]
+    check_all(make_inputs(w, DEV), w.causal, w.softmax_scale, torch.float32, deterministic)
+
+
+def test_f32_deterministic_is_bitwise_repeatable():
+    w = WORKLOADS["c1_causal"]
+    x = make_inputs(w.with_(H=3, Tq=300, Tk=300), DEV)
+    a = run(x, True, w.softmax_scale, 1)
+    b = run(x, True, w.softmax_scale, 1)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+
+
+@pytest.mark.parametrize("dt,d", [(torch.float32, 16), (torch.bfloat16, 64)])
+@pytest.mark.parametrize("Tq,Tk", [(0, 5), (5, 0)])
+def test_empty_sides_give_zero_gradients(dt, d, Tq, Tk):
+    x = make_random((1, 2, Tq, d), (1, 2, Tk, d), (1, 2, Tk, d), seed=2, dtype=dt, device=DEV)
+    o, lse = pkg.forward(x["Q"], x["K"], x["V"], causal=False, scale=0.2)
+    dq, dk, dv = [torch.full_like(t, 7.0) for t in (x["Q"], x["K"], x["V"])]
+    ws = torch.empty(1 << 16, dtype=torch.uint8, device=DEV)
+    pkg.attn_bwd(x["Q"], x["K"], x["V"], o, lse, x["dO"], dq, dk, dv, 1, 2, Tq, Tk, d, d, 0.2, 0,
+                 pkg.ATTN_F32 if dt == torch.float32 else pkg.ATTN_BF16, 0, ws, ws.numel())
+    torch.cuda.synchronize()
+    for t in (dq, dk, dv):
+        assert torch.all(t == 0)

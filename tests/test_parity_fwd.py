@@ -1,0 +1,165 @@
+"""GPU forward vs the CPU float64 oracle, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_tiled_softmax_attn_gb300 as pkg
+from exact_tiled_softmax_attn_gb300.workloads import WORKLOADS, make_inputs, make_random
+from oracle import attention as ref
+
+from parity import check_lse, check_o
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    pkg.load_library()
+    yield
+    assert pkg.attn_device_status() == pkg.ATTN_OK
+
+
+def run_fwd(x, causal, scale):
+    o, lse = pkg.forward(x["Q"], x["K"], x["V"], causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def oracle_fwd(x, causal, scale, heads=None):
+    return ref.forward(x["Q"], x["K"], x["V"], scale, causal, heads=heads)
+
+
+# ------------------------------------------------------------------ fp32
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("block_n", [32, 64, 128])
+def test_f32_c1_every_tile_size(causal, block_n):
+    w = WORKLOADS["c1_causal" if causal else "c1"]
+    x = make_inputs(w, DEV)
+    B, H, Tq, Tk, d, dv = w.B, w.H, w.Tq, w.Tk, w.d, w.dv
+    o = torch.empty(B, H, Tq, dv, device=DEV)
+    lse = torch.empty(B, H, Tq, device=DEV)
+    pkg.attn_fwd_f32_blocked(x["Q"], x["K"], x["V"], o, lse, B, H, Tq, Tk, d, dv, w.softmax_scale, causal,
+                             block_n)
+    torch.cuda.synchronize()
+    O, L = oracle_fwd(x, causal, w.softmax_scale)
+    check_o(o, O, torch.float32)
+    check_lse(lse, L, torch.float32)
+
+
+F32_SHAPES = [  # B, H, Tq, Tk, d, dv
+    (1, 1, 1, 1, 1, 1),
+    (2, 3, 77, 133, 40, 24),
+    (1, 2, 200, 65, 128, 128),
+    (1, 1, 33, 300, 7, 128),
+    (3, 1, 64, 64, 64, 64),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", F32_SHAPES)
+def test_f32_ragged_shapes(shape, causal):
+    B, H, Tq, Tk, d, dv = shape
+    x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, dv), seed=Tq + Tk, device=DEV)
+    scale = 1 / math.sqrt(d)
+    o, lse = run_fwd(x, causal, scale)
+    O, L = oracle_fwd(x, causal, scale)
+    check_o(o, O, torch.float32)
+    check_lse(lse, L, torch.float32)
+
+
+@pytest.mark.parametrize("name", ["c4", "c4_scale1"])
+def test_f32_c4_banded_keys_full_size(name):
+    w = WORKLOADS[name]
+    x = make_inputs(w, DEV)
+    o, lse = run_fwd(x, w.causal, w.softmax_scale)
+    O, L = oracle_fwd(x, w.causal, w.softmax_scale)
+    if name == "c4_scale1":
+        assert np.abs(L).max() > 1000      # the logits really pass +-1000
+    check_o(o, O, torch.float32)
+    check_lse(lse, L, torch.float32)
+
+
+# ------------------------------------------------------------------ bf16
+
+BF16_SHAPES = [  # B, H, Tq, Tk, d
+    (1, 1, 1, 1, 64),
+    (2, 3, 300, 300, 64),
+    (1, 2, 257, 129, 128),
+    (1, 1, 128, 1000, 128),
+    (2, 2, 512, 512, 128),
+    (1, 1, 700, 70, 64),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", BF16_SHAPES)
+def test_bf16_ragged_shapes(shape, causal):
+    B, H, Tq, Tk, d = shape
+    x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, d), seed=Tq * 3 + Tk, dtype=torch.bfloat16,
+                    device=DEV)
+    scale = 1 / math.sqrt(d)
+    o, lse = run_fwd(x, causal, scale)
+    O, L = oracle_fwd(x, causal, scale)
+    check_o(o, O, torch.bfloat16)
+    check_lse(lse, L, torch.bfloat16)
+
+
+def test_bf16_large_logits_across_tiles():
+    # scores beyond +-1000 in alternating 128-key bands stay finite and exact
+    B, H, T, d = 1, 2, 640, 128
+    x = make_random((B, H, T, d), (B, H, T, d), (B, H, T, d), seed=5, dtype=torch.float32, device="cpu")
+    sign = torch.where((torch.arange(T) // 128) % 2 == 0, 40.0, -40.0).view(1, 1, T, 1)
+    x = {k: (v * sign if k == "K" else v).to(torch.bfloat16).to(DEV) for k, v in x.items()}
+    for causal in (False, True):
+        o, lse = run_fwd(x, causal, 1.0)
+        O, L = oracle_fwd(x, causal, 1.0)
+        assert np.abs(L).max() > 1000
+        check_o(o, O, torch.bfloat16)
+        check_lse(lse, L, torch.bfloat16)
+
+
+def test_bf16_c2_full_size():
+    w = WORKLOADS["c2"]
+    x = make_inputs(w, DEV)
+    o, lse = run_fwd(x, w.causal, w.softmax_scale)
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    O, L = oracle_fwd(x, w.causal, w.softmax_scale, heads=heads)
+    check_o(o, O, torch.bfloat16)
+    check_lse(lse, L, torch.bfloat16)
+
+
+@pytest.mark.parametrize("name,heads", [("c3", [(0, 0), (1, 15)]), ("c5", [(0, 7)])])
+def test_bf16_full_size_sampled_heads(name, heads):
+    w = WORKLOADS[name]
+    x = make_inputs(w, DEV, with_dO=False)
+    o, lse = run_fwd(x, w.causal, w.softmax_scale)
+    rows = np.unique(np.concatenate([np.arange(0, 200), np.arange(w.Tq - 200, w.Tq),
+                                     np.random.default_rng(0).integers(0, w.Tq, 600)]))
+    for b, h in heads:
+        O, L = ref.forward_head(x["Q"][b, h], x["K"][b, h], x["V"][b, h], w.softmax_scale, w.causal, rows=rows)
+        check_o(o[b, h, rows], O, torch.bfloat16)
+        check_lse(lse[b, h, rows], L, torch.bfloat16)
+
+
+# ------------------------------------------------------------------ edge cases and invariants
+
+@pytest.mark.parametrize("dt,d", [(torch.float32, 32), (torch.bfloat16, 64)])
+def test_no_keys_gives_zero_and_neg_inf(dt, d):
+    x = make_random((2, 2, 5, d), (2, 2, 0, d), (2, 2, 0, d), seed=1, dtype=dt, device=DEV)
+    o, lse = run_fwd(x, False, 0.3)
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+def test_inputs_unchanged_and_repeatable(dt):
+    x = make_random((1, 2, 200, 64), (1, 2, 300, 64), (1, 2, 300, 64), seed=3, dtype=dt, device=DEV)
+    keep = {k: v.clone() for k, v in x.items()}
+    o1, l1 = run_fwd(x, True, 0.125)
+    o2, l2 = run_fwd(x, True, 0.125)
+    for k in x:
+        assert torch.equal(x[k], keep[k]), k
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
