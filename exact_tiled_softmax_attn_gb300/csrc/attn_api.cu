@@ -244,12 +244,17 @@ size_t attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int d, int dv, attn
   return bwd_layout(B, H, Tq, d, dtype, deterministic).total;
 }
 
-attn_status_t attn_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
-                       const void* dO, void* dQ, void* dK, void* dV, int B, int H, int Tq, int Tk, int d, int dv,
-                       float scale, int causal, attn_dtype_t dtype, int deterministic, void* workspace,
-                       size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace attn {
+namespace {
+attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO,
+                       void* dQ, void* dK, void* dV, int B, int H, int Tq, int Tk, int d, int dv, float scale,
+                       int causal, attn_dtype_t dtype, int deterministic, void* workspace, size_t workspace_bytes,
+                       int phase, void* stream) {
   attn_status_t s = check_common(B, H, Tq, Tk, d, dv, scale, causal, dtype);
   if (s != ATTN_OK) return s;
+  if (phase < 0 || phase > 3) return ATTN_ERR_INVALID_ARG;
   if (deterministic != 0 && deterministic != 1) return ATTN_ERR_INVALID_ARG;
   const size_t es = elem_size(dtype);
   const size_t bh = static_cast<size_t>(B) * H;
@@ -285,6 +290,7 @@ attn_status_t attn_bwd(const void* Q, const void* K, const void* V, const void* 
   cudaError_t e = cudaSuccess;
   if (Tq == 0 || Tk == 0) {
     // no (query, key) pair: every gradient is zero
+    if (phase != 0 && phase != 2) return ATTN_OK;
     if ((e = launch_zero(dQ, bq, st)) == cudaSuccess && (e = launch_zero(dK, bk, st)) == cudaSuccess)
       e = launch_zero(dV, bv, st);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
@@ -303,6 +309,7 @@ attn_status_t attn_bwd(const void* Q, const void* K, const void* V, const void* 
   a.D = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.d_off);
   a.dQacc = L.acc_bytes ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.acc_off) : nullptr;
   a.deterministic = deterministic;
+  a.phase = phase;
   a.status = di->status;
   a.num_sms = di->num_sms;
   a.stream = st;
@@ -321,6 +328,26 @@ attn_status_t attn_bwd(const void* Q, const void* K, const void* V, const void* 
     e = launch_bwd_bf16(a);
   }
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+}  // namespace
+}  // namespace attn
+
+extern "C" {
+
+attn_status_t attn_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+                       const void* dO, void* dQ, void* dK, void* dV, int B, int H, int Tq, int Tk, int d, int dv,
+                       float scale, int causal, attn_dtype_t dtype, int deterministic, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return bwd_impl(Q, K, V, O, LSE, dO, dQ, dK, dV, B, H, Tq, Tk, d, dv, scale, causal, dtype, deterministic,
+                  workspace, workspace_bytes, 0, stream);
+}
+
+attn_status_t attn_bwd_phase(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+                             const void* dO, void* dQ, void* dK, void* dV, int B, int H, int Tq, int Tk, int d,
+                             int dv, float scale, int causal, attn_dtype_t dtype, int deterministic, void* workspace,
+                             size_t workspace_bytes, int phase, void* stream) {
+  return bwd_impl(Q, K, V, O, LSE, dO, dQ, dK, dV, B, H, Tq, Tk, d, dv, scale, causal, dtype, deterministic,
+                  workspace, workspace_bytes, phase, stream);
 }
 
 attn_status_t attn_device_status(void* stream) {

@@ -1,5 +1,866 @@
-// placeholder, replaced by the tcgen05 backward
+// bf16 attention backward on tcgen05 tensor cores (sm_103a).
+//
+// Recomputes P tile by tile from the stored log-sum-exp instead of keeping
+// it ("The Hidden Recurrence in Softmax Attention", section "Flash Attention
+// Backward Pass"), and forms the gradient terms of "attention_backprop"
+// (sections "Gradient of V and P", "Gradient of S", "Gradient of Q and K"):
+//   D  = rowsum(dO o O)                        (preprocess kernel)
+//   P  = exp(scale * Q K^T - LSE)
+//   dV = P^T dO,   dP = dO V^T,   dS = P o (dP - D)
+//   dK = scale * dS^T Q,          dQ = scale * dS K
+//
+// dK/dV kernel: one persistent CTA per SM; a work unit is one 128-key tile of
+// one head, and the CTA loops over the query tiles that can see it. K and V
+// stay in shared memory for the whole unit; Q, dO (TMA) and LSE, D (plain
+// loads) stream through a two-stage ring. Warp roles (12 warps, 3 warpgroups):
+//   warp 0      producer (lane 0 issues TMA; all lanes stage LSE and D)
+//   warp 1      MMA issuer (lane 0); allocates and frees TMEM
+//   warps 2-3   idle (they complete the first warpgroup's register release)
+//   warps 4-7   P / dS group: one thread per key row of the tile
+//   warps 8-11  dQ group: adds each dQ tile into the fp32 accumulator, then
+//               writes dK and dV at the end of the unit
+// The first warpgroup gives up registers (setmaxnreg) so the P / dS group,
+// which keeps a packed row of P^T in registers, can hold 224 per thread
+// (112 + 224 + 168 per thread of each warpgroup = the launch's 384 x 168).
+// TMEM (512 columns): dV [0,128), dK [128,256), S^T [256,384), dP^T [384,512).
+// Per query tile the MMA warp issues
+//   S^T  = K Q^T        (A = K, B = Q, both K-major in smem)
+//   dP^T = V dO^T       (A = V, B = dO)
+//   dV  += P^T dO       (A = P^T bf16 in TMEM over S^T, B = dO MN-major)
+//   dK  += dS^T Q       (A = dS^T bf16 in TMEM over dP^T, B = Q MN-major)
+//   dQ   = dS K         (A = dS from smem, MN-major; B = K MN-major) -> over dP^T
+// The last product is skipped in deterministic mode, where a separate dQ
+// kernel (one CTA per query tile looping over key tiles in a fixed order)
+// accumulates dQ in TMEM and writes it once.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "common.cuh"
 #include "launch.h"
+#include "ptx.cuh"
+
 namespace attn {
-cudaError_t launch_bwd_bf16(const LaunchBwd&) { return cudaErrorNotSupported; }
+namespace bwd {
+
+constexpr int BT = 128;                   // rows per tile (keys and queries)
+constexpr int BOX_BYTES = 128 * 64 * 2;   // one TMA box: 128 rows x 64 bf16
+constexpr int NUM_THREADS = 384;         // dK/dV kernel: three warpgroups
+constexpr int REG_CTRL = 112;             // producer / MMA warpgroup
+constexpr int REG_PDS = 224;             // P / dS warpgroup
+constexpr int REG_LAUNCH = 168;          // 65536 / 384, what the launch bound gives
+constexpr float LOG2E = 1.4426950408889634f;
+
+// Unit order: 0 = head-major, 1 = heavy (large block index) first,
+// 2 = heavy (small block index) first.
+struct Order {
+  int n_blocks, n_heads, mode;
+  __device__ bool unit(int cta, int grid, int round, int* bh, int* blk) const {
+    const int base = round * grid;
+    const int total = n_blocks * n_heads;
+    if (base >= total) return false;
+    const int x = base + ((round & 1) ? (grid - 1 - cta) : cta);
+    if (x >= total) return false;
+    if (mode == 0) {
+      *bh = x / n_blocks;
+      *blk = x % n_blocks;
+    } else if (mode == 1) {
+      *blk = n_blocks - 1 - x / n_heads;
+      *bh = x % n_heads;
+    } else {
+      *blk = x / n_heads;
+      *bh = x % n_heads;
+    }
+    return true;
+  }
+};
+
+struct Params {
+  Problem p;
+  const float* LSE;
+  const float* D;
+  float* dQacc;            // atomic path: fp32 [BH, Tq, d], pre-zeroed
+  __nv_bfloat16* dQ;       // deterministic path output
+  __nv_bfloat16* dK;
+  __nv_bfloat16* dV;
+  uint32_t* status;
+  Order order;
+  int n_q_tiles, n_k_tiles;
+  float sc2;               // scale * log2(e)
+};
+
+// Query tiles [first, first + count) that see key tile kb.
+__device__ __forceinline__ void q_range(const Params& P, int kb, int* first, int* count) {
+  const int f = P.p.causal ? kb : 0;
+  *first = f;
+  *count = P.n_q_tiles > f ? P.n_q_tiles - f : 0;
 }
+
+// Byte offset of element (row, col) inside a 128-row tile stored as 64-column
+// boxes with the 128-byte swizzle (the layout TMA writes and the MMA reads).
+__device__ __forceinline__ uint32_t sw128_offset(int row, int col) {
+  return (col >> 6) * BOX_BYTES + (row >> 3) * 1024 + (row & 7) * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) +
+         (col & 7) * 2;
+}
+
+template <int HD>
+struct CfgKV {
+  static constexpr int KB = HD / 64;
+  static constexpr int TILE = BT * HD * 2;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + TILE;
+  static constexpr int OFF_Q = OFF_V + TILE;          // [2]
+  static constexpr int OFF_DO = OFF_Q + 2 * TILE;     // [2]
+  static constexpr int OFF_DS = OFF_DO + 2 * TILE;    // dS, 128 q x 128 keys bf16, MN-major
+  static constexpr int DS_BYTES = BT * BT * 2;
+  static constexpr int OFF_LSE = OFF_DS + DS_BYTES;   // [2][128] fp32 (LSE * log2 e, +inf = no key)
+  static constexpr int OFF_D = OFF_LSE + 2 * BT * 4;  // [2][128] fp32
+  static constexpr int OFF_BAR = OFF_D + 2 * BT * 4;
+  // kv_full, kv_empty, q_full[2], q_empty[2], s_full, dp_full, p_full, ds_full,
+  // dq_full, dq_free, acc_full, acc_free, drain
+  static constexpr int NBAR = 15;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16;
+  static constexpr uint32_t IDESC_S = ptx::idesc_bf16(BT, BT, false, false);
+  static constexpr uint32_t IDESC_ACC = ptx::idesc_bf16(BT, HD, false, true);   // dV, dK (A in TMEM)
+  static constexpr uint32_t IDESC_DQ = ptx::idesc_bf16(BT, HD, true, true);     // dQ = dS K
+};
+
+template <int HD, bool ATOMIC_DQ>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                const Params P) {
+  using C = CfgKV<HD>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if ((ptx::smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicOr(P.status, ATTN_DEV_BAD_SMEM);
+    return;
+  }
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sdO = smem + C::OFF_DO;
+  uint8_t* sdS = smem + C::OFF_DS;
+  float* sLSE = reinterpret_cast<float*>(smem + C::OFF_LSE);
+  float* sD = reinterpret_cast<float*>(smem + C::OFF_D);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* kv_empty = bars + 1;
+  uint64_t* q_full = bars + 2;    // [2]
+  uint64_t* q_empty = bars + 4;   // [2]
+  uint64_t* s_full = bars + 6;
+  uint64_t* dp_full = bars + 7;
+  uint64_t* p_full = bars + 8;
+  uint64_t* ds_full = bars + 9;
+  uint64_t* dq_full = bars + 10;
+  uint64_t* dq_free = bars + 11;
+  uint64_t* acc_full = bars + 12;
+  uint64_t* acc_free = bars + 13;
+  uint64_t* drain = bars + 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(kv_full, 1);
+    ptx::mbar_init(kv_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(q_full + s, 1);
+      ptx::mbar_init(q_empty + s, 1);
+    }
+    ptx::mbar_init(s_full, 1);
+    ptx::mbar_init(dp_full, 1);
+    ptx::mbar_init(p_full, 128);
+    ptx::mbar_init(ds_full, 128);
+    ptx::mbar_init(dq_full, 1);
+    ptx::mbar_init(dq_free, 128);
+    ptx::mbar_init(acc_full, 1);
+    ptx::mbar_init(acc_free, 128);
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t T_DV = 0, T_DK = 128, T_ST = 256, T_DP = 384;
+
+  const int grid = gridDim.x, cta = blockIdx.x;
+  const int Tq = P.p.Tq, Tk = P.p.Tk;
+
+  const int wg = warp >> 2;
+  if (wg == 0) {
+   ptx::reg_release<REG_CTRL>();
+   if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    ptx::WaitCtx w{abort_flag, P.status, 1u};
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tmQ);
+      ptx::tma_prefetch_desc(&tmK);
+      ptx::tma_prefetch_desc(&tmV);
+      ptx::tma_prefetch_desc(&tmdO);
+    }
+    uint32_t u_it = 0, q_it = 0;
+    bool ok = true;
+    int bh, kb;
+    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &kb); ++round) {
+      int q0, nq;
+      q_range(P, kb, &q0, &nq);
+      if (nq == 0) continue;
+      if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(kv_empty, (u_it & 1u) ^ 1u, w)))) break;
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
+        for (int b = 0; b < C::KB; ++b) {
+          ptx::tma_load_3d(sK + b * BOX_BYTES, &tmK, kv_full, b * 64, kb * BT, bh);
+          ptx::tma_load_3d(sV + b * BOX_BYTES, &tmV, kv_full, b * 64, kb * BT, bh);
+        }
+      }
+      for (int ii = 0; ii < nq; ++ii, ++q_it) {
+        const int st = q_it & 1;
+        const uint32_t ph = (q_it >> 1) & 1u;
+        if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(q_empty + st, ph ^ 1u, w)))) break;
+        const int qt = q0 + ii;
+        // LSE (as log2 units; +inf where the row has no key or is past Tq) and D
+        for (int r = lane; r < BT; r += 32) {
+          const int q = qt * BT + r;
+          float l2 = CUDART_INF_F, dd = 0.f;
+          if (q < Tq) {
+            const float lse = P.LSE[static_cast<size_t>(bh) * Tq + q];
+            l2 = (lse == -CUDART_INF_F) ? CUDART_INF_F : lse * LOG2E;
+            dd = P.D[static_cast<size_t>(bh) * Tq + q];
+          }
+          sLSE[st * BT + r] = l2;
+          sD[st * BT + r] = dd;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(q_full + st, 2 * C::TILE);
+          for (int b = 0; b < C::KB; ++b) {
+            ptx::tma_load_3d(sQ + st * C::TILE + b * BOX_BYTES, &tmQ, q_full + st, b * 64, qt * BT, bh);
+            ptx::tma_load_3d(sdO + st * C::TILE + b * BOX_BYTES, &tmdO, q_full + st, b * 64, qt * BT, bh);
+          }
+        }
+      }
+      ++u_it;
+    }
+    if (!ok && lane == 0) {
+      if (u_it > 0 || q_it > 0) ptx::mbar_wait_drain(kv_full, u_it & 1u);
+      for (uint32_t n = (q_it > 2u ? q_it - 2u : 0u); n < q_it; ++n) ptx::mbar_wait_drain(q_full + (n & 1), (n >> 1) & 1u);
+    }
+   } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    ptx::WaitCtx w{abort_flag, P.status, 2u};
+    const uint32_t aK = ptx::smem_u32(sK), aV = ptx::smem_u32(sV), aQ = ptx::smem_u32(sQ),
+                   adO = ptx::smem_u32(sdO), adS = ptx::smem_u32(sdS);
+    auto kmaj = [](uint32_t base, int kk) {  // K-major operand, k-step kk of 16 elements
+      return ptx::sdesc_sw128(base + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
+    };
+    auto mnmaj = [](uint32_t base, int kk) {  // MN-major operand, k-step kk of 16 rows
+      return ptx::sdesc_sw128(base + kk * 2048, BOX_BYTES, 1024);
+    };
+    auto mma_st = [&](int st) {
+      for (int kk = 0; kk < HD / 16; ++kk)
+        ptx::mma_ss(tmem + T_ST, kmaj(aK, kk), kmaj(aQ + st * C::TILE, kk), C::IDESC_S, kk > 0);
+    };
+    auto mma_dpt = [&](int st) {
+      for (int kk = 0; kk < HD / 16; ++kk)
+        ptx::mma_ss(tmem + T_DP, kmaj(aV, kk), kmaj(adO + st * C::TILE, kk), C::IDESC_S, kk > 0);
+    };
+    uint32_t u_it = 0, q_it = 0, pp = 0, dqf = 0;
+    bool ok = true;
+    int bh, kb;
+    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &kb); ++round) {
+      int q0, nq;
+      q_range(P, kb, &q0, &nq);
+      if (nq == 0) continue;
+      if (!(ok = ptx::mbar_wait(kv_full, u_it & 1u, w))) break;
+      if (!(ok = ptx::mbar_wait(acc_free, (u_it & 1u) ^ 1u, w))) break;
+      {
+        const int st = q_it & 1;
+        if (!(ok = ptx::mbar_wait(q_full + st, (q_it >> 1) & 1u, w))) break;
+        ptx::tc_fence_after();
+        mma_st(st);
+        ptx::mma_commit(s_full);
+        if (ATOMIC_DQ && dqf > 0) {
+          if (!(ok = ptx::mbar_wait(dq_free, (dqf - 1) & 1u, w))) break;
+          ptx::tc_fence_after();
+        }
+        mma_dpt(st);
+        ptx::mma_commit(dp_full);
+      }
+      for (int ii = 0; ii < nq; ++ii) {
+        const uint32_t it = q_it + ii;
+        const int st = it & 1, stn = (it + 1) & 1;
+        // dV += P^T dO
+        if (!(ok = ptx::mbar_wait(p_full, pp & 1u, w))) break;
+        ptx::tc_fence_after();
+        for (int kk = 0; kk < BT / 16; ++kk)
+          ptx::mma_ts(tmem + T_DV, tmem + T_ST + kk * 8, mnmaj(adO + st * C::TILE, kk), C::IDESC_ACC,
+                      (ii > 0 || kk > 0) ? 1u : 0u);
+        // next S^T (overwrites P^T only after the product above has read it)
+        if (ii + 1 < nq) {
+          if (!(ok = ptx::mbar_wait(q_full + stn, ((it + 1) >> 1) & 1u, w))) break;
+          ptx::tc_fence_after();
+          mma_st(stn);
+          ptx::mma_commit(s_full);
+        }
+        // dK += dS^T Q
+        if (!(ok = ptx::mbar_wait(ds_full, pp & 1u, w))) break;
+        ++pp;
+        ptx::tc_fence_after();
+        for (int kk = 0; kk < BT / 16; ++kk)
+          ptx::mma_ts(tmem + T_DK, tmem + T_DP + kk * 8, mnmaj(aQ + st * C::TILE, kk), C::IDESC_ACC,
+                      (ii > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(q_empty + st);
+        if (ATOMIC_DQ) {
+          // dQ = dS K into the dP^T columns
+          for (int kk = 0; kk < BT / 16; ++kk)
+            ptx::mma_ss(tmem + T_DP, mnmaj(adS, kk), mnmaj(aK, kk), C::IDESC_DQ, kk > 0);
+          ptx::mma_commit(dq_full);
+          ++dqf;
+        }
+        if (ii + 1 < nq) {
+          if (ATOMIC_DQ) {
+            if (!(ok = ptx::mbar_wait(dq_free, (dqf - 1) & 1u, w))) break;
+            ptx::tc_fence_after();
+          }
+          mma_dpt(stn);
+          ptx::mma_commit(dp_full);
+        }
+      }
+      if (!ok) break;
+      ptx::mma_commit(acc_full);
+      ptx::mma_commit(kv_empty);
+      q_it += nq;
+      ++u_it;
+    }
+    if (!ok) {
+      ptx::mma_commit(drain);
+      ptx::mbar_wait_drain(drain, 0u);
+    }
+   }
+  } else if (wg == 1) {
+    ptx::reg_acquire<REG_PDS>();
+    // ------------------------------------------------------------ P / dS (thread = key row)
+    const int quad = warp & 3;
+    const int j = quad * 32 + lane;                 // key row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tST = tmem + lane_off + T_ST, tDP = tmem + lane_off + T_DP;
+    ptx::WaitCtx w{abort_flag, P.status, 3u};
+    const float sc2 = P.sc2;
+    uint32_t q_it = 0, sp = 0;
+    bool ok = true;
+    int bh, kb;
+    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &kb); ++round) {
+      int q0, nq;
+      q_range(P, kb, &q0, &nq);
+      if (nq == 0) continue;
+      const int key = kb * BT + j;
+      const bool key_ok = key < Tk;
+      for (int ii = 0; ii < nq; ++ii, ++q_it, ++sp) {
+        const int st = q_it & 1;
+        const int qt = q0 + ii;
+        const float* lse2 = sLSE + st * BT;
+        const float* dd = sD + st * BT;
+        // the staged LSE / D of this tile are visible once q_full completed
+        if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(q_full + st, (q_it >> 1) & 1u, w)))) break;
+        if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(s_full, sp & 1u, w)))) break;
+        ptx::tc_fence_after();
+        // pass 1: P^T_j,q = 2^(s * scale * log2e - LSE2_q), masked; stored bf16 over S^T.
+        // The packed values stay in registers for pass 2: once p_full is
+        // signalled the MMA warp may overwrite S^T with the next tile's scores.
+        const int lim = P.p.causal ? key - qt * BT : 0;   // q index (within tile) below which P = 0
+        uint32_t pkeep[4][16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          ptx::tmem_ld32(tST + c * 32, r);
+          ptx::tmem_ld_wait(r);
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
+            const int qa = c * 32 + 2 * i;
+            const float4 l4 = ptx::lds128(lse2 + qa);
+            float p0 = ptx::ex2(fmaf(__uint_as_float(r[2 * i]), sc2, -l4.x));
+            float p1 = ptx::ex2(fmaf(__uint_as_float(r[2 * i + 1]), sc2, -l4.y));
+            float p2 = ptx::ex2(fmaf(__uint_as_float(r[2 * i + 2]), sc2, -l4.z));
+            float p3 = ptx::ex2(fmaf(__uint_as_float(r[2 * i + 3]), sc2, -l4.w));
+            if (qa < lim || !key_ok) p0 = 0.f;
+            if (qa + 1 < lim || !key_ok) p1 = 0.f;
+            if (qa + 2 < lim || !key_ok) p2 = 0.f;
+            if (qa + 3 < lim || !key_ok) p3 = 0.f;
+            pkeep[c][i] = ptx::pack_bf16(p0, p1);
+            pkeep[c][i + 1] = ptx::pack_bf16(p2, p3);
+          }
+          ptx::tmem_st16(tST + c * 16, pkeep[c]);
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(p_full);
+        // pass 2: dS^T_j,q = P^T (dP^T - D_q); bf16 over dP^T and into smem (dS, MN-major)
+        if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dp_full, sp & 1u, w)))) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          ptx::tmem_ld32(tDP + c * 32, r);
+          ptx::tmem_ld_wait(r);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
+            const int qa = c * 32 + 2 * i;
+            const float4 d4 = ptx::lds128(dd + qa);
+            const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pkeep[c][i]));
+            const float2 pg = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pkeep[c][i + 1]));
+            pk[i] = ptx::pack_bf16(pf.x * (__uint_as_float(r[2 * i]) - d4.x), pf.y * (__uint_as_float(r[2 * i + 1]) - d4.y));
+            pk[i + 1] = ptx::pack_bf16(pg.x * (__uint_as_float(r[2 * i + 2]) - d4.z),
+                                       pg.y * (__uint_as_float(r[2 * i + 3]) - d4.w));
+          }
+          ptx::tmem_st16(tDP + c * 16, pk);
+          // dS is MN-major for the dQ product: row = key j, column = query
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint32_t off = sw128_offset(j, c * 32 + v * 8);
+            *reinterpret_cast<uint4*>(sdS + off) = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+        ptx::tmem_st_wait();
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(ds_full);
+      }
+    }
+  } else if (wg == 2) {
+    // ------------------------------------------------------------ dQ adds; dK / dV epilogue
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;                 // TMEM lane = row
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    ptx::WaitCtx w{abort_flag, P.status, 4u};
+    const float scale = P.p.scale;
+    uint32_t u_it = 0, dqf = 0;
+    bool ok = true;
+    int bh, kb;
+    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &kb); ++round) {
+      int q0, nq;
+      q_range(P, kb, &q0, &nq);
+      const int key = kb * BT + r;
+      const bool key_ok = key < Tk;
+      __nv_bfloat16* dk_row = P.dK + (static_cast<size_t>(bh) * Tk + (key_ok ? key : 0)) * HD;
+      __nv_bfloat16* dv_row = P.dV + (static_cast<size_t>(bh) * Tk + (key_ok ? key : 0)) * HD;
+      if (nq == 0) {
+        if (key_ok) {
+          for (int c = 0; c < HD / 8; ++c) {
+            reinterpret_cast<uint4*>(dk_row)[c] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4*>(dv_row)[c] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        continue;
+      }
+      if (ATOMIC_DQ) {
+        for (int ii = 0; ii < nq; ++ii, ++dqf) {
+          if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dq_full, dqf & 1u, w)))) break;
+          ptx::tc_fence_after();
+          const int q = (q0 + ii) * BT + r;
+          float* acc = P.dQacc + (static_cast<size_t>(bh) * Tq + (q < Tq ? q : 0)) * HD;
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t v[32];
+            ptx::tmem_ld32(tmem + lane_off + T_DP + c * 32, v);
+            ptx::tmem_ld_wait(v);
+            if (q < Tq) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                ptx::red_add_v4(acc + c * 32 + 4 * e, __uint_as_float(v[4 * e]) * scale,
+                                __uint_as_float(v[4 * e + 1]) * scale, __uint_as_float(v[4 * e + 2]) * scale,
+                                __uint_as_float(v[4 * e + 3]) * scale);
+            }
+          }
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(dq_free);
+        }
+        if (!ok) break;
+      }
+      if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(acc_full, u_it & 1u, w)))) break;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t v[32], k[32];
+        ptx::tmem_ld32(tmem + lane_off + T_DV + c * 32, v);
+        ptx::tmem_ld32(tmem + lane_off + T_DK + c * 32, k);
+        ptx::tmem_ld_wait(v);
+        ptx::tmem_ld_wait(k);
+        if (key_ok) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint4 a, b;
+            a.x = ptx::pack_bf16(__uint_as_float(v[8 * e + 0]), __uint_as_float(v[8 * e + 1]));
+            a.y = ptx::pack_bf16(__uint_as_float(v[8 * e + 2]), __uint_as_float(v[8 * e + 3]));
+            a.z = ptx::pack_bf16(__uint_as_float(v[8 * e + 4]), __uint_as_float(v[8 * e + 5]));
+            a.w = ptx::pack_bf16(__uint_as_float(v[8 * e + 6]), __uint_as_float(v[8 * e + 7]));
+            b.x = ptx::pack_bf16(__uint_as_float(k[8 * e + 0]) * scale, __uint_as_float(k[8 * e + 1]) * scale);
+            b.y = ptx::pack_bf16(__uint_as_float(k[8 * e + 2]) * scale, __uint_as_float(k[8 * e + 3]) * scale);
+            b.z = ptx::pack_bf16(__uint_as_float(k[8 * e + 4]) * scale, __uint_as_float(k[8 * e + 5]) * scale);
+            b.w = ptx::pack_bf16(__uint_as_float(k[8 * e + 6]) * scale, __uint_as_float(k[8 * e + 7]) * scale);
+            reinterpret_cast<uint4*>(dv_row + c * 32)[e] = a;
+            reinterpret_cast<uint4*>(dk_row + c * 32)[e] = b;
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(acc_free);
+      ++u_it;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- deterministic dQ
+
+template <int HD>
+struct CfgQ {
+  static constexpr int KB = HD / 64;
+  static constexpr int TILE = BT * HD * 2;
+  static constexpr int NS = 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_DO = OFF_Q + TILE;
+  static constexpr int OFF_K = OFF_DO + TILE;          // [NS]
+  static constexpr int OFF_V = OFF_K + NS * TILE;      // [NS]
+  static constexpr int OFF_BAR = OFF_V + NS * TILE;
+  // q_full, q_empty, kv_full[NS], kv_empty[NS], s_full, s_free, dp_full, ds_full, dq_full, drain
+  static constexpr int NBAR = 2 + 2 * NS + 6;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16;
+  static constexpr uint32_t IDESC_S = ptx::idesc_bf16(BT, BT, false, false);
+  static constexpr uint32_t IDESC_DQ = ptx::idesc_bf16(BT, HD, false, true);
+};
+constexpr int DQ_THREADS = 192;
+
+// One persistent CTA per SM; a unit is one 128-row query tile of one head.
+// For each key tile (fixed ascending order): S = Q K^T, dP = dO V^T (both in
+// TMEM, one thread per query row), dS = P o (dP - D) written bf16 over dP,
+// and dQ += dS K accumulates in TMEM. Warps: 0 producer, 1 MMA, 2-5 rows.
+template <int HD>
+__global__ void __launch_bounds__(DQ_THREADS, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+              const Params P) {
+  using C = CfgQ<HD>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if ((ptx::smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicOr(P.status, ATTN_DEV_BAD_SMEM);
+    return;
+  }
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sdO = smem + C::OFF_DO;
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* kv_full = bars + 2;            // [NS]
+  uint64_t* kv_empty = kv_full + C::NS;    // [NS]
+  uint64_t* s_full = kv_empty + C::NS;
+  uint64_t* s_free = s_full + 1;
+  uint64_t* dp_full = s_full + 2;
+  uint64_t* ds_full = s_full + 3;
+  uint64_t* dq_full = s_full + 4;
+  uint64_t* drain = s_full + 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(q_full, 1);
+    ptx::mbar_init(q_empty, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      ptx::mbar_init(kv_full + s, 1);
+      ptx::mbar_init(kv_empty + s, 1);
+    }
+    ptx::mbar_init(s_full, 1);
+    ptx::mbar_init(s_free, 128);
+    ptx::mbar_init(dp_full, 1);
+    ptx::mbar_init(ds_full, 128);
+    ptx::mbar_init(dq_full, 1);
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t T_S = 0, T_DP = 128, T_DQ = 256;
+  const int grid = gridDim.x, cta = blockIdx.x;
+  const int Tq = P.p.Tq, Tk = P.p.Tk;
+  auto nk_of = [&](int qt) { return P.p.causal ? min(qt + 1, P.n_k_tiles) : P.n_k_tiles; };
+
+  if (warp == 0 && lane == 0) {
+    ptx::WaitCtx w{abort_flag, P.status, 5u};
+    uint32_t u_it = 0, k_it = 0;
+    bool ok = true;
+    int bh, qt;
+    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qt); ++round) {
+      const int nk = nk_of(qt);
+      if (!(ok = ptx::mbar_wait(q_empty, (u_it & 1u) ^ 1u, w))) break;
+      ptx::mbar_arrive_expect_tx(q_full, 2 * C::TILE);
+      for (int b = 0; b < C::KB; ++b) {
+        ptx::tma_load_3d(sQ + b * BOX_BYTES, &tmQ, q_full, b * 64, qt * BT, bh);
+        ptx::tma_load_3d(sdO + b * BOX_BYTES, &tmdO, q_full, b * 64, qt * BT, bh);
+      }
+      for (int j = 0; j < nk; ++j, ++k_it) {
+        const int st = k_it % C::NS;
+        if (!(ok = ptx::mbar_wait(kv_empty + st, ((k_it / C::NS) & 1u) ^ 1u, w))) break;
+        ptx::mbar_arrive_expect_tx(kv_full + st, 2 * C::TILE);
+        for (int b = 0; b < C::KB; ++b) {
+          ptx::tma_load_3d(sK + st * C::TILE + b * BOX_BYTES, &tmK, kv_full + st, b * 64, j * BT, bh);
+          ptx::tma_load_3d(sV + st * C::TILE + b * BOX_BYTES, &tmV, kv_full + st, b * 64, j * BT, bh);
+        }
+      }
+      ++u_it;
+    }
+    if (!ok) {
+      for (uint32_t n = (k_it > (uint32_t)C::NS ? k_it - C::NS : 0u); n < k_it; ++n)
+        ptx::mbar_wait_drain(kv_full + n % C::NS, (n / C::NS) & 1u);
+      if (u_it > 0) ptx::mbar_wait_drain(q_full, (u_it - 1) & 1u);
+    }
+  } else if (warp == 1 && lane == 0) {
+    ptx::WaitCtx w{abort_flag, P.status, 6u};
+    const uint32_t aQ = ptx::smem_u32(sQ), adO = ptx::smem_u32(sdO), aK = ptx::smem_u32(sK), aV = ptx::smem_u32(sV);
+    auto kmaj = [](uint32_t base, int kk) {
+      return ptx::sdesc_sw128(base + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
+    };
+    auto mnmaj = [](uint32_t base, int kk) { return ptx::sdesc_sw128(base + kk * 2048, BOX_BYTES, 1024); };
+    uint32_t u_it = 0, k_it = 0, sp = 0;
+    bool ok = true;
+    int bh, qt;
+    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qt); ++round) {
+      const int nk = nk_of(qt);
+      if (!(ok = ptx::mbar_wait(q_full, u_it & 1u, w))) break;
+      // S for the first key tile
+      {
+        const int st = k_it % C::NS;
+        if (!(ok = ptx::mbar_wait(kv_full + st, (k_it / C::NS) & 1u, w))) break;
+        ptx::tc_fence_after();
+        for (int kk = 0; kk < HD / 16; ++kk)
+          ptx::mma_ss(tmem + T_S, kmaj(aQ, kk), kmaj(aK + st * C::TILE, kk), C::IDESC_S, kk > 0);
+        ptx::mma_commit(s_full);
+      }
+      for (int j = 0; j < nk; ++j, ++sp) {
+        const uint32_t it = k_it + j;
+        const int st = it % C::NS;
+        // dP = dO V^T (the dP columns are free: the previous dQ product read dS from them)
+        for (int kk = 0; kk < HD / 16; ++kk)
+          ptx::mma_ss(tmem + T_DP, kmaj(adO, kk), kmaj(aV + st * C::TILE, kk), C::IDESC_S, kk > 0);
+        ptx::mma_commit(dp_full);
+        // next S once the row threads have read this one
+        if (j + 1 < nk) {
+          const uint32_t itn = it + 1;
+          const int stn = itn % C::NS;
+          if (!(ok = ptx::mbar_wait(kv_full + stn, (itn / C::NS) & 1u, w))) break;
+          if (!(ok = ptx::mbar_wait(s_free, sp & 1u, w))) break;
+          ptx::tc_fence_after();
+          for (int kk = 0; kk < HD / 16; ++kk)
+            ptx::mma_ss(tmem + T_S, kmaj(aQ, kk), kmaj(aK + stn * C::TILE, kk), C::IDESC_S, kk > 0);
+          ptx::mma_commit(s_full);
+        }
+        // dQ += dS K
+        if (!(ok = ptx::mbar_wait(ds_full, sp & 1u, w))) break;
+        ptx::tc_fence_after();
+        for (int kk = 0; kk < BT / 16; ++kk)
+          ptx::mma_ts(tmem + T_DQ, tmem + T_DP + kk * 8, mnmaj(aK + st * C::TILE, kk), C::IDESC_DQ,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(kv_empty + st);
+      }
+      if (!ok) break;
+      ptx::mma_commit(dq_full);
+      ptx::mma_commit(q_empty);
+      k_it += nk;
+      ++u_it;
+    }
+    if (!ok) {
+      ptx::mma_commit(drain);
+      ptx::mbar_wait_drain(drain, 0u);
+    }
+  } else if (warp >= 2) {
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_off + T_S, tDP = tmem + lane_off + T_DP, tDQ = tmem + lane_off + T_DQ;
+    ptx::WaitCtx w{abort_flag, P.status, 7u};
+    const float sc2 = P.sc2, scale = P.p.scale;
+    uint32_t u_it = 0, sp = 0;
+    bool ok = true;
+    int bh, qt;
+    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qt); ++round) {
+      const int nk = nk_of(qt);
+      const int q = qt * BT + r;
+      const bool q_ok = q < Tq;
+      float lse2 = CUDART_INF_F, dd = 0.f;
+      if (q_ok) {
+        const float lse = P.LSE[static_cast<size_t>(bh) * Tq + q];
+        lse2 = (lse == -CUDART_INF_F) ? CUDART_INF_F : lse * LOG2E;
+        dd = P.D[static_cast<size_t>(bh) * Tq + q];
+      }
+      for (int j = 0; j < nk; ++j, ++sp) {
+        if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(s_full, sp & 1u, w)))) break;
+        ptx::tc_fence_after();
+        float p[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld32(tS + c * 32, v);
+          ptx::tmem_ld_wait(v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) p[c * 32 + i] = ptx::ex2(fmaf(__uint_as_float(v[i]), sc2, -lse2));
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(s_free);
+        const int kv0 = j * BT;
+        if (kv0 + BT > Tk || (P.p.causal && kv0 + BT - 1 > qt * BT)) {
+          const int lim = min(Tk - kv0, P.p.causal ? q - kv0 + 1 : BT);   // keys [0, lim) allowed
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (i >= lim) p[i] = 0.f;
+        }
+        if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dp_full, sp & 1u, w)))) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld32(tDP + c * 32, v);
+          ptx::tmem_ld_wait(v);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = ptx::pack_bf16(p[c * 32 + 2 * i] * (__uint_as_float(v[2 * i]) - dd),
+                                   p[c * 32 + 2 * i + 1] * (__uint_as_float(v[2 * i + 1]) - dd));
+          ptx::tmem_st16(tDP + c * 16, pk);
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(ds_full);
+      }
+      if (!ok) break;
+      if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dq_full, u_it & 1u, w)))) break;
+      ptx::tc_fence_after();
+      __nv_bfloat16* row = P.dQ + (static_cast<size_t>(bh) * Tq + (q_ok ? q : 0)) * HD;
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld32(tDQ + c * 32, v);
+        ptx::tmem_ld_wait(v);
+        if (q_ok) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint4 a;
+            a.x = ptx::pack_bf16(__uint_as_float(v[8 * e + 0]) * scale, __uint_as_float(v[8 * e + 1]) * scale);
+            a.y = ptx::pack_bf16(__uint_as_float(v[8 * e + 2]) * scale, __uint_as_float(v[8 * e + 3]) * scale);
+            a.z = ptx::pack_bf16(__uint_as_float(v[8 * e + 4]) * scale, __uint_as_float(v[8 * e + 5]) * scale);
+            a.w = ptx::pack_bf16(__uint_as_float(v[8 * e + 6]) * scale, __uint_as_float(v[8 * e + 7]) * scale);
+            reinterpret_cast<uint4*>(row + c * 32)[e] = a;
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ++u_it;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// dQ (bf16) = dQ accumulator (fp32, already scaled)
+__global__ void convert_dq_kernel(const float4* __restrict__ acc, uint2* __restrict__ out, size_t n4) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const float4 v = acc[i];
+    out[i] = make_uint2(ptx::pack_bf16(v.x, v.y), ptx::pack_bf16(v.z, v.w));
+  }
+}
+
+template <int HD>
+cudaError_t launch(const LaunchBwd& a) {
+  const Problem& p = a.p;
+  const bool atomic = !a.deterministic;
+  const bool pre = a.phase == 0 || a.phase == 1, main = a.phase == 0 || a.phase == 2,
+             conv = a.phase == 0 || a.phase == 3;
+  cudaError_t e = cudaSuccess;
+  if (pre) {
+    e = launch_bwd_preprocess(p, a.O, a.dO, 2, a.D, atomic ? a.dQacc : nullptr, p.d, a.num_sms, a.stream);
+    if (e != cudaSuccess) return e;
+  }
+  Params P{};
+  P.p = p;
+  P.LSE = a.LSE;
+  P.D = a.D;
+  P.dQacc = a.dQacc;
+  P.dQ = static_cast<__nv_bfloat16*>(a.dQ);
+  P.dK = static_cast<__nv_bfloat16*>(a.dK);
+  P.dV = static_cast<__nv_bfloat16*>(a.dV);
+  P.status = a.status;
+  P.n_q_tiles = (p.Tq + BT - 1) / BT;
+  P.n_k_tiles = (p.Tk + BT - 1) / BT;
+  P.sc2 = p.scale * LOG2E;
+  const int heads = p.B * p.H;
+  if (main) {
+    P.order = Order{P.n_k_tiles, heads, p.causal ? 2 : 0};
+    const int units = P.n_k_tiles * heads;
+    const int grid = units < a.num_sms ? units : a.num_sms;
+    auto kern = atomic ? dkdv_kernel<HD, true> : dkdv_kernel<HD, false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgKV<HD>::SMEM);
+    if (e != cudaSuccess) return e;
+    // The register split must fit the launch allocation (see reg_acquire).
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+    if (fa.numRegs < REG_CTRL || fa.numRegs > REG_PDS || 2 * fa.numRegs < REG_CTRL + REG_PDS)
+      return cudaErrorInvalidConfiguration;
+    kern<<<grid, NUM_THREADS, CfgKV<HD>::SMEM, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO, P);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (atomic) {
+    if (!conv) return cudaSuccess;
+    const size_t n4 = static_cast<size_t>(heads) * p.Tq * p.d / 4;
+    convert_dq_kernel<<<a.num_sms * 4, 256, 0, a.stream>>>(reinterpret_cast<const float4*>(a.dQacc),
+                                                            static_cast<uint2*>(a.dQ), n4);
+    return cudaGetLastError();
+  }
+  if (!main) return cudaSuccess;
+  P.order = Order{P.n_q_tiles, heads, p.causal ? 1 : 0};
+  const int units = P.n_q_tiles * heads;
+  const int grid = units < a.num_sms ? units : a.num_sms;
+  e = cudaFuncSetAttribute(dq_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgQ<HD>::SMEM);
+  if (e != cudaSuccess) return e;
+  dq_kernel<HD><<<grid, DQ_THREADS, CfgQ<HD>::SMEM, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO, P);
+  return cudaGetLastError();
+}
+
+}  // namespace bwd
+
+cudaError_t launch_bwd_bf16(const LaunchBwd& a) {
+  if (a.p.d == 128) return bwd::launch<128>(a);
+  return bwd::launch<64>(a);
+}
+
+}  // namespace attn

@@ -10,11 +10,14 @@
 //
 // One persistent CTA per SM walks a causal-aware list of work units. A unit is
 // two 128-row query tiles (256 rows) of one head; both tiles share every K/V
-// tile that TMA brings in. Warp roles (10 warps):
+// tile that TMA brings in. Warp roles (12 warps, 3 warpgroups):
 //   warp 0      TMA producer: lane 0 loads Q and K, lane 1 loads V
 //   warp 1      MMA issuer (lane 0); also allocates and frees TMEM
-//   warps 2-5   softmax group for query tile 0 (one thread per query row)
-//   warps 6-9   softmax group for query tile 1
+//   warps 2-3   idle (they complete the first warpgroup's register release)
+//   warps 4-7   softmax group for query tile 0 (one thread per query row)
+//   warps 8-11  softmax group for query tile 1
+// The first warpgroup gives up registers (setmaxnreg) so each softmax thread
+// can hold its whole 128-score row.
 // TMEM (512 columns): tile t keeps its score tile S_t at columns [256t, 256t+128)
 // and its accumulator O_t at [256t+128, 256t+128+dv). The softmax threads write
 // P_t (bf16) over the first 64 columns of S_t, and the PV product reads it from
@@ -45,7 +48,9 @@ constexpr int BM = 128;          // query rows per tile
 constexpr int BN = 128;          // keys per tile
 constexpr int BOX_BYTES = 128 * 64 * 2;   // one TMA box: 128 rows x 64 bf16 (128-byte swizzle span)
 constexpr float TAU = 8.0f;      // lazy-rescale threshold in log2 units
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 384;   // three warpgroups
+constexpr int REG_CTRL = 96;        // producer / MMA warpgroup
+constexpr int REG_SOFTMAX = 200;   // each softmax warpgroup
 
 template <int HD>
 struct Cfg {
@@ -147,7 +152,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int grid = gridDim.x;
   const int cta = blockIdx.x;
 
-  if (warp == 0 && lane < 2) {
+  const int wg = warp >> 2;
+  if (wg == 0) {
+   ptx::reg_release<REG_CTRL>();
+   if (warp == 0 && lane < 2) {
     // ------------------------------------------------------------ producer
     ptx::WaitCtx w{abort_flag, P.status, 1u + lane};
     const bool is_qk = (lane == 0);
@@ -189,7 +197,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::mbar_wait_drain((is_qk ? k_full : v_full) + n % C::NS, (n / C::NS) & 1u);
       if (is_qk && u_it > 0) ptx::mbar_wait_drain(q_full, (u_it - 1) & 1u);
     }
-  } else if (warp == 1 && lane == 0) {
+   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     ptx::WaitCtx w{abort_flag, P.status, 3u};
     const uint32_t sQa = ptx::smem_u32(sQ), sKa = ptx::smem_u32(sK), sVa = ptx::smem_u32(sV);
@@ -271,9 +279,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::mma_commit(drain);
       ptx::mbar_wait_drain(drain, 0u);
     }
-  } else if (warp >= 2) {
+   }
+  } else {
+    ptx::reg_acquire<REG_SOFTMAX>();
     // ------------------------------------------------------------ softmax
-    const int t = (warp - 2) >> 2;          // query tile of this group
+    const int t = wg - 1;                   // query tile of this group
     const int quad = warp & 3;              // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;         // row within the tile
     const uint32_t tS = tmem + (static_cast<uint32_t>(quad * 32) << 16) + t * 256;
@@ -416,6 +426,11 @@ cudaError_t launch(const LaunchFwd& a) {
   auto kern = attn_fwd_bf16_kernel<HD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
+  // The register split must fit the launch allocation (see reg_acquire).
+  cudaFuncAttributes fa;
+  if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+  if (fa.numRegs < REG_CTRL || fa.numRegs > REG_SOFTMAX || 3 * fa.numRegs < REG_CTRL + 2 * REG_SOFTMAX)
+    return cudaErrorInvalidConfiguration;
   kern<<<grid, NUM_THREADS, C::SMEM, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, P);
   return cudaGetLastError();
 }

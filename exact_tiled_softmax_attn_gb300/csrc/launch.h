@@ -44,6 +44,7 @@ struct LaunchBwd {
   float* D;                 // [B,H,Tq] workspace
   float* dQacc;             // [B,H,Tq,d] fp32 workspace (bf16 atomic path), else null
   int deterministic;
+  int phase;                // 0 = all; 1 = preprocess; 2 = main kernels; 3 = dQ conversion
   uint32_t* status;
   int num_sms;
   cudaStream_t stream;

@@ -92,6 +92,21 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
   return true;
 }
 
+// ---------------------------------------------------------------- registers
+
+// Per-warpgroup register budget (all four warps of a warpgroup execute it).
+// The increases of all warpgroups must fit in what the decreases released
+// from the launch allocation, or setmaxnreg.inc waits forever; every kernel
+// using these checks its launch register count on the host first.
+template <uint32_t N>
+__device__ __forceinline__ void reg_release() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void reg_acquire() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- proxies
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -226,6 +241,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : ATTN_R8(0), ATTN_R8(8)
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : ATTN_W8(0), ATTN_W8(8) : : "memory");
+}
+
 // Completes every outstanding tcgen05.ld of this thread. The registers are
 // passed through so the compiler cannot hoist their uses above the wait.
 __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
@@ -257,6 +284,15 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 #undef ATTN_R8
 #undef ATTN_W8
 #undef ATTN_I8
+
+// 16-byte shared-memory load kept in program order (bounds register live ranges).
+__device__ __forceinline__ float4 lds128(const float* p) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(smem_u32(p)));
+  return v;
+}
 
 // ---------------------------------------------------------------- math
 

@@ -402,10 +402,14 @@ cudaError_t launch_fwd_f32(const LaunchFwd& a) {
 
 cudaError_t launch_bwd_f32(const LaunchBwd& a) {
   const Problem& p = a.p;
-  // D = rowsum(dO o O); dQ zeroed when it is accumulated with atomics.
-  cudaError_t e = launch_bwd_preprocess(p, a.O, a.dO, 4, a.D, a.deterministic ? nullptr : static_cast<float*>(a.dQ),
-                                        p.d, a.num_sms, a.stream);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (a.phase == 0 || a.phase == 1) {
+    // D = rowsum(dO o O); dQ zeroed when it is accumulated with atomics.
+    e = launch_bwd_preprocess(p, a.O, a.dO, 4, a.D, a.deterministic ? nullptr : static_cast<float*>(a.dQ), p.d,
+                              a.num_sms, a.stream);
+    if (e != cudaSuccess) return e;
+  }
+  if (a.phase != 0 && a.phase != 2) return cudaSuccess;
   simt::BwdArgs b{static_cast<const float*>(a.Q), static_cast<const float*>(a.K), static_cast<const float*>(a.V),
                   static_cast<const float*>(a.dO), a.LSE, a.D, static_cast<float*>(a.dQ),
                   static_cast<float*>(a.dK), static_cast<float*>(a.dV), p};

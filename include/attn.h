@@ -119,6 +119,23 @@ ATTN_API attn_status_t attn_bwd(const void* Q, const void* K, const void* V, con
                        size_t workspace_bytes, void* stream);
 
 /*
+ * The backward split into its three launch groups, for measurement: the
+ * same arguments as attn_bwd plus `phase`:
+ *   1  preprocess: D = rowsum(dO o O) (and zeroing of the fp32 dQ
+ *      accumulator when deterministic == 0)
+ *   2  main kernels: dK, dV and the dQ accumulation (or, deterministic,
+ *      the separate dQ pass)
+ *   3  dQ conversion from the fp32 accumulator (bf16 with deterministic
+ *      == 0; a no-op otherwise)
+ * Calling phases 1, 2, 3 in order on one stream equals one attn_bwd call;
+ * phase 0 is attn_bwd itself. Other values give ATTN_ERR_INVALID_ARG.
+ */
+ATTN_API attn_status_t attn_bwd_phase(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+                                      const void* dO, void* dQ, void* dK, void* dV, int B, int H, int Tq, int Tk,
+                                      int d, int dv, float scale, int causal, attn_dtype_t dtype, int deterministic,
+                                      void* workspace, size_t workspace_bytes, int phase, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word that
  * the kernels set when a bounded wait gives up (ATTN_ERR_TIMEOUT) or a launch
  * precondition fails on the device (ATTN_ERR_CUDA). ATTN_OK otherwise.

@@ -91,3 +91,79 @@ def test_empty_sides_give_zero_gradients(dt, d, Tq, Tk):
     torch.cuda.synchronize()
     for t in (dq, dk, dv):
         assert torch.all(t == 0)
+
+
+# ------------------------------------------------------------------ bf16
+
+BF16_SHAPES = [  # B, H, Tq, Tk, d
+    (1, 1, 1, 1, 64),
+    (2, 3, 300, 300, 64),
+    (1, 2, 257, 129, 128),
+    (1, 1, 130, 700, 128),
+    (2, 2, 512, 512, 128),
+    (1, 1, 700, 70, 64),
+]
+
+
+@pytest.mark.parametrize("deterministic", [0, 1])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", BF16_SHAPES)
+def test_bf16_ragged(shape, causal, deterministic):
+    B, H, Tq, Tk, d = shape
+    x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, d), seed=Tq * 5 + Tk, dtype=torch.bfloat16,
+                    device=DEV)
+    check_all(x, causal, 1 / math.sqrt(d), torch.bfloat16, deterministic)
+
+
+@pytest.mark.parametrize("deterministic", [0, 1])
+def test_bf16_c2_full_size(deterministic):
+    w = WORKLOADS["c2"]
+    check_all(make_inputs(w, DEV), w.causal, w.softmax_scale, torch.bfloat16, deterministic)
+
+
+@pytest.mark.parametrize("deterministic", [0, 1])
+@pytest.mark.parametrize("name,heads", [("c3", [(0, 3), (1, 12)]), ("c5", [(0, 31)])])
+def test_bf16_full_size_sampled_heads(name, heads, deterministic):
+    w = WORKLOADS[name]
+    check_all(make_inputs(w, DEV), w.causal, w.softmax_scale, torch.bfloat16, deterministic, heads=heads)
+
+
+def test_bf16_large_logits_across_tiles():
+    B, H, T, d = 1, 2, 640, 128
+    x = make_random((B, H, T, d), (B, H, T, d), (B, H, T, d), seed=9, device="cpu")
+    sign = torch.where((torch.arange(T) // 128) % 2 == 0, 40.0, -40.0).view(1, 1, T, 1)
+    x = {k: (v * sign if k == "K" else v).to(torch.bfloat16).to(DEV) for k, v in x.items()}
+    for causal in (False, True):
+        for det in (0, 1):
+            check_all(x, causal, 1.0 / math.sqrt(d), torch.bfloat16, det)
+
+
+def test_bf16_deterministic_is_bitwise_repeatable():
+    x = make_random((2, 3, 700, 128), (2, 3, 700, 128), (2, 3, 700, 128), seed=4, dtype=torch.bfloat16,
+                    device=DEV)
+    a = run(x, True, 0.088, 1)
+    b = run(x, True, 0.088, 1)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+
+
+def test_bf16_atomic_and_deterministic_agree():
+    x = make_random((1, 4, 1024, 64), (1, 4, 1024, 64), (1, 4, 1024, 64), seed=6, dtype=torch.bfloat16,
+                    device=DEV)
+    a = run(x, True, 0.125, 0)
+    b = run(x, True, 0.125, 1)
+    for u, v, name in zip(a[2:], b[2:], ("dQ", "dK", "dV")):
+        check_grad(u, v, torch.bfloat16, name)
+    assert torch.equal(a[3], b[3]) and torch.equal(a[4], b[4])   # dK, dV do not depend on the dQ mode
+
+
+def test_bf16_inputs_unchanged():
+    x = make_random((1, 2, 300, 64), (1, 2, 200, 64), (1, 2, 200, 64), seed=8, dtype=torch.bfloat16, device=DEV)
+    keep = {k: v.clone() for k, v in x.items()}
+    o, lse, *_ = run(x, False, 0.1, 0)
+    o2, lse2 = o.clone(), lse.clone()
+    pkg.backward(x["Q"], x["K"], x["V"], o, lse, x["dO"], causal=False, scale=0.1, deterministic=1)
+    torch.cuda.synchronize()
+    for k in x:
+        assert torch.equal(x[k], keep[k]), k
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
