@@ -1,0 +1,402 @@
+#!/usr/bin/env python
+"""Benchmark: exact tiled softmax attention, forward + backward, on GB300.
+
+One step = attn_fwd + attn_bwd (the whole hot path) over one batch of the
+headline workload (B=2, H=16, Tq=Tk=8192, d=dv=128, bf16, causal), inputs
+resident in HBM. Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs one process per GPU under torch.distributed (each rank processes
+its own batch: weak scaling); the reported time is the max over ranks.
+--impl reference times the CPU float64 oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s fwd+bwd (bf16, causal, 1 GB300)"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ("fwd_bf16.cu", "bwd_bf16.cu", "small.cu", "ptx.cuh", "common.cuh")
+
+
+# ---------------------------------------------------------------- helpers
+
+def useful_flops_rows(w, rows):
+    """Useful fwd+bwd FLOPs of the given query rows: 4*d per (query, key) pair
+    forward and 2.5x that backward. Under the causal mask row i counts i + 1/2
+    keys, so that all Tq rows of a square problem sum to the halved full count
+    (the convention of the GPU metric)."""
+    import numpy as np
+    rows = np.asarray(rows, dtype=np.float64)
+    keys = np.minimum(rows + 0.5, w.Tk) if w.causal else np.full(rows.shape, float(w.Tk))
+    return 3.5 * 4.0 * w.d * float(keys.sum())
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "exact_tiled_softmax_attn_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained"), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def load_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when the summary was taken on different kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        e = j[kernel]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return e["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.windows = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc is None:
+            return {"error": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        samples = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                samples.append((ts, float(parts[1]), float(parts[2]), parts[4:8]))
+            except Exception:
+                continue
+        inside = [s for s in samples if any(a - 0.05 <= s[0] <= b + 0.05 for a, b in self.windows)]
+        use = inside if inside else samples
+        if not use:
+            return {"error": "no samples"}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in use for n, v in zip(names, s[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(s[1] for s in use), "sm_max_mhz": max(s[2] for s in use),
+                "reasons": reasons, "samples": len(use), "in_timed_region": bool(inside)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float) -> float:
+    """Max of `value` over all ranks (identity without torch.distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- CPU oracle legs
+
+def oracle_sample(w, x, rows):
+    """Run the CPU float64 oracle forward + backward on the given query rows of
+    head (0, 0); returns seconds."""
+    from oracle import attention as ref
+    t0 = time.perf_counter()
+    ref.backward_head(x["Q"][0, 0], x["K"][0, 0], x["V"][0, 0], x["dO"][0, 0], w.softmax_scale, w.causal,
+                      rows=rows)
+    return time.perf_counter() - t0
+
+
+def spread_rows(w, n):
+    import numpy as np
+    n = max(1, min(n, w.Tq))
+    return np.unique(np.linspace(0, w.Tq - 1, n).astype(np.int64))
+
+
+def cpu_baseline(w, x, target_s=15.0):
+    """The oracle on a bounded sample of the workload (~10-30 s of CPU work)."""
+    probe = spread_rows(w, 128)
+    t = oracle_sample(w, x, probe)
+    n = int(min(w.Tq, max(128, 128 * target_s / max(t, 1e-3))))
+    rows = spread_rows(w, n)
+    t = oracle_sample(w, x, rows)
+    fl = useful_flops_rows(w, rows)
+    return {"value": fl / t / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"float64 numpy oracle, fwd+bwd of {rows.size} query rows spread over head (0,0) of "
+                      f"{w.name} (Tk={w.Tk}, d={w.d}); useful FLOPs of those rows / {t:.2f} s"}
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    from exact_tiled_softmax_attn_gb300.workloads import make_inputs
+    x = make_inputs(w.with_(B=1, H=1))
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    cal = spread_rows(w, 64)
+    t = oracle_sample(w, x, cal)
+    n = int(min(w.Tq, max(64, 64 * budget / max(t, 1e-3))))
+    rows = spread_rows(w, n)
+    for _ in range(args.warmup):
+        oracle_sample(w, x, rows)
+    total = 0.0
+    for _ in range(args.steps):
+        total += oracle_sample(w, x, rows)
+    fl = useful_flops_rows(w, rows) * args.steps
+    value = fl / total / 1e12
+    sample = (f"float64 numpy oracle, fwd+bwd of {rows.size} query rows spread over head (0,0) of {w.name} "
+              f"per step (useful FLOPs of those rows)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {"workload": f"{w.name}: B={w.B} H={w.H} Tq={w.Tq} Tk={w.Tk} d={w.d} dv={w.dv} {w.dtype} "
+                        f"{'causal' if w.causal else 'no mask'}, scale={w.softmax_scale:.6g}",
+            "B": w.B, "H": w.H, "Tq": w.Tq, "Tk": w.Tk, "d": w.d, "dv": w.dv, "causal": w.causal,
+            "l2": "256 MiB written between timed steps (outside the timed region); per-step inputs "
+                  f"{4 * w.B * w.H * w.Tq * w.d * (2 if w.dtype == 'bf16' else 4) / 1e6:.0f} MB > 129 MB L2"}
+
+
+# ---------------------------------------------------------------- GPU leg
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import exact_tiled_softmax_attn_gb300 as pkg
+    from exact_tiled_softmax_attn_gb300.workloads import make_inputs
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pkg.load_library()
+    code = pkg.ATTN_BF16 if w.dtype == "bf16" else pkg.ATTN_F32
+    B, H, Tq, Tk, d, dv = w.B, w.H, w.Tq, w.Tk, w.d, w.dv
+    det = int(args.deterministic)
+
+    host = make_inputs(w.with_(seed=w.seed + 1000 * rank))
+    x = {k: v.to(dev) for k, v in host.items()}
+    o = torch.empty(B, H, Tq, dv, dtype=w.torch_dtype, device=dev)
+    lse = torch.empty(B, H, Tq, dtype=torch.float32, device=dev)
+    dq, dk, dvv = torch.empty_like(x["Q"]), torch.empty_like(x["K"]), torch.empty_like(x["V"])
+    ws_bytes = pkg.attn_bwd_workspace_size(B, H, Tq, Tk, d, dv, code, det)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sc = w.softmax_scale
+
+    def fwd():
+        pkg.attn_fwd(x["Q"], x["K"], x["V"], o, lse, B, H, Tq, Tk, d, dv, sc, w.causal, code, stream)
+
+    def bwd_phase(ph):
+        pkg.attn_bwd_phase(x["Q"], x["K"], x["V"], o, lse, x["dO"], dq, dk, dvv, B, H, Tq, Tk, d, dv, sc,
+                           w.causal, code, det, ws, ws.numel(), ph, stream)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fwd()
+        if ev is not None:
+            ev[1].record(stream)
+        for ph in (1, 2, 3):
+            bwd_phase(ph)
+            if ev is not None:
+                ev[1 + ph].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert pkg.attn_device_status(stream) == pkg.ATTN_OK
+
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()                  # evict L2 between steps (not timed)
+        step(events[i])
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier()
+    if clocks:
+        clocks.mark(t_wall0, t_wall1)
+    per = [[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in events]    # ms: fwd, pre, main, conv
+    step_ms = [sum(p) for p in per]
+    total_ms = reduce_max(sum(step_ms))
+    fwd_ms = statistics.mean(p[0] for p in per)
+    pre_ms = statistics.mean(p[1] for p in per)
+    main_ms = statistics.mean(p[2] for p in per)
+    conv_ms = statistics.mean(p[3] for p in per)
+    bwd_ms = pre_ms + main_ms + conv_ms
+    F, Bf = w.fwd_flop(), w.bwd_flop()
+    value = world * args.steps * (F + Bf) / (total_ms * 1e-3) / 1e12
+    assert pkg.attn_device_status(stream) == pkg.ATTN_OK
+
+    # ---- end to end through the public API, host buffers in and out
+    pinned = {k: v.pin_memory() for k, v in host.items()}
+    out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for n, t in (("O", o), ("LSE", lse), ("dQ", dq), ("dK", dk), ("dV", dvv))}
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+    e2e_steps = max(1, min(args.steps, 20))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_total = 0.0
+    for i in range(e2e_steps + 1):
+        flush.zero_()
+        ev0.record(stream)
+        for k in x:
+            x[k].copy_(pinned[k], non_blocking=True)
+        fwd()
+        pkg.attn_bwd(x["Q"], x["K"], x["V"], o, lse, x["dO"], dq, dk, dvv, B, H, Tq, Tk, d, dv, sc, w.causal, code,
+                     det, ws, ws.numel(), stream)
+        for n, t in (("O", o), ("LSE", lse), ("dQ", dq), ("dK", dk), ("dV", dvv)):
+            out_host[n].copy_(t, non_blocking=True)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        if i > 0:      # the first pass warms the copy engines
+            e2e_total += ev0.elapsed_time(ev1)
+    e2e_total = reduce_max(e2e_total)
+    e2e_value = world * e2e_steps * (F + Bf) / (e2e_total * 1e-3) / 1e12
+    if clocks:
+        clk = clocks.stop()
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+
+    peaks = load_peaks()
+    peak = peaks["bf16_tflops"]
+    kernels = {
+        "fwd (attn_fwd_bf16_kernel)": {"ms": fwd_ms, "tflops": F / (fwd_ms * 1e-3) / 1e12},
+        "bwd main (dkdv_kernel)": {"ms": main_ms, "tflops": Bf / (main_ms * 1e-3) / 1e12},
+        "bwd preprocess": {"ms": pre_ms,
+                           "gbs": B * H * Tq * (2 * dv * 2 + 4 + (d * 4 if not det else 0)) / (pre_ms * 1e-3) / 1e9},
+        "dQ convert": {"ms": conv_ms, "gbs": B * H * Tq * d * (4 + 2) / (conv_ms * 1e-3) / 1e9 if conv_ms > 0 else None},
+    }
+    for k in ("fwd (attn_fwd_bf16_kernel)", "bwd main (dkdv_kernel)"):
+        kernels[k]["frac_of_peak"] = kernels[k]["tflops"] / peak
+    kernels["bwd preprocess"]["frac_of_hbm"] = kernels["bwd preprocess"]["gbs"] / peaks["hbm_gbs"]
+    dom = max(("fwd (attn_fwd_bf16_kernel)", fwd_ms, F), ("bwd main (dkdv_kernel)", main_ms, Bf), key=lambda t: t[1])
+    achieved = dom[2] / (dom[1] * 1e-3) / 1e12
+    traffic = load_traffic("dkdv_kernel" if "dkdv" in dom[0] else "attn_fwd_bf16_kernel")
+    cfg = workload_config(w)
+    cfg.update({"dq_mode": "deterministic" if det else "atomic",
+                "fwd_tflops": F / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": Bf / (bwd_ms * 1e-3) / 1e12,
+                "fwd_bwd_frac_of_dense_bf16_peak": (F + Bf) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12 / peak,
+                "peak_source": f"{peaks['source']} bf16_tflops {peak}", "kernels": kernels})
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+        "roofline": {"bound": "tensor", "kernel": dom[0], "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_note": f"{peaks['source']} dense bf16 burst (cuBLAS 8192^3)"},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "gpu_launches": args.steps * 4,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, host)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[1])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c3")
+    ap.add_argument("--deterministic", action="store_true", help="dQ in a separate fixed-order pass")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from exact_tiled_softmax_attn_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

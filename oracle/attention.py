@@ -96,11 +96,15 @@ def forward_head(q, k, v, scale, causal=False, rows=None, row_chunk=512):
     return o, lse
 
 
-def backward_head(q, k, v, do, scale, causal=False, row_chunk=512):
+def backward_head(q, k, v, do, scale, causal=False, row_chunk=512, rows=None):
     """One head: closed-form gradients in float64.
 
     Returns dict with dq [Tq,d], dk [Tk,d], dv [Tk,dv], and the forward
     o, lse and D = rowsum(dO o O) that the gradients use.
+
+    ``rows`` restricts the work to those global query rows (a sample): their
+    dq, o, lse and D are filled (other rows stay 0 / -inf), and dk, dv hold
+    the contributions of those rows only.
     """
     q, k, v, do = _as64(q), _as64(k), _as64(v), _as64(do)
     Tq = q.shape[0]
@@ -110,8 +114,9 @@ def backward_head(q, k, v, do, scale, causal=False, row_chunk=512):
     o = np.zeros((Tq, v.shape[1]))
     lse = np.full(Tq, -np.inf)
     D = np.zeros(Tq)
-    for r0 in range(0, Tq, row_chunk):
-        r = np.arange(r0, min(Tq, r0 + row_chunk))
+    rows = np.arange(Tq) if rows is None else np.asarray(rows, dtype=np.int64)
+    for c0 in range(0, rows.size, row_chunk):
+        r = rows[c0:c0 + row_chunk]
         p, lse[r] = _softmax_rows(_scores(q[r], k, scale, causal, r))
         o[r] = p @ v
         D[r] = np.sum(do[r] * o[r], axis=1)           # ROW_SUM(dL/dO o O)

@@ -1,0 +1,61 @@
+"""Host-side logic of bench.py (no GPU): the cross-rank max reduction that the
+multi-GPU run uses, on 2 gloo ranks, and the FLOP accounting."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+from exact_tiled_softmax_attn_gb300.workloads import WORKLOADS
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        got = bench.reduce_max(10.0 * (rank + 1))
+        bench.barrier()
+        q.put((rank, got))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_reduce_max_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = dict(q.get(timeout=5) for _ in range(2))
+    assert res == {0: 20.0, 1: 20.0}
+
+
+def test_reduce_max_without_process_group_is_identity():
+    assert bench.reduce_max(3.5) == 3.5
+
+
+@pytest.mark.parametrize("name", ["c1", "c1_causal", "c2", "c3", "c4", "c5"])
+def test_row_flops_sum_to_the_workload_count(name):
+    w = WORKLOADS[name]
+    one_head = (w.fwd_flop() + w.bwd_flop()) / (w.B * w.H)
+    assert np.isclose(bench.useful_flops_rows(w, np.arange(w.Tq)), one_head, rtol=1e-12)
+
+
+def test_spread_rows_are_sorted_unique_and_in_range():
+    w = WORKLOADS["c3"]
+    r = bench.spread_rows(w, 1000)
+    assert r[0] == 0 and r[-1] == w.Tq - 1 and np.all(np.diff(r) > 0)

@@ -282,6 +282,18 @@ def test_chunked_rows_equal_unchunked():
         np.testing.assert_allclose(a[k], b[k], rtol=1e-12, atol=1e-13)
 
 
+def test_backward_row_samples_add_up_to_the_full_result():
+    rng = np.random.default_rng(16)
+    Q, K, V, dO = (rng.standard_normal(s) for s in ((40, 6), (40, 6), (40, 5), (40, 5)))
+    full = A.backward_head(Q, K, V, dO, 0.4, True)
+    a = A.backward_head(Q, K, V, dO, 0.4, True, row_chunk=7, rows=np.arange(0, 40, 2))
+    b = A.backward_head(Q, K, V, dO, 0.4, True, row_chunk=7, rows=np.arange(1, 40, 2))
+    np.testing.assert_allclose(a["dk"] + b["dk"], full["dk"], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(a["dv"] + b["dv"], full["dv"], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(a["dq"][::2], full["dq"][::2], rtol=1e-12, atol=1e-13)
+    assert np.all(a["dq"][1::2] == 0)
+
+
 def test_sampled_rows_equal_full_rows():
     rng = np.random.default_rng(15)
     Q, K, V = rng.standard_normal((50, 8)), rng.standard_normal((50, 8)), rng.standard_normal((50, 3))
