@@ -67,16 +67,16 @@ def load_peaks():
 def load_traffic(kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
     when the summary was taken on different kernel sources."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         with open(p) as f:
-            j = json.load(f)
-        e = j[kernel]
-        if e.get("source_hash") != kernel_source_hash():
-            return None
-        return e["dram_bytes_per_launch"]
-    except Exception:
-        return None
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel:
+                    return float(parts[2]) if parts[1] == kernel_source_hash() else None
+    except OSError:
+        pass
+    return None
 
 
 class ClockSampler:
