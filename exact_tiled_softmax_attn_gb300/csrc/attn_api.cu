@@ -8,7 +8,7 @@
 
 #include <mutex>
 
-#include "../../include/attn.h"
+#include "attn.h"
 #include "common.cuh"
 #include "launch.h"
 #include "ptx.cuh"
