@@ -23,7 +23,7 @@ __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA",
     "ATTN_ERR_TIMEOUT", "ATTN_ERR_WORKSPACE", "ATTN_F32", "ATTN_BF16",
     "attn_fwd", "attn_fwd_f32_blocked", "attn_bwd", "attn_bwd_phase", "attn_bwd_workspace_size",
-    "attn_device_status",
+    "attn_bwd_noalloc", "ATTN_NOALLOC_SCRATCH_BYTES", "attn_device_status",
     "attn_selftest_wait_timeout", "attn_strerror", "attn_last_cuda_error", "attn_version",
     "forward", "backward",
 ]
@@ -44,6 +44,7 @@ _SIGNATURES = {
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _SZ, _P]),
     "attn_bwd_phase": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _SZ,
                             _I, _P]),
+    "attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
     "attn_device_status": (_I, [_P]),
     "attn_selftest_wait_timeout": (_I, [_I, _P]),
     "attn_strerror": (ctypes.c_char_p, [_I]),
@@ -164,6 +165,20 @@ def attn_bwd_phase(Q, K, V, O, LSE, dO, dQ, dK, dV, B, H, Tq, Tk, d, dv, scale, 
     if check:
         _check(st, "attn_bwd_phase")
     return st
+
+
+def attn_bwd_noalloc(Q, K, V, O, LSE, dO, dQ, dK, dV, B, H, Tq, Tk, d, dv, scale, causal, dtype, deterministic,
+                     stream=None, check=True) -> int:
+    """attn_bwd with the library's static scratch buffer instead of a workspace."""
+    st = load_library().attn_bwd_noalloc(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _ptr(dO), _ptr(dQ),
+                                         _ptr(dK), _ptr(dV), B, H, Tq, Tk, d, dv, float(scale), int(causal),
+                                         int(dtype), int(deterministic), _stream(stream))
+    if check:
+        _check(st, "attn_bwd_noalloc")
+    return st
+
+
+ATTN_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 def attn_device_status(stream=None) -> int:

@@ -136,6 +136,41 @@ ATTN_API attn_status_t attn_bwd_phase(const void* Q, const void* K, const void* 
                                       void* workspace, size_t workspace_bytes, int phase, void* stream);
 
 /*
+ * Size of the static scratch buffer behind attn_bwd_noalloc (64 MiB). Every
+ * device that loads the library holds a buffer of this size until the
+ * process exits.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * attn_bwd for callers that cannot allocate device memory: a host without
+ * its own CUDA allocator or memory pool, a plug-in that may not grow the
+ * process's device footprint, or a loop where a cudaMalloc (which can
+ * synchronise the device) is not acceptable. The pages have no counterpart
+ * to this call; it exists only for such callers.
+ *
+ * Arguments, layout and results are those of attn_bwd, without the workspace
+ * arguments: the workspace lives in a static device buffer of
+ * ATTN_NOALLOC_SCRATCH_BYTES inside the library. Nothing is allocated and no
+ * allocating routine is called. Problems whose attn_bwd_workspace_size
+ * exceeds that size are rejected with ATTN_ERR_WORKSPACE before anything is
+ * enqueued (for bf16 with deterministic == 0 the need is B*H*Tq*(d+1)*4
+ * bytes; deterministic == 1 or fp32 needs only B*H*Tq*4).
+ *
+ * The first call on a device (with that device current) looks up the
+ * buffer's device address once; make that first call before any stream
+ * capture begins. All calls on a device share the one buffer and leave their
+ * data in it; each call overwrites everything it reads back (D, and the fp32
+ * dQ accumulator, which it zeroes first). Calls whose kernels can overlap on
+ * the GPU (different streams without ordering, or several host threads) race
+ * on the buffer and corrupt each other's gradients: order them on one stream.
+ */
+ATTN_API attn_status_t attn_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
+                                        const float* LSE, const void* dO, void* dQ, void* dK, void* dV, int B,
+                                        int H, int Tq, int Tk, int d, int dv, float scale, int causal,
+                                        attn_dtype_t dtype, int deterministic, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word that
  * the kernels set when a bounded wait gives up (ATTN_ERR_TIMEOUT) or a launch
  * precondition fails on the device (ATTN_ERR_CUDA). ATTN_OK otherwise.

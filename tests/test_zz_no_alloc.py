@@ -1,0 +1,60 @@
+"""attn_bwd_noalloc: the backward for callers that cannot allocate device
+memory (no CUDA allocator of their own, or not allowed to grow the device
+footprint at run time). Its workspace is the library's static scratch
+buffer. Checked against attn_bwd with a caller-allocated workspace, on two
+calls in a row (the second call finds the first call's data in the shared
+buffer). This file sorts last so a stop-at-first-failure run has already run
+every other test."""
+import math
+
+import pytest
+import torch
+
+import exact_tiled_softmax_attn_gb300 as pkg
+from exact_tiled_softmax_attn_gb300.workloads import make_random
+
+from parity import check_grad
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+CASES = [  # B, H, Tq, Tk, d, dtype, causal, deterministic
+    (1, 4, 1000, 1000, 128, torch.bfloat16, True, 0),
+    (2, 2, 300, 700, 64, torch.bfloat16, False, 0),
+    (1, 3, 513, 513, 128, torch.bfloat16, True, 1),
+    (2, 2, 77, 133, 40, torch.float32, True, 0),
+]
+
+
+def _reference(x, causal, scale, det):
+    o, lse = pkg.forward(x["Q"], x["K"], x["V"], causal=causal, scale=scale)
+    dq, dk, dv = pkg.backward(x["Q"], x["K"], x["V"], o, lse, x["dO"], causal=causal, scale=scale,
+                              deterministic=det)
+    return o, lse, (dq, dk, dv)
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_noalloc_matches_workspace_backward_twice(case):
+    B, H, Tq, Tk, d, dt, causal, det = case
+    code = pkg.ATTN_BF16 if dt == torch.bfloat16 else pkg.ATTN_F32
+    assert pkg.attn_bwd_workspace_size(B, H, Tq, Tk, d, d, code, det) <= pkg.ATTN_NOALLOC_SCRATCH_BYTES
+    x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, d), seed=Tq + Tk + d, dtype=dt, device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    o, lse, want = _reference(x, causal, scale, det)
+    for _ in range(2):
+        got = [torch.full_like(t, float("nan")) for t in (x["Q"], x["K"], x["V"])]
+        pkg.attn_bwd_noalloc(x["Q"], x["K"], x["V"], o, lse, x["dO"], *got, B, H, Tq, Tk, d, d, scale, causal,
+                             code, det)
+        torch.cuda.synchronize()
+        for g, w, name in zip(got, want, ("dQ", "dK", "dV")):
+            check_grad(g, w, dt, name)
+    assert pkg.attn_device_status() == pkg.ATTN_OK
+
+
+def test_noalloc_rejects_problems_beyond_its_buffer():
+    # bf16 with the fp32 dQ accumulator: B*H*Tq*(d+1)*4 bytes > 64 MiB
+    B, H, T, d = 4, 16, 2048, 128
+    assert pkg.attn_bwd_workspace_size(B, H, T, T, d, d, pkg.ATTN_BF16, 0) > pkg.ATTN_NOALLOC_SCRATCH_BYTES
+    st = pkg.attn_bwd_noalloc(0x100000, 0x200000, 0x300000, 0x400000, 0x500000, 0x600000, 0x700000,
+                              0x800000, 0x900000, B, H, T, T, d, d, 0.088, 1, pkg.ATTN_BF16, 0, check=False)
+    assert st == pkg.ATTN_ERR_WORKSPACE
