@@ -346,8 +346,9 @@ def run_ours(args, w):
     kernels = {
         "fwd (attn_fwd_bf16_kernel)": {"ms": fwd_ms, "tflops": F / (fwd_ms * 1e-3) / 1e12},
         "bwd main (dkdv_kernel)": {"ms": main_ms, "tflops": Bf / (main_ms * 1e-3) / 1e12},
+        # reads O, dO, LSE; writes D and LSE*log2(e) (padded rows) and zeroes the dQ accumulator
         "bwd preprocess": {"ms": pre_ms,
-                           "gbs": B * H * Tq * (2 * dv * 2 + 4 + (d * 4 if not det else 0)) / (pre_ms * 1e-3) / 1e9},
+                           "gbs": B * H * Tq * (2 * dv * 2 + 4 + 8 + (d * 4 if not det else 0)) / (pre_ms * 1e-3) / 1e9},
         "dQ convert": {"ms": conv_ms, "gbs": B * H * Tq * d * (4 + 2) / (conv_ms * 1e-3) / 1e9 if conv_ms > 0 else None},
     }
     for k in ("fwd (attn_fwd_bf16_kernel)", "bwd main (dkdv_kernel)"):

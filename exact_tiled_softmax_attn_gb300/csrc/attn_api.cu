@@ -132,16 +132,19 @@ attn_status_t check_ptr(const void* p, size_t bytes, size_t align) {
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct BwdLayout {
-  size_t d_off, d_bytes, acc_off, acc_bytes, total;
+  size_t lse2_off, d_off, acc_off, acc_bytes, total;
 };
+// Workspace: LSE2 [B*H, Tq_pad] fp32 | D [B*H, Tq_pad] fp32 | (bf16 with fp32
+// dQ accumulation) dQacc [B*H*Tq, d] fp32; each part 256-byte aligned.
 BwdLayout bwd_layout(int B, int H, int Tq, int d, attn_dtype_t dt, int deterministic) {
   BwdLayout L{};
-  const size_t rows = static_cast<size_t>(B) * H * Tq;
-  L.d_off = 0;
-  L.d_bytes = rows * sizeof(float);
-  L.acc_off = round_up(L.d_bytes, 256);
-  L.acc_bytes = (dt == ATTN_BF16 && !deterministic) ? rows * d * sizeof(float) : 0;
-  L.total = L.acc_bytes ? L.acc_off + L.acc_bytes : L.d_bytes;
+  const size_t rows_pad = static_cast<size_t>(B) * H * padded_rows(Tq);
+  const size_t part = round_up(rows_pad * sizeof(float), 256);
+  L.lse2_off = 0;
+  L.d_off = part;
+  L.acc_off = 2 * part;
+  L.acc_bytes = (dt == ATTN_BF16 && !deterministic) ? static_cast<size_t>(B) * H * Tq * d * sizeof(float) : 0;
+  L.total = rows_pad ? L.acc_off + L.acc_bytes : 0;
   return L;
 }
 
@@ -307,6 +310,7 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
   a.dK = dK;
   a.dV = dV;
   a.D = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.d_off);
+  a.LSE2 = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.lse2_off);
   a.dQacc = L.acc_bytes ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.acc_off) : nullptr;
   a.deterministic = deterministic;
   a.phase = phase;

@@ -13,15 +13,15 @@
 // one head, and the CTA loops over the query tiles that can see it. K and V
 // stay in shared memory for the whole unit; Q, dO (TMA) and LSE, D (plain
 // loads) stream through a two-stage ring. Warp roles (12 warps, 3 warpgroups):
-//   warp 0      producer (lane 0 issues TMA; all lanes stage LSE and D)
+//   warp 0      producer (lane 0 issues the TMA and bulk copies)
 //   warp 1      MMA issuer (lane 0); allocates and frees TMEM
 //   warps 2-3   idle (they complete the first warpgroup's register release)
 //   warps 4-7   P / dS group: one thread per key row of the tile
 //   warps 8-11  dQ group: adds each dQ tile into the fp32 accumulator, then
 //               writes dK and dV at the end of the unit
 // The first warpgroup gives up registers (setmaxnreg) so the P / dS group,
-// which keeps a packed row of P^T in registers, can hold 224 per thread
-// (112 + 224 + 168 per thread of each warpgroup = the launch's 384 x 168).
+// which keeps a packed row of P^T in registers, can hold 232 per thread
+// (112 + 232 + 160 per thread of each warpgroup = the launch's 384 x 168).
 // TMEM (512 columns): dV [0,128), dK [128,256), S^T [256,384), dP^T [384,512).
 // Per query tile the MMA warp issues
 //   S^T  = K Q^T        (A = K, B = Q, both K-major in smem)
@@ -48,7 +48,8 @@ constexpr int BT = 128;                   // rows per tile (keys and queries)
 constexpr int BOX_BYTES = 128 * 64 * 2;   // one TMA box: 128 rows x 64 bf16
 constexpr int NUM_THREADS = 384;         // dK/dV kernel: three warpgroups
 constexpr int REG_CTRL = 112;             // producer / MMA warpgroup
-constexpr int REG_PDS = 224;             // P / dS warpgroup
+constexpr int REG_PDS = 232;             // P / dS warpgroup
+constexpr int REG_DQ = 160;              // dQ / epilogue warpgroup
 constexpr int REG_LAUNCH = 168;          // 65536 / 384, what the launch bound gives
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -78,8 +79,9 @@ struct Order {
 
 struct Params {
   Problem p;
-  const float* LSE;
-  const float* D;
+  const float* LSE2;       // [BH, Tq_pad]: LSE * log2(e), +inf on padding / no-key rows
+  const float* D;          // [BH, Tq_pad]
+  int Tq_pad;
   float* dQacc;            // atomic path: fp32 [BH, Tq, d], pre-zeroed
   __nv_bfloat16* dQ;       // deterministic path output
   __nv_bfloat16* dK;
@@ -199,15 +201,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int wg = warp >> 2;
   if (wg == 0) {
    ptx::reg_release<REG_CTRL>();
-   if (warp == 0) {
+   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
     ptx::WaitCtx w{abort_flag, P.status, 1u};
-    if (lane == 0) {
-      ptx::tma_prefetch_desc(&tmQ);
-      ptx::tma_prefetch_desc(&tmK);
-      ptx::tma_prefetch_desc(&tmV);
-      ptx::tma_prefetch_desc(&tmdO);
-    }
+    ptx::tma_prefetch_desc(&tmQ);
+    ptx::tma_prefetch_desc(&tmK);
+    ptx::tma_prefetch_desc(&tmV);
+    ptx::tma_prefetch_desc(&tmdO);
     uint32_t u_it = 0, q_it = 0;
     bool ok = true;
     int bh, kb;
@@ -215,43 +215,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int q0, nq;
       q_range(P, kb, &q0, &nq);
       if (nq == 0) continue;
-      if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(kv_empty, (u_it & 1u) ^ 1u, w)))) break;
-      if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
-        for (int b = 0; b < C::KB; ++b) {
-          ptx::tma_load_3d(sK + b * BOX_BYTES, &tmK, kv_full, b * 64, kb * BT, bh);
-          ptx::tma_load_3d(sV + b * BOX_BYTES, &tmV, kv_full, b * 64, kb * BT, bh);
-        }
+      if (!(ok = ptx::mbar_wait(kv_empty, (u_it & 1u) ^ 1u, w))) break;
+      ptx::mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
+      for (int b = 0; b < C::KB; ++b) {
+        ptx::tma_load_3d(sK + b * BOX_BYTES, &tmK, kv_full, b * 64, kb * BT, bh);
+        ptx::tma_load_3d(sV + b * BOX_BYTES, &tmV, kv_full, b * 64, kb * BT, bh);
       }
       for (int ii = 0; ii < nq; ++ii, ++q_it) {
         const int st = q_it & 1;
         const uint32_t ph = (q_it >> 1) & 1u;
-        if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(q_empty + st, ph ^ 1u, w)))) break;
+        if (!(ok = ptx::mbar_wait(q_empty + st, ph ^ 1u, w))) break;
         const int qt = q0 + ii;
-        // LSE (as log2 units; +inf where the row has no key or is past Tq) and D
-        for (int r = lane; r < BT; r += 32) {
-          const int q = qt * BT + r;
-          float l2 = CUDART_INF_F, dd = 0.f;
-          if (q < Tq) {
-            const float lse = P.LSE[static_cast<size_t>(bh) * Tq + q];
-            l2 = (lse == -CUDART_INF_F) ? CUDART_INF_F : lse * LOG2E;
-            dd = P.D[static_cast<size_t>(bh) * Tq + q];
-          }
-          sLSE[st * BT + r] = l2;
-          sD[st * BT + r] = dd;
+        const size_t row0 = static_cast<size_t>(bh) * P.Tq_pad + static_cast<size_t>(qt) * BT;
+        ptx::mbar_arrive_expect_tx(q_full + st, 2 * C::TILE + 2 * BT * 4);
+        for (int b = 0; b < C::KB; ++b) {
+          ptx::tma_load_3d(sQ + st * C::TILE + b * BOX_BYTES, &tmQ, q_full + st, b * 64, qt * BT, bh);
+          ptx::tma_load_3d(sdO + st * C::TILE + b * BOX_BYTES, &tmdO, q_full + st, b * 64, qt * BT, bh);
         }
-        __syncwarp();
-        if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(q_full + st, 2 * C::TILE);
-          for (int b = 0; b < C::KB; ++b) {
-            ptx::tma_load_3d(sQ + st * C::TILE + b * BOX_BYTES, &tmQ, q_full + st, b * 64, qt * BT, bh);
-            ptx::tma_load_3d(sdO + st * C::TILE + b * BOX_BYTES, &tmdO, q_full + st, b * 64, qt * BT, bh);
-          }
-        }
+        ptx::bulk_load(sLSE + st * BT, P.LSE2 + row0, BT * 4, q_full + st);
+        ptx::bulk_load(sD + st * BT, P.D + row0, BT * 4, q_full + st);
       }
       ++u_it;
     }
-    if (!ok && lane == 0) {
+    if (!ok) {
       if (u_it > 0 || q_it > 0) ptx::mbar_wait_drain(kv_full, u_it & 1u);
       for (uint32_t n = (q_it > 2u ? q_it - 2u : 0u); n < q_it; ++n) ptx::mbar_wait_drain(q_full + (n & 1), (n >> 1) & 1u);
     }
@@ -379,11 +365,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // signalled the MMA warp may overwrite S^T with the next tile's scores.
         const int lim = P.p.causal ? key - qt * BT : 0;   // q index (within tile) below which P = 0
         uint32_t pkeep[4][16];
+        uint32_t rs[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tST + c * 32, rs[c]);   // all four in flight
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld_wait(rs[c]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          ptx::tmem_ld32(tST + c * 32, r);
-          ptx::tmem_ld_wait(r);
+          const uint32_t (&r)[32] = rs[c];
 #pragma unroll
           for (int i = 0; i < 16; i += 2) {
             const int qa = c * 32 + 2 * i;
@@ -407,11 +396,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // pass 2: dS^T_j,q = P^T (dP^T - D_q); bf16 over dP^T and into smem (dS, MN-major)
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dp_full, sp & 1u, w)))) break;
         ptx::tc_fence_after();
+        // two 32-column chunks in flight at a time (all four would not fit
+        // beside the 64 registers of packed P^T)
+        uint32_t rd[2][32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          ptx::tmem_ld32(tDP + c * 32, r);
-          ptx::tmem_ld_wait(r);
+          if ((c & 1) == 0) {
+            ptx::tmem_ld32(tDP + c * 32, rd[0]);
+            ptx::tmem_ld32(tDP + c * 32 + 32, rd[1]);
+            ptx::tmem_ld_wait(rd[0]);
+            ptx::tmem_ld_wait(rd[1]);
+          }
+          const uint32_t (&r)[32] = rd[c & 1];
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; i += 2) {
@@ -438,6 +434,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
   } else if (wg == 2) {
+    ptx::reg_release<REG_DQ>();
     // ------------------------------------------------------------ dQ adds; dK / dV epilogue
     const int quad = warp & 3;
     const int r = quad * 32 + lane;                 // TMEM lane = row
@@ -712,23 +709,23 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       const int nk = nk_of(qt);
       const int q = qt * BT + r;
       const bool q_ok = q < Tq;
-      float lse2 = CUDART_INF_F, dd = 0.f;
-      if (q_ok) {
-        const float lse = P.LSE[static_cast<size_t>(bh) * Tq + q];
-        lse2 = (lse == -CUDART_INF_F) ? CUDART_INF_F : lse * LOG2E;
-        dd = P.D[static_cast<size_t>(bh) * Tq + q];
-      }
+      // padding rows hold LSE2 = +inf and D = 0, so their P and dS are 0
+      const float lse2 = P.LSE2[static_cast<size_t>(bh) * P.Tq_pad + q];
+      const float dd = P.D[static_cast<size_t>(bh) * P.Tq_pad + q];
       for (int j = 0; j < nk; ++j, ++sp) {
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(s_full, sp & 1u, w)))) break;
         ptx::tc_fence_after();
         float p[128];
+        {
+          uint32_t v[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          ptx::tmem_ld32(tS + c * 32, v);
-          ptx::tmem_ld_wait(v);
+          for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, v[c]);   // all four in flight
 #pragma unroll
-          for (int i = 0; i < 32; ++i) p[c * 32 + i] = ptx::ex2(fmaf(__uint_as_float(v[i]), sc2, -lse2));
+          for (int c = 0; c < 4; ++c) ptx::tmem_ld_wait(v[c]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) p[c * 32 + i] = ptx::ex2(fmaf(__uint_as_float(v[c][i]), sc2, -lse2));
         }
         ptx::tc_fence_before();
         ptx::mbar_arrive(s_free);
@@ -741,16 +738,18 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         }
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dp_full, sp & 1u, w)))) break;
         ptx::tc_fence_after();
+        uint32_t v[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tDP + c * 32, v[c]);   // all four in flight
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld_wait(v[c]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          ptx::tmem_ld32(tDP + c * 32, v);
-          ptx::tmem_ld_wait(v);
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            pk[i] = ptx::pack_bf16(p[c * 32 + 2 * i] * (__uint_as_float(v[2 * i]) - dd),
-                                   p[c * 32 + 2 * i + 1] * (__uint_as_float(v[2 * i + 1]) - dd));
+            pk[i] = ptx::pack_bf16(p[c * 32 + 2 * i] * (__uint_as_float(v[c][2 * i]) - dd),
+                                   p[c * 32 + 2 * i + 1] * (__uint_as_float(v[c][2 * i + 1]) - dd));
           ptx::tmem_st16(tDP + c * 16, pk);
         }
         ptx::tmem_st_wait();
@@ -808,13 +807,15 @@ cudaError_t launch(const LaunchBwd& a) {
              conv = a.phase == 0 || a.phase == 3;
   cudaError_t e = cudaSuccess;
   if (pre) {
-    e = launch_bwd_preprocess(p, a.O, a.dO, 2, a.D, atomic ? a.dQacc : nullptr, p.d, a.num_sms, a.stream);
+    e = launch_bwd_preprocess(p, a.O, a.dO, a.LSE, 2, a.D, a.LSE2, atomic ? a.dQacc : nullptr, p.d, a.num_sms,
+                              a.stream);
     if (e != cudaSuccess) return e;
   }
   Params P{};
   P.p = p;
-  P.LSE = a.LSE;
+  P.LSE2 = a.LSE2;
   P.D = a.D;
+  P.Tq_pad = padded_rows(p.Tq);
   P.dQacc = a.dQacc;
   P.dQ = static_cast<__nv_bfloat16*>(a.dQ);
   P.dK = static_cast<__nv_bfloat16*>(a.dK);
@@ -834,7 +835,7 @@ cudaError_t launch(const LaunchBwd& a) {
     // The register split must fit the launch allocation (see reg_acquire).
     cudaFuncAttributes fa;
     if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
-    if (fa.numRegs < REG_CTRL || fa.numRegs > REG_PDS || 2 * fa.numRegs < REG_CTRL + REG_PDS)
+    if (fa.numRegs != REG_LAUNCH || REG_CTRL + REG_PDS + REG_DQ > 3 * REG_LAUNCH)
       return cudaErrorInvalidConfiguration;
     kern<<<grid, NUM_THREADS, CfgKV<HD>::SMEM, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO, P);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

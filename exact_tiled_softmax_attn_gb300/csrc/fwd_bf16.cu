@@ -320,9 +320,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int i = 0; i < 128; ++i)
             if (i >= lim) s[i] = -CUDART_INF_F;
         }
-        float mx = s[0];
+        // row max as 8 independent chains (a single chain is ~128 dependent ops)
+        float m8[8];
 #pragma unroll
-        for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(s[k], s[k + 8]);
+#pragma unroll
+        for (int i = 16; i < 128; i += 8)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], s[i + k]);
+        float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         mx *= sc2;
         const float m_new = fmaxf(m_used, mx);
         // Lazy rescale: move the reference max only when it grows by > TAU.
@@ -337,7 +344,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           m_used = m_new;
         }
         const float ref = (m_used == -CUDART_INF_F) ? 0.f : m_used;   // the -inf rule
-        float lsum = 0.f;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};   // row sum as 4 independent chains
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t pk[32];
@@ -345,12 +352,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int i = 0; i < 32; ++i) {
             const float p0 = ptx::ex2(fmaf(s[64 * h + 2 * i], sc2, -ref));
             const float p1 = ptx::ex2(fmaf(s[64 * h + 2 * i + 1], sc2, -ref));
-            lsum += p0 + p1;
+            ls[i & 3] += p0 + p1;
             pk[i] = ptx::pack_bf16(p0, p1);
           }
           ptx::tmem_st32(tS + 32 * h, pk);
         }
-        l += lsum;
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         if (__any_sync(0xffffffffu, need)) {
           // O_t *= corr before the next PV product accumulates into it. The
           // previous PV into O_t is complete: it was issued before the S

@@ -224,7 +224,7 @@ __device__ __forceinline__ void load_qrow_stats(float* sLse, float* sD, const fl
   if (threadIdx.x < BM) {
     const int qi = q0 + threadIdx.x;
     sLse[threadIdx.x] = qi < Tq ? LSE[bh * Tq + qi] : -CUDART_INF_F;
-    sD[threadIdx.x] = qi < Tq ? D[bh * Tq + qi] : 0.f;
+    sD[threadIdx.x] = qi < Tq ? D[bh * padded_rows(Tq) + qi] : 0.f;
   }
 }
 
@@ -405,8 +405,8 @@ cudaError_t launch_bwd_f32(const LaunchBwd& a) {
   cudaError_t e = cudaSuccess;
   if (a.phase == 0 || a.phase == 1) {
     // D = rowsum(dO o O); dQ zeroed when it is accumulated with atomics.
-    e = launch_bwd_preprocess(p, a.O, a.dO, 4, a.D, a.deterministic ? nullptr : static_cast<float*>(a.dQ), p.d,
-                              a.num_sms, a.stream);
+    e = launch_bwd_preprocess(p, a.O, a.dO, a.LSE, 4, a.D, a.LSE2,
+                              a.deterministic ? nullptr : static_cast<float*>(a.dQ), p.d, a.num_sms, a.stream);
     if (e != cudaSuccess) return e;
   }
   if (a.phase != 0 && a.phase != 2) return cudaSuccess;

@@ -37,13 +37,17 @@ __device__ __forceinline__ float dot16(const uint4& a, const uint4& b, const flo
 
 // D_i = sum_c dO_ic * O_ic ("attention_backprop", section "Gradient of S":
 // ROW_SUM(dL/dO o O); the delta-l term of "The Hidden Recurrence in Softmax
-// Attention", section "Flash Attention Backward Pass"). Each group of LPR
-// lanes reads one row with 16-byte loads; rows are walked grid-stride.
-// Optionally zeroes the matching row of an fp32 accumulator.
+// Attention", section "Flash Attention Backward Pass"), written with the
+// stored log-sum-exp in log2 units into [B*H, Tq_pad] arrays whose padding
+// rows hold D = 0 and LSE2 = +inf (so exp2(s - LSE2) = 0 there). The backward
+// fetches a 128-row slice of each with one bulk copy. Each group of LPR lanes
+// reads one row with 16-byte loads; rows are walked grid-stride. Optionally
+// zeroes the matching row of an fp32 accumulator.
 template <typename T>
 __global__ void __launch_bounds__(NT) preprocess_vec(const T* __restrict__ O, const T* __restrict__ dO,
-                                                      float* __restrict__ D, float* __restrict__ zero_rows,
-                                                      int zero_cols, long long rows, int dv) {
+                                                      const float* __restrict__ LSE, float* __restrict__ D,
+                                                      float* __restrict__ LSE2, float* __restrict__ zero_rows,
+                                                      int zero_cols, long long rows_pad, int Tq, int Tq_pad, int dv) {
   const int chunks = dv * static_cast<int>(sizeof(T)) / 16;   // 16-byte chunks per row (<= 32)
   const int lpr = chunks;                                      // lanes per row
   const int rows_per_warp = 32 / lpr;
@@ -51,37 +55,54 @@ __global__ void __launch_bounds__(NT) preprocess_vec(const T* __restrict__ O, co
   const int sub = lane / lpr, c = lane - sub * lpr;
   const long long warp_id = (static_cast<long long>(blockIdx.x) * NT + threadIdx.x) >> 5;
   const long long n_warps = (static_cast<long long>(gridDim.x) * NT) >> 5;
-  for (long long r0 = warp_id * rows_per_warp; r0 < rows; r0 += n_warps * rows_per_warp) {
-    const long long r = r0 + sub;
+  for (long long r0 = warp_id * rows_per_warp; r0 < rows_pad; r0 += n_warps * rows_per_warp) {
+    const long long rp = r0 + sub;
+    const long long bh = rp / Tq_pad;
+    const int q = static_cast<int>(rp - bh * Tq_pad);
+    const long long r = bh * Tq + q;                           // unpadded row
+    const bool inside = (sub < rows_per_warp) && (rp < rows_pad);
+    const bool real = inside && q < Tq;
     float s = 0.f;
-    const bool ok = (sub < rows_per_warp) && (r < rows);
-    if (ok) {
+    if (real) {
       const uint4 a = reinterpret_cast<const uint4*>(O + r * dv)[c];
       const uint4 b = reinterpret_cast<const uint4*>(dO + r * dv)[c];
       s = dot16(a, b, static_cast<const T*>(nullptr));
     }
     for (int o = lpr >> 1; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (ok && c == 0) D[r] = s;
-    if (ok && zero_rows) {
+    if (inside && c == 0) {
+      D[rp] = s;
+      const float lse = real ? LSE[r] : -CUDART_INF_F;
+      LSE2[rp] = (lse == -CUDART_INF_F) ? CUDART_INF_F : lse * 1.4426950408889634f;
+    }
+    if (real && zero_rows) {
       float4* z = reinterpret_cast<float4*>(zero_rows + r * zero_cols);
       for (int k = c; k < zero_cols / 4; k += lpr) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 }
 
-// Generic fp32 version (any dv): one warp per row.
+// Generic fp32 version (any dv): one warp per padded row.
 __global__ void __launch_bounds__(NT) preprocess_f32(const float* __restrict__ O, const float* __restrict__ dO,
-                                                      float* __restrict__ D, float* __restrict__ zero_rows,
-                                                      int zero_cols, long long rows, int dv) {
+                                                      const float* __restrict__ LSE, float* __restrict__ D,
+                                                      float* __restrict__ LSE2, float* __restrict__ zero_rows,
+                                                      int zero_cols, long long rows_pad, int Tq, int Tq_pad, int dv) {
   const int lane = threadIdx.x & 31;
   const long long warp_id = (static_cast<long long>(blockIdx.x) * NT + threadIdx.x) >> 5;
   const long long n_warps = (static_cast<long long>(gridDim.x) * NT) >> 5;
-  for (long long r = warp_id; r < rows; r += n_warps) {
+  for (long long rp = warp_id; rp < rows_pad; rp += n_warps) {
+    const long long bh = rp / Tq_pad;
+    const int q = static_cast<int>(rp - bh * Tq_pad);
+    const long long r = bh * Tq + q;
     float s = 0.f;
-    for (int c = lane; c < dv; c += 32) s = fmaf(O[r * dv + c], dO[r * dv + c], s);
+    if (q < Tq)
+      for (int c = lane; c < dv; c += 32) s = fmaf(O[r * dv + c], dO[r * dv + c], s);
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) D[r] = s;
-    if (zero_rows)
+    if (lane == 0) {
+      D[rp] = s;
+      const float lse = q < Tq ? LSE[r] : -CUDART_INF_F;
+      LSE2[rp] = (lse == -CUDART_INF_F) ? CUDART_INF_F : lse * 1.4426950408889634f;
+    }
+    if (zero_rows && q < Tq)
       for (int c = lane; c < zero_cols; c += 32) zero_rows[r * zero_cols + c] = 0.f;
   }
 }
@@ -100,26 +121,29 @@ __global__ void zero_kernel(uint8_t* p, size_t bytes) {
 
 }  // namespace small
 
-cudaError_t launch_bwd_preprocess(const Problem& p, const void* O, const void* dO, int elem_bytes, float* D,
-                                  float* zero_rows, int zero_cols, int num_sms, cudaStream_t s) {
-  const long long rows = static_cast<long long>(p.B) * p.H * p.Tq;
-  if (rows == 0) return cudaSuccess;
+cudaError_t launch_bwd_preprocess(const Problem& p, const void* O, const void* dO, const float* LSE, int elem_bytes,
+                                  float* D, float* LSE2, float* zero_rows, int zero_cols, int num_sms,
+                                  cudaStream_t s) {
+  const int Tq_pad = padded_rows(p.Tq);
+  const long long rows_pad = static_cast<long long>(p.B) * p.H * Tq_pad;
+  if (rows_pad == 0) return cudaSuccess;
   const int grid = num_sms * 8;
-  const bool vec = (p.dv * elem_bytes) % 16 == 0 && (p.dv * elem_bytes) / 16 <= 32 &&
-                   ((p.dv * elem_bytes) / 16 & ((p.dv * elem_bytes) / 16 - 1)) == 0 &&
+  const int chunks = p.dv * elem_bytes / 16;
+  const bool vec = (p.dv * elem_bytes) % 16 == 0 && chunks <= 32 && (chunks & (chunks - 1)) == 0 &&
                    (reinterpret_cast<uintptr_t>(O) % 16 == 0) && (reinterpret_cast<uintptr_t>(dO) % 16 == 0) &&
                    (zero_rows == nullptr || (zero_cols % 4 == 0 && reinterpret_cast<uintptr_t>(zero_rows) % 16 == 0));
   if (elem_bytes == 2) {
     small::preprocess_vec<__nv_bfloat16><<<grid, small::NT, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), D, zero_rows, zero_cols, rows,
-        p.dv);
+        static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, D, LSE2, zero_rows,
+        zero_cols, rows_pad, p.Tq, Tq_pad, p.dv);
   } else if (vec) {
     small::preprocess_vec<float><<<grid, small::NT, 0, s>>>(static_cast<const float*>(O),
-                                                             static_cast<const float*>(dO), D, zero_rows,
-                                                             zero_cols, rows, p.dv);
+                                                             static_cast<const float*>(dO), LSE, D, LSE2,
+                                                             zero_rows, zero_cols, rows_pad, p.Tq, Tq_pad, p.dv);
   } else {
     small::preprocess_f32<<<grid, small::NT, 0, s>>>(static_cast<const float*>(O), static_cast<const float*>(dO),
-                                                      D, zero_rows, zero_cols, rows, p.dv);
+                                                      LSE, D, LSE2, zero_rows, zero_cols, rows_pad, p.Tq, Tq_pad,
+                                                      p.dv);
   }
   return cudaGetLastError();
 }

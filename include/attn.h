@@ -92,8 +92,10 @@ ATTN_API attn_status_t attn_fwd_f32_blocked(const float* Q, const float* K, cons
 
 /*
  * Bytes of device workspace attn_bwd needs for this problem (0 is possible).
- * Holds D [B,H,Tq] fp32 and, for bf16 with deterministic == 0, the fp32 dQ
- * accumulator [B,H,Tq,d]. Returns 0 for invalid arguments as well.
+ * Holds LSE * log2(e) and D = rowsum(dO o O), each [B*H, Tq_pad] fp32 with
+ * Tq_pad = Tq rounded up to a multiple of 128, and, for bf16 with
+ * deterministic == 0, the fp32 dQ accumulator [B,H,Tq,d]; each part starts on
+ * a 256-byte boundary. Returns 0 for invalid arguments as well.
  */
 ATTN_API size_t attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype,
                                int deterministic);
@@ -154,8 +156,8 @@ ATTN_API attn_status_t attn_bwd_phase(const void* Q, const void* K, const void* 
  * ATTN_NOALLOC_SCRATCH_BYTES inside the library. Nothing is allocated and no
  * allocating routine is called. Problems whose attn_bwd_workspace_size
  * exceeds that size are rejected with ATTN_ERR_WORKSPACE before anything is
- * enqueued (for bf16 with deterministic == 0 the need is B*H*Tq*(d+1)*4
- * bytes; deterministic == 1 or fp32 needs only B*H*Tq*4).
+ * enqueued (for bf16 with deterministic == 0 the need is about
+ * B*H*Tq*(d+2)*4 bytes; deterministic == 1 or fp32 needs about B*H*Tq*8).
  *
  * The first call on a device (with that device current) looks up the
  * buffer's device address once; make that first call before any stream

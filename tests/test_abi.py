@@ -93,13 +93,13 @@ def test_blocked_forward_validates_block(lib):
 
 
 def test_workspace_size(lib):
-    f32 = B.attn_bwd_workspace_size(2, 3, 100, 50, 64, 64, B.ATTN_F32, 0)
-    assert f32 == 2 * 3 * 100 * 4
-    bf_det = B.attn_bwd_workspace_size(2, 3, 100, 50, 64, 64, B.ATTN_BF16, 1)
-    assert bf_det == 2 * 3 * 100 * 4
-    bf_atomic = B.attn_bwd_workspace_size(2, 3, 100, 50, 64, 64, B.ATTN_BF16, 0)
-    d_bytes = 2 * 3 * 100 * 4
-    assert bf_atomic == (d_bytes + 255) // 256 * 256 + 2 * 3 * 100 * 64 * 4
+    # LSE*log2(e) and D, each [B*H, Tq rounded up to 128] fp32 and 256-byte
+    # aligned, then (bf16 with fp32 dQ accumulation) the [B*H*Tq, d] accumulator
+    part = (2 * 3 * 128 * 4 + 255) // 256 * 256
+    assert B.attn_bwd_workspace_size(2, 3, 100, 50, 64, 64, B.ATTN_F32, 0) == 2 * part
+    assert B.attn_bwd_workspace_size(2, 3, 100, 50, 64, 64, B.ATTN_BF16, 1) == 2 * part
+    assert B.attn_bwd_workspace_size(2, 3, 100, 50, 64, 64, B.ATTN_BF16, 0) == 2 * part + 2 * 3 * 100 * 64 * 4
+    assert B.attn_bwd_workspace_size(2, 3, 0, 50, 64, 64, B.ATTN_BF16, 0) == 0
     assert B.attn_bwd_workspace_size(-1, 3, 100, 50, 64, 64, B.ATTN_BF16, 0) == 0
 
 

@@ -52,7 +52,7 @@ def test_noalloc_matches_workspace_backward_twice(case):
 
 
 def test_noalloc_rejects_problems_beyond_its_buffer():
-    # bf16 with the fp32 dQ accumulator: B*H*Tq*(d+1)*4 bytes > 64 MiB
+    # bf16 with the fp32 dQ accumulator: about B*H*Tq*(d+2)*4 bytes > 64 MiB
     B, H, T, d = 4, 16, 2048, 128
     assert pkg.attn_bwd_workspace_size(B, H, T, T, d, d, pkg.ATTN_BF16, 0) > pkg.ATTN_NOALLOC_SCRATCH_BYTES
     st = pkg.attn_bwd_noalloc(0x100000, 0x200000, 0x300000, 0x400000, 0x500000, 0x600000, 0x700000,
