@@ -72,21 +72,23 @@ attn_status_t encoder(EncodeTiledFn* fn) {
   return ATTN_OK;
 }
 
-// 3-D bf16 map over a [planes, rows, inner] array, 128-byte swizzled boxes of
-// 128 rows x 64 elements. Rows past `rows` read as zero within each plane.
-attn_status_t make_map(CUtensorMap* m, const void* base, int inner, int rows, int planes) {
+// 3-D map over a [planes, rows, inner] array with 128-byte swizzled boxes of
+// 128 rows x (128 bytes of elements): 64 bf16 or 32 fp32. Rows past `rows`
+// read as zero within each plane (and are not written by reduces).
+attn_status_t make_map(CUtensorMap* m, const void* base, int inner, int rows, int planes, bool f32 = false) {
   EncodeTiledFn enc;
   attn_status_t s = encoder(&enc);
   if (s != ATTN_OK) return s;
+  const cuuint64_t es = f32 ? 4 : 2;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(planes)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 2,
-                                 static_cast<cuuint64_t>(inner) * 2 * static_cast<cuuint64_t>(rows)};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * es,
+                                 static_cast<cuuint64_t>(inner) * es * static_cast<cuuint64_t>(rows)};
+  const cuuint32_t box[3] = {f32 ? 32u : 64u, 128, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     t_last_cuda_error = static_cast<int>(r);
     return ATTN_ERR_CUDA;
@@ -320,7 +322,7 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
   if (dtype == ATTN_F32) {
     e = launch_bwd_f32(a);
   } else {
-    CUtensorMap mq, mk, mv, mdo;
+    CUtensorMap mq, mk, mv, mdo, mdq;
     if ((s = make_map(&mq, Q, d, Tq, static_cast<int>(bh))) != ATTN_OK) return s;
     if ((s = make_map(&mk, K, d, Tk, static_cast<int>(bh))) != ATTN_OK) return s;
     if ((s = make_map(&mv, V, dv, Tk, static_cast<int>(bh))) != ATTN_OK) return s;
@@ -329,6 +331,11 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
     a.tmK = &mk;
     a.tmV = &mv;
     a.tmdO = &mdo;
+    a.tmdQacc = nullptr;
+    if (a.dQacc) {
+      if ((s = make_map(&mdq, a.dQacc, d, Tq, static_cast<int>(bh), true)) != ATTN_OK) return s;
+      a.tmdQacc = &mdq;
+    }
     e = launch_bwd_bf16(a);
   }
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);

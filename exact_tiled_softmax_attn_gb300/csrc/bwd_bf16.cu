@@ -11,17 +11,18 @@
 //
 // dK/dV kernel: one persistent CTA per SM; a work unit is one 128-key tile of
 // one head, and the CTA loops over the query tiles that can see it. K and V
-// stay in shared memory for the whole unit; Q, dO (TMA) and LSE, D (plain
-// loads) stream through a two-stage ring. Warp roles (12 warps, 3 warpgroups):
-//   warp 0      producer (lane 0 issues the TMA and bulk copies)
-//   warp 1      MMA issuer (lane 0); allocates and frees TMEM
-//   warps 2-3   idle (they complete the first warpgroup's register release)
-//   warps 4-7   P / dS group: one thread per key row of the tile
-//   warps 8-11  dQ group: adds each dQ tile into the fp32 accumulator, then
-//               writes dK and dV at the end of the unit
-// The first warpgroup gives up registers (setmaxnreg) so the P / dS group,
-// which keeps a packed row of P^T in registers, can hold 232 per thread
-// (112 + 232 + 160 per thread of each warpgroup = the launch's 384 x 168).
+// stay in shared memory for the whole unit; Q, dO (TMA) and the 128-row slices
+// of LSE2 and D (bulk copies) stream through a two-stage ring. Warp roles (16
+// warps, 4 warpgroups):
+//   warp 0       producer (lane 0 issues the TMA and bulk copies)
+//   warp 1       MMA issuer (lane 0); allocates and frees TMEM
+//   warps 2-3    idle (they complete the first warpgroup's register release)
+//   warps 4-7    P / dS, query columns 0-63 of the tile (one thread per key row)
+//   warps 8-11   P / dS, query columns 64-127
+//   warps 12-15  dQ group: reads each dQ tile out of TMEM, stages it in the dS
+//                buffer in two 64-column halves and adds it into the fp32
+//                accumulator with TMA reduce-add; writes dK and dV per unit
+// setmaxnreg splits the launch's 512 x 128 registers as 104 / 152 / 152 / 104.
 // TMEM (512 columns): dV [0,128), dK [128,256), S^T [256,384), dP^T [384,512).
 // Per query tile the MMA warp issues
 //   S^T  = K Q^T        (A = K, B = Q, both K-major in smem)
@@ -46,11 +47,11 @@ namespace bwd {
 
 constexpr int BT = 128;                   // rows per tile (keys and queries)
 constexpr int BOX_BYTES = 128 * 64 * 2;   // one TMA box: 128 rows x 64 bf16
-constexpr int NUM_THREADS = 384;         // dK/dV kernel: three warpgroups
-constexpr int REG_CTRL = 112;             // producer / MMA warpgroup
-constexpr int REG_PDS = 232;             // P / dS warpgroup
-constexpr int REG_DQ = 160;              // dQ / epilogue warpgroup
-constexpr int REG_LAUNCH = 168;          // 65536 / 384, what the launch bound gives
+constexpr int KV_THREADS = 512;          // dK/dV kernel: four warpgroups
+constexpr int KV_REG_CTRL = 104;         // producer / MMA warpgroup
+constexpr int KV_REG_PDS = 152;          // each of the two P / dS warpgroups
+constexpr int KV_REG_DQ = 104;           // dQ / epilogue warpgroup
+constexpr int KV_REG_LAUNCH = 128;       // 65536 / 512, what the launch bound gives
 constexpr float LOG2E = 1.4426950408889634f;
 
 // Unit order: 0 = head-major, 1 = heavy (large block index) first,
@@ -114,14 +115,16 @@ struct CfgKV {
   static constexpr int OFF_V = OFF_K + TILE;
   static constexpr int OFF_Q = OFF_V + TILE;          // [2]
   static constexpr int OFF_DO = OFF_Q + 2 * TILE;     // [2]
-  static constexpr int OFF_DS = OFF_DO + 2 * TILE;    // dS, 128 q x 128 keys bf16, MN-major
+  // dS, 128 q x 128 keys bf16, MN-major; in atomic mode it then stages one
+  // 64-column half of the fp32 dQ tile (two 128 x 32 boxes) for the TMA reduce
+  static constexpr int OFF_DS = OFF_DO + 2 * TILE;
   static constexpr int DS_BYTES = BT * BT * 2;
   static constexpr int OFF_LSE = OFF_DS + DS_BYTES;   // [2][128] fp32 (LSE * log2 e, +inf = no key)
   static constexpr int OFF_D = OFF_LSE + 2 * BT * 4;  // [2][128] fp32
   static constexpr int OFF_BAR = OFF_D + 2 * BT * 4;
   // kv_full, kv_empty, q_full[2], q_empty[2], s_full, dp_full, p_full, ds_full,
-  // dq_full, dq_free, acc_full, acc_free, drain
-  static constexpr int NBAR = 15;
+  // dq_full, dq_free, acc_full, acc_free, stage_full, stage_free, sds_free, drain
+  static constexpr int NBAR = 18;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16(BT, BT, false, false);
@@ -129,11 +132,17 @@ struct CfgKV {
   static constexpr uint32_t IDESC_DQ = ptx::idesc_bf16(BT, HD, true, true);     // dQ = dS K
 };
 
+// TMEM column of k-step kk (16 query columns, 8 packed columns) of the bf16
+// P^T / dS^T operand: query columns 64h.. are packed at column 64h, where the
+// half-h group read its fp32 scores, so no group overwrites columns the other
+// group has not read yet.
+__device__ __forceinline__ uint32_t packed_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
+
 template <int HD, bool ATOMIC_DQ>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(KV_THREADS, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                const Params P) {
+                const __grid_constant__ CUtensorMap tmdQ, const Params P) {
   using C = CfgKV<HD>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
@@ -162,7 +171,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* dq_free = bars + 11;
   uint64_t* acc_full = bars + 12;
   uint64_t* acc_free = bars + 13;
-  uint64_t* drain = bars + 14;
+  uint64_t* stage_full = bars + 14;
+  uint64_t* stage_free = bars + 15;
+  uint64_t* sds_free = bars + 16;
+  uint64_t* drain = bars + 17;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
 
@@ -175,12 +187,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     ptx::mbar_init(s_full, 1);
     ptx::mbar_init(dp_full, 1);
-    ptx::mbar_init(p_full, 128);
-    ptx::mbar_init(ds_full, 128);
+    ptx::mbar_init(p_full, 256);
+    ptx::mbar_init(ds_full, 256);
     ptx::mbar_init(dq_full, 1);
     ptx::mbar_init(dq_free, 128);
     ptx::mbar_init(acc_full, 1);
     ptx::mbar_init(acc_free, 128);
+    ptx::mbar_init(stage_full, 128);
+    ptx::mbar_init(stage_free, 1);
+    ptx::mbar_init(sds_free, 1);
     ptx::mbar_init(drain, 1);
     *abort_flag = 0u;
     ptx::fence_mbar_init();
@@ -197,149 +212,152 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int grid = gridDim.x, cta = blockIdx.x;
   const int Tq = P.p.Tq, Tk = P.p.Tk;
-
   const int wg = warp >> 2;
+
   if (wg == 0) {
-   ptx::reg_release<REG_CTRL>();
-   if (warp == 0 && lane == 0) {
-    // ------------------------------------------------------------ producer
-    ptx::WaitCtx w{abort_flag, P.status, 1u};
-    ptx::tma_prefetch_desc(&tmQ);
-    ptx::tma_prefetch_desc(&tmK);
-    ptx::tma_prefetch_desc(&tmV);
-    ptx::tma_prefetch_desc(&tmdO);
-    uint32_t u_it = 0, q_it = 0;
-    bool ok = true;
-    int bh, kb;
-    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &kb); ++round) {
-      int q0, nq;
-      q_range(P, kb, &q0, &nq);
-      if (nq == 0) continue;
-      if (!(ok = ptx::mbar_wait(kv_empty, (u_it & 1u) ^ 1u, w))) break;
-      ptx::mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
-      for (int b = 0; b < C::KB; ++b) {
-        ptx::tma_load_3d(sK + b * BOX_BYTES, &tmK, kv_full, b * 64, kb * BT, bh);
-        ptx::tma_load_3d(sV + b * BOX_BYTES, &tmV, kv_full, b * 64, kb * BT, bh);
-      }
-      for (int ii = 0; ii < nq; ++ii, ++q_it) {
-        const int st = q_it & 1;
-        const uint32_t ph = (q_it >> 1) & 1u;
-        if (!(ok = ptx::mbar_wait(q_empty + st, ph ^ 1u, w))) break;
-        const int qt = q0 + ii;
-        const size_t row0 = static_cast<size_t>(bh) * P.Tq_pad + static_cast<size_t>(qt) * BT;
-        ptx::mbar_arrive_expect_tx(q_full + st, 2 * C::TILE + 2 * BT * 4);
+    ptx::reg_release<KV_REG_CTRL>();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- producer
+      ptx::WaitCtx w{abort_flag, P.status, 1u};
+      ptx::tma_prefetch_desc(&tmQ);
+      ptx::tma_prefetch_desc(&tmK);
+      ptx::tma_prefetch_desc(&tmV);
+      ptx::tma_prefetch_desc(&tmdO);
+      uint32_t u_it = 0, q_it = 0;
+      bool ok = true;
+      int bh, kb;
+      for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &kb); ++round) {
+        int q0, nq;
+        q_range(P, kb, &q0, &nq);
+        if (nq == 0) continue;
+        if (!(ok = ptx::mbar_wait(kv_empty, (u_it & 1u) ^ 1u, w))) break;
+        ptx::mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
         for (int b = 0; b < C::KB; ++b) {
-          ptx::tma_load_3d(sQ + st * C::TILE + b * BOX_BYTES, &tmQ, q_full + st, b * 64, qt * BT, bh);
-          ptx::tma_load_3d(sdO + st * C::TILE + b * BOX_BYTES, &tmdO, q_full + st, b * 64, qt * BT, bh);
+          ptx::tma_load_3d(sK + b * BOX_BYTES, &tmK, kv_full, b * 64, kb * BT, bh);
+          ptx::tma_load_3d(sV + b * BOX_BYTES, &tmV, kv_full, b * 64, kb * BT, bh);
         }
-        ptx::bulk_load(sLSE + st * BT, P.LSE2 + row0, BT * 4, q_full + st);
-        ptx::bulk_load(sD + st * BT, P.D + row0, BT * 4, q_full + st);
-      }
-      ++u_it;
-    }
-    if (!ok) {
-      if (u_it > 0 || q_it > 0) ptx::mbar_wait_drain(kv_full, u_it & 1u);
-      for (uint32_t n = (q_it > 2u ? q_it - 2u : 0u); n < q_it; ++n) ptx::mbar_wait_drain(q_full + (n & 1), (n >> 1) & 1u);
-    }
-   } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
-    ptx::WaitCtx w{abort_flag, P.status, 2u};
-    const uint32_t aK = ptx::smem_u32(sK), aV = ptx::smem_u32(sV), aQ = ptx::smem_u32(sQ),
-                   adO = ptx::smem_u32(sdO), adS = ptx::smem_u32(sdS);
-    auto kmaj = [](uint32_t base, int kk) {  // K-major operand, k-step kk of 16 elements
-      return ptx::sdesc_sw128(base + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
-    };
-    auto mnmaj = [](uint32_t base, int kk) {  // MN-major operand, k-step kk of 16 rows
-      return ptx::sdesc_sw128(base + kk * 2048, BOX_BYTES, 1024);
-    };
-    auto mma_st = [&](int st) {
-      for (int kk = 0; kk < HD / 16; ++kk)
-        ptx::mma_ss(tmem + T_ST, kmaj(aK, kk), kmaj(aQ + st * C::TILE, kk), C::IDESC_S, kk > 0);
-    };
-    auto mma_dpt = [&](int st) {
-      for (int kk = 0; kk < HD / 16; ++kk)
-        ptx::mma_ss(tmem + T_DP, kmaj(aV, kk), kmaj(adO + st * C::TILE, kk), C::IDESC_S, kk > 0);
-    };
-    uint32_t u_it = 0, q_it = 0, pp = 0, dqf = 0;
-    bool ok = true;
-    int bh, kb;
-    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &kb); ++round) {
-      int q0, nq;
-      q_range(P, kb, &q0, &nq);
-      if (nq == 0) continue;
-      if (!(ok = ptx::mbar_wait(kv_full, u_it & 1u, w))) break;
-      if (!(ok = ptx::mbar_wait(acc_free, (u_it & 1u) ^ 1u, w))) break;
-      {
-        const int st = q_it & 1;
-        if (!(ok = ptx::mbar_wait(q_full + st, (q_it >> 1) & 1u, w))) break;
-        ptx::tc_fence_after();
-        mma_st(st);
-        ptx::mma_commit(s_full);
-        if (ATOMIC_DQ && dqf > 0) {
-          if (!(ok = ptx::mbar_wait(dq_free, (dqf - 1) & 1u, w))) break;
-          ptx::tc_fence_after();
+        for (int ii = 0; ii < nq; ++ii, ++q_it) {
+          const int st = q_it & 1;
+          const uint32_t ph = (q_it >> 1) & 1u;
+          if (!(ok = ptx::mbar_wait(q_empty + st, ph ^ 1u, w))) break;
+          const int qt = q0 + ii;
+          const size_t row0 = static_cast<size_t>(bh) * P.Tq_pad + static_cast<size_t>(qt) * BT;
+          ptx::mbar_arrive_expect_tx(q_full + st, 2 * C::TILE + 2 * BT * 4);
+          for (int b = 0; b < C::KB; ++b) {
+            ptx::tma_load_3d(sQ + st * C::TILE + b * BOX_BYTES, &tmQ, q_full + st, b * 64, qt * BT, bh);
+            ptx::tma_load_3d(sdO + st * C::TILE + b * BOX_BYTES, &tmdO, q_full + st, b * 64, qt * BT, bh);
+          }
+          ptx::bulk_load(sLSE + st * BT, P.LSE2 + row0, BT * 4, q_full + st);
+          ptx::bulk_load(sD + st * BT, P.D + row0, BT * 4, q_full + st);
         }
-        mma_dpt(st);
-        ptx::mma_commit(dp_full);
+        ++u_it;
       }
-      for (int ii = 0; ii < nq; ++ii) {
-        const uint32_t it = q_it + ii;
-        const int st = it & 1, stn = (it + 1) & 1;
-        // dV += P^T dO
-        if (!(ok = ptx::mbar_wait(p_full, pp & 1u, w))) break;
-        ptx::tc_fence_after();
-        for (int kk = 0; kk < BT / 16; ++kk)
-          ptx::mma_ts(tmem + T_DV, tmem + T_ST + kk * 8, mnmaj(adO + st * C::TILE, kk), C::IDESC_ACC,
-                      (ii > 0 || kk > 0) ? 1u : 0u);
-        // next S^T (overwrites P^T only after the product above has read it)
-        if (ii + 1 < nq) {
-          if (!(ok = ptx::mbar_wait(q_full + stn, ((it + 1) >> 1) & 1u, w))) break;
+      if (!ok) {
+        if (u_it > 0 || q_it > 0) ptx::mbar_wait_drain(kv_full, u_it & 1u);
+        for (uint32_t n = (q_it > 2u ? q_it - 2u : 0u); n < q_it; ++n)
+          ptx::mbar_wait_drain(q_full + (n & 1), (n >> 1) & 1u);
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      ptx::WaitCtx w{abort_flag, P.status, 2u};
+      const uint32_t aK = ptx::smem_u32(sK), aV = ptx::smem_u32(sV), aQ = ptx::smem_u32(sQ),
+                     adO = ptx::smem_u32(sdO), adS = ptx::smem_u32(sdS);
+      auto kmaj = [](uint32_t base, int kk) {  // K-major operand, k-step kk of 16 elements
+        return ptx::sdesc_sw128(base + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
+      };
+      auto mnmaj = [](uint32_t base, int kk) {  // MN-major operand, k-step kk of 16 rows
+        return ptx::sdesc_sw128(base + kk * 2048, BOX_BYTES, 1024);
+      };
+      auto mma_st = [&](int st) {
+        for (int kk = 0; kk < HD / 16; ++kk)
+          ptx::mma_ss(tmem + T_ST, kmaj(aK, kk), kmaj(aQ + st * C::TILE, kk), C::IDESC_S, kk > 0);
+      };
+      auto mma_dpt = [&](int st) {
+        for (int kk = 0; kk < HD / 16; ++kk)
+          ptx::mma_ss(tmem + T_DP, kmaj(aV, kk), kmaj(adO + st * C::TILE, kk), C::IDESC_S, kk > 0);
+      };
+      uint32_t u_it = 0, q_it = 0, pp = 0, dqf = 0;
+      bool ok = true;
+      int bh, kb;
+      for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &kb); ++round) {
+        int q0, nq;
+        q_range(P, kb, &q0, &nq);
+        if (nq == 0) continue;
+        if (!(ok = ptx::mbar_wait(kv_full, u_it & 1u, w))) break;
+        if (!(ok = ptx::mbar_wait(acc_free, (u_it & 1u) ^ 1u, w))) break;
+        {
+          const int st = q_it & 1;
+          if (!(ok = ptx::mbar_wait(q_full + st, (q_it >> 1) & 1u, w))) break;
           ptx::tc_fence_after();
-          mma_st(stn);
+          mma_st(st);
           ptx::mma_commit(s_full);
-        }
-        // dK += dS^T Q
-        if (!(ok = ptx::mbar_wait(ds_full, pp & 1u, w))) break;
-        ++pp;
-        ptx::tc_fence_after();
-        for (int kk = 0; kk < BT / 16; ++kk)
-          ptx::mma_ts(tmem + T_DK, tmem + T_DP + kk * 8, mnmaj(aQ + st * C::TILE, kk), C::IDESC_ACC,
-                      (ii > 0 || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(q_empty + st);
-        if (ATOMIC_DQ) {
-          // dQ = dS K into the dP^T columns
-          for (int kk = 0; kk < BT / 16; ++kk)
-            ptx::mma_ss(tmem + T_DP, mnmaj(adS, kk), mnmaj(aK, kk), C::IDESC_DQ, kk > 0);
-          ptx::mma_commit(dq_full);
-          ++dqf;
-        }
-        if (ii + 1 < nq) {
-          if (ATOMIC_DQ) {
+          if (ATOMIC_DQ && dqf > 0) {
             if (!(ok = ptx::mbar_wait(dq_free, (dqf - 1) & 1u, w))) break;
             ptx::tc_fence_after();
           }
-          mma_dpt(stn);
+          mma_dpt(st);
           ptx::mma_commit(dp_full);
         }
+        for (int ii = 0; ii < nq; ++ii) {
+          const uint32_t it = q_it + ii;
+          const int st = it & 1, stn = (it + 1) & 1;
+          // dV += P^T dO
+          if (!(ok = ptx::mbar_wait(p_full, pp & 1u, w))) break;
+          ptx::tc_fence_after();
+          for (int kk = 0; kk < BT / 16; ++kk)
+            ptx::mma_ts(tmem + T_DV, tmem + T_ST + packed_col(kk), mnmaj(adO + st * C::TILE, kk), C::IDESC_ACC,
+                        (ii > 0 || kk > 0) ? 1u : 0u);
+          // next S^T (overwrites P^T only after the product above has read it)
+          if (ii + 1 < nq) {
+            if (!(ok = ptx::mbar_wait(q_full + stn, ((it + 1) >> 1) & 1u, w))) break;
+            ptx::tc_fence_after();
+            mma_st(stn);
+            ptx::mma_commit(s_full);
+          }
+          // dK += dS^T Q
+          if (!(ok = ptx::mbar_wait(ds_full, pp & 1u, w))) break;
+          ++pp;
+          ptx::tc_fence_after();
+          for (int kk = 0; kk < BT / 16; ++kk)
+            ptx::mma_ts(tmem + T_DK, tmem + T_DP + packed_col(kk), mnmaj(aQ + st * C::TILE, kk), C::IDESC_ACC,
+                        (ii > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_commit(q_empty + st);
+          if (ATOMIC_DQ) {
+            // dQ = dS K into the dP^T columns
+            for (int kk = 0; kk < BT / 16; ++kk)
+              ptx::mma_ss(tmem + T_DP, mnmaj(adS, kk), mnmaj(aK, kk), C::IDESC_DQ, kk > 0);
+            ptx::mma_commit(dq_full);
+            ++dqf;
+          }
+          if (ii + 1 < nq) {
+            if (ATOMIC_DQ) {
+              if (!(ok = ptx::mbar_wait(dq_free, (dqf - 1) & 1u, w))) break;
+              ptx::tc_fence_after();
+            }
+            mma_dpt(stn);
+            ptx::mma_commit(dp_full);
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(acc_full);
+        ptx::mma_commit(kv_empty);
+        q_it += nq;
+        ++u_it;
       }
-      if (!ok) break;
-      ptx::mma_commit(acc_full);
-      ptx::mma_commit(kv_empty);
-      q_it += nq;
-      ++u_it;
+      if (!ok) {
+        ptx::mma_commit(drain);
+        ptx::mbar_wait_drain(drain, 0u);
+      }
     }
-    if (!ok) {
-      ptx::mma_commit(drain);
-      ptx::mbar_wait_drain(drain, 0u);
-    }
-   }
-  } else if (wg == 1) {
-    ptx::reg_acquire<REG_PDS>();
+  } else if (wg <= 2) {
+    ptx::reg_acquire<KV_REG_PDS>();
     // ------------------------------------------------------------ P / dS (thread = key row)
+    // Group h handles query columns [64h, 64h + 64) of the tile.
+    const int h = wg - 1;
     const int quad = warp & 3;
     const int j = quad * 32 + lane;                 // key row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tST = tmem + lane_off + T_ST, tDP = tmem + lane_off + T_DP;
+    const uint32_t tST = tmem + lane_off + T_ST + 64 * h, tDP = tmem + lane_off + T_DP + 64 * h;
     ptx::WaitCtx w{abort_flag, P.status, 3u};
     const float sc2 = P.sc2;
     uint32_t q_it = 0, sp = 0;
@@ -354,77 +372,86 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int ii = 0; ii < nq; ++ii, ++q_it, ++sp) {
         const int st = q_it & 1;
         const int qt = q0 + ii;
-        const float* lse2 = sLSE + st * BT;
-        const float* dd = sD + st * BT;
+        const float* lse2 = sLSE + st * BT + 64 * h;
+        const float* dd = sD + st * BT + 64 * h;
         // the staged LSE / D of this tile are visible once q_full completed
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(q_full + st, (q_it >> 1) & 1u, w)))) break;
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(s_full, sp & 1u, w)))) break;
         ptx::tc_fence_after();
-        // pass 1: P^T_j,q = 2^(s * scale * log2e - LSE2_q), masked; stored bf16 over S^T.
-        // The packed values stay in registers for pass 2: once p_full is
-        // signalled the MMA warp may overwrite S^T with the next tile's scores.
-        const int lim = P.p.causal ? key - qt * BT : 0;   // q index (within tile) below which P = 0
-        uint32_t pkeep[4][16];
-        uint32_t rs[4][32];
+        // pass 1: P^T_j,q = 2^(s * scale * log2e - LSE2_q), masked; packed bf16
+        // over the first half of this group's S^T columns. The packed values
+        // stay in registers for pass 2: once p_full is signalled the MMA warp
+        // may overwrite S^T with the next tile's scores.
+        uint32_t pkeep[2][16];
+        {
+          uint32_t rs[2][32];
+          ptx::tmem_ld32(tST, rs[0]);
+          ptx::tmem_ld32(tST + 32, rs[1]);
+          ptx::tmem_ld_wait(rs[0]);
+          ptx::tmem_ld_wait(rs[1]);
+          // query column (within this group) below which P = 0: the diagonal
+          // tile of the causal mask, or every column for a key past Tk
+          const int lim = !key_ok ? 64 : (P.p.causal && qt == kb ? j - 64 * h : 0);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tST + c * 32, rs[c]);   // all four in flight
+          for (int c = 0; c < 2; ++c) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) ptx::tmem_ld_wait(rs[c]);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t (&r)[32] = rs[c];
-#pragma unroll
-          for (int i = 0; i < 16; i += 2) {
-            const int qa = c * 32 + 2 * i;
-            const float4 l4 = ptx::lds128(lse2 + qa);
-            float p0 = ptx::ex2(fmaf(__uint_as_float(r[2 * i]), sc2, -l4.x));
-            float p1 = ptx::ex2(fmaf(__uint_as_float(r[2 * i + 1]), sc2, -l4.y));
-            float p2 = ptx::ex2(fmaf(__uint_as_float(r[2 * i + 2]), sc2, -l4.z));
-            float p3 = ptx::ex2(fmaf(__uint_as_float(r[2 * i + 3]), sc2, -l4.w));
-            if (qa < lim || !key_ok) p0 = 0.f;
-            if (qa + 1 < lim || !key_ok) p1 = 0.f;
-            if (qa + 2 < lim || !key_ok) p2 = 0.f;
-            if (qa + 3 < lim || !key_ok) p3 = 0.f;
-            pkeep[c][i] = ptx::pack_bf16(p0, p1);
-            pkeep[c][i + 1] = ptx::pack_bf16(p2, p3);
+            for (int i = 0; i < 16; i += 2) {
+              const int qa = c * 32 + 2 * i;
+              const float4 l4 = ptx::lds128(lse2 + qa);
+              float p0 = ptx::ex2(fmaf(__uint_as_float(rs[c][2 * i]), sc2, -l4.x));
+              float p1 = ptx::ex2(fmaf(__uint_as_float(rs[c][2 * i + 1]), sc2, -l4.y));
+              float p2 = ptx::ex2(fmaf(__uint_as_float(rs[c][2 * i + 2]), sc2, -l4.z));
+              float p3 = ptx::ex2(fmaf(__uint_as_float(rs[c][2 * i + 3]), sc2, -l4.w));
+              if (lim > 0) {
+                if (qa < lim) p0 = 0.f;
+                if (qa + 1 < lim) p1 = 0.f;
+                if (qa + 2 < lim) p2 = 0.f;
+                if (qa + 3 < lim) p3 = 0.f;
+              }
+              pkeep[c][i] = ptx::pack_bf16(p0, p1);
+              pkeep[c][i + 1] = ptx::pack_bf16(p2, p3);
+            }
+            ptx::tmem_st16(tST + c * 16, pkeep[c]);
           }
-          ptx::tmem_st16(tST + c * 16, pkeep[c]);
         }
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         ptx::mbar_arrive(p_full);
         // pass 2: dS^T_j,q = P^T (dP^T - D_q); bf16 over dP^T and into smem (dS, MN-major)
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dp_full, sp & 1u, w)))) break;
+        if (ATOMIC_DQ) {
+          // the dQ group has finished staging the previous dQ tile in the dS buffer
+          if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(sds_free, (q_it & 1u) ^ 1u, w)))) break;
+        }
         ptx::tc_fence_after();
-        // two 32-column chunks in flight at a time (all four would not fit
-        // beside the 64 registers of packed P^T)
-        uint32_t rd[2][32];
+        {
+          uint32_t rd[2][32];
+          ptx::tmem_ld32(tDP, rd[0]);
+          ptx::tmem_ld32(tDP + 32, rd[1]);
+          ptx::tmem_ld_wait(rd[0]);
+          ptx::tmem_ld_wait(rd[1]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if ((c & 1) == 0) {
-            ptx::tmem_ld32(tDP + c * 32, rd[0]);
-            ptx::tmem_ld32(tDP + c * 32 + 32, rd[1]);
-            ptx::tmem_ld_wait(rd[0]);
-            ptx::tmem_ld_wait(rd[1]);
-          }
-          const uint32_t (&r)[32] = rd[c & 1];
-          uint32_t pk[16];
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; i += 2) {
-            const int qa = c * 32 + 2 * i;
-            const float4 d4 = ptx::lds128(dd + qa);
-            const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pkeep[c][i]));
-            const float2 pg = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pkeep[c][i + 1]));
-            pk[i] = ptx::pack_bf16(pf.x * (__uint_as_float(r[2 * i]) - d4.x), pf.y * (__uint_as_float(r[2 * i + 1]) - d4.y));
-            pk[i + 1] = ptx::pack_bf16(pg.x * (__uint_as_float(r[2 * i + 2]) - d4.z),
-                                       pg.y * (__uint_as_float(r[2 * i + 3]) - d4.w));
-          }
-          ptx::tmem_st16(tDP + c * 16, pk);
-          // dS is MN-major for the dQ product: row = key j, column = query
+            for (int i = 0; i < 16; i += 2) {
+              const int qa = c * 32 + 2 * i;
+              const float4 d4 = ptx::lds128(dd + qa);
+              const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pkeep[c][i]));
+              const float2 pg = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pkeep[c][i + 1]));
+              pk[i] = ptx::pack_bf16(pf.x * (__uint_as_float(rd[c][2 * i]) - d4.x),
+                                     pf.y * (__uint_as_float(rd[c][2 * i + 1]) - d4.y));
+              pk[i + 1] = ptx::pack_bf16(pg.x * (__uint_as_float(rd[c][2 * i + 2]) - d4.z),
+                                         pg.y * (__uint_as_float(rd[c][2 * i + 3]) - d4.w));
+            }
+            ptx::tmem_st16(tDP + c * 16, pk);
+            // dS is MN-major for the dQ product: row = key j, column = query
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const uint32_t off = sw128_offset(j, c * 32 + v * 8);
-            *reinterpret_cast<uint4*>(sdS + off) = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            for (int v = 0; v < 4; ++v) {
+              const uint32_t off = sw128_offset(j, 64 * h + c * 32 + v * 8);
+              *reinterpret_cast<uint4*>(sdS + off) =
+                  make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
           }
         }
         ptx::tmem_st_wait();
@@ -433,17 +460,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::mbar_arrive(ds_full);
       }
     }
-  } else if (wg == 2) {
-    ptx::reg_release<REG_DQ>();
-    // ------------------------------------------------------------ dQ adds; dK / dV epilogue
+  } else {
+    ptx::reg_release<KV_REG_DQ>();
+    // ------------------------------------------------------------ dQ reduce; dK / dV epilogue
     const int quad = warp & 3;
     const int r = quad * 32 + lane;                 // TMEM lane = row
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const bool leader = (threadIdx.x == 3 * 128);
     ptx::WaitCtx w{abort_flag, P.status, 4u};
     const float scale = P.p.scale;
-    uint32_t u_it = 0, dqf = 0;
+    uint32_t u_it = 0, dqf = 0, sfull = 0;
     bool ok = true;
     int bh, kb;
+    // one 64-column half of the fp32 dQ tile into the staging boxes (128-byte
+    // swizzle: 16-byte chunk c of row r at chunk position c ^ (r & 7))
+    auto stage_half = [&](const uint32_t (&v)[2][32]) {
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 x = make_uint4(__float_as_uint(__uint_as_float(v[b][4 * c]) * scale),
+                               __float_as_uint(__uint_as_float(v[b][4 * c + 1]) * scale),
+                               __float_as_uint(__uint_as_float(v[b][4 * c + 2]) * scale),
+                               __float_as_uint(__uint_as_float(v[b][4 * c + 3]) * scale));
+          *reinterpret_cast<uint4*>(sdS + b * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) = x;
+        }
+    };
     for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &kb); ++round) {
       int q0, nq;
       q_range(P, kb, &q0, &nq);
@@ -462,25 +504,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (ATOMIC_DQ) {
         for (int ii = 0; ii < nq; ++ii, ++dqf) {
+          const int qt = q0 + ii;
           if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dq_full, dqf & 1u, w)))) break;
           ptx::tc_fence_after();
-          const int q = (q0 + ii) * BT + r;
-          float* acc = P.dQacc + (static_cast<size_t>(bh) * Tq + (q < Tq ? q : 0)) * HD;
-#pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t v[32];
-            ptx::tmem_ld32(tmem + lane_off + T_DP + c * 32, v);
-            ptx::tmem_ld_wait(v);
-            if (q < Tq) {
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                ptx::red_add_v4(acc + c * 32 + 4 * e, __uint_as_float(v[4 * e]) * scale,
-                                __uint_as_float(v[4 * e + 1]) * scale, __uint_as_float(v[4 * e + 2]) * scale,
-                                __uint_as_float(v[4 * e + 3]) * scale);
+          for (int half = 0; half < HD / 64; ++half) {
+            uint32_t v[2][32];
+            ptx::tmem_ld32(tmem + lane_off + T_DP + 64 * half, v[0]);
+            ptx::tmem_ld32(tmem + lane_off + T_DP + 64 * half + 32, v[1]);
+            ptx::tmem_ld_wait(v[0]);
+            ptx::tmem_ld_wait(v[1]);
+            if (half == HD / 64 - 1) {
+              // the whole tile is in registers: hand the TMEM columns back
+              ptx::tc_fence_before();
+              ptx::mbar_arrive(dq_free);
             }
+            if (half > 0) {
+              // the copy engine has read the previous half out of the buffer
+              if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(stage_free, (dqf & 1u), w)))) break;
+            }
+            stage_half(v);
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(stage_full);
+            if (leader) {
+              if (ptx::mbar_wait(stage_full, sfull & 1u, w)) {
+                ptx::tma_reduce_add_3d(&tmdQ, sdS, 64 * half, qt * BT, bh);
+                ptx::tma_reduce_add_3d(&tmdQ, sdS + 16384, 64 * half + 32, qt * BT, bh);
+                ptx::bulk_commit_group();
+                ptx::bulk_wait_group_read0();
+                ptx::mbar_arrive(half == HD / 64 - 1 ? sds_free : stage_free);
+              } else {
+                ok = false;
+              }
+            }
+            ++sfull;
+            if (!(ok = __all_sync(0xffffffffu, ok))) break;   // the leader's warp leaves together
           }
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(dq_free);
+          if (!ok) break;
         }
         if (!ok) break;
       }
@@ -514,6 +573,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::mbar_arrive(acc_free);
       ++u_it;
     }
+    // every reduce issued by this CTA has landed before it exits
+    if (ATOMIC_DQ && leader) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
 
   ptx::tc_fence_before();
@@ -835,9 +896,10 @@ cudaError_t launch(const LaunchBwd& a) {
     // The register split must fit the launch allocation (see reg_acquire).
     cudaFuncAttributes fa;
     if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
-    if (fa.numRegs != REG_LAUNCH || REG_CTRL + REG_PDS + REG_DQ > 3 * REG_LAUNCH)
+    if (fa.numRegs != KV_REG_LAUNCH || KV_REG_CTRL + 2 * KV_REG_PDS + KV_REG_DQ > 4 * KV_REG_LAUNCH)
       return cudaErrorInvalidConfiguration;
-    kern<<<grid, NUM_THREADS, CfgKV<HD>::SMEM, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO, P);
+    kern<<<grid, KV_THREADS, CfgKV<HD>::SMEM, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO,
+                                                           atomic ? *a.tmdQacc : *a.tmQ, P);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (atomic) {
