@@ -591,14 +591,16 @@ template <int HD>
 struct CfgQ {
   static constexpr int KB = HD / 64;
   static constexpr int TILE = BT * HD * 2;
-  static constexpr int NS = 2;
+  // K and V tiles share one FIFO ring of tile-sized slots, loaded in the
+  // order they are consumed (K_0, V_0, K_1, V_1, ...): five slots give each
+  // tile about two key steps of lead over its first use.
+  static constexpr int NSLOT = (HD == 128) ? 5 : 10;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = OFF_Q + TILE;
-  static constexpr int OFF_K = OFF_DO + TILE;          // [NS]
-  static constexpr int OFF_V = OFF_K + NS * TILE;      // [NS]
-  static constexpr int OFF_BAR = OFF_V + NS * TILE;
-  // q_full, q_empty, kv_full[NS], kv_empty[NS], s_full, s_free, dp_full, ds_full, dq_full, drain
-  static constexpr int NBAR = 2 + 2 * NS + 6;
+  static constexpr int OFF_KV = OFF_DO + TILE;         // [NSLOT]
+  static constexpr int OFF_BAR = OFF_KV + NSLOT * TILE;
+  // q_full, q_empty, kv_full[NSLOT], kv_empty[NSLOT], s_full, s_free, dp_full, ds_full, dq_full, drain
+  static constexpr int NBAR = 2 + 2 * NSLOT + 6;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16(BT, BT, false, false);
@@ -625,14 +627,13 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   }
   uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sdO = smem + C::OFF_DO;
-  uint8_t* sK = smem + C::OFF_K;
-  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sKV = smem + C::OFF_KV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* kv_full = bars + 2;            // [NS]
-  uint64_t* kv_empty = kv_full + C::NS;    // [NS]
-  uint64_t* s_full = kv_empty + C::NS;
+  uint64_t* kv_full = bars + 2;               // [NSLOT]
+  uint64_t* kv_empty = kv_full + C::NSLOT;    // [NSLOT]
+  uint64_t* s_full = kv_empty + C::NSLOT;
   uint64_t* s_free = s_full + 1;
   uint64_t* dp_full = s_full + 2;
   uint64_t* ds_full = s_full + 3;
@@ -643,7 +644,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
     ptx::mbar_init(q_empty, 1);
-    for (int s = 0; s < C::NS; ++s) {
+    for (int s = 0; s < C::NSLOT; ++s) {
       ptx::mbar_init(kv_full + s, 1);
       ptx::mbar_init(kv_empty + s, 1);
     }
@@ -668,6 +669,9 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   const int grid = gridDim.x, cta = blockIdx.x;
   const int Tq = P.p.Tq, Tk = P.p.Tk;
   auto nk_of = [&](int qt) { return P.p.causal ? min(qt + 1, P.n_k_tiles) : P.n_k_tiles; };
+  // K_j is stream item 2 (k_it + j), V_j item 2 (k_it + j) + 1 (k_it runs across units)
+  auto slot = [](uint32_t item) { return static_cast<int>(item % C::NSLOT); };
+  auto par = [](uint32_t item) { return (item / C::NSLOT) & 1u; };
 
   if (warp == 0 && lane == 0) {
     ptx::WaitCtx w{abort_flag, P.status, 5u};
@@ -682,25 +686,30 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         ptx::tma_load_3d(sQ + b * BOX_BYTES, &tmQ, q_full, b * 64, qt * BT, bh);
         ptx::tma_load_3d(sdO + b * BOX_BYTES, &tmdO, q_full, b * 64, qt * BT, bh);
       }
-      for (int j = 0; j < nk; ++j, ++k_it) {
-        const int st = k_it % C::NS;
-        if (!(ok = ptx::mbar_wait(kv_empty + st, ((k_it / C::NS) & 1u) ^ 1u, w))) break;
-        ptx::mbar_arrive_expect_tx(kv_full + st, 2 * C::TILE);
-        for (int b = 0; b < C::KB; ++b) {
-          ptx::tma_load_3d(sK + st * C::TILE + b * BOX_BYTES, &tmK, kv_full + st, b * 64, j * BT, bh);
-          ptx::tma_load_3d(sV + st * C::TILE + b * BOX_BYTES, &tmV, kv_full + st, b * 64, j * BT, bh);
+      uint32_t issued = 2 * k_it;   // stream items issued so far
+      for (int j = 0; ok && j < nk; ++j, ++k_it) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const uint32_t item = 2 * k_it + kv;
+          if (!(ok = ptx::mbar_wait(kv_empty + slot(item), par(item) ^ 1u, w))) break;
+          ptx::mbar_arrive_expect_tx(kv_full + slot(item), C::TILE);
+          for (int b = 0; b < C::KB; ++b)
+            ptx::tma_load_3d(sKV + slot(item) * C::TILE + b * BOX_BYTES, kv ? &tmV : &tmK, kv_full + slot(item),
+                             b * 64, j * BT, bh);
+          issued = item + 1;
         }
+      }
+      if (!ok) {
+        // Let the copies already in flight land before the CTA exits.
+        for (uint32_t n = (issued > (uint32_t)C::NSLOT ? issued - C::NSLOT : 0u); n < issued; ++n)
+          ptx::mbar_wait_drain(kv_full + slot(n), par(n));
+        ptx::mbar_wait_drain(q_full, u_it & 1u);
+        break;
       }
       ++u_it;
     }
-    if (!ok) {
-      for (uint32_t n = (k_it > (uint32_t)C::NS ? k_it - C::NS : 0u); n < k_it; ++n)
-        ptx::mbar_wait_drain(kv_full + n % C::NS, (n / C::NS) & 1u);
-      if (u_it > 0) ptx::mbar_wait_drain(q_full, (u_it - 1) & 1u);
-    }
   } else if (warp == 1 && lane == 0) {
     ptx::WaitCtx w{abort_flag, P.status, 6u};
-    const uint32_t aQ = ptx::smem_u32(sQ), adO = ptx::smem_u32(sdO), aK = ptx::smem_u32(sK), aV = ptx::smem_u32(sV);
+    const uint32_t aQ = ptx::smem_u32(sQ), adO = ptx::smem_u32(sdO), aKV = ptx::smem_u32(sKV);
     auto kmaj = [](uint32_t base, int kk) {
       return ptx::sdesc_sw128(base + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
     };
@@ -713,38 +722,38 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       if (!(ok = ptx::mbar_wait(q_full, u_it & 1u, w))) break;
       // S for the first key tile
       {
-        const int st = k_it % C::NS;
-        if (!(ok = ptx::mbar_wait(kv_full + st, (k_it / C::NS) & 1u, w))) break;
+        const uint32_t ik = 2 * k_it;
+        if (!(ok = ptx::mbar_wait(kv_full + slot(ik), par(ik), w))) break;
         ptx::tc_fence_after();
         for (int kk = 0; kk < HD / 16; ++kk)
-          ptx::mma_ss(tmem + T_S, kmaj(aQ, kk), kmaj(aK + st * C::TILE, kk), C::IDESC_S, kk > 0);
+          ptx::mma_ss(tmem + T_S, kmaj(aQ, kk), kmaj(aKV + slot(ik) * C::TILE, kk), C::IDESC_S, kk > 0);
         ptx::mma_commit(s_full);
       }
       for (int j = 0; j < nk; ++j, ++sp) {
-        const uint32_t it = k_it + j;
-        const int st = it % C::NS;
+        const uint32_t ik = 2 * (k_it + j), iv = ik + 1, ikn = ik + 2;
         // dP = dO V^T (the dP columns are free: the previous dQ product read dS from them)
+        if (!(ok = ptx::mbar_wait(kv_full + slot(iv), par(iv), w))) break;
+        ptx::tc_fence_after();
         for (int kk = 0; kk < HD / 16; ++kk)
-          ptx::mma_ss(tmem + T_DP, kmaj(adO, kk), kmaj(aV + st * C::TILE, kk), C::IDESC_S, kk > 0);
+          ptx::mma_ss(tmem + T_DP, kmaj(adO, kk), kmaj(aKV + slot(iv) * C::TILE, kk), C::IDESC_S, kk > 0);
         ptx::mma_commit(dp_full);
+        ptx::mma_commit(kv_empty + slot(iv));
         // next S once the row threads have read this one
         if (j + 1 < nk) {
-          const uint32_t itn = it + 1;
-          const int stn = itn % C::NS;
-          if (!(ok = ptx::mbar_wait(kv_full + stn, (itn / C::NS) & 1u, w))) break;
+          if (!(ok = ptx::mbar_wait(kv_full + slot(ikn), par(ikn), w))) break;
           if (!(ok = ptx::mbar_wait(s_free, sp & 1u, w))) break;
           ptx::tc_fence_after();
           for (int kk = 0; kk < HD / 16; ++kk)
-            ptx::mma_ss(tmem + T_S, kmaj(aQ, kk), kmaj(aK + stn * C::TILE, kk), C::IDESC_S, kk > 0);
+            ptx::mma_ss(tmem + T_S, kmaj(aQ, kk), kmaj(aKV + slot(ikn) * C::TILE, kk), C::IDESC_S, kk > 0);
           ptx::mma_commit(s_full);
         }
         // dQ += dS K
         if (!(ok = ptx::mbar_wait(ds_full, sp & 1u, w))) break;
         ptx::tc_fence_after();
         for (int kk = 0; kk < BT / 16; ++kk)
-          ptx::mma_ts(tmem + T_DQ, tmem + T_DP + kk * 8, mnmaj(aK + st * C::TILE, kk), C::IDESC_DQ,
+          ptx::mma_ts(tmem + T_DQ, tmem + T_DP + kk * 8, mnmaj(aKV + slot(ik) * C::TILE, kk), C::IDESC_DQ,
                       (j > 0 || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(kv_empty + st);
+        ptx::mma_commit(kv_empty + slot(ik));
       }
       if (!ok) break;
       ptx::mma_commit(dq_full);

@@ -11,7 +11,7 @@
 // One persistent CTA per SM walks a causal-aware list of work units. A unit is
 // two 128-row query tiles (256 rows) of one head; both tiles share every K/V
 // tile that TMA brings in. Warp roles (12 warps, 3 warpgroups):
-//   warp 0      TMA producer: lane 0 loads Q and K, lane 1 loads V
+//   warp 0      TMA producer (lane 0): Q, then K and V tiles through one ring
 //   warp 1      MMA issuer (lane 0); also allocates and frees TMEM
 //   warps 2-3   idle (they complete the first warpgroup's register release)
 //   warps 4-7   softmax group for query tile 0 (one thread per query row)
@@ -56,14 +56,16 @@ template <int HD>
 struct Cfg {
   static constexpr int KB = HD / 64;                   // 64-column swizzle blocks per row
   static constexpr int TILE = BM * HD * 2;             // bytes of one 128-row tile
-  static constexpr int NS = (HD == 128) ? 2 : 4;       // K/V pipeline stages
+  // K and V tiles share one FIFO ring of tile-sized slots, loaded in the
+  // order they are consumed (K_0, V_0, K_1, V_1, ...). Five slots give every
+  // tile about two key steps of lead over its first use, which covers the
+  // ~2 us a TMA load of a tile takes under load.
+  static constexpr int NSLOT = (HD == 128) ? 5 : 10;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + 2 * TILE;
-  static constexpr int OFF_V = OFF_K + NS * TILE;
-  static constexpr int OFF_BAR = OFF_V + NS * TILE;
-  // barriers: q_full, q_empty, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS],
-  //           s_full[2], p_full[2], o_full[2], drain
-  static constexpr int NBAR = 2 + 4 * NS + 7;
+  static constexpr int OFF_KV = OFF_Q + 2 * TILE;
+  static constexpr int OFF_BAR = OFF_KV + NSLOT * TILE;
+  // barriers: q_full, q_empty, full[NSLOT], empty[NSLOT], s_full[2], p_full[2], o_full[2], drain
+  static constexpr int NBAR = 2 + 2 * NSLOT + 7;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16(BM, BN, false, false);
@@ -106,16 +108,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 
   uint8_t* sQ = smem + C::OFF_Q;
-  uint8_t* sK = smem + C::OFF_K;
-  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sKV = smem + C::OFF_KV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;
-  uint64_t* k_empty = k_full + C::NS;
-  uint64_t* v_full = k_empty + C::NS;
-  uint64_t* v_empty = v_full + C::NS;
-  uint64_t* s_full = v_empty + C::NS;   // [2]
+  uint64_t* kv_full = bars + 2;            // [NSLOT]
+  uint64_t* kv_empty = kv_full + C::NSLOT; // [NSLOT]
+  uint64_t* s_full = kv_empty + C::NSLOT;  // [2]
   uint64_t* p_full = s_full + 2;        // [2]
   uint64_t* o_full = p_full + 2;        // [2]
   uint64_t* drain = o_full + 2;
@@ -125,11 +124,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
     ptx::mbar_init(q_empty, 1);
-    for (int s = 0; s < C::NS; ++s) {
-      ptx::mbar_init(k_full + s, 1);
-      ptx::mbar_init(k_empty + s, 1);
-      ptx::mbar_init(v_full + s, 1);
-      ptx::mbar_init(v_empty + s, 1);
+    for (int s = 0; s < C::NSLOT; ++s) {
+      ptx::mbar_init(kv_full + s, 1);
+      ptx::mbar_init(kv_empty + s, 1);
     }
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(s_full + t, 1);
@@ -155,71 +152,70 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int wg = warp >> 2;
   if (wg == 0) {
    ptx::reg_release<REG_CTRL>();
-   if (warp == 0 && lane < 2) {
+   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
-    ptx::WaitCtx w{abort_flag, P.status, 1u + lane};
-    const bool is_qk = (lane == 0);
-    if (is_qk) {
-      ptx::tma_prefetch_desc(&tmQ);
-      ptx::tma_prefetch_desc(&tmK);
-    } else {
-      ptx::tma_prefetch_desc(&tmV);
-    }
-    uint32_t kv_it = 0, u_it = 0;
+    // Item i of the K/V stream (i = 2 * tile + {0: K, 1: V}) goes to slot
+    // i % NSLOT; the counters run across work units.
+    ptx::WaitCtx w{abort_flag, P.status, 1u};
+    ptx::tma_prefetch_desc(&tmQ);
+    ptx::tma_prefetch_desc(&tmK);
+    ptx::tma_prefetch_desc(&tmV);
+    uint32_t item = 0, u_it = 0;
     bool ok = true;
     int bh, qb;
     for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qb); ++round) {
       int n0, n1;
       tile_counts(P, qb, &n0, &n1);
-      if (is_qk) {
-        if (!(ok = ptx::mbar_wait(q_empty, (u_it & 1u) ^ 1u, w))) break;
-        ptx::mbar_arrive_expect_tx(q_full, 2 * C::TILE);
-        for (int t = 0; t < 2; ++t)
+      if (!(ok = ptx::mbar_wait(q_empty, (u_it & 1u) ^ 1u, w))) break;
+      ptx::mbar_arrive_expect_tx(q_full, 2 * C::TILE);
+      for (int t = 0; t < 2; ++t)
+        for (int b = 0; b < C::KB; ++b)
+          ptx::tma_load_3d(sQ + t * C::TILE + b * BOX_BYTES, &tmQ, q_full, b * 64, (2 * qb + t) * BM, bh);
+      for (int j = 0; ok && j < n1; ++j) {
+        for (int kv = 0; kv < 2; ++kv, ++item) {
+          const int sl = item % C::NSLOT;
+          const uint32_t ph = (item / C::NSLOT) & 1u;
+          if (!(ok = ptx::mbar_wait(kv_empty + sl, ph ^ 1u, w))) break;
+          ptx::mbar_arrive_expect_tx(kv_full + sl, C::TILE);
+          const CUtensorMap* map = kv ? &tmV : &tmK;
           for (int b = 0; b < C::KB; ++b)
-            ptx::tma_load_3d(sQ + t * C::TILE + b * BOX_BYTES, &tmQ, q_full, b * 64, (2 * qb + t) * BM, bh);
-      }
-      for (int j = 0; j < n1; ++j, ++kv_it) {
-        const int st = kv_it % C::NS;
-        const uint32_t ph = (kv_it / C::NS) & 1u;
-        uint64_t* empty = is_qk ? k_empty + st : v_empty + st;
-        uint64_t* full = is_qk ? k_full + st : v_full + st;
-        uint8_t* dst = is_qk ? sK + st * C::TILE : sV + st * C::TILE;
-        const CUtensorMap* map = is_qk ? &tmK : &tmV;
-        if (!(ok = ptx::mbar_wait(empty, ph ^ 1u, w))) break;
-        ptx::mbar_arrive_expect_tx(full, C::TILE);
-        for (int b = 0; b < C::KB; ++b) ptx::tma_load_3d(dst + b * BOX_BYTES, map, full, b * 64, j * BN, bh);
+            ptx::tma_load_3d(sKV + sl * C::TILE + b * BOX_BYTES, map, kv_full + sl, b * 64, j * BN, bh);
+        }
       }
       ++u_it;
     }
     if (!ok) {
       // Let the copies already in flight land before the CTA exits.
-      for (uint32_t n = (kv_it > (uint32_t)C::NS ? kv_it - C::NS : 0u); n < kv_it; ++n)
-        ptx::mbar_wait_drain((is_qk ? k_full : v_full) + n % C::NS, (n / C::NS) & 1u);
-      if (is_qk && u_it > 0) ptx::mbar_wait_drain(q_full, (u_it - 1) & 1u);
+      for (uint32_t n = (item > (uint32_t)C::NSLOT ? item - C::NSLOT : 0u); n < item; ++n)
+        ptx::mbar_wait_drain(kv_full + n % C::NSLOT, (n / C::NSLOT) & 1u);
+      if (u_it > 0) ptx::mbar_wait_drain(q_full, (u_it - 1) & 1u);
     }
    } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     ptx::WaitCtx w{abort_flag, P.status, 3u};
-    const uint32_t sQa = ptx::smem_u32(sQ), sKa = ptx::smem_u32(sK), sVa = ptx::smem_u32(sV);
-    auto mma_S = [&](int t, int st) {
+    const uint32_t sQa = ptx::smem_u32(sQ), sKVa = ptx::smem_u32(sKV);
+    auto mma_S = [&](int t, int sl) {
       const uint32_t d = tmem + t * 256;
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk) {
         const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
         const uint64_t a = ptx::sdesc_sw128(sQa + t * C::TILE + off, 16, 1024);
-        const uint64_t b = ptx::sdesc_sw128(sKa + st * C::TILE + off, 16, 1024);
+        const uint64_t b = ptx::sdesc_sw128(sKVa + sl * C::TILE + off, 16, 1024);
         ptx::mma_ss(d, a, b, C::IDESC_S, kk > 0 ? 1u : 0u);
       }
     };
-    auto mma_PV = [&](int t, int st, bool acc) {
+    auto mma_PV = [&](int t, int sl, bool acc) {
       const uint32_t d = tmem + t * 256 + 128;
       const uint32_t a = tmem + t * 256;  // P_t, bf16 pairs in the first 64 columns of S_t
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk) {
-        const uint64_t b = ptx::sdesc_sw128(sVa + st * C::TILE + kk * 2048, BOX_BYTES, 1024);
+        const uint64_t b = ptx::sdesc_sw128(sKVa + sl * C::TILE + kk * 2048, BOX_BYTES, 1024);
         ptx::mma_ts(d, a + kk * 8, b, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
       }
     };
+    // K_j is stream item 2 (kv_it + j), V_j item 2 (kv_it + j) + 1
+    auto slot = [](uint32_t item) { return static_cast<int>(item % C::NSLOT); };
+    auto par = [](uint32_t item) { return (item / C::NSLOT) & 1u; };
     uint32_t kv_it = 0, u_it = 0, pp[2] = {0u, 0u};
     bool ok = true;
     int bh, qb;
@@ -228,46 +224,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tile_counts(P, qb, &n0, &n1);
       if (!(ok = ptx::mbar_wait(q_full, u_it & 1u, w))) break;
       {
-        const int st = kv_it % C::NS;
-        if (!(ok = ptx::mbar_wait(k_full + st, (kv_it / C::NS) & 1u, w))) break;
+        const uint32_t ik = 2 * kv_it;
+        if (!(ok = ptx::mbar_wait(kv_full + slot(ik), par(ik), w))) break;
         ptx::tc_fence_after();
-        mma_S(0, st);
+        mma_S(0, slot(ik));
         ptx::mma_commit(s_full + 0);
-        mma_S(1, st);
+        mma_S(1, slot(ik));
         ptx::mma_commit(s_full + 1);
-        ptx::mma_commit(k_empty + st);
+        ptx::mma_commit(kv_empty + slot(ik));
       }
       for (int j = 0; j < n1; ++j) {
-        const uint32_t it = kv_it + j, itn = it + 1;
-        const int st = it % C::NS, stn = itn % C::NS;
-        const uint32_t phn = (itn / C::NS) & 1u;
-        if (!(ok = ptx::mbar_wait(v_full + st, (it / C::NS) & 1u, w))) break;
+        const uint32_t iv = 2 * (kv_it + j) + 1, ikn = iv + 1;   // V_j, K_{j+1}
+        if (!(ok = ptx::mbar_wait(kv_full + slot(iv), par(iv), w))) break;
         if (j < n0) {
           if (!(ok = ptx::mbar_wait(p_full + 0, pp[0] & 1u, w))) break;
           ++pp[0];
           ptx::tc_fence_after();
-          mma_PV(0, st, j > 0);
+          mma_PV(0, slot(iv), j > 0);
           if (j == n0 - 1) {
             ptx::mma_commit(o_full + 0);
           } else {
-            if (!(ok = ptx::mbar_wait(k_full + stn, phn, w))) break;
+            if (!(ok = ptx::mbar_wait(kv_full + slot(ikn), par(ikn), w))) break;
             ptx::tc_fence_after();
-            mma_S(0, stn);
+            mma_S(0, slot(ikn));
             ptx::mma_commit(s_full + 0);
           }
         }
         if (!(ok = ptx::mbar_wait(p_full + 1, pp[1] & 1u, w))) break;
         ++pp[1];
         ptx::tc_fence_after();
-        mma_PV(1, st, j > 0);
+        mma_PV(1, slot(iv), j > 0);
         if (j == n1 - 1) ptx::mma_commit(o_full + 1);
-        ptx::mma_commit(v_empty + st);
+        ptx::mma_commit(kv_empty + slot(iv));
         if (j + 1 < n1) {
-          if (!(ok = ptx::mbar_wait(k_full + stn, phn, w))) break;
+          if (!(ok = ptx::mbar_wait(kv_full + slot(ikn), par(ikn), w))) break;
           ptx::tc_fence_after();
-          mma_S(1, stn);
+          mma_S(1, slot(ikn));
           ptx::mma_commit(s_full + 1);
-          ptx::mma_commit(k_empty + stn);
+          ptx::mma_commit(kv_empty + slot(ikn));
         }
       }
       if (!ok) break;
