@@ -257,8 +257,12 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         for (uint32_t n = (q_it > 2u ? q_it - 2u : 0u); n < q_it; ++n)
           ptx::mbar_wait_drain(q_full + (n & 1), (n >> 1) & 1u);
       }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
+      // The whole warp follows the schedule and waits; the lane elect.sync
+      // picks (lane 0) issues the MMAs and commits. A commit tracks the MMAs
+      // of its own thread, so the issuing lane must not change; a change is
+      // reported through the status word.
       ptx::WaitCtx w{abort_flag, P.status, 2u};
       const uint32_t aK = ptx::smem_u32(sK), aV = ptx::smem_u32(sV), aQ = ptx::smem_u32(sQ),
                      adO = ptx::smem_u32(sdO), adS = ptx::smem_u32(sdS);
@@ -269,85 +273,118 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         return ptx::sdesc_sw128(base + kk * 2048, BOX_BYTES, 1024);
       };
       auto mma_st = [&](int st) {
+#pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
           ptx::mma_ss(tmem + T_ST, kmaj(aK, kk), kmaj(aQ + st * C::TILE, kk), C::IDESC_S, kk > 0);
       };
       auto mma_dpt = [&](int st) {
+#pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
           ptx::mma_ss(tmem + T_DP, kmaj(aV, kk), kmaj(adO + st * C::TILE, kk), C::IDESC_S, kk > 0);
       };
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, w));
+      };
       uint32_t u_it = 0, q_it = 0, pp = 0, dqf = 0;
-      bool ok = true;
+      bool ok = true, moved = false;
       int bh, kb;
       for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &kb); ++round) {
         int q0, nq;
         q_range(P, kb, &q0, &nq);
         if (nq == 0) continue;
-        if (!(ok = ptx::mbar_wait(kv_full, u_it & 1u, w))) break;
-        if (!(ok = ptx::mbar_wait(acc_free, (u_it & 1u) ^ 1u, w))) break;
+        if (!(ok = wait(kv_full, u_it & 1u))) break;
+        if (!(ok = wait(acc_free, (u_it & 1u) ^ 1u))) break;
         {
           const int st = q_it & 1;
-          if (!(ok = ptx::mbar_wait(q_full + st, (q_it >> 1) & 1u, w))) break;
+          if (!(ok = wait(q_full + st, (q_it >> 1) & 1u))) break;
           ptx::tc_fence_after();
-          mma_st(st);
-          ptx::mma_commit(s_full);
+          if (ptx::elect_one()) {
+            moved |= lane != 0;
+            mma_st(st);
+            ptx::mma_commit(s_full);
+          }
+          __syncwarp();
           if (ATOMIC_DQ && dqf > 0) {
-            if (!(ok = ptx::mbar_wait(dq_free, (dqf - 1) & 1u, w))) break;
+            if (!(ok = wait(dq_free, (dqf - 1) & 1u))) break;
             ptx::tc_fence_after();
           }
-          mma_dpt(st);
-          ptx::mma_commit(dp_full);
+          if (ptx::elect_one()) {
+            moved |= lane != 0;
+            mma_dpt(st);
+            ptx::mma_commit(dp_full);
+          }
+          __syncwarp();
         }
         for (int ii = 0; ii < nq; ++ii) {
           const uint32_t it = q_it + ii;
           const int st = it & 1, stn = (it + 1) & 1;
-          // dV += P^T dO
-          if (!(ok = ptx::mbar_wait(p_full, pp & 1u, w))) break;
+          const bool more = ii + 1 < nq;
+          // dV += P^T dO, then the next S^T (it overwrites P^T only after the
+          // product above has read it)
+          if (!(ok = wait(p_full, pp & 1u))) break;
+          if (more && !(ok = wait(q_full + stn, ((it + 1) >> 1) & 1u))) break;
           ptx::tc_fence_after();
-          for (int kk = 0; kk < BT / 16; ++kk)
-            ptx::mma_ts(tmem + T_DV, tmem + T_ST + packed_col(kk), mnmaj(adO + st * C::TILE, kk), C::IDESC_ACC,
-                        (ii > 0 || kk > 0) ? 1u : 0u);
-          // next S^T (overwrites P^T only after the product above has read it)
-          if (ii + 1 < nq) {
-            if (!(ok = ptx::mbar_wait(q_full + stn, ((it + 1) >> 1) & 1u, w))) break;
-            ptx::tc_fence_after();
-            mma_st(stn);
-            ptx::mma_commit(s_full);
+          if (ptx::elect_one()) {
+            moved |= lane != 0;
+#pragma unroll
+            for (int kk = 0; kk < BT / 16; ++kk)
+              ptx::mma_ts(tmem + T_DV, tmem + T_ST + packed_col(kk), mnmaj(adO + st * C::TILE, kk), C::IDESC_ACC,
+                          (ii > 0 || kk > 0) ? 1u : 0u);
+            if (more) {
+              mma_st(stn);
+              ptx::mma_commit(s_full);
+            }
           }
-          // dK += dS^T Q
-          if (!(ok = ptx::mbar_wait(ds_full, pp & 1u, w))) break;
+          __syncwarp();
+          // dK += dS^T Q (and, atomic mode, dQ = dS K into the dP^T columns)
+          if (!(ok = wait(ds_full, pp & 1u))) break;
           ++pp;
           ptx::tc_fence_after();
-          for (int kk = 0; kk < BT / 16; ++kk)
-            ptx::mma_ts(tmem + T_DK, tmem + T_DP + packed_col(kk), mnmaj(aQ + st * C::TILE, kk), C::IDESC_ACC,
-                        (ii > 0 || kk > 0) ? 1u : 0u);
-          ptx::mma_commit(q_empty + st);
-          if (ATOMIC_DQ) {
-            // dQ = dS K into the dP^T columns
+          if (ptx::elect_one()) {
+            moved |= lane != 0;
+#pragma unroll
             for (int kk = 0; kk < BT / 16; ++kk)
-              ptx::mma_ss(tmem + T_DP, mnmaj(adS, kk), mnmaj(aK, kk), C::IDESC_DQ, kk > 0);
-            ptx::mma_commit(dq_full);
-            ++dqf;
-          }
-          if (ii + 1 < nq) {
+              ptx::mma_ts(tmem + T_DK, tmem + T_DP + packed_col(kk), mnmaj(aQ + st * C::TILE, kk), C::IDESC_ACC,
+                          (ii > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_commit(q_empty + st);
             if (ATOMIC_DQ) {
-              if (!(ok = ptx::mbar_wait(dq_free, (dqf - 1) & 1u, w))) break;
+#pragma unroll
+              for (int kk = 0; kk < BT / 16; ++kk)
+                ptx::mma_ss(tmem + T_DP, mnmaj(adS, kk), mnmaj(aK, kk), C::IDESC_DQ, kk > 0);
+              ptx::mma_commit(dq_full);
+            }
+          }
+          __syncwarp();
+          if (ATOMIC_DQ) ++dqf;
+          if (more) {
+            if (ATOMIC_DQ) {
+              if (!(ok = wait(dq_free, (dqf - 1) & 1u))) break;
               ptx::tc_fence_after();
             }
-            mma_dpt(stn);
-            ptx::mma_commit(dp_full);
+            if (ptx::elect_one()) {
+              moved |= lane != 0;
+              mma_dpt(stn);
+              ptx::mma_commit(dp_full);
+            }
+            __syncwarp();
           }
         }
         if (!ok) break;
-        ptx::mma_commit(acc_full);
-        ptx::mma_commit(kv_empty);
+        if (ptx::elect_one()) {
+          moved |= lane != 0;
+          ptx::mma_commit(acc_full);
+          ptx::mma_commit(kv_empty);
+        }
+        __syncwarp();
         q_it += nq;
         ++u_it;
       }
       if (!ok) {
-        ptx::mma_commit(drain);
+        if (ptx::elect_one()) ptx::mma_commit(drain);
+        __syncwarp();
         ptx::mbar_wait_drain(drain, 0u);
       }
+      if (__any_sync(0xffffffffu, moved) && lane == 0) atomicOr(P.status, ATTN_DEV_ISSUER);
     }
   } else if (wg <= 2) {
     ptx::reg_acquire<KV_REG_PDS>();
@@ -707,64 +744,96 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       }
       ++u_it;
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
+    // The whole warp follows the schedule and waits; the elected lane (lane 0)
+    // issues the MMAs and commits (see the dK/dV kernel).
     ptx::WaitCtx w{abort_flag, P.status, 6u};
     const uint32_t aQ = ptx::smem_u32(sQ), adO = ptx::smem_u32(sdO), aKV = ptx::smem_u32(sKV);
     auto kmaj = [](uint32_t base, int kk) {
       return ptx::sdesc_sw128(base + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
     };
     auto mnmaj = [](uint32_t base, int kk) { return ptx::sdesc_sw128(base + kk * 2048, BOX_BYTES, 1024); };
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, w));
+    };
     uint32_t u_it = 0, k_it = 0, sp = 0;
-    bool ok = true;
+    bool ok = true, moved = false;
     int bh, qt;
     for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qt); ++round) {
       const int nk = nk_of(qt);
-      if (!(ok = ptx::mbar_wait(q_full, u_it & 1u, w))) break;
+      if (!(ok = wait(q_full, u_it & 1u))) break;
       // S for the first key tile
       {
         const uint32_t ik = 2 * k_it;
-        if (!(ok = ptx::mbar_wait(kv_full + slot(ik), par(ik), w))) break;
+        if (!(ok = wait(kv_full + slot(ik), par(ik)))) break;
         ptx::tc_fence_after();
-        for (int kk = 0; kk < HD / 16; ++kk)
-          ptx::mma_ss(tmem + T_S, kmaj(aQ, kk), kmaj(aKV + slot(ik) * C::TILE, kk), C::IDESC_S, kk > 0);
-        ptx::mma_commit(s_full);
+        if (ptx::elect_one()) {
+          moved |= lane != 0;
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk)
+            ptx::mma_ss(tmem + T_S, kmaj(aQ, kk), kmaj(aKV + slot(ik) * C::TILE, kk), C::IDESC_S, kk > 0);
+          ptx::mma_commit(s_full);
+        }
+        __syncwarp();
       }
       for (int j = 0; j < nk; ++j, ++sp) {
         const uint32_t ik = 2 * (k_it + j), iv = ik + 1, ikn = ik + 2;
+        const bool more = j + 1 < nk;
         // dP = dO V^T (the dP columns are free: the previous dQ product read dS from them)
-        if (!(ok = ptx::mbar_wait(kv_full + slot(iv), par(iv), w))) break;
+        if (!(ok = wait(kv_full + slot(iv), par(iv)))) break;
         ptx::tc_fence_after();
-        for (int kk = 0; kk < HD / 16; ++kk)
-          ptx::mma_ss(tmem + T_DP, kmaj(adO, kk), kmaj(aKV + slot(iv) * C::TILE, kk), C::IDESC_S, kk > 0);
-        ptx::mma_commit(dp_full);
-        ptx::mma_commit(kv_empty + slot(iv));
-        // next S once the row threads have read this one
-        if (j + 1 < nk) {
-          if (!(ok = ptx::mbar_wait(kv_full + slot(ikn), par(ikn), w))) break;
-          if (!(ok = ptx::mbar_wait(s_free, sp & 1u, w))) break;
-          ptx::tc_fence_after();
+        if (ptx::elect_one()) {
+          moved |= lane != 0;
+#pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk)
-            ptx::mma_ss(tmem + T_S, kmaj(aQ, kk), kmaj(aKV + slot(ikn) * C::TILE, kk), C::IDESC_S, kk > 0);
-          ptx::mma_commit(s_full);
+            ptx::mma_ss(tmem + T_DP, kmaj(adO, kk), kmaj(aKV + slot(iv) * C::TILE, kk), C::IDESC_S, kk > 0);
+          ptx::mma_commit(dp_full);
+          ptx::mma_commit(kv_empty + slot(iv));
+        }
+        __syncwarp();
+        // next S once the row threads have read this one
+        if (more) {
+          if (!(ok = wait(kv_full + slot(ikn), par(ikn)))) break;
+          if (!(ok = wait(s_free, sp & 1u))) break;
+          ptx::tc_fence_after();
+          if (ptx::elect_one()) {
+            moved |= lane != 0;
+#pragma unroll
+            for (int kk = 0; kk < HD / 16; ++kk)
+              ptx::mma_ss(tmem + T_S, kmaj(aQ, kk), kmaj(aKV + slot(ikn) * C::TILE, kk), C::IDESC_S, kk > 0);
+            ptx::mma_commit(s_full);
+          }
+          __syncwarp();
         }
         // dQ += dS K
-        if (!(ok = ptx::mbar_wait(ds_full, sp & 1u, w))) break;
+        if (!(ok = wait(ds_full, sp & 1u))) break;
         ptx::tc_fence_after();
-        for (int kk = 0; kk < BT / 16; ++kk)
-          ptx::mma_ts(tmem + T_DQ, tmem + T_DP + kk * 8, mnmaj(aKV + slot(ik) * C::TILE, kk), C::IDESC_DQ,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(kv_empty + slot(ik));
+        if (ptx::elect_one()) {
+          moved |= lane != 0;
+#pragma unroll
+          for (int kk = 0; kk < BT / 16; ++kk)
+            ptx::mma_ts(tmem + T_DQ, tmem + T_DP + kk * 8, mnmaj(aKV + slot(ik) * C::TILE, kk), C::IDESC_DQ,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_commit(kv_empty + slot(ik));
+        }
+        __syncwarp();
       }
       if (!ok) break;
-      ptx::mma_commit(dq_full);
-      ptx::mma_commit(q_empty);
+      if (ptx::elect_one()) {
+        moved |= lane != 0;
+        ptx::mma_commit(dq_full);
+        ptx::mma_commit(q_empty);
+      }
+      __syncwarp();
       k_it += nk;
       ++u_it;
     }
     if (!ok) {
-      ptx::mma_commit(drain);
+      if (ptx::elect_one()) ptx::mma_commit(drain);
+      __syncwarp();
       ptx::mbar_wait_drain(drain, 0u);
     }
+    if (__any_sync(0xffffffffu, moved) && lane == 0) atomicOr(P.status, ATTN_DEV_ISSUER);
   } else if (warp >= 2) {
     const int quad = warp & 3;
     const int r = quad * 32 + lane;

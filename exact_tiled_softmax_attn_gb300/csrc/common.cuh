@@ -10,6 +10,7 @@ namespace attn {
 // Device status word bits (OR-ed by kernels; read back by the host).
 constexpr uint32_t ATTN_DEV_TIMEOUT = 1u;     // a bounded pipeline wait gave up
 constexpr uint32_t ATTN_DEV_BAD_SMEM = 2u;    // dynamic shared memory not 1024-byte aligned
+constexpr uint32_t ATTN_DEV_ISSUER = 4u;      // elect.sync picked a lane other than 0 to issue MMAs
 
 // Upper bound on any single wait inside a kernel. Legitimate waits here last
 // micro- to milliseconds; reaching this means a producer never arrived.

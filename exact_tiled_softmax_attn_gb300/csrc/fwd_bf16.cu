@@ -12,7 +12,7 @@
 // two 128-row query tiles (256 rows) of one head; both tiles share every K/V
 // tile that TMA brings in. Warp roles (12 warps, 3 warpgroups):
 //   warp 0      TMA producer (lane 0): Q, then K and V tiles through one ring
-//   warp 1      MMA issuer (lane 0); also allocates and frees TMEM
+//   warp 1      MMA issuer (one elected lane); also allocates and frees TMEM
 //   warps 2-3   idle (they complete the first warpgroup's register release)
 //   warps 4-7   softmax group for query tile 0 (one thread per query row)
 //   warps 8-11  softmax group for query tile 1
@@ -190,8 +190,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::mbar_wait_drain(kv_full + n % C::NSLOT, (n / C::NSLOT) & 1u);
       if (u_it > 0) ptx::mbar_wait_drain(q_full, (u_it - 1) & 1u);
     }
-   } else if (warp == 1 && lane == 0) {
+   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // The whole warp follows the schedule and waits; the lane elect.sync
+    // picks (lane 0) issues each step's MMAs and commits. A commit tracks the
+    // MMAs of its own thread, so the issuing lane must not change; a change
+    // is reported through the status word.
     ptx::WaitCtx w{abort_flag, P.status, 3u};
     const uint32_t sQa = ptx::smem_u32(sQ), sKVa = ptx::smem_u32(sKV);
     auto mma_S = [&](int t, int sl) {
@@ -213,66 +217,82 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::mma_ts(d, a + kk * 8, b, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
       }
     };
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, w));
+    };
     // K_j is stream item 2 (kv_it + j), V_j item 2 (kv_it + j) + 1
     auto slot = [](uint32_t item) { return static_cast<int>(item % C::NSLOT); };
     auto par = [](uint32_t item) { return (item / C::NSLOT) & 1u; };
     uint32_t kv_it = 0, u_it = 0, pp[2] = {0u, 0u};
-    bool ok = true;
+    bool ok = true, moved = false;
     int bh, qb;
     for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qb); ++round) {
       int n0, n1;
       tile_counts(P, qb, &n0, &n1);
-      if (!(ok = ptx::mbar_wait(q_full, u_it & 1u, w))) break;
-      {
-        const uint32_t ik = 2 * kv_it;
-        if (!(ok = ptx::mbar_wait(kv_full + slot(ik), par(ik), w))) break;
-        ptx::tc_fence_after();
+      if (!(ok = wait(q_full, u_it & 1u))) break;
+      const uint32_t ik = 2 * kv_it;
+      if (!(ok = wait(kv_full + slot(ik), par(ik)))) break;
+      ptx::tc_fence_after();
+      if (ptx::elect_one()) {
+        moved |= lane != 0;
         mma_S(0, slot(ik));
         ptx::mma_commit(s_full + 0);
         mma_S(1, slot(ik));
         ptx::mma_commit(s_full + 1);
         ptx::mma_commit(kv_empty + slot(ik));
       }
+      __syncwarp();
       for (int j = 0; j < n1; ++j) {
         const uint32_t iv = 2 * (kv_it + j) + 1, ikn = iv + 1;   // V_j, K_{j+1}
-        if (!(ok = ptx::mbar_wait(kv_full + slot(iv), par(iv), w))) break;
+        if (!(ok = wait(kv_full + slot(iv), par(iv)))) break;
         if (j < n0) {
-          if (!(ok = ptx::mbar_wait(p_full + 0, pp[0] & 1u, w))) break;
+          const bool more = j + 1 < n0;
+          if (!(ok = wait(p_full + 0, pp[0] & 1u))) break;
           ++pp[0];
+          if (more && !(ok = wait(kv_full + slot(ikn), par(ikn)))) break;
           ptx::tc_fence_after();
-          mma_PV(0, slot(iv), j > 0);
-          if (j == n0 - 1) {
-            ptx::mma_commit(o_full + 0);
-          } else {
-            if (!(ok = ptx::mbar_wait(kv_full + slot(ikn), par(ikn), w))) break;
-            ptx::tc_fence_after();
-            mma_S(0, slot(ikn));
-            ptx::mma_commit(s_full + 0);
+          if (ptx::elect_one()) {
+            moved |= lane != 0;
+            mma_PV(0, slot(iv), j > 0);
+            if (more) {
+              mma_S(0, slot(ikn));
+              ptx::mma_commit(s_full + 0);
+            } else {
+              ptx::mma_commit(o_full + 0);
+            }
+          }
+          __syncwarp();
+        }
+        const bool more = j + 1 < n1;
+        if (!(ok = wait(p_full + 1, pp[1] & 1u))) break;
+        ++pp[1];
+        if (more && !(ok = wait(kv_full + slot(ikn), par(ikn)))) break;
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) {
+          moved |= lane != 0;
+          mma_PV(1, slot(iv), j > 0);
+          if (!more) ptx::mma_commit(o_full + 1);
+          ptx::mma_commit(kv_empty + slot(iv));
+          if (more) {
+            mma_S(1, slot(ikn));
+            ptx::mma_commit(s_full + 1);
+            ptx::mma_commit(kv_empty + slot(ikn));
           }
         }
-        if (!(ok = ptx::mbar_wait(p_full + 1, pp[1] & 1u, w))) break;
-        ++pp[1];
-        ptx::tc_fence_after();
-        mma_PV(1, slot(iv), j > 0);
-        if (j == n1 - 1) ptx::mma_commit(o_full + 1);
-        ptx::mma_commit(kv_empty + slot(iv));
-        if (j + 1 < n1) {
-          if (!(ok = ptx::mbar_wait(kv_full + slot(ikn), par(ikn), w))) break;
-          ptx::tc_fence_after();
-          mma_S(1, slot(ikn));
-          ptx::mma_commit(s_full + 1);
-          ptx::mma_commit(kv_empty + slot(ikn));
-        }
+        __syncwarp();
       }
       if (!ok) break;
-      ptx::mma_commit(q_empty);
+      if (ptx::elect_one()) ptx::mma_commit(q_empty);
+      __syncwarp();
       kv_it += n1;
       ++u_it;
     }
     if (!ok) {
-      ptx::mma_commit(drain);
+      if (ptx::elect_one()) ptx::mma_commit(drain);
+      __syncwarp();
       ptx::mbar_wait_drain(drain, 0u);
     }
+    if (__any_sync(0xffffffffu, moved) && lane == 0) atomicOr(P.status, ATTN_DEV_ISSUER);
    }
   } else {
     ptx::reg_acquire<REG_SOFTMAX>();

@@ -233,6 +233,21 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// Elects one lane of the converged warp (elect.sync). The MMA roles run their
+// schedule with the whole warp, so operand descriptors are warp-uniform
+// values, and let the elected lane issue each step's tcgen05 operations.
+// Issuing from a lane chosen with `lane == 0` instead measured about twice as
+// slow per MMA once other warps of the same SM sub-partition were busy.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(e));
+  return e != 0;
+}
+
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
