@@ -482,17 +482,19 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
                                          pg.y * (__uint_as_float(rd[c][2 * i + 3]) - d4.w));
             }
             ptx::tmem_st16(tDP + c * 16, pk);
-            // dS is MN-major for the dQ product: row = key j, column = query
+            if (ATOMIC_DQ) {
+              // dS is MN-major for the dQ product: row = key j, column = query
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const uint32_t off = sw128_offset(j, 64 * h + c * 32 + v * 8);
-              *reinterpret_cast<uint4*>(sdS + off) =
-                  make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+              for (int v = 0; v < 4; ++v) {
+                const uint32_t off = sw128_offset(j, 64 * h + c * 32 + v * 8);
+                *reinterpret_cast<uint4*>(sdS + off) =
+                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+              }
             }
           }
         }
         ptx::tmem_st_wait();
-        ptx::fence_proxy_async_smem();
+        if (ATOMIC_DQ) ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         ptx::mbar_arrive(ds_full);
       }
@@ -628,16 +630,20 @@ template <int HD>
 struct CfgQ {
   static constexpr int KB = HD / 64;
   static constexpr int TILE = BT * HD * 2;
-  // K and V tiles share one FIFO ring of tile-sized slots, loaded in the
-  // order they are consumed (K_0, V_0, K_1, V_1, ...): five slots give each
-  // tile about two key steps of lead over its first use.
-  static constexpr int NSLOT = (HD == 128) ? 5 : 10;
+  // K and V tiles have rings of their own. A K tile stays resident from its
+  // S product to its dQ product one step later, a V tile only until its dP
+  // product, so K gets three slots and V two: both then arrive about one key
+  // step ahead of their first use.
+  static constexpr int NSK = (HD == 128) ? 3 : 6;
+  static constexpr int NSV = (HD == 128) ? 2 : 4;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = OFF_Q + TILE;
-  static constexpr int OFF_KV = OFF_DO + TILE;         // [NSLOT]
-  static constexpr int OFF_BAR = OFF_KV + NSLOT * TILE;
-  // q_full, q_empty, kv_full[NSLOT], kv_empty[NSLOT], s_full, s_free, dp_full, ds_full, dq_full, drain
-  static constexpr int NBAR = 2 + 2 * NSLOT + 6;
+  static constexpr int OFF_K = OFF_DO + TILE;          // [NSK]
+  static constexpr int OFF_V = OFF_K + NSK * TILE;     // [NSV]
+  static constexpr int OFF_BAR = OFF_V + NSV * TILE;
+  // q_full, q_empty, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full, s_free, dp_full[2],
+  // ds_full[2], dq_full, drain
+  static constexpr int NBAR = 2 + 2 * NSK + 2 * NSV + 8;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16(BT, BT, false, false);
@@ -649,6 +655,9 @@ constexpr int DQ_THREADS = 192;
 // For each key tile (fixed ascending order): S = Q K^T, dP = dO V^T (both in
 // TMEM, one thread per query row), dS = P o (dP - D) written bf16 over dP,
 // and dQ += dS K accumulates in TMEM. Warps: 0 producer, 1 MMA, 2-5 rows.
+// TMEM: S [0, 128), dQ [128, 256), dP/dS in two buffers [256, 384) and
+// [384, 512) alternating by step, so the MMA warp computes dP of step j + 1
+// while the row threads still turn dP of step j into dS.
 template <int HD>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -664,31 +673,40 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   }
   uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sdO = smem + C::OFF_DO;
-  uint8_t* sKV = smem + C::OFF_KV;
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* kv_full = bars + 2;               // [NSLOT]
-  uint64_t* kv_empty = kv_full + C::NSLOT;    // [NSLOT]
-  uint64_t* s_full = kv_empty + C::NSLOT;
+  uint64_t* k_full = bars + 2;               // [NSK]
+  uint64_t* k_empty = k_full + C::NSK;       // [NSK]
+  uint64_t* v_full = k_empty + C::NSK;       // [NSV]
+  uint64_t* v_empty = v_full + C::NSV;       // [NSV]
+  uint64_t* s_full = v_empty + C::NSV;
   uint64_t* s_free = s_full + 1;
-  uint64_t* dp_full = s_full + 2;
-  uint64_t* ds_full = s_full + 3;
-  uint64_t* dq_full = s_full + 4;
-  uint64_t* drain = s_full + 5;
+  uint64_t* dp_full = s_full + 2;   // [2], by step parity
+  uint64_t* ds_full = s_full + 4;   // [2], by step parity
+  uint64_t* dq_full = s_full + 6;
+  uint64_t* drain = s_full + 7;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
     ptx::mbar_init(q_empty, 1);
-    for (int s = 0; s < C::NSLOT; ++s) {
-      ptx::mbar_init(kv_full + s, 1);
-      ptx::mbar_init(kv_empty + s, 1);
+    for (int s = 0; s < C::NSK; ++s) {
+      ptx::mbar_init(k_full + s, 1);
+      ptx::mbar_init(k_empty + s, 1);
+    }
+    for (int s = 0; s < C::NSV; ++s) {
+      ptx::mbar_init(v_full + s, 1);
+      ptx::mbar_init(v_empty + s, 1);
     }
     ptx::mbar_init(s_full, 1);
     ptx::mbar_init(s_free, 128);
-    ptx::mbar_init(dp_full, 1);
-    ptx::mbar_init(ds_full, 128);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(dp_full + b, 1);
+      ptx::mbar_init(ds_full + b, 128);
+    }
     ptx::mbar_init(dq_full, 1);
     ptx::mbar_init(drain, 1);
     *abort_flag = 0u;
@@ -702,13 +720,17 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t T_S = 0, T_DP = 128, T_DQ = 256;
+  const uint32_t T_S = 0, T_DQ = 128;
+  auto t_dp = [](uint32_t step) { return 256u + 128u * (step & 1u); };   // dP / dS buffer of a step
   const int grid = gridDim.x, cta = blockIdx.x;
   const int Tq = P.p.Tq, Tk = P.p.Tk;
   auto nk_of = [&](int qt) { return P.p.causal ? min(qt + 1, P.n_k_tiles) : P.n_k_tiles; };
-  // K_j is stream item 2 (k_it + j), V_j item 2 (k_it + j) + 1 (k_it runs across units)
-  auto slot = [](uint32_t item) { return static_cast<int>(item % C::NSLOT); };
-  auto par = [](uint32_t item) { return (item / C::NSLOT) & 1u; };
+  // Key tile j of a unit is the CTA's tile number t = k_it + j (k_it runs
+  // across units); its K sits in K slot t % NSK, its V in V slot t % NSV.
+  auto kslot = [](uint32_t t) { return static_cast<int>(t % C::NSK); };
+  auto kpar = [](uint32_t t) { return (t / C::NSK) & 1u; };
+  auto vslot = [](uint32_t t) { return static_cast<int>(t % C::NSV); };
+  auto vpar = [](uint32_t t) { return (t / C::NSV) & 1u; };
 
   if (warp == 0 && lane == 0) {
     ptx::WaitCtx w{abort_flag, P.status, 5u};
@@ -723,22 +745,26 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         ptx::tma_load_3d(sQ + b * BOX_BYTES, &tmQ, q_full, b * 64, qt * BT, bh);
         ptx::tma_load_3d(sdO + b * BOX_BYTES, &tmdO, q_full, b * 64, qt * BT, bh);
       }
-      uint32_t issued = 2 * k_it;   // stream items issued so far
+      uint32_t k_issued = k_it, v_issued = k_it;   // tiles issued so far
       for (int j = 0; ok && j < nk; ++j, ++k_it) {
-        for (int kv = 0; kv < 2; ++kv) {
-          const uint32_t item = 2 * k_it + kv;
-          if (!(ok = ptx::mbar_wait(kv_empty + slot(item), par(item) ^ 1u, w))) break;
-          ptx::mbar_arrive_expect_tx(kv_full + slot(item), C::TILE);
-          for (int b = 0; b < C::KB; ++b)
-            ptx::tma_load_3d(sKV + slot(item) * C::TILE + b * BOX_BYTES, kv ? &tmV : &tmK, kv_full + slot(item),
-                             b * 64, j * BT, bh);
-          issued = item + 1;
-        }
+        const uint32_t t = k_it;
+        if (!(ok = ptx::mbar_wait(k_empty + kslot(t), kpar(t) ^ 1u, w))) break;
+        ptx::mbar_arrive_expect_tx(k_full + kslot(t), C::TILE);
+        for (int b = 0; b < C::KB; ++b)
+          ptx::tma_load_3d(sK + kslot(t) * C::TILE + b * BOX_BYTES, &tmK, k_full + kslot(t), b * 64, j * BT, bh);
+        k_issued = t + 1;
+        if (!(ok = ptx::mbar_wait(v_empty + vslot(t), vpar(t) ^ 1u, w))) break;
+        ptx::mbar_arrive_expect_tx(v_full + vslot(t), C::TILE);
+        for (int b = 0; b < C::KB; ++b)
+          ptx::tma_load_3d(sV + vslot(t) * C::TILE + b * BOX_BYTES, &tmV, v_full + vslot(t), b * 64, j * BT, bh);
+        v_issued = t + 1;
       }
       if (!ok) {
         // Let the copies already in flight land before the CTA exits.
-        for (uint32_t n = (issued > (uint32_t)C::NSLOT ? issued - C::NSLOT : 0u); n < issued; ++n)
-          ptx::mbar_wait_drain(kv_full + slot(n), par(n));
+        for (uint32_t n = (k_issued > (uint32_t)C::NSK ? k_issued - C::NSK : 0u); n < k_issued; ++n)
+          ptx::mbar_wait_drain(k_full + kslot(n), kpar(n));
+        for (uint32_t n = (v_issued > (uint32_t)C::NSV ? v_issued - C::NSV : 0u); n < v_issued; ++n)
+          ptx::mbar_wait_drain(v_full + vslot(n), vpar(n));
         ptx::mbar_wait_drain(q_full, u_it & 1u);
         break;
       }
@@ -748,7 +774,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     // The whole warp follows the schedule and waits; the elected lane (lane 0)
     // issues the MMAs and commits (see the dK/dV kernel).
     ptx::WaitCtx w{abort_flag, P.status, 6u};
-    const uint32_t aQ = ptx::smem_u32(sQ), adO = ptx::smem_u32(sdO), aKV = ptx::smem_u32(sKV);
+    const uint32_t aQ = ptx::smem_u32(sQ), adO = ptx::smem_u32(sdO), aK = ptx::smem_u32(sK),
+                   aV = ptx::smem_u32(sV);
     auto kmaj = [](uint32_t base, int kk) {
       return ptx::sdesc_sw128(base + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
     };
@@ -759,62 +786,73 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     uint32_t u_it = 0, k_it = 0, sp = 0;
     bool ok = true, moved = false;
     int bh, qt;
+    auto mma_s = [&](uint32_t t) {   // S = Q K^T with key tile t
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk)
+        ptx::mma_ss(tmem + T_S, kmaj(aQ, kk), kmaj(aK + kslot(t) * C::TILE, kk), C::IDESC_S, kk > 0);
+    };
+    auto mma_dp = [&](uint32_t t, uint32_t step) {   // dP = dO V^T into the step's buffer
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk)
+        ptx::mma_ss(tmem + t_dp(step), kmaj(adO, kk), kmaj(aV + vslot(t) * C::TILE, kk), C::IDESC_S, kk > 0);
+      ptx::mma_commit(dp_full + (step & 1u));
+      ptx::mma_commit(v_empty + vslot(t));
+    };
     for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qt); ++round) {
       const int nk = nk_of(qt);
       if (!(ok = wait(q_full, u_it & 1u))) break;
-      // S for the first key tile
+      // S and dP of the first key tile
       {
-        const uint32_t ik = 2 * k_it;
-        if (!(ok = wait(kv_full + slot(ik), par(ik)))) break;
+        const uint32_t t = k_it;
+        if (!(ok = wait(k_full + kslot(t), kpar(t)))) break;
         ptx::tc_fence_after();
         if (ptx::elect_one()) {
           moved |= lane != 0;
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk)
-            ptx::mma_ss(tmem + T_S, kmaj(aQ, kk), kmaj(aKV + slot(ik) * C::TILE, kk), C::IDESC_S, kk > 0);
+          mma_s(t);
           ptx::mma_commit(s_full);
+        }
+        __syncwarp();
+        if (!(ok = wait(v_full + vslot(t), vpar(t)))) break;
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) {
+          moved |= lane != 0;
+          mma_dp(t, sp);
         }
         __syncwarp();
       }
       for (int j = 0; j < nk; ++j, ++sp) {
-        const uint32_t ik = 2 * (k_it + j), iv = ik + 1, ikn = ik + 2;
-        const bool more = j + 1 < nk;
-        // dP = dO V^T (the dP columns are free: the previous dQ product read dS from them)
-        if (!(ok = wait(kv_full + slot(iv), par(iv)))) break;
-        ptx::tc_fence_after();
-        if (ptx::elect_one()) {
-          moved |= lane != 0;
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk)
-            ptx::mma_ss(tmem + T_DP, kmaj(adO, kk), kmaj(aKV + slot(iv) * C::TILE, kk), C::IDESC_S, kk > 0);
-          ptx::mma_commit(dp_full);
-          ptx::mma_commit(kv_empty + slot(iv));
-        }
-        __syncwarp();
-        // next S once the row threads have read this one
-        if (more) {
-          if (!(ok = wait(kv_full + slot(ikn), par(ikn)))) break;
+        const uint32_t t = k_it + j, tn = t + 1;
+        if (j + 1 < nk) {
+          // S of the next key tile once the row threads have read this one,
+          // then its dP into the other buffer (whose dS the previous dQ
+          // product has consumed: MMAs run in issue order)
+          if (!(ok = wait(k_full + kslot(tn), kpar(tn)))) break;
           if (!(ok = wait(s_free, sp & 1u))) break;
           ptx::tc_fence_after();
           if (ptx::elect_one()) {
             moved |= lane != 0;
-#pragma unroll
-            for (int kk = 0; kk < HD / 16; ++kk)
-              ptx::mma_ss(tmem + T_S, kmaj(aQ, kk), kmaj(aKV + slot(ikn) * C::TILE, kk), C::IDESC_S, kk > 0);
+            mma_s(tn);
             ptx::mma_commit(s_full);
+          }
+          __syncwarp();
+          if (!(ok = wait(v_full + vslot(tn), vpar(tn)))) break;
+          ptx::tc_fence_after();
+          if (ptx::elect_one()) {
+            moved |= lane != 0;
+            mma_dp(tn, sp + 1);
           }
           __syncwarp();
         }
         // dQ += dS K
-        if (!(ok = wait(ds_full, sp & 1u))) break;
+        if (!(ok = wait(ds_full + (sp & 1u), (sp >> 1) & 1u))) break;
         ptx::tc_fence_after();
         if (ptx::elect_one()) {
           moved |= lane != 0;
 #pragma unroll
           for (int kk = 0; kk < BT / 16; ++kk)
-            ptx::mma_ts(tmem + T_DQ, tmem + T_DP + kk * 8, mnmaj(aKV + slot(ik) * C::TILE, kk), C::IDESC_DQ,
+            ptx::mma_ts(tmem + T_DQ, tmem + t_dp(sp) + kk * 8, mnmaj(aK + kslot(t) * C::TILE, kk), C::IDESC_DQ,
                         (j > 0 || kk > 0) ? 1u : 0u);
-          ptx::mma_commit(kv_empty + slot(ik));
+          ptx::mma_commit(k_empty + kslot(t));
         }
         __syncwarp();
       }
@@ -838,7 +876,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_off + T_S, tDP = tmem + lane_off + T_DP, tDQ = tmem + lane_off + T_DQ;
+    const uint32_t tS = tmem + lane_off + T_S, tDQ = tmem + lane_off + T_DQ;
     ptx::WaitCtx w{abort_flag, P.status, 7u};
     const float sc2 = P.sc2, scale = P.p.scale;
     uint32_t u_it = 0, sp = 0;
@@ -875,8 +913,9 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           for (int i = 0; i < 128; ++i)
             if (i >= lim) p[i] = 0.f;
         }
-        if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dp_full, sp & 1u, w)))) break;
+        if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dp_full + (sp & 1u), (sp >> 1) & 1u, w)))) break;
         ptx::tc_fence_after();
+        const uint32_t tDP = tmem + lane_off + t_dp(sp);
         uint32_t v[4][32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tDP + c * 32, v[c]);   // all four in flight
@@ -893,7 +932,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         }
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(ds_full);
+        ptx::mbar_arrive(ds_full + (sp & 1u));
       }
       if (!ok) break;
       if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dq_full, u_it & 1u, w)))) break;
