@@ -107,24 +107,34 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int col) {
          (col & 7) * 2;
 }
 
-template <int HD>
+template <int HD, bool ATOMIC_DQ>
 struct CfgKV {
   static constexpr int KB = HD / 64;
   static constexpr int TILE = BT * HD * 2;
+  // Q tiles, dO tiles and the LSE*log2(e) / D slices of a query tile have
+  // rings of their own. A Q tile stays resident from its S^T product to its
+  // dK product at the end of the step, a dO tile from its dP^T product to its
+  // dV product in the middle of the next one, the slices until the P/dS
+  // threads finish the step. The deterministic variant, which needs no dS
+  // buffer in shared memory, gives Q three slots; atomic mode keeps two.
+  static constexpr int NQ = ATOMIC_DQ ? 2 : 3;
+  static constexpr int NO = 2;
+  static constexpr int NL = 2;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE;
-  static constexpr int OFF_Q = OFF_V + TILE;          // [2]
-  static constexpr int OFF_DO = OFF_Q + 2 * TILE;     // [2]
-  // dS, 128 q x 128 keys bf16, MN-major; in atomic mode it then stages one
+  static constexpr int OFF_Q = OFF_V + TILE;          // [NQ]
+  static constexpr int OFF_DO = OFF_Q + NQ * TILE;    // [NO]
+  // atomic mode: dS, 128 q x 128 keys bf16, MN-major; it then stages one
   // 64-column half of the fp32 dQ tile (two 128 x 32 boxes) for the TMA reduce
-  static constexpr int OFF_DS = OFF_DO + 2 * TILE;
-  static constexpr int DS_BYTES = BT * BT * 2;
-  static constexpr int OFF_LSE = OFF_DS + DS_BYTES;   // [2][128] fp32 (LSE * log2 e, +inf = no key)
-  static constexpr int OFF_D = OFF_LSE + 2 * BT * 4;  // [2][128] fp32
-  static constexpr int OFF_BAR = OFF_D + 2 * BT * 4;
-  // kv_full, kv_empty, q_full[2], q_empty[2], s_full, dp_full, p_full, ds_full,
-  // dq_full, dq_free, acc_full, acc_free, stage_full, stage_free, sds_free, drain
-  static constexpr int NBAR = 18;
+  static constexpr int OFF_DS = OFF_DO + NO * TILE;
+  static constexpr int DS_BYTES = ATOMIC_DQ ? BT * BT * 2 : 0;
+  static constexpr int OFF_LSE = OFF_DS + DS_BYTES;   // [NL][128] fp32 (LSE * log2 e, +inf = no key)
+  static constexpr int OFF_D = OFF_LSE + NL * BT * 4; // [NL][128] fp32
+  static constexpr int OFF_BAR = OFF_D + NL * BT * 4;
+  // kv_full, kv_empty, q_full[NQ], q_empty[NQ], o_full[NO], o_empty[NO], l_full[NL], l_empty[NL],
+  // s_full, dp_full, p_full, ds_full, dq_full, dq_free, acc_full, acc_free, stage_full, stage_free,
+  // sds_free, drain
+  static constexpr int NBAR = 2 + 2 * NQ + 2 * NO + 2 * NL + 12;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16(BT, BT, false, false);
@@ -143,7 +153,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const __grid_constant__ CUtensorMap tmdQ, const Params P) {
-  using C = CfgKV<HD>;
+  using C = CfgKV<HD, ATOMIC_DQ>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -161,29 +171,41 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bars + 0;
   uint64_t* kv_empty = bars + 1;
-  uint64_t* q_full = bars + 2;    // [2]
-  uint64_t* q_empty = bars + 4;   // [2]
-  uint64_t* s_full = bars + 6;
-  uint64_t* dp_full = bars + 7;
-  uint64_t* p_full = bars + 8;
-  uint64_t* ds_full = bars + 9;
-  uint64_t* dq_full = bars + 10;
-  uint64_t* dq_free = bars + 11;
-  uint64_t* acc_full = bars + 12;
-  uint64_t* acc_free = bars + 13;
-  uint64_t* stage_full = bars + 14;
-  uint64_t* stage_free = bars + 15;
-  uint64_t* sds_free = bars + 16;
-  uint64_t* drain = bars + 17;
+  uint64_t* q_full = bars + 2;             // [NQ]
+  uint64_t* q_empty = q_full + C::NQ;      // [NQ]
+  uint64_t* o_full = q_empty + C::NQ;      // [NO]
+  uint64_t* o_empty = o_full + C::NO;      // [NO]
+  uint64_t* l_full = o_empty + C::NO;      // [NL]
+  uint64_t* l_empty = l_full + C::NL;      // [NL]
+  uint64_t* s_full = l_empty + C::NL;
+  uint64_t* dp_full = s_full + 1;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* ds_full = s_full + 3;
+  uint64_t* dq_full = s_full + 4;
+  uint64_t* dq_free = s_full + 5;
+  uint64_t* acc_full = s_full + 6;
+  uint64_t* acc_free = s_full + 7;
+  uint64_t* stage_full = s_full + 8;
+  uint64_t* stage_free = s_full + 9;
+  uint64_t* sds_free = s_full + 10;
+  uint64_t* drain = s_full + 11;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(kv_full, 1);
     ptx::mbar_init(kv_empty, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::NQ; ++s) {
       ptx::mbar_init(q_full + s, 1);
       ptx::mbar_init(q_empty + s, 1);
+    }
+    for (int s = 0; s < C::NO; ++s) {
+      ptx::mbar_init(o_full + s, 1);
+      ptx::mbar_init(o_empty + s, 1);
+    }
+    for (int s = 0; s < C::NL; ++s) {
+      ptx::mbar_init(l_full + s, 1);
+      ptx::mbar_init(l_empty + s, 256);
     }
     ptx::mbar_init(s_full, 1);
     ptx::mbar_init(dp_full, 1);
@@ -209,6 +231,13 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t T_DV = 0, T_DK = 128, T_ST = 256, T_DP = 384;
+  // Query tile number n (counted across units) uses Q slot n % NQ and dO slot n % NO.
+  auto qslot = [](uint32_t n) { return static_cast<int>(n % C::NQ); };
+  auto qpar = [](uint32_t n) { return (n / C::NQ) & 1u; };
+  auto oslot = [](uint32_t n) { return static_cast<int>(n % C::NO); };
+  auto opar = [](uint32_t n) { return (n / C::NO) & 1u; };
+  auto lslot = [](uint32_t n) { return static_cast<int>(n % C::NL); };
+  auto lpar = [](uint32_t n) { return (n / C::NL) & 1u; };
 
   const int grid = gridDim.x, cta = blockIdx.x;
   const int Tq = P.p.Tq, Tk = P.p.Tk;
@@ -223,7 +252,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       ptx::tma_prefetch_desc(&tmK);
       ptx::tma_prefetch_desc(&tmV);
       ptx::tma_prefetch_desc(&tmdO);
-      uint32_t u_it = 0, q_it = 0;
+      uint32_t u_it = 0, q_it = 0, q_issued = 0, o_issued = 0, l_issued = 0;
       bool ok = true;
       int bh, kb;
       for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &kb); ++round) {
@@ -237,25 +266,37 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           ptx::tma_load_3d(sV + b * BOX_BYTES, &tmV, kv_full, b * 64, kb * BT, bh);
         }
         for (int ii = 0; ii < nq; ++ii, ++q_it) {
-          const int st = q_it & 1;
-          const uint32_t ph = (q_it >> 1) & 1u;
-          if (!(ok = ptx::mbar_wait(q_empty + st, ph ^ 1u, w))) break;
+          const int qs = qslot(q_it), os = oslot(q_it);
           const int qt = q0 + ii;
           const size_t row0 = static_cast<size_t>(bh) * P.Tq_pad + static_cast<size_t>(qt) * BT;
-          ptx::mbar_arrive_expect_tx(q_full + st, 2 * C::TILE + 2 * BT * 4);
-          for (int b = 0; b < C::KB; ++b) {
-            ptx::tma_load_3d(sQ + st * C::TILE + b * BOX_BYTES, &tmQ, q_full + st, b * 64, qt * BT, bh);
-            ptx::tma_load_3d(sdO + st * C::TILE + b * BOX_BYTES, &tmdO, q_full + st, b * 64, qt * BT, bh);
-          }
-          ptx::bulk_load(sLSE + st * BT, P.LSE2 + row0, BT * 4, q_full + st);
-          ptx::bulk_load(sD + st * BT, P.D + row0, BT * 4, q_full + st);
+          if (!(ok = ptx::mbar_wait(q_empty + qs, qpar(q_it) ^ 1u, w))) break;
+          ptx::mbar_arrive_expect_tx(q_full + qs, C::TILE);
+          for (int b = 0; b < C::KB; ++b)
+            ptx::tma_load_3d(sQ + qs * C::TILE + b * BOX_BYTES, &tmQ, q_full + qs, b * 64, qt * BT, bh);
+          q_issued = q_it + 1;
+          const int ls = lslot(q_it);
+          if (!(ok = ptx::mbar_wait(l_empty + ls, lpar(q_it) ^ 1u, w))) break;
+          ptx::mbar_arrive_expect_tx(l_full + ls, 2 * BT * 4);
+          ptx::bulk_load(sLSE + ls * BT, P.LSE2 + row0, BT * 4, l_full + ls);
+          ptx::bulk_load(sD + ls * BT, P.D + row0, BT * 4, l_full + ls);
+          l_issued = q_it + 1;
+          if (!(ok = ptx::mbar_wait(o_empty + os, opar(q_it) ^ 1u, w))) break;
+          ptx::mbar_arrive_expect_tx(o_full + os, C::TILE);
+          for (int b = 0; b < C::KB; ++b)
+            ptx::tma_load_3d(sdO + os * C::TILE + b * BOX_BYTES, &tmdO, o_full + os, b * 64, qt * BT, bh);
+          o_issued = q_it + 1;
         }
         ++u_it;
       }
       if (!ok) {
+        // Let the copies already in flight land before the CTA exits.
         if (u_it > 0 || q_it > 0) ptx::mbar_wait_drain(kv_full, u_it & 1u);
-        for (uint32_t n = (q_it > 2u ? q_it - 2u : 0u); n < q_it; ++n)
-          ptx::mbar_wait_drain(q_full + (n & 1), (n >> 1) & 1u);
+        for (uint32_t n = (q_issued > (uint32_t)C::NQ ? q_issued - C::NQ : 0u); n < q_issued; ++n)
+          ptx::mbar_wait_drain(q_full + qslot(n), qpar(n));
+        for (uint32_t n = (o_issued > (uint32_t)C::NO ? o_issued - C::NO : 0u); n < o_issued; ++n)
+          ptx::mbar_wait_drain(o_full + oslot(n), opar(n));
+        for (uint32_t n = (l_issued > (uint32_t)C::NL ? l_issued - C::NL : 0u); n < l_issued; ++n)
+          ptx::mbar_wait_drain(l_full + lslot(n), lpar(n));
       }
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
@@ -272,15 +313,15 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       auto mnmaj = [](uint32_t base, int kk) {  // MN-major operand, k-step kk of 16 rows
         return ptx::sdesc_sw128(base + kk * 2048, BOX_BYTES, 1024);
       };
-      auto mma_st = [&](int st) {
+      auto mma_st = [&](uint32_t n) {   // S^T = K Q^T for query tile n
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          ptx::mma_ss(tmem + T_ST, kmaj(aK, kk), kmaj(aQ + st * C::TILE, kk), C::IDESC_S, kk > 0);
+          ptx::mma_ss(tmem + T_ST, kmaj(aK, kk), kmaj(aQ + qslot(n) * C::TILE, kk), C::IDESC_S, kk > 0);
       };
-      auto mma_dpt = [&](int st) {
+      auto mma_dpt = [&](uint32_t n) {   // dP^T = V dO^T for query tile n
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          ptx::mma_ss(tmem + T_DP, kmaj(aV, kk), kmaj(adO + st * C::TILE, kk), C::IDESC_S, kk > 0);
+          ptx::mma_ss(tmem + T_DP, kmaj(aV, kk), kmaj(adO + oslot(n) * C::TILE, kk), C::IDESC_S, kk > 0);
       };
       auto wait = [&](uint64_t* bar, uint32_t parity) {
         return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, w));
@@ -295,43 +336,43 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         if (!(ok = wait(kv_full, u_it & 1u))) break;
         if (!(ok = wait(acc_free, (u_it & 1u) ^ 1u))) break;
         {
-          const int st = q_it & 1;
-          if (!(ok = wait(q_full + st, (q_it >> 1) & 1u))) break;
+          if (!(ok = wait(q_full + qslot(q_it), qpar(q_it)))) break;
           ptx::tc_fence_after();
           if (ptx::elect_one()) {
             moved |= lane != 0;
-            mma_st(st);
+            mma_st(q_it);
             ptx::mma_commit(s_full);
           }
           __syncwarp();
           if (ATOMIC_DQ && dqf > 0) {
             if (!(ok = wait(dq_free, (dqf - 1) & 1u))) break;
-            ptx::tc_fence_after();
           }
+          if (!(ok = wait(o_full + oslot(q_it), opar(q_it)))) break;
+          ptx::tc_fence_after();
           if (ptx::elect_one()) {
             moved |= lane != 0;
-            mma_dpt(st);
+            mma_dpt(q_it);
             ptx::mma_commit(dp_full);
           }
           __syncwarp();
         }
         for (int ii = 0; ii < nq; ++ii) {
           const uint32_t it = q_it + ii;
-          const int st = it & 1, stn = (it + 1) & 1;
           const bool more = ii + 1 < nq;
           // dV += P^T dO, then the next S^T (it overwrites P^T only after the
           // product above has read it)
           if (!(ok = wait(p_full, pp & 1u))) break;
-          if (more && !(ok = wait(q_full + stn, ((it + 1) >> 1) & 1u))) break;
+          if (more && !(ok = wait(q_full + qslot(it + 1), qpar(it + 1)))) break;
           ptx::tc_fence_after();
           if (ptx::elect_one()) {
             moved |= lane != 0;
 #pragma unroll
             for (int kk = 0; kk < BT / 16; ++kk)
-              ptx::mma_ts(tmem + T_DV, tmem + T_ST + packed_col(kk), mnmaj(adO + st * C::TILE, kk), C::IDESC_ACC,
-                          (ii > 0 || kk > 0) ? 1u : 0u);
+              ptx::mma_ts(tmem + T_DV, tmem + T_ST + packed_col(kk), mnmaj(adO + oslot(it) * C::TILE, kk),
+                          C::IDESC_ACC, (ii > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_commit(o_empty + oslot(it));
             if (more) {
-              mma_st(stn);
+              mma_st(it + 1);
               ptx::mma_commit(s_full);
             }
           }
@@ -344,9 +385,9 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
             moved |= lane != 0;
 #pragma unroll
             for (int kk = 0; kk < BT / 16; ++kk)
-              ptx::mma_ts(tmem + T_DK, tmem + T_DP + packed_col(kk), mnmaj(aQ + st * C::TILE, kk), C::IDESC_ACC,
-                          (ii > 0 || kk > 0) ? 1u : 0u);
-            ptx::mma_commit(q_empty + st);
+              ptx::mma_ts(tmem + T_DK, tmem + T_DP + packed_col(kk), mnmaj(aQ + qslot(it) * C::TILE, kk),
+                          C::IDESC_ACC, (ii > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_commit(q_empty + qslot(it));
             if (ATOMIC_DQ) {
 #pragma unroll
               for (int kk = 0; kk < BT / 16; ++kk)
@@ -359,11 +400,12 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           if (more) {
             if (ATOMIC_DQ) {
               if (!(ok = wait(dq_free, (dqf - 1) & 1u))) break;
-              ptx::tc_fence_after();
             }
+            if (!(ok = wait(o_full + oslot(it + 1), opar(it + 1)))) break;
+            ptx::tc_fence_after();
             if (ptx::elect_one()) {
               moved |= lane != 0;
-              mma_dpt(stn);
+              mma_dpt(it + 1);
               ptx::mma_commit(dp_full);
             }
             __syncwarp();
@@ -407,12 +449,12 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       const int key = kb * BT + j;
       const bool key_ok = key < Tk;
       for (int ii = 0; ii < nq; ++ii, ++q_it, ++sp) {
-        const int st = q_it & 1;
+        const int ls = lslot(q_it);
         const int qt = q0 + ii;
-        const float* lse2 = sLSE + st * BT + 64 * h;
-        const float* dd = sD + st * BT + 64 * h;
-        // the staged LSE / D of this tile are visible once q_full completed
-        if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(q_full + st, (q_it >> 1) & 1u, w)))) break;
+        const float* lse2 = sLSE + ls * BT + 64 * h;
+        const float* dd = sD + ls * BT + 64 * h;
+        // the staged LSE / D slices of this tile are visible once l_full completed
+        if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(l_full + ls, lpar(q_it), w)))) break;
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(s_full, sp & 1u, w)))) break;
         ptx::tc_fence_after();
         // pass 1: P^T_j,q = 2^(s * scale * log2e - LSE2_q), masked; packed bf16
@@ -497,6 +539,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         if (ATOMIC_DQ) ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         ptx::mbar_arrive(ds_full);
+        ptx::mbar_arrive(l_empty + ls);   // done with this tile's LSE / D slices
       }
     }
   } else {
@@ -1008,14 +1051,15 @@ cudaError_t launch(const LaunchBwd& a) {
     const int units = P.n_k_tiles * heads;
     const int grid = units < a.num_sms ? units : a.num_sms;
     auto kern = atomic ? dkdv_kernel<HD, true> : dkdv_kernel<HD, false>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgKV<HD>::SMEM);
+    const int smem = atomic ? CfgKV<HD, true>::SMEM : CfgKV<HD, false>::SMEM;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // The register split must fit the launch allocation (see reg_acquire).
     cudaFuncAttributes fa;
     if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
     if (fa.numRegs != KV_REG_LAUNCH || KV_REG_CTRL + 2 * KV_REG_PDS + KV_REG_DQ > 4 * KV_REG_LAUNCH)
       return cudaErrorInvalidConfiguration;
-    kern<<<grid, KV_THREADS, CfgKV<HD>::SMEM, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO,
+    kern<<<grid, KV_THREADS, smem, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO,
                                                            atomic ? *a.tmdQacc : *a.tmQ, P);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
