@@ -245,7 +245,7 @@ def run_ours(args, w):
     pkg.load_library()
     code = pkg.ATTN_BF16 if w.dtype == "bf16" else pkg.ATTN_F32
     B, H, Tq, Tk, d, dv = w.B, w.H, w.Tq, w.Tk, w.d, w.dv
-    det = int(args.deterministic)
+    det = int(args.dq_mode == "deterministic")
 
     host = make_inputs(w.with_(seed=w.seed + 1000 * rank))
     x = {k: v.to(dev) for k, v in host.items()}
@@ -265,16 +265,20 @@ def run_ours(args, w):
         pkg.attn_bwd_phase(x["Q"], x["K"], x["V"], o, lse, x["dO"], dq, dk, dvv, B, H, Tq, Tk, d, dv, sc,
                            w.causal, code, det, ws, ws.numel(), ph, stream)
 
+    # backward launch groups in order: preprocess, dK/dV kernel, dQ kernel
+    # (deterministic only), dQ conversion (atomic only)
+    phases = (1, 4, 5, 3)
+
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
         fwd()
         if ev is not None:
             ev[1].record(stream)
-        for ph in (1, 2, 3):
+        for i, ph in enumerate(phases):
             bwd_phase(ph)
             if ev is not None:
-                ev[1 + ph].record(stream)
+                ev[2 + i].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -285,7 +289,7 @@ def run_ours(args, w):
     if clocks:
         clocks.start()
         time.sleep(0.3)
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
@@ -297,13 +301,11 @@ def run_ours(args, w):
     barrier()
     if clocks:
         clocks.mark(t_wall0, t_wall1)
-    per = [[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in events]    # ms: fwd, pre, main, conv
+    per = [[e[j].elapsed_time(e[j + 1]) for j in range(5)] for e in events]   # ms: fwd, pre, kv, q, conv
     step_ms = [sum(p) for p in per]
     total_ms = reduce_max(sum(step_ms))
-    fwd_ms = statistics.mean(p[0] for p in per)
-    pre_ms = statistics.mean(p[1] for p in per)
-    main_ms = statistics.mean(p[2] for p in per)
-    conv_ms = statistics.mean(p[3] for p in per)
+    fwd_ms, pre_ms, kv_ms, q_ms, conv_ms = (statistics.mean(p[j] for p in per) for j in range(5))
+    main_ms = kv_ms + q_ms
     bwd_ms = pre_ms + main_ms + conv_ms
     F, Bf = w.fwd_flop(), w.bwd_flop()
     value = world * args.steps * (F + Bf) / (total_ms * 1e-3) / 1e12
@@ -343,20 +345,35 @@ def run_ours(args, w):
 
     peaks = load_peaks()
     peak = peaks["bf16_tflops"]
-    kernels = {
-        "fwd (attn_fwd_bf16_kernel)": {"ms": fwd_ms, "tflops": F / (fwd_ms * 1e-3) / 1e12},
-        "bwd main (dkdv_kernel)": {"ms": main_ms, "tflops": Bf / (main_ms * 1e-3) / 1e12},
+    # Algorithmic FLOP per kernel, in units of one causal matmul (F / 2): the
+    # forward does S and PV; the dK/dV kernel S, dP, dV, dK (and, atomic mode,
+    # dQ); the deterministic dQ kernel's own product is dQ (it recomputes S
+    # and dP, which is counted under "executed").
+    mm = F / 2
+    kernels = {"fwd (attn_fwd_bf16_kernel)": {"ms": fwd_ms, "flop": F}}
+    if det:
+        kernels["bwd dK/dV (dkdv_kernel)"] = {"ms": kv_ms, "flop": 4 * mm}
+        kernels["bwd dQ (dq_kernel)"] = {"ms": q_ms, "flop": mm, "executed_flop": 3 * mm}
+    else:
+        kernels["bwd dK/dV + dQ atomics (dkdv_kernel)"] = {"ms": kv_ms, "flop": 5 * mm}
+    for k, v in kernels.items():
+        v["tflops"] = v["flop"] / (v["ms"] * 1e-3) / 1e12
+        v["frac_of_peak"] = v["tflops"] / peak
+        if "executed_flop" in v:
+            v["executed_tflops"] = v["executed_flop"] / (v["ms"] * 1e-3) / 1e12
+    kernels.update({
+        "bwd main (all main kernels)": {"ms": main_ms, "tflops": Bf / (main_ms * 1e-3) / 1e12},
         # reads O, dO, LSE; writes D and LSE*log2(e) (padded rows) and zeroes the dQ accumulator
         "bwd preprocess": {"ms": pre_ms,
                            "gbs": B * H * Tq * (2 * dv * 2 + 4 + 8 + (d * 4 if not det else 0)) / (pre_ms * 1e-3) / 1e9},
-        "dQ convert": {"ms": conv_ms, "gbs": B * H * Tq * d * (4 + 2) / (conv_ms * 1e-3) / 1e9 if conv_ms > 0 else None},
-    }
-    for k in ("fwd (attn_fwd_bf16_kernel)", "bwd main (dkdv_kernel)"):
-        kernels[k]["frac_of_peak"] = kernels[k]["tflops"] / peak
+        "dQ convert": {"ms": conv_ms, "gbs": B * H * Tq * d * (4 + 2) / (conv_ms * 1e-3) / 1e9 if not det else None},
+    })
+    kernels["bwd main (all main kernels)"]["frac_of_peak"] = kernels["bwd main (all main kernels)"]["tflops"] / peak
     kernels["bwd preprocess"]["frac_of_hbm"] = kernels["bwd preprocess"]["gbs"] / peaks["hbm_gbs"]
-    dom = max(("fwd (attn_fwd_bf16_kernel)", fwd_ms, F), ("bwd main (dkdv_kernel)", main_ms, Bf), key=lambda t: t[1])
-    achieved = dom[2] / (dom[1] * 1e-3) / 1e12
-    traffic = load_traffic("dkdv_kernel" if "dkdv" in dom[0] else "attn_fwd_bf16_kernel")
+    # the dominant kernel: the longest of the single kernels
+    dom = max((k for k, v in kernels.items() if "flop" in v), key=lambda k: kernels[k]["ms"])
+    achieved = kernels[dom]["tflops"]
+    traffic = load_traffic(dom.split("(")[-1].rstrip(")"))
     cfg = workload_config(w)
     cfg.update({"dq_mode": "deterministic" if det else "atomic",
                 "fwd_tflops": F / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": Bf / (bwd_ms * 1e-3) / 1e12,
@@ -366,7 +383,7 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
-        "roofline": {"bound": "tensor", "kernel": dom[0], "achieved": achieved, "peak": peak, "unit": UNIT,
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_note": f"{peaks['source']} dense bf16 burst (cuBLAS 8192^3)"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -387,7 +404,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="c3")
-    ap.add_argument("--deterministic", action="store_true", help="dQ in a separate fixed-order pass")
+    ap.add_argument("--dq-mode", choices=["deterministic", "atomic"], default="deterministic",
+                    help="dQ in a separate fixed-order pass (default) or by fp32 atomics inside the dK/dV kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

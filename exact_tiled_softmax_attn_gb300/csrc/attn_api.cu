@@ -259,7 +259,7 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
                        int phase, void* stream) {
   attn_status_t s = check_common(B, H, Tq, Tk, d, dv, scale, causal, dtype);
   if (s != ATTN_OK) return s;
-  if (phase < 0 || phase > 3) return ATTN_ERR_INVALID_ARG;
+  if (phase < 0 || phase > 5) return ATTN_ERR_INVALID_ARG;
   if (deterministic != 0 && deterministic != 1) return ATTN_ERR_INVALID_ARG;
   const size_t es = elem_size(dtype);
   const size_t bh = static_cast<size_t>(B) * H;
@@ -295,7 +295,7 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
   cudaError_t e = cudaSuccess;
   if (Tq == 0 || Tk == 0) {
     // no (query, key) pair: every gradient is zero
-    if (phase != 0 && phase != 2) return ATTN_OK;
+    if (phase != 0 && phase != 2 && phase != 4) return ATTN_OK;
     if ((e = launch_zero(dQ, bq, st)) == cudaSuccess && (e = launch_zero(dK, bk, st)) == cudaSuccess)
       e = launch_zero(dV, bv, st);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);

@@ -1024,8 +1024,9 @@ template <int HD>
 cudaError_t launch(const LaunchBwd& a) {
   const Problem& p = a.p;
   const bool atomic = !a.deterministic;
-  const bool pre = a.phase == 0 || a.phase == 1, main = a.phase == 0 || a.phase == 2,
-             conv = a.phase == 0 || a.phase == 3;
+  const bool pre = a.phase == 0 || a.phase == 1, conv = a.phase == 0 || a.phase == 3;
+  const bool main_kv = a.phase == 0 || a.phase == 2 || a.phase == 4;
+  const bool main_q = a.phase == 0 || a.phase == 2 || a.phase == 5;
   cudaError_t e = cudaSuccess;
   if (pre) {
     e = launch_bwd_preprocess(p, a.O, a.dO, a.LSE, 2, a.D, a.LSE2, atomic ? a.dQacc : nullptr, p.d, a.num_sms,
@@ -1046,7 +1047,7 @@ cudaError_t launch(const LaunchBwd& a) {
   P.n_k_tiles = (p.Tk + BT - 1) / BT;
   P.sc2 = p.scale * LOG2E;
   const int heads = p.B * p.H;
-  if (main) {
+  if (main_kv) {
     P.order = Order{P.n_k_tiles, heads, p.causal ? 2 : 0};
     const int units = P.n_k_tiles * heads;
     const int grid = units < a.num_sms ? units : a.num_sms;
@@ -1070,7 +1071,7 @@ cudaError_t launch(const LaunchBwd& a) {
                                                             static_cast<uint2*>(a.dQ), n4);
     return cudaGetLastError();
   }
-  if (!main) return cudaSuccess;
+  if (!main_q) return cudaSuccess;
   P.order = Order{P.n_q_tiles, heads, p.causal ? 1 : 0};
   const int units = P.n_q_tiles * heads;
   const int grid = units < a.num_sms ? units : a.num_sms;

@@ -409,7 +409,9 @@ cudaError_t launch_bwd_f32(const LaunchBwd& a) {
                               a.deterministic ? nullptr : static_cast<float*>(a.dQ), p.d, a.num_sms, a.stream);
     if (e != cudaSuccess) return e;
   }
-  if (a.phase != 0 && a.phase != 2) return cudaSuccess;
+  const bool kv = a.phase == 0 || a.phase == 2 || a.phase == 4;
+  const bool q = a.deterministic && (a.phase == 0 || a.phase == 2 || a.phase == 5);
+  if (!kv && !q) return cudaSuccess;
   simt::BwdArgs b{static_cast<const float*>(a.Q), static_cast<const float*>(a.K), static_cast<const float*>(a.V),
                   static_cast<const float*>(a.dO), a.LSE, a.D, static_cast<float*>(a.dQ),
                   static_cast<float*>(a.dK), static_cast<float*>(a.dV), p};
@@ -418,13 +420,13 @@ cudaError_t launch_bwd_f32(const LaunchBwd& a) {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(simt::dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  if (p.Tk > 0) {
+  if (kv && p.Tk > 0) {
     dim3 g1((p.Tk + simt::BNB - 1) / simt::BNB, p.B * p.H);
     simt::dkdv_kernel<<<g1, simt::NT, smem, a.stream>>>(b, a.deterministic ? 0 : 1);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  if (a.deterministic) {
+  if (q) {
     dim3 g2((p.Tq + simt::BM - 1) / simt::BM, p.B * p.H);
     simt::dq_kernel<<<g2, simt::NT, smem, a.stream>>>(b);
     e = cudaGetLastError();

@@ -121,16 +121,18 @@ ATTN_API attn_status_t attn_bwd(const void* Q, const void* K, const void* V, con
                        size_t workspace_bytes, void* stream);
 
 /*
- * The backward split into its three launch groups, for measurement: the
- * same arguments as attn_bwd plus `phase`:
+ * The backward split into its launch groups, for measurement: the same
+ * arguments as attn_bwd plus `phase`:
  *   1  preprocess: D = rowsum(dO o O) (and zeroing of the fp32 dQ
  *      accumulator when deterministic == 0)
- *   2  main kernels: dK, dV and the dQ accumulation (or, deterministic,
- *      the separate dQ pass)
+ *   2  main kernels: phases 4 and 5 in this order
  *   3  dQ conversion from the fp32 accumulator (bf16 with deterministic
  *      == 0; a no-op otherwise)
- * Calling phases 1, 2, 3 in order on one stream equals one attn_bwd call;
- * phase 0 is attn_bwd itself. Other values give ATTN_ERR_INVALID_ARG.
+ *   4  the dK/dV kernel alone (with deterministic == 0 it also accumulates dQ)
+ *   5  the separate dQ kernel alone (deterministic == 1; a no-op otherwise)
+ * Calling phases 1, 2, 3 (or 1, 4, 5, 3) in order on one stream equals one
+ * attn_bwd call; phase 0 is attn_bwd itself. Other values give
+ * ATTN_ERR_INVALID_ARG.
  */
 ATTN_API attn_status_t attn_bwd_phase(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
                                       const void* dO, void* dQ, void* dK, void* dV, int B, int H, int Tq, int Tk,

@@ -128,6 +128,14 @@ def test_backward_host_validation(lib, kw, status):
     assert _bwd(**kw) == status
 
 
+def test_backward_phase_range(lib):
+    args = dict(Q=0x100000, K=0x200000, V=0x300000, O=0x400000, LSE=0x500000, dO=0x600000, dQ=0x700000,
+                dK=0x800000, dV=0x900000, B=1, H=1, Tq=8, Tk=8, d=64, dv=64, scale=0.125, causal=0,
+                dtype=B.ATTN_BF16, deterministic=0, workspace=0xA00000, workspace_bytes=1 << 20)
+    for ph in (-1, 6):
+        assert B.attn_bwd_phase(**args, phase=ph, stream=0, check=False) == B.ATTN_ERR_INVALID_ARG
+
+
 def test_error_text_carries_status(lib):
     with pytest.raises(B.AttnError) as e:
         B.attn_fwd(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 1, 1, 8, 8, 96, 96, 0.1, 0, B.ATTN_BF16,

@@ -167,3 +167,30 @@ def test_bf16_inputs_unchanged():
     for k in x:
         assert torch.equal(x[k], keep[k]), k
     assert torch.equal(o, o2) and torch.equal(lse, lse2)
+
+
+@pytest.mark.parametrize("dt,d", [(torch.float32, 64), (torch.bfloat16, 128)])
+@pytest.mark.parametrize("deterministic", [0, 1])
+def test_phases_equal_one_call(dt, d, deterministic):
+    # preprocess, dK/dV kernel, dQ kernel, dQ conversion launched one by one
+    # (phases 1, 4, 5, 3) give what one attn_bwd call gives
+    B, H, T = 1, 3, 515
+    x = make_random((B, H, T, d), (B, H, T, d), (B, H, T, d), seed=11, dtype=dt, device=DEV)
+    code = pkg.ATTN_BF16 if dt == torch.bfloat16 else pkg.ATTN_F32
+    o, lse = pkg.forward(x["Q"], x["K"], x["V"], causal=True, scale=0.09)
+    ws = torch.empty(max(pkg.attn_bwd_workspace_size(B, H, T, T, d, d, code, deterministic), 256),
+                     dtype=torch.uint8, device=DEV)
+    outs = []
+    for phases in ((0,), (1, 4, 5, 3)):
+        g = [torch.full_like(x["Q"], float("nan")) for _ in range(3)]
+        for ph in phases:
+            pkg.attn_bwd_phase(x["Q"], x["K"], x["V"], o, lse, x["dO"], g[0], g[1], g[2], B, H, T, T, d, d, 0.09,
+                               True, code, deterministic, ws, ws.numel(), ph)
+        torch.cuda.synchronize()
+        outs.append(g)
+    (dq0, dk0, dv0), (dq1, dk1, dv1) = outs
+    assert torch.equal(dk0, dk1) and torch.equal(dv0, dv1)
+    if deterministic:
+        assert torch.equal(dq0, dq1)
+    else:
+        check_grad(dq1, dq0, dt, "dQ")
