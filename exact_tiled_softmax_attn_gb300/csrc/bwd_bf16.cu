@@ -308,10 +308,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       const uint32_t aK = ptx::smem_u32(sK), aV = ptx::smem_u32(sV), aQ = ptx::smem_u32(sQ),
                      adO = ptx::smem_u32(sdO), adS = ptx::smem_u32(sdS);
       auto kmaj = [](uint32_t base, int kk) {  // K-major operand, k-step kk of 16 elements
-        return ptx::sdesc_sw128(base + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
+        return ptx::sdesc_advance(ptx::sdesc_sw128(base, 16, 1024), (kk >> 2) * BOX_BYTES + (kk & 3) * 32);
       };
       auto mnmaj = [](uint32_t base, int kk) {  // MN-major operand, k-step kk of 16 rows
-        return ptx::sdesc_sw128(base + kk * 2048, BOX_BYTES, 1024);
+        return ptx::sdesc_advance(ptx::sdesc_sw128(base, BOX_BYTES, 1024), kk * 2048);
       };
       auto mma_st = [&](uint32_t n) {   // S^T = K Q^T for query tile n
 #pragma unroll
@@ -820,9 +820,11 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     const uint32_t aQ = ptx::smem_u32(sQ), adO = ptx::smem_u32(sdO), aK = ptx::smem_u32(sK),
                    aV = ptx::smem_u32(sV);
     auto kmaj = [](uint32_t base, int kk) {
-      return ptx::sdesc_sw128(base + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024);
+      return ptx::sdesc_advance(ptx::sdesc_sw128(base, 16, 1024), (kk >> 2) * BOX_BYTES + (kk & 3) * 32);
     };
-    auto mnmaj = [](uint32_t base, int kk) { return ptx::sdesc_sw128(base + kk * 2048, BOX_BYTES, 1024); };
+    auto mnmaj = [](uint32_t base, int kk) {
+      return ptx::sdesc_advance(ptx::sdesc_sw128(base, BOX_BYTES, 1024), kk * 2048);
+    };
     auto wait = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, w));
     };

@@ -203,8 +203,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk) {
         const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-        const uint64_t a = ptx::sdesc_sw128(sQa + t * C::TILE + off, 16, 1024);
-        const uint64_t b = ptx::sdesc_sw128(sKVa + sl * C::TILE + off, 16, 1024);
+        const uint64_t a = ptx::sdesc_advance(ptx::sdesc_sw128(sQa + t * C::TILE, 16, 1024), off);
+        const uint64_t b = ptx::sdesc_advance(ptx::sdesc_sw128(sKVa + sl * C::TILE, 16, 1024), off);
         ptx::mma_ss(d, a, b, C::IDESC_S, kk > 0 ? 1u : 0u);
       }
     };
@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t a = tmem + t * 256;  // P_t, bf16 pairs in the first 64 columns of S_t
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk) {
-        const uint64_t b = ptx::sdesc_sw128(sKVa + sl * C::TILE + kk * 2048, BOX_BYTES, 1024);
+        const uint64_t b = ptx::sdesc_advance(ptx::sdesc_sw128(sKVa + sl * C::TILE, BOX_BYTES, 1024), kk * 2048);
         ptx::mma_ts(d, a + kk * 8, b, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
       }
     };
@@ -334,16 +334,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int i = 0; i < 128; ++i)
             if (i >= lim) s[i] = -CUDART_INF_F;
         }
-        // row max as 8 independent chains (a single chain is ~128 dependent ops)
-        float m8[8];
+        // row max as 4 independent chains of three-input maxima
+        float m4[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(s[k], s[k + 8]);
+        for (int k = 0; k < 4; ++k) m4[k] = fmaxf(s[k], s[k + 4]);
 #pragma unroll
-        for (int i = 16; i < 128; i += 8)
+        for (int i = 8; i < 128; i += 8)
 #pragma unroll
-          for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], s[i + k]);
-        float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          for (int k = 0; k < 4; ++k) m4[k] = ptx::fmax3(m4[k], s[i + k], s[i + 4 + k]);
+        float mx = ptx::fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
         mx *= sc2;
         const float m_new = fmaxf(m_used, mx);
         // Lazy rescale: move the reference max only when it grows by > TAU.
@@ -358,20 +357,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           m_used = m_new;
         }
         const float ref = (m_used == -CUDART_INF_F) ? 0.f : m_used;   // the -inf rule
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};   // row sum as 4 independent chains
+        // p = 2^(s * sc2 - ref), two lanes per fma / add instruction; the row
+        // sum runs as 4 independent pairs of partial sums
+        const float2 sc2v = make_float2(sc2, sc2), nrefv = make_float2(-ref, -ref);
+        float2 ls[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ls[k] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t pk[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float p0 = ptx::ex2(fmaf(s[64 * h + 2 * i], sc2, -ref));
-            const float p1 = ptx::ex2(fmaf(s[64 * h + 2 * i + 1], sc2, -ref));
-            ls[i & 3] += p0 + p1;
-            pk[i] = ptx::pack_bf16(p0, p1);
+            const float2 x = ptx::ffma2(make_float2(s[64 * h + 2 * i], s[64 * h + 2 * i + 1]), sc2v, nrefv);
+            const float2 p = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+            ls[i & 3] = ptx::fadd2(ls[i & 3], p);
+            pk[i] = ptx::pack_bf16(p.x, p.y);
           }
           ptx::tmem_st32(tS + 32 * h, pk);
         }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        l += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
         if (__any_sync(0xffffffffu, need)) {
           // O_t *= corr before the next PV product accumulates into it. The
           // previous PV into O_t is complete: it was issued before the S
