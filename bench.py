@@ -311,29 +311,59 @@ def run_ours(args, w):
     value = world * args.steps * (F + Bf) / (total_ms * 1e-3) / 1e12
     assert pkg.attn_device_status(stream) == pkg.ATTN_OK
 
-    # ---- end to end through the public API, host buffers in and out
+    # ---- end to end through the public API, host buffers in and out. Every
+    # step copies its four inputs from pinned host memory and reads all five
+    # results back. Two device buffer sets let step i+1's host-to-device copy
+    # and step i-1's device-to-host copy run on copy streams of their own
+    # while step i's kernels run (inputs > L2, so no flush between steps).
     pinned = {k: v.pin_memory() for k, v in host.items()}
-    out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                for n, t in (("O", o), ("LSE", lse), ("dQ", dq), ("dK", dk), ("dV", dvv))}
+    outs = (("O", o), ("LSE", lse), ("dQ", dq), ("dK", dk), ("dV", dvv))
+    dev_in = [x, {k: torch.empty_like(v) for k, v in x.items()}]
+    dev_out = [dict(outs), {n: torch.empty_like(t) for n, t in outs}]
+    host_out = [{n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs} for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
-    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
-    e2e_steps = max(1, min(args.steps, 20))
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_total = 0.0
-    for i in range(e2e_steps + 1):
-        flush.zero_()
-        ev0.record(stream)
-        for k in x:
-            x[k].copy_(pinned[k], non_blocking=True)
-        fwd()
-        pkg.attn_bwd(x["Q"], x["K"], x["V"], o, lse, x["dO"], dq, dk, dvv, B, H, Tq, Tk, d, dv, sc, w.causal, code,
-                     det, ws, ws.numel(), stream)
-        for n, t in (("O", o), ("LSE", lse), ("dQ", dq), ("dK", dk), ("dV", dvv)):
-            out_host[n].copy_(t, non_blocking=True)
-        ev1.record(stream)
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def e2e_run(n):
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        comp_done = [torch.cuda.Event() for _ in range(2)]
+        out_done = [torch.cuda.Event() for _ in range(2)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        for i in range(n):
+            b = i % 2
+            xi, oi = dev_in[b], dev_out[b]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(comp_done[b])       # step i-2 no longer reads these inputs
+                for k in xi:
+                    xi[k].copy_(pinned[k], non_blocking=True)
+                in_ready[b].record(s_in)
+            stream.wait_event(in_ready[b])
+            if i >= 2:
+                stream.wait_event(out_done[b])          # step i-2's results have left the device
+            pkg.attn_fwd(xi["Q"], xi["K"], xi["V"], oi["O"], oi["LSE"], B, H, Tq, Tk, d, dv, sc, w.causal, code,
+                         stream)
+            pkg.attn_bwd(xi["Q"], xi["K"], xi["V"], oi["O"], oi["LSE"], xi["dO"], oi["dQ"], oi["dK"], oi["dV"],
+                         B, H, Tq, Tk, d, dv, sc, w.causal, code, det, ws, ws.numel(), stream)
+            comp_done[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[b])
+                for n_ in host_out[b]:
+                    host_out[b][n_].copy_(oi[n_], non_blocking=True)
+                out_done[b].record(s_out)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+        t1.record(stream)
         torch.cuda.synchronize()
-        if i > 0:      # the first pass warms the copy engines
-            e2e_total += ev0.elapsed_time(ev1)
+        return t0.elapsed_time(t1)
+
+    e2e_steps = max(2, min(args.steps, 20))
+    e2e_run(2)                                   # warms the copy engines and streams
+    e2e_total = e2e_run(e2e_steps)
     e2e_total = reduce_max(e2e_total)
     e2e_value = world * e2e_steps * (F + Bf) / (e2e_total * 1e-3) / 1e12
     if clocks:
@@ -387,7 +417,9 @@ def run_ours(args, w):
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_note": f"{peaks['source']} dense bf16 burst (cuBLAS 8192^3)"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps},
+                "steps": e2e_steps,
+                "pipeline": "two buffer sets; step i+1 host-to-device and step i-1 device-to-host copies "
+                            "overlap step i's kernels on separate streams"},
         "gpu_launches": args.steps * 4,
         "clocks": clk,
     }

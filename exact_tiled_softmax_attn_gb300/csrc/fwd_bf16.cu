@@ -242,14 +242,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::mma_commit(kv_empty + slot(ik));
       }
       __syncwarp();
+      // V_0 and K_1: each step waits for the next step's tiles while its own
+      // MMAs run, so only the softmax handshakes are left on the critical path
+      if (!(ok = wait(kv_full + slot(ik + 1), par(ik + 1)))) break;
+      if (n1 > 1 && !(ok = wait(kv_full + slot(ik + 2), par(ik + 2)))) break;
       for (int j = 0; j < n1; ++j) {
-        const uint32_t iv = 2 * (kv_it + j) + 1, ikn = iv + 1;   // V_j, K_{j+1}
-        if (!(ok = wait(kv_full + slot(iv), par(iv)))) break;
+        const uint32_t iv = 2 * (kv_it + j) + 1, ikn = iv + 1;   // V_j, K_{j+1}: resident
         if (j < n0) {
           const bool more = j + 1 < n0;
           if (!(ok = wait(p_full + 0, pp[0] & 1u))) break;
           ++pp[0];
-          if (more && !(ok = wait(kv_full + slot(ikn), par(ikn)))) break;
           ptx::tc_fence_after();
           if (ptx::elect_one()) {
             moved |= lane != 0;
@@ -266,7 +268,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool more = j + 1 < n1;
         if (!(ok = wait(p_full + 1, pp[1] & 1u))) break;
         ++pp[1];
-        if (more && !(ok = wait(kv_full + slot(ikn), par(ikn)))) break;
         ptx::tc_fence_after();
         if (ptx::elect_one()) {
           moved |= lane != 0;
@@ -280,6 +281,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         __syncwarp();
+        if (more && !(ok = wait(kv_full + slot(iv + 2), par(iv + 2)))) break;              // V_{j+1}
+        if (j + 2 < n1 && !(ok = wait(kv_full + slot(ikn + 2), par(ikn + 2)))) break;   // K_{j+2}
       }
       if (!ok) break;
       if (ptx::elect_one()) ptx::mma_commit(q_empty);
