@@ -136,7 +136,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct BwdLayout {
   size_t lse2_off, d_off, acc_off, acc_bytes, total;
 };
-// Workspace: LSE2 [B*H, Tq_pad] fp32 | D [B*H, Tq_pad] fp32 | (bf16 with fp32
+// Workspace: NLSE2 [B*H, Tq_pad] fp32 | D [B*H, Tq_pad] fp32 | (bf16 with fp32
 // dQ accumulation) dQacc [B*H*Tq, d] fp32; each part 256-byte aligned.
 BwdLayout bwd_layout(int B, int H, int Tq, int d, attn_dtype_t dt, int deterministic) {
   BwdLayout L{};
@@ -312,7 +312,7 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
   a.dK = dK;
   a.dV = dV;
   a.D = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.d_off);
-  a.LSE2 = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.lse2_off);
+  a.NLSE2 = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.lse2_off);
   a.dQacc = L.acc_bytes ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.acc_off) : nullptr;
   a.deterministic = deterministic;
   a.phase = phase;

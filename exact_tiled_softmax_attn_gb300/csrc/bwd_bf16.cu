@@ -12,7 +12,7 @@
 // dK/dV kernel: one persistent CTA per SM; a work unit is one 128-key tile of
 // one head, and the CTA loops over the query tiles that can see it. K and V
 // stay in shared memory for the whole unit; Q, dO (TMA) and the 128-row slices
-// of LSE2 and D (bulk copies) stream through a two-stage ring. Warp roles (16
+// of NLSE2 and D (bulk copies) stream through a two-stage ring. Warp roles (16
 // warps, 4 warpgroups):
 //   warp 0       producer (lane 0 issues the TMA and bulk copies)
 //   warp 1       MMA issuer (lane 0); allocates and frees TMEM
@@ -80,7 +80,7 @@ struct Order {
 
 struct Params {
   Problem p;
-  const float* LSE2;       // [BH, Tq_pad]: LSE * log2(e), +inf on padding / no-key rows
+  const float* NLSE2;      // [BH, Tq_pad]: -LSE * log2(e), -inf on padding / no-key rows
   const float* D;          // [BH, Tq_pad]
   int Tq_pad;
   float* dQacc;            // atomic path: fp32 [BH, Tq, d], pre-zeroed
@@ -111,7 +111,7 @@ template <int HD, bool ATOMIC_DQ>
 struct CfgKV {
   static constexpr int KB = HD / 64;
   static constexpr int TILE = BT * HD * 2;
-  // Q tiles, dO tiles and the LSE*log2(e) / D slices of a query tile have
+  // Q tiles, dO tiles and the -LSE*log2(e) / D slices of a query tile have
   // rings of their own. A Q tile stays resident from its S^T product to its
   // dK product at the end of the step, a dO tile from its dP^T product to its
   // dV product in the middle of the next one, the slices until the P/dS
@@ -128,7 +128,7 @@ struct CfgKV {
   // 64-column half of the fp32 dQ tile (two 128 x 32 boxes) for the TMA reduce
   static constexpr int OFF_DS = OFF_DO + NO * TILE;
   static constexpr int DS_BYTES = ATOMIC_DQ ? BT * BT * 2 : 0;
-  static constexpr int OFF_LSE = OFF_DS + DS_BYTES;   // [NL][128] fp32 (LSE * log2 e, +inf = no key)
+  static constexpr int OFF_LSE = OFF_DS + DS_BYTES;   // [NL][128] fp32 (-LSE * log2 e, -inf = no key)
   static constexpr int OFF_D = OFF_LSE + NL * BT * 4; // [NL][128] fp32
   static constexpr int OFF_BAR = OFF_D + NL * BT * 4;
   // kv_full, kv_empty, q_full[NQ], q_empty[NQ], o_full[NO], o_empty[NO], l_full[NL], l_empty[NL],
@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           const int ls = lslot(q_it);
           if (!(ok = ptx::mbar_wait(l_empty + ls, lpar(q_it) ^ 1u, w))) break;
           ptx::mbar_arrive_expect_tx(l_full + ls, 2 * BT * 4);
-          ptx::bulk_load(sLSE + ls * BT, P.LSE2 + row0, BT * 4, l_full + ls);
+          ptx::bulk_load(sLSE + ls * BT, P.NLSE2 + row0, BT * 4, l_full + ls);
           ptx::bulk_load(sD + ls * BT, P.D + row0, BT * 4, l_full + ls);
           l_issued = q_it + 1;
           if (!(ok = ptx::mbar_wait(o_empty + os, opar(q_it) ^ 1u, w))) break;
@@ -355,14 +355,18 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
             ptx::mma_commit(dp_full);
           }
           __syncwarp();
+          // Q and dO of the next query tile: each step waits for the tiles of
+          // the step after it while its own MMAs run, so only the P/dS
+          // handshakes are left on the critical path
+          if (nq > 1 && !(ok = wait(q_full + qslot(q_it + 1), qpar(q_it + 1)))) break;
+          if (nq > 1 && !(ok = wait(o_full + oslot(q_it + 1), opar(q_it + 1)))) break;
         }
         for (int ii = 0; ii < nq; ++ii) {
           const uint32_t it = q_it + ii;
-          const bool more = ii + 1 < nq;
+          const bool more = ii + 1 < nq;   // Q and dO of tile it + 1 are resident
           // dV += P^T dO, then the next S^T (it overwrites P^T only after the
           // product above has read it)
           if (!(ok = wait(p_full, pp & 1u))) break;
-          if (more && !(ok = wait(q_full + qslot(it + 1), qpar(it + 1)))) break;
           ptx::tc_fence_after();
           if (ptx::elect_one()) {
             moved |= lane != 0;
@@ -401,7 +405,6 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
             if (ATOMIC_DQ) {
               if (!(ok = wait(dq_free, (dqf - 1) & 1u))) break;
             }
-            if (!(ok = wait(o_full + oslot(it + 1), opar(it + 1)))) break;
             ptx::tc_fence_after();
             if (ptx::elect_one()) {
               moved |= lane != 0;
@@ -409,6 +412,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
               ptx::mma_commit(dp_full);
             }
             __syncwarp();
+          }
+          if (ii + 2 < nq) {
+            if (!(ok = wait(q_full + qslot(it + 2), qpar(it + 2)))) break;
+            if (!(ok = wait(o_full + oslot(it + 2), opar(it + 2)))) break;
           }
         }
         if (!ok) break;
@@ -439,6 +446,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     const uint32_t tST = tmem + lane_off + T_ST + 64 * h, tDP = tmem + lane_off + T_DP + 64 * h;
     ptx::WaitCtx w{abort_flag, P.status, 3u};
     const float sc2 = P.sc2;
+    const float2 sc2v = make_float2(sc2, sc2), neg1 = make_float2(-1.f, -1.f);
     uint32_t q_it = 0, sp = 0;
     bool ok = true;
     int bh, kb;
@@ -451,13 +459,13 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       for (int ii = 0; ii < nq; ++ii, ++q_it, ++sp) {
         const int ls = lslot(q_it);
         const int qt = q0 + ii;
-        const float* lse2 = sLSE + ls * BT + 64 * h;
+        const float* nlse2 = sLSE + ls * BT + 64 * h;
         const float* dd = sD + ls * BT + 64 * h;
         // the staged LSE / D slices of this tile are visible once l_full completed
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(l_full + ls, lpar(q_it), w)))) break;
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(s_full, sp & 1u, w)))) break;
         ptx::tc_fence_after();
-        // pass 1: P^T_j,q = 2^(s * scale * log2e - LSE2_q), masked; packed bf16
+        // pass 1: P^T_j,q = 2^(s * scale * log2e - LSE_q * log2e), masked; packed bf16
         // over the first half of this group's S^T columns. The packed values
         // stay in registers for pass 2: once p_full is signalled the MMA warp
         // may overwrite S^T with the next tile's scores.
@@ -476,11 +484,13 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 16; i += 2) {
               const int qa = c * 32 + 2 * i;
-              const float4 l4 = ptx::lds128(lse2 + qa);
-              float p0 = ptx::ex2(fmaf(__uint_as_float(rs[c][2 * i]), sc2, -l4.x));
-              float p1 = ptx::ex2(fmaf(__uint_as_float(rs[c][2 * i + 1]), sc2, -l4.y));
-              float p2 = ptx::ex2(fmaf(__uint_as_float(rs[c][2 * i + 2]), sc2, -l4.z));
-              float p3 = ptx::ex2(fmaf(__uint_as_float(rs[c][2 * i + 3]), sc2, -l4.w));
+              const float4 l4 = ptx::lds128(nlse2 + qa);
+              const float2 x01 = ptx::ffma2(make_float2(__uint_as_float(rs[c][2 * i]), __uint_as_float(rs[c][2 * i + 1])),
+                                            sc2v, make_float2(l4.x, l4.y));
+              const float2 x23 = ptx::ffma2(make_float2(__uint_as_float(rs[c][2 * i + 2]),
+                                                        __uint_as_float(rs[c][2 * i + 3])),
+                                            sc2v, make_float2(l4.z, l4.w));
+              float p0 = ptx::ex2(x01.x), p1 = ptx::ex2(x01.y), p2 = ptx::ex2(x23.x), p3 = ptx::ex2(x23.y);
               if (lim > 0) {
                 if (qa < lim) p0 = 0.f;
                 if (qa + 1 < lim) p1 = 0.f;
@@ -518,10 +528,15 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
               const float4 d4 = ptx::lds128(dd + qa);
               const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pkeep[c][i]));
               const float2 pg = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pkeep[c][i + 1]));
-              pk[i] = ptx::pack_bf16(pf.x * (__uint_as_float(rd[c][2 * i]) - d4.x),
-                                     pf.y * (__uint_as_float(rd[c][2 * i + 1]) - d4.y));
-              pk[i + 1] = ptx::pack_bf16(pg.x * (__uint_as_float(rd[c][2 * i + 2]) - d4.z),
-                                         pg.y * (__uint_as_float(rd[c][2 * i + 3]) - d4.w));
+              // (dP - D) as -D * 1 + dP, two lanes per instruction
+              const float2 e01 = ptx::ffma2(make_float2(d4.x, d4.y), neg1,
+                                            make_float2(__uint_as_float(rd[c][2 * i]), __uint_as_float(rd[c][2 * i + 1])));
+              const float2 e23 = ptx::ffma2(make_float2(d4.z, d4.w), neg1,
+                                            make_float2(__uint_as_float(rd[c][2 * i + 2]),
+                                                        __uint_as_float(rd[c][2 * i + 3])));
+              const float2 s01 = ptx::fmul2(pf, e01), s23 = ptx::fmul2(pg, e23);
+              pk[i] = ptx::pack_bf16(s01.x, s01.y);
+              pk[i + 1] = ptx::pack_bf16(s23.x, s23.y);
             }
             ptx::tmem_st16(tDP + c * 16, pk);
             if (ATOMIC_DQ) {
@@ -864,14 +879,17 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           mma_dp(t, sp);
         }
         __syncwarp();
+        // K and V of the next key tile: each step waits for the tiles of the
+        // step after it while its own MMAs run
+        if (nk > 1 && !(ok = wait(k_full + kslot(t + 1), kpar(t + 1)))) break;
+        if (nk > 1 && !(ok = wait(v_full + vslot(t + 1), vpar(t + 1)))) break;
       }
       for (int j = 0; j < nk; ++j, ++sp) {
-        const uint32_t t = k_it + j, tn = t + 1;
+        const uint32_t t = k_it + j, tn = t + 1;   // K and V of tile tn are resident
         if (j + 1 < nk) {
           // S of the next key tile once the row threads have read this one,
           // then its dP into the other buffer (whose dS the previous dQ
           // product has consumed: MMAs run in issue order)
-          if (!(ok = wait(k_full + kslot(tn), kpar(tn)))) break;
           if (!(ok = wait(s_free, sp & 1u))) break;
           ptx::tc_fence_after();
           if (ptx::elect_one()) {
@@ -880,8 +898,6 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
             ptx::mma_commit(s_full);
           }
           __syncwarp();
-          if (!(ok = wait(v_full + vslot(tn), vpar(tn)))) break;
-          ptx::tc_fence_after();
           if (ptx::elect_one()) {
             moved |= lane != 0;
             mma_dp(tn, sp + 1);
@@ -900,6 +916,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           ptx::mma_commit(k_empty + kslot(t));
         }
         __syncwarp();
+        if (j + 2 < nk) {
+          if (!(ok = wait(k_full + kslot(t + 2), kpar(t + 2)))) break;
+          if (!(ok = wait(v_full + vslot(t + 2), vpar(t + 2)))) break;
+        }
       }
       if (!ok) break;
       if (ptx::elect_one()) {
@@ -931,8 +951,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       const int nk = nk_of(qt);
       const int q = qt * BT + r;
       const bool q_ok = q < Tq;
-      // padding rows hold LSE2 = +inf and D = 0, so their P and dS are 0
-      const float lse2 = P.LSE2[static_cast<size_t>(bh) * P.Tq_pad + q];
+      // padding rows hold NLSE2 = -inf and D = 0, so their P and dS are 0
+      const float nlse2 = P.NLSE2[static_cast<size_t>(bh) * P.Tq_pad + q];
       const float dd = P.D[static_cast<size_t>(bh) * P.Tq_pad + q];
       for (int j = 0; j < nk; ++j, ++sp) {
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(s_full, sp & 1u, w)))) break;
@@ -947,7 +967,12 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int i = 0; i < 32; ++i) p[c * 32 + i] = ptx::ex2(fmaf(__uint_as_float(v[c][i]), sc2, -lse2));
+            for (int i = 0; i < 32; i += 2) {
+              const float2 x = ptx::ffma2(make_float2(__uint_as_float(v[c][i]), __uint_as_float(v[c][i + 1])),
+                                          make_float2(sc2, sc2), make_float2(nlse2, nlse2));
+              p[c * 32 + i] = ptx::ex2(x.x);
+              p[c * 32 + i + 1] = ptx::ex2(x.y);
+            }
         }
         ptx::tc_fence_before();
         ptx::mbar_arrive(s_free);
@@ -970,9 +995,12 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = ptx::pack_bf16(p[c * 32 + 2 * i] * (__uint_as_float(v[c][2 * i]) - dd),
-                                   p[c * 32 + 2 * i + 1] * (__uint_as_float(v[c][2 * i + 1]) - dd));
+          for (int i = 0; i < 16; ++i) {
+            const float2 e = ptx::fadd2(make_float2(__uint_as_float(v[c][2 * i]), __uint_as_float(v[c][2 * i + 1])),
+                                        make_float2(-dd, -dd));
+            const float2 r = ptx::fmul2(make_float2(p[c * 32 + 2 * i], p[c * 32 + 2 * i + 1]), e);
+            pk[i] = ptx::pack_bf16(r.x, r.y);
+          }
           ptx::tmem_st16(tDP + c * 16, pk);
         }
         ptx::tmem_st_wait();
@@ -1031,13 +1059,13 @@ cudaError_t launch(const LaunchBwd& a) {
   const bool main_q = a.phase == 0 || a.phase == 2 || a.phase == 5;
   cudaError_t e = cudaSuccess;
   if (pre) {
-    e = launch_bwd_preprocess(p, a.O, a.dO, a.LSE, 2, a.D, a.LSE2, atomic ? a.dQacc : nullptr, p.d, a.num_sms,
+    e = launch_bwd_preprocess(p, a.O, a.dO, a.LSE, 2, a.D, a.NLSE2, atomic ? a.dQacc : nullptr, p.d, a.num_sms,
                               a.stream);
     if (e != cudaSuccess) return e;
   }
   Params P{};
   P.p = p;
-  P.LSE2 = a.LSE2;
+  P.NLSE2 = a.NLSE2;
   P.D = a.D;
   P.Tq_pad = padded_rows(p.Tq);
   P.dQacc = a.dQacc;

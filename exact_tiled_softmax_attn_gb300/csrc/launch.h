@@ -43,7 +43,7 @@ struct LaunchBwd {
   void* dK;
   void* dV;
   float* D;                 // [B*H, Tq_pad] workspace, Tq_pad = Tq rounded up to 128
-  float* LSE2;              // [B*H, Tq_pad] workspace: LSE * log2(e), +inf for padding / no-key rows
+  float* NLSE2;             // [B*H, Tq_pad] workspace: -LSE * log2(e), -inf for padding / no-key rows
   float* dQacc;             // [B,H,Tq,d] fp32 workspace (bf16 atomic path), else null
   int deterministic;
   int phase;                // 0 all; 1 preprocess; 2 main kernels (4 then 5); 3 dQ conversion;
@@ -67,11 +67,11 @@ cudaError_t launch_fill_empty_fwd(const Problem& p, void* O, float* LSE, int ele
 cudaError_t launch_zero(void* ptr, size_t bytes, cudaStream_t s);
 // Rows of every head padded to a multiple of 128 (the backward's tile height).
 __host__ __device__ inline int padded_rows(int T) { return (T + 127) / 128 * 128; }
-// D = rowsum(dO o O) and LSE2 = LSE * log2(e) (+inf where LSE = -inf or the
+// D = rowsum(dO o O) and NLSE2 = -LSE * log2(e) (-inf where LSE = -inf or the
 // row is padding) in [B*H, Tq_pad] layout; optionally zeroes `zero_rows`
 // ([B*H*Tq] rows of `zero_cols` floats).
 cudaError_t launch_bwd_preprocess(const Problem& p, const void* O, const void* dO, const float* LSE, int elem_bytes,
-                                  float* D, float* LSE2, float* zero_rows, int zero_cols, int num_sms,
+                                  float* D, float* NLSE2, float* zero_rows, int zero_cols, int num_sms,
                                   cudaStream_t s);
 
 }  // namespace attn

@@ -405,7 +405,7 @@ cudaError_t launch_bwd_f32(const LaunchBwd& a) {
   cudaError_t e = cudaSuccess;
   if (a.phase == 0 || a.phase == 1) {
     // D = rowsum(dO o O); dQ zeroed when it is accumulated with atomics.
-    e = launch_bwd_preprocess(p, a.O, a.dO, a.LSE, 4, a.D, a.LSE2,
+    e = launch_bwd_preprocess(p, a.O, a.dO, a.LSE, 4, a.D, a.NLSE2,
                               a.deterministic ? nullptr : static_cast<float*>(a.dQ), p.d, a.num_sms, a.stream);
     if (e != cudaSuccess) return e;
   }

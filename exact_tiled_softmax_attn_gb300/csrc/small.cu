@@ -39,14 +39,14 @@ __device__ __forceinline__ float dot16(const uint4& a, const uint4& b, const flo
 // ROW_SUM(dL/dO o O); the delta-l term of "The Hidden Recurrence in Softmax
 // Attention", section "Flash Attention Backward Pass"), written with the
 // stored log-sum-exp in log2 units into [B*H, Tq_pad] arrays whose padding
-// rows hold D = 0 and LSE2 = +inf (so exp2(s - LSE2) = 0 there). The backward
+// rows hold D = 0 and NLSE2 = -inf (so exp2(s + NLSE2) = 0 there). The backward
 // fetches a 128-row slice of each with one bulk copy. Each group of LPR lanes
 // reads one row with 16-byte loads; rows are walked grid-stride. Optionally
 // zeroes the matching row of an fp32 accumulator.
 template <typename T>
 __global__ void __launch_bounds__(NT) preprocess_vec(const T* __restrict__ O, const T* __restrict__ dO,
                                                       const float* __restrict__ LSE, float* __restrict__ D,
-                                                      float* __restrict__ LSE2, float* __restrict__ zero_rows,
+                                                      float* __restrict__ NLSE2, float* __restrict__ zero_rows,
                                                       int zero_cols, long long rows_pad, int Tq, int Tq_pad, int dv) {
   const int chunks = dv * static_cast<int>(sizeof(T)) / 16;   // 16-byte chunks per row (<= 32)
   const int lpr = chunks;                                      // lanes per row
@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(NT) preprocess_vec(const T* __restrict__ O, co
     if (inside && c == 0) {
       D[rp] = s;
       const float lse = real ? LSE[r] : -CUDART_INF_F;
-      LSE2[rp] = (lse == -CUDART_INF_F) ? CUDART_INF_F : lse * 1.4426950408889634f;
+      NLSE2[rp] = (lse == -CUDART_INF_F) ? -CUDART_INF_F : -lse * 1.4426950408889634f;
     }
     if (real && zero_rows) {
       float4* z = reinterpret_cast<float4*>(zero_rows + r * zero_cols);
@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(NT) preprocess_vec(const T* __restrict__ O, co
 // Generic fp32 version (any dv): one warp per padded row.
 __global__ void __launch_bounds__(NT) preprocess_f32(const float* __restrict__ O, const float* __restrict__ dO,
                                                       const float* __restrict__ LSE, float* __restrict__ D,
-                                                      float* __restrict__ LSE2, float* __restrict__ zero_rows,
+                                                      float* __restrict__ NLSE2, float* __restrict__ zero_rows,
                                                       int zero_cols, long long rows_pad, int Tq, int Tq_pad, int dv) {
   const int lane = threadIdx.x & 31;
   const long long warp_id = (static_cast<long long>(blockIdx.x) * NT + threadIdx.x) >> 5;
@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(NT) preprocess_f32(const float* __restrict__ O
     if (lane == 0) {
       D[rp] = s;
       const float lse = q < Tq ? LSE[r] : -CUDART_INF_F;
-      LSE2[rp] = (lse == -CUDART_INF_F) ? CUDART_INF_F : lse * 1.4426950408889634f;
+      NLSE2[rp] = (lse == -CUDART_INF_F) ? -CUDART_INF_F : -lse * 1.4426950408889634f;
     }
     if (zero_rows && q < Tq)
       for (int c = lane; c < zero_cols; c += 32) zero_rows[r * zero_cols + c] = 0.f;
@@ -122,7 +122,7 @@ __global__ void zero_kernel(uint8_t* p, size_t bytes) {
 }  // namespace small
 
 cudaError_t launch_bwd_preprocess(const Problem& p, const void* O, const void* dO, const float* LSE, int elem_bytes,
-                                  float* D, float* LSE2, float* zero_rows, int zero_cols, int num_sms,
+                                  float* D, float* NLSE2, float* zero_rows, int zero_cols, int num_sms,
                                   cudaStream_t s) {
   const int Tq_pad = padded_rows(p.Tq);
   const long long rows_pad = static_cast<long long>(p.B) * p.H * Tq_pad;
@@ -134,15 +134,15 @@ cudaError_t launch_bwd_preprocess(const Problem& p, const void* O, const void* d
                    (zero_rows == nullptr || (zero_cols % 4 == 0 && reinterpret_cast<uintptr_t>(zero_rows) % 16 == 0));
   if (elem_bytes == 2) {
     small::preprocess_vec<__nv_bfloat16><<<grid, small::NT, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, D, LSE2, zero_rows,
+        static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, D, NLSE2, zero_rows,
         zero_cols, rows_pad, p.Tq, Tq_pad, p.dv);
   } else if (vec) {
     small::preprocess_vec<float><<<grid, small::NT, 0, s>>>(static_cast<const float*>(O),
-                                                             static_cast<const float*>(dO), LSE, D, LSE2,
+                                                             static_cast<const float*>(dO), LSE, D, NLSE2,
                                                              zero_rows, zero_cols, rows_pad, p.Tq, Tq_pad, p.dv);
   } else {
     small::preprocess_f32<<<grid, small::NT, 0, s>>>(static_cast<const float*>(O), static_cast<const float*>(dO),
-                                                      LSE, D, LSE2, zero_rows, zero_cols, rows_pad, p.Tq, Tq_pad,
+                                                      LSE, D, NLSE2, zero_rows, zero_cols, rows_pad, p.Tq, Tq_pad,
                                                       p.dv);
   }
   return cudaGetLastError();

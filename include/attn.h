@@ -92,7 +92,7 @@ ATTN_API attn_status_t attn_fwd_f32_blocked(const float* Q, const float* K, cons
 
 /*
  * Bytes of device workspace attn_bwd needs for this problem (0 is possible).
- * Holds LSE * log2(e) and D = rowsum(dO o O), each [B*H, Tq_pad] fp32 with
+ * Holds -LSE * log2(e) and D = rowsum(dO o O), each [B*H, Tq_pad] fp32 with
  * Tq_pad = Tq rounded up to a multiple of 128, and, for bf16 with
  * deterministic == 0, the fp32 dQ accumulator [B,H,Tq,d]; each part starts on
  * a 256-byte boundary. Returns 0 for invalid arguments as well.

@@ -93,7 +93,7 @@ def test_blocked_forward_validates_block(lib):
 
 
 def test_workspace_size(lib):
-    # LSE*log2(e) and D, each [B*H, Tq rounded up to 128] fp32 and 256-byte
+    # -LSE*log2(e) and D, each [B*H, Tq rounded up to 128] fp32 and 256-byte
     # aligned, then (bf16 with fp32 dQ accumulation) the [B*H*Tq, d] accumulator
     part = (2 * 3 * 128 * 4 + 255) // 256 * 256
     assert B.attn_bwd_workspace_size(2, 3, 100, 50, 64, 64, B.ATTN_F32, 0) == 2 * part
