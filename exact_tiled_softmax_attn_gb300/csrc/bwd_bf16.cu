@@ -359,11 +359,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           // the step after it while its own MMAs run, so only the P/dS
           // handshakes are left on the critical path
           if (nq > 1 && !(ok = wait(q_full + qslot(q_it + 1), qpar(q_it + 1)))) break;
-          if (nq > 1 && !(ok = wait(o_full + oslot(q_it + 1), opar(q_it + 1)))) break;
         }
         for (int ii = 0; ii < nq; ++ii) {
           const uint32_t it = q_it + ii;
-          const bool more = ii + 1 < nq;   // Q and dO of tile it + 1 are resident
+          const bool more = ii + 1 < nq;   // Q of tile it + 1 is resident
           // dV += P^T dO, then the next S^T (it overwrites P^T only after the
           // product above has read it)
           if (!(ok = wait(p_full, pp & 1u))) break;
@@ -405,6 +404,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
             if (ATOMIC_DQ) {
               if (!(ok = wait(dq_free, (dqf - 1) & 1u))) break;
             }
+            if (!(ok = wait(o_full + oslot(it + 1), opar(it + 1)))) break;
             ptx::tc_fence_after();
             if (ptx::elect_one()) {
               moved |= lane != 0;
@@ -413,10 +413,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
             }
             __syncwarp();
           }
-          if (ii + 2 < nq) {
-            if (!(ok = wait(q_full + qslot(it + 2), qpar(it + 2)))) break;
-            if (!(ok = wait(o_full + oslot(it + 2), opar(it + 2)))) break;
-          }
+          if (ii + 2 < nq && !(ok = wait(q_full + qslot(it + 2), qpar(it + 2)))) break;
         }
         if (!ok) break;
         if (ptx::elect_one()) {
@@ -879,13 +876,12 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           mma_dp(t, sp);
         }
         __syncwarp();
-        // K and V of the next key tile: each step waits for the tiles of the
-        // step after it while its own MMAs run
+        // K of the next key tile: each step waits for the K tile of the step
+        // after it while its own MMAs run
         if (nk > 1 && !(ok = wait(k_full + kslot(t + 1), kpar(t + 1)))) break;
-        if (nk > 1 && !(ok = wait(v_full + vslot(t + 1), vpar(t + 1)))) break;
       }
       for (int j = 0; j < nk; ++j, ++sp) {
-        const uint32_t t = k_it + j, tn = t + 1;   // K and V of tile tn are resident
+        const uint32_t t = k_it + j, tn = t + 1;   // K of tile tn is resident
         if (j + 1 < nk) {
           // S of the next key tile once the row threads have read this one,
           // then its dP into the other buffer (whose dS the previous dQ
@@ -898,6 +894,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
             ptx::mma_commit(s_full);
           }
           __syncwarp();
+          if (!(ok = wait(v_full + vslot(tn), vpar(tn)))) break;
+          ptx::tc_fence_after();
           if (ptx::elect_one()) {
             moved |= lane != 0;
             mma_dp(tn, sp + 1);
@@ -916,10 +914,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           ptx::mma_commit(k_empty + kslot(t));
         }
         __syncwarp();
-        if (j + 2 < nk) {
-          if (!(ok = wait(k_full + kslot(t + 2), kpar(t + 2)))) break;
-          if (!(ok = wait(v_full + vslot(t + 2), vpar(t + 2)))) break;
-        }
+        if (j + 2 < nk && !(ok = wait(k_full + kslot(t + 2), kpar(t + 2)))) break;
       }
       if (!ok) break;
       if (ptx::elect_one()) {
@@ -964,6 +959,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, v[c]);   // all four in flight
 #pragma unroll
           for (int c = 0; c < 4; ++c) ptx::tmem_ld_wait(v[c]);
+          // S is in registers: the next S product may overwrite it while the
+          // exponentials below run
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(s_free);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -974,8 +973,6 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
               p[c * 32 + i + 1] = ptx::ex2(x.y);
             }
         }
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(s_free);
         const int kv0 = j * BT;
         if (kv0 + BT > Tk || (P.p.causal && kv0 + BT - 1 > qt * BT)) {
           const int lim = min(Tk - kv0, P.p.causal ? q - kv0 + 1 : BT);   // keys [0, lim) allowed
