@@ -23,7 +23,7 @@ __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA",
     "ATTN_ERR_TIMEOUT", "ATTN_ERR_WORKSPACE", "ATTN_F32", "ATTN_BF16",
     "attn_fwd", "attn_fwd_f32_blocked", "attn_bwd", "attn_bwd_phase", "attn_bwd_workspace_size",
-    "attn_bwd_noalloc", "ATTN_NOALLOC_SCRATCH_BYTES", "attn_device_status",
+    "attn_bwd_noalloc", "ATTN_NOALLOC_SCRATCH_BYTES", "attn_online_softmax_step", "attn_device_status",
     "attn_selftest_wait_timeout", "attn_strerror", "attn_last_cuda_error", "attn_version",
     "forward", "backward",
 ]
@@ -45,6 +45,7 @@ _SIGNATURES = {
     "attn_bwd_phase": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _SZ,
                             _I, _P]),
     "attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
+    "attn_online_softmax_step": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
     "attn_device_status": (_I, [_P]),
     "attn_selftest_wait_timeout": (_I, [_I, _P]),
     "attn_strerror": (ctypes.c_char_p, [_I]),
@@ -139,6 +140,14 @@ def attn_fwd_f32_blocked(Q, K, V, O, LSE, B, H, Tq, Tk, d, dv, scale, causal, bl
                                              float(scale), int(causal), int(block_n), _stream(stream))
     if check:
         _check(st, "attn_fwd_f32_blocked")
+    return st
+
+
+def attn_online_softmax_step(m, l, acc, scores, v_block, n, bs, dv, stream=None, check=True) -> int:
+    st = load_library().attn_online_softmax_step(_ptr(m), _ptr(l), _ptr(acc), _ptr(scores), _ptr(v_block), int(n),
+                                                 int(bs), int(dv), _stream(stream))
+    if check:
+        _check(st, "attn_online_softmax_step")
     return st
 
 

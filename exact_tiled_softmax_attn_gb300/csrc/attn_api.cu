@@ -378,6 +378,32 @@ attn_status_t attn_device_status(void* stream) {
   return ATTN_OK;
 }
 
+attn_status_t attn_online_softmax_step(float* m, float* l, float* acc, const float* scores, const float* v_block,
+                                       int n, int bs, int dv, void* stream) {
+  if (n < 0 || bs < 0 || dv < 1 || dv > 512) return ATTN_ERR_INVALID_ARG;
+  const size_t nn = static_cast<size_t>(n);
+  const size_t bm = nn * 4, ba = nn * dv * 4, bsc = nn * bs * 4, bv = static_cast<size_t>(bs) * dv * 4;
+  attn_status_t s;
+  float* outs[3] = {m, l, acc};
+  const size_t out_bytes[3] = {bm, bm, ba};
+  for (int i = 0; i < 3; ++i)
+    if ((s = check_ptr(outs[i], out_bytes[i], 4)) != ATTN_OK) return s;
+  if ((s = check_ptr(scores, bsc, 4)) != ATTN_OK) return s;
+  if ((s = check_ptr(v_block, bv, 4)) != ATTN_OK) return s;
+  const Range ro[3] = {range(m, bm), range(l, bm), range(acc, ba)};
+  for (int i = 0; i < 3; ++i) {
+    if (overlap(ro[i], range(scores, bsc)) || overlap(ro[i], range(v_block, bv))) return ATTN_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 3; ++j)
+      if (overlap(ro[i], ro[j])) return ATTN_ERR_INVALID_ARG;
+  }
+  if (n == 0) return ATTN_OK;
+  DeviceInfo* di;
+  if ((s = device_info(&di)) != ATTN_OK) return s;
+  const cudaError_t e =
+      launch_online_softmax_step(m, l, acc, scores, v_block, n, bs, dv, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
 attn_status_t attn_selftest_wait_timeout(int limit_ms, void* stream) {
   if (limit_ms < 1 || limit_ms > 5000) return ATTN_ERR_INVALID_ARG;
   DeviceInfo* di;

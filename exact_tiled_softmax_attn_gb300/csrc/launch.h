@@ -65,6 +65,9 @@ size_t fwd_bf16_smem_bytes(int d);
 // shared small kernels
 cudaError_t launch_fill_empty_fwd(const Problem& p, void* O, float* LSE, int elem_bytes, cudaStream_t s);
 cudaError_t launch_zero(void* ptr, size_t bytes, cudaStream_t s);
+// One online-softmax step over n rows (fp32 state, fp64 arithmetic), dv <= 512.
+cudaError_t launch_online_softmax_step(float* m, float* l, float* acc, const float* scores, const float* v, int n,
+                                       int bs, int dv, cudaStream_t s);
 // Rows of every head padded to a multiple of 128 (the backward's tile height).
 __host__ __device__ inline int padded_rows(int T) { return (T + 127) / 128 * 128; }
 // D = rowsum(dO o O) and NLSE2 = -LSE * log2(e) (-inf where LSE = -inf or the

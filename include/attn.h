@@ -175,6 +175,28 @@ ATTN_API attn_status_t attn_bwd_noalloc(const void* Q, const void* K, const void
                                         attn_dtype_t dtype, int deterministic, void* stream);
 
 /*
+ * One step of the online softmax, on the device: for each of the n query
+ * rows, fold one block of bs keys into the running state ("Tiled attention
+ * with an online softmax", section "Task": the online_softmax_step of the
+ * page; "The Hidden Recurrence in Softmax Attention", section "Chunk-wise
+ * Mode with Online Softmax Re-scale"):
+ *   m' = max(m, max_j s_ij), with 0 used for m' inside the exponentials when
+ *        m' = -inf (a row with no allowed key so far)
+ *   l' = exp(m - m') l + sum_j exp(s_ij - m')
+ *   acc' = exp(m - m') acc + sum_j exp(s_ij - m') v_j
+ * m, l [n] and acc [n, dv] (row-major) are fp32 device buffers updated in
+ * place; a fresh row is m = -inf, l = 0, acc = 0, and acc / l is its
+ * attention output once every block has been folded in. scores [n, bs] fp32
+ * (-inf marks a blocked key) and v_block [bs, dv] fp32 are read only. The
+ * arithmetic runs in fp64. n, bs >= 0 and 1 <= dv <= 512; buffers 4-byte
+ * aligned, the three outputs disjoint from each other and from the inputs,
+ * else ATTN_ERR_INVALID_ARG / ATTN_ERR_MISALIGNED before any launch.
+ * Asynchronous on `stream`.
+ */
+ATTN_API attn_status_t attn_online_softmax_step(float* m, float* l, float* acc, const float* scores,
+                                                const float* v_block, int n, int bs, int dv, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word that
  * the kernels set when a bounded wait gives up (ATTN_ERR_TIMEOUT) or a launch
  * precondition fails on the device (ATTN_ERR_CUDA). ATTN_OK otherwise.

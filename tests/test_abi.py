@@ -136,6 +136,23 @@ def test_backward_phase_range(lib):
         assert B.attn_bwd_phase(**args, phase=ph, stream=0, check=False) == B.ATTN_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("kw,status", [
+    (dict(n=-1), B.ATTN_ERR_INVALID_ARG),
+    (dict(bs=-2), B.ATTN_ERR_INVALID_ARG),
+    (dict(dv=0), B.ATTN_ERR_INVALID_ARG),
+    (dict(dv=513), B.ATTN_ERR_INVALID_ARG),
+    (dict(m=None), B.ATTN_ERR_INVALID_ARG),
+    (dict(scores=0x400002), B.ATTN_ERR_MISALIGNED),
+    (dict(l=0x100000), B.ATTN_ERR_INVALID_ARG),            # l overlaps m
+    (dict(acc=0x400000), B.ATTN_ERR_INVALID_ARG),          # acc overlaps scores
+    (dict(n=0, m=None, l=None, acc=None, scores=None), B.ATTN_OK),
+])
+def test_step_host_validation(lib, kw, status):
+    a = dict(m=0x100000, l=0x200000, acc=0x300000, scores=0x400000, v_block=0x500000, n=8, bs=16, dv=32)
+    a.update(kw)
+    assert B.attn_online_softmax_step(**a, stream=0, check=False) == status
+
+
 def test_error_text_carries_status(lib):
     with pytest.raises(B.AttnError) as e:
         B.attn_fwd(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 1, 1, 8, 8, 96, 96, 0.1, 0, B.ATTN_BF16,
