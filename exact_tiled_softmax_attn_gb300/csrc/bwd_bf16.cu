@@ -704,12 +704,14 @@ struct CfgQ {
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16(BT, BT, false, false);
   static constexpr uint32_t IDESC_DQ = ptx::idesc_bf16(BT, HD, false, true);
 };
-constexpr int DQ_THREADS = 192;
+constexpr int DQ_THREADS = 320;
 
 // One persistent CTA per SM; a unit is one 128-row query tile of one head.
 // For each key tile (fixed ascending order): S = Q K^T, dP = dO V^T (both in
-// TMEM, one thread per query row), dS = P o (dP - D) written bf16 over dP,
-// and dQ += dS K accumulates in TMEM. Warps: 0 producer, 1 MMA, 2-5 rows.
+// TMEM), dS = P o (dP - D) written bf16 over dP, and dQ += dS K accumulates
+// in TMEM. Warps: 0 producer, 1 MMA, 2-5 and 6-9 two row groups; group g
+// works on key columns [64g, 64g + 64) of every query row (one thread per
+// row each) and packs its dS at columns [64g, 64g + 32) of the dP buffer.
 // TMEM: S [0, 128), dQ [128, 256), dP/dS in two buffers [256, 384) and
 // [384, 512) alternating by step, so the MMA warp computes dP of step j + 1
 // while the row threads still turn dP of step j into dS.
@@ -757,10 +759,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       ptx::mbar_init(v_empty + s, 1);
     }
     ptx::mbar_init(s_full, 1);
-    ptx::mbar_init(s_free, 128);
+    ptx::mbar_init(s_free, 256);
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(dp_full + b, 1);
-      ptx::mbar_init(ds_full + b, 128);
+      ptx::mbar_init(ds_full + b, 256);
     }
     ptx::mbar_init(dq_full, 1);
     ptx::mbar_init(drain, 1);
@@ -909,7 +911,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           moved |= lane != 0;
 #pragma unroll
           for (int kk = 0; kk < BT / 16; ++kk)
-            ptx::mma_ts(tmem + T_DQ, tmem + t_dp(sp) + kk * 8, mnmaj(aK + kslot(t) * C::TILE, kk), C::IDESC_DQ,
+            ptx::mma_ts(tmem + T_DQ, tmem + t_dp(sp) + packed_col(kk), mnmaj(aK + kslot(t) * C::TILE, kk),
+                        C::IDESC_DQ,
                         (j > 0 || kk > 0) ? 1u : 0u);
           ptx::mma_commit(k_empty + kslot(t));
         }
@@ -933,11 +936,12 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     }
     if (__any_sync(0xffffffffu, moved) && lane == 0) atomicOr(P.status, ATTN_DEV_ISSUER);
   } else if (warp >= 2) {
+    const int g = (warp - 2) >> 2;          // row group: key columns [64g, 64g + 64)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_off + T_S, tDQ = tmem + lane_off + T_DQ;
-    ptx::WaitCtx w{abort_flag, P.status, 7u};
+    const uint32_t tS = tmem + lane_off + T_S + 64 * g, tDQ = tmem + lane_off + T_DQ + (HD / 2) * g;
+    ptx::WaitCtx w{abort_flag, P.status, 7u + g};
     const float sc2 = P.sc2, scale = P.p.scale;
     uint32_t u_it = 0, sp = 0;
     bool ok = true;
@@ -952,19 +956,19 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       for (int j = 0; j < nk; ++j, ++sp) {
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(s_full, sp & 1u, w)))) break;
         ptx::tc_fence_after();
-        float p[128];
+        float p[64];
         {
-          uint32_t v[4][32];
+          uint32_t v[2][32];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, v[c]);   // all four in flight
+          for (int c = 0; c < 2; ++c) ptx::tmem_ld32(tS + c * 32, v[c]);   // both in flight
 #pragma unroll
-          for (int c = 0; c < 4; ++c) ptx::tmem_ld_wait(v[c]);
+          for (int c = 0; c < 2; ++c) ptx::tmem_ld_wait(v[c]);
           // S is in registers: the next S product may overwrite it while the
           // exponentials below run
           ptx::tc_fence_before();
           ptx::mbar_arrive(s_free);
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
               const float2 x = ptx::ffma2(make_float2(__uint_as_float(v[c][i]), __uint_as_float(v[c][i + 1])),
@@ -973,31 +977,32 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
               p[c * 32 + i + 1] = ptx::ex2(x.y);
             }
         }
-        const int kv0 = j * BT;
-        if (kv0 + BT > Tk || (P.p.causal && kv0 + BT - 1 > qt * BT)) {
-          const int lim = min(Tk - kv0, P.p.causal ? q - kv0 + 1 : BT);   // keys [0, lim) allowed
+        const int kv0 = j * BT + 64 * g;         // key of this thread's first column
+        if (kv0 + 64 > Tk || (P.p.causal && kv0 + 63 > q)) {
+          const int lim = min(Tk - kv0, P.p.causal ? q - kv0 + 1 : 64);   // columns [0, lim) allowed
 #pragma unroll
-          for (int i = 0; i < 128; ++i)
+          for (int i = 0; i < 64; ++i)
             if (i >= lim) p[i] = 0.f;
         }
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dp_full + (sp & 1u), (sp >> 1) & 1u, w)))) break;
         ptx::tc_fence_after();
-        const uint32_t tDP = tmem + lane_off + t_dp(sp);
-        uint32_t v[4][32];
+        const uint32_t tDP = tmem + lane_off + t_dp(sp) + 64 * g;
+        uint32_t v[2][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tDP + c * 32, v[c]);   // all four in flight
+        for (int c = 0; c < 2; ++c) ptx::tmem_ld32(tDP + c * 32, v[c]);   // both in flight
 #pragma unroll
-        for (int c = 0; c < 4; ++c) ptx::tmem_ld_wait(v[c]);
+        for (int c = 0; c < 2; ++c) ptx::tmem_ld_wait(v[c]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float2 e = ptx::fadd2(make_float2(__uint_as_float(v[c][2 * i]), __uint_as_float(v[c][2 * i + 1])),
                                         make_float2(-dd, -dd));
-            const float2 r = ptx::fmul2(make_float2(p[c * 32 + 2 * i], p[c * 32 + 2 * i + 1]), e);
-            pk[i] = ptx::pack_bf16(r.x, r.y);
+            const float2 rr = ptx::fmul2(make_float2(p[c * 32 + 2 * i], p[c * 32 + 2 * i + 1]), e);
+            pk[i] = ptx::pack_bf16(rr.x, rr.y);
           }
+          // packed over this group's own first 32 columns (already read)
           ptx::tmem_st16(tDP + c * 16, pk);
         }
         ptx::tmem_st_wait();
@@ -1007,9 +1012,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       if (!ok) break;
       if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dq_full, u_it & 1u, w)))) break;
       ptx::tc_fence_after();
-      __nv_bfloat16* row = P.dQ + (static_cast<size_t>(bh) * Tq + (q_ok ? q : 0)) * HD;
+      // this group writes dQ columns [g HD / 2, (g + 1) HD / 2) of its row
+      __nv_bfloat16* row = P.dQ + (static_cast<size_t>(bh) * Tq + (q_ok ? q : 0)) * HD + (HD / 2) * g;
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int c = 0; c < HD / 64; ++c) {
         uint32_t v[32];
         ptx::tmem_ld32(tDQ + c * 32, v);
         ptx::tmem_ld_wait(v);
