@@ -334,7 +334,6 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         q_range(P, kb, &q0, &nq);
         if (nq == 0) continue;
         if (!(ok = wait(kv_full, u_it & 1u))) break;
-        if (!(ok = wait(acc_free, (u_it & 1u) ^ 1u))) break;
         {
           if (!(ok = wait(q_full + qslot(q_it), qpar(q_it)))) break;
           ptx::tc_fence_after();
@@ -353,6 +352,9 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
             moved |= lane != 0;
             mma_dpt(q_it);
             ptx::mma_commit(dp_full);
+            // deterministic: K and V are read by no later MMA of a one-tile
+            // unit, so the next unit's tiles may start loading now
+            if (!ATOMIC_DQ && nq == 1) ptx::mma_commit(kv_empty);
           }
           __syncwarp();
           // Q and dO of the next query tile: each step waits for the tiles of
@@ -364,7 +366,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           const uint32_t it = q_it + ii;
           const bool more = ii + 1 < nq;   // Q of tile it + 1 is resident
           // dV += P^T dO, then the next S^T (it overwrites P^T only after the
-          // product above has read it)
+          // product above has read it). The first dV of a unit overwrites
+          // the accumulator: the epilogue must have read the previous one
+          // (its S^T and dP^T products above overlap that epilogue).
+          if (ii == 0 && !(ok = wait(acc_free, (u_it & 1u) ^ 1u))) break;
           if (!(ok = wait(p_full, pp & 1u))) break;
           ptx::tc_fence_after();
           if (ptx::elect_one()) {
@@ -410,6 +415,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
               moved |= lane != 0;
               mma_dpt(it + 1);
               ptx::mma_commit(dp_full);
+              // deterministic: that was the last MMA reading K or V in this
+              // unit (the last S^T went out with dV above), so the next
+              // unit's K and V may start loading during the last step
+              if (!ATOMIC_DQ && ii + 2 == nq) ptx::mma_commit(kv_empty);
             }
             __syncwarp();
           }
@@ -419,7 +428,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         if (ptx::elect_one()) {
           moved |= lane != 0;
           ptx::mma_commit(acc_full);
-          ptx::mma_commit(kv_empty);
+          if (ATOMIC_DQ) ptx::mma_commit(kv_empty);   // the dQ products read K up to the last step
         }
         __syncwarp();
         q_it += nq;
@@ -876,6 +885,9 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         if (ptx::elect_one()) {
           moved |= lane != 0;
           mma_dp(t, sp);
+          // Q and dO are read by no later MMA of a one-tile unit: the next
+          // unit's tiles may start loading now
+          if (nk == 1) ptx::mma_commit(q_empty);
         }
         __syncwarp();
         // K of the next key tile: each step waits for the K tile of the step
@@ -901,6 +913,9 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           if (ptx::elect_one()) {
             moved |= lane != 0;
             mma_dp(tn, sp + 1);
+            // the last S and dP of the unit are out: Q and dO are free for
+            // the next unit while the last dQ products run
+            if (j + 2 == nk) ptx::mma_commit(q_empty);
           }
           __syncwarp();
         }
@@ -923,7 +938,6 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       if (ptx::elect_one()) {
         moved |= lane != 0;
         ptx::mma_commit(dq_full);
-        ptx::mma_commit(q_empty);
       }
       __syncwarp();
       k_it += nk;

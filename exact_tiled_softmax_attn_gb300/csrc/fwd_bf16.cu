@@ -240,6 +240,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mma_S(1, slot(ik));
         ptx::mma_commit(s_full + 1);
         ptx::mma_commit(kv_empty + slot(ik));
+        if (n1 == 1) ptx::mma_commit(q_empty);   // no later MMA reads Q: the next unit's may load
       }
       __syncwarp();
       // V_0 and K_1: each step waits for the next step's tiles while its own
@@ -278,6 +279,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mma_S(1, slot(ikn));
             ptx::mma_commit(s_full + 1);
             ptx::mma_commit(kv_empty + slot(ikn));
+            // the unit's last S products are out (tile 0 ends no later than
+            // tile 1): Q is free for the next unit during the last step
+            if (j + 2 == n1) ptx::mma_commit(q_empty);
           }
         }
         __syncwarp();
@@ -285,8 +289,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (j + 2 < n1 && !(ok = wait(kv_full + slot(ikn + 2), par(ikn + 2)))) break;   // K_{j+2}
       }
       if (!ok) break;
-      if (ptx::elect_one()) ptx::mma_commit(q_empty);
-      __syncwarp();
       kv_it += n1;
       ++u_it;
     }
