@@ -132,9 +132,9 @@ struct CfgKV {
   static constexpr int OFF_D = OFF_LSE + NL * BT * 4; // [NL][128] fp32
   static constexpr int OFF_BAR = OFF_D + NL * BT * 4;
   // kv_full, kv_empty, q_full[NQ], q_empty[NQ], o_full[NO], o_empty[NO], l_full[NL], l_empty[NL],
-  // s_full, dp_full, p_full, ds_full, dq_full, dq_free, acc_full, acc_free, stage_full, stage_free,
-  // sds_free, drain
-  static constexpr int NBAR = 2 + 2 * NQ + 2 * NO + 2 * NL + 12;
+  // s_full, dp_full, p_full, ds_full, dq_full, dq_free, acc_full, dv_free, stage_full, stage_free,
+  // sds_free, drain, dk_free
+  static constexpr int NBAR = 2 + 2 * NQ + 2 * NO + 2 * NL + 13;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16(BT, BT, false, false);
@@ -184,7 +184,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   uint64_t* dq_full = s_full + 4;
   uint64_t* dq_free = s_full + 5;
   uint64_t* acc_full = s_full + 6;
-  uint64_t* acc_free = s_full + 7;
+  uint64_t* dv_free = s_full + 7;    // the epilogue has read the dV accumulator
+  uint64_t* dk_free = s_full + 12;   // ... and the dK accumulator
   uint64_t* stage_full = s_full + 8;
   uint64_t* stage_free = s_full + 9;
   uint64_t* sds_free = s_full + 10;
@@ -214,7 +215,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     ptx::mbar_init(dq_full, 1);
     ptx::mbar_init(dq_free, 128);
     ptx::mbar_init(acc_full, 1);
-    ptx::mbar_init(acc_free, 128);
+    ptx::mbar_init(dv_free, 128);
+    ptx::mbar_init(dk_free, 128);
     ptx::mbar_init(stage_full, 128);
     ptx::mbar_init(stage_free, 1);
     ptx::mbar_init(sds_free, 1);
@@ -366,10 +368,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           const uint32_t it = q_it + ii;
           const bool more = ii + 1 < nq;   // Q of tile it + 1 is resident
           // dV += P^T dO, then the next S^T (it overwrites P^T only after the
-          // product above has read it). The first dV of a unit overwrites
-          // the accumulator: the epilogue must have read the previous one
-          // (its S^T and dP^T products above overlap that epilogue).
-          if (ii == 0 && !(ok = wait(acc_free, (u_it & 1u) ^ 1u))) break;
+          // product above has read it). The first dV (dK) of a unit
+          // overwrites the accumulator: the epilogue must have read the
+          // previous unit's (its S^T and dP^T products overlap that epilogue).
+          if (ii == 0 && !(ok = wait(dv_free, (u_it & 1u) ^ 1u))) break;
           if (!(ok = wait(p_full, pp & 1u))) break;
           ptx::tc_fence_after();
           if (ptx::elect_one()) {
@@ -386,6 +388,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           }
           __syncwarp();
           // dK += dS^T Q (and, atomic mode, dQ = dS K into the dP^T columns)
+          if (ii == 0 && !(ok = wait(dk_free, (u_it & 1u) ^ 1u))) break;
           if (!(ok = wait(ds_full, pp & 1u))) break;
           ++pp;
           ptx::tc_fence_after();
@@ -648,32 +651,37 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       }
       if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(acc_full, u_it & 1u, w)))) break;
       ptx::tc_fence_after();
+      // dV first, released as soon as it is in registers and stored, then
+      // dK (scaled by the softmax scale: dK = scale dS^T Q)
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        uint32_t v[32], k[32];
-        ptx::tmem_ld32(tmem + lane_off + T_DV + c * 32, v);
-        ptx::tmem_ld32(tmem + lane_off + T_DK + c * 32, k);
-        ptx::tmem_ld_wait(v);
-        ptx::tmem_ld_wait(k);
-        if (key_ok) {
+      for (int acc = 0; acc < 2; ++acc) {
+        const uint32_t tcol = tmem + lane_off + (acc ? T_DK : T_DV);
+        __nv_bfloat16* orow = acc ? dk_row : dv_row;
+        const float mul = acc ? scale : 1.0f;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 a, b;
-            a.x = ptx::pack_bf16(__uint_as_float(v[8 * e + 0]), __uint_as_float(v[8 * e + 1]));
-            a.y = ptx::pack_bf16(__uint_as_float(v[8 * e + 2]), __uint_as_float(v[8 * e + 3]));
-            a.z = ptx::pack_bf16(__uint_as_float(v[8 * e + 4]), __uint_as_float(v[8 * e + 5]));
-            a.w = ptx::pack_bf16(__uint_as_float(v[8 * e + 6]), __uint_as_float(v[8 * e + 7]));
-            b.x = ptx::pack_bf16(__uint_as_float(k[8 * e + 0]) * scale, __uint_as_float(k[8 * e + 1]) * scale);
-            b.y = ptx::pack_bf16(__uint_as_float(k[8 * e + 2]) * scale, __uint_as_float(k[8 * e + 3]) * scale);
-            b.z = ptx::pack_bf16(__uint_as_float(k[8 * e + 4]) * scale, __uint_as_float(k[8 * e + 5]) * scale);
-            b.w = ptx::pack_bf16(__uint_as_float(k[8 * e + 6]) * scale, __uint_as_float(k[8 * e + 7]) * scale);
-            reinterpret_cast<uint4*>(dv_row + c * 32)[e] = a;
-            reinterpret_cast<uint4*>(dk_row + c * 32)[e] = b;
+        for (int c = 0; c < HD / 32; c += 2) {
+          uint32_t v[2][32];
+          ptx::tmem_ld32(tcol + c * 32, v[0]);
+          ptx::tmem_ld32(tcol + c * 32 + 32, v[1]);
+          ptx::tmem_ld_wait(v[0]);
+          ptx::tmem_ld_wait(v[1]);
+          if (key_ok) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                uint4 a;
+                a.x = ptx::pack_bf16(__uint_as_float(v[h][8 * e + 0]) * mul, __uint_as_float(v[h][8 * e + 1]) * mul);
+                a.y = ptx::pack_bf16(__uint_as_float(v[h][8 * e + 2]) * mul, __uint_as_float(v[h][8 * e + 3]) * mul);
+                a.z = ptx::pack_bf16(__uint_as_float(v[h][8 * e + 4]) * mul, __uint_as_float(v[h][8 * e + 5]) * mul);
+                a.w = ptx::pack_bf16(__uint_as_float(v[h][8 * e + 6]) * mul, __uint_as_float(v[h][8 * e + 7]) * mul);
+                reinterpret_cast<uint4*>(orow + (c + h) * 32)[e] = a;
+              }
           }
         }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(acc ? dk_free : dv_free);
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(acc_free);
       ++u_it;
     }
     // every reduce issued by this CTA has landed before it exits
