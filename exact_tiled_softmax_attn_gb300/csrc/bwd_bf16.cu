@@ -704,10 +704,10 @@ struct CfgQ {
   static constexpr int TILE = BT * HD * 2;
   // K and V tiles have rings of their own. A K tile stays resident from its
   // S product to its dQ product one step later, a V tile only until its dP
-  // product, so K gets three slots and V two: both then arrive about one key
-  // step ahead of their first use.
-  static constexpr int NSK = (HD == 128) ? 3 : 6;
-  static constexpr int NSV = (HD == 128) ? 2 : 4;
+  // product, so K gets four slots and V one: a K tile then arrives about two
+  // key steps ahead of its first use, a V tile one.
+  static constexpr int NSK = (HD == 128) ? 4 : 8;
+  static constexpr int NSV = (HD == 128) ? 1 : 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = OFF_Q + TILE;
   static constexpr int OFF_K = OFF_DO + TILE;          // [NSK]
