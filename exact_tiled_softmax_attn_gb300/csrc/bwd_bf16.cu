@@ -48,9 +48,16 @@ namespace bwd {
 constexpr int BT = 128;                   // rows per tile (keys and queries)
 constexpr int BOX_BYTES = 128 * 64 * 2;   // one TMA box: 128 rows x 64 bf16
 constexpr int KV_THREADS = 512;          // dK/dV kernel: four warpgroups
-constexpr int KV_REG_CTRL = 104;         // producer / MMA warpgroup
-constexpr int KV_REG_PDS = 152;          // each of the two P / dS warpgroups
-constexpr int KV_REG_DQ = 104;           // dQ / epilogue warpgroup
+// Per-warpgroup register budgets of the dK/dV kernel (setmaxnreg). The
+// deterministic variant has no dQ staging in its last warpgroup (only the
+// dK/dV epilogue) and gives the P/dS threads room to hold a tile's 64
+// LSE and D values in registers.
+template <bool ATOMIC_DQ>
+struct KvRegs {
+  static constexpr int CTRL = ATOMIC_DQ ? 104 : 96;   // producer / MMA warpgroup
+  static constexpr int PDS = ATOMIC_DQ ? 152 : 168;   // each of the two P / dS warpgroups
+  static constexpr int DQ = ATOMIC_DQ ? 104 : 80;     // dQ / epilogue warpgroup
+};
 constexpr int KV_REG_LAUNCH = 128;       // 65536 / 512, what the launch bound gives
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -246,7 +253,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   const int wg = warp >> 2;
 
   if (wg == 0) {
-    ptx::reg_release<KV_REG_CTRL>();
+    ptx::reg_release<KvRegs<ATOMIC_DQ>::CTRL>();
     if (warp == 0 && lane == 0) {
       // ---------------------------------------------------------- producer
       ptx::WaitCtx w{abort_flag, P.status, 1u};
@@ -445,7 +452,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       if (__any_sync(0xffffffffu, moved) && lane == 0) atomicOr(P.status, ATTN_DEV_ISSUER);
     }
   } else if (wg <= 2) {
-    ptx::reg_acquire<KV_REG_PDS>();
+    ptx::reg_acquire<KvRegs<ATOMIC_DQ>::PDS>();
     // ------------------------------------------------------------ P / dS (thread = key row)
     // Group h handles query columns [64h, 64h + 64) of the tile.
     const int h = wg - 1;
@@ -472,6 +479,19 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         const float* dd = sD + ls * BT + 64 * h;
         // the staged LSE / D slices of this tile are visible once l_full completed
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(l_full + ls, lpar(q_it), w)))) break;
+        // deterministic: this tile's 64 -LSE*log2(e) values into registers
+        // while S^T is being computed
+        float nl[ATOMIC_DQ ? 1 : 64];
+        if (!ATOMIC_DQ) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float4 t4 = reinterpret_cast<const float4*>(nlse2)[i];
+            nl[4 * i] = t4.x;
+            nl[4 * i + 1] = t4.y;
+            nl[4 * i + 2] = t4.z;
+            nl[4 * i + 3] = t4.w;
+          }
+        }
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(s_full, sp & 1u, w)))) break;
         ptx::tc_fence_after();
         // pass 1: P^T_j,q = 2^(s * scale * log2e - LSE_q * log2e), masked; packed bf16
@@ -493,7 +513,9 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 16; i += 2) {
               const int qa = c * 32 + 2 * i;
-              const float4 l4 = ptx::lds128(nlse2 + qa);
+              const float4 l4 = ATOMIC_DQ ? ptx::lds128(nlse2 + qa)
+                                          : make_float4(nl[qa & 63], nl[(qa + 1) & 63], nl[(qa + 2) & 63],
+                                                        nl[(qa + 3) & 63]);
               const float2 x01 = ptx::ffma2(make_float2(__uint_as_float(rs[c][2 * i]), __uint_as_float(rs[c][2 * i + 1])),
                                             sc2v, make_float2(l4.x, l4.y));
               const float2 x23 = ptx::ffma2(make_float2(__uint_as_float(rs[c][2 * i + 2]),
@@ -516,6 +538,17 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         ptx::tc_fence_before();
         ptx::mbar_arrive(p_full);
         // pass 2: dS^T_j,q = P^T (dP^T - D_q); bf16 over dP^T and into smem (dS, MN-major)
+        float dl[ATOMIC_DQ ? 1 : 64];
+        if (!ATOMIC_DQ) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float4 t4 = reinterpret_cast<const float4*>(dd)[i];
+            dl[4 * i] = t4.x;
+            dl[4 * i + 1] = t4.y;
+            dl[4 * i + 2] = t4.z;
+            dl[4 * i + 3] = t4.w;
+          }
+        }
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dp_full, sp & 1u, w)))) break;
         if (ATOMIC_DQ) {
           // the dQ group has finished staging the previous dQ tile in the dS buffer
@@ -534,7 +567,9 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 16; i += 2) {
               const int qa = c * 32 + 2 * i;
-              const float4 d4 = ptx::lds128(dd + qa);
+              const float4 d4 = ATOMIC_DQ ? ptx::lds128(dd + qa)
+                                          : make_float4(dl[qa & 63], dl[(qa + 1) & 63], dl[(qa + 2) & 63],
+                                                        dl[(qa + 3) & 63]);
               const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pkeep[c][i]));
               const float2 pg = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pkeep[c][i + 1]));
               // (dP - D) as -D * 1 + dP, two lanes per instruction
@@ -567,7 +602,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       }
     }
   } else {
-    ptx::reg_release<KV_REG_DQ>();
+    ptx::reg_release<KvRegs<ATOMIC_DQ>::DQ>();
     // ------------------------------------------------------------ dQ reduce; dK / dV epilogue
     const int quad = warp & 3;
     const int r = quad * 32 + lane;                 // TMEM lane = row
@@ -1113,7 +1148,9 @@ cudaError_t launch(const LaunchBwd& a) {
     // The register split must fit the launch allocation (see reg_acquire).
     cudaFuncAttributes fa;
     if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
-    if (fa.numRegs != KV_REG_LAUNCH || KV_REG_CTRL + 2 * KV_REG_PDS + KV_REG_DQ > 4 * KV_REG_LAUNCH)
+    const int split = atomic ? KvRegs<true>::CTRL + 2 * KvRegs<true>::PDS + KvRegs<true>::DQ
+                             : KvRegs<false>::CTRL + 2 * KvRegs<false>::PDS + KvRegs<false>::DQ;
+    if (fa.numRegs != KV_REG_LAUNCH || split > 4 * KV_REG_LAUNCH)
       return cudaErrorInvalidConfiguration;
     kern<<<grid, KV_THREADS, smem, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO,
                                                            atomic ? *a.tmdQacc : *a.tmQ, P);
