@@ -265,9 +265,10 @@ def run_ours(args, w):
         pkg.attn_bwd_phase(x["Q"], x["K"], x["V"], o, lse, x["dO"], dq, dk, dvv, B, H, Tq, Tk, d, dv, sc,
                            w.causal, code, det, ws, ws.numel(), ph, stream)
 
-    # backward launch groups in order: preprocess, dK/dV kernel, dQ kernel
-    # (deterministic only), dQ conversion (atomic only)
-    phases = (1, 4, 5, 3)
+    # backward launch groups in order: preprocess (atomic dQ only for bf16),
+    # dQ kernel (deterministic only; it also forms D), dK/dV kernel, dQ
+    # conversion (atomic only)
+    phases = (1, 5, 4, 3)
 
     def step(ev=None):
         if ev is not None:
@@ -301,10 +302,10 @@ def run_ours(args, w):
     barrier()
     if clocks:
         clocks.mark(t_wall0, t_wall1)
-    per = [[e[j].elapsed_time(e[j + 1]) for j in range(5)] for e in events]   # ms: fwd, pre, kv, q, conv
+    per = [[e[j].elapsed_time(e[j + 1]) for j in range(5)] for e in events]   # ms: fwd, pre, q, kv, conv
     step_ms = [sum(p) for p in per]
     total_ms = reduce_max(sum(step_ms))
-    fwd_ms, pre_ms, kv_ms, q_ms, conv_ms = (statistics.mean(p[j] for p in per) for j in range(5))
+    fwd_ms, pre_ms, q_ms, kv_ms, conv_ms = (statistics.mean(p[j] for p in per) for j in range(5))
     main_ms = kv_ms + q_ms
     bwd_ms = pre_ms + main_ms + conv_ms
     F, Bf = w.fwd_flop(), w.bwd_flop()
@@ -394,12 +395,14 @@ def run_ours(args, w):
     kernels.update({
         "bwd main (all main kernels)": {"ms": main_ms, "tflops": Bf / (main_ms * 1e-3) / 1e12},
         # reads O, dO, LSE; writes D and LSE*log2(e) (padded rows) and zeroes the dQ accumulator
+        # atomic dQ only (bf16): the deterministic dQ kernel forms D itself
         "bwd preprocess": {"ms": pre_ms,
-                           "gbs": B * H * Tq * (2 * dv * 2 + 4 + 8 + (d * 4 if not det else 0)) / (pre_ms * 1e-3) / 1e9},
+                           "gbs": B * H * Tq * (2 * dv * 2 + 4 + 8 + d * 4) / (pre_ms * 1e-3) / 1e9 if not det else None},
         "dQ convert": {"ms": conv_ms, "gbs": B * H * Tq * d * (4 + 2) / (conv_ms * 1e-3) / 1e9 if not det else None},
     })
     kernels["bwd main (all main kernels)"]["frac_of_peak"] = kernels["bwd main (all main kernels)"]["tflops"] / peak
-    kernels["bwd preprocess"]["frac_of_hbm"] = kernels["bwd preprocess"]["gbs"] / peaks["hbm_gbs"]
+    if kernels["bwd preprocess"]["gbs"] is not None:
+        kernels["bwd preprocess"]["frac_of_hbm"] = kernels["bwd preprocess"]["gbs"] / peaks["hbm_gbs"]
     # the dominant kernel: the longest of the single kernels
     dom = max((k for k, v in kernels.items() if "flop" in v), key=lambda k: kernels[k]["ms"])
     achieved = kernels[dom]["tflops"]
@@ -420,7 +423,7 @@ def run_ours(args, w):
                 "steps": e2e_steps,
                 "pipeline": "two buffer sets; step i+1 host-to-device and step i-1 device-to-host copies "
                             "overlap step i's kernels on separate streams"},
-        "gpu_launches": args.steps * 4,
+        "gpu_launches": args.steps * (3 if det else 4),   # fwd, dQ, dK/dV | fwd, preprocess, dK/dV, convert
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -87,8 +87,10 @@ struct Order {
 
 struct Params {
   Problem p;
-  const float* NLSE2;      // [BH, Tq_pad]: -LSE * log2(e), -inf on padding / no-key rows
-  const float* D;          // [BH, Tq_pad]
+  float* NLSE2;            // [BH, Tq_pad]: -LSE * log2(e), -inf on padding / no-key rows
+  float* D;                // [BH, Tq_pad]
+  const __nv_bfloat16* O;  // forward output (deterministic dQ kernel: D of its rows)
+  const float* LSE;        // [BH, Tq] natural-log LSE from the forward
   int Tq_pad;
   float* dQacc;            // atomic path: fp32 [BH, Tq, d], pre-zeroed
   __nv_bfloat16* dQ;       // deterministic path output
@@ -747,10 +749,11 @@ struct CfgQ {
   static constexpr int OFF_DO = OFF_Q + TILE;
   static constexpr int OFF_K = OFF_DO + TILE;          // [NSK]
   static constexpr int OFF_V = OFF_K + NSK * TILE;     // [NSV]
-  static constexpr int OFF_BAR = OFF_V + NSV * TILE;
+  static constexpr int OFF_DPART = OFF_V + NSV * TILE;   // [2][128] fp32 partial D of the row groups
+  static constexpr int OFF_BAR = OFF_DPART + 2 * BT * 4;
   // q_full, q_empty, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full, s_free, dp_full[2],
-  // ds_full[2], dq_full, drain
-  static constexpr int NBAR = 2 + 2 * NSK + 2 * NSV + 8;
+  // ds_full[2], dq_full, drain, dpart_full
+  static constexpr int NBAR = 2 + 2 * NSK + 2 * NSV + 9;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16(BT, BT, false, false);
@@ -759,9 +762,11 @@ struct CfgQ {
 constexpr int DQ_THREADS = 320;
 
 // One persistent CTA per SM; a unit is one 128-row query tile of one head.
-// For each key tile (fixed ascending order): S = Q K^T, dP = dO V^T (both in
-// TMEM), dS = P o (dP - D) written bf16 over dP, and dQ += dS K accumulates
-// in TMEM. Warps: 0 producer, 1 MMA, 2-5 and 6-9 two row groups; group g
+// The row threads first form the tile's D = rowsum(dO o O) (dO from shared
+// memory, O from global memory) and -LSE * log2(e), which they use and store
+// for the dK/dV kernel that runs after this one. Then, for each key tile
+// (fixed ascending order): S = Q K^T, dP = dO V^T (both in TMEM), dS =
+// P o (dP - D) written bf16 over dP, and dQ += dS K accumulates in TMEM. Warps: 0 producer, 1 MMA, 2-5 and 6-9 two row groups; group g
 // works on key columns [64g, 64g + 64) of every query row (one thread per
 // row each) and packs its dS at columns [64g, 64g + 32) of the dP buffer.
 // TMEM: S [0, 128), dQ [128, 256), dP/dS in two buffers [256, 384) and
@@ -797,6 +802,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   uint64_t* ds_full = s_full + 4;   // [2], by step parity
   uint64_t* dq_full = s_full + 6;
   uint64_t* drain = s_full + 7;
+  uint64_t* dpart_full = s_full + 8;   // both row groups have written their partial D
+  float* dpart = reinterpret_cast<float*>(smem + C::OFF_DPART);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
   if (threadIdx.x == 0) {
@@ -818,6 +825,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     }
     ptx::mbar_init(dq_full, 1);
     ptx::mbar_init(drain, 1);
+    ptx::mbar_init(dpart_full, 256);
     *abort_flag = 0u;
     ptx::fence_mbar_init();
   }
@@ -848,6 +856,15 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     int bh, qt;
     for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qt); ++round) {
       const int nk = nk_of(qt);
+      {
+        // the next unit's O rows (its D) into L2 while this unit runs
+        int bh2, qt2;
+        if (P.order.unit(cta, grid, round + 1, &bh2, &qt2)) {
+          const int rows = min(BT, Tq - qt2 * BT);
+          ptx::bulk_prefetch_l2(P.O + (static_cast<size_t>(bh2) * Tq + static_cast<size_t>(qt2) * BT) * HD,
+                                static_cast<uint32_t>(rows) * HD * 2);
+        }
+      }
       if (!(ok = ptx::mbar_wait(q_empty, (u_it & 1u) ^ 1u, w))) break;
       ptx::mbar_arrive_expect_tx(q_full, 2 * C::TILE);
       for (int b = 0; b < C::KB; ++b) {
@@ -1007,9 +1024,23 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       const int nk = nk_of(qt);
       const int q = qt * BT + r;
       const bool q_ok = q < Tq;
-      // padding rows hold NLSE2 = -inf and D = 0, so their P and dS are 0
-      const float nlse2 = P.NLSE2[static_cast<size_t>(bh) * P.Tq_pad + q];
-      const float dd = P.D[static_cast<size_t>(bh) * P.Tq_pad + q];
+      // D_q = sum_c dO_qc O_qc ("attention_backprop", section "Gradient of
+      // S": ROW_SUM(dL/dO o O)) over this group's half of the columns, dO
+      // from the resident tile, O from global memory; padding rows get D = 0
+      // and -LSE * log2(e) = -inf, so their P and dS are 0
+      // this row's O columns come in while the first S is computed; the
+      // dot product and the exchange with the other group follow the first
+      // step's exponentials (D is first needed for the first dS)
+      uint4 o4[HD / 16];
+#pragma unroll
+      for (int k = 0; k < HD / 16; ++k) {
+        o4[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (q_ok)
+          o4[k] = *reinterpret_cast<const uint4*>(P.O + (static_cast<size_t>(bh) * Tq + q) * HD + (HD / 2) * g + 8 * k);
+      }
+      const float lse = q_ok ? P.LSE[static_cast<size_t>(bh) * Tq + q] : -CUDART_INF_F;
+      const float nlse2 = (lse == -CUDART_INF_F) ? -CUDART_INF_F : -lse * LOG2E;
+      float dd = 0.f;
       for (int j = 0; j < nk; ++j, ++sp) {
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(s_full, sp & 1u, w)))) break;
         ptx::tc_fence_after();
@@ -1033,6 +1064,31 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
               p[c * 32 + i] = ptx::ex2(x.x);
               p[c * 32 + i + 1] = ptx::ex2(x.y);
             }
+        }
+        if (j == 0) {
+          // dO of the tile is resident once q_full completed
+          if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(q_full, u_it & 1u, w)))) break;
+          float part = 0.f;
+#pragma unroll
+          for (int k = 0; k < HD / 16; ++k) {
+            const uint4 d4 = *reinterpret_cast<const uint4*>(sdO + sw128_offset(r, (HD / 2) * g + 8 * k));
+            const __nv_bfloat162* ov = reinterpret_cast<const __nv_bfloat162*>(&o4[k]);
+            const __nv_bfloat162* dv = reinterpret_cast<const __nv_bfloat162*>(&d4);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 a = __bfloat1622float2(ov[e]), b = __bfloat1622float2(dv[e]);
+              part = fmaf(a.x, b.x, part);
+              part = fmaf(a.y, b.y, part);
+            }
+          }
+          dpart[g * BT + r] = part;
+          ptx::mbar_arrive(dpart_full);
+          if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dpart_full, u_it & 1u, w)))) break;
+          dd = dpart[r] + dpart[BT + r];
+          if (g == 0) {
+            P.D[static_cast<size_t>(bh) * P.Tq_pad + q] = dd;
+            P.NLSE2[static_cast<size_t>(bh) * P.Tq_pad + q] = nlse2;
+          }
         }
         const int kv0 = j * BT + 64 * g;         // key of this thread's first column
         if (kv0 + 64 > Tk || (P.p.causal && kv0 + 63 > q)) {
@@ -1114,7 +1170,9 @@ template <int HD>
 cudaError_t launch(const LaunchBwd& a) {
   const Problem& p = a.p;
   const bool atomic = !a.deterministic;
-  const bool pre = a.phase == 0 || a.phase == 1, conv = a.phase == 0 || a.phase == 3;
+  // Deterministic: the dQ kernel forms D and -LSE * log2(e) itself and runs
+  // before the dK/dV kernel, which reads them; there is no preprocess.
+  const bool pre = atomic && (a.phase == 0 || a.phase == 1), conv = a.phase == 0 || a.phase == 3;
   const bool main_kv = a.phase == 0 || a.phase == 2 || a.phase == 4;
   const bool main_q = a.phase == 0 || a.phase == 2 || a.phase == 5;
   cudaError_t e = cudaSuccess;
@@ -1127,6 +1185,8 @@ cudaError_t launch(const LaunchBwd& a) {
   P.p = p;
   P.NLSE2 = a.NLSE2;
   P.D = a.D;
+  P.O = static_cast<const __nv_bfloat16*>(a.O);
+  P.LSE = a.LSE;
   P.Tq_pad = padded_rows(p.Tq);
   P.dQacc = a.dQacc;
   P.dQ = static_cast<__nv_bfloat16*>(a.dQ);
@@ -1137,6 +1197,15 @@ cudaError_t launch(const LaunchBwd& a) {
   P.n_k_tiles = (p.Tk + BT - 1) / BT;
   P.sc2 = p.scale * LOG2E;
   const int heads = p.B * p.H;
+  if (!atomic && main_q) {
+    P.order = Order{P.n_q_tiles, heads, p.causal ? 1 : 0};
+    const int units = P.n_q_tiles * heads;
+    const int grid = units < a.num_sms ? units : a.num_sms;
+    e = cudaFuncSetAttribute(dq_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgQ<HD>::SMEM);
+    if (e != cudaSuccess) return e;
+    dq_kernel<HD><<<grid, DQ_THREADS, CfgQ<HD>::SMEM, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO, P);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   if (main_kv) {
     P.order = Order{P.n_k_tiles, heads, p.causal ? 2 : 0};
     const int units = P.n_k_tiles * heads;
@@ -1163,14 +1232,7 @@ cudaError_t launch(const LaunchBwd& a) {
                                                             static_cast<uint2*>(a.dQ), n4);
     return cudaGetLastError();
   }
-  if (!main_q) return cudaSuccess;
-  P.order = Order{P.n_q_tiles, heads, p.causal ? 1 : 0};
-  const int units = P.n_q_tiles * heads;
-  const int grid = units < a.num_sms ? units : a.num_sms;
-  e = cudaFuncSetAttribute(dq_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgQ<HD>::SMEM);
-  if (e != cudaSuccess) return e;
-  dq_kernel<HD><<<grid, DQ_THREADS, CfgQ<HD>::SMEM, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO, P);
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace bwd

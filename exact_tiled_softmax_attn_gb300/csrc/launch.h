@@ -46,7 +46,7 @@ struct LaunchBwd {
   float* NLSE2;             // [B*H, Tq_pad] workspace: -LSE * log2(e), -inf for padding / no-key rows
   float* dQacc;             // [B,H,Tq,d] fp32 workspace (bf16 atomic path), else null
   int deterministic;
-  int phase;                // 0 all; 1 preprocess; 2 main kernels (4 then 5); 3 dQ conversion;
+  int phase;                // 0 all; 1 preprocess; 2 main kernels (5 then 4); 3 dQ conversion;
                             // 4 dK/dV kernel; 5 deterministic dQ kernel
   uint32_t* status;
   int num_sms;

@@ -123,14 +123,16 @@ ATTN_API attn_status_t attn_bwd(const void* Q, const void* K, const void* V, con
 /*
  * The backward split into its launch groups, for measurement: the same
  * arguments as attn_bwd plus `phase`:
- *   1  preprocess: D = rowsum(dO o O) (and zeroing of the fp32 dQ
- *      accumulator when deterministic == 0)
- *   2  main kernels: phases 4 and 5 in this order
+ *   1  preprocess: D = rowsum(dO o O) and -LSE * log2(e) (and zeroing of the
+ *      fp32 dQ accumulator when deterministic == 0); a no-op for bf16 with
+ *      deterministic == 1, where the dQ kernel forms D itself
+ *   2  main kernels: phases 5 and 4 in this order
  *   3  dQ conversion from the fp32 accumulator (bf16 with deterministic
  *      == 0; a no-op otherwise)
  *   4  the dK/dV kernel alone (with deterministic == 0 it also accumulates dQ)
- *   5  the separate dQ kernel alone (deterministic == 1; a no-op otherwise)
- * Calling phases 1, 2, 3 (or 1, 4, 5, 3) in order on one stream equals one
+ *   5  the separate dQ kernel alone (deterministic == 1; a no-op otherwise);
+ *      for bf16 it also writes the D and -LSE * log2(e) phase 4 reads
+ * Calling phases 1, 2, 3 (or 1, 5, 4, 3) in order on one stream equals one
  * attn_bwd call; phase 0 is attn_bwd itself. Other values give
  * ATTN_ERR_INVALID_ARG.
  */

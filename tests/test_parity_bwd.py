@@ -154,7 +154,11 @@ def test_bf16_atomic_and_deterministic_agree():
     b = run(x, True, 0.125, 1)
     for u, v, name in zip(a[2:], b[2:], ("dQ", "dK", "dV")):
         check_grad(u, v, torch.bfloat16, name)
-    assert torch.equal(a[3], b[3]) and torch.equal(a[4], b[4])   # dK, dV do not depend on the dQ mode
+    # dK and dV differ only through D, which the two modes sum in a
+    # different order (the deterministic dQ kernel forms it itself)
+    for u, v, name in zip(a[3:], b[3:], ("dK", "dV")):
+        err = (u.float() - v.float()).norm() / v.float().norm()
+        assert err <= 2e-3, f"{name} differs between dQ modes by {err:.2e}"
 
 
 def test_bf16_inputs_unchanged():
@@ -172,8 +176,8 @@ def test_bf16_inputs_unchanged():
 @pytest.mark.parametrize("dt,d", [(torch.float32, 64), (torch.bfloat16, 128)])
 @pytest.mark.parametrize("deterministic", [0, 1])
 def test_phases_equal_one_call(dt, d, deterministic):
-    # preprocess, dK/dV kernel, dQ kernel, dQ conversion launched one by one
-    # (phases 1, 4, 5, 3) give what one attn_bwd call gives
+    # preprocess, dQ kernel, dK/dV kernel, dQ conversion launched one by one
+    # (phases 1, 5, 4, 3) give what one attn_bwd call gives
     B, H, T = 1, 3, 515
     x = make_random((B, H, T, d), (B, H, T, d), (B, H, T, d), seed=11, dtype=dt, device=DEV)
     code = pkg.ATTN_BF16 if dt == torch.bfloat16 else pkg.ATTN_F32
@@ -181,7 +185,7 @@ def test_phases_equal_one_call(dt, d, deterministic):
     ws = torch.empty(max(pkg.attn_bwd_workspace_size(B, H, T, T, d, d, code, deterministic), 256),
                      dtype=torch.uint8, device=DEV)
     outs = []
-    for phases in ((0,), (1, 4, 5, 3)):
+    for phases in ((0,), (1, 5, 4, 3)):
         g = [torch.full_like(x["Q"], float("nan")) for _ in range(3)]
         for ph in phases:
             pkg.attn_bwd_phase(x["Q"], x["K"], x["V"], o, lse, x["dO"], g[0], g[1], g[2], B, H, T, T, d, d, 0.09,
