@@ -29,7 +29,7 @@ sys.path.insert(0, ROOT)
 METRIC = "attention TFLOP/s fwd+bwd (bf16, causal, 1 GB300)"
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_SOURCES = ("fwd_bf16.cu", "bwd_bf16.cu", "small.cu", "ptx.cuh", "common.cuh")
+KERNEL_SOURCES = ("fwd_bf16.cu", "bwd_bf16.cu", "small.cu", "splitkv.cu", "ptx.cuh", "common.cuh")
 
 
 # ---------------------------------------------------------------- helpers
@@ -223,7 +223,7 @@ def workload_config(w):
                         f"{'causal' if w.causal else 'no mask'}, scale={w.softmax_scale:.6g}",
             "B": w.B, "H": w.H, "Tq": w.Tq, "Tk": w.Tk, "d": w.d, "dv": w.dv, "causal": w.causal,
             "l2": "256 MiB written between timed steps (outside the timed region); per-step inputs "
-                  f"{4 * w.B * w.H * w.Tq * w.d * (2 if w.dtype == 'bf16' else 4) / 1e6:.0f} MB > 129 MB L2"}
+                  f"{w.B * w.H * (w.Tq + w.Tk) * (w.d + w.dv) * (2 if w.dtype == 'bf16' else 4) / 1e6:.0f} MB"}
 
 
 # ---------------------------------------------------------------- GPU leg
@@ -258,8 +258,23 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream()
     sc = w.softmax_scale
 
+    # forward: attn_fwd, or with --splitkv the split-KV forward (key ranges
+    # as separate work units, then the merge kernel)
+    n_splits = 1
+    if args.splitkv is not None:
+        n_splits = pkg.attn_fwd_splitkv_splits(B, H, Tq, Tk, d, dv, code, args.splitkv)
+        sk_bytes = pkg.attn_fwd_splitkv_workspace_size(B, H, Tq, Tk, d, dv, code, args.splitkv)
+        sk_ws = torch.empty(max(sk_bytes, 256), dtype=torch.uint8, device=dev)
+
+    def fwd_call(xi, oi, li, st):
+        if args.splitkv is None:
+            pkg.attn_fwd(xi["Q"], xi["K"], xi["V"], oi, li, B, H, Tq, Tk, d, dv, sc, w.causal, code, st)
+        else:
+            pkg.attn_fwd_splitkv(xi["Q"], xi["K"], xi["V"], oi, li, B, H, Tq, Tk, d, dv, sc, w.causal, code,
+                                 args.splitkv, sk_ws, sk_ws.numel(), st)
+
     def fwd():
-        pkg.attn_fwd(x["Q"], x["K"], x["V"], o, lse, B, H, Tq, Tk, d, dv, sc, w.causal, code, stream)
+        fwd_call(x, o, lse, stream)
 
     def bwd_phase(ph):
         pkg.attn_bwd_phase(x["Q"], x["K"], x["V"], o, lse, x["dO"], dq, dk, dvv, B, H, Tq, Tk, d, dv, sc,
@@ -346,8 +361,7 @@ def run_ours(args, w):
             stream.wait_event(in_ready[b])
             if i >= 2:
                 stream.wait_event(out_done[b])          # step i-2's results have left the device
-            pkg.attn_fwd(xi["Q"], xi["K"], xi["V"], oi["O"], oi["LSE"], B, H, Tq, Tk, d, dv, sc, w.causal, code,
-                         stream)
+            fwd_call(xi, oi["O"], oi["LSE"], stream)
             pkg.attn_bwd(xi["Q"], xi["K"], xi["V"], oi["O"], oi["LSE"], xi["dO"], oi["dQ"], oi["dK"], oi["dV"],
                          B, H, Tq, Tk, d, dv, sc, w.causal, code, det, ws, ws.numel(), stream)
             comp_done[b].record(stream)
@@ -381,7 +395,9 @@ def run_ours(args, w):
     # dQ); the deterministic dQ kernel's own product is dQ (it recomputes S
     # and dP, which is counted under "executed").
     mm = F / 2
-    kernels = {"fwd (attn_fwd_bf16_kernel)": {"ms": fwd_ms, "flop": F}}
+    fwd_name = "fwd (attn_fwd_bf16_kernel)" if n_splits == 1 else \
+        f"fwd split-KV, {n_splits} splits (attn_fwd_bf16_kernel + merge)"
+    kernels = {fwd_name: {"ms": fwd_ms, "flop": F}}
     if det:
         kernels["bwd dK/dV (dkdv_kernel)"] = {"ms": kv_ms, "flop": 4 * mm}
         kernels["bwd dQ (dq_kernel)"] = {"ms": q_ms, "flop": mm, "executed_flop": 3 * mm}
@@ -408,7 +424,7 @@ def run_ours(args, w):
     achieved = kernels[dom]["tflops"]
     traffic = load_traffic(dom.split("(")[-1].rstrip(")"))
     cfg = workload_config(w)
-    cfg.update({"dq_mode": "deterministic" if det else "atomic",
+    cfg.update({"dq_mode": "deterministic" if det else "atomic", "fwd_splits": n_splits,
                 "fwd_tflops": F / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": Bf / (bwd_ms * 1e-3) / 1e12,
                 "fwd_bwd_frac_of_dense_bf16_peak": (F + Bf) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12 / peak,
                 "peak_source": f"{peaks['source']} bf16_tflops {peak}", "kernels": kernels})
@@ -423,7 +439,8 @@ def run_ours(args, w):
                 "steps": e2e_steps,
                 "pipeline": "two buffer sets; step i+1 host-to-device and step i-1 device-to-host copies "
                             "overlap step i's kernels on separate streams"},
-        "gpu_launches": args.steps * (3 if det else 4),   # fwd, dQ, dK/dV | fwd, preprocess, dK/dV, convert
+        # fwd (+ split-KV merge), dQ, dK/dV | fwd (+ merge), preprocess, dK/dV, convert
+        "gpu_launches": args.steps * ((3 if det else 4) + (1 if n_splits > 1 else 0)),
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -441,6 +458,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="c3")
     ap.add_argument("--dq-mode", choices=["deterministic", "atomic"], default="deterministic",
                     help="dQ in a separate fixed-order pass (default) or by fp32 atomics inside the dK/dV kernel")
+    ap.add_argument("--splitkv", type=int, default=None,
+                    help="run the forward through attn_fwd_splitkv with this many key splits (0 = automatic)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -22,7 +22,8 @@ __all__ = [
     "LIB_PATH", "EXPORTED_SYMBOLS", "AttnError", "load_library",
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA",
     "ATTN_ERR_TIMEOUT", "ATTN_ERR_WORKSPACE", "ATTN_F32", "ATTN_BF16",
-    "attn_fwd", "attn_fwd_f32_blocked", "attn_bwd", "attn_bwd_phase", "attn_bwd_workspace_size",
+    "attn_fwd", "attn_fwd_f32_blocked", "attn_fwd_splitkv", "attn_fwd_splitkv_splits",
+    "attn_fwd_splitkv_workspace_size", "attn_bwd", "attn_bwd_phase", "attn_bwd_workspace_size",
     "attn_bwd_noalloc", "ATTN_NOALLOC_SCRATCH_BYTES", "attn_online_softmax_step", "attn_device_status",
     "attn_selftest_wait_timeout", "attn_strerror", "attn_last_cuda_error", "attn_version",
     "forward", "backward",
@@ -40,6 +41,9 @@ _P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
     "attn_fwd_f32_blocked": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "attn_fwd_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _SZ, _P]),
+    "attn_fwd_splitkv_splits": (_I, [_I, _I, _I, _I, _I, _I, _I, _I]),
+    "attn_fwd_splitkv_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "attn_bwd_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _SZ, _P]),
     "attn_bwd_phase": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _SZ,
@@ -143,6 +147,24 @@ def attn_fwd_f32_blocked(Q, K, V, O, LSE, B, H, Tq, Tk, d, dv, scale, causal, bl
     return st
 
 
+def attn_fwd_splitkv(Q, K, V, O, LSE, B, H, Tq, Tk, d, dv, scale, causal, dtype, num_splits, workspace,
+                     workspace_bytes, stream=None, check=True) -> int:
+    st = load_library().attn_fwd_splitkv(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, H, Tq, Tk, d, dv,
+                                         float(scale), int(causal), int(dtype), int(num_splits), _ptr(workspace),
+                                         int(workspace_bytes), _stream(stream))
+    if check:
+        _check(st, "attn_fwd_splitkv")
+    return st
+
+
+def attn_fwd_splitkv_splits(B, H, Tq, Tk, d, dv, dtype, num_splits) -> int:
+    return load_library().attn_fwd_splitkv_splits(B, H, Tq, Tk, d, dv, int(dtype), int(num_splits))
+
+
+def attn_fwd_splitkv_workspace_size(B, H, Tq, Tk, d, dv, dtype, num_splits) -> int:
+    return load_library().attn_fwd_splitkv_workspace_size(B, H, Tq, Tk, d, dv, int(dtype), int(num_splits))
+
+
 def attn_online_softmax_step(m, l, acc, scores, v_block, n, bs, dv, stream=None, check=True) -> int:
     st = load_library().attn_online_softmax_step(_ptr(m), _ptr(l), _ptr(acc), _ptr(scores), _ptr(v_block), int(n),
                                                  int(bs), int(dv), _stream(stream))
@@ -213,13 +235,24 @@ def _shape(q, k, v):
     return B, H, Tq, Tk, d, dv
 
 
-def forward(q, k, v, causal: bool = False, scale: Optional[float] = None, stream=None):
-    """O, LSE = attention(q, k, v). Allocates O (q.dtype) and LSE (fp32) with torch."""
+def forward(q, k, v, causal: bool = False, scale: Optional[float] = None, stream=None,
+            num_splits: Optional[int] = None):
+    """O, LSE = attention(q, k, v). Allocates O (q.dtype) and LSE (fp32) with torch.
+
+    num_splits selects the split-KV forward (0 = automatic, n >= 1 = that many
+    key splits); None is the plain forward."""
     B, H, Tq, Tk, d, dv = _shape(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     o = torch.empty(B, H, Tq, dv, dtype=q.dtype, device=q.device)
     lse = torch.empty(B, H, Tq, dtype=torch.float32, device=q.device)
-    attn_fwd(q, k, v, o, lse, B, H, Tq, Tk, d, dv, scale, causal, _dtype_code(q), stream)
+    dt = _dtype_code(q)
+    if num_splits is None:
+        attn_fwd(q, k, v, o, lse, B, H, Tq, Tk, d, dv, scale, causal, dt, stream)
+    else:
+        nbytes = attn_fwd_splitkv_workspace_size(B, H, Tq, Tk, d, dv, dt, num_splits)
+        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+        attn_fwd_splitkv(q, k, v, o, lse, B, H, Tq, Tk, d, dv, scale, causal, dt, num_splits, ws, ws.numel(),
+                         stream)
     return o, lse
 
 

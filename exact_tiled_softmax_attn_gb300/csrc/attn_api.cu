@@ -150,11 +150,49 @@ BwdLayout bwd_layout(int B, int H, int Tq, int d, attn_dtype_t dt, int determini
   return L;
 }
 
+// Split-KV forward: effective number of key splits for a request (0 = pick
+// one so that the query-tile pairs times the splits fill the SMs once, with
+// at least two key tiles per split), clamped to [1, min(key tiles, 64)]; the
+// key tiles per split go to *split_tiles. fp32 problems never split.
+int splitkv_count(int B, int H, int Tq, int Tk, attn_dtype_t dt, int req, int num_sms, int* split_tiles) {
+  const int nkb = (Tk + 127) / 128;
+  int S = req;
+  if (dt != ATTN_BF16 || nkb <= 1 || B == 0 || H == 0 || Tq == 0) {
+    S = 1;
+  } else if (req == 0) {
+    const long long units = static_cast<long long>(B) * H * ((Tq + 255) / 256);
+    S = units >= num_sms ? 1 : static_cast<int>((num_sms + units - 1) / units);
+    S = S < nkb / 2 ? S : (nkb / 2 > 1 ? nkb / 2 : 1);
+  }
+  if (S > nkb) S = nkb;
+  if (S > 64) S = 64;
+  if (S < 1) S = 1;
+  const int cs = (nkb + S - 1) / S;
+  *split_tiles = cs;
+  return nkb > 0 ? (nkb + cs - 1) / cs : 1;
+}
+
+struct SplitLayout {
+  size_t lse_off, total;
+};
+// Workspace of the split-KV forward: Opart [S][B*H*Tq][dv] fp32 | LSEpart
+// [S][B*H*Tq] fp32, each part 256-byte aligned; nothing when S = 1.
+SplitLayout split_layout(int B, int H, int Tq, int dv, int S) {
+  SplitLayout L{};
+  if (S <= 1) return L;
+  const size_t rows = static_cast<size_t>(B) * H * Tq;
+  L.lse_off = round_up(static_cast<size_t>(S) * rows * dv * sizeof(float), 256);
+  L.total = L.lse_off + round_up(static_cast<size_t>(S) * rows * sizeof(float), 256);
+  return L;
+}
+
 attn_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Tq,
                        int Tk, int d, int dv, float scale, int causal, attn_dtype_t dtype, int block_n,
-                       void* stream) {
+                       int split_req, void* workspace, size_t workspace_bytes, void* stream) {
   attn_status_t s = check_common(B, H, Tq, Tk, d, dv, scale, causal, dtype);
   if (s != ATTN_OK) return s;
+  if (split_req < 0) return ATTN_ERR_INVALID_ARG;
+  if (dtype == ATTN_F32 && split_req > 1) return ATTN_ERR_UNSUPPORTED;
   const size_t es = elem_size(dtype);
   const size_t bh = static_cast<size_t>(B) * H;
   const size_t align = dtype == ATTN_BF16 ? 16 : 4;
@@ -169,10 +207,25 @@ attn_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, flo
   for (Range in : {range(Q, bq), range(K, bk), range(V, bv)})
     if (overlap(ro, in) || overlap(rl, in)) return ATTN_ERR_INVALID_ARG;
   if (overlap(ro, rl)) return ATTN_ERR_INVALID_ARG;
+  int split_tiles = 0, n_splits = 1;
+  SplitLayout SL{};
+  DeviceInfo* di = nullptr;
+  if (split_req != 1) {
+    // only the automatic choice needs the device (its SM count)
+    if (split_req == 0 && dtype == ATTN_BF16 && (s = device_info(&di)) != ATTN_OK) return s;
+    n_splits = splitkv_count(B, H, Tq, Tk, dtype, split_req, di ? di->num_sms : 0, &split_tiles);
+    SL = split_layout(B, H, Tq, dv, n_splits);
+    if (SL.total > 0) {
+      if (workspace == nullptr || workspace_bytes < SL.total || reinterpret_cast<uintptr_t>(workspace) % 256)
+        return ATTN_ERR_WORKSPACE;
+      const Range rw = range(workspace, SL.total);
+      for (Range other : {range(Q, bq), range(K, bk), range(V, bv), ro, rl})
+        if (overlap(rw, other)) return ATTN_ERR_WORKSPACE;
+    }
+  }
   if (bh == 0 || Tq == 0) return ATTN_OK;
 
-  DeviceInfo* di;
-  if ((s = device_info(&di)) != ATTN_OK) return s;
+  if (di == nullptr && (s = device_info(&di)) != ATTN_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Problem p{B, H, Tq, Tk, d, dv, scale, causal};
   if (Tk == 0) {
@@ -189,6 +242,12 @@ attn_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, flo
   a.status = di->status;
   a.num_sms = di->num_sms;
   a.block_n = block_n;
+  a.n_splits = n_splits;
+  a.split_tiles = split_tiles;
+  if (n_splits > 1) {
+    a.Opart = static_cast<float*>(workspace);
+    a.LSEpart = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + SL.lse_off);
+  }
   a.stream = st;
   cudaError_t e;
   if (dtype == ATTN_F32) {
@@ -202,6 +261,8 @@ attn_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, flo
     a.tmK = &mk;
     a.tmV = &mv;
     e = launch_fwd_bf16(a);
+    if (e == cudaSuccess && n_splits > 1)
+      e = launch_splitkv_merge(p, a.Opart, a.LSEpart, n_splits, split_tiles, O, LSE, di->num_sms, st);
   }
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
@@ -233,14 +294,41 @@ extern "C" {
 
 attn_status_t attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Tq,
                        int Tk, int d, int dv, float scale, int causal, attn_dtype_t dtype, void* stream) {
-  return fwd_impl(Q, K, V, O, LSE, B, H, Tq, Tk, d, dv, scale, causal, dtype, 64, stream);
+  return fwd_impl(Q, K, V, O, LSE, B, H, Tq, Tk, d, dv, scale, causal, dtype, 64, 1, nullptr, 0, stream);
+}
+
+int attn_fwd_splitkv_splits(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype, int num_splits) {
+  if (check_common(B, H, Tq, Tk, d, dv, 1.0f, 0, dtype) != ATTN_OK || num_splits < 0) return -1;
+  if (dtype == ATTN_F32 && num_splits > 1) return -1;
+  int num_sms = 0;
+  if (num_splits == 0 && dtype == ATTN_BF16) {
+    DeviceInfo* di;
+    if (device_info(&di) != ATTN_OK) return -1;
+    num_sms = di->num_sms;
+  }
+  int cs;
+  return splitkv_count(B, H, Tq, Tk, dtype, num_splits, num_sms, &cs);
+}
+
+size_t attn_fwd_splitkv_workspace_size(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype,
+                                       int num_splits) {
+  const int S = attn_fwd_splitkv_splits(B, H, Tq, Tk, d, dv, dtype, num_splits);
+  if (S < 1) return 0;
+  return split_layout(B, H, Tq, dv, S).total;
+}
+
+attn_status_t attn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                               int Tq, int Tk, int d, int dv, float scale, int causal, attn_dtype_t dtype,
+                               int num_splits, void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_impl(Q, K, V, O, LSE, B, H, Tq, Tk, d, dv, scale, causal, dtype, 64, num_splits, workspace,
+                  workspace_bytes, stream);
 }
 
 attn_status_t attn_fwd_f32_blocked(const float* Q, const float* K, const float* V, float* O, float* LSE, int B,
                                    int H, int Tq, int Tk, int d, int dv, float scale, int causal, int block_n,
                                    void* stream) {
   if (block_n != 32 && block_n != 64 && block_n != 128) return ATTN_ERR_UNSUPPORTED;
-  return fwd_impl(Q, K, V, O, LSE, B, H, Tq, Tk, d, dv, scale, causal, ATTN_F32, block_n, stream);
+  return fwd_impl(Q, K, V, O, LSE, B, H, Tq, Tk, d, dv, scale, causal, ATTN_F32, block_n, 1, nullptr, 0, stream);
 }
 
 size_t attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype,

@@ -80,6 +80,14 @@ struct Params {
   UnitOrder order;
   int n_kv_tiles;
   float sc2;   // scale * log2(e)
+  // Split-KV mode (n_splits > 1): split s of a query-tile pair covers key
+  // tiles [s * split_tiles, (s + 1) * split_tiles) and writes its normalised
+  // partial output and log-sum-exp (fp32) to Opart [n_splits][B*H*Tq][dv]
+  // and LSEpart [n_splits][B*H*Tq] instead of O and LSE.
+  int n_splits;
+  int split_tiles;
+  float* Opart;
+  float* LSEpart;
 };
 
 __device__ __forceinline__ void tile_counts(const Params& P, int qb, int* n0, int* n1) {
@@ -91,6 +99,26 @@ __device__ __forceinline__ void tile_counts(const Params& P, int qb, int* n0, in
     *n0 = nkb;
     *n1 = nkb;
   }
+}
+
+// Key tiles of work unit `blk`: query-tile pair qb, first key tile j0, and
+// n0 / n1 key tiles for its first / second query tile (n0 <= n1, possibly 0
+// for the first tile of a split). False when the unit has no key tile.
+__device__ __forceinline__ bool unit_tiles(const Params& P, int blk, int* qb, int* j0, int* n0, int* n1) {
+  if (P.n_splits <= 1) {
+    *qb = blk;
+    *j0 = 0;
+    tile_counts(P, blk, n0, n1);
+    return true;
+  }
+  *qb = blk / P.n_splits;
+  const int s = blk - *qb * P.n_splits;
+  int a0, a1;
+  tile_counts(P, *qb, &a0, &a1);
+  *j0 = s * P.split_tiles;
+  *n0 = max(0, min(a0 - *j0, P.split_tiles));
+  *n1 = max(0, min(a1 - *j0, P.split_tiles));
+  return *n1 > 0;
 }
 
 template <int HD>
@@ -162,10 +190,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tma_prefetch_desc(&tmV);
     uint32_t item = 0, u_it = 0;
     bool ok = true;
-    int bh, qb;
-    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qb); ++round) {
-      int n0, n1;
-      tile_counts(P, qb, &n0, &n1);
+    int bh, blk;
+    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &blk); ++round) {
+      int qb, j0, n0, n1;
+      if (!unit_tiles(P, blk, &qb, &j0, &n0, &n1)) continue;
       if (!(ok = ptx::mbar_wait(q_empty, (u_it & 1u) ^ 1u, w))) break;
       ptx::mbar_arrive_expect_tx(q_full, 2 * C::TILE);
       for (int t = 0; t < 2; ++t)
@@ -179,7 +207,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ptx::mbar_arrive_expect_tx(kv_full + sl, C::TILE);
           const CUtensorMap* map = kv ? &tmV : &tmK;
           for (int b = 0; b < C::KB; ++b)
-            ptx::tma_load_3d(sKV + sl * C::TILE + b * BOX_BYTES, map, kv_full + sl, b * 64, j * BN, bh);
+            ptx::tma_load_3d(sKV + sl * C::TILE + b * BOX_BYTES, map, kv_full + sl, b * 64, (j0 + j) * BN, bh);
         }
       }
       ++u_it;
@@ -225,18 +253,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto par = [](uint32_t item) { return (item / C::NSLOT) & 1u; };
     uint32_t kv_it = 0, u_it = 0, pp[2] = {0u, 0u};
     bool ok = true, moved = false;
-    int bh, qb;
-    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qb); ++round) {
-      int n0, n1;
-      tile_counts(P, qb, &n0, &n1);
+    int bh, blk;
+    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &blk); ++round) {
+      int qb, j0, n0, n1;
+      if (!unit_tiles(P, blk, &qb, &j0, &n0, &n1)) continue;
       if (!(ok = wait(q_full, u_it & 1u))) break;
       const uint32_t ik = 2 * kv_it;
       if (!(ok = wait(kv_full + slot(ik), par(ik)))) break;
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
         moved |= lane != 0;
-        mma_S(0, slot(ik));
-        ptx::mma_commit(s_full + 0);
+        if (n0 > 0) {   // (a split may hold no key tile for the first query tile)
+          mma_S(0, slot(ik));
+          ptx::mma_commit(s_full + 0);
+        }
         mma_S(1, slot(ik));
         ptx::mma_commit(s_full + 1);
         ptx::mma_commit(kv_empty + slot(ik));
@@ -312,11 +342,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int Tq = P.p.Tq, Tk = P.p.Tk;
     uint32_t sp = 0, op = 0;
     bool ok = true;
-    int bh, qb;
-    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qb); ++round) {
-      int n0, n1;
-      tile_counts(P, qb, &n0, &n1);
+    int bh, blk;
+    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &blk); ++round) {
+      int qb, j0, n0, n1;
+      if (!unit_tiles(P, blk, &qb, &j0, &n0, &n1)) continue;
       const int nt = t ? n1 : n0;
+      if (nt == 0) continue;   // nothing to write: the merge reads no partial for these rows
       const int qt = 2 * qb + t;
       const int q_row = qt * BM + r;
       float m_used = -CUDART_INF_F, l = 0.f;
@@ -331,7 +362,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) ptx::tmem_ld_wait(raw[c]);
         float* s = reinterpret_cast<float*>(&raw[0][0]);
-        const int kv0 = j * BN;
+        const int kv0 = (j0 + j) * BN;
         const bool diag = P.p.causal && (kv0 + BN - 1 > qt * BM);
         if (diag || kv0 + BN > Tk) {
           const int lim = min(Tk - kv0, P.p.causal ? q_row - kv0 + 1 : BN);  // keys [0, lim) allowed
@@ -406,6 +437,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::tc_fence_after();
       const float inv_l = (l > 0.f) ? 1.0f / l : 0.f;
       const bool row_ok = q_row < Tq;
+      const float lse_row = (l > 0.f) ? (m_used + log2f(l)) * 0.69314718055994530942f : -CUDART_INF_F;
+      if (P.n_splits > 1) {
+        // partial result of this split: O_s = A / l in fp32 and LSE_s
+        const size_t rows = static_cast<size_t>(P.p.B) * P.p.H * Tq;
+        const size_t row = static_cast<size_t>(blk % P.n_splits) * rows + static_cast<size_t>(bh) * Tq +
+                           (row_ok ? q_row : 0);
+        float* prow = P.Opart + row * HD;
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t o[32];
+          ptx::tmem_ld32(tO + c * 32, o);
+          ptx::tmem_ld_wait(o);
+          if (row_ok) {
+            float4* dst = reinterpret_cast<float4*>(prow + c * 32);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                   __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+          }
+        }
+        if (row_ok) P.LSEpart[row] = lse_row;
+        ptx::tc_fence_before();
+        continue;
+      }
       __nv_bfloat16* orow = P.O + (static_cast<size_t>(bh) * Tq + (row_ok ? q_row : 0)) * HD;
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
@@ -422,10 +477,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
-      if (row_ok) {
-        P.LSE[static_cast<size_t>(bh) * Tq + q_row] =
-            (l > 0.f) ? (m_used + log2f(l)) * 0.69314718055994530942f : -CUDART_INF_F;
-      }
+      if (row_ok) P.LSE[static_cast<size_t>(bh) * Tq + q_row] = lse_row;
       ptx::tc_fence_before();
     }
   }
@@ -447,10 +499,15 @@ cudaError_t launch(const LaunchFwd& a) {
   P.LSE = a.LSE;
   P.status = a.status;
   P.n_kv_tiles = (a.p.Tk + BN - 1) / BN;
-  P.order.n_blocks = (a.p.Tq + 2 * BM - 1) / (2 * BM);
+  P.n_splits = a.n_splits > 1 ? a.n_splits : 1;
+  P.split_tiles = a.split_tiles;
+  P.Opart = a.Opart;
+  P.LSEpart = a.LSEpart;
+  P.order.n_blocks = (a.p.Tq + 2 * BM - 1) / (2 * BM) * P.n_splits;
   P.order.n_heads = a.p.B * a.p.H;
   P.order.heavy_last = a.p.causal ? 1 : 0;
   P.sc2 = a.p.scale * 1.4426950408889634f;
+  if (static_cast<long long>(P.order.n_blocks) * P.order.n_heads > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int units = P.order.count();
   const int grid = units < a.num_sms ? units : a.num_sms;
   auto kern = attn_fwd_bf16_kernel<HD>;

@@ -23,6 +23,13 @@ struct LaunchFwd {
   uint32_t* status;
   int num_sms;
   int block_n;              // fp32 path: keys per tile (32, 64 or 128)
+  // bf16 split-KV forward: n_splits > 1 key ranges of split_tiles 128-key
+  // tiles each; partial outputs [n_splits][B*H*Tq][dv] and log-sum-exps
+  // [n_splits][B*H*Tq] (fp32) instead of O and LSE
+  int n_splits;
+  int split_tiles;
+  float* Opart;
+  float* LSEpart;
   cudaStream_t stream;
 };
 
@@ -61,6 +68,11 @@ cudaError_t launch_bwd_f32(const LaunchBwd& a);
 cudaError_t launch_fwd_bf16(const LaunchFwd& a);
 cudaError_t launch_bwd_bf16(const LaunchBwd& a);
 size_t fwd_bf16_smem_bytes(int d);
+
+// O, LSE from the split-KV partials (rows of query tile qt read the splits
+// that hold at least one of its key tiles)
+cudaError_t launch_splitkv_merge(const Problem& p, const float* Opart, const float* LSEpart, int n_splits,
+                                 int split_tiles, void* O, float* LSE, int num_sms, cudaStream_t s);
 
 // shared small kernels
 cudaError_t launch_fill_empty_fwd(const Problem& p, void* O, float* LSE, int elem_bytes, cudaStream_t s);

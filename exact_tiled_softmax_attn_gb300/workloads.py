@@ -8,7 +8,7 @@ Layout of every tensor is [batch, heads, seq_len, head_dim], contiguous
 ("attention_backprop", section "Forward Pass": Q, K, V are
 [batch_size, num_heads, seq_len, head_dim]).
 
-The five named workloads:
+The named workloads:
 
 =====  ===========================================  =====  ======  ==========  ====
 name   shape                                        dtype  mask    scale       seed
@@ -21,6 +21,8 @@ c4     B2  H8  Tq=1000 Tk=4000 d=dv=128             f32    none    1/sqrt(128) 3
        K rows scaled by +40 / -40 in alternating 128-key bands
        (also run at scale 1.0, where the logits pass +-1000)
 c5     B1  H32 Tq=Tk=32768 d=dv=128                 bf16   causal  1/sqrt(128) 4
+s1     B1  H8  Tq=256 Tk=65536 d=dv=128             bf16   none    1/sqrt(128) 5
+       (few query tiles, many keys: the split-KV forward's case)
 =====  ===========================================  =====  ======  ==========  ====
 
 Draw order: one CPU ``torch.Generator`` seeded with the workload's seed
@@ -84,6 +86,9 @@ WORKLOADS: Dict[str, Workload] = {
     "c4_scale1": Workload("c4_scale1", 2, 8, 1000, 4000, 128, 128, "f32", False, 3,
                           scale=1.0, k_bands=40.0),
     "c5": Workload("c5", 1, 32, 32768, 32768, 128, 128, "bf16", True, 4),
+    # few query tiles against many keys (8 query-tile pairs for 152 SMs): the
+    # split-KV forward's case
+    "s1": Workload("s1", 1, 8, 256, 65536, 128, 128, "bf16", False, 5),
 }
 
 

@@ -91,6 +91,49 @@ ATTN_API attn_status_t attn_fwd_f32_blocked(const float* Q, const float* K, cons
                                    void* stream);
 
 /*
+ * Split-KV forward for problems with few query tiles per SM (small B*H*Tq,
+ * long Tk): the key tiles of every pair of 128-row query tiles are divided
+ * into S contiguous ranges ("splits") that run as separate work units; each
+ * writes its partial softmax state for its keys (O_s = A_s / l_s and LSE_s,
+ * fp32) to `workspace`, and a merge kernel combines the splits with the
+ * associative rescale of the running max, sum and accumulator ("The Hidden
+ * Recurrence in Softmax Attention", section "Chunk-wise Mode with Online
+ * Softmax Re-scale": chunk states rescaled to a common maximum and added):
+ *   M = max_s LSE_s, w_s = exp(LSE_s - M), O = sum_s w_s O_s / sum_s w_s,
+ *   LSE = M + log sum_s w_s.
+ * Same inputs, outputs, layout and mask as attn_fwd; O and LSE agree with
+ * attn_fwd up to fp32 rounding order. num_splits = 0 picks S so that the
+ * query-tile pairs times S fill the SMs about once (at least two key tiles
+ * per split); num_splits >= 1 asks for that many, clamped to the number of
+ * 128-key tiles and 64. S = 1 is attn_fwd itself (no workspace). bf16 only
+ * for S > 1: an fp32 problem with num_splits > 1 returns ATTN_ERR_UNSUPPORTED
+ * (num_splits 0 or 1 runs the fp32 attn_fwd). `workspace` (256-byte aligned,
+ * at least attn_fwd_splitkv_workspace_size bytes, not overlapping any other
+ * argument; may be NULL when that is 0) holds Opart [S][B*H*Tq][dv] then
+ * LSEpart [S][B*H*Tq], both fp32; else ATTN_ERR_WORKSPACE. Other errors as
+ * attn_fwd; asynchronous on `stream`.
+ */
+ATTN_API attn_status_t attn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
+                                        int H, int Tq, int Tk, int d, int dv, float scale, int causal,
+                                        attn_dtype_t dtype, int num_splits, void* workspace,
+                                        size_t workspace_bytes, void* stream);
+
+/*
+ * The number of splits S attn_fwd_splitkv uses for these arguments (>= 1;
+ * num_splits = 0 consults the current device's SM count), or -1 for invalid
+ * arguments.
+ */
+ATTN_API int attn_fwd_splitkv_splits(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype,
+                                     int num_splits);
+
+/*
+ * Bytes of workspace attn_fwd_splitkv needs (0 when S = 1 or the arguments
+ * are invalid).
+ */
+ATTN_API size_t attn_fwd_splitkv_workspace_size(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype,
+                                                int num_splits);
+
+/*
  * Bytes of device workspace attn_bwd needs for this problem (0 is possible).
  * Holds -LSE * log2(e) and D = rowsum(dO o O), each [B*H, Tq_pad] fp32 with
  * Tq_pad = Tq rounded up to a multiple of 128, and, for bf16 with
