@@ -115,7 +115,7 @@ attn_status_t check_common(int B, int H, int Tq, int Tk, int d, int dv, float sc
   if (dt == ATTN_F32) {
     if (d > 128 || dv > 128) return ATTN_ERR_UNSUPPORTED;
   } else {
-    if (d != dv || (d != 64 && d != 128)) return ATTN_ERR_UNSUPPORTED;
+    if ((d != 64 && d != 128) || (dv != 64 && dv != 128)) return ATTN_ERR_UNSUPPORTED;
   }
   // every index of every tensor must fit the kernels' 64-bit arithmetic and
   // the per-head row counts must fit int (TMA coordinates are int32)

@@ -4,7 +4,7 @@
 // it ("The Hidden Recurrence in Softmax Attention", section "Flash Attention
 // Backward Pass"), and forms the gradient terms of "attention_backprop"
 // (sections "Gradient of V and P", "Gradient of S", "Gradient of Q and K"):
-//   D  = rowsum(dO o O)                        (preprocess kernel)
+//   D  = rowsum(dO o O)                        (dQ kernel, or the preprocess kernel in atomic mode)
 //   P  = exp(scale * Q K^T - LSE)
 //   dV = P^T dO,   dP = dO V^T,   dS = P o (dP - D)
 //   dK = scale * dS^T Q,          dQ = scale * dS K
@@ -116,10 +116,13 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int col) {
          (col & 7) * 2;
 }
 
-template <int HD, bool ATOMIC_DQ>
+// HD = d (Q, K, dQ, dK rows), HV = dv (V, O, dO, dV rows); each 64 or 128.
+template <int HD, int HV, bool ATOMIC_DQ>
 struct CfgKV {
-  static constexpr int KB = HD / 64;
-  static constexpr int TILE = BT * HD * 2;
+  static constexpr int KB = HD / 64;        // 64-column boxes per Q / K row
+  static constexpr int KBV = HV / 64;       // ... per V / dO row
+  static constexpr int TILE = BT * HD * 2;  // one 128-row Q or K tile
+  static constexpr int TILE_V = BT * HV * 2;  // one 128-row V or dO tile
   // Q tiles, dO tiles and the -LSE*log2(e) / D slices of a query tile have
   // rings of their own. A Q tile stays resident from its S^T product to its
   // dK product at the end of the step, a dO tile from its dP^T product to its
@@ -131,11 +134,11 @@ struct CfgKV {
   static constexpr int NL = 2;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE;
-  static constexpr int OFF_Q = OFF_V + TILE;          // [NQ]
+  static constexpr int OFF_Q = OFF_V + TILE_V;        // [NQ]
   static constexpr int OFF_DO = OFF_Q + NQ * TILE;    // [NO]
   // atomic mode: dS, 128 q x 128 keys bf16, MN-major; it then stages one
   // 64-column half of the fp32 dQ tile (two 128 x 32 boxes) for the TMA reduce
-  static constexpr int OFF_DS = OFF_DO + NO * TILE;
+  static constexpr int OFF_DS = OFF_DO + NO * TILE_V;
   static constexpr int DS_BYTES = ATOMIC_DQ ? BT * BT * 2 : 0;
   static constexpr int OFF_LSE = OFF_DS + DS_BYTES;   // [NL][128] fp32 (-LSE * log2 e, -inf = no key)
   static constexpr int OFF_D = OFF_LSE + NL * BT * 4; // [NL][128] fp32
@@ -147,7 +150,8 @@ struct CfgKV {
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16(BT, BT, false, false);
-  static constexpr uint32_t IDESC_ACC = ptx::idesc_bf16(BT, HD, false, true);   // dV, dK (A in TMEM)
+  static constexpr uint32_t IDESC_DV = ptx::idesc_bf16(BT, HV, false, true);    // dV (A in TMEM)
+  static constexpr uint32_t IDESC_DK = ptx::idesc_bf16(BT, HD, false, true);    // dK (A in TMEM)
   static constexpr uint32_t IDESC_DQ = ptx::idesc_bf16(BT, HD, true, true);     // dQ = dS K
 };
 
@@ -157,12 +161,12 @@ struct CfgKV {
 // group has not read yet.
 __device__ __forceinline__ uint32_t packed_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
-template <int HD, bool ATOMIC_DQ>
+template <int HD, int HV, bool ATOMIC_DQ>
 __global__ void __launch_bounds__(KV_THREADS, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const __grid_constant__ CUtensorMap tmdQ, const Params P) {
-  using C = CfgKV<HD, ATOMIC_DQ>;
+  using C = CfgKV<HD, HV, ATOMIC_DQ>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -271,11 +275,9 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         q_range(P, kb, &q0, &nq);
         if (nq == 0) continue;
         if (!(ok = ptx::mbar_wait(kv_empty, (u_it & 1u) ^ 1u, w))) break;
-        ptx::mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
-        for (int b = 0; b < C::KB; ++b) {
-          ptx::tma_load_3d(sK + b * BOX_BYTES, &tmK, kv_full, b * 64, kb * BT, bh);
-          ptx::tma_load_3d(sV + b * BOX_BYTES, &tmV, kv_full, b * 64, kb * BT, bh);
-        }
+        ptx::mbar_arrive_expect_tx(kv_full, C::TILE + C::TILE_V);
+        for (int b = 0; b < C::KB; ++b) ptx::tma_load_3d(sK + b * BOX_BYTES, &tmK, kv_full, b * 64, kb * BT, bh);
+        for (int b = 0; b < C::KBV; ++b) ptx::tma_load_3d(sV + b * BOX_BYTES, &tmV, kv_full, b * 64, kb * BT, bh);
         for (int ii = 0; ii < nq; ++ii, ++q_it) {
           const int qs = qslot(q_it), os = oslot(q_it);
           const int qt = q0 + ii;
@@ -292,9 +294,9 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           ptx::bulk_load(sD + ls * BT, P.D + row0, BT * 4, l_full + ls);
           l_issued = q_it + 1;
           if (!(ok = ptx::mbar_wait(o_empty + os, opar(q_it) ^ 1u, w))) break;
-          ptx::mbar_arrive_expect_tx(o_full + os, C::TILE);
-          for (int b = 0; b < C::KB; ++b)
-            ptx::tma_load_3d(sdO + os * C::TILE + b * BOX_BYTES, &tmdO, o_full + os, b * 64, qt * BT, bh);
+          ptx::mbar_arrive_expect_tx(o_full + os, C::TILE_V);
+          for (int b = 0; b < C::KBV; ++b)
+            ptx::tma_load_3d(sdO + os * C::TILE_V + b * BOX_BYTES, &tmdO, o_full + os, b * 64, qt * BT, bh);
           o_issued = q_it + 1;
         }
         ++u_it;
@@ -331,8 +333,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       };
       auto mma_dpt = [&](uint32_t n) {   // dP^T = V dO^T for query tile n
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          ptx::mma_ss(tmem + T_DP, kmaj(aV, kk), kmaj(adO + oslot(n) * C::TILE, kk), C::IDESC_S, kk > 0);
+        for (int kk = 0; kk < HV / 16; ++kk)
+          ptx::mma_ss(tmem + T_DP, kmaj(aV, kk), kmaj(adO + oslot(n) * C::TILE_V, kk), C::IDESC_S, kk > 0);
       };
       auto wait = [&](uint64_t* bar, uint32_t parity) {
         return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, w));
@@ -387,8 +389,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
             moved |= lane != 0;
 #pragma unroll
             for (int kk = 0; kk < BT / 16; ++kk)
-              ptx::mma_ts(tmem + T_DV, tmem + T_ST + packed_col(kk), mnmaj(adO + oslot(it) * C::TILE, kk),
-                          C::IDESC_ACC, (ii > 0 || kk > 0) ? 1u : 0u);
+              ptx::mma_ts(tmem + T_DV, tmem + T_ST + packed_col(kk), mnmaj(adO + oslot(it) * C::TILE_V, kk),
+                          C::IDESC_DV, (ii > 0 || kk > 0) ? 1u : 0u);
             ptx::mma_commit(o_empty + oslot(it));
             if (more) {
               mma_st(it + 1);
@@ -406,7 +408,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < BT / 16; ++kk)
               ptx::mma_ts(tmem + T_DK, tmem + T_DP + packed_col(kk), mnmaj(aQ + qslot(it) * C::TILE, kk),
-                          C::IDESC_ACC, (ii > 0 || kk > 0) ? 1u : 0u);
+                          C::IDESC_DK, (ii > 0 || kk > 0) ? 1u : 0u);
             ptx::mma_commit(q_empty + qslot(it));
             if (ATOMIC_DQ) {
 #pragma unroll
@@ -635,13 +637,11 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       const int key = kb * BT + r;
       const bool key_ok = key < Tk;
       __nv_bfloat16* dk_row = P.dK + (static_cast<size_t>(bh) * Tk + (key_ok ? key : 0)) * HD;
-      __nv_bfloat16* dv_row = P.dV + (static_cast<size_t>(bh) * Tk + (key_ok ? key : 0)) * HD;
+      __nv_bfloat16* dv_row = P.dV + (static_cast<size_t>(bh) * Tk + (key_ok ? key : 0)) * HV;
       if (nq == 0) {
         if (key_ok) {
-          for (int c = 0; c < HD / 8; ++c) {
-            reinterpret_cast<uint4*>(dk_row)[c] = make_uint4(0, 0, 0, 0);
-            reinterpret_cast<uint4*>(dv_row)[c] = make_uint4(0, 0, 0, 0);
-          }
+          for (int c = 0; c < HD / 8; ++c) reinterpret_cast<uint4*>(dk_row)[c] = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < HV / 8; ++c) reinterpret_cast<uint4*>(dv_row)[c] = make_uint4(0, 0, 0, 0);
         }
         continue;
       }
@@ -696,7 +696,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         __nv_bfloat16* orow = acc ? dk_row : dv_row;
         const float mul = acc ? scale : 1.0f;
 #pragma unroll
-        for (int c = 0; c < HD / 32; c += 2) {
+        for (int c = 0; c < (acc ? HD : HV) / 32; c += 2) {
           uint32_t v[2][32];
           ptx::tmem_ld32(tcol + c * 32, v[0]);
           ptx::tmem_ld32(tcol + c * 32 + 32, v[1]);
@@ -735,21 +735,24 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
 
 // ---------------------------------------------------------------- deterministic dQ
 
-template <int HD>
+template <int HD, int HV>
 struct CfgQ {
-  static constexpr int KB = HD / 64;
-  static constexpr int TILE = BT * HD * 2;
+  static constexpr int KB = HD / 64;          // 64-column boxes per Q / K row
+  static constexpr int KBV = HV / 64;         // ... per V / dO row
+  static constexpr int TILE = BT * HD * 2;    // one 128-row Q or K tile
+  static constexpr int TILE_V = BT * HV * 2;  // one 128-row V or dO tile
   // K and V tiles have rings of their own. A K tile stays resident from its
   // S product to its dQ product one step later, a V tile only until its dP
-  // product, so K gets four slots and V one: a K tile then arrives about two
-  // key steps ahead of its first use, a V tile one.
-  static constexpr int NSK = (HD == 128) ? 4 : 8;
-  static constexpr int NSV = (HD == 128) ? 1 : 2;
+  // product, so at d = dv = 128 K gets four slots and V one: a K tile then
+  // arrives about two key steps ahead of its first use, a V tile one. The
+  // smaller tiles of d or dv = 64 leave room for more slots.
+  static constexpr int NSK = (HD == 64 && HV == 64) ? 8 : 4;
+  static constexpr int NSV = (HD == 128 && HV == 128) ? 1 : (HD == 64 && HV == 64) ? 2 : 3;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = OFF_Q + TILE;
-  static constexpr int OFF_K = OFF_DO + TILE;          // [NSK]
+  static constexpr int OFF_K = OFF_DO + TILE_V;        // [NSK]
   static constexpr int OFF_V = OFF_K + NSK * TILE;     // [NSV]
-  static constexpr int OFF_DPART = OFF_V + NSV * TILE;   // [2][128] fp32 partial D of the row groups
+  static constexpr int OFF_DPART = OFF_V + NSV * TILE_V;   // [2][128] fp32 partial D of the row groups
   static constexpr int OFF_BAR = OFF_DPART + 2 * BT * 4;
   // q_full, q_empty, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full, s_free, dp_full[2],
   // ds_full[2], dq_full, drain, dpart_full
@@ -772,12 +775,12 @@ constexpr int DQ_THREADS = 320;
 // TMEM: S [0, 128), dQ [128, 256), dP/dS in two buffers [256, 384) and
 // [384, 512) alternating by step, so the MMA warp computes dP of step j + 1
 // while the row threads still turn dP of step j into dS.
-template <int HD>
+template <int HD, int HV>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
               const Params P) {
-  using C = CfgQ<HD>;
+  using C = CfgQ<HD, HV>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -861,16 +864,14 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         int bh2, qt2;
         if (P.order.unit(cta, grid, round + 1, &bh2, &qt2)) {
           const int rows = min(BT, Tq - qt2 * BT);
-          ptx::bulk_prefetch_l2(P.O + (static_cast<size_t>(bh2) * Tq + static_cast<size_t>(qt2) * BT) * HD,
-                                static_cast<uint32_t>(rows) * HD * 2);
+          ptx::bulk_prefetch_l2(P.O + (static_cast<size_t>(bh2) * Tq + static_cast<size_t>(qt2) * BT) * HV,
+                                static_cast<uint32_t>(rows) * HV * 2);
         }
       }
       if (!(ok = ptx::mbar_wait(q_empty, (u_it & 1u) ^ 1u, w))) break;
-      ptx::mbar_arrive_expect_tx(q_full, 2 * C::TILE);
-      for (int b = 0; b < C::KB; ++b) {
-        ptx::tma_load_3d(sQ + b * BOX_BYTES, &tmQ, q_full, b * 64, qt * BT, bh);
-        ptx::tma_load_3d(sdO + b * BOX_BYTES, &tmdO, q_full, b * 64, qt * BT, bh);
-      }
+      ptx::mbar_arrive_expect_tx(q_full, C::TILE + C::TILE_V);
+      for (int b = 0; b < C::KB; ++b) ptx::tma_load_3d(sQ + b * BOX_BYTES, &tmQ, q_full, b * 64, qt * BT, bh);
+      for (int b = 0; b < C::KBV; ++b) ptx::tma_load_3d(sdO + b * BOX_BYTES, &tmdO, q_full, b * 64, qt * BT, bh);
       uint32_t k_issued = k_it, v_issued = k_it;   // tiles issued so far
       for (int j = 0; ok && j < nk; ++j, ++k_it) {
         const uint32_t t = k_it;
@@ -880,9 +881,9 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           ptx::tma_load_3d(sK + kslot(t) * C::TILE + b * BOX_BYTES, &tmK, k_full + kslot(t), b * 64, j * BT, bh);
         k_issued = t + 1;
         if (!(ok = ptx::mbar_wait(v_empty + vslot(t), vpar(t) ^ 1u, w))) break;
-        ptx::mbar_arrive_expect_tx(v_full + vslot(t), C::TILE);
-        for (int b = 0; b < C::KB; ++b)
-          ptx::tma_load_3d(sV + vslot(t) * C::TILE + b * BOX_BYTES, &tmV, v_full + vslot(t), b * 64, j * BT, bh);
+        ptx::mbar_arrive_expect_tx(v_full + vslot(t), C::TILE_V);
+        for (int b = 0; b < C::KBV; ++b)
+          ptx::tma_load_3d(sV + vslot(t) * C::TILE_V + b * BOX_BYTES, &tmV, v_full + vslot(t), b * 64, j * BT, bh);
         v_issued = t + 1;
       }
       if (!ok) {
@@ -921,8 +922,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     };
     auto mma_dp = [&](uint32_t t, uint32_t step) {   // dP = dO V^T into the step's buffer
 #pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk)
-        ptx::mma_ss(tmem + t_dp(step), kmaj(adO, kk), kmaj(aV + vslot(t) * C::TILE, kk), C::IDESC_S, kk > 0);
+      for (int kk = 0; kk < HV / 16; ++kk)
+        ptx::mma_ss(tmem + t_dp(step), kmaj(adO, kk), kmaj(aV + vslot(t) * C::TILE_V, kk), C::IDESC_S, kk > 0);
       ptx::mma_commit(dp_full + (step & 1u));
       ptx::mma_commit(v_empty + vslot(t));
     };
@@ -1031,12 +1032,12 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       // this row's O columns come in while the first S is computed; the
       // dot product and the exchange with the other group follow the first
       // step's exponentials (D is first needed for the first dS)
-      uint4 o4[HD / 16];
+      uint4 o4[HV / 16];
 #pragma unroll
-      for (int k = 0; k < HD / 16; ++k) {
+      for (int k = 0; k < HV / 16; ++k) {
         o4[k] = make_uint4(0u, 0u, 0u, 0u);
         if (q_ok)
-          o4[k] = *reinterpret_cast<const uint4*>(P.O + (static_cast<size_t>(bh) * Tq + q) * HD + (HD / 2) * g + 8 * k);
+          o4[k] = *reinterpret_cast<const uint4*>(P.O + (static_cast<size_t>(bh) * Tq + q) * HV + (HV / 2) * g + 8 * k);
       }
       const float lse = q_ok ? P.LSE[static_cast<size_t>(bh) * Tq + q] : -CUDART_INF_F;
       const float nlse2 = (lse == -CUDART_INF_F) ? -CUDART_INF_F : -lse * LOG2E;
@@ -1070,8 +1071,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(q_full, u_it & 1u, w)))) break;
           float part = 0.f;
 #pragma unroll
-          for (int k = 0; k < HD / 16; ++k) {
-            const uint4 d4 = *reinterpret_cast<const uint4*>(sdO + sw128_offset(r, (HD / 2) * g + 8 * k));
+          for (int k = 0; k < HV / 16; ++k) {
+            const uint4 d4 = *reinterpret_cast<const uint4*>(sdO + sw128_offset(r, (HV / 2) * g + 8 * k));
             const __nv_bfloat162* ov = reinterpret_cast<const __nv_bfloat162*>(&o4[k]);
             const __nv_bfloat162* dv = reinterpret_cast<const __nv_bfloat162*>(&d4);
 #pragma unroll
@@ -1166,7 +1167,7 @@ __global__ void convert_dq_kernel(const float4* __restrict__ acc, uint2* __restr
   }
 }
 
-template <int HD>
+template <int HD, int HV>
 cudaError_t launch(const LaunchBwd& a) {
   const Problem& p = a.p;
   const bool atomic = !a.deterministic;
@@ -1201,17 +1202,21 @@ cudaError_t launch(const LaunchBwd& a) {
     P.order = Order{P.n_q_tiles, heads, p.causal ? 1 : 0};
     const int units = P.n_q_tiles * heads;
     const int grid = units < a.num_sms ? units : a.num_sms;
-    e = cudaFuncSetAttribute(dq_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgQ<HD>::SMEM);
+    using CQ = CfgQ<HD, HV>;
+    static_assert(CQ::SMEM <= 227 * 1024, "shared memory");
+    e = cudaFuncSetAttribute(dq_kernel<HD, HV>, cudaFuncAttributeMaxDynamicSharedMemorySize, CQ::SMEM);
     if (e != cudaSuccess) return e;
-    dq_kernel<HD><<<grid, DQ_THREADS, CfgQ<HD>::SMEM, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO, P);
+    dq_kernel<HD, HV><<<grid, DQ_THREADS, CQ::SMEM, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO, P);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (main_kv) {
     P.order = Order{P.n_k_tiles, heads, p.causal ? 2 : 0};
     const int units = P.n_k_tiles * heads;
     const int grid = units < a.num_sms ? units : a.num_sms;
-    auto kern = atomic ? dkdv_kernel<HD, true> : dkdv_kernel<HD, false>;
-    const int smem = atomic ? CfgKV<HD, true>::SMEM : CfgKV<HD, false>::SMEM;
+    static_assert(CfgKV<HD, HV, true>::SMEM <= 227 * 1024 && CfgKV<HD, HV, false>::SMEM <= 227 * 1024,
+                  "shared memory");
+    auto kern = atomic ? dkdv_kernel<HD, HV, true> : dkdv_kernel<HD, HV, false>;
+    const int smem = atomic ? CfgKV<HD, HV, true>::SMEM : CfgKV<HD, HV, false>::SMEM;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // The register split must fit the launch allocation (see reg_acquire).
@@ -1238,8 +1243,8 @@ cudaError_t launch(const LaunchBwd& a) {
 }  // namespace bwd
 
 cudaError_t launch_bwd_bf16(const LaunchBwd& a) {
-  if (a.p.d == 128) return bwd::launch<128>(a);
-  return bwd::launch<64>(a);
+  if (a.p.d == 128) return a.p.dv == 128 ? bwd::launch<128, 128>(a) : bwd::launch<128, 64>(a);
+  return a.p.dv == 128 ? bwd::launch<64, 128>(a) : bwd::launch<64, 64>(a);
 }
 
 }  // namespace attn

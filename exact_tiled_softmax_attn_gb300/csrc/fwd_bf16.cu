@@ -52,24 +52,30 @@ constexpr int NUM_THREADS = 384;   // three warpgroups
 constexpr int REG_CTRL = 96;        // producer / MMA warpgroup
 constexpr int REG_SOFTMAX = 200;   // each softmax warpgroup
 
-template <int HD>
+// HD = d (Q and K rows), HV = dv (V and O rows); each 64 or 128.
+template <int HD, int HV>
 struct Cfg {
-  static constexpr int KB = HD / 64;                   // 64-column swizzle blocks per row
-  static constexpr int TILE = BM * HD * 2;             // bytes of one 128-row tile
+  static constexpr int KB = HD / 64;                   // 64-column swizzle blocks per Q / K row
+  static constexpr int KBV = HV / 64;                  // ... per V row
+  static constexpr int TILE = BM * HD * 2;             // bytes of one 128-row Q or K tile
+  static constexpr int TILE_V = BN * HV * 2;           // bytes of one 128-row V tile
+  static constexpr int SLOT = TILE > TILE_V ? TILE : TILE_V;
   // K and V tiles share one FIFO ring of tile-sized slots, loaded in the
-  // order they are consumed (K_0, V_0, K_1, V_1, ...). Five slots give every
-  // tile about two key steps of lead over its first use, which covers the
-  // ~2 us a TMA load of a tile takes under load.
-  static constexpr int NSLOT = (HD == 128) ? 5 : 10;
+  // order they are consumed (K_0, V_0, K_1, V_1, ...). Five 32 KB slots give
+  // every tile about two key steps of lead over its first use, which covers
+  // the ~2 us a TMA load of a tile takes under load; the ring takes what the
+  // two Q tiles leave of the shared memory, at most ten slots.
+  static constexpr int NSLOT_FIT = (227 * 1024 - 2 * TILE - 1024) / SLOT;
+  static constexpr int NSLOT = NSLOT_FIT < 10 ? NSLOT_FIT : 10;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = OFF_Q + 2 * TILE;
-  static constexpr int OFF_BAR = OFF_KV + NSLOT * TILE;
+  static constexpr int OFF_BAR = OFF_KV + NSLOT * SLOT;
   // barriers: q_full, q_empty, full[NSLOT], empty[NSLOT], s_full[2], p_full[2], o_full[2], drain
   static constexpr int NBAR = 2 + 2 * NSLOT + 7;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16(BM, BN, false, false);
-  static constexpr uint32_t IDESC_PV = ptx::idesc_bf16(BM, HD, false, true);
+  static constexpr uint32_t IDESC_PV = ptx::idesc_bf16(BM, HV, false, true);
 };
 
 struct Params {
@@ -121,11 +127,11 @@ __device__ __forceinline__ bool unit_tiles(const Params& P, int blk, int* qb, in
   return *n1 > 0;
 }
 
-template <int HD>
+template <int HD, int HV>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const Params P) {
-  using C = Cfg<HD>;
+  using C = Cfg<HD, HV>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -204,10 +210,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int sl = item % C::NSLOT;
           const uint32_t ph = (item / C::NSLOT) & 1u;
           if (!(ok = ptx::mbar_wait(kv_empty + sl, ph ^ 1u, w))) break;
-          ptx::mbar_arrive_expect_tx(kv_full + sl, C::TILE);
+          ptx::mbar_arrive_expect_tx(kv_full + sl, kv ? C::TILE_V : C::TILE);
           const CUtensorMap* map = kv ? &tmV : &tmK;
-          for (int b = 0; b < C::KB; ++b)
-            ptx::tma_load_3d(sKV + sl * C::TILE + b * BOX_BYTES, map, kv_full + sl, b * 64, (j0 + j) * BN, bh);
+          for (int b = 0; b < (kv ? C::KBV : C::KB); ++b)
+            ptx::tma_load_3d(sKV + sl * C::SLOT + b * BOX_BYTES, map, kv_full + sl, b * 64, (j0 + j) * BN, bh);
         }
       }
       ++u_it;
@@ -232,7 +238,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int kk = 0; kk < HD / 16; ++kk) {
         const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
         const uint64_t a = ptx::sdesc_advance(ptx::sdesc_sw128(sQa + t * C::TILE, 16, 1024), off);
-        const uint64_t b = ptx::sdesc_advance(ptx::sdesc_sw128(sKVa + sl * C::TILE, 16, 1024), off);
+        const uint64_t b = ptx::sdesc_advance(ptx::sdesc_sw128(sKVa + sl * C::SLOT, 16, 1024), off);
         ptx::mma_ss(d, a, b, C::IDESC_S, kk > 0 ? 1u : 0u);
       }
     };
@@ -241,7 +247,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t a = tmem + t * 256;  // P_t, bf16 pairs in the first 64 columns of S_t
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk) {
-        const uint64_t b = ptx::sdesc_advance(ptx::sdesc_sw128(sKVa + sl * C::TILE, BOX_BYTES, 1024), kk * 2048);
+        const uint64_t b = ptx::sdesc_advance(ptx::sdesc_sw128(sKVa + sl * C::SLOT, BOX_BYTES, 1024), kk * 2048);
         ptx::mma_ts(d, a + kk * 8, b, C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
       }
     };
@@ -417,7 +423,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // previous PV into O_t is complete: it was issued before the S
           // product whose completion s_full reported.
 #pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
+          for (int c = 0; c < HV / 32; ++c) {
             uint32_t o[32];
             ptx::tmem_ld32(tO + c * 32, o);
             ptx::tmem_ld_wait(o);
@@ -443,9 +449,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const size_t rows = static_cast<size_t>(P.p.B) * P.p.H * Tq;
         const size_t row = static_cast<size_t>(blk % P.n_splits) * rows + static_cast<size_t>(bh) * Tq +
                            (row_ok ? q_row : 0);
-        float* prow = P.Opart + row * HD;
+        float* prow = P.Opart + row * HV;
 #pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {
+        for (int c = 0; c < HV / 32; ++c) {
           uint32_t o[32];
           ptx::tmem_ld32(tO + c * 32, o);
           ptx::tmem_ld_wait(o);
@@ -461,9 +467,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::tc_fence_before();
         continue;
       }
-      __nv_bfloat16* orow = P.O + (static_cast<size_t>(bh) * Tq + (row_ok ? q_row : 0)) * HD;
+      __nv_bfloat16* orow = P.O + (static_cast<size_t>(bh) * Tq + (row_ok ? q_row : 0)) * HV;
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int c = 0; c < HV / 32; ++c) {
         uint32_t o[32];
         ptx::tmem_ld32(tO + c * 32, o);
         ptx::tmem_ld_wait(o);
@@ -490,9 +496,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <int HD>
+template <int HD, int HV>
 cudaError_t launch(const LaunchFwd& a) {
-  using C = Cfg<HD>;
+  using C = Cfg<HD, HV>;
+  static_assert(C::SMEM <= 227 * 1024, "shared memory");
   Params P;
   P.p = a.p;
   P.O = reinterpret_cast<__nv_bfloat16*>(a.O);
@@ -510,7 +517,7 @@ cudaError_t launch(const LaunchFwd& a) {
   if (static_cast<long long>(P.order.n_blocks) * P.order.n_heads > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int units = P.order.count();
   const int grid = units < a.num_sms ? units : a.num_sms;
-  auto kern = attn_fwd_bf16_kernel<HD>;
+  auto kern = attn_fwd_bf16_kernel<HD, HV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   // The register split must fit the launch allocation (see reg_acquire).
@@ -525,10 +532,8 @@ cudaError_t launch(const LaunchFwd& a) {
 }  // namespace fwd
 
 cudaError_t launch_fwd_bf16(const LaunchFwd& a) {
-  if (a.p.d == 128) return fwd::launch<128>(a);
-  return fwd::launch<64>(a);
+  if (a.p.d == 128) return a.p.dv == 128 ? fwd::launch<128, 128>(a) : fwd::launch<128, 64>(a);
+  return a.p.dv == 128 ? fwd::launch<64, 128>(a) : fwd::launch<64, 64>(a);
 }
-
-size_t fwd_bf16_smem_bytes(int d) { return d == 128 ? fwd::Cfg<128>::SMEM : fwd::Cfg<64>::SMEM; }
 
 }  // namespace attn

@@ -67,7 +67,6 @@ cudaError_t launch_bwd_f32(const LaunchBwd& a);
 // bf16 (tcgen05 / TMA)
 cudaError_t launch_fwd_bf16(const LaunchFwd& a);
 cudaError_t launch_bwd_bf16(const LaunchBwd& a);
-size_t fwd_bf16_smem_bytes(int d);
 
 // O, LSE from the split-KV partials (rows of query tile qt read the splits
 // that hold at least one of its key tiles)

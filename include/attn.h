@@ -35,7 +35,9 @@
  *
  * Supported shapes:
  *   ATTN_F32 : 1 <= d, dv <= 128, any B, H, Tq, Tk >= 0
- *   ATTN_BF16: d == dv, d in {64, 128}, any B, H, Tq, Tk >= 0
+ *   ATTN_BF16: d in {64, 128} and dv in {64, 128} (d != dv allowed: the
+ *              page's task takes V with its own head dimension), any B, H,
+ *              Tq, Tk >= 0
  * Zero-sized problems are valid: Tk == 0 gives O = 0 and LSE = -inf (a row
  * with no allowed key), and empty gradients are written as zeros.
  */

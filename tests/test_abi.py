@@ -66,7 +66,8 @@ def _fwd(**kw):
     (dict(causal=2), B.ATTN_ERR_INVALID_ARG),
     (dict(dtype=7), B.ATTN_ERR_INVALID_ARG),
     (dict(d=96, dv=96), B.ATTN_ERR_UNSUPPORTED),
-    (dict(d=64, dv=128), B.ATTN_ERR_UNSUPPORTED),
+    (dict(d=64, dv=96), B.ATTN_ERR_UNSUPPORTED),
+    (dict(d=256, dv=128), B.ATTN_ERR_UNSUPPORTED),
     (dict(dtype=B.ATTN_F32, d=129), B.ATTN_ERR_UNSUPPORTED),
     (dict(Q=None), B.ATTN_ERR_INVALID_ARG),
     (dict(LSE=None), B.ATTN_ERR_INVALID_ARG),

@@ -115,6 +115,24 @@ def test_bf16_ragged(shape, causal, deterministic):
     check_all(x, causal, 1 / math.sqrt(d), torch.bfloat16, deterministic)
 
 
+MIXED_DV_SHAPES = [  # B, H, Tq, Tk, d, dv
+    (1, 2, 300, 257, 64, 128),
+    (2, 1, 200, 700, 128, 64),
+    (1, 1, 640, 640, 64, 128),
+    (1, 1, 257, 1000, 128, 64),
+]
+
+
+@pytest.mark.parametrize("deterministic", [0, 1])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", MIXED_DV_SHAPES)
+def test_bf16_d_neq_dv(shape, causal, deterministic):
+    B, H, Tq, Tk, d, dv = shape
+    x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, dv), seed=Tq * 3 + Tk + dv, dtype=torch.bfloat16,
+                    device=DEV)
+    check_all(x, causal, 1 / math.sqrt(d), torch.bfloat16, deterministic)
+
+
 @pytest.mark.parametrize("deterministic", [0, 1])
 def test_bf16_c2_full_size(deterministic):
     w = WORKLOADS["c2"]

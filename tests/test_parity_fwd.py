@@ -95,6 +95,28 @@ BF16_SHAPES = [  # B, H, Tq, Tk, d
 ]
 
 
+MIXED_DV_SHAPES = [  # B, H, Tq, Tk, d, dv
+    (1, 2, 300, 257, 64, 128),
+    (2, 1, 200, 700, 128, 64),
+    (1, 1, 1024, 1024, 64, 128),
+    (1, 1, 129, 4000, 128, 64),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", MIXED_DV_SHAPES)
+def test_bf16_d_neq_dv(shape, causal):
+    B, H, Tq, Tk, d, dv = shape
+    x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, dv), seed=Tq + 5 * Tk + d, dtype=torch.bfloat16,
+                    device=DEV)
+    scale = 1 / math.sqrt(d)
+    o, lse = run_fwd(x, causal, scale)
+    assert o.shape == (B, H, Tq, dv)
+    O, L = oracle_fwd(x, causal, scale)
+    check_o(o, O, torch.bfloat16)
+    check_lse(lse, L, torch.bfloat16)
+
+
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("shape", BF16_SHAPES)
 def test_bf16_ragged_shapes(shape, causal):

@@ -109,6 +109,22 @@ def test_splitkv_matches_oracle(shape, causal):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", [(1, 2, 200, 3000, 64, 128, 5), (1, 1, 128, 5000, 128, 64, 0)])
+def test_splitkv_d_neq_dv(shape, causal):
+    Bn, H, Tq, Tk, d, dv, ns = shape
+    x = make_random((Bn, H, Tq, d), (Bn, H, Tk, d), (Bn, H, Tk, dv), seed=Tk + dv, dtype=torch.bfloat16,
+                    device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    o, lse = B.forward(x["Q"], x["K"], x["V"], causal=causal, scale=scale, num_splits=ns)
+    torch.cuda.synchronize()
+    assert B.attn_device_status() == B.ATTN_OK
+    O, L = ref.forward(x["Q"], x["K"], x["V"], scale, causal)
+    check_o(o, O, torch.bfloat16)
+    check_lse(lse, L, torch.bfloat16)
+
+
+@pytest.mark.gpu
 def test_splitkv_long_keys_sampled_rows():
     """B=1 H=4 Tq=256 Tk=65536, automatic split count: sampled query rows of
     two heads against the oracle, with and without the causal mask."""
