@@ -35,14 +35,15 @@ KERNEL_SOURCES = ("fwd_bf16.cu", "bwd_bf16.cu", "small.cu", "splitkv.cu", "ptx.c
 # ---------------------------------------------------------------- helpers
 
 def useful_flops_rows(w, rows):
-    """Useful fwd+bwd FLOPs of the given query rows: 4*d per (query, key) pair
-    forward and 2.5x that backward. Under the causal mask row i counts i + 1/2
-    keys, so that all Tq rows of a square problem sum to the halved full count
-    (the convention of the GPU metric)."""
+    """Useful fwd+bwd FLOPs of the given query rows: 2*(d + dv) per (query,
+    key) pair forward and 2*(3d + 2dv) backward (14 d per pair when d = dv).
+    Under the causal mask row i counts i + 1/2 keys, so that all Tq rows of a
+    square problem sum to the halved full count (the convention of the GPU
+    metric)."""
     import numpy as np
     rows = np.asarray(rows, dtype=np.float64)
     keys = np.minimum(rows + 0.5, w.Tk) if w.causal else np.full(rows.shape, float(w.Tk))
-    return 3.5 * 4.0 * w.d * float(keys.sum())
+    return (2.0 * (w.d + w.dv) + 2.0 * (3 * w.d + 2 * w.dv)) * float(keys.sum())
 
 
 def kernel_source_hash() -> str:
@@ -390,19 +391,20 @@ def run_ours(args, w):
 
     peaks = load_peaks()
     peak = peaks["bf16_tflops"]
-    # Algorithmic FLOP per kernel, in units of one causal matmul (F / 2): the
-    # forward does S and PV; the dK/dV kernel S, dP, dV, dK (and, atomic mode,
-    # dQ); the deterministic dQ kernel's own product is dQ (it recomputes S
-    # and dP, which is counted under "executed").
-    mm = F / 2
+    # Algorithmic FLOP per kernel: a product of depth d (S, dQ, dK) costs md,
+    # one of depth dv (PV, dP, dV) mv. The forward does S and PV; the dK/dV
+    # kernel S, dP, dV, dK (and, atomic mode, dQ); the deterministic dQ
+    # kernel's own product is dQ (it recomputes S and dP, which is counted
+    # under "executed").
+    md, mv = w.pair_flop() * w.d, w.pair_flop() * w.dv
     fwd_name = "fwd (attn_fwd_bf16_kernel)" if n_splits == 1 else \
         f"fwd split-KV, {n_splits} splits (attn_fwd_bf16_kernel + merge)"
     kernels = {fwd_name: {"ms": fwd_ms, "flop": F}}
     if det:
-        kernels["bwd dK/dV (dkdv_kernel)"] = {"ms": kv_ms, "flop": 4 * mm}
-        kernels["bwd dQ (dq_kernel)"] = {"ms": q_ms, "flop": mm, "executed_flop": 3 * mm}
+        kernels["bwd dK/dV (dkdv_kernel)"] = {"ms": kv_ms, "flop": 2 * md + 2 * mv}
+        kernels["bwd dQ (dq_kernel)"] = {"ms": q_ms, "flop": md, "executed_flop": 2 * md + mv}
     else:
-        kernels["bwd dK/dV + dQ atomics (dkdv_kernel)"] = {"ms": kv_ms, "flop": 5 * mm}
+        kernels["bwd dK/dV + dQ atomics (dkdv_kernel)"] = {"ms": kv_ms, "flop": 3 * md + 2 * mv}
     for k, v in kernels.items():
         v["tflops"] = v["flop"] / (v["ms"] * 1e-3) / 1e12
         v["frac_of_peak"] = v["tflops"] / peak

@@ -110,8 +110,9 @@ __device__ __forceinline__ void tile_counts(const Params& P, int qb, int* n0, in
 // Key tiles of work unit `blk`: query-tile pair qb, first key tile j0, and
 // n0 / n1 key tiles for its first / second query tile (n0 <= n1, possibly 0
 // for the first tile of a split). False when the unit has no key tile.
+template <bool SPLIT>
 __device__ __forceinline__ bool unit_tiles(const Params& P, int blk, int* qb, int* j0, int* n0, int* n1) {
-  if (P.n_splits <= 1) {
+  if (!SPLIT) {
     *qb = blk;
     *j0 = 0;
     tile_counts(P, blk, n0, n1);
@@ -127,7 +128,8 @@ __device__ __forceinline__ bool unit_tiles(const Params& P, int blk, int* qb, in
   return *n1 > 0;
 }
 
-template <int HD, int HV>
+// SPLIT: the split-KV variant (key ranges per unit, fp32 partial epilogue).
+template <int HD, int HV, bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const Params P) {
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int bh, blk;
     for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &blk); ++round) {
       int qb, j0, n0, n1;
-      if (!unit_tiles(P, blk, &qb, &j0, &n0, &n1)) continue;
+      if (!unit_tiles<SPLIT>(P, blk, &qb, &j0, &n0, &n1)) continue;
       if (!(ok = ptx::mbar_wait(q_empty, (u_it & 1u) ^ 1u, w))) break;
       ptx::mbar_arrive_expect_tx(q_full, 2 * C::TILE);
       for (int t = 0; t < 2; ++t)
@@ -262,14 +264,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int bh, blk;
     for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &blk); ++round) {
       int qb, j0, n0, n1;
-      if (!unit_tiles(P, blk, &qb, &j0, &n0, &n1)) continue;
+      if (!unit_tiles<SPLIT>(P, blk, &qb, &j0, &n0, &n1)) continue;
       if (!(ok = wait(q_full, u_it & 1u))) break;
       const uint32_t ik = 2 * kv_it;
       if (!(ok = wait(kv_full + slot(ik), par(ik)))) break;
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
         moved |= lane != 0;
-        if (n0 > 0) {   // (a split may hold no key tile for the first query tile)
+        if (!SPLIT || n0 > 0) {   // (a split may hold no key tile for the first query tile)
           mma_S(0, slot(ik));
           ptx::mma_commit(s_full + 0);
         }
@@ -351,9 +353,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int bh, blk;
     for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &blk); ++round) {
       int qb, j0, n0, n1;
-      if (!unit_tiles(P, blk, &qb, &j0, &n0, &n1)) continue;
+      if (!unit_tiles<SPLIT>(P, blk, &qb, &j0, &n0, &n1)) continue;
       const int nt = t ? n1 : n0;
-      if (nt == 0) continue;   // nothing to write: the merge reads no partial for these rows
+      if (SPLIT && nt == 0) continue;   // nothing to write: the merge reads no partial for these rows
       const int qt = 2 * qb + t;
       const int q_row = qt * BM + r;
       float m_used = -CUDART_INF_F, l = 0.f;
@@ -444,7 +446,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const float inv_l = (l > 0.f) ? 1.0f / l : 0.f;
       const bool row_ok = q_row < Tq;
       const float lse_row = (l > 0.f) ? (m_used + log2f(l)) * 0.69314718055994530942f : -CUDART_INF_F;
-      if (P.n_splits > 1) {
+      if (SPLIT) {
         // partial result of this split: O_s = A / l in fp32 and LSE_s
         const size_t rows = static_cast<size_t>(P.p.B) * P.p.H * Tq;
         const size_t row = static_cast<size_t>(blk % P.n_splits) * rows + static_cast<size_t>(bh) * Tq +
@@ -517,7 +519,7 @@ cudaError_t launch(const LaunchFwd& a) {
   if (static_cast<long long>(P.order.n_blocks) * P.order.n_heads > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int units = P.order.count();
   const int grid = units < a.num_sms ? units : a.num_sms;
-  auto kern = attn_fwd_bf16_kernel<HD, HV>;
+  auto kern = P.n_splits > 1 ? attn_fwd_bf16_kernel<HD, HV, true> : attn_fwd_bf16_kernel<HD, HV, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   // The register split must fit the launch allocation (see reg_acquire).

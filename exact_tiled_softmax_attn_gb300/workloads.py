@@ -23,6 +23,7 @@ c4     B2  H8  Tq=1000 Tk=4000 d=dv=128             f32    none    1/sqrt(128) 3
 c5     B1  H32 Tq=Tk=32768 d=dv=128                 bf16   causal  1/sqrt(128) 4
 s1     B1  H8  Tq=256 Tk=65536 d=dv=128             bf16   none    1/sqrt(128) 5
        (few query tiles, many keys: the split-KV forward's case)
+m1     B2  H16 Tq=Tk=4096  d=64 dv=128              bf16   causal  1/sqrt(64)  6
 =====  ===========================================  =====  ======  ==========  ====
 
 Draw order: one CPU ``torch.Generator`` seeded with the workload's seed
@@ -64,14 +65,22 @@ class Workload:
     def torch_dtype(self) -> torch.dtype:
         return {"f32": torch.float32, "bf16": torch.bfloat16}[self.dtype]
 
-    def fwd_flop(self) -> float:
-        """Useful attention FLOPs of one forward: 4*B*H*Tq*Tk*d, halved under causal."""
-        f = 4.0 * self.B * self.H * self.Tq * self.Tk * self.d
+    def pair_flop(self) -> float:
+        """2 * B*H*Tq*Tk, halved under causal: a contraction of depth k over all
+        allowed (query, key) pairs costs pair_flop() * k."""
+        f = 2.0 * self.B * self.H * self.Tq * self.Tk
         return f * 0.5 if self.causal else f
 
+    def fwd_flop(self) -> float:
+        """Useful attention FLOPs of one forward: S = Q K^T (depth d) and P V
+        (depth dv); 4*B*H*Tq*Tk*d when d = dv, halved under causal."""
+        return self.pair_flop() * (self.d + self.dv)
+
     def bwd_flop(self) -> float:
-        """Useful attention FLOPs of one backward: 2.5 x the forward count."""
-        return 2.5 * self.fwd_flop()
+        """Useful attention FLOPs of one backward: S (d), dP = dO V^T (dv),
+        dV = P^T dO (dv), dQ = dS K (d), dK = dS^T Q (d); 2.5 x the forward
+        count when d = dv."""
+        return self.pair_flop() * (3 * self.d + 2 * self.dv)
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -89,6 +98,8 @@ WORKLOADS: Dict[str, Workload] = {
     # few query tiles against many keys (8 query-tile pairs for 152 SMs): the
     # split-KV forward's case
     "s1": Workload("s1", 1, 8, 256, 65536, 128, 128, "bf16", False, 5),
+    # V with its own head dimension (d = 64, dv = 128)
+    "m1": Workload("m1", 2, 16, 4096, 4096, 64, 128, "bf16", True, 6),
 }
 
 
