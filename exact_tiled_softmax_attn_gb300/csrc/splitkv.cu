@@ -39,12 +39,16 @@ __global__ void __launch_bounds__(NT) merge_kernel(const float* __restrict__ Opa
     const int qt = q / 128;
     const int nt = causal ? min(qt + 1, n_kv_tiles) : n_kv_tiles;
     const int ns = min(n_splits, (nt + split_tiles - 1) / split_tiles);
+    // the loops over splits are unrolled so that several partial rows are in
+    // flight at once (the kernel is bound by load latency, not bandwidth)
     float mx = -CUDART_INF_F;
+#pragma unroll 4
     for (int s = 0; s < ns; ++s) mx = fmaxf(mx, LSEpart[static_cast<long long>(s) * rows + r]);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float lse = -CUDART_INF_F;
     if (mx != -CUDART_INF_F) {
       float wsum = 0.f;
+#pragma unroll 4
       for (int s = 0; s < ns; ++s) {
         const float ls = LSEpart[static_cast<long long>(s) * rows + r];
         const float wgt = expf(ls - mx);   // 0 for a split with no allowed key
