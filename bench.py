@@ -66,9 +66,11 @@ def load_peaks():
         with open(p) as f:
             j = json.load(f)
         return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
-                "bf16_tflops_sustained": j.get("bf16_tflops_sustained"), "source": "measured"}
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained"),
+                "sm_max_mhz": j.get("sm_max_mhz", 2070.0), "source": "measured"}
     except Exception:
-        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0,
+                "source": "fallback"}
 
 
 def load_traffic(kernel: str):
@@ -254,6 +256,7 @@ def run_ours(args, w):
     code = pkg.ATTN_BF16 if w.dtype == "bf16" else pkg.ATTN_F32
     B, H, Tq, Tk, d, dv = w.B, w.H, w.Tq, w.Tk, w.d, w.dv
     det = int(args.dq_mode == "deterministic")
+    es = 2 if w.dtype == "bf16" else 4   # bytes per input element
 
     host = make_inputs(w.with_(seed=w.seed + 1000 * rank))
     x = {k: v.to(dev) for k, v in host.items()}
@@ -404,14 +407,22 @@ def run_ours(args, w):
     # kernel's own product is dQ (it recomputes S and dP, which is counted
     # under "executed").
     md, mv = w.pair_flop() * w.d, w.pair_flop() * w.dv
-    fwd_name = "fwd (attn_fwd_bf16_kernel)" if n_splits == 1 else \
-        f"fwd split-KV, {n_splits} splits (attn_fwd_bf16_kernel + merge)"
+    f32 = w.dtype == "f32"
+    if f32:
+        # the CUDA-core path: FP32 FMA throughput (its scores accumulate in fp64)
+        props = torch.cuda.get_device_properties(dev)
+        peak = props.multi_processor_count * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    tag = "simt " if f32 else ""
+    if n_splits > 1:
+        fwd_name = f"fwd split-KV, {n_splits} splits (attn_fwd_bf16_kernel + merge)"
+    else:
+        fwd_name = "fwd (simt fwd_kernel)" if f32 else "fwd (attn_fwd_bf16_kernel)"
     kernels = {fwd_name: {"ms": fwd_ms, "flop": F}}
     if det:
-        kernels["bwd dK/dV (dkdv_kernel)"] = {"ms": kv_ms, "flop": 2 * md + 2 * mv}
-        kernels["bwd dQ (dq_kernel)"] = {"ms": q_ms, "flop": md, "executed_flop": 2 * md + mv}
+        kernels[f"bwd dK/dV ({tag}dkdv_kernel)"] = {"ms": kv_ms, "flop": 2 * md + 2 * mv}
+        kernels[f"bwd dQ ({tag}dq_kernel)"] = {"ms": q_ms, "flop": md, "executed_flop": 2 * md + mv}
     else:
-        kernels["bwd dK/dV + dQ atomics (dkdv_kernel)"] = {"ms": kv_ms, "flop": 3 * md + 2 * mv}
+        kernels[f"bwd dK/dV + dQ atomics ({tag}dkdv_kernel)"] = {"ms": kv_ms, "flop": 3 * md + 2 * mv}
     for k, v in kernels.items():
         v["tflops"] = v["flop"] / (v["ms"] * 1e-3) / 1e12
         v["frac_of_peak"] = v["tflops"] / peak
@@ -422,8 +433,10 @@ def run_ours(args, w):
         # reads O, dO, LSE; writes D and LSE*log2(e) (padded rows) and zeroes the dQ accumulator
         # atomic dQ only (bf16): the deterministic dQ kernel forms D itself
         "bwd preprocess": {"ms": pre_ms,
-                           "gbs": B * H * Tq * (2 * dv * 2 + 4 + 8 + d * 4) / (pre_ms * 1e-3) / 1e9 if not det else None},
-        "dQ convert": {"ms": conv_ms, "gbs": B * H * Tq * d * (4 + 2) / (conv_ms * 1e-3) / 1e9 if not det else None},
+                           "gbs": B * H * Tq * (2 * dv * es + 4 + 8 + (0 if det else d * 4)) / (pre_ms * 1e-3) / 1e9
+                           if (f32 or not det) else None},
+        "dQ convert": {"ms": conv_ms,
+                       "gbs": B * H * Tq * d * (4 + 2) / (conv_ms * 1e-3) / 1e9 if not (det or f32) else None},
     })
     kernels["bwd main (all main kernels)"]["frac_of_peak"] = kernels["bwd main (all main kernels)"]["tflops"] / peak
     if kernels["bwd preprocess"]["gbs"] is not None:
@@ -435,21 +448,26 @@ def run_ours(args, w):
     cfg = workload_config(w)
     cfg.update({"dq_mode": "deterministic" if det else "atomic", "fwd_splits": n_splits,
                 "fwd_tflops": F / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": Bf / (bwd_ms * 1e-3) / 1e12,
-                "fwd_bwd_frac_of_dense_bf16_peak": (F + Bf) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12 / peak,
-                "peak_source": f"{peaks['source']} bf16_tflops {peak}", "kernels": kernels})
+                "fwd_bwd_frac_of_peak": (F + Bf) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12 / peak,
+                "peak_source": f"derived FP32 FMA {peak:.1f}" if f32 else f"{peaks['source']} bf16_tflops {peak}",
+                "kernels": kernels})
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
-        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_note": f"{peaks['source']} dense bf16 burst (cuBLAS 8192^3)"},
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32" if f32 else "bf16", "data": "synthetic",
+        "config": cfg,
+        "roofline": {"bound": "alu" if f32 else "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "unit": UNIT, "frac": achieved / peak, "traffic": traffic,
+                     "peak_note": "FP32 FMA peak derived as SMs x 128 lanes x 2 FLOP x max SM clock"
+                     if f32 else f"{peaks['source']} dense bf16 burst (cuBLAS 8192^3)"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps,
                 "pipeline": "two buffer sets; step i+1 host-to-device and step i-1 device-to-host copies "
                             "overlap step i's kernels on separate streams"},
-        # fwd (+ split-KV merge), dQ, dK/dV | fwd (+ merge), preprocess, dK/dV, convert
-        "gpu_launches": args.steps * ((3 if det else 4) + (1 if n_splits > 1 else 0)),
+        # bf16: fwd (+ split-KV merge), dQ, dK/dV | fwd (+ merge), preprocess, dK/dV, convert
+        # fp32: fwd, preprocess, dK/dV, dQ | fwd, preprocess, dK/dV
+        "gpu_launches": args.steps * ((4 if det else 3) if f32 else
+                                      ((3 if det else 4) + (1 if n_splits > 1 else 0))),
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -5,12 +5,13 @@
 // sections "Gradient of V and P", "Gradient of S", "Gradient of Q and K"),
 // for fp32 inputs of any head size up to 128.
 //
-// Precision: a score s = scale * q.k is accumulated in fp64 from the fp32
-// inputs (each fp32 x fp32 product is exact in fp64), and s - m is formed in
-// fp64 before it is rounded to fp32 for exp. Accumulating s in fp32 instead
-// leaves a logit error of ~1e-5..1e-4 once |s| reaches the hundreds (keys
-// scaled by +-40), which the softmax turns into output errors above 1e-5.
-// Everything after the exponent (P, sums, P V, dP, dS, dQ, dK, dV) is fp32.
+// Precision: a score q.k is accumulated in twice the fp32 precision (the
+// compensated dot product below, fp32 instructions only) and held in fp64;
+// scale * q.k and s - m are formed in fp64 before rounding to fp32 for exp.
+// Accumulating s in plain fp32 instead leaves a logit error of ~1e-5..1e-4
+// once |s| reaches the hundreds (keys scaled by +-40), which the softmax turns
+// into output errors above 1e-5. Everything after the exponent (P, sums, P V,
+// dP, dS, dQ, dK, dV) is fp32.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include <stdint.h>
@@ -30,6 +31,29 @@ __device__ __forceinline__ double warp_max_d(double v) {
   for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
+// sum_k a_k b_k by the compensated dot product of Ogita, Rump and Oishi
+// ("Accurate Sum and Dot Product", SIAM J. Sci. Comput. 26(6), 2005,
+// algorithm Dot2): each product splits exactly into p + e with one FMA, and
+// the running sum is carried as s + c with Knuth's TwoSum, so the result is
+// as accurate as a dot product accumulated in twice the fp32 precision while
+// using only fp32 instructions (this GPU's fp64 rate is a small fraction of
+// its fp32 rate). The _rn intrinsics keep the compiler from contracting the
+// separate roundings the method relies on into FMAs. s + c is returned in
+// fp64, where it is exact.
+__device__ __forceinline__ double dot2(const float* a, const float* b, int n) {
+  float s = 0.f, c = 0.f;
+  for (int k = 0; k < n; ++k) {
+    const float p = __fmul_rn(a[k], b[k]);
+    const float e = __fmaf_rn(a[k], b[k], -p);   // a b - p, exactly
+    const float t = __fadd_rn(s, p);
+    const float z = __fsub_rn(t, s);
+    const float err = __fadd_rn(__fsub_rn(s, __fsub_rn(t, z)), __fsub_rn(p, z));   // s + p - t, exactly
+    s = t;
+    c = __fadd_rn(c, __fadd_rn(err, e));
+  }
+  return static_cast<double>(s) + static_cast<double>(c);
+}
+
 __device__ __forceinline__ float warp_sum_f(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -87,14 +111,11 @@ __global__ void __launch_bounds__(NT) fwd_kernel(const float* __restrict__ Q, co
     load_rows(sK, ldk, K + (bh * Tk + kv0) * d, BN, d, Tk - kv0);
     load_rows(sV, dv, V + (bh * Tk + kv0) * dv, BN, dv, Tk - kv0);
     __syncthreads();
-    // scores, fp64 accumulation of exact fp32 products
+    // scores, compensated (twice fp32 precision) accumulation
     for (int e = threadIdx.x; e < BM * BN; e += NT) {
       const int i = e / BN, j = e - i * BN;
       const int qi = q0 + i, kj = kv0 + j;
-      double s = 0.0;
-      const float* qr = sQ + i * ldk;
-      const float* kr = sK + j * ldk;
-      for (int c = 0; c < d; ++c) s = fma(static_cast<double>(qr[c]), static_cast<double>(kr[c]), s);
+      const double s = dot2(sQ + i * ldk, sK + j * ldk, d);
       const bool blocked = (kj >= Tk) || (p.causal && kj > qi);
       sS[i * (BN + 1) + j] = blocked ? -CUDART_INF : s * scale;
     }
@@ -203,10 +224,7 @@ __device__ __forceinline__ void tile_p_ds(const float* sQ, const float* sK, cons
     const bool blocked = (qi >= p.Tq) || (kj >= p.Tk) || (p.causal && kj > qi) || (sLse[i] == -CUDART_INF_F);
     float pij = 0.f, dsij = 0.f;
     if (!blocked) {
-      double s = 0.0;
-      const float* qr = sQ + i * (d + 1);
-      const float* kr = sK + j * (d + 1);
-      for (int c = 0; c < d; ++c) s = fma(static_cast<double>(qr[c]), static_cast<double>(kr[c]), s);
+      const double s = dot2(sQ + i * (d + 1), sK + j * (d + 1), d);
       pij = expf(static_cast<float>(s * static_cast<double>(p.scale) - static_cast<double>(sLse[i])));
       float dp = 0.f;
       const float* gr = sdO + i * (dv + 1);
