@@ -264,6 +264,7 @@ def run_ours(args, w):
     lse = torch.empty(B, H, Tq, dtype=torch.float32, device=dev)
     dq, dk, dvv = torch.empty_like(x["Q"]), torch.empty_like(x["K"]), torch.empty_like(x["V"])
     ws_bytes = pkg.attn_bwd_workspace_size(B, H, Tq, Tk, d, dv, code, det)
+    dq_splits = pkg.attn_bwd_dq_splits(B, H, Tq, Tk, d, dv, code, det)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -435,8 +436,10 @@ def run_ours(args, w):
         "bwd preprocess": {"ms": pre_ms,
                            "gbs": B * H * Tq * (2 * dv * es + 4 + 8 + (0 if det else d * 4)) / (pre_ms * 1e-3) / 1e9
                            if (f32 or not det) else None},
+        # atomic: fp32 accumulator -> bf16; deterministic with split dQ: the partials' sum -> bf16
         "dQ convert": {"ms": conv_ms,
-                       "gbs": B * H * Tq * d * (4 + 2) / (conv_ms * 1e-3) / 1e9 if not (det or f32) else None},
+                       "gbs": B * H * Tq * d * (4 * (1 if not det else dq_splits) + 2) / (conv_ms * 1e-3) / 1e9
+                       if not f32 and (not det or dq_splits > 1) else None},
     })
     kernels["bwd main (all main kernels)"]["frac_of_peak"] = kernels["bwd main (all main kernels)"]["tflops"] / peak
     if kernels["bwd preprocess"]["gbs"] is not None:
@@ -446,7 +449,7 @@ def run_ours(args, w):
     achieved = kernels[dom]["tflops"]
     traffic = load_traffic(dom.split("(")[-1].rstrip(")"))
     cfg = workload_config(w)
-    cfg.update({"dq_mode": "deterministic" if det else "atomic", "fwd_splits": n_splits,
+    cfg.update({"dq_mode": "deterministic" if det else "atomic", "fwd_splits": n_splits, "dq_splits": dq_splits,
                 "fwd_tflops": F / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": Bf / (bwd_ms * 1e-3) / 1e12,
                 "fwd_bwd_frac_of_peak": (F + Bf) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12 / peak,
                 "peak_source": f"derived FP32 FMA {peak:.1f}" if f32 else f"{peaks['source']} bf16_tflops {peak}",
@@ -464,10 +467,11 @@ def run_ours(args, w):
                 "steps": e2e_steps,
                 "pipeline": "two buffer sets; step i+1 host-to-device and step i-1 device-to-host copies "
                             "overlap step i's kernels on separate streams"},
-        # bf16: fwd (+ split-KV merge), dQ, dK/dV | fwd (+ merge), preprocess, dK/dV, convert
-        # fp32: fwd, preprocess, dK/dV, dQ | fwd, preprocess, dK/dV
+        # bf16: fwd (+ split-KV merge), dQ (+ split reduction), dK/dV | fwd (+ merge), preprocess,
+        # dK/dV, convert; fp32: fwd, preprocess, dK/dV, dQ | fwd, preprocess, dK/dV
         "gpu_launches": args.steps * ((4 if det else 3) if f32 else
-                                      ((3 if det else 4) + (1 if n_splits > 1 else 0))),
+                                      ((3 if det else 4) + (1 if n_splits > 1 else 0) +
+                                       (1 if det and dq_splits > 1 else 0))),
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:

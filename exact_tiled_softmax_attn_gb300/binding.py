@@ -23,7 +23,7 @@ __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED", "ATTN_ERR_CUDA",
     "ATTN_ERR_TIMEOUT", "ATTN_ERR_WORKSPACE", "ATTN_F32", "ATTN_BF16",
     "attn_fwd", "attn_fwd_f32_blocked", "attn_fwd_splitkv", "attn_fwd_splitkv_splits",
-    "attn_fwd_splitkv_workspace_size", "attn_bwd", "attn_bwd_phase", "attn_bwd_workspace_size",
+    "attn_fwd_splitkv_workspace_size", "attn_bwd", "attn_bwd_phase", "attn_bwd_workspace_size", "attn_bwd_dq_splits",
     "attn_bwd_noalloc", "ATTN_NOALLOC_SCRATCH_BYTES", "attn_online_softmax_step", "attn_device_status",
     "attn_selftest_wait_timeout", "attn_strerror", "attn_last_cuda_error", "attn_version",
     "forward", "backward",
@@ -45,6 +45,7 @@ _SIGNATURES = {
     "attn_fwd_splitkv_splits": (_I, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "attn_fwd_splitkv_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "attn_bwd_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
+    "attn_bwd_dq_splits": (_I, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _SZ, _P]),
     "attn_bwd_phase": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _SZ,
                             _I, _P]),
@@ -175,6 +176,10 @@ def attn_online_softmax_step(m, l, acc, scores, v_block, n, bs, dv, stream=None,
 
 def attn_bwd_workspace_size(B, H, Tq, Tk, d, dv, dtype, deterministic) -> int:
     return load_library().attn_bwd_workspace_size(B, H, Tq, Tk, d, dv, int(dtype), int(deterministic))
+
+
+def attn_bwd_dq_splits(B, H, Tq, Tk, d, dv, dtype, deterministic) -> int:
+    return load_library().attn_bwd_dq_splits(B, H, Tq, Tk, d, dv, int(dtype), int(deterministic))
 
 
 def attn_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, B, H, Tq, Tk, d, dv, scale, causal, dtype, deterministic,

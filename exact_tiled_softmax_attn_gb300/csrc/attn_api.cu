@@ -135,17 +135,46 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct BwdLayout {
   size_t lse2_off, d_off, acc_off, acc_bytes, total;
+  int dq_splits, dq_split_tiles;   // split deterministic dQ (bf16): acc holds the partials
 };
+// The deterministic bf16 dQ kernel runs one unit per 128-row query tile; when
+// a problem has few query tiles against many key tiles (fewer units than
+// half a GB300's 152 SMs, at least 8 key tiles), each query tile's keys are
+// split into ranges so that at most 152 units run (one wave), each with at
+// least 4 key tiles; at most 64 splits. A rule of the shapes only, so the workspace size
+// needs no device.
+constexpr int kDqSplitTargetUnits = 152;
+void dq_split_count(int B, int H, int Tq, int Tk, attn_dtype_t dt, int deterministic, int* S, int* cs) {
+  const long long units = static_cast<long long>(B) * H * ((Tq + 127) / 128);
+  const int nkt = (Tk + 127) / 128;
+  *S = 1;
+  *cs = nkt;
+  if (dt != ATTN_BF16 || !deterministic || units == 0 || units >= kDqSplitTargetUnits / 2 || nkt < 8) return;
+  long long want = kDqSplitTargetUnits / units;   // one wave: units * S <= 152
+  if (want > nkt / 4) want = nkt / 4;
+  if (want > 64) want = 64;
+  if (want < 2) return;
+  *cs = (nkt + static_cast<int>(want) - 1) / static_cast<int>(want);
+  *S = (nkt + *cs - 1) / *cs;
+  if (*S < 2) {
+    *S = 1;
+    *cs = nkt;
+  }
+}
+
 // Workspace: NLSE2 [B*H, Tq_pad] fp32 | D [B*H, Tq_pad] fp32 | (bf16 with fp32
-// dQ accumulation) dQacc [B*H*Tq, d] fp32; each part 256-byte aligned.
-BwdLayout bwd_layout(int B, int H, int Tq, int d, attn_dtype_t dt, int deterministic) {
+// dQ accumulation) dQacc [B*H*Tq, d] fp32, or (bf16 deterministic with split
+// dQ) the partials [S][B*H*Tq, d] fp32; each part 256-byte aligned.
+BwdLayout bwd_layout(int B, int H, int Tq, int Tk, int d, attn_dtype_t dt, int deterministic) {
   BwdLayout L{};
   const size_t rows_pad = static_cast<size_t>(B) * H * padded_rows(Tq);
   const size_t part = round_up(rows_pad * sizeof(float), 256);
+  dq_split_count(B, H, Tq, Tk, dt, deterministic, &L.dq_splits, &L.dq_split_tiles);
   L.lse2_off = 0;
   L.d_off = part;
   L.acc_off = 2 * part;
-  L.acc_bytes = (dt == ATTN_BF16 && !deterministic) ? static_cast<size_t>(B) * H * Tq * d * sizeof(float) : 0;
+  const size_t acc = static_cast<size_t>(B) * H * Tq * d * sizeof(float);
+  L.acc_bytes = (dt == ATTN_BF16 && !deterministic) ? acc : (L.dq_splits > 1 ? L.dq_splits * acc : 0);
   L.total = rows_pad ? L.acc_off + L.acc_bytes : 0;
   return L;
 }
@@ -334,7 +363,13 @@ attn_status_t attn_fwd_f32_blocked(const float* Q, const float* K, const float* 
 size_t attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype,
                                int deterministic) {
   if (check_common(B, H, Tq, Tk, d, dv, 1.0f, 0, dtype) != ATTN_OK) return 0;
-  return bwd_layout(B, H, Tq, d, dtype, deterministic).total;
+  return bwd_layout(B, H, Tq, Tk, d, dtype, deterministic).total;
+}
+
+int attn_bwd_dq_splits(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype, int deterministic) {
+  if (check_common(B, H, Tq, Tk, d, dv, 1.0f, 0, dtype) != ATTN_OK) return -1;
+  if (deterministic != 0 && deterministic != 1) return -1;
+  return bwd_layout(B, H, Tq, Tk, d, dtype, deterministic).dq_splits;
 }
 
 }  // extern "C"
@@ -362,7 +397,7 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
   const size_t out_bytes[3] = {bq, bk, bv};
   for (int i = 0; i < 3; ++i)
     if ((s = check_ptr(outs[i], out_bytes[i], align)) != ATTN_OK) return s;
-  const BwdLayout L = bwd_layout(B, H, Tq, d, dtype, deterministic);
+  const BwdLayout L = bwd_layout(B, H, Tq, Tk, d, dtype, deterministic);
   if (L.total > 0) {
     if (workspace == nullptr || workspace_bytes < L.total || reinterpret_cast<uintptr_t>(workspace) % 256)
       return ATTN_ERR_WORKSPACE;
@@ -401,7 +436,11 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
   a.dV = dV;
   a.D = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.d_off);
   a.NLSE2 = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.lse2_off);
-  a.dQacc = L.acc_bytes ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.acc_off) : nullptr;
+  float* acc = L.acc_bytes ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + L.acc_off) : nullptr;
+  a.dQacc = deterministic ? nullptr : acc;
+  a.dq_splits = L.dq_splits;
+  a.dq_split_tiles = L.dq_split_tiles;
+  a.dQpart = L.dq_splits > 1 ? acc : nullptr;
   a.deterministic = deterministic;
   a.phase = phase;
   a.status = di->status;

@@ -94,6 +94,12 @@ struct Params {
   int Tq_pad;
   float* dQacc;            // atomic path: fp32 [BH, Tq, d], pre-zeroed
   __nv_bfloat16* dQ;       // deterministic path output
+  // deterministic dQ kernel split over key ranges (dq_splits > 1): split s of
+  // a query tile covers key tiles [s * dq_split_tiles, (s + 1) * dq_split_tiles)
+  // and writes scale * its partial dQ (fp32) to dQpart [dq_splits][BH*Tq][d];
+  // a reduction adds the splits in order
+  int dq_splits, dq_split_tiles;
+  float* dQpart;
   __nv_bfloat16* dK;
   __nv_bfloat16* dV;
   uint32_t* status;
@@ -107,6 +113,19 @@ __device__ __forceinline__ void q_range(const Params& P, int kb, int* first, int
   const int f = P.p.causal ? kb : 0;
   *first = f;
   *count = P.n_q_tiles > f ? P.n_q_tiles - f : 0;
+}
+
+// Deterministic dQ unit `blk` of a head: query tile qt, key split s, first key
+// tile j0 and key tile count nk (0 when the split lies past the tile's keys).
+template <bool SPLIT>
+__device__ __forceinline__ bool dq_unit(const Params& P, int blk, int* qt, int* s, int* j0, int* nk) {
+  const int S = SPLIT ? P.dq_splits : 1;
+  *qt = SPLIT ? blk / S : blk;
+  *s = SPLIT ? blk - *qt * S : 0;
+  const int n = P.p.causal ? min(*qt + 1, P.n_k_tiles) : P.n_k_tiles;
+  *j0 = SPLIT ? *s * P.dq_split_tiles : 0;
+  *nk = SPLIT ? max(0, min(n - *j0, P.dq_split_tiles)) : n;
+  return *nk > 0;
 }
 
 // Byte offset of element (row, col) inside a 128-row tile stored as 64-column
@@ -775,7 +794,8 @@ constexpr int DQ_THREADS = 320;
 // TMEM: S [0, 128), dQ [128, 256), dP/dS in two buffers [256, 384) and
 // [384, 512) alternating by step, so the MMA warp computes dP of step j + 1
 // while the row threads still turn dP of step j into dS.
-template <int HD, int HV>
+// SPLIT: key ranges per unit, fp32 partial dQ (see Params).
+template <int HD, int HV, bool SPLIT>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -844,7 +864,6 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   auto t_dp = [](uint32_t step) { return 256u + 128u * (step & 1u); };   // dP / dS buffer of a step
   const int grid = gridDim.x, cta = blockIdx.x;
   const int Tq = P.p.Tq, Tk = P.p.Tk;
-  auto nk_of = [&](int qt) { return P.p.causal ? min(qt + 1, P.n_k_tiles) : P.n_k_tiles; };
   // Key tile j of a unit is the CTA's tile number t = k_it + j (k_it runs
   // across units); its K sits in K slot t % NSK, its V in V slot t % NSV.
   auto kslot = [](uint32_t t) { return static_cast<int>(t % C::NSK); };
@@ -856,13 +875,15 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     ptx::WaitCtx w{abort_flag, P.status, 5u};
     uint32_t u_it = 0, k_it = 0;
     bool ok = true;
-    int bh, qt;
-    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qt); ++round) {
-      const int nk = nk_of(qt);
+    int bh, blk;
+    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &blk); ++round) {
+      int qt, sp_, j0, nk;
+      if (!dq_unit<SPLIT>(P, blk, &qt, &sp_, &j0, &nk)) continue;
       {
         // the next unit's O rows (its D) into L2 while this unit runs
-        int bh2, qt2;
-        if (P.order.unit(cta, grid, round + 1, &bh2, &qt2)) {
+        int bh2, blk2;
+        if (P.order.unit(cta, grid, round + 1, &bh2, &blk2)) {
+          const int qt2 = SPLIT ? blk2 / P.dq_splits : blk2;
           const int rows = min(BT, Tq - qt2 * BT);
           ptx::bulk_prefetch_l2(P.O + (static_cast<size_t>(bh2) * Tq + static_cast<size_t>(qt2) * BT) * HV,
                                 static_cast<uint32_t>(rows) * HV * 2);
@@ -878,12 +899,13 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         if (!(ok = ptx::mbar_wait(k_empty + kslot(t), kpar(t) ^ 1u, w))) break;
         ptx::mbar_arrive_expect_tx(k_full + kslot(t), C::TILE);
         for (int b = 0; b < C::KB; ++b)
-          ptx::tma_load_3d(sK + kslot(t) * C::TILE + b * BOX_BYTES, &tmK, k_full + kslot(t), b * 64, j * BT, bh);
+          ptx::tma_load_3d(sK + kslot(t) * C::TILE + b * BOX_BYTES, &tmK, k_full + kslot(t), b * 64, (j0 + j) * BT, bh);
         k_issued = t + 1;
         if (!(ok = ptx::mbar_wait(v_empty + vslot(t), vpar(t) ^ 1u, w))) break;
         ptx::mbar_arrive_expect_tx(v_full + vslot(t), C::TILE_V);
         for (int b = 0; b < C::KBV; ++b)
-          ptx::tma_load_3d(sV + vslot(t) * C::TILE_V + b * BOX_BYTES, &tmV, v_full + vslot(t), b * 64, j * BT, bh);
+          ptx::tma_load_3d(sV + vslot(t) * C::TILE_V + b * BOX_BYTES, &tmV, v_full + vslot(t), b * 64, (j0 + j) * BT,
+                           bh);
         v_issued = t + 1;
       }
       if (!ok) {
@@ -914,7 +936,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     };
     uint32_t u_it = 0, k_it = 0, sp = 0;
     bool ok = true, moved = false;
-    int bh, qt;
+    int bh, blk;
     auto mma_s = [&](uint32_t t) {   // S = Q K^T with key tile t
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk)
@@ -927,8 +949,9 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       ptx::mma_commit(dp_full + (step & 1u));
       ptx::mma_commit(v_empty + vslot(t));
     };
-    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qt); ++round) {
-      const int nk = nk_of(qt);
+    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &blk); ++round) {
+      int qt, sp_, j0, nk;
+      if (!dq_unit<SPLIT>(P, blk, &qt, &sp_, &j0, &nk)) continue;
       if (!(ok = wait(q_full, u_it & 1u))) break;
       // S and dP of the first key tile
       {
@@ -1020,9 +1043,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     const float sc2 = P.sc2, scale = P.p.scale;
     uint32_t u_it = 0, sp = 0;
     bool ok = true;
-    int bh, qt;
-    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qt); ++round) {
-      const int nk = nk_of(qt);
+    int bh, blk;
+    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &blk); ++round) {
+      int qt, split, j0, nk;
+      if (!dq_unit<SPLIT>(P, blk, &qt, &split, &j0, &nk)) continue;
       const int q = qt * BT + r;
       const bool q_ok = q < Tq;
       // D_q = sum_c dO_qc O_qc ("attention_backprop", section "Gradient of
@@ -1086,12 +1110,12 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           ptx::mbar_arrive(dpart_full);
           if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dpart_full, u_it & 1u, w)))) break;
           dd = dpart[r] + dpart[BT + r];
-          if (g == 0) {
+          if (g == 0 && split == 0) {   // (every split forms the same D)
             P.D[static_cast<size_t>(bh) * P.Tq_pad + q] = dd;
             P.NLSE2[static_cast<size_t>(bh) * P.Tq_pad + q] = nlse2;
           }
         }
-        const int kv0 = j * BT + 64 * g;         // key of this thread's first column
+        const int kv0 = (j0 + j) * BT + 64 * g;  // key of this thread's first column
         if (kv0 + 64 > Tk || (P.p.causal && kv0 + 63 > q)) {
           const int lim = min(Tk - kv0, P.p.causal ? q - kv0 + 1 : 64);   // columns [0, lim) allowed
 #pragma unroll
@@ -1127,6 +1151,27 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dq_full, u_it & 1u, w)))) break;
       ptx::tc_fence_after();
       // this group writes dQ columns [g HD / 2, (g + 1) HD / 2) of its row
+      if (SPLIT) {
+        const size_t rows = static_cast<size_t>(P.p.B) * P.p.H * Tq;
+        float* prow = P.dQpart + (static_cast<size_t>(split) * rows + static_cast<size_t>(bh) * Tq + (q_ok ? q : 0)) *
+                                     HD + (HD / 2) * g;
+#pragma unroll
+        for (int c = 0; c < HD / 64; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld32(tDQ + c * 32, v);
+          ptx::tmem_ld_wait(v);
+          if (q_ok) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              reinterpret_cast<float4*>(prow + c * 32)[e] =
+                  make_float4(__uint_as_float(v[4 * e]) * scale, __uint_as_float(v[4 * e + 1]) * scale,
+                              __uint_as_float(v[4 * e + 2]) * scale, __uint_as_float(v[4 * e + 3]) * scale);
+          }
+        }
+        ptx::tc_fence_before();
+        ++u_it;
+        continue;
+      }
       __nv_bfloat16* row = P.dQ + (static_cast<size_t>(bh) * Tq + (q_ok ? q : 0)) * HD + (HD / 2) * g;
 #pragma unroll
       for (int c = 0; c < HD / 64; ++c) {
@@ -1155,6 +1200,30 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// dQ (bf16) = the sum of the split dQ kernel's partials (fp32, already
+// scaled) in split order, over the splits that hold key tiles of the row's
+// query tile; one thread per 4 columns of a row.
+__global__ void reduce_dq_kernel(const float* __restrict__ part, uint2* __restrict__ out, long long rows, int Tq,
+                                 int d, int n_splits, int split_tiles, int n_k_tiles, int causal) {
+  const long long n4 = rows * (d / 4);
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const long long r = i / (d / 4);
+    const int qt = static_cast<int>(r % Tq) / BT;
+    const int nt = causal ? min(qt + 1, n_k_tiles) : n_k_tiles;
+    const int ns = min(n_splits, (nt + split_tiles - 1) / split_tiles);
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < ns; ++s) {
+      const float4 v = reinterpret_cast<const float4*>(part)[static_cast<long long>(s) * n4 + i];
+      a.x += v.x;
+      a.y += v.y;
+      a.z += v.z;
+      a.w += v.w;
+    }
+    out[i] = make_uint2(ptx::pack_bf16(a.x, a.y), ptx::pack_bf16(a.z, a.w));
   }
 }
 
@@ -1198,15 +1267,21 @@ cudaError_t launch(const LaunchBwd& a) {
   P.n_k_tiles = (p.Tk + BT - 1) / BT;
   P.sc2 = p.scale * LOG2E;
   const int heads = p.B * p.H;
+  const bool split_dq = !atomic && a.dq_splits > 1;
+  P.dq_splits = split_dq ? a.dq_splits : 1;
+  P.dq_split_tiles = split_dq ? a.dq_split_tiles : P.n_k_tiles;
+  P.dQpart = a.dQpart;
   if (!atomic && main_q) {
-    P.order = Order{P.n_q_tiles, heads, p.causal ? 1 : 0};
-    const int units = P.n_q_tiles * heads;
+    P.order = Order{P.n_q_tiles * P.dq_splits, heads, p.causal ? 1 : 0};
+    if (static_cast<long long>(P.n_q_tiles) * P.dq_splits * heads > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const int units = P.n_q_tiles * P.dq_splits * heads;
     const int grid = units < a.num_sms ? units : a.num_sms;
     using CQ = CfgQ<HD, HV>;
     static_assert(CQ::SMEM <= 227 * 1024, "shared memory");
-    e = cudaFuncSetAttribute(dq_kernel<HD, HV>, cudaFuncAttributeMaxDynamicSharedMemorySize, CQ::SMEM);
+    auto kern = split_dq ? dq_kernel<HD, HV, true> : dq_kernel<HD, HV, false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CQ::SMEM);
     if (e != cudaSuccess) return e;
-    dq_kernel<HD, HV><<<grid, DQ_THREADS, CQ::SMEM, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO, P);
+    kern<<<grid, DQ_THREADS, CQ::SMEM, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO, P);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (main_kv) {
@@ -1229,6 +1304,12 @@ cudaError_t launch(const LaunchBwd& a) {
     kern<<<grid, KV_THREADS, smem, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO,
                                                            atomic ? *a.tmdQacc : *a.tmQ, P);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (split_dq && conv) {
+    const long long rows = static_cast<long long>(heads) * p.Tq;
+    reduce_dq_kernel<<<a.num_sms * 8, 256, 0, a.stream>>>(a.dQpart, static_cast<uint2*>(a.dQ), rows, p.Tq, p.d,
+                                                          P.dq_splits, P.dq_split_tiles, P.n_k_tiles, p.causal);
+    return cudaGetLastError();
   }
   if (atomic) {
     if (!conv) return cudaSuccess;

@@ -52,8 +52,14 @@ struct LaunchBwd {
   float* D;                 // [B*H, Tq_pad] workspace, Tq_pad = Tq rounded up to 128
   float* NLSE2;             // [B*H, Tq_pad] workspace: -LSE * log2(e), -inf for padding / no-key rows
   float* dQacc;             // [B,H,Tq,d] fp32 workspace (bf16 atomic path), else null
+  // bf16 deterministic path with few query tiles: the dQ kernel splits each
+  // query tile's keys into dq_splits ranges of dq_split_tiles tiles, writes
+  // fp32 partials to dQpart [dq_splits][B*H*Tq][d], and phase 3 adds them
+  int dq_splits;
+  int dq_split_tiles;
+  float* dQpart;
   int deterministic;
-  int phase;                // 0 all; 1 preprocess; 2 main kernels (5 then 4); 3 dQ conversion;
+  int phase;                // 0 all; 1 preprocess; 2 main kernels (5 then 4); 3 dQ conversion / split reduction;
                             // 4 dK/dV kernel; 5 deterministic dQ kernel
   uint32_t* status;
   int num_sms;

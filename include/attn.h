@@ -139,11 +139,25 @@ ATTN_API size_t attn_fwd_splitkv_workspace_size(int B, int H, int Tq, int Tk, in
  * Bytes of device workspace attn_bwd needs for this problem (0 is possible).
  * Holds -LSE * log2(e) and D = rowsum(dO o O), each [B*H, Tq_pad] fp32 with
  * Tq_pad = Tq rounded up to a multiple of 128, and, for bf16 with
- * deterministic == 0, the fp32 dQ accumulator [B,H,Tq,d]; each part starts on
- * a 256-byte boundary. Returns 0 for invalid arguments as well.
+ * deterministic == 0, the fp32 dQ accumulator [B,H,Tq,d], or, for bf16 with
+ * deterministic == 1 and S = attn_bwd_dq_splits(...) > 1, S fp32 partial dQ
+ * arrays [S][B,H,Tq,d]; each part starts on a 256-byte boundary. Returns 0
+ * for invalid arguments as well.
  */
 ATTN_API size_t attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype,
                                int deterministic);
+
+/*
+ * Number of key splits S the deterministic bf16 backward uses for dQ (1 when
+ * it does not split; -1 for invalid arguments). The dQ kernel runs one unit
+ * per 128-row query tile; when there are fewer such units than 76 (half of a
+ * GB300's 152 SMs) and at least 8 key tiles, each query tile's keys are cut
+ * into S ranges (at most 152 units in all, at least 4 key tiles each, S <= 64)
+ * whose partial dQ go to the workspace and are then added in split order, so
+ * the result stays bitwise reproducible. A rule of the shapes only.
+ */
+ATTN_API int attn_bwd_dq_splits(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype,
+                                int deterministic);
 
 /*
  * Backward pass: dQ, dK, dV from Q, K, V, the forward's O and LSE, and dO.

@@ -93,6 +93,24 @@ def test_blocked_forward_validates_block(lib):
     assert st == B.ATTN_ERR_UNSUPPORTED
 
 
+@pytest.mark.parametrize("shape,det,want", [
+    ((2, 16, 8192, 8192, 128), 1, 1),    # 2048 query tiles: no split
+    ((1, 2, 128, 4096, 128), 1, 8),      # 2 query tiles, 32 key tiles: 8 splits of 4
+    ((1, 2, 128, 4096, 128), 0, 1),      # atomic dQ never splits
+    ((1, 8, 256, 65536, 128), 1, 9),     # 16 query tiles: 144 units, one wave
+    ((1, 1, 256, 3000, 64), 1, 6),       # 24 key tiles: at least 4 per split
+    ((1, 1, 128, 700, 128), 1, 1),       # 6 key tiles: too few to split
+])
+def test_dq_split_rule(lib, shape, det, want):
+    B_, H, Tq, Tk, d = shape
+    assert B.attn_bwd_dq_splits(B_, H, Tq, Tk, d, d, B.ATTN_BF16, det) == want
+    assert B.attn_bwd_dq_splits(B_, H, Tq, Tk, d, d, B.ATTN_F32, det) == 1
+    part = (B_ * H * ((Tq + 127) // 128 * 128) * 4 + 255) // 256 * 256
+    acc = B_ * H * Tq * d * 4
+    ws = B.attn_bwd_workspace_size(B_, H, Tq, Tk, d, d, B.ATTN_BF16, det)
+    assert ws == 2 * part + (acc if det == 0 else (want * acc if want > 1 else 0))
+
+
 def test_workspace_size(lib):
     # -LSE*log2(e) and D, each [B*H, Tq rounded up to 128] fp32 and 256-byte
     # aligned, then (bf16 with fp32 dQ accumulation) the [B*H*Tq, d] accumulator

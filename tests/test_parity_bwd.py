@@ -133,6 +133,33 @@ def test_bf16_d_neq_dv(shape, causal, deterministic):
     check_all(x, causal, 1 / math.sqrt(d), torch.bfloat16, deterministic)
 
 
+SPLIT_DQ_SHAPES = [  # B, H, Tq, Tk, d, dv: few query tiles, many key tiles
+    (1, 2, 128, 4096, 128, 128),
+    (1, 1, 256, 3000, 64, 128),
+    (2, 1, 200, 2500, 128, 64),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SPLIT_DQ_SHAPES)
+def test_bf16_split_dq_deterministic(shape, causal):
+    """The deterministic backward with dQ split over key ranges (partials
+    added in split order): parity with the oracle, bitwise equal across two
+    runs, and close to the atomic mode."""
+    B, H, Tq, Tk, d, dv = shape
+    assert pkg.attn_bwd_dq_splits(B, H, Tq, Tk, d, dv, pkg.ATTN_BF16, 1) > 1
+    x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, dv), seed=Tq + Tk, dtype=torch.bfloat16, device=DEV)
+    scale = 1 / math.sqrt(d)
+    check_all(x, causal, scale, torch.bfloat16, 1)
+    o, lse, dq1, dk1, dv1 = run(x, causal, scale, 1)
+    _, _, dq2, dk2, dv2 = run(x, causal, scale, 1)
+    assert torch.equal(dq1, dq2) and torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    # the atomic mode forms dS from S^T in its own kernel (other fp32 rounding
+    # before the bf16 dS): the two agree to about twice one mode's error
+    _, _, dqa, _, _ = run(x, causal, scale, 0)
+    assert (dq1.float() - dqa.float()).norm() <= 1e-2 * dqa.float().norm()
+
+
 @pytest.mark.parametrize("deterministic", [0, 1])
 def test_bf16_c2_full_size(deterministic):
     w = WORKLOADS["c2"]
