@@ -59,7 +59,7 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1,  /* null pointer, negative size, non-finite or non-positive scale, overlap */
-  ATTN_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement (e.g. bf16 with d = 96) */
+  ATTN_ERR_UNSUPPORTED = 2,  /* valid request the library does not implement (e.g. bf16 with d = 96) */
   ATTN_ERR_MISALIGNED = 3,   /* a pointer breaks the alignment rule of its dtype (bf16: 16 B, f32: 4 B) */
   ATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed; see attn_last_cuda_error() */
   ATTN_ERR_TIMEOUT = 5,      /* a kernel's bounded pipeline wait gave up (reported by attn_device_status) */
