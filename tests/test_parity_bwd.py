@@ -137,6 +137,7 @@ SPLIT_DQ_SHAPES = [  # B, H, Tq, Tk, d, dv: few query tiles, many key tiles
     (1, 2, 128, 4096, 128, 128),
     (1, 1, 256, 3000, 64, 128),
     (2, 1, 200, 2500, 128, 64),
+    (1, 1, 1300, 1100, 128, 128),  # Tq > Tk: causal query tiles see 1 ... all 9 key tiles
 ]
 
 
