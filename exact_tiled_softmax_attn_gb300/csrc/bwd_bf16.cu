@@ -12,8 +12,8 @@
 // dK/dV kernel: one persistent CTA per SM; a work unit is one 128-key tile of
 // one head, and the CTA loops over the query tiles that can see it. K and V
 // stay in shared memory for the whole unit; Q, dO (TMA) and the 128-row slices
-// of NLSE2 and D (bulk copies) stream through a two-stage ring. Warp roles (16
-// warps, 4 warpgroups):
+// of NLSE2 and D (bulk copies) stream through rings of their own. Warp roles
+// (16 warps, 4 warpgroups):
 //   warp 0       producer (lane 0 issues the TMA and bulk copies)
 //   warp 1       MMA issuer (lane 0); allocates and frees TMEM
 //   warps 2-3    idle (they complete the first warpgroup's register release)
@@ -22,7 +22,8 @@
 //   warps 12-15  dQ group: reads each dQ tile out of TMEM, stages it in the dS
 //                buffer in two 64-column halves and adds it into the fp32
 //                accumulator with TMA reduce-add; writes dK and dV per unit
-// setmaxnreg splits the launch's 512 x 128 registers as 104 / 152 / 152 / 104.
+// setmaxnreg splits the launch's 512 x 128 registers as 104 / 152 / 152 / 104
+// (atomic dQ) or 96 / 168 / 168 / 80 (deterministic).
 // TMEM (512 columns): dV [0,128), dK [128,256), S^T [256,384), dP^T [384,512).
 // Per query tile the MMA warp issues
 //   S^T  = K Q^T        (A = K, B = Q, both K-major in smem)
@@ -31,8 +32,11 @@
 //   dK  += dS^T Q       (A = dS^T bf16 in TMEM over dP^T, B = Q MN-major)
 //   dQ   = dS K         (A = dS from smem, MN-major; B = K MN-major) -> over dP^T
 // The last product is skipped in deterministic mode, where a separate dQ
-// kernel (one CTA per query tile looping over key tiles in a fixed order)
-// accumulates dQ in TMEM and writes it once.
+// kernel (a unit per query tile looping over key tiles in a fixed order, or
+// per query tile and key range when query tiles are few) accumulates dQ in
+// TMEM and writes it once (or its range's fp32 partial, added in order by
+// reduce_dq_kernel). The dQ and dK/dV kernels take d (Q, K, dQ, dK) and dv (V,
+// O, dO, dV) as separate template parameters, each 64 or 128.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math_constants.h>
@@ -788,9 +792,10 @@ constexpr int DQ_THREADS = 320;
 // memory, O from global memory) and -LSE * log2(e), which they use and store
 // for the dK/dV kernel that runs after this one. Then, for each key tile
 // (fixed ascending order): S = Q K^T, dP = dO V^T (both in TMEM), dS =
-// P o (dP - D) written bf16 over dP, and dQ += dS K accumulates in TMEM. Warps: 0 producer, 1 MMA, 2-5 and 6-9 two row groups; group g
-// works on key columns [64g, 64g + 64) of every query row (one thread per
-// row each) and packs its dS at columns [64g, 64g + 32) of the dP buffer.
+// P o (dP - D) written bf16 over dP, and dQ += dS K accumulates in TMEM.
+// Warps: 0 producer, 1 MMA, 2-5 and 6-9 two row groups; group g works on key
+// columns [64g, 64g + 64) of every query row (one thread per row each) and
+// packs its dS at columns [64g, 64g + 32) of the dP buffer.
 // TMEM: S [0, 128), dQ [128, 256), dP/dS in two buffers [256, 384) and
 // [384, 512) alternating by step, so the MMA warp computes dP of step j + 1
 // while the row threads still turn dP of step j into dS.
