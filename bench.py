@@ -53,10 +53,16 @@ def useful_flops_rows(w, rows):
 
 
 def kernel_source_hash(kernel: str) -> str:
+    """Hash of the kernel's sources with comments and blank space removed, so
+    that editing a comment does not void a committed measurement."""
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "exact_tiled_softmax_attn_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "exact_tiled_softmax_attn_gb300", "csrc", f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
