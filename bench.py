@@ -468,6 +468,9 @@ def run_ours(args, w):
     cfg.update({"dq_mode": "deterministic" if det else "atomic", "fwd_splits": n_splits, "dq_splits": dq_splits,
                 "fwd_tflops": F / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": Bf / (bwd_ms * 1e-3) / 1e12,
                 "fwd_bwd_frac_of_peak": (F + Bf) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12 / peak,
+                # the same against the measured power-capped (seconds-long) bf16 rate
+                "fwd_bwd_frac_of_sustained_peak": None if f32 or not peaks.get("bf16_tflops_sustained") else
+                (F + Bf) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"],
                 "peak_source": f"derived FP32 FMA {peak:.1f}" if f32 else f"{peaks['source']} bf16_tflops {peak}",
                 "kernels": kernels})
     line = {
