@@ -219,22 +219,23 @@ def test_bf16_inputs_unchanged():
     assert torch.equal(o, o2) and torch.equal(lse, lse2)
 
 
-@pytest.mark.parametrize("dt,d", [(torch.float32, 64), (torch.bfloat16, 128)])
+@pytest.mark.parametrize("dt,d,Tq,Tk", [(torch.float32, 64, 515, 515), (torch.bfloat16, 128, 515, 515),
+                                        (torch.bfloat16, 128, 128, 4096)])   # the last: split dQ when deterministic
 @pytest.mark.parametrize("deterministic", [0, 1])
-def test_phases_equal_one_call(dt, d, deterministic):
-    # preprocess, dQ kernel, dK/dV kernel, dQ conversion launched one by one
-    # (phases 1, 5, 4, 3) give what one attn_bwd call gives
-    B, H, T = 1, 3, 515
-    x = make_random((B, H, T, d), (B, H, T, d), (B, H, T, d), seed=11, dtype=dt, device=DEV)
+def test_phases_equal_one_call(dt, d, Tq, Tk, deterministic):
+    # preprocess, dQ kernel, dK/dV kernel, dQ conversion / split reduction
+    # launched one by one (phases 1, 5, 4, 3) give what one attn_bwd call gives
+    B, H = 1, 3
+    x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, d), seed=11, dtype=dt, device=DEV)
     code = pkg.ATTN_BF16 if dt == torch.bfloat16 else pkg.ATTN_F32
     o, lse = pkg.forward(x["Q"], x["K"], x["V"], causal=True, scale=0.09)
-    ws = torch.empty(max(pkg.attn_bwd_workspace_size(B, H, T, T, d, d, code, deterministic), 256),
+    ws = torch.empty(max(pkg.attn_bwd_workspace_size(B, H, Tq, Tk, d, d, code, deterministic), 256),
                      dtype=torch.uint8, device=DEV)
     outs = []
     for phases in ((0,), (1, 5, 4, 3)):
-        g = [torch.full_like(x["Q"], float("nan")) for _ in range(3)]
+        g = [torch.full_like(t, float("nan")) for t in (x["Q"], x["K"], x["V"])]
         for ph in phases:
-            pkg.attn_bwd_phase(x["Q"], x["K"], x["V"], o, lse, x["dO"], g[0], g[1], g[2], B, H, T, T, d, d, 0.09,
+            pkg.attn_bwd_phase(x["Q"], x["K"], x["V"], o, lse, x["dO"], g[0], g[1], g[2], B, H, Tq, Tk, d, d, 0.09,
                                True, code, deterministic, ws, ws.numel(), ph)
         torch.cuda.synchronize()
         outs.append(g)

@@ -22,6 +22,7 @@ CASES = [  # B, H, Tq, Tk, d, dtype, causal, deterministic
     (1, 4, 1000, 1000, 128, torch.bfloat16, True, 0),
     (2, 2, 300, 700, 64, torch.bfloat16, False, 0),
     (1, 3, 513, 513, 128, torch.bfloat16, True, 1),
+    (1, 2, 128, 4096, 128, torch.bfloat16, False, 1),   # deterministic with split dQ partials
     (2, 2, 77, 133, 40, torch.float32, True, 0),
 ]
 
