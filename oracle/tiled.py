@@ -27,7 +27,7 @@ import math
 
 import numpy as np
 
-__all__ = ["online_softmax_step", "flash_attention"]
+__all__ = ["online_softmax_step", "flash_attention", "merge_states", "chunked_attention"]
 
 
 def online_softmax_step(m, l, acc, scores, v_block):
@@ -86,3 +86,62 @@ def flash_attention(Q, K, V, block_size, causal=False, scale=None):
     out = np.where(live[:, None], acc / np.where(live, l, 1.0)[:, None], 0.0)
     lse = np.where(live, m + np.log(np.where(live, l, 1.0)), -np.inf)
     return out, lse
+
+
+def merge_states(states):
+    """Combine the running states (m, l, acc) that the step builds for the
+    same query rows over disjoint key chunks into the state over all of them.
+
+    Each chunk's state is rescaled to the common maximum and added, the same
+    rescale the step applies to the running state when a block raises the
+    maximum ("The Hidden Recurrence in Softmax Attention", section "Chunk-wise
+    Mode with Online Softmax Re-scale"), here applied to a second chunk's
+    state in place of a block of raw scores:
+        m = max_c m_c,  w_c = exp(m_c - m),  l = sum_c w_c l_c,  acc = sum_c w_c acc_c
+    with 0 in place of m inside the exponentials when m = -inf (no chunk has
+    an allowed key for the row).
+    """
+    ms = [np.asarray(st[0], dtype=np.float64) for st in states]
+    m = ms[0]
+    for mc in ms[1:]:
+        m = np.maximum(m, mc)
+    ref = np.where(np.isneginf(m), 0.0, m)
+    l = np.zeros_like(m)
+    acc = np.zeros_like(np.asarray(states[0][2], dtype=np.float64))
+    for (mc, lc, ac) in states:
+        w = np.exp(np.asarray(mc, dtype=np.float64) - ref)   # 0 for a chunk with no allowed key
+        l = l + w * np.asarray(lc, dtype=np.float64)
+        acc = acc + w[:, None] * np.asarray(ac, dtype=np.float64)
+    return m, l, acc
+
+
+def chunked_attention(Q, K, V, chunk_bounds, block_size=64, causal=False, scale=None):
+    """Single head, keys split at chunk_bounds (e.g. [0, 300, 301, Tk]): each
+    chunk runs the block-by-block step from the empty state on its own keys,
+    the chunk states are merged with merge_states, and the output is
+    acc / l (0 where l = 0) with lse = m + log l (-inf where l = 0).
+    Returns (output [Tq, dv], lse [Tq]).
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    Tq, d = Q.shape
+    dv = V.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    states = []
+    for c0, c1 in zip(chunk_bounds[:-1], chunk_bounds[1:]):
+        m = np.full(Tq, -np.inf)
+        l = np.zeros(Tq)
+        acc = np.zeros((Tq, dv))
+        for b0 in range(c0, c1, block_size):
+            b1 = min(b0 + block_size, c1)
+            s = scale * (Q @ K[b0:b1].T)
+            if causal:
+                s = np.where(np.arange(b0, b1)[None, :] > np.arange(Tq)[:, None], -np.inf, s)
+            m, l, acc = online_softmax_step(m, l, acc, s, V[b0:b1])
+        states.append((m, l, acc))
+    m, l, acc = merge_states(states)
+    out = np.where(l[:, None] > 0, acc / np.where(l > 0, l, 1.0)[:, None], 0.0)
+    lse = np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), -np.inf)
+    return out, lse
+

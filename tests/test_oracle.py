@@ -83,6 +83,59 @@ def test_block_size_invariance(shape, causal):
         np.testing.assert_array_equal(a, c)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape,bounds", [
+    ((9, 40, 5, 3), [0, 13, 40]),
+    ((9, 40, 5, 3), [0, 1, 2, 39, 40]),        # one-key chunks
+    ((50, 70, 8, 6), [0, 20, 20, 45, 70]),     # an empty chunk
+    ((30, 10, 4, 4), [0, 3, 6, 10]),           # causal: rows 0-2 see no key of the later chunks
+])
+def test_merged_key_chunks_equal_whole_softmax(shape, bounds, causal):
+    """Keys split into chunks, each chunk's state built from the empty state,
+    states merged by rescaling to the common maximum: the whole-row softmax."""
+    Tq, Tk, d, dv = shape
+    rng = np.random.default_rng(Tq + 7 * Tk)
+    Q, K, V = rng.standard_normal((Tq, d)), 3 * rng.standard_normal((Tk, d)), rng.standard_normal((Tk, dv))
+    o_ref, lse_ref = A.forward_head(Q, K, V, 1.0 / math.sqrt(d), causal)
+    for bs in (1, 4, 64):
+        o, lse = T.chunked_attention(Q, K, V, bounds, block_size=bs, causal=causal)
+        np.testing.assert_allclose(o, o_ref, atol=1e-12, rtol=1e-11)
+        np.testing.assert_allclose(lse, lse_ref, atol=1e-12, rtol=1e-12)
+
+
+def test_merging_states_with_no_key_keeps_the_empty_state():
+    empty = (np.full(2, -np.inf), np.zeros(2), np.zeros((2, 3)))
+    m, l, acc = T.merge_states([empty, empty])
+    assert np.all(np.isneginf(m)) and np.all(l == 0) and np.all(acc == 0)
+    one = (np.array([0.5, -1.0]), np.array([2.0, 3.0]), np.ones((2, 3)))
+    m, l, acc = T.merge_states([empty, one, empty])
+    np.testing.assert_array_equal(m, one[0])
+    np.testing.assert_array_equal(l, one[1])
+    np.testing.assert_array_equal(acc, one[2])
+
+
+MERGE_MUTANTS = [
+    ("w = np.exp(np.asarray(mc, dtype=np.float64) - ref)", "w = np.exp(ref - np.asarray(mc, dtype=np.float64))"),
+    ("l = l + w * np.asarray(lc, dtype=np.float64)", "l = l + np.asarray(lc, dtype=np.float64)"),   # unscaled sums
+    ("acc = acc + w[:, None] * np.asarray(ac, dtype=np.float64)", "acc = acc + np.asarray(ac, dtype=np.float64)"),
+]
+
+
+@pytest.mark.parametrize("old,new", MERGE_MUTANTS)
+def test_planted_merge_mistakes_are_caught(old, new):
+    bad, _ = _mutant(T, "merge_states", old, new)
+    ns = dict(vars(T))
+    ns["merge_states"] = bad
+    src = inspect.getsource(T.chunked_attention)
+    exec(compile(src, "<chunked with mutant merge>", "exec"), ns)
+    rng = np.random.default_rng(3)
+    Q, K, V = rng.standard_normal((6, 4)), 3 * rng.standard_normal((20, 4)), rng.standard_normal((20, 2))
+    o_ref, lse_ref = A.forward_head(Q, K, V, 0.5)
+    with np.errstate(all="ignore"):
+        o, lse = ns["chunked_attention"](Q, K, V, [0, 7, 20], block_size=4, scale=0.5)
+    assert not (np.allclose(o, o_ref, atol=1e-6) and np.allclose(lse, lse_ref, atol=1e-6))
+
+
 def test_huge_scores_across_blocks_stay_finite_and_exact():
     # scores > 1000 in one block and < -1000 in the next (and the reverse)
     d = 4
