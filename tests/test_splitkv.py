@@ -126,6 +126,18 @@ def test_splitkv_d_neq_dv(shape, causal):
 
 
 @pytest.mark.gpu
+def test_splitkv_fp32_runs_the_plain_forward():
+    """fp32 never splits: num_splits 0 or 1 gives exactly attn_fwd's result."""
+    x = make_random((1, 2, 70, d := 48), (1, 2, 300, d), (1, 2, 300, 40), seed=5, dtype=torch.float32, device="cuda")
+    o1, l1 = B.forward(x["Q"], x["K"], x["V"], causal=True, scale=0.2)
+    for ns in (0, 1):
+        assert B.attn_fwd_splitkv_splits(1, 2, 70, 300, d, 40, B.ATTN_F32, ns) == 1
+        o, l = B.forward(x["Q"], x["K"], x["V"], causal=True, scale=0.2, num_splits=ns)
+        torch.cuda.synchronize()
+        assert torch.equal(o, o1) and torch.equal(l, l1)
+
+
+@pytest.mark.gpu
 def test_splitkv_long_keys_sampled_rows():
     """B=1 H=4 Tq=256 Tk=65536, automatic split count: sampled query rows of
     two heads against the oracle, with and without the causal mask."""
