@@ -187,7 +187,8 @@ ATTN_API attn_status_t attn_bwd(const void* Q, const void* K, const void* V, con
  *      deterministic == 1, where the dQ kernel forms D itself
  *   2  main kernels: phases 5 and 4 in this order
  *   3  dQ conversion from the fp32 accumulator (bf16 with deterministic
- *      == 0; a no-op otherwise)
+ *      == 0), or the in-order sum of the split dQ partials (bf16 with
+ *      deterministic == 1 and attn_bwd_dq_splits(...) > 1); a no-op otherwise
  *   4  the dK/dV kernel alone (with deterministic == 0 it also accumulates dQ)
  *   5  the separate dQ kernel alone (deterministic == 1; a no-op otherwise);
  *      for bf16 it also writes the D and -LSE * log2(e) phase 4 reads
