@@ -895,6 +895,11 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         }
       }
       if (!(ok = ptx::mbar_wait(q_empty, (u_it & 1u) ^ 1u, w))) break;
+      // the row threads read dO from shared memory for D at their first key
+      // tile, which can come after the unit's last MMA has read Q and dO (a
+      // unit of one or two key tiles): the next unit's tiles wait for both
+      // groups' partial D of the previous unit as well
+      if (!(ok = ptx::mbar_wait(dpart_full, (u_it & 1u) ^ 1u, w))) break;
       ptx::mbar_arrive_expect_tx(q_full, C::TILE + C::TILE_V);
       for (int b = 0; b < C::KB; ++b) ptx::tma_load_3d(sQ + b * BOX_BYTES, &tmQ, q_full, b * 64, qt * BT, bh);
       for (int b = 0; b < C::KBV; ++b) ptx::tma_load_3d(sdO + b * BOX_BYTES, &tmdO, q_full, b * 64, qt * BT, bh);
