@@ -164,6 +164,19 @@ def test_bf16_split_dq_deterministic(shape, causal):
 
 
 @pytest.mark.parametrize("deterministic", [0, 1])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", [(20, 16, 130, 128), (40, 8, 256, 64), (75, 4, 70, 128), (3, 100, 1, 64)])
+def test_bf16_many_short_units(shape, causal, deterministic):
+    """More units than SMs, each of one or two tiles: every kernel walks
+    several short units per CTA, so tile loads for the next unit overlap the
+    last steps of the previous one."""
+    B, H, T, d = shape
+    x = make_random((B, H, T, d), (B, H, T, d), (B, H, T, d), seed=B * H + T, dtype=torch.bfloat16, device=DEV)
+    check_all(x, causal, 1 / math.sqrt(d), torch.bfloat16, deterministic,
+              heads=[(0, 0), (B // 2, H // 2), (B - 1, H - 1)])
+
+
+@pytest.mark.parametrize("deterministic", [0, 1])
 def test_bf16_many_small_heads(deterministic):
     """256 heads of 200 rows: far more units than SMs, every unit ragged."""
     B, H, T, d = 16, 16, 200, 64
