@@ -81,6 +81,7 @@ SHAPES = [  # B, H, Tq, Tk, d, num_splits
     (1, 1, 1000, 3000, 128, 64),
     (1, 2, 1300, 700, 64, 3),    # Tq > Tk: under the causal mask the last query tiles see every key
     (4, 40, 256, 1024, 64, 3),   # 480 units: several split units per CTA
+    (8, 40, 256, 256, 64, 2),    # causal: the second range holds no key tile for the first query tile
 ]
 
 
