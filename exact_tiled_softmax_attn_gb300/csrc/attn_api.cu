@@ -113,7 +113,7 @@ attn_status_t check_common(int B, int H, int Tq, int Tk, int d, int dv, float sc
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (dt != ATTN_F32 && dt != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
   if (dt == ATTN_F32) {
-    if (d > 128 || dv > 128) return ATTN_ERR_UNSUPPORTED;
+    if (d > 256 || dv > 256) return ATTN_ERR_UNSUPPORTED;
   } else {
     if ((d != 64 && d != 128) || (dv != 64 && dv != 128)) return ATTN_ERR_UNSUPPORTED;
   }
@@ -222,6 +222,9 @@ attn_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, flo
   if (s != ATTN_OK) return s;
   if (split_req < 0) return ATTN_ERR_INVALID_ARG;
   if (dtype == ATTN_F32 && split_req > 1) return ATTN_ERR_UNSUPPORTED;
+  // the CUDA-core forward keeps a key tile of K and V rows in shared memory:
+  // with d or dv above 128 a 128-key tile does not fit
+  if (dtype == ATTN_F32 && fwd_f32_smem_bytes(block_n, d, dv) > 227 * 1024) return ATTN_ERR_UNSUPPORTED;
   const size_t es = elem_size(dtype);
   const size_t bh = static_cast<size_t>(B) * H;
   const size_t align = dtype == ATTN_BF16 ? 16 : 4;

@@ -3,7 +3,7 @@
 // Same tiled algorithm as the tensor-core path ("Tiled attention with an
 // online softmax", section "Task"; gradients from "attention_backprop",
 // sections "Gradient of V and P", "Gradient of S", "Gradient of Q and K"),
-// for fp32 inputs of any head size up to 128.
+// for fp32 inputs of any head size up to 256.
 //
 // Precision: a score q.k is accumulated in twice the fp32 precision (the
 // compensated dot product below, fp32 instructions only) and held in fp64;
@@ -24,7 +24,7 @@ namespace simt {
 
 constexpr int BM = 32;          // query rows per tile
 constexpr int NT = 256;         // threads per CTA
-constexpr int MAXD = 128;       // largest supported d and dv
+constexpr int MAXD = 256;       // largest supported d and dv
 
 __device__ __forceinline__ double warp_max_d(double v) {
 #pragma unroll
@@ -409,6 +409,14 @@ size_t bwd_smem(int d, int dv) {
 }
 
 }  // namespace simt
+
+size_t fwd_f32_smem_bytes(int block_n, int d, int dv) {
+  switch (block_n) {
+    case 32: return simt::fwd_smem<32>(d, dv);
+    case 128: return simt::fwd_smem<128>(d, dv);
+    default: return simt::fwd_smem<64>(d, dv);
+  }
+}
 
 cudaError_t launch_fwd_f32(const LaunchFwd& a) {
   switch (a.block_n) {

@@ -34,7 +34,9 @@
  * checks means nothing was enqueued.
  *
  * Supported shapes:
- *   ATTN_F32 : 1 <= d, dv <= 128, any B, H, Tq, Tk >= 0
+ *   ATTN_F32 : 1 <= d, dv <= 256, any B, H, Tq, Tk >= 0 (attn_fwd_f32_blocked
+ *              with block_n = 128 returns ATTN_ERR_UNSUPPORTED when its key
+ *              tile does not fit in shared memory, above d = dv = 150 or so)
  *   ATTN_BF16: d in {64, 128} and dv in {64, 128} (d != dv allowed: the
  *              page's task takes V with its own head dimension), any B, H,
  *              Tq, Tk >= 0

@@ -68,7 +68,7 @@ def _fwd(**kw):
     (dict(d=96, dv=96), B.ATTN_ERR_UNSUPPORTED),
     (dict(d=64, dv=96), B.ATTN_ERR_UNSUPPORTED),
     (dict(d=256, dv=128), B.ATTN_ERR_UNSUPPORTED),
-    (dict(dtype=B.ATTN_F32, d=129), B.ATTN_ERR_UNSUPPORTED),
+    (dict(dtype=B.ATTN_F32, d=257), B.ATTN_ERR_UNSUPPORTED),
     (dict(Q=None), B.ATTN_ERR_INVALID_ARG),
     (dict(LSE=None), B.ATTN_ERR_INVALID_ARG),
     (dict(Q=0x10008), B.ATTN_ERR_MISALIGNED),
@@ -85,6 +85,13 @@ def test_empty_problems_need_no_device(lib):
     assert _fwd(B=0) == B.ATTN_OK
     assert _fwd(Tq=0) == B.ATTN_OK
     assert _fwd(B=0, Q=None, K=None, V=None, O=None, LSE=None) == B.ATTN_OK
+
+
+def test_blocked_forward_key_tile_must_fit_shared_memory(lib):
+    # d = dv = 256 with 128-key tiles needs ~330 KB of shared memory per CTA
+    st = B.attn_fwd_f32_blocked(0x100000, 0x200000, 0x300000, 0x400000, 0x500000, 1, 1, 8, 8, 256, 256, 0.1, 0,
+                                128, stream=0, check=False)
+    assert st == B.ATTN_ERR_UNSUPPORTED
 
 
 def test_blocked_forward_validates_block(lib):

@@ -51,7 +51,8 @@ def test_f32_c1(name, deterministic):
     check_all(make_inputs(w, DEV), w.causal, w.softmax_scale, torch.float32, deterministic)
 
 
-F32_SHAPES = [(1, 1, 1, 1, 1, 1), (2, 3, 77, 133, 40, 24), (1, 2, 200, 65, 128, 128), (1, 1, 33, 300, 7, 128)]
+F32_SHAPES = [(1, 1, 1, 1, 1, 1), (2, 3, 77, 133, 40, 24), (1, 2, 200, 65, 128, 128), (1, 1, 33, 300, 7, 128),
+              (1, 2, 100, 150, 256, 256), (1, 1, 70, 90, 200, 136)]   # head sizes above 128
 
 
 @pytest.mark.parametrize("deterministic", [0, 1])

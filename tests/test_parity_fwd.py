@@ -56,6 +56,8 @@ F32_SHAPES = [  # B, H, Tq, Tk, d, dv
     (1, 2, 200, 65, 128, 128),
     (1, 1, 33, 300, 7, 128),
     (3, 1, 64, 64, 64, 64),
+    (1, 2, 100, 150, 256, 256),   # head sizes above 128
+    (1, 1, 70, 90, 200, 136),
 ]
 
 
