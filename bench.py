@@ -35,26 +35,32 @@ KERNEL_SOURCES = {
     "attn_fwd_bf16_kernel": ("fwd_bf16.cu", "ptx.cuh", "common.cuh", "launch.h"),
     "dkdv_kernel": ("bwd_bf16.cu", "ptx.cuh", "common.cuh", "launch.h"),
     "dq_kernel": ("bwd_bf16.cu", "ptx.cuh", "common.cuh", "launch.h"),
+    "attn_fwd_d256_kernel": ("fwd_bf16_d256.cu", "ptx.cuh", "common.cuh", "launch.h"),
 }
 
 
 # ---------------------------------------------------------------- helpers
 
-def useful_flops_rows(w, rows):
+def useful_flops_rows(w, rows, fwd_only=False):
     """Useful fwd+bwd FLOPs of the given query rows: 2*(d + dv) per (query,
-    key) pair forward and 2*(3d + 2dv) backward (14 d per pair when d = dv).
+    key) pair forward and 2*(3d + 2dv) backward (14 d per pair when d = dv);
+    the forward's share alone with fwd_only.
     Under the causal mask row i counts i + 1/2 keys, so that all Tq rows of a
     square problem sum to the halved full count (the convention of the GPU
     metric)."""
     import numpy as np
     rows = np.asarray(rows, dtype=np.float64)
     keys = np.minimum(rows + 0.5, w.Tk) if w.causal else np.full(rows.shape, float(w.Tk))
-    return (2.0 * (w.d + w.dv) + 2.0 * (3 * w.d + 2 * w.dv)) * float(keys.sum())
+    per_pair = 2.0 * (w.d + w.dv) + (0.0 if fwd_only else 2.0 * (3 * w.d + 2 * w.dv))
+    return per_pair * float(keys.sum())
 
 
 def kernel_source_hash(kernel: str) -> str:
     """Hash of the kernel's sources with comments and blank space removed, so
-    that editing a comment does not void a committed measurement."""
+    that editing a comment does not void a committed measurement. Plain
+    declarations of other launch functions (`cudaError_t f(...);`,
+    `size_t f(...);`) are dropped too: they declare code in other files and
+    cannot change this kernel."""
     import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
@@ -62,6 +68,8 @@ def kernel_source_hash(kernel: str) -> str:
             text = fh.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
         text = re.sub(r"//[^\n]*", " ", text)
+        text = " ".join(text.split())
+        text = re.sub(r"(?:cudaError_t|size_t) \w+\([^(){};]*\);", " ", text)
         h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
@@ -174,15 +182,19 @@ def barrier():
 
 # ---------------------------------------------------------------- CPU oracle legs
 
-def oracle_sample(w, x, rows, n_heads=1):
-    """Run the CPU float64 oracle forward + backward on the given query rows of
-    the first n_heads heads (in (b, h) order); returns seconds."""
+def oracle_sample(w, x, rows, n_heads=1, fwd_only=False):
+    """Run the CPU float64 oracle forward + backward (forward alone with
+    fwd_only) on the given query rows of the first n_heads heads (in (b, h)
+    order); returns seconds."""
     from oracle import attention as ref
     t0 = time.perf_counter()
     for k in range(n_heads):
         b, h = divmod(k, x["Q"].shape[1])
-        ref.backward_head(x["Q"][b, h], x["K"][b, h], x["V"][b, h], x["dO"][b, h], w.softmax_scale, w.causal,
-                          rows=rows)
+        if fwd_only:
+            ref.forward_head(x["Q"][b, h], x["K"][b, h], x["V"][b, h], w.softmax_scale, w.causal, rows=rows)
+        else:
+            ref.backward_head(x["Q"][b, h], x["K"][b, h], x["V"][b, h], x["dO"][b, h], w.softmax_scale, w.causal,
+                              rows=rows)
     return time.perf_counter() - t0
 
 
@@ -192,24 +204,25 @@ def spread_rows(w, n):
     return np.unique(np.linspace(0, w.Tq - 1, n).astype(np.int64))
 
 
-def cpu_baseline(w, x, target_s=15.0):
+def cpu_baseline(w, x, target_s=15.0, fwd_only=False):
     """The oracle on a bounded sample of the workload (~10-30 s of CPU work):
     query rows spread over head (0, 0), then, when all its rows take less than
     that, whole heads in (b, h) order."""
     probe = spread_rows(w, 128)
-    t = oracle_sample(w, x, probe)
+    t = oracle_sample(w, x, probe, fwd_only=fwd_only)
     n = int(min(w.Tq, max(128, 128 * target_s / max(t, 1e-3))))
     rows = spread_rows(w, n)
-    t = oracle_sample(w, x, rows)
+    t = oracle_sample(w, x, rows, fwd_only=fwd_only)
     n_heads = 1
     if rows.size == w.Tq and t < target_s / 2:
         n_heads = int(min(w.B * w.H, max(1, target_s // max(t, 1e-3))))
         if n_heads > 1:
-            t = oracle_sample(w, x, rows, n_heads)
-    fl = useful_flops_rows(w, rows) * n_heads
+            t = oracle_sample(w, x, rows, n_heads, fwd_only=fwd_only)
+    fl = useful_flops_rows(w, rows, fwd_only) * n_heads
     where = "head (0,0)" if n_heads == 1 else f"each of the first {n_heads} heads"
+    what = "fwd" if fwd_only else "fwd+bwd"
     return {"value": fl / t / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"float64 numpy oracle, fwd+bwd of {rows.size} query rows spread over {where} of "
+            "sample": f"float64 numpy oracle, {what} of {rows.size} query rows spread over {where} of "
                       f"{w.name} (Tk={w.Tk}, d={w.d}); useful FLOPs of those rows / {t:.2f} s"}
 
 
@@ -220,18 +233,20 @@ def run_reference(args, w):
     from exact_tiled_softmax_attn_gb300.workloads import make_inputs
     x = make_inputs(w.with_(B=1, H=1))
     budget = 150.0 / max(1, args.steps + args.warmup)
+    fo = args.fwd_only
     cal = spread_rows(w, 64)
-    t = oracle_sample(w, x, cal)
+    t = oracle_sample(w, x, cal, fwd_only=fo)
     n = int(min(w.Tq, max(64, 64 * budget / max(t, 1e-3))))
     rows = spread_rows(w, n)
     for _ in range(args.warmup):
-        oracle_sample(w, x, rows)
+        oracle_sample(w, x, rows, fwd_only=fo)
     total = 0.0
     for _ in range(args.steps):
-        total += oracle_sample(w, x, rows)
-    fl = useful_flops_rows(w, rows) * args.steps
+        total += oracle_sample(w, x, rows, fwd_only=fo)
+    fl = useful_flops_rows(w, rows, fo) * args.steps
     value = fl / total / 1e12
-    sample = (f"float64 numpy oracle, fwd+bwd of {rows.size} query rows spread over head (0,0) of {w.name} "
+    sample = (f"float64 numpy oracle, {'fwd' if fo else 'fwd+bwd'} of {rows.size} query rows spread over "
+              f"head (0,0) of {w.name} "
               f"per step (useful FLOPs of those rows)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
@@ -310,8 +325,8 @@ def run_ours(args, w):
 
     # backward launch groups in order: preprocess (atomic dQ only for bf16),
     # dQ kernel (deterministic only; it also forms D), dK/dV kernel, dQ
-    # conversion (atomic only)
-    phases = (1, 5, 4, 3)
+    # conversion (atomic only); none with --fwd-only
+    phases = () if args.fwd_only else (1, 5, 4, 3)
 
     def step(ev=None):
         if ev is not None:
@@ -322,6 +337,9 @@ def run_ours(args, w):
         for i, ph in enumerate(phases):
             bwd_phase(ph)
             if ev is not None:
+                ev[2 + i].record(stream)
+        if ev is not None:
+            for i in range(len(phases), 4):
                 ev[2 + i].record(stream)
 
     for _ in range(args.warmup):
@@ -351,7 +369,7 @@ def run_ours(args, w):
     fwd_ms, pre_ms, q_ms, kv_ms, conv_ms = (statistics.mean(p[j] for p in per) for j in range(5))
     main_ms = kv_ms + q_ms
     bwd_ms = pre_ms + main_ms + conv_ms
-    F, Bf = w.fwd_flop(), w.bwd_flop()
+    F, Bf = w.fwd_flop(), (0.0 if args.fwd_only else w.bwd_flop())
     value = world * args.steps * (F + Bf) / (total_ms * 1e-3) / 1e12
     assert pkg.attn_device_status(stream) == pkg.ATTN_OK
 
@@ -360,8 +378,12 @@ def run_ours(args, w):
     # results back. Two device buffer sets let step i+1's host-to-device copy
     # and step i-1's device-to-host copy run on copy streams of their own
     # while step i's kernels run (inputs > L2, so no flush between steps).
+    outs = (("O", o), ("LSE", lse)) if args.fwd_only else \
+        (("O", o), ("LSE", lse), ("dQ", dq), ("dK", dk), ("dV", dvv))
+    if args.fwd_only:                  # the forward's inputs and results only
+        host = {k: v for k, v in host.items() if k != "dO"}
+        x = {k: v for k, v in x.items() if k != "dO"}
     pinned = {k: v.pin_memory() for k, v in host.items()}
-    outs = (("O", o), ("LSE", lse), ("dQ", dq), ("dK", dk), ("dV", dvv))
     dev_in = [x, {k: torch.empty_like(v) for k, v in x.items()}]
     dev_out = [dict(outs), {n: torch.empty_like(t) for n, t in outs}]
     host_out = [{n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs} for _ in range(2)]
@@ -390,7 +412,8 @@ def run_ours(args, w):
             if i >= 2:
                 stream.wait_event(out_done[b])          # step i-2's results have left the device
             fwd_call(xi, oi["O"], oi["LSE"], stream)
-            pkg.attn_bwd(xi["Q"], xi["K"], xi["V"], oi["O"], oi["LSE"], xi["dO"], oi["dQ"], oi["dK"], oi["dV"],
+            if not args.fwd_only:
+                pkg.attn_bwd(xi["Q"], xi["K"], xi["V"], oi["O"], oi["LSE"], xi["dO"], oi["dQ"], oi["dK"], oi["dV"],
                          B, H, Tq, Tk, d, dv, sc, w.causal, code, det, ws, ws.numel(), stream)
             comp_done[b].record(stream)
             with torch.cuda.stream(s_out):
@@ -433,9 +456,12 @@ def run_ours(args, w):
     if n_splits > 1:
         fwd_name = f"fwd split-KV, {n_splits} splits (attn_fwd_bf16_kernel + merge)"
     else:
-        fwd_name = "fwd (simt fwd_kernel)" if f32 else "fwd (attn_fwd_bf16_kernel)"
+        fwd_name = "fwd (simt fwd_kernel)" if f32 else \
+            "fwd (attn_fwd_d256_kernel)" if w.d > 128 else "fwd (attn_fwd_bf16_kernel)"
     kernels = {fwd_name: {"ms": fwd_ms, "flop": F}}
-    if det:
+    if args.fwd_only:
+        pass
+    elif det:
         kernels[f"bwd dK/dV ({tag}dkdv_kernel)"] = {"ms": kv_ms, "flop": 2 * md + 2 * mv}
         kernels[f"bwd dQ ({tag}dq_kernel)"] = {"ms": q_ms, "flop": md, "executed_flop": 2 * md + mv}
     else:
@@ -445,28 +471,33 @@ def run_ours(args, w):
         v["frac_of_peak"] = v["tflops"] / peak
         if "executed_flop" in v:
             v["executed_tflops"] = v["executed_flop"] / (v["ms"] * 1e-3) / 1e12
-    kernels.update({
-        "bwd main (all main kernels)": {"ms": main_ms, "tflops": Bf / (main_ms * 1e-3) / 1e12},
-        # reads O, dO, LSE; writes D and LSE*log2(e) (padded rows) and zeroes the dQ accumulator
-        # atomic dQ only (bf16): the deterministic dQ kernel forms D itself
-        "bwd preprocess": {"ms": pre_ms,
-                           "gbs": B * H * Tq * (2 * dv * es + 4 + 8 + (0 if det else d * 4)) / (pre_ms * 1e-3) / 1e9
-                           if (f32 or not det) else None},
-        # atomic: fp32 accumulator -> bf16; deterministic with split dQ: the partials' sum -> bf16
-        "dQ convert": {"ms": conv_ms,
-                       "gbs": B * H * Tq * d * (4 * (1 if not det else dq_splits) + 2) / (conv_ms * 1e-3) / 1e9
-                       if not f32 and (not det or dq_splits > 1) else None},
-    })
-    kernels["bwd main (all main kernels)"]["frac_of_peak"] = kernels["bwd main (all main kernels)"]["tflops"] / peak
-    if kernels["bwd preprocess"]["gbs"] is not None:
-        kernels["bwd preprocess"]["frac_of_hbm"] = kernels["bwd preprocess"]["gbs"] / peaks["hbm_gbs"]
+    if not args.fwd_only:
+        kernels.update({
+            "bwd main (all main kernels)": {"ms": main_ms, "tflops": Bf / (main_ms * 1e-3) / 1e12},
+            # reads O, dO, LSE; writes D and LSE*log2(e) (padded rows) and zeroes the dQ accumulator
+            # atomic dQ only (bf16): the deterministic dQ kernel forms D itself
+            "bwd preprocess": {"ms": pre_ms,
+                               "gbs": B * H * Tq * (2 * dv * es + 4 + 8 + (0 if det else d * 4)) / (pre_ms * 1e-3) / 1e9
+                               if (f32 or not det) else None},
+            # atomic: fp32 accumulator -> bf16; deterministic with split dQ: the partials' sum -> bf16
+            "dQ convert": {"ms": conv_ms,
+                           "gbs": B * H * Tq * d * (4 * (1 if not det else dq_splits) + 2) / (conv_ms * 1e-3) / 1e9
+                           if not f32 and (not det or dq_splits > 1) else None},
+        })
+        kernels["bwd main (all main kernels)"]["frac_of_peak"] = \
+            kernels["bwd main (all main kernels)"]["tflops"] / peak
+        if kernels["bwd preprocess"]["gbs"] is not None:
+            kernels["bwd preprocess"]["frac_of_hbm"] = kernels["bwd preprocess"]["gbs"] / peaks["hbm_gbs"]
     # the dominant kernel: the longest of the single kernels
     dom = max((k for k, v in kernels.items() if "flop" in v), key=lambda k: kernels[k]["ms"])
     achieved = kernels[dom]["tflops"]
     traffic = load_traffic(dom.split("(")[-1].rstrip(")"))
     cfg = workload_config(w)
-    cfg.update({"dq_mode": "deterministic" if det else "atomic", "fwd_splits": n_splits, "dq_splits": dq_splits,
-                "fwd_tflops": F / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": Bf / (bwd_ms * 1e-3) / 1e12,
+    cfg.update({"pass": "forward only" if args.fwd_only else "forward + backward",
+                "dq_mode": None if args.fwd_only else ("deterministic" if det else "atomic"),
+                "fwd_splits": n_splits, "dq_splits": None if args.fwd_only else dq_splits,
+                "fwd_tflops": F / (fwd_ms * 1e-3) / 1e12,
+                "bwd_tflops": None if args.fwd_only else Bf / (bwd_ms * 1e-3) / 1e12,
                 "fwd_bwd_frac_of_peak": (F + Bf) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12 / peak,
                 # the same against the measured power-capped (seconds-long) bf16 rate
                 "fwd_bwd_frac_of_sustained_peak": None if f32 or not peaks.get("bf16_tflops_sustained") else
@@ -488,13 +519,14 @@ def run_ours(args, w):
                             "overlap step i's kernels on separate streams"},
         # bf16: fwd (+ split-KV merge), dQ (+ split reduction), dK/dV | fwd (+ merge), preprocess,
         # dK/dV, convert; fp32: fwd, preprocess, dK/dV, dQ | fwd, preprocess, dK/dV
-        "gpu_launches": args.steps * ((4 if det else 3) if f32 else
+        "gpu_launches": args.steps * ((1 + (1 if n_splits > 1 else 0)) if args.fwd_only else
+                                      (4 if det else 3) if f32 else
                                       ((3 if det else 4) + (1 if n_splits > 1 else 0) +
                                        (1 if det and dq_splits > 1 else 0))),
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, host)
+        line["cpu_baseline"] = cpu_baseline(w, host, fwd_only=args.fwd_only)
     print(json.dumps(line), flush=True)
     return 0
 
@@ -511,6 +543,8 @@ def main(argv=None):
     ap.add_argument("--splitkv", type=int, default=None,
                     help="run the forward through attn_fwd_splitkv with this many key splits (0 = automatic)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fwd-only", action="store_true",
+                    help="time the forward alone (its FLOPs only); the only pass for bf16 d = 256")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -73,9 +73,10 @@ attn_status_t encoder(EncodeTiledFn* fn) {
 }
 
 // 3-D map over a [planes, rows, inner] array with 128-byte swizzled boxes of
-// 128 rows x (128 bytes of elements): 64 bf16 or 32 fp32. Rows past `rows`
-// read as zero within each plane (and are not written by reduces).
-attn_status_t make_map(CUtensorMap* m, const void* base, int inner, int rows, int planes, bool f32 = false) {
+// box_rows rows x (128 bytes of elements): 64 bf16 or 32 fp32. Rows past
+// `rows` read as zero within each plane (and are not written by reduces).
+attn_status_t make_map(CUtensorMap* m, const void* base, int inner, int rows, int planes, bool f32 = false,
+                       unsigned box_rows = 128) {
   EncodeTiledFn enc;
   attn_status_t s = encoder(&enc);
   if (s != ATTN_OK) return s;
@@ -84,7 +85,7 @@ attn_status_t make_map(CUtensorMap* m, const void* base, int inner, int rows, in
                               static_cast<cuuint64_t>(planes)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * es,
                                  static_cast<cuuint64_t>(inner) * es * static_cast<cuuint64_t>(rows)};
-  const cuuint32_t box[3] = {f32 ? 32u : 64u, 128, 1};
+  const cuuint32_t box[3] = {f32 ? 32u : 64u, box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -115,7 +116,10 @@ attn_status_t check_common(int B, int H, int Tq, int Tk, int d, int dv, float sc
   if (dt == ATTN_F32) {
     if (d > 256 || dv > 256) return ATTN_ERR_UNSUPPORTED;
   } else {
-    if ((d != 64 && d != 128) || (dv != 64 && dv != 128)) return ATTN_ERR_UNSUPPORTED;
+    // d, dv in {64, 128}; or d = 256 (forward only) with dv in {64, 128, 256}
+    const bool small = (d == 64 || d == 128) && (dv == 64 || dv == 128);
+    const bool wide = d == 256 && (dv == 64 || dv == 128 || dv == 256);
+    if (!small && !wide) return ATTN_ERR_UNSUPPORTED;
   }
   // every index of every tensor must fit the kernels' 64-bit arithmetic and
   // the per-head row counts must fit int (TMA coordinates are int32)
@@ -182,11 +186,12 @@ BwdLayout bwd_layout(int B, int H, int Tq, int Tk, int d, attn_dtype_t dt, int d
 // Split-KV forward: effective number of key splits for a request (0 = pick
 // one so that the query-tile pairs times the splits fill the SMs once, with
 // at least two key tiles per split), clamped to [1, min(key tiles, 64)]; the
-// key tiles per split go to *split_tiles. fp32 problems never split.
-int splitkv_count(int B, int H, int Tq, int Tk, attn_dtype_t dt, int req, int num_sms, int* split_tiles) {
+// key tiles per split go to *split_tiles. fp32 problems and d = 256 never split.
+int splitkv_count(int B, int H, int Tq, int Tk, int d, attn_dtype_t dt, int req, int num_sms, int* split_tiles) {
+  const bool d_is_wide = d > 128;   // the d = 256 forward has no split variant
   const int nkb = (Tk + 127) / 128;
   int S = req;
-  if (dt != ATTN_BF16 || nkb <= 1 || B == 0 || H == 0 || Tq == 0) {
+  if (dt != ATTN_BF16 || nkb <= 1 || B == 0 || H == 0 || Tq == 0 || d_is_wide) {
     S = 1;
   } else if (req == 0) {
     const long long units = static_cast<long long>(B) * H * ((Tq + 255) / 256);
@@ -245,7 +250,7 @@ attn_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, flo
   if (split_req != 1) {
     // only the automatic choice needs the device (its SM count)
     if (split_req == 0 && dtype == ATTN_BF16 && (s = device_info(&di)) != ATTN_OK) return s;
-    n_splits = splitkv_count(B, H, Tq, Tk, dtype, split_req, di ? di->num_sms : 0, &split_tiles);
+    n_splits = splitkv_count(B, H, Tq, Tk, d, dtype, split_req, di ? di->num_sms : 0, &split_tiles);
     SL = split_layout(B, H, Tq, dv, n_splits);
     if (SL.total > 0) {
       if (workspace == nullptr || workspace_bytes < SL.total || reinterpret_cast<uintptr_t>(workspace) % 256)
@@ -285,14 +290,16 @@ attn_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, flo
   if (dtype == ATTN_F32) {
     e = launch_fwd_f32(a);
   } else {
+    // the d = 256 forward streams 64-key tiles of K and V
+    const unsigned kv_rows = d == 256 ? 64u : 128u;
     CUtensorMap mq, mk, mv;
     if ((s = make_map(&mq, Q, d, Tq, static_cast<int>(bh))) != ATTN_OK) return s;
-    if ((s = make_map(&mk, K, d, Tk, static_cast<int>(bh))) != ATTN_OK) return s;
-    if ((s = make_map(&mv, V, dv, Tk, static_cast<int>(bh))) != ATTN_OK) return s;
+    if ((s = make_map(&mk, K, d, Tk, static_cast<int>(bh), false, kv_rows)) != ATTN_OK) return s;
+    if ((s = make_map(&mv, V, dv, Tk, static_cast<int>(bh), false, kv_rows)) != ATTN_OK) return s;
     a.tmQ = &mq;
     a.tmK = &mk;
     a.tmV = &mv;
-    e = launch_fwd_bf16(a);
+    e = d == 256 ? launch_fwd_bf16_d256(a) : launch_fwd_bf16(a);
     if (e == cudaSuccess && n_splits > 1)
       e = launch_splitkv_merge(p, a.Opart, a.LSEpart, n_splits, split_tiles, O, LSE, di->num_sms, st);
   }
@@ -339,7 +346,7 @@ int attn_fwd_splitkv_splits(int B, int H, int Tq, int Tk, int d, int dv, attn_dt
     num_sms = di->num_sms;
   }
   int cs;
-  return splitkv_count(B, H, Tq, Tk, dtype, num_splits, num_sms, &cs);
+  return splitkv_count(B, H, Tq, Tk, d, dtype, num_splits, num_sms, &cs);
 }
 
 size_t attn_fwd_splitkv_workspace_size(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype,
@@ -366,11 +373,13 @@ attn_status_t attn_fwd_f32_blocked(const float* Q, const float* K, const float* 
 size_t attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype,
                                int deterministic) {
   if (check_common(B, H, Tq, Tk, d, dv, 1.0f, 0, dtype) != ATTN_OK) return 0;
+  if (dtype == ATTN_BF16 && (d > 128 || dv > 128)) return 0;   // no bf16 backward there
   return bwd_layout(B, H, Tq, Tk, d, dtype, deterministic).total;
 }
 
 int attn_bwd_dq_splits(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype, int deterministic) {
   if (check_common(B, H, Tq, Tk, d, dv, 1.0f, 0, dtype) != ATTN_OK) return -1;
+  if (dtype == ATTN_BF16 && (d > 128 || dv > 128)) return -1;
   if (deterministic != 0 && deterministic != 1) return -1;
   return bwd_layout(B, H, Tq, Tk, d, dtype, deterministic).dq_splits;
 }
@@ -385,6 +394,9 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
                        int phase, void* stream) {
   attn_status_t s = check_common(B, H, Tq, Tk, d, dv, scale, causal, dtype);
   if (s != ATTN_OK) return s;
+  // the tensor-core backward keeps dV and dK accumulators of d and dv columns
+  // next to two 128-column score buffers in TMEM: d, dv <= 128
+  if (dtype == ATTN_BF16 && (d > 128 || dv > 128)) return ATTN_ERR_UNSUPPORTED;
   if (phase < 0 || phase > 5) return ATTN_ERR_INVALID_ARG;
   if (deterministic != 0 && deterministic != 1) return ATTN_ERR_INVALID_ARG;
   const size_t es = elem_size(dtype);

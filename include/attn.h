@@ -39,7 +39,10 @@
  *              tile does not fit in shared memory, above d = dv = 150 or so)
  *   ATTN_BF16: d in {64, 128} and dv in {64, 128} (d != dv allowed: the
  *              page's task takes V with its own head dimension), any B, H,
- *              Tq, Tk >= 0
+ *              Tq, Tk >= 0; and for the forward alone (attn_fwd,
+ *              attn_fwd_splitkv) also d = 256 with dv in {64, 128, 256}.
+ *              attn_bwd with bf16 and d or dv above 128 returns
+ *              ATTN_ERR_UNSUPPORTED (use ATTN_F32 there).
  * Zero-sized problems are valid: Tk == 0 gives O = 0 and LSE = -inf (a row
  * with no allowed key), and empty gradients are written as zeros.
  */
@@ -111,7 +114,8 @@ ATTN_API attn_status_t attn_fwd_f32_blocked(const float* Q, const float* K, cons
  * per split); num_splits >= 1 asks for that many, clamped to the number of
  * 128-key tiles and 64. S = 1 is attn_fwd itself (no workspace). bf16 only
  * for S > 1: an fp32 problem with num_splits > 1 returns ATTN_ERR_UNSUPPORTED
- * (num_splits 0 or 1 runs the fp32 attn_fwd). `workspace` (256-byte aligned,
+ * (num_splits 0 or 1 runs the fp32 attn_fwd). bf16 with d = 256 always runs
+ * unsplit (S = 1). `workspace` (256-byte aligned,
  * at least attn_fwd_splitkv_workspace_size bytes, not overlapping any other
  * argument; may be NULL when that is 0) holds Opart [S][B*H*Tq][dv] then
  * LSEpart [S][B*H*Tq], both fp32; else ATTN_ERR_WORKSPACE. Other errors as

@@ -67,7 +67,8 @@ def _fwd(**kw):
     (dict(dtype=7), B.ATTN_ERR_INVALID_ARG),
     (dict(d=96, dv=96), B.ATTN_ERR_UNSUPPORTED),
     (dict(d=64, dv=96), B.ATTN_ERR_UNSUPPORTED),
-    (dict(d=256, dv=128), B.ATTN_ERR_UNSUPPORTED),
+    (dict(d=128, dv=256), B.ATTN_ERR_UNSUPPORTED),   # dv = 256 only with d = 256
+    (dict(d=512, dv=128), B.ATTN_ERR_UNSUPPORTED),
     (dict(dtype=B.ATTN_F32, d=257), B.ATTN_ERR_UNSUPPORTED),
     (dict(Q=None), B.ATTN_ERR_INVALID_ARG),
     (dict(LSE=None), B.ATTN_ERR_INVALID_ARG),
@@ -149,6 +150,7 @@ def _bwd(**kw):
     (dict(dO=None), B.ATTN_ERR_INVALID_ARG),
     (dict(dV=0x900008), B.ATTN_ERR_MISALIGNED),
     (dict(d=80, dv=80), B.ATTN_ERR_UNSUPPORTED),
+    (dict(d=256, dv=256), B.ATTN_ERR_UNSUPPORTED),   # the d = 256 tensor-core path is forward only
 ])
 def test_backward_host_validation(lib, kw, status):
     assert _bwd(**kw) == status
@@ -184,3 +186,10 @@ def test_error_text_carries_status(lib):
         B.attn_fwd(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 1, 1, 8, 8, 96, 96, 0.1, 0, B.ATTN_BF16,
                    stream=0)
     assert "unsupported" in str(e.value)
+
+
+def test_d256_bf16_is_forward_only(lib):
+    assert B.attn_bwd_workspace_size(1, 1, 128, 128, 256, 256, B.ATTN_BF16, 1) == 0
+    assert B.attn_bwd_dq_splits(1, 1, 128, 128, 256, 256, B.ATTN_BF16, 1) == -1
+    assert B.attn_fwd_splitkv_splits(1, 1, 128, 8192, 256, 256, B.ATTN_BF16, 8) == 1
+

@@ -48,11 +48,13 @@ def test_reduce_max_without_process_group_is_identity():
     assert bench.reduce_max(3.5) == 3.5
 
 
-@pytest.mark.parametrize("name", ["c1", "c1_causal", "c2", "c3", "c4", "c5"])
+@pytest.mark.parametrize("name", ["c1", "c1_causal", "c2", "c3", "c4", "c5", "s1", "m1", "w256"])
 def test_row_flops_sum_to_the_workload_count(name):
     w = WORKLOADS[name]
     one_head = (w.fwd_flop() + w.bwd_flop()) / (w.B * w.H)
     assert np.isclose(bench.useful_flops_rows(w, np.arange(w.Tq)), one_head, rtol=1e-12)
+    fwd_head = w.fwd_flop() / (w.B * w.H)
+    assert np.isclose(bench.useful_flops_rows(w, np.arange(w.Tq), fwd_only=True), fwd_head, rtol=1e-12)
 
 
 def test_spread_rows_are_sorted_unique_and_in_range():

@@ -105,6 +105,48 @@ MIXED_DV_SHAPES = [  # B, H, Tq, Tk, d, dv
 ]
 
 
+D256_SHAPES = [  # B, H, Tq, Tk, dv: d = 256 (one query tile per unit, 64-key tiles)
+    (1, 2, 300, 257, 256),
+    (2, 1, 129, 700, 128),
+    (1, 1, 1, 1, 64),
+    (1, 2, 512, 512, 256),
+    (3, 60, 200, 200, 256),   # several units per CTA
+    (1, 1, 1000, 64, 128),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", D256_SHAPES)
+def test_bf16_d256_forward(shape, causal):
+    B, H, Tq, Tk, dv = shape
+    d = 256
+    x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, dv), seed=Tq + 3 * Tk + dv, dtype=torch.bfloat16,
+                    device=DEV)
+    scale = 1 / math.sqrt(d)
+    o, lse = run_fwd(x, causal, scale)
+    assert o.shape == (B, H, Tq, dv)
+    heads = [(0, 0), (B - 1, H - 1)]
+    O, L = oracle_fwd(x, causal, scale, heads=heads)
+    check_o(torch.stack([o[b, h] for b, h in heads]), np.stack([np.asarray(O)[b, h] for b, h in heads]),
+            torch.bfloat16)
+    check_lse(torch.stack([lse[b, h] for b, h in heads]), np.stack([np.asarray(L)[b, h] for b, h in heads]),
+              torch.bfloat16)
+
+
+def test_bf16_d256_large_logits():
+    # scores beyond +-1000 across 64-key tiles stay finite and exact
+    B, H, T, d = 1, 1, 384, 256
+    x = make_random((B, H, T, d), (B, H, T, d), (B, H, T, d), seed=6, dtype=torch.float32, device="cpu")
+    sign = torch.where((torch.arange(T) // 64) % 2 == 0, 30.0, -30.0).view(1, 1, T, 1)
+    x = {k: (v * sign if k == "K" else v).to(torch.bfloat16).to(DEV) for k, v in x.items()}
+    for causal in (False, True):
+        o, lse = run_fwd(x, causal, 1.0)
+        O, L = oracle_fwd(x, causal, 1.0)
+        assert np.abs(L).max() > 1000
+        check_o(o, O, torch.bfloat16)
+        check_lse(lse, L, torch.bfloat16)
+
+
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("shape", MIXED_DV_SHAPES)
 def test_bf16_d_neq_dv(shape, causal):
@@ -156,7 +198,8 @@ def test_bf16_c2_full_size():
     check_lse(lse, L, torch.bfloat16)
 
 
-@pytest.mark.parametrize("name,heads", [("c3", [(0, 0), (1, 15)]), ("c5", [(0, 7)])])
+@pytest.mark.parametrize("name,heads", [("c3", [(0, 0), (1, 15)]), ("c5", [(0, 7)]), ("m1", [(1, 3)]),
+                                        ("w256", [(0, 0), (1, 15)])])
 def test_bf16_full_size_sampled_heads(name, heads):
     w = WORKLOADS[name]
     x = make_inputs(w, DEV, with_dO=False)
