@@ -290,12 +290,12 @@ attn_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, flo
   if (dtype == ATTN_F32) {
     e = launch_fwd_f32(a);
   } else {
-    // the d = 256 forward streams 64-key tiles of K and V
-    const unsigned kv_rows = d == 256 ? 64u : 128u;
+    // the d = 256 forward loads V by 64-key halves of its 128-key tiles
+    const unsigned v_rows = d == 256 ? 64u : 128u;
     CUtensorMap mq, mk, mv;
     if ((s = make_map(&mq, Q, d, Tq, static_cast<int>(bh))) != ATTN_OK) return s;
-    if ((s = make_map(&mk, K, d, Tk, static_cast<int>(bh), false, kv_rows)) != ATTN_OK) return s;
-    if ((s = make_map(&mv, V, dv, Tk, static_cast<int>(bh), false, kv_rows)) != ATTN_OK) return s;
+    if ((s = make_map(&mk, K, d, Tk, static_cast<int>(bh))) != ATTN_OK) return s;
+    if ((s = make_map(&mv, V, dv, Tk, static_cast<int>(bh), false, v_rows)) != ATTN_OK) return s;
     a.tmQ = &mq;
     a.tmK = &mk;
     a.tmV = &mv;

@@ -4,17 +4,23 @@
 // an online softmax", section "Task"; "The Hidden Recurrence in Softmax
 // Attention", section "Chunk-wise Mode with Online Softmax Re-scale"), laid
 // out for a 256-wide Q row: a 128 x 256 bf16 Q tile is 64 KB, so a unit is one
-// 128-row query tile of one head (not two) and keys come in tiles of 64 (a
-// 64 x 256 K tile is 32 KB), through a five-slot K/V ring.
+// 128-row query tile of one head (not two). Keys come in tiles of 128 so that
+// the score product Q K^T has N = 128: with both operands in shared memory an
+// N = 64 product is held back by the shared-memory reads of its A operand
+// (about 63% of the tensor rate, against the full rate at N = 128). A K or V
+// tile is 64 KB (dv = 256), so each streams through a ring of five 32 KB
+// slots as two items: K by halves of d (two 128-row x 64-column boxes), V by
+// halves of the key range (dv / 64 boxes of 64 rows). Each half is released
+// as soon as the products that read it complete.
 //
 // Warp roles (8 warps): warp 0 lane 0 TMA producer; warp 1 MMA issuer (one
 // elected lane) and TMEM owner; warps 2-3 idle; warps 4-7 the softmax group,
 // one thread per query row.
-// TMEM (512 columns allocated): two score buffers of 64 fp32 columns at 0 and
-// 64, so the product S_{j+2} = Q K_{j+2}^T is issued as soon as P_j V_j has
-// read P_j out of its buffer while the softmax still works on S_{j+1}; the
-// accumulator O at [128, 128 + dv). P_j goes back over the first 32 columns
-// of its buffer as packed bf16 and is the A operand of P_j V_j.
+// TMEM (512 columns allocated): two score buffers of 128 fp32 columns at 0
+// and 128, so the product S_{j+2} = Q K_{j+2}^T is issued as soon as P_j V_j
+// has read P_j out of its buffer while the softmax still works on S_{j+1};
+// the accumulator O at [256, 256 + dv). P_j goes back over the first 64
+// columns of its buffer as packed bf16 and is the A operand of P_j V_j.
 // The lazy rescale of O (when the running max grows by more than TAU) waits
 // for the previous P V product, which the score product alone no longer
 // orders: every step past the first waits for that product's completion.
@@ -31,21 +37,22 @@ namespace attn {
 namespace fwd256 {
 
 constexpr int BM = 128;                  // query rows per unit
-constexpr int BN = 64;                   // keys per tile
+constexpr int BN = 128;                  // keys per tile
 constexpr int HD = 256;                  // Q / K head size
 constexpr int QBOX = BM * 64 * 2;        // TMA box of Q: 128 rows x 64 bf16
-constexpr int KBOX = BN * 64 * 2;        // TMA box of K or V: 64 rows x 64 bf16
+constexpr int KBOX = BN * 64 * 2;        // TMA box of K: 128 rows x 64 bf16
+constexpr int VBOX = 64 * 64 * 2;        // TMA box of V: 64 rows x 64 bf16
 constexpr float TAU = 8.0f;              // lazy-rescale threshold (log2 units)
 constexpr int NUM_THREADS = 256;
-constexpr uint32_t T_O = 128;            // TMEM column of the O accumulator
+constexpr uint32_t T_O = 256;            // TMEM column of the O accumulator
 
 template <int HV>
 struct Cfg {
   static constexpr int VB = HV / 64;             // 64-column boxes per V row
   static constexpr int TILE_Q = BM * HD * 2;     // 64 KB
-  static constexpr int TILE_K = BN * HD * 2;     // 32 KB
-  static constexpr int TILE_V = BN * HV * 2;     // <= 32 KB
-  static constexpr int SLOT = TILE_K;
+  static constexpr int ITEM_K = 2 * KBOX;        // half of d of a K tile: 32 KB
+  static constexpr int ITEM_V = VB * VBOX;       // half of the keys of a V tile: <= 32 KB
+  static constexpr int SLOT = ITEM_K;
   static constexpr int NSLOT = 5;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = OFF_Q + TILE_Q;
@@ -64,13 +71,13 @@ struct Params {
   float* LSE;
   uint32_t* status;
   UnitOrder order;   // units: (head, 128-row query tile)
-  int n_kv_tiles;    // 64-key tiles
+  int n_kv_tiles;    // 128-key tiles
   float sc2;         // scale * log2(e)
 };
 
-// 64-key tiles that query tile qt sees.
+// 128-key tiles that query tile qt sees.
 __device__ __forceinline__ int tiles_of(const Params& P, int qt) {
-  return P.p.causal ? min(P.n_kv_tiles, 2 * qt + 2) : P.n_kv_tiles;
+  return P.p.causal ? min(P.n_kv_tiles, qt + 1) : P.n_kv_tiles;
 }
 
 template <int HV>
@@ -126,7 +133,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int grid = gridDim.x, cta = blockIdx.x;
-  // ring item i: K of tile i / 2 (even i) or its V (odd i), in slot i % NSLOT
+  // Ring items, in the order the MMAs consume them: K_0, K_1, then V_j
+  // followed by K_{j+2} for each j (a unit of one tile: K_0, V_0); every
+  // tile is two items (K: d columns [0, 128) then [128, 256); V: keys
+  // [0, 64) then [64, 128) of the tile). Item i sits in slot i % NSLOT.
   auto slot = [](uint32_t item) { return static_cast<int>(item % C::NSLOT); };
   auto par = [](uint32_t item) { return (item / C::NSLOT) & 1u; };
 
@@ -144,14 +154,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!(ok = ptx::mbar_wait(q_empty, (u_it & 1u) ^ 1u, w))) break;
       ptx::mbar_arrive_expect_tx(q_full, C::TILE_Q);
       for (int b = 0; b < HD / 64; ++b) ptx::tma_load_3d(sQ + b * QBOX, &tmQ, q_full, b * 64, qt * BM, bh);
-      for (int j = 0; ok && j < nk; ++j) {
-        for (int kv = 0; kv < 2; ++kv, ++item) {
+      auto load = [&](int kv, int j) {   // both halves of K (kv = 0) or V (kv = 1) of key tile j
+        for (int h = 0; ok && h < 2; ++h) {
           const int sl = slot(item);
-          if (!(ok = ptx::mbar_wait(kv_empty + sl, par(item) ^ 1u, w))) break;
-          ptx::mbar_arrive_expect_tx(kv_full + sl, kv ? C::TILE_V : C::TILE_K);
-          for (int b = 0; b < (kv ? C::VB : HD / 64); ++b)
-            ptx::tma_load_3d(sKV + sl * C::SLOT + b * KBOX, kv ? &tmV : &tmK, kv_full + sl, b * 64, j * BN, bh);
+          if (!(ok = ptx::mbar_wait(kv_empty + sl, par(item) ^ 1u, w))) return;
+          uint8_t* dst = sKV + sl * C::SLOT;
+          if (kv == 0) {
+            ptx::mbar_arrive_expect_tx(kv_full + sl, C::ITEM_K);
+            for (int b = 0; b < 2; ++b)
+              ptx::tma_load_3d(dst + b * KBOX, &tmK, kv_full + sl, (2 * h + b) * 64, j * BN, bh);
+          } else {
+            ptx::mbar_arrive_expect_tx(kv_full + sl, C::ITEM_V);
+            for (int b = 0; b < C::VB; ++b)
+              ptx::tma_load_3d(dst + b * VBOX, &tmV, kv_full + sl, b * 64, j * BN + h * 64, bh);
+          }
+          ++item;
         }
+      };
+      for (int j = 0; ok && j < 2 && j < nk; ++j) load(0, j);
+      for (int j = 0; ok && j < nk; ++j) {
+        load(1, j);
+        if (ok && j + 2 < nk) load(0, j + 2);
       }
       ++u_it;
     }
@@ -167,74 +190,83 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // issues the MMAs and commits (a commit tracks its own thread's MMAs).
     ptx::WaitCtx w{abort_flag, P.status, 3u};
     const uint32_t sQa = ptx::smem_u32(sQ), sKVa = ptx::smem_u32(sKV);
-    auto mma_S = [&](uint32_t g, int sl) {   // S_g = Q K_g^T into score buffer g & 1
-      const uint32_t d = tmem + 64 * (g & 1u);
+    // half h of S_g = Q K_g^T (d columns [128 h, 128 h + 128)) into score
+    // buffer g & 1, from the K item in slot sl
+    auto mma_S = [&](uint32_t g, int h, int sl) {
+      const uint32_t d = tmem + 128 * (g & 1u);
       const uint64_t a0 = ptx::sdesc_sw128(sQa, 16, 1024);
       const uint64_t b0 = ptx::sdesc_sw128(sKVa + sl * C::SLOT, 16, 1024);
 #pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk)
-        ptx::mma_ss(d, ptx::sdesc_advance(a0, (kk >> 2) * QBOX + (kk & 3) * 32),
-                    ptx::sdesc_advance(b0, (kk >> 2) * KBOX + (kk & 3) * 32), C::IDESC_S, kk > 0 ? 1u : 0u);
+      for (int kk = 0; kk < 8; ++kk)
+        ptx::mma_ss(d, ptx::sdesc_advance(a0, (2 * h + (kk >> 2)) * QBOX + (kk & 3) * 32),
+                    ptx::sdesc_advance(b0, (kk >> 2) * KBOX + (kk & 3) * 32), C::IDESC_S,
+                    (h > 0 || kk > 0) ? 1u : 0u);
     };
-    auto mma_PV = [&](uint32_t g, int sl, bool acc) {   // O (+)= P_g V_g
-      const uint32_t a = tmem + 64 * (g & 1u);            // P_g: bf16 pairs in the first 32 columns
-      const uint64_t b0 = ptx::sdesc_sw128(sKVa + sl * C::SLOT, KBOX, 1024);
+    // half h of O (+)= P_g V_g (keys [64 h, 64 h + 64) of the tile), from the
+    // V item in slot sl
+    auto mma_PV = [&](uint32_t g, int h, int sl, bool acc) {
+      const uint32_t a = tmem + 128 * (g & 1u) + 32 * h;   // P_g: bf16 pairs in the first 64 columns
+      const uint64_t b0 = ptx::sdesc_sw128(sKVa + sl * C::SLOT, VBOX, 1024);
 #pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk)
+      for (int kk = 0; kk < 4; ++kk)
         ptx::mma_ts(tmem + T_O, a + kk * 8, ptx::sdesc_advance(b0, kk * 2048), C::IDESC_PV,
-                    (acc || kk > 0) ? 1u : 0u);
+                    (acc || h > 0 || kk > 0) ? 1u : 0u);
     };
     auto wait = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, w));
     };
     uint32_t g0 = 0, u_it = 0;   // g0: global index of the unit's first key tile
+    uint32_t item = 0;           // ring position, advanced in the producer's order
     bool ok = true, moved = false;
     int bh, qt;
     for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qt); ++round) {
       const int nk = tiles_of(P, qt);
       if (!(ok = wait(q_full, u_it & 1u))) break;
-      // the scores of the first two key tiles
-      for (int jj = 0; jj < 2 && jj < nk; ++jj) {
-        const uint32_t g = g0 + jj, ik = 2 * g;
-        if (!(ok = wait(kv_full + slot(ik), par(ik)))) break;
-        ptx::tc_fence_after();
-        if (ptx::elect_one()) {
-          moved |= lane != 0;
-          mma_S(g, slot(ik));
-          ptx::mma_commit(s_full + (g & 1u));
-          ptx::mma_commit(kv_empty + slot(ik));
-          if (jj + 1 == nk) ptx::mma_commit(q_empty);   // the unit's last S product is out
-        }
-        __syncwarp();
-      }
-      if (!ok) break;
-      for (int j = 0; j < nk; ++j) {
-        const uint32_t g = g0 + j, iv = 2 * g + 1;
-        if (!(ok = wait(p_full + (g & 1u), (g >> 1) & 1u))) break;
-        if (!(ok = wait(kv_full + slot(iv), par(iv)))) break;
-        ptx::tc_fence_after();
-        if (ptx::elect_one()) {
-          moved |= lane != 0;
-          mma_PV(g, slot(iv), j > 0);
-          ptx::mma_commit(kv_empty + slot(iv));
-          ptx::mma_commit(pv_done);
-          if (j + 1 == nk) ptx::mma_commit(o_full);
-        }
-        __syncwarp();
-        if (j + 2 < nk) {
-          // S_{g+2} into the buffer P_g V_g has just read (MMAs run in issue order)
-          const uint32_t ik = 2 * (g + 2);
-          if (!(ok = wait(kv_full + slot(ik), par(ik)))) break;
+      // S_g in two halves, each released as soon as it has been read; the
+      // second half also completes the score buffer (and, for the unit's
+      // last tile, its use of Q)
+      auto issue_S = [&](uint32_t g, bool last_S) {
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t ik = item++;
+          if (!(ok = wait(kv_full + slot(ik), par(ik)))) return;
           ptx::tc_fence_after();
           if (ptx::elect_one()) {
             moved |= lane != 0;
-            mma_S(g + 2, slot(ik));
-            ptx::mma_commit(s_full + (g & 1u));
+            mma_S(g, h, slot(ik));
             ptx::mma_commit(kv_empty + slot(ik));
-            if (j + 3 == nk) ptx::mma_commit(q_empty);   // the unit's last S product is out
+            if (h == 1) {
+              ptx::mma_commit(s_full + (g & 1u));
+              if (last_S) ptx::mma_commit(q_empty);
+            }
           }
           __syncwarp();
         }
+      };
+      // the scores of the first two key tiles
+      for (int jj = 0; ok && jj < 2 && jj < nk; ++jj) issue_S(g0 + jj, jj + 1 == nk);
+      if (!ok) break;
+      for (int j = 0; j < nk; ++j) {
+        const uint32_t g = g0 + j;
+        if (!(ok = wait(p_full + (g & 1u), (g >> 1) & 1u))) break;
+        for (int h = 0; ok && h < 2; ++h) {
+          const uint32_t iv = item++;
+          if (!(ok = wait(kv_full + slot(iv), par(iv)))) break;
+          ptx::tc_fence_after();
+          if (ptx::elect_one()) {
+            moved |= lane != 0;
+            mma_PV(g, h, slot(iv), j > 0);
+            ptx::mma_commit(kv_empty + slot(iv));
+            if (h == 1) {
+              ptx::mma_commit(pv_done);
+              if (j + 1 == nk) ptx::mma_commit(o_full);
+            }
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
+        // S_{g+2} into the buffer P_g V_g has just read (MMAs run in issue order)
+        if (j + 2 < nk) issue_S(g + 2, j + 3 == nk);
+        if (!ok) break;
       }
       if (!ok) break;
       g0 += nk;
@@ -264,14 +296,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float m_used = -CUDART_INF_F, l = 0.f;
       for (int j = 0; j < nk; ++j) {
         const uint32_t g = g0 + j;
-        const uint32_t tS = tmem + lane_off + 64 * (g & 1u);
+        const uint32_t tS = tmem + lane_off + 128 * (g & 1u);
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(s_full + (g & 1u), (g >> 1) & 1u, w)))) break;
         ptx::tc_fence_after();
-        uint32_t raw[2][32];
-        ptx::tmem_ld32(tS, raw[0]);
-        ptx::tmem_ld32(tS + 32, raw[1]);
-        ptx::tmem_ld_wait(raw[0]);
-        ptx::tmem_ld_wait(raw[1]);
+        uint32_t raw[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32 * c, raw[c]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld_wait(raw[c]);
         float* s = reinterpret_cast<float*>(&raw[0][0]);
         const int kv0 = j * BN;
         if ((P.p.causal && kv0 + BN - 1 > qt * BM) || kv0 + BN > Tk) {
@@ -304,15 +336,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float2 ls[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) ls[k] = make_float2(0.f, 0.f);
-        uint32_t pk[32];
+        // P over the first 64 columns of the buffer, 32 at a time (the scores
+        // of both halves are already in registers)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float2 x = ptx::ffma2(make_float2(s[2 * i], s[2 * i + 1]), sc2v, nrefv);
-          const float2 pp = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
-          ls[i & 3] = ptx::fadd2(ls[i & 3], pp);
-          pk[i] = ptx::pack_bf16(pp.x, pp.y);
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int c = 64 * hh + 2 * i;
+            const float2 x = ptx::ffma2(make_float2(s[c], s[c + 1]), sc2v, nrefv);
+            const float2 pp = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+            ls[i & 3] = ptx::fadd2(ls[i & 3], pp);
+            pk[i] = ptx::pack_bf16(pp.x, pp.y);
+          }
+          ptx::tmem_st32(tS + 32 * hh, pk);
         }
-        ptx::tmem_st32(tS, pk);
         l += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
         if (j > 0) {
           // the previous P V product is complete before O is rescaled (and

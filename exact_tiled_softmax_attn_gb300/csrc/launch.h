@@ -73,8 +73,8 @@ cudaError_t launch_bwd_f32(const LaunchBwd& a);
 
 // bf16 (tcgen05 / TMA)
 cudaError_t launch_fwd_bf16(const LaunchFwd& a);
-// d = 256 (dv 64, 128 or 256): one 128-row query tile per unit, 64-key tiles;
-// tmK / tmV must be built with 64-row boxes
+// d = 256 (dv 64, 128 or 256): one 128-row query tile per unit, 128-key
+// tiles; tmK must be built with 128-row boxes and tmV with 64-row boxes
 cudaError_t launch_fwd_bf16_d256(const LaunchFwd& a);
 cudaError_t launch_bwd_bf16(const LaunchBwd& a);
 

@@ -105,13 +105,15 @@ MIXED_DV_SHAPES = [  # B, H, Tq, Tk, d, dv
 ]
 
 
-D256_SHAPES = [  # B, H, Tq, Tk, dv: d = 256 (one query tile per unit, 64-key tiles)
+D256_SHAPES = [  # B, H, Tq, Tk, dv: d = 256 (one query tile per unit, 128-key tiles)
     (1, 2, 300, 257, 256),
     (2, 1, 129, 700, 128),
     (1, 1, 1, 1, 64),
     (1, 2, 512, 512, 256),
     (3, 60, 200, 200, 256),   # several units per CTA
-    (1, 1, 1000, 64, 128),
+    (1, 1, 1000, 64, 128),    # the second 64-key half of the only V tile lies past Tk
+    (1, 2, 130, 100, 256),    # a partial second half
+    (1, 1, 640, 1000, 64),    # causal units of 1 to 5 key tiles, ragged last tile
 ]
 
 
