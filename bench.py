@@ -27,6 +27,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "attention TFLOP/s fwd+bwd (bf16, causal, 1 GB300)"
+METRIC_FWD = "attention TFLOP/s fwd only (bf16, causal, 1 GB300)"   # --fwd-only
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
 # the sources each profiled kernel is built from (a committed DRAM-traffic
@@ -248,7 +249,7 @@ def run_reference(args, w):
     sample = (f"float64 numpy oracle, {'fwd' if fo else 'fwd+bwd'} of {rows.size} query rows spread over "
               f"head (0,0) of {w.name} "
               f"per step (useful FLOPs of those rows)")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+    line = {"impl": "reference", "metric": METRIC_FWD if fo else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_config(w),
@@ -505,7 +506,8 @@ def run_ours(args, w):
                 "peak_source": f"derived FP32 FMA {peak:.1f}" if f32 else f"{peaks['source']} bf16_tflops {peak}",
                 "kernels": kernels})
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC_FWD if args.fwd_only else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32" if f32 else "bf16", "data": "synthetic",
         "config": cfg,
