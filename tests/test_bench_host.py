@@ -61,3 +61,28 @@ def test_spread_rows_are_sorted_unique_and_in_range():
     w = WORKLOADS["c3"]
     r = bench.spread_rows(w, 1000)
     assert r[0] == 0 and r[-1] == w.Tq - 1 and np.all(np.diff(r) > 0)
+
+
+def test_oracle_legs_forward_only_on_a_small_workload():
+    from exact_tiled_softmax_attn_gb300.workloads import make_inputs
+    w = WORKLOADS["c1_causal"]
+    x = make_inputs(w)
+    rows = bench.spread_rows(w, 16)
+    assert bench.oracle_sample(w, x, rows, fwd_only=True) >= 0.0
+    cb = bench.cpu_baseline(w, x, target_s=0.05, fwd_only=True)
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["sample"].startswith("float64 numpy oracle, fwd of")
+
+
+@pytest.mark.parametrize("fwd_only", [False, True])
+def test_reference_arm_prints_one_json_line(fwd_only):
+    import json
+    import subprocess
+    import sys
+    cmd = [sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl", "reference", "--workload", "c1",
+           "--steps", "3", "--warmup", "3"] + (["--fwd-only"] if fwd_only else [])
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, env={**os.environ, "CUDA_VISIBLE_DEVICES": ""})
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 3
+    assert line["metric"] == (bench.METRIC_FWD if fwd_only else bench.METRIC)
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
