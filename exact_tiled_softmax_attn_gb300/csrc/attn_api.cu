@@ -184,17 +184,19 @@ BwdLayout bwd_layout(int B, int H, int Tq, int Tk, int d, attn_dtype_t dt, int d
 }
 
 // Split-KV forward: effective number of key splits for a request (0 = pick
-// one so that the query-tile pairs times the splits fill the SMs once, with
+// one so that the forward's units times the splits fill the SMs once, with
 // at least two key tiles per split), clamped to [1, min(key tiles, 64)]; the
-// key tiles per split go to *split_tiles. fp32 problems and d = 256 never split.
+// key tiles per split go to *split_tiles. fp32 problems never split. A unit
+// is a pair of 128-row query tiles for d <= 128 and one query tile for
+// d = 256; key tiles are 128 keys for both.
 int splitkv_count(int B, int H, int Tq, int Tk, int d, attn_dtype_t dt, int req, int num_sms, int* split_tiles) {
-  const bool d_is_wide = d > 128;   // the d = 256 forward has no split variant
+  const int rows_per_unit = d > 128 ? 128 : 256;
   const int nkb = (Tk + 127) / 128;
   int S = req;
-  if (dt != ATTN_BF16 || nkb <= 1 || B == 0 || H == 0 || Tq == 0 || d_is_wide) {
+  if (dt != ATTN_BF16 || nkb <= 1 || B == 0 || H == 0 || Tq == 0) {
     S = 1;
   } else if (req == 0) {
-    const long long units = static_cast<long long>(B) * H * ((Tq + 255) / 256);
+    const long long units = static_cast<long long>(B) * H * ((Tq + rows_per_unit - 1) / rows_per_unit);
     S = units >= num_sms ? 1 : static_cast<int>((num_sms + units - 1) / units);
     S = S < nkb / 2 ? S : (nkb / 2 > 1 ? nkb / 2 : 1);
   }

@@ -70,9 +70,17 @@ struct Params {
   __nv_bfloat16* O;
   float* LSE;
   uint32_t* status;
-  UnitOrder order;   // units: (head, 128-row query tile)
+  UnitOrder order;   // units: (head, 128-row query tile [, key range])
   int n_kv_tiles;    // 128-key tiles
   float sc2;         // scale * log2(e)
+  // Split-KV mode (n_splits > 1): key range s of a query tile covers key
+  // tiles [s * split_tiles, (s + 1) * split_tiles) and writes its normalised
+  // partial output and log-sum-exp (fp32) to Opart [n_splits][B*H*Tq][dv]
+  // and LSEpart [n_splits][B*H*Tq] instead of O and LSE.
+  int n_splits;
+  int split_tiles;
+  float* Opart;
+  float* LSEpart;
 };
 
 // 128-key tiles that query tile qt sees.
@@ -80,7 +88,25 @@ __device__ __forceinline__ int tiles_of(const Params& P, int qt) {
   return P.p.causal ? min(P.n_kv_tiles, qt + 1) : P.n_kv_tiles;
 }
 
-template <int HV>
+// Work unit `blk`: query tile qt, key range sp, first key tile j0 and tile
+// count nk. nk = 0 for a range that starts past the query tile's last key
+// tile (causal): no role touches such a unit and the merge never reads it.
+template <bool SPLIT>
+__device__ __forceinline__ void unit_range(const Params& P, int blk, int* qt, int* sp, int* j0, int* nk) {
+  if (!SPLIT) {
+    *qt = blk;
+    *sp = 0;
+    *j0 = 0;
+    *nk = tiles_of(P, blk);
+    return;
+  }
+  *qt = blk / P.n_splits;
+  *sp = blk - *qt * P.n_splits;
+  *j0 = *sp * P.split_tiles;
+  *nk = max(0, min(tiles_of(P, *qt) - *j0, P.split_tiles));
+}
+
+template <int HV, bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const Params P) {
@@ -148,9 +174,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tma_prefetch_desc(&tmV);
     uint32_t item = 0, u_it = 0;
     bool ok = true;
-    int bh, qt;
-    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qt); ++round) {
-      const int nk = tiles_of(P, qt);
+    int bh, blk;
+    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &blk); ++round) {
+      int qt, sp, j0, nk;
+      unit_range<SPLIT>(P, blk, &qt, &sp, &j0, &nk);
+      if (nk == 0) continue;
       if (!(ok = ptx::mbar_wait(q_empty, (u_it & 1u) ^ 1u, w))) break;
       ptx::mbar_arrive_expect_tx(q_full, C::TILE_Q);
       for (int b = 0; b < HD / 64; ++b) ptx::tma_load_3d(sQ + b * QBOX, &tmQ, q_full, b * 64, qt * BM, bh);
@@ -162,11 +190,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (kv == 0) {
             ptx::mbar_arrive_expect_tx(kv_full + sl, C::ITEM_K);
             for (int b = 0; b < 2; ++b)
-              ptx::tma_load_3d(dst + b * KBOX, &tmK, kv_full + sl, (2 * h + b) * 64, j * BN, bh);
+              ptx::tma_load_3d(dst + b * KBOX, &tmK, kv_full + sl, (2 * h + b) * 64, (j0 + j) * BN, bh);
           } else {
             ptx::mbar_arrive_expect_tx(kv_full + sl, C::ITEM_V);
             for (int b = 0; b < C::VB; ++b)
-              ptx::tma_load_3d(dst + b * VBOX, &tmV, kv_full + sl, b * 64, j * BN + h * 64, bh);
+              ptx::tma_load_3d(dst + b * VBOX, &tmV, kv_full + sl, b * 64, (j0 + j) * BN + h * 64, bh);
           }
           ++item;
         }
@@ -218,9 +246,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t g0 = 0, u_it = 0;   // g0: global index of the unit's first key tile
     uint32_t item = 0;           // ring position, advanced in the producer's order
     bool ok = true, moved = false;
-    int bh, qt;
-    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qt); ++round) {
-      const int nk = tiles_of(P, qt);
+    int bh, blk;
+    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &blk); ++round) {
+      int qt, sp, j0, nk;
+      unit_range<SPLIT>(P, blk, &qt, &sp, &j0, &nk);
+      if (nk == 0) continue;
       if (!(ok = wait(q_full, u_it & 1u))) break;
       // S_g in two halves, each released as soon as it has been read; the
       // second half also completes the score buffer (and, for the unit's
@@ -289,9 +319,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int Tq = P.p.Tq, Tk = P.p.Tk;
     uint32_t g0 = 0, u_it = 0;
     bool ok = true;
-    int bh, qt;
-    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qt); ++round) {
-      const int nk = tiles_of(P, qt);
+    int bh, blk;
+    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &blk); ++round) {
+      int qt, sp, j0, nk;
+      unit_range<SPLIT>(P, blk, &qt, &sp, &j0, &nk);
+      if (nk == 0) continue;
       const int q_row = qt * BM + r;
       float m_used = -CUDART_INF_F, l = 0.f;
       for (int j = 0; j < nk; ++j) {
@@ -305,7 +337,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) ptx::tmem_ld_wait(raw[c]);
         float* s = reinterpret_cast<float*>(&raw[0][0]);
-        const int kv0 = j * BN;
+        const int kv0 = (j0 + j) * BN;
         if ((P.p.causal && kv0 + BN - 1 > qt * BM) || kv0 + BN > Tk) {
           const int lim = min(Tk - kv0, P.p.causal ? q_row - kv0 + 1 : BN);   // keys [0, lim) allowed
 #pragma unroll
@@ -379,6 +411,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::tc_fence_after();
       const float inv_l = (l > 0.f) ? 1.0f / l : 0.f;
       const bool row_ok = q_row < Tq;
+      const float lse_row = (l > 0.f) ? (m_used + log2f(l)) * 0.69314718055994530942f : -CUDART_INF_F;
+      if (SPLIT) {
+        // partial result of this key range: O_s = A / l in fp32 and LSE_s
+        const size_t rows = static_cast<size_t>(P.p.B) * P.p.H * Tq;
+        const size_t row = static_cast<size_t>(sp) * rows + static_cast<size_t>(bh) * Tq + (row_ok ? q_row : 0);
+        float* prow = P.Opart + row * HV;
+#pragma unroll 1
+        for (int c = 0; c < HV / 32; ++c) {
+          uint32_t o[32];
+          ptx::tmem_ld32(tO + c * 32, o);
+          ptx::tmem_ld_wait(o);
+          if (row_ok) {
+            float4* dst = reinterpret_cast<float4*>(prow + c * 32);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                   __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+          }
+        }
+        if (row_ok) P.LSEpart[row] = lse_row;
+        ptx::tc_fence_before();
+        g0 += nk;
+        ++u_it;
+        continue;
+      }
       __nv_bfloat16* orow = P.O + (static_cast<size_t>(bh) * Tq + (row_ok ? q_row : 0)) * HV;
 #pragma unroll
       for (int c = 0; c < HV / 32; ++c) {
@@ -395,9 +452,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int v = 0; v < 4; ++v) dst[v] = make_uint4(ob[4 * v], ob[4 * v + 1], ob[4 * v + 2], ob[4 * v + 3]);
         }
       }
-      if (row_ok)
-        P.LSE[static_cast<size_t>(bh) * Tq + q_row] =
-            (l > 0.f) ? (m_used + log2f(l)) * 0.69314718055994530942f : -CUDART_INF_F;
+      if (row_ok) P.LSE[static_cast<size_t>(bh) * Tq + q_row] = lse_row;
       ptx::tc_fence_before();
       g0 += nk;
       ++u_it;
@@ -422,14 +477,19 @@ cudaError_t launch(const LaunchFwd& a) {
   P.LSE = a.LSE;
   P.status = a.status;
   P.n_kv_tiles = (a.p.Tk + BN - 1) / BN;
-  P.order.n_blocks = (a.p.Tq + BM - 1) / BM;
+  P.n_splits = a.n_splits > 1 ? a.n_splits : 1;
+  P.split_tiles = a.split_tiles;
+  P.Opart = a.Opart;
+  P.LSEpart = a.LSEpart;
+  const long long n_blocks = static_cast<long long>((a.p.Tq + BM - 1) / BM) * P.n_splits;
+  if (n_blocks * a.p.B * a.p.H > 0x7fffffffLL) return cudaErrorInvalidValue;
+  P.order.n_blocks = static_cast<int>(n_blocks);
   P.order.n_heads = a.p.B * a.p.H;
   P.order.heavy_last = a.p.causal ? 1 : 0;
   P.sc2 = a.p.scale * 1.4426950408889634f;
-  if (static_cast<long long>(P.order.n_blocks) * P.order.n_heads > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int units = P.order.count();
   const int grid = units < a.num_sms ? units : a.num_sms;
-  auto kern = attn_fwd_d256_kernel<HV>;
+  auto kern = P.n_splits > 1 ? attn_fwd_d256_kernel<HV, true> : attn_fwd_d256_kernel<HV, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, NUM_THREADS, C::SMEM, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, P);

@@ -24,7 +24,8 @@ namespace splitkv {
 constexpr int NT = 256;
 constexpr int kMaxSplits = 64;
 
-// One warp per output row; lane c handles columns [4c, 4c + 4) (dv <= 128).
+// One warp per output row; lane c handles columns [4c, 4c + 4) and, for dv
+// above 128, [128 + 4c, 128 + 4c + 4) (dv <= 256).
 __global__ void __launch_bounds__(NT) merge_kernel(const float* __restrict__ Opart, const float* __restrict__ LSEpart,
                                                    __nv_bfloat16* __restrict__ O, float* __restrict__ LSE,
                                                    long long rows, int Tq, int dv, int n_splits, int split_tiles,
@@ -35,7 +36,8 @@ __global__ void __launch_bounds__(NT) merge_kernel(const float* __restrict__ Opa
   for (long long r = warp_id; r < rows; r += n_warps) {
     const int q = static_cast<int>(r % Tq);
     // key tiles of this row's query tile, as the forward's units count them
-    // (query tiles pair up as 2 qb, 2 qb + 1)
+    // (the d <= 128 forward pairs query tiles as 2 qb, 2 qb + 1, the d = 256
+    // one takes them singly; with 128-key tiles either way)
     const int qt = q / 128;
     const int nt = causal ? min(qt + 1, n_kv_tiles) : n_kv_tiles;
     const int ns = min(n_splits, (nt + split_tiles - 1) / split_tiles);
@@ -44,7 +46,7 @@ __global__ void __launch_bounds__(NT) merge_kernel(const float* __restrict__ Opa
     float mx = -CUDART_INF_F;
 #pragma unroll 4
     for (int s = 0; s < ns; ++s) mx = fmaxf(mx, LSEpart[static_cast<long long>(s) * rows + r]);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
     float lse = -CUDART_INF_F;
     if (mx != -CUDART_INF_F) {
       float wsum = 0.f;
@@ -53,27 +55,37 @@ __global__ void __launch_bounds__(NT) merge_kernel(const float* __restrict__ Opa
         const float ls = LSEpart[static_cast<long long>(s) * rows + r];
         const float wgt = expf(ls - mx);   // 0 for a split with no allowed key
         wsum += wgt;
-        if (4 * lane < dv) {
-          const float4 o = reinterpret_cast<const float4*>(Opart + (static_cast<long long>(s) * rows + r) * dv)[lane];
-          acc.x = fmaf(wgt, o.x, acc.x);
-          acc.y = fmaf(wgt, o.y, acc.y);
-          acc.z = fmaf(wgt, o.z, acc.z);
-          acc.w = fmaf(wgt, o.w, acc.w);
+        const float4* orow = reinterpret_cast<const float4*>(Opart + (static_cast<long long>(s) * rows + r) * dv);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (4 * (lane + 32 * h) < dv) {
+            const float4 o = orow[lane + 32 * h];
+            acc[h].x = fmaf(wgt, o.x, acc[h].x);
+            acc[h].y = fmaf(wgt, o.y, acc[h].y);
+            acc[h].z = fmaf(wgt, o.z, acc[h].z);
+            acc[h].w = fmaf(wgt, o.w, acc[h].w);
+          }
         }
       }
       const float inv = 1.0f / wsum;
-      acc.x *= inv;
-      acc.y *= inv;
-      acc.z *= inv;
-      acc.w *= inv;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        acc[h].x *= inv;
+        acc[h].y *= inv;
+        acc[h].z *= inv;
+        acc[h].w *= inv;
+      }
       lse = mx + logf(wsum);
     }
-    if (4 * lane < dv) {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&lo);
-      pk.y = *reinterpret_cast<uint32_t*>(&hi);
-      reinterpret_cast<uint2*>(O + r * dv)[lane] = pk;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (4 * (lane + 32 * h) < dv) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc[h].x, acc[h].y), hi = __floats2bfloat162_rn(acc[h].z, acc[h].w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<uint32_t*>(&hi);
+        reinterpret_cast<uint2*>(O + r * dv)[lane + 32 * h] = pk;
+      }
     }
     if (lane == 0) LSE[r] = lse;
   }
@@ -85,7 +97,7 @@ cudaError_t launch_splitkv_merge(const Problem& p, const float* Opart, const flo
                                  int split_tiles, void* O, float* LSE, int num_sms, cudaStream_t s) {
   const long long rows = static_cast<long long>(p.B) * p.H * p.Tq;
   if (rows == 0) return cudaSuccess;
-  if (p.dv > 128 || p.dv % 4 != 0 || n_splits < 1 || n_splits > splitkv::kMaxSplits || split_tiles < 1)
+  if (p.dv > 256 || p.dv % 4 != 0 || n_splits < 1 || n_splits > splitkv::kMaxSplits || split_tiles < 1)
     return cudaErrorInvalidValue;
   const long long want = (rows + splitkv::NT / 32 - 1) / (splitkv::NT / 32);
   const int grid = static_cast<int>(want < num_sms * 16LL ? want : num_sms * 16LL);

@@ -110,12 +110,12 @@ ATTN_API attn_status_t attn_fwd_f32_blocked(const float* Q, const float* K, cons
  *   LSE = M + log sum_s w_s.
  * Same inputs, outputs, layout and mask as attn_fwd; O and LSE agree with
  * attn_fwd up to fp32 rounding order. num_splits = 0 picks S so that the
- * query-tile pairs times S fill the SMs about once (at least two key tiles
- * per split); num_splits >= 1 asks for that many, clamped to the number of
+ * forward's units (pairs of 128-row query tiles; single query tiles for
+ * d = 256) times S fill the SMs about once (at least two key tiles per
+ * split); num_splits >= 1 asks for that many, clamped to the number of
  * 128-key tiles and 64. S = 1 is attn_fwd itself (no workspace). bf16 only
  * for S > 1: an fp32 problem with num_splits > 1 returns ATTN_ERR_UNSUPPORTED
- * (num_splits 0 or 1 runs the fp32 attn_fwd). bf16 with d = 256 always runs
- * unsplit (S = 1). `workspace` (256-byte aligned,
+ * (num_splits 0 or 1 runs the fp32 attn_fwd). `workspace` (256-byte aligned,
  * at least attn_fwd_splitkv_workspace_size bytes, not overlapping any other
  * argument; may be NULL when that is 0) holds Opart [S][B*H*Tq][dv] then
  * LSEpart [S][B*H*Tq], both fp32; else ATTN_ERR_WORKSPACE. Other errors as

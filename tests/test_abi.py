@@ -191,5 +191,11 @@ def test_error_text_carries_status(lib):
 def test_d256_bf16_is_forward_only(lib):
     assert B.attn_bwd_workspace_size(1, 1, 128, 128, 256, 256, B.ATTN_BF16, 1) == 0
     assert B.attn_bwd_dq_splits(1, 1, 128, 128, 256, 256, B.ATTN_BF16, 1) == -1
-    assert B.attn_fwd_splitkv_splits(1, 1, 128, 8192, 256, 256, B.ATTN_BF16, 8) == 1
+    # the forward splits at d = 256 as at d <= 128: 64 key tiles in 8 ranges of 8
+    assert B.attn_fwd_splitkv_splits(1, 1, 128, 8192, 256, 256, B.ATTN_BF16, 8) == 8
+    assert B.attn_fwd_splitkv_splits(1, 1, 128, 8192, 256, 64, B.ATTN_BF16, 100) == 64
+    rows = 1 * 1 * 128
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert B.attn_fwd_splitkv_workspace_size(1, 1, 128, 8192, 256, 256, B.ATTN_BF16, 8) == \
+        r256(8 * rows * 256 * 4) + r256(8 * rows * 4)
 

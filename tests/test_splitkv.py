@@ -128,6 +128,32 @@ def test_splitkv_d_neq_dv(shape, causal):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", [
+    (1, 2, 128, 3000, 256, 5),    # dv = 256: the merge's second column half
+    (1, 1, 300, 1000, 128, 3),    # causal: the last range holds no key tile for the first query tile
+    (1, 1, 130, 2000, 64, 0),     # automatic split count
+    (2, 3, 1, 700, 256, 64),      # more splits asked for than key tiles
+])
+def test_splitkv_d256(shape, causal):
+    Bn, H, Tq, Tk, dv, ns = shape
+    d = 256
+    x = make_random((Bn, H, Tq, d), (Bn, H, Tk, d), (Bn, H, Tk, dv), seed=Tq + Tk + dv, dtype=torch.bfloat16,
+                    device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    o, lse = B.forward(x["Q"], x["K"], x["V"], causal=causal, scale=scale, num_splits=ns)
+    torch.cuda.synchronize()
+    assert B.attn_device_status() == B.ATTN_OK
+    O, L = ref.forward(x["Q"], x["K"], x["V"], scale, causal)
+    check_o(o, O, torch.bfloat16)
+    check_lse(lse, L, torch.bfloat16)
+    o1, lse1 = B.forward(x["Q"], x["K"], x["V"], causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert (lse - lse1).abs().max().item() <= 1e-4
+    assert (o.float() - o1.float()).abs().max().item() <= 2.0 ** -7 * max(1.0, o1.float().abs().max().item())
+
+
+@pytest.mark.gpu
 def test_splitkv_fp32_runs_the_plain_forward():
     """fp32 never splits: num_splits 0 or 1 gives exactly attn_fwd's result."""
     x = make_random((1, 2, 70, d := 48), (1, 2, 300, d), (1, 2, 300, 40), seed=5, dtype=torch.float32, device="cuda")
