@@ -108,6 +108,17 @@ Range range(const void* p, size_t bytes) {
   return {lo, lo + bytes};
 }
 
+// bf16 shapes. The forward takes d and dv in [8, 256], multiples of 8 (a row
+// of Q, K, V or O is then a whole number of 16-byte TMA and store units): the
+// kernels run on the next tile width up (64, 128 or 256 columns), the tensor
+// maps read the missing columns of Q, K and V as zeros, which leave S and the
+// first dv columns of O unchanged, and the epilogues write dv columns. The
+// backward takes d, dv in {64, 128}.
+bool bf16_fwd_shape(int d, int dv) { return d % 8 == 0 && dv % 8 == 0 && d <= 256 && dv <= 256; }
+bool bf16_bwd_shape(int d, int dv) { return (d == 64 || d == 128) && (dv == 64 || dv == 128); }
+// rows wider than 128 columns go to the d = 256 forward kernel
+bool bf16_wide(int d, int dv) { return d > 128 || dv > 128; }
+
 attn_status_t check_common(int B, int H, int Tq, int Tk, int d, int dv, float scale, int causal, attn_dtype_t dt) {
   if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || d <= 0 || dv <= 0) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -115,11 +126,8 @@ attn_status_t check_common(int B, int H, int Tq, int Tk, int d, int dv, float sc
   if (dt != ATTN_F32 && dt != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
   if (dt == ATTN_F32) {
     if (d > 256 || dv > 256) return ATTN_ERR_UNSUPPORTED;
-  } else {
-    // d, dv in {64, 128}; or d = 256 (forward only) with dv in {64, 128, 256}
-    const bool small = (d == 64 || d == 128) && (dv == 64 || dv == 128);
-    const bool wide = d == 256 && (dv == 64 || dv == 128 || dv == 256);
-    if (!small && !wide) return ATTN_ERR_UNSUPPORTED;
+  } else if (!bf16_fwd_shape(d, dv)) {
+    return ATTN_ERR_UNSUPPORTED;
   }
   // every index of every tensor must fit the kernels' 64-bit arithmetic and
   // the per-head row counts must fit int (TMA coordinates are int32)
@@ -187,10 +195,11 @@ BwdLayout bwd_layout(int B, int H, int Tq, int Tk, int d, attn_dtype_t dt, int d
 // one so that the forward's units times the splits fill the SMs once, with
 // at least two key tiles per split), clamped to [1, min(key tiles, 64)]; the
 // key tiles per split go to *split_tiles. fp32 problems never split. A unit
-// is a pair of 128-row query tiles for d <= 128 and one query tile for
-// d = 256; key tiles are 128 keys for both.
-int splitkv_count(int B, int H, int Tq, int Tk, int d, attn_dtype_t dt, int req, int num_sms, int* split_tiles) {
-  const int rows_per_unit = d > 128 ? 128 : 256;
+// is a pair of 128-row query tiles for rows of up to 128 columns and one
+// query tile for wider rows; key tiles are 128 keys for both.
+int splitkv_count(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dt, int req, int num_sms,
+                  int* split_tiles) {
+  const int rows_per_unit = bf16_wide(d, dv) ? 128 : 256;
   const int nkb = (Tk + 127) / 128;
   int S = req;
   if (dt != ATTN_BF16 || nkb <= 1 || B == 0 || H == 0 || Tq == 0) {
@@ -252,7 +261,7 @@ attn_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, flo
   if (split_req != 1) {
     // only the automatic choice needs the device (its SM count)
     if (split_req == 0 && dtype == ATTN_BF16 && (s = device_info(&di)) != ATTN_OK) return s;
-    n_splits = splitkv_count(B, H, Tq, Tk, d, dtype, split_req, di ? di->num_sms : 0, &split_tiles);
+    n_splits = splitkv_count(B, H, Tq, Tk, d, dv, dtype, split_req, di ? di->num_sms : 0, &split_tiles);
     SL = split_layout(B, H, Tq, dv, n_splits);
     if (SL.total > 0) {
       if (workspace == nullptr || workspace_bytes < SL.total || reinterpret_cast<uintptr_t>(workspace) % 256)
@@ -292,8 +301,9 @@ attn_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, flo
   if (dtype == ATTN_F32) {
     e = launch_fwd_f32(a);
   } else {
-    // the d = 256 forward loads V by 64-key halves of its 128-key tiles
-    const unsigned v_rows = d == 256 ? 64u : 128u;
+    // the wide-row forward loads V by 64-key halves of its 128-key tiles
+    const bool wide = bf16_wide(d, dv);
+    const unsigned v_rows = wide ? 64u : 128u;
     CUtensorMap mq, mk, mv;
     if ((s = make_map(&mq, Q, d, Tq, static_cast<int>(bh))) != ATTN_OK) return s;
     if ((s = make_map(&mk, K, d, Tk, static_cast<int>(bh))) != ATTN_OK) return s;
@@ -301,7 +311,7 @@ attn_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, flo
     a.tmQ = &mq;
     a.tmK = &mk;
     a.tmV = &mv;
-    e = d == 256 ? launch_fwd_bf16_d256(a) : launch_fwd_bf16(a);
+    e = wide ? launch_fwd_bf16_d256(a) : launch_fwd_bf16(a);
     if (e == cudaSuccess && n_splits > 1)
       e = launch_splitkv_merge(p, a.Opart, a.LSEpart, n_splits, split_tiles, O, LSE, di->num_sms, st);
   }
@@ -348,7 +358,7 @@ int attn_fwd_splitkv_splits(int B, int H, int Tq, int Tk, int d, int dv, attn_dt
     num_sms = di->num_sms;
   }
   int cs;
-  return splitkv_count(B, H, Tq, Tk, d, dtype, num_splits, num_sms, &cs);
+  return splitkv_count(B, H, Tq, Tk, d, dv, dtype, num_splits, num_sms, &cs);
 }
 
 size_t attn_fwd_splitkv_workspace_size(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype,
@@ -375,13 +385,13 @@ attn_status_t attn_fwd_f32_blocked(const float* Q, const float* K, const float* 
 size_t attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype,
                                int deterministic) {
   if (check_common(B, H, Tq, Tk, d, dv, 1.0f, 0, dtype) != ATTN_OK) return 0;
-  if (dtype == ATTN_BF16 && (d > 128 || dv > 128)) return 0;   // no bf16 backward there
+  if (dtype == ATTN_BF16 && !bf16_bwd_shape(d, dv)) return 0;   // no bf16 backward there
   return bwd_layout(B, H, Tq, Tk, d, dtype, deterministic).total;
 }
 
 int attn_bwd_dq_splits(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype, int deterministic) {
   if (check_common(B, H, Tq, Tk, d, dv, 1.0f, 0, dtype) != ATTN_OK) return -1;
-  if (dtype == ATTN_BF16 && (d > 128 || dv > 128)) return -1;
+  if (dtype == ATTN_BF16 && !bf16_bwd_shape(d, dv)) return -1;
   if (deterministic != 0 && deterministic != 1) return -1;
   return bwd_layout(B, H, Tq, Tk, d, dtype, deterministic).dq_splits;
 }
@@ -398,7 +408,7 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
   if (s != ATTN_OK) return s;
   // the tensor-core backward keeps dV and dK accumulators of d and dv columns
   // next to two 128-column score buffers in TMEM: d, dv <= 128
-  if (dtype == ATTN_BF16 && (d > 128 || dv > 128)) return ATTN_ERR_UNSUPPORTED;
+  if (dtype == ATTN_BF16 && !bf16_bwd_shape(d, dv)) return ATTN_ERR_UNSUPPORTED;
   if (phase < 0 || phase > 5) return ATTN_ERR_INVALID_ARG;
   if (deterministic != 0 && deterministic != 1) return ATTN_ERR_INVALID_ARG;
   const size_t es = elem_size(dtype);

@@ -348,6 +348,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::WaitCtx w{abort_flag, P.status, 4u + t};
     const float sc2 = P.sc2;
     const int Tq = P.p.Tq, Tk = P.p.Tk;
+    const int dv = P.p.dv;   // <= HV; a multiple of 8
     uint32_t sp = 0, op = 0;
     bool ok = true;
     int bh, blk;
@@ -451,7 +452,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const size_t rows = static_cast<size_t>(P.p.B) * P.p.H * Tq;
         const size_t row = static_cast<size_t>(blk % P.n_splits) * rows + static_cast<size_t>(bh) * Tq +
                            (row_ok ? q_row : 0);
-        float* prow = P.Opart + row * HV;
+        float* prow = P.Opart + row * dv;
 #pragma unroll 1
         for (int c = 0; c < HV / 32; ++c) {
           uint32_t o[32];
@@ -461,15 +462,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             float4* dst = reinterpret_cast<float4*>(prow + c * 32);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
-              dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                                   __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+              if (c * 32 + 4 * v < dv)   // dv < HV: the padded columns stay unwritten
+                dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                     __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
           }
         }
         if (row_ok) P.LSEpart[row] = lse_row;
         ptx::tc_fence_before();
         continue;
       }
-      __nv_bfloat16* orow = P.O + (static_cast<size_t>(bh) * Tq + (row_ok ? q_row : 0)) * HV;
+      __nv_bfloat16* orow = P.O + (static_cast<size_t>(bh) * Tq + (row_ok ? q_row : 0)) * dv;
 #pragma unroll
       for (int c = 0; c < HV / 32; ++c) {
         uint32_t o[32];
@@ -482,7 +484,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          for (int v = 0; v < 4; ++v)
+            if (c * 32 + 8 * v < dv)   // dv < HV: the padded columns stay unwritten
+              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
       if (row_ok) P.LSE[static_cast<size_t>(bh) * Tq + q_row] = lse_row;
@@ -534,8 +538,9 @@ cudaError_t launch(const LaunchFwd& a) {
 }  // namespace fwd
 
 cudaError_t launch_fwd_bf16(const LaunchFwd& a) {
-  if (a.p.d == 128) return a.p.dv == 128 ? fwd::launch<128, 128>(a) : fwd::launch<128, 64>(a);
-  return a.p.dv == 128 ? fwd::launch<64, 128>(a) : fwd::launch<64, 64>(a);
+  // d or dv below the tile width runs on the next width up (zero columns)
+  if (a.p.d > 64) return a.p.dv > 64 ? fwd::launch<128, 128>(a) : fwd::launch<128, 64>(a);
+  return a.p.dv > 64 ? fwd::launch<64, 128>(a) : fwd::launch<64, 64>(a);
 }
 
 }  // namespace attn

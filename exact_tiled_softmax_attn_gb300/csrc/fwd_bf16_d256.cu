@@ -317,6 +317,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::WaitCtx w{abort_flag, P.status, 4u};
     const float sc2 = P.sc2;
     const int Tq = P.p.Tq, Tk = P.p.Tk;
+    const int dv = P.p.dv;   // <= HV; a multiple of 8
     uint32_t g0 = 0, u_it = 0;
     bool ok = true;
     int bh, blk;
@@ -416,7 +417,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // partial result of this key range: O_s = A / l in fp32 and LSE_s
         const size_t rows = static_cast<size_t>(P.p.B) * P.p.H * Tq;
         const size_t row = static_cast<size_t>(sp) * rows + static_cast<size_t>(bh) * Tq + (row_ok ? q_row : 0);
-        float* prow = P.Opart + row * HV;
+        float* prow = P.Opart + row * dv;
 #pragma unroll 1
         for (int c = 0; c < HV / 32; ++c) {
           uint32_t o[32];
@@ -426,8 +427,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             float4* dst = reinterpret_cast<float4*>(prow + c * 32);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
-              dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                                   __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+              if (c * 32 + 4 * v < dv)   // dv < HV: the padded columns stay unwritten
+                dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                     __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
           }
         }
         if (row_ok) P.LSEpart[row] = lse_row;
@@ -436,7 +438,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ++u_it;
         continue;
       }
-      __nv_bfloat16* orow = P.O + (static_cast<size_t>(bh) * Tq + (row_ok ? q_row : 0)) * HV;
+      __nv_bfloat16* orow = P.O + (static_cast<size_t>(bh) * Tq + (row_ok ? q_row : 0)) * dv;
 #pragma unroll
       for (int c = 0; c < HV / 32; ++c) {
         uint32_t o[32];
@@ -449,7 +451,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(ob[4 * v], ob[4 * v + 1], ob[4 * v + 2], ob[4 * v + 3]);
+          for (int v = 0; v < 4; ++v)
+            if (c * 32 + 8 * v < dv)   // dv < HV: the padded columns stay unwritten
+              dst[v] = make_uint4(ob[4 * v], ob[4 * v + 1], ob[4 * v + 2], ob[4 * v + 3]);
         }
       }
       if (row_ok) P.LSE[static_cast<size_t>(bh) * Tq + q_row] = lse_row;
@@ -499,8 +503,9 @@ cudaError_t launch(const LaunchFwd& a) {
 }  // namespace fwd256
 
 cudaError_t launch_fwd_bf16_d256(const LaunchFwd& a) {
-  if (a.p.dv == 256) return fwd256::launch<256>(a);
-  if (a.p.dv == 128) return fwd256::launch<128>(a);
+  // d below 256 and dv below the V tile width run with zero columns
+  if (a.p.dv > 128) return fwd256::launch<256>(a);
+  if (a.p.dv > 64) return fwd256::launch<128>(a);
   return fwd256::launch<64>(a);
 }
 

@@ -37,12 +37,14 @@
  *   ATTN_F32 : 1 <= d, dv <= 256, any B, H, Tq, Tk >= 0 (attn_fwd_f32_blocked
  *              with block_n = 128 returns ATTN_ERR_UNSUPPORTED when its key
  *              tile does not fit in shared memory, above d = dv = 150 or so)
- *   ATTN_BF16: d in {64, 128} and dv in {64, 128} (d != dv allowed: the
- *              page's task takes V with its own head dimension), any B, H,
- *              Tq, Tk >= 0; and for the forward alone (attn_fwd,
- *              attn_fwd_splitkv) also d = 256 with dv in {64, 128, 256}.
- *              attn_bwd with bf16 and d or dv above 128 returns
- *              ATTN_ERR_UNSUPPORTED (use ATTN_F32 there).
+ *   ATTN_BF16: forward (attn_fwd, attn_fwd_splitkv): d and dv multiples
+ *              of 8 from 8 to 256, independently (the page's task takes V
+ *              with its own head dimension); a width below 64, 128 or 256
+ *              runs on the next of those tile widths with zero columns, so
+ *              64, 128 and 256 are the efficient sizes. Backward (attn_bwd):
+ *              d and dv in {64, 128}; other bf16 widths return
+ *              ATTN_ERR_UNSUPPORTED (ATTN_F32 covers them). Any B, H, Tq,
+ *              Tk >= 0.
  * Zero-sized problems are valid: Tk == 0 gives O = 0 and LSE = -inf (a row
  * with no allowed key), and empty gradients are written as zeros.
  */

@@ -65,9 +65,9 @@ def _fwd(**kw):
     (dict(scale=-1.0), B.ATTN_ERR_INVALID_ARG),
     (dict(causal=2), B.ATTN_ERR_INVALID_ARG),
     (dict(dtype=7), B.ATTN_ERR_INVALID_ARG),
-    (dict(d=96, dv=96), B.ATTN_ERR_UNSUPPORTED),
-    (dict(d=64, dv=96), B.ATTN_ERR_UNSUPPORTED),
-    (dict(d=128, dv=256), B.ATTN_ERR_UNSUPPORTED),   # dv = 256 only with d = 256
+    (dict(d=100, dv=100), B.ATTN_ERR_UNSUPPORTED),   # bf16 rows are whole 16-byte units: d % 8 == 0
+    (dict(d=64, dv=60), B.ATTN_ERR_UNSUPPORTED),
+    (dict(d=128, dv=264), B.ATTN_ERR_UNSUPPORTED),   # at most 256 columns
     (dict(d=512, dv=128), B.ATTN_ERR_UNSUPPORTED),
     (dict(dtype=B.ATTN_F32, d=257), B.ATTN_ERR_UNSUPPORTED),
     (dict(Q=None), B.ATTN_ERR_INVALID_ARG),
@@ -149,7 +149,8 @@ def _bwd(**kw):
     (dict(dQ=0x600000), B.ATTN_ERR_INVALID_ARG),          # output overlaps dO
     (dict(dO=None), B.ATTN_ERR_INVALID_ARG),
     (dict(dV=0x900008), B.ATTN_ERR_MISALIGNED),
-    (dict(d=80, dv=80), B.ATTN_ERR_UNSUPPORTED),
+    (dict(d=80, dv=80), B.ATTN_ERR_UNSUPPORTED),     # the bf16 backward takes d, dv in {64, 128}
+    (dict(d=64, dv=96), B.ATTN_ERR_UNSUPPORTED),
     (dict(d=256, dv=256), B.ATTN_ERR_UNSUPPORTED),   # the d = 256 tensor-core path is forward only
 ])
 def test_backward_host_validation(lib, kw, status):
@@ -183,7 +184,7 @@ def test_step_host_validation(lib, kw, status):
 
 def test_error_text_carries_status(lib):
     with pytest.raises(B.AttnError) as e:
-        B.attn_fwd(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 1, 1, 8, 8, 96, 96, 0.1, 0, B.ATTN_BF16,
+        B.attn_fwd(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 1, 1, 8, 8, 100, 100, 0.1, 0, B.ATTN_BF16,
                    stream=0)
     assert "unsupported" in str(e.value)
 

@@ -117,6 +117,46 @@ D256_SHAPES = [  # B, H, Tq, Tk, dv: d = 256 (one query tile per unit, 128-key t
 ]
 
 
+PAD_SHAPES = [  # B, H, Tq, Tk, d, dv: widths below the tile width they run on (zero columns)
+    (1, 2, 200, 300, 96, 96),      # the d <= 128 kernel at 128 / 128
+    (2, 1, 130, 257, 40, 72),      # 64 / 128
+    (1, 1, 300, 500, 120, 8),      # dv = 8: one 16-byte store per row
+    (1, 2, 129, 200, 200, 136),    # the wide-row kernel, V tile 256
+    (1, 1, 257, 300, 64, 256),     # d = 64 on the wide-row kernel (dv = 256)
+    (1, 1, 100, 140, 248, 24),     # V tile 64 on the wide-row kernel
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("split", [None, 3])
+@pytest.mark.parametrize("shape", PAD_SHAPES)
+def test_bf16_padded_widths(shape, split, causal):
+    """d, dv multiples of 8 below 64 / 128 / 256 run on the next tile width:
+    the same result as the oracle, and nothing is written past O's last row
+    (O lies at the start of a larger buffer filled with a sentinel)."""
+    B, H, Tq, Tk, d, dv = shape
+    x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, dv), seed=Tq + Tk + d + dv, dtype=torch.bfloat16,
+                    device=DEV)
+    scale = 1 / math.sqrt(d)
+    n = B * H * Tq * dv
+    buf = torch.full((n + 4096,), 7.0, dtype=torch.bfloat16, device=DEV)
+    o = buf[:n].view(B, H, Tq, dv)
+    lse = torch.empty(B, H, Tq, dtype=torch.float32, device=DEV)
+    if split is None:
+        pkg.attn_fwd(x["Q"], x["K"], x["V"], o, lse, B, H, Tq, Tk, d, dv, scale, causal, pkg.ATTN_BF16)
+    else:
+        nbytes = pkg.attn_fwd_splitkv_workspace_size(B, H, Tq, Tk, d, dv, pkg.ATTN_BF16, split)
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=DEV)
+        pkg.attn_fwd_splitkv(x["Q"], x["K"], x["V"], o, lse, B, H, Tq, Tk, d, dv, scale, causal, pkg.ATTN_BF16,
+                             split, ws, ws.numel())
+    torch.cuda.synchronize()
+    assert pkg.attn_device_status() == pkg.ATTN_OK
+    assert torch.all(buf[n:] == 7.0)
+    O, L = oracle_fwd(x, causal, scale)
+    check_o(o, O, torch.bfloat16)
+    check_lse(lse, L, torch.bfloat16)
+
+
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("shape", D256_SHAPES)
 def test_bf16_d256_forward(shape, causal):

@@ -40,7 +40,10 @@ def test_split_count_invalid_and_fp32():
     assert B.attn_fwd_splitkv_splits(1, 1, 128, 1024, 128, 128, B.ATTN_BF16, -1) == -1
     assert B.attn_fwd_splitkv_splits(1, 1, 128, 1024, 128, 128, B.ATTN_F32, 2) == -1
     assert B.attn_fwd_splitkv_splits(1, 1, 128, 1024, 128, 128, B.ATTN_F32, 0) == 1
-    assert B.attn_fwd_splitkv_splits(1, 1, 128, 1024, 96, 96, B.ATTN_BF16, 2) == -1
+    assert B.attn_fwd_splitkv_splits(1, 1, 128, 1024, 100, 100, B.ATTN_BF16, 2) == -1
+    # padded widths split like the tile width they run on
+    assert B.attn_fwd_splitkv_splits(1, 1, 128, 1024, 96, 40, B.ATTN_BF16, 2) == 2
+    assert B.attn_fwd_splitkv_splits(1, 1, 128, 1024, 72, 200, B.ATTN_BF16, 3) == 3
 
 
 def test_workspace_size_formula():
