@@ -200,3 +200,39 @@ def test_d256_bf16_is_forward_only(lib):
     assert B.attn_fwd_splitkv_workspace_size(1, 1, 128, 8192, 256, 256, B.ATTN_BF16, 8) == \
         r256(8 * rows * 256 * 4) + r256(8 * rows * 4)
 
+
+
+def test_plain_c_program_uses_the_header_and_library(lib, tmp_path):
+    """The boundary needs no Python or torch: a C99 program that includes
+    attn.h (with -Wall -Werror -pedantic) links libattn.so and calls the
+    host-only entry points."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_attn.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include "attn.h"
+int main(void) {
+  size_t ws = attn_bwd_workspace_size(1, 2, 300, 300, 64, 64, ATTN_BF16, 0);
+  int s1 = attn_fwd_splitkv_splits(1, 1, 128, 8192, 128, 128, ATTN_BF16, 8);
+  attn_status_t st = attn_fwd(0, 0, 0, 0, 0, 1, 1, 8, 8, 100, 100, 0.1f, 0, ATTN_BF16, 0);
+  printf("%d %zu %d %d %s\n", attn_version(), ws, s1, (int)st, attn_strerror(st));
+  return 0;
+}
+''')
+    exe = tmp_path / "use_attn"
+    libdir = os.path.dirname(B.LIB_PATH)
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-o", str(exe), "-L", libdir, "-lattn", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120,
+                       env={**os.environ, "CUDA_VISIBLE_DEVICES": ""})
+    assert r.returncode == 0, r.stderr
+    version, ws, s1, st, text = r.stdout.split(maxsplit=4)
+    assert int(version) == B.attn_version()
+    assert int(ws) == B.attn_bwd_workspace_size(1, 2, 300, 300, 64, 64, B.ATTN_BF16, 0)
+    assert int(s1) == 8 and int(st) == B.ATTN_ERR_UNSUPPORTED and "unsupported" in text
