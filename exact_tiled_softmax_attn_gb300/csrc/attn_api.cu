@@ -191,6 +191,45 @@ BwdLayout bwd_layout(int B, int H, int Tq, int Tk, int d, attn_dtype_t dt, int d
   return L;
 }
 
+// bf16 backward at widths other than 64 and 128 (multiples of 8 up to 128):
+// Q, K, V, O and dO are copied into rows of the next tile width dp, dvp with
+// zero columns, the backward runs on those copies, and the first d / dv
+// columns of its gradients are copied out. The zero columns add nothing to
+// S = QK^T, dP = dO V^T or D = rowsum(dO o O), so P and dS are those of the
+// unpadded problem and the gradients' first columns are its gradients.
+bool bf16_bwd_padded(int d, int dv) { return !bf16_bwd_shape(d, dv) && d <= 128 && dv <= 128; }
+
+struct PadLayout {
+  int dp, dvp;
+  size_t q, k, v, o, dO, dq, dk, dv, inner, total;   // byte offsets in the workspace; inner: the backward's own
+};
+// Workspace of the padded backward: Qp | Kp | Vp | Op | dOp | dQp | dKp | dVp
+// (bf16, rows of dp or dvp columns), each 256-byte aligned, then the
+// workspace of the backward at (dp, dvp).
+PadLayout pad_layout(int B, int H, int Tq, int Tk, int d, int dv, int deterministic) {
+  PadLayout L{};
+  L.dp = d <= 64 ? 64 : 128;
+  L.dvp = dv <= 64 ? 64 : 128;
+  const size_t bh = static_cast<size_t>(B) * H;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = round_up(off + bytes, 256);
+    return at;
+  };
+  L.q = take(bh * Tq * L.dp * 2);
+  L.k = take(bh * Tk * L.dp * 2);
+  L.v = take(bh * Tk * L.dvp * 2);
+  L.o = take(bh * Tq * L.dvp * 2);
+  L.dO = take(bh * Tq * L.dvp * 2);
+  L.dq = take(bh * Tq * L.dp * 2);
+  L.dk = take(bh * Tk * L.dp * 2);
+  L.dv = take(bh * Tk * L.dvp * 2);
+  L.inner = off;
+  L.total = off + bwd_layout(B, H, Tq, Tk, L.dp, ATTN_BF16, deterministic).total;
+  return L;
+}
+
 // Split-KV forward: effective number of key splits for a request (0 = pick
 // one so that the forward's units times the splits fill the SMs once, with
 // at least two key tiles per split), clamped to [1, min(key tiles, 64)]; the
@@ -385,15 +424,19 @@ attn_status_t attn_fwd_f32_blocked(const float* Q, const float* K, const float* 
 size_t attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype,
                                int deterministic) {
   if (check_common(B, H, Tq, Tk, d, dv, 1.0f, 0, dtype) != ATTN_OK) return 0;
-  if (dtype == ATTN_BF16 && !bf16_bwd_shape(d, dv)) return 0;   // no bf16 backward there
+  if (dtype == ATTN_BF16 && !bf16_bwd_shape(d, dv)) {
+    if (!bf16_bwd_padded(d, dv) || (deterministic != 0 && deterministic != 1)) return 0;   // no bf16 backward there
+    return pad_layout(B, H, Tq, Tk, d, dv, deterministic).total;
+  }
   return bwd_layout(B, H, Tq, Tk, d, dtype, deterministic).total;
 }
 
 int attn_bwd_dq_splits(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype, int deterministic) {
   if (check_common(B, H, Tq, Tk, d, dv, 1.0f, 0, dtype) != ATTN_OK) return -1;
-  if (dtype == ATTN_BF16 && !bf16_bwd_shape(d, dv)) return -1;
+  if (dtype == ATTN_BF16 && !bf16_bwd_shape(d, dv) && !bf16_bwd_padded(d, dv)) return -1;
   if (deterministic != 0 && deterministic != 1) return -1;
-  return bwd_layout(B, H, Tq, Tk, d, dtype, deterministic).dq_splits;
+  const int dk = dtype == ATTN_BF16 && bf16_bwd_padded(d, dv) ? pad_layout(B, H, Tq, Tk, d, dv, deterministic).dp : d;
+  return bwd_layout(B, H, Tq, Tk, dk, dtype, deterministic).dq_splits;
 }
 
 }  // extern "C"
@@ -407,9 +450,12 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
   attn_status_t s = check_common(B, H, Tq, Tk, d, dv, scale, causal, dtype);
   if (s != ATTN_OK) return s;
   // the tensor-core backward keeps dV and dK accumulators of d and dv columns
-  // next to two 128-column score buffers in TMEM: d, dv <= 128
-  if (dtype == ATTN_BF16 && !bf16_bwd_shape(d, dv)) return ATTN_ERR_UNSUPPORTED;
+  // next to two 128-column score buffers in TMEM: d, dv <= 128; widths other
+  // than 64 and 128 run on zero-padded copies (one call: no phases)
+  const bool padded = dtype == ATTN_BF16 && !bf16_bwd_shape(d, dv);
+  if (padded && !bf16_bwd_padded(d, dv)) return ATTN_ERR_UNSUPPORTED;
   if (phase < 0 || phase > 5) return ATTN_ERR_INVALID_ARG;
+  if (padded && phase != 0) return ATTN_ERR_UNSUPPORTED;
   if (deterministic != 0 && deterministic != 1) return ATTN_ERR_INVALID_ARG;
   const size_t es = elem_size(dtype);
   const size_t bh = static_cast<size_t>(B) * H;
@@ -425,12 +471,14 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
   for (int i = 0; i < 3; ++i)
     if ((s = check_ptr(outs[i], out_bytes[i], align)) != ATTN_OK) return s;
   const BwdLayout L = bwd_layout(B, H, Tq, Tk, d, dtype, deterministic);
-  if (L.total > 0) {
-    if (workspace == nullptr || workspace_bytes < L.total || reinterpret_cast<uintptr_t>(workspace) % 256)
+  const PadLayout PL = padded ? pad_layout(B, H, Tq, Tk, d, dv, deterministic) : PadLayout{};
+  const size_t ws_total = padded ? PL.total : L.total;
+  if (ws_total > 0) {
+    if (workspace == nullptr || workspace_bytes < ws_total || reinterpret_cast<uintptr_t>(workspace) % 256)
       return ATTN_ERR_WORKSPACE;
   }
   // outputs must not overlap inputs, each other, or the workspace
-  Range ro[4] = {range(dQ, bq), range(dK, bk), range(dV, bv), range(workspace, L.total)};
+  Range ro[4] = {range(dQ, bq), range(dK, bk), range(dV, bv), range(workspace, ws_total)};
   for (int i = 0; i < 4; ++i) {
     for (int j = 0; j < 6; ++j)
       if (overlap(ro[i], range(ins[j], in_bytes[j]))) return i == 3 ? ATTN_ERR_WORKSPACE : ATTN_ERR_INVALID_ARG;
@@ -449,6 +497,25 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
     if ((e = launch_zero(dQ, bq, st)) == cudaSuccess && (e = launch_zero(dK, bk, st)) == cudaSuccess)
       e = launch_zero(dV, bv, st);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+  }
+  if (padded) {
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    const long long rq = static_cast<long long>(bh) * Tq, rk = static_cast<long long>(bh) * Tk;
+    const int ns = di->num_sms;
+    if ((e = launch_pad_rows(Q, w + PL.q, rq, d, PL.dp, ns, st)) != cudaSuccess ||
+        (e = launch_pad_rows(K, w + PL.k, rk, d, PL.dp, ns, st)) != cudaSuccess ||
+        (e = launch_pad_rows(V, w + PL.v, rk, dv, PL.dvp, ns, st)) != cudaSuccess ||
+        (e = launch_pad_rows(O, w + PL.o, rq, dv, PL.dvp, ns, st)) != cudaSuccess ||
+        (e = launch_pad_rows(dO, w + PL.dO, rq, dv, PL.dvp, ns, st)) != cudaSuccess)
+      return cuda_fail(e);
+    s = bwd_impl(w + PL.q, w + PL.k, w + PL.v, w + PL.o, LSE, w + PL.dO, w + PL.dq, w + PL.dk, w + PL.dv, B, H, Tq,
+                 Tk, PL.dp, PL.dvp, scale, causal, dtype, deterministic, w + PL.inner, PL.total - PL.inner, 0, stream);
+    if (s != ATTN_OK) return s;
+    if ((e = launch_crop_rows(w + PL.dq, dQ, rq, PL.dp, d, ns, st)) != cudaSuccess ||
+        (e = launch_crop_rows(w + PL.dk, dK, rk, PL.dp, d, ns, st)) != cudaSuccess ||
+        (e = launch_crop_rows(w + PL.dv, dV, rk, PL.dvp, dv, ns, st)) != cudaSuccess)
+      return cuda_fail(e);
+    return ATTN_OK;
   }
   LaunchBwd a{};
   a.p = Problem{B, H, Tq, Tk, d, dv, scale, causal};

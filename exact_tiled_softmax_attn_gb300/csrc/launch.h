@@ -86,6 +86,11 @@ cudaError_t launch_splitkv_merge(const Problem& p, const float* Opart, const flo
 // shared small kernels
 cudaError_t launch_fill_empty_fwd(const Problem& p, void* O, float* LSE, int elem_bytes, cudaStream_t s);
 cudaError_t launch_zero(void* ptr, size_t bytes, cudaStream_t s);
+// bf16 rows of width w copied into rows of width wp >= w with zero columns
+// (pad), or the first w columns of rows of width wp copied out (crop); w and
+// wp multiples of 8, both buffers 16-byte aligned.
+cudaError_t launch_pad_rows(const void* src, void* dst, long long rows, int w, int wp, int num_sms, cudaStream_t s);
+cudaError_t launch_crop_rows(const void* src, void* dst, long long rows, int wp, int w, int num_sms, cudaStream_t s);
 // One online-softmax step over n rows (fp32 state, fp64 arithmetic), dv <= 512.
 cudaError_t launch_online_softmax_step(float* m, float* l, float* acc, const float* scores, const float* v, int n,
                                        int bs, int dv, cudaStream_t s);

@@ -119,6 +119,32 @@ __global__ void zero_kernel(uint8_t* p, size_t bytes) {
   for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < bytes; i += stride) p[i] = 0;
 }
 
+// Row width change of a [rows][w] bf16 array into [rows][wp] (pad: wp >= w,
+// the new columns zero) or [rows][wp] into [rows][w] (crop: the first w
+// columns), in 16-byte units: w8 = w / 8 and wp8 = wp / 8 units per row.
+// One thread per 16-byte unit of the destination.
+__global__ void pad_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long rows, int w8,
+                                int wp8) {
+  const long long n = rows * wp8;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const long long r = i / wp8;
+    const int c = static_cast<int>(i - r * wp8);
+    dst[i] = c < w8 ? src[r * w8 + c] : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+__global__ void crop_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long rows, int wp8,
+                                 int w8) {
+  const long long n = rows * w8;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const long long r = i / w8;
+    const int c = static_cast<int>(i - r * w8);
+    dst[i] = src[r * wp8 + c];
+  }
+}
+
 }  // namespace small
 
 cudaError_t launch_bwd_preprocess(const Problem& p, const void* O, const void* dO, const float* LSE, int elem_bytes,
@@ -153,6 +179,24 @@ cudaError_t launch_fill_empty_fwd(const Problem& p, void* O, float* LSE, int ele
   const size_t o_bytes = n_lse * p.dv * elem_bytes;
   if (n_lse == 0) return cudaSuccess;
   small::fill_empty_kernel<<<1024, 256, 0, s>>>(static_cast<uint8_t*>(O), o_bytes, LSE, n_lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pad_rows(const void* src, void* dst, long long rows, int w, int wp, int num_sms,
+                            cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  if (w % 8 || wp % 8 || w <= 0 || wp < w) return cudaErrorInvalidValue;
+  small::pad_rows_kernel<<<num_sms * 8, 256, 0, s>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), rows,
+                                                       w / 8, wp / 8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_crop_rows(const void* src, void* dst, long long rows, int wp, int w, int num_sms,
+                             cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  if (w % 8 || wp % 8 || w <= 0 || wp < w) return cudaErrorInvalidValue;
+  small::crop_rows_kernel<<<num_sms * 8, 256, 0, s>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
+                                                        rows, wp / 8, w / 8);
   return cudaGetLastError();
 }
 

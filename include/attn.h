@@ -42,9 +42,11 @@
  *              with its own head dimension); a width below 64, 128 or 256
  *              runs on the next of those tile widths with zero columns, so
  *              64, 128 and 256 are the efficient sizes. Backward (attn_bwd):
- *              d and dv in {64, 128}; other bf16 widths return
- *              ATTN_ERR_UNSUPPORTED (ATTN_F32 covers them). Any B, H, Tq,
- *              Tk >= 0.
+ *              d and dv multiples of 8 up to 128; widths other than 64 and
+ *              128 run on zero-padded copies of the inputs held in the
+ *              workspace (attn_bwd_phase takes only 64 and 128); wider bf16
+ *              rows return ATTN_ERR_UNSUPPORTED (ATTN_F32 covers them). Any
+ *              B, H, Tq, Tk >= 0.
  * Zero-sized problems are valid: Tk == 0 gives O = 0 and LSE = -inf (a row
  * with no allowed key), and empty gradients are written as zeros.
  */

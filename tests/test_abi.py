@@ -149,8 +149,8 @@ def _bwd(**kw):
     (dict(dQ=0x600000), B.ATTN_ERR_INVALID_ARG),          # output overlaps dO
     (dict(dO=None), B.ATTN_ERR_INVALID_ARG),
     (dict(dV=0x900008), B.ATTN_ERR_MISALIGNED),
-    (dict(d=80, dv=80), B.ATTN_ERR_UNSUPPORTED),     # the bf16 backward takes d, dv in {64, 128}
-    (dict(d=64, dv=96), B.ATTN_ERR_UNSUPPORTED),
+    (dict(d=136, dv=64), B.ATTN_ERR_UNSUPPORTED),    # the bf16 backward takes d, dv <= 128
+    (dict(d=100, dv=64), B.ATTN_ERR_UNSUPPORTED),    # a multiple of 8
     (dict(d=256, dv=256), B.ATTN_ERR_UNSUPPORTED),   # the d = 256 tensor-core path is forward only
 ])
 def test_backward_host_validation(lib, kw, status):
@@ -236,3 +236,24 @@ int main(void) {
     assert int(version) == B.attn_version()
     assert int(ws) == B.attn_bwd_workspace_size(1, 2, 300, 300, 64, 64, B.ATTN_BF16, 0)
     assert int(s1) == 8 and int(st) == B.ATTN_ERR_UNSUPPORTED and "unsupported" in text
+
+
+def test_padded_bf16_backward_workspace_and_phases(lib):
+    """bf16 widths other than 64 / 128 (multiples of 8 up to 128) run the
+    backward on zero-padded copies held in the workspace, as one call."""
+    r256 = lambda x: (x + 255) // 256 * 256
+    for det in (0, 1):
+        B_, H, Tq, Tk, d, dv = 1, 2, 300, 500, 96, 40
+        dp, dvp = 128, 64
+        bh = B_ * H
+        pads = [bh * Tq * dp, bh * Tk * dp, bh * Tk * dvp, bh * Tq * dvp, bh * Tq * dvp, bh * Tq * dp, bh * Tk * dp,
+                bh * Tk * dvp]
+        inner = B.attn_bwd_workspace_size(B_, H, Tq, Tk, dp, dvp, B.ATTN_BF16, det)
+        assert B.attn_bwd_workspace_size(B_, H, Tq, Tk, d, dv, B.ATTN_BF16, det) == sum(r256(2 * n) for n in pads) + inner
+        assert B.attn_bwd_dq_splits(B_, H, Tq, Tk, d, dv, B.ATTN_BF16, det) == \
+            B.attn_bwd_dq_splits(B_, H, Tq, Tk, dp, dvp, B.ATTN_BF16, det)
+    args = dict(Q=0x100000, K=0x200000, V=0x300000, O=0x400000, LSE=0x500000, dO=0x600000, dQ=0x700000,
+                dK=0x800000, dV=0x900000, B=1, H=1, Tq=8, Tk=8, d=96, dv=96, scale=0.125, causal=0,
+                dtype=B.ATTN_BF16, deterministic=1, workspace=0xA00000, workspace_bytes=1 << 20)
+    for ph in (1, 2, 3, 4, 5):
+        assert B.attn_bwd_phase(**args, phase=ph, stream=0, check=False) == B.ATTN_ERR_UNSUPPORTED

@@ -134,6 +134,48 @@ def test_bf16_d_neq_dv(shape, causal, deterministic):
     check_all(x, causal, 1 / math.sqrt(d), torch.bfloat16, deterministic)
 
 
+PAD_BWD_SHAPES = [  # B, H, Tq, Tk, d, dv: bf16 widths other than 64 / 128 (zero-padded copies)
+    (1, 2, 200, 300, 96, 96),
+    (2, 1, 130, 257, 40, 72),
+    (1, 1, 300, 500, 120, 8),
+]
+
+
+@pytest.mark.parametrize("deterministic", [0, 1])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", PAD_BWD_SHAPES)
+def test_bf16_padded_widths_backward(shape, causal, deterministic):
+    B, H, Tq, Tk, d, dv = shape
+    x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, dv), seed=Tq + Tk + d + 5 * dv, dtype=torch.bfloat16,
+                    device=DEV)
+    check_all(x, causal, 1 / math.sqrt(d), torch.bfloat16, deterministic)
+
+
+def test_bf16_padded_backward_writes_only_its_gradients():
+    """The cropped gradients land in place: a sentinel after each of dQ, dK,
+    dV is untouched."""
+    B, H, Tq, Tk, d, dv = 1, 2, 150, 200, 40, 24
+    x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, dv), seed=11, dtype=torch.bfloat16, device=DEV)
+    scale = 1 / math.sqrt(d)
+    o, lse = pkg.forward(x["Q"], x["K"], x["V"], causal=True, scale=scale)
+    outs = []
+    for shape in ((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, dv)):
+        n = math.prod(shape)
+        buf = torch.full((n + 2048,), 5.0, dtype=torch.bfloat16, device=DEV)
+        outs.append((buf, n, buf[:n].view(shape)))
+    ws_bytes = pkg.attn_bwd_workspace_size(B, H, Tq, Tk, d, dv, pkg.ATTN_BF16, 1)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=DEV)
+    pkg.attn_bwd(x["Q"], x["K"], x["V"], o, lse, x["dO"], outs[0][2], outs[1][2], outs[2][2], B, H, Tq, Tk, d, dv,
+                 scale, 1, pkg.ATTN_BF16, 1, ws, ws.numel())
+    torch.cuda.synchronize()
+    assert pkg.attn_device_status() == pkg.ATTN_OK
+    for buf, n, _ in outs:
+        assert torch.all(buf[n:] == 5.0)
+    r = ref.backward(x["Q"], x["K"], x["V"], x["dO"], scale, True)
+    for (_, _, g), name in zip(outs, ("dQ", "dK", "dV")):
+        check_grad(g, r[name], torch.bfloat16, name)
+
+
 SPLIT_DQ_SHAPES = [  # B, H, Tq, Tk, d, dv: few query tiles, many key tiles
     (1, 1, 1, 5000, 128, 128),     # one query row: 9 key ranges
     (1, 2, 128, 4096, 128, 128),
