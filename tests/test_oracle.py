@@ -428,3 +428,26 @@ def test_planted_step_mistakes_are_caught(golden, old, new):
         m, l, acc = bad(*args)
     ok = (np.allclose(l, g["l_new"], atol=PRINT_TOL) and np.allclose(acc, g["acc_new"], atol=PRINT_TOL))
     assert not ok
+
+
+def test_zero_columns_change_nothing():
+    """Zero columns appended to Q and K (d -> dp) and to V and dO (dv -> dvp)
+    leave S = scale QK^T, P, LSE and D = rowsum(dO o O) as they were: O and
+    the gradients gain zero columns and keep their first d / dv columns. The
+    bf16 paths for widths below a tile width rely on exactly this."""
+    rng = np.random.default_rng(3)
+    Tq, Tk, d, dv, dp, dvp = 37, 53, 40, 24, 64, 128
+    q, k = rng.standard_normal((Tq, d)), rng.standard_normal((Tk, d))
+    v, do = rng.standard_normal((Tk, dv)), rng.standard_normal((Tq, dv))
+
+    def pad(a, w):
+        return np.concatenate([a, np.zeros((a.shape[0], w - a.shape[1]))], axis=1)
+
+    for causal in (False, True):
+        r = A.backward_head(q, k, v, do, 0.3, causal)
+        rp = A.backward_head(pad(q, dp), pad(k, dp), pad(v, dvp), pad(do, dvp), 0.3, causal)
+        np.testing.assert_allclose(rp["lse"], r["lse"], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(rp["D"], r["D"], rtol=0, atol=1e-12)
+        for key, w in (("o", dv), ("dq", d), ("dk", d), ("dv", dv)):
+            np.testing.assert_allclose(rp[key][:, :w], r[key], rtol=0, atol=1e-12)
+            assert np.all(rp[key][:, w:] == 0.0)
