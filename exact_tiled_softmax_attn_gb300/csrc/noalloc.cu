@@ -62,8 +62,9 @@ extern "C" attn_status_t attn_bwd_noalloc(const void* Q, const void* K, const vo
   void* scratch = nullptr;
   const cudaError_t e = attn::scratch_address(&scratch);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
-  // attn_bwd writes D in full and zeroes the fp32 dQ accumulator before it
-  // accumulates, so whatever an earlier call left in the scratch is not read.
+  // attn_bwd writes D (and, for padded bf16 widths, the padded copies of its
+  // inputs) in full and zeroes the fp32 dQ accumulator before it accumulates,
+  // so whatever an earlier call left in the scratch is not read.
   return attn_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, B, H, Tq, Tk, d, dv, scale, causal, dtype, deterministic,
                   scratch, attn::kNoAllocScratchBytes, stream);
 }
