@@ -151,6 +151,16 @@ def test_bf16_padded_widths_backward(shape, causal, deterministic):
     check_all(x, causal, 1 / math.sqrt(d), torch.bfloat16, deterministic)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_padded_widths_split_dq(causal):
+    """Few query tiles against many keys at a padded width: the deterministic
+    dQ pass of the padded problem splits its key ranges."""
+    B, H, Tq, Tk, d, dv = 1, 1, 128, 4096, 96, 96
+    assert pkg.attn_bwd_dq_splits(B, H, Tq, Tk, d, dv, pkg.ATTN_BF16, 1) > 1
+    x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, dv), seed=23, dtype=torch.bfloat16, device=DEV)
+    check_all(x, causal, 1 / math.sqrt(d), torch.bfloat16, 1)
+
+
 def test_bf16_padded_backward_writes_only_its_gradients():
     """The cropped gradients land in place: a sentinel after each of dQ, dK,
     dV is untouched."""

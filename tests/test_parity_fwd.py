@@ -124,6 +124,7 @@ PAD_SHAPES = [  # B, H, Tq, Tk, d, dv: widths below the tile width they run on (
     (1, 2, 129, 200, 200, 136),    # the wide-row kernel, V tile 256
     (1, 1, 257, 300, 64, 256),     # d = 64 on the wide-row kernel (dv = 256)
     (1, 1, 100, 140, 248, 24),     # V tile 64 on the wide-row kernel
+    (3, 40, 200, 200, 96, 40),     # several units per CTA
 ]
 
 
