@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tma_prefetch_desc(&tmQ);
     ptx::tma_prefetch_desc(&tmK);
     ptx::tma_prefetch_desc(&tmV);
-    uint32_t item = 0, u_it = 0;
+    uint32_t item = 0, u_it = 0, q_issued = 0;   // q_issued: Q loads issued (one per unit)
     bool ok = true;
     int bh, blk;
     for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &blk); ++round) {
@@ -207,6 +207,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int t = 0; t < 2; ++t)
         for (int b = 0; b < C::KB; ++b)
           ptx::tma_load_3d(sQ + t * C::TILE + b * BOX_BYTES, &tmQ, q_full, b * 64, (2 * qb + t) * BM, bh);
+      q_issued = u_it + 1;
       for (int j = 0; ok && j < n1; ++j) {
         for (int kv = 0; kv < 2; ++kv, ++item) {
           const int sl = item % C::NSLOT;
@@ -224,7 +225,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // Let the copies already in flight land before the CTA exits.
       for (uint32_t n = (item > (uint32_t)C::NSLOT ? item - C::NSLOT : 0u); n < item; ++n)
         ptx::mbar_wait_drain(kv_full + n % C::NSLOT, (n / C::NSLOT) & 1u);
-      if (u_it > 0) ptx::mbar_wait_drain(q_full, (u_it - 1) & 1u);
+      // the last Q load issued (possibly this unit's, still in flight)
+      if (q_issued > 0) ptx::mbar_wait_drain(q_full, (q_issued - 1) & 1u);
     }
    } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer

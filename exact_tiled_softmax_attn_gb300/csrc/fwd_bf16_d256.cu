@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tma_prefetch_desc(&tmQ);
     ptx::tma_prefetch_desc(&tmK);
     ptx::tma_prefetch_desc(&tmV);
-    uint32_t item = 0, u_it = 0;
+    uint32_t item = 0, u_it = 0, q_issued = 0;   // q_issued: Q loads issued (one per unit)
     bool ok = true;
     int bh, blk;
     for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &blk); ++round) {
@@ -182,6 +182,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!(ok = ptx::mbar_wait(q_empty, (u_it & 1u) ^ 1u, w))) break;
       ptx::mbar_arrive_expect_tx(q_full, C::TILE_Q);
       for (int b = 0; b < HD / 64; ++b) ptx::tma_load_3d(sQ + b * QBOX, &tmQ, q_full, b * 64, qt * BM, bh);
+      q_issued = u_it + 1;
       auto load = [&](int kv, int j) {   // both halves of K (kv = 0) or V (kv = 1) of key tile j
         for (int h = 0; ok && h < 2; ++h) {
           const int sl = slot(item);
@@ -210,7 +211,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // Let the copies already in flight land before the CTA exits.
       for (uint32_t n = (item > (uint32_t)C::NSLOT ? item - C::NSLOT : 0u); n < item; ++n)
         ptx::mbar_wait_drain(kv_full + slot(n), par(n));
-      if (u_it > 0) ptx::mbar_wait_drain(q_full, (u_it - 1) & 1u);
+      // the last Q load issued (possibly this unit's, still in flight)
+      if (q_issued > 0) ptx::mbar_wait_drain(q_full, (q_issued - 1) & 1u);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
