@@ -151,8 +151,12 @@ ATTN_API size_t attn_fwd_splitkv_workspace_size(int B, int H, int Tq, int Tk, in
  * Tq_pad = Tq rounded up to a multiple of 128, and, for bf16 with
  * deterministic == 0, the fp32 dQ accumulator [B,H,Tq,d], or, for bf16 with
  * deterministic == 1 and S = attn_bwd_dq_splits(...) > 1, S fp32 partial dQ
- * arrays [S][B,H,Tq,d]; each part starts on a 256-byte boundary. Returns 0
- * for invalid arguments as well.
+ * arrays [S][B,H,Tq,d]; each part starts on a 256-byte boundary. For bf16
+ * widths other than 64 and 128 it first holds zero-padded bf16 copies of Q,
+ * K, V, O, dO and of the three gradients, in rows of the next tile width (64
+ * or 128 columns), then the workspace above for the padded widths; the
+ * padded problem's dQ splits are the ones attn_bwd_dq_splits reports.
+ * Returns 0 for invalid arguments as well.
  */
 ATTN_API size_t attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype,
                                int deterministic);
