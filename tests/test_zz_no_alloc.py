@@ -24,6 +24,7 @@ CASES = [  # B, H, Tq, Tk, d, dtype, causal, deterministic
     (1, 3, 513, 513, 128, torch.bfloat16, True, 1),
     (1, 2, 128, 4096, 128, torch.bfloat16, False, 1),   # deterministic with split dQ partials
     (2, 2, 77, 133, 40, torch.float32, True, 0),
+    (1, 2, 300, 400, 96, torch.bfloat16, True, 1),      # bf16 width 96: padded copies in the scratch
 ]
 
 
