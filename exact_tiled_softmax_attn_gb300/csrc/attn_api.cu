@@ -435,8 +435,10 @@ int attn_bwd_dq_splits(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t
   if (check_common(B, H, Tq, Tk, d, dv, 1.0f, 0, dtype) != ATTN_OK) return -1;
   if (dtype == ATTN_BF16 && !bf16_bwd_shape(d, dv) && !bf16_bwd_padded(d, dv)) return -1;
   if (deterministic != 0 && deterministic != 1) return -1;
-  const int dk = dtype == ATTN_BF16 && bf16_bwd_padded(d, dv) ? pad_layout(B, H, Tq, Tk, d, dv, deterministic).dp : d;
-  return bwd_layout(B, H, Tq, Tk, dk, dtype, deterministic).dq_splits;
+  // the width the backward runs at (the padded one for other bf16 widths)
+  const int d_run =
+      dtype == ATTN_BF16 && bf16_bwd_padded(d, dv) ? pad_layout(B, H, Tq, Tk, d, dv, deterministic).dp : d;
+  return bwd_layout(B, H, Tq, Tk, d_run, dtype, deterministic).dq_splits;
 }
 
 }  // extern "C"
