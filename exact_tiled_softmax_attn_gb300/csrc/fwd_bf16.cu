@@ -52,7 +52,9 @@ constexpr int NUM_THREADS = 384;   // three warpgroups
 constexpr int REG_CTRL = 96;        // producer / MMA warpgroup
 constexpr int REG_SOFTMAX = 200;   // each softmax warpgroup
 
-// HD = d (Q and K rows), HV = dv (V and O rows); each 64 or 128.
+// Tile widths HD >= d (Q and K rows) and HV >= dv (V and O rows), each 64 or
+// 128; a narrower d or dv reads its missing columns as zeros through the
+// tensor maps, and the epilogue writes only the first dv columns.
 template <int HD, int HV>
 struct Cfg {
   static constexpr int KB = HD / 64;                   // 64-column swizzle blocks per Q / K row
