@@ -1,4 +1,7 @@
-// bf16 attention forward for head size d = 256 on tcgen05 tensor cores.
+// bf16 attention forward for head size d = 256 on tcgen05 tensor cores (and
+// for any row wider than 128 columns: d or dv up to 256, a multiple of 8; the
+// tensor maps read the columns up to 256, or up to the V tile width of 64,
+// 128 or 256, as zeros, and the epilogue writes the first dv columns).
 //
 // The same tiled online softmax as the d <= 128 forward ("Tiled attention with
 // an online softmax", section "Task"; "The Hidden Recurrence in Softmax
