@@ -9,6 +9,8 @@ resident in HBM. Prints one JSON line (rank 0).
 
 N > 1 runs one process per GPU under torch.distributed (each rank processes
 its own batch: weak scaling); the reported time is the max over ranks.
+Started without torch.distributed, --gpus N > 1 launches the N ranks itself
+(torch.distributed.run, one node); under it, N must equal WORLD_SIZE.
 --impl reference times the CPU float64 oracle on the host cores instead.
 """
 from __future__ import annotations
@@ -163,6 +165,35 @@ def dist_setup():
     return world, rank, local
 
 
+def rank_seed(w, rank: int) -> int:
+    """Seed of a rank's batch: every rank draws its own inputs (weak scaling
+    over independent (b, h) problems)."""
+    return w.seed + 1000 * rank
+
+
+def free_port() -> int:
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def relaunch(n: int, argv) -> int:
+    """Run this script as n ranks on one node (one process per GPU) under
+    torch.distributed.run; returns its exit code."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={free_port()}", os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
+def run_dry(args, w):
+    """Print this rank's launch plan (one JSON line per rank) without touching a GPU."""
+    world, rank, local = dist_setup()
+    print(json.dumps({"dry_run": True, "impl": args.impl, "rank": rank, "world": world, "local_rank": local,
+                      "n_gpus": world, "seed": rank_seed(w, rank), "workload": w.name}), flush=True)
+    return 0
+
+
 def reduce_max(value: float) -> float:
     """Max of `value` over all ranks (identity without torch.distributed)."""
     import torch
@@ -278,6 +309,8 @@ def run_ours(args, w):
     from exact_tiled_softmax_attn_gb300.workloads import make_inputs
 
     world, rank, local = dist_setup()
+    if local >= torch.cuda.device_count():
+        raise SystemExit(f"rank {rank}: local rank {local} but {torch.cuda.device_count()} visible GPU(s)")
     if world > 1:
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
@@ -290,7 +323,7 @@ def run_ours(args, w):
     det = int(args.dq_mode == "deterministic")
     es = 2 if w.dtype == "bf16" else 4   # bytes per input element
 
-    host = make_inputs(w.with_(seed=w.seed + 1000 * rank))
+    host = make_inputs(w.with_(seed=rank_seed(w, rank)))
     x = {k: v.to(dev) for k, v in host.items()}
     o = torch.empty(B, H, Tq, dv, dtype=w.torch_dtype, device=dev)
     lse = torch.empty(B, H, Tq, dtype=torch.float32, device=dev)
@@ -547,11 +580,25 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fwd-only", action="store_true",
                     help="time the forward alone (its FLOPs only); the only pass for bf16 d = 256")
+    ap.add_argument("--dry-run", action="store_true",
+                    help="print each rank's launch plan (rank, world, device, input seed) and exit")
+    argv = sys.argv[1:] if argv is None else list(argv)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    # --gpus N: one rank per GPU. Launched without torch.distributed, N > 1
+    # starts the N ranks itself; launched under it, N must be its world size.
+    if "WORLD_SIZE" not in os.environ:
+        if args.gpus > 1:
+            return relaunch(args.gpus, argv)
+    elif int(os.environ["WORLD_SIZE"]) != args.gpus:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={os.environ['WORLD_SIZE']}")
     from exact_tiled_softmax_attn_gb300.workloads import WORKLOADS
     w = WORKLOADS[args.workload]
+    if args.dry_run:
+        return run_dry(args, w)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

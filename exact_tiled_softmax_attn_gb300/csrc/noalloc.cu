@@ -28,24 +28,30 @@ constexpr size_t kNoAllocScratchBytes = ATTN_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
-struct ScratchSlot {
-  std::once_flag once;
-  cudaError_t err = cudaSuccess;
-  void* ptr = nullptr;
-};
-ScratchSlot g_slots[kMaxDevices];
+std::mutex g_slots_mu;
+void* g_slots[kMaxDevices];   // device address of the scratch per device, once looked up
 
-// Device address of the scratch on the current device, resolved once per
-// device (on the first call made with that device current).
+// Device address of the scratch on the current device. Only a successful
+// lookup is kept: with lazy module loading the first lookup on a device is
+// also what loads this file's module and reserves the buffer there, and it
+// can fail (for example while the device's memory is full); the next call
+// then tries again instead of failing for good.
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  ScratchSlot& s = g_slots[dev];
-  std::call_once(s.once, [&] { s.err = cudaGetSymbolAddress(&s.ptr, g_noalloc_scratch); });
-  if (s.err != cudaSuccess) return s.err;
-  *out = s.ptr;
+  std::lock_guard<std::mutex> lock(g_slots_mu);
+  if (g_slots[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+      cudaGetLastError();   // leave no sticky record of the failed lookup
+      return e;
+    }
+    g_slots[dev] = p;
+  }
+  *out = g_slots[dev];
   return cudaSuccess;
 }
 

@@ -168,7 +168,10 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int d, int
  * GB300's 152 SMs) and at least 8 key tiles, each query tile's keys are cut
  * into S ranges (at most 152 units in all, at least 4 key tiles each, S <= 64)
  * whose partial dQ go to the workspace and are then added in split order, so
- * the result stays bitwise reproducible. A rule of the shapes only.
+ * the result stays bitwise reproducible. A rule of the shapes only, so that
+ * the workspace size needs no device: the 152 is GB300's SM count, and on a
+ * device with another SM count the split stays correct but fills the SMs
+ * less evenly.
  */
 ATTN_API int attn_bwd_dq_splits(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype,
                                 int deterministic);
@@ -216,9 +219,12 @@ ATTN_API attn_status_t attn_bwd_phase(const void* Q, const void* K, const void* 
                                       void* workspace, size_t workspace_bytes, int phase, void* stream);
 
 /*
- * Size of the static scratch buffer behind attn_bwd_noalloc (64 MiB). Every
- * device that loads the library holds a buffer of this size until the
- * process exits.
+ * Size of the static scratch buffer behind attn_bwd_noalloc (64 MiB). A
+ * device holds a buffer of this size from the moment the library's code is
+ * loaded on it until the process exits. With CUDA's lazy module loading (the
+ * default since CUDA 12.2) that moment is the first attn_bwd_noalloc call on
+ * the device; with eager loading (CUDA_MODULE_LOADING=EAGER) it is the
+ * library's first use of the device.
  */
 #define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 
@@ -231,16 +237,20 @@ ATTN_API attn_status_t attn_bwd_phase(const void* Q, const void* K, const void* 
  *
  * Arguments, layout and results are those of attn_bwd, without the workspace
  * arguments: the workspace lives in a static device buffer of
- * ATTN_NOALLOC_SCRATCH_BYTES inside the library. Nothing is allocated and no
- * allocating routine is called. Problems whose attn_bwd_workspace_size
+ * ATTN_NOALLOC_SCRATCH_BYTES inside the library (static device data of the
+ * library's module, not a cudaMalloc). The call calls no cudaMalloc,
+ * cudaFree or other allocating routine. Problems whose attn_bwd_workspace_size
  * exceeds that size are rejected with ATTN_ERR_WORKSPACE before anything is
  * enqueued (for bf16 with deterministic == 0 the need is about
  * B*H*Tq*(d+2)*4 bytes; deterministic == 1 or fp32 needs about B*H*Tq*8).
  *
  * The first call on a device (with that device current) looks up the
- * buffer's device address once; make that first call before any stream
- * capture begins. All calls on a device share the one buffer and leave their
- * data in it; each call overwrites everything it reads back (D, and the fp32
+ * buffer's device address, and under lazy module loading that lookup is
+ * also what reserves the 64 MiB on the device, so it can fail with
+ * ATTN_ERR_CUDA (for example while the device's memory is full). Only a
+ * successful lookup is kept: after a failure the next call tries again.
+ * Make the first call on each device before any stream capture begins.
+ * All calls on a device share the one buffer and leave their data in it; each call overwrites everything it reads back (D, and the fp32
  * dQ accumulator, which it zeroes first). Calls whose kernels can overlap on
  * the GPU (different streams without ordering, or several host threads) race
  * on the buffer and corrupt each other's gradients: order them on one stream.

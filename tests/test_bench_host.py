@@ -1,5 +1,7 @@
 """Host-side logic of bench.py (no GPU): the cross-rank max reduction that the
-multi-GPU run uses, on 2 gloo ranks, and the FLOP accounting."""
+multi-GPU run uses, on 2 gloo ranks; the launch of one rank per GPU by
+--gpus N (ranks, devices and input seeds, through --dry-run); the reference
+arm under several ranks; and the FLOP accounting."""
 import os
 import socket
 
@@ -104,3 +106,52 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+
+
+def _json_lines(out):
+    import json
+    return [json.loads(ln) for ln in out.splitlines() if ln.startswith("{")]
+
+
+def test_gpus_flag_without_torchrun_starts_one_rank_per_gpu():
+    """bench.py --gpus 2 started plainly launches two ranks itself, each with
+    its own input seed (seed + 1000 * rank) and the world size in n_gpus."""
+    import subprocess
+    import sys
+    w = WORKLOADS["c3"]
+    cmd = [sys.executable, os.path.join(bench.ROOT, "bench.py"), "--gpus", "2", "--dry-run", "--workload", "c3"]
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, env={**env, "CUDA_VISIBLE_DEVICES": ""})
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = sorted(_json_lines(r.stdout), key=lambda j: j["rank"])
+    assert [j["rank"] for j in lines] == [0, 1]
+    assert all(j["world"] == 2 and j["n_gpus"] == 2 and j["dry_run"] for j in lines)
+    assert [j["local_rank"] for j in lines] == [0, 1]
+    assert [j["seed"] for j in lines] == [w.seed, w.seed + 1000]
+
+
+def test_reference_arm_with_gpus_flag_alone_reports_the_world_size():
+    import subprocess
+    import sys
+    cmd = [sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl", "reference", "--workload", "c1",
+           "--gpus", "2", "--steps", "3", "--warmup", "3"]
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600,
+                       env={**env, "CUDA_VISIBLE_DEVICES": "", "OMP_NUM_THREADS": "1"})
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1 and lines[0]["n_gpus"] == 2 and lines[0]["impl"] == "reference"
+
+
+def test_gpus_flag_must_match_the_launcher_world_size():
+    import subprocess
+    import sys
+    cmd = [sys.executable, os.path.join(bench.ROOT, "bench.py"), "--gpus", "2", "--dry-run"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=120,
+                       env={**os.environ, "WORLD_SIZE": "1", "RANK": "0", "LOCAL_RANK": "0"})
+    assert r.returncode != 0 and "WORLD_SIZE" in r.stderr
+
+
+def test_rank_seeds_are_distinct():
+    w = WORKLOADS["c3"]
+    assert len({bench.rank_seed(w, r) for r in range(8)}) == 8 and bench.rank_seed(w, 0) == w.seed
