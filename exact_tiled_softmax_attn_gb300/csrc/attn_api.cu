@@ -545,15 +545,17 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
   if (dtype == ATTN_F32) {
     e = launch_bwd_f32(a);
   } else {
-    CUtensorMap mq, mk, mv, mdo, mdq;
+    CUtensorMap mq, mk, mv, mdo, mo, mdq;
     if ((s = make_map(&mq, Q, d, Tq, static_cast<int>(bh))) != ATTN_OK) return s;
     if ((s = make_map(&mk, K, d, Tk, static_cast<int>(bh))) != ATTN_OK) return s;
     if ((s = make_map(&mv, V, dv, Tk, static_cast<int>(bh))) != ATTN_OK) return s;
     if ((s = make_map(&mdo, dO, dv, Tq, static_cast<int>(bh))) != ATTN_OK) return s;
+    if ((s = make_map(&mo, O, dv, Tq, static_cast<int>(bh))) != ATTN_OK) return s;
     a.tmQ = &mq;
     a.tmK = &mk;
     a.tmV = &mv;
     a.tmdO = &mdo;
+    a.tmO = &mo;
     a.tmdQacc = nullptr;
     if (a.dQacc) {
       if ((s = make_map(&mdq, a.dQacc, d, Tq, static_cast<int>(bh), true)) != ATTN_OK) return s;

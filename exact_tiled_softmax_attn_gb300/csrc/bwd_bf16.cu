@@ -35,7 +35,9 @@
 // kernel (a unit per query tile looping over key tiles in a fixed order, or
 // per query tile and key range when query tiles are few) accumulates dQ in
 // TMEM and writes it once (or its range's fp32 partial, added in order by
-// reduce_dq_kernel). The dQ and dK/dV kernels take d (Q, K, dQ, dK) and dv (V,
+// reduce_dq_kernel). That kernel keeps Q and dO in TMEM as the A operands of
+// S = Q K^T and dP = dO V^T, so all three of its products per key tile read
+// only a K or V tile from shared memory. The dQ and dK/dV kernels take d (Q, K, dQ, dK) and dv (V,
 // O, dO, dV) as separate template parameters, each 64 or 128.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -93,7 +95,6 @@ struct Params {
   Problem p;
   float* NLSE2;            // [BH, Tq_pad]: -LSE * log2(e), -inf on padding / no-key rows
   float* D;                // [BH, Tq_pad]
-  const __nv_bfloat16* O;  // forward output (deterministic dQ kernel: D of its rows)
   const float* LSE;        // [BH, Tq] natural-log LSE from the forward
   int Tq_pad;
   float* dQacc;            // atomic path: fp32 [BH, Tq, d], pre-zeroed
@@ -758,53 +759,61 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
 
 // ---------------------------------------------------------------- deterministic dQ
 
+// Every tile the dQ kernel reads passes through one FIFO ring of equal slots
+// in the order it is consumed: per unit its Q, dO and O tiles, then K_0, V_0,
+// K_1, V_1, ... of its key tiles. The row threads move Q and dO from their
+// slots into tensor memory (and use dO and O for D = rowsum(dO o O)), after
+// which the slots go back to the ring; Q and dO then serve from tensor memory
+// as the A operands of S = Q K^T and dP = dO V^T. Each of the three products
+// per key tile therefore reads only its B operand (a K or V tile) from shared
+// memory: 96 KB of operand reads per key tile at d = dv = 128 instead of 160,
+// and the slots Q and dO would occupy all unit long stream K and V instead.
 template <int HD, int HV>
 struct CfgQ {
   static constexpr int KB = HD / 64;          // 64-column boxes per Q / K row
-  static constexpr int KBV = HV / 64;         // ... per V / dO row
+  static constexpr int KBV = HV / 64;         // ... per V / dO / O row
   static constexpr int TILE = BT * HD * 2;    // one 128-row Q or K tile
-  static constexpr int TILE_V = BT * HV * 2;  // one 128-row V or dO tile
-  // K and V tiles have rings of their own. A K tile stays resident from its
-  // S product to its dQ product one step later, a V tile only until its dP
-  // product, so at d = dv = 128 K gets four slots and V one: a K tile then
-  // arrives about two key steps ahead of its first use, a V tile one. The
-  // smaller tiles of d or dv = 64 leave room for more slots.
-  static constexpr int NSK = (HD == 64 && HV == 64) ? 8 : 4;
-  static constexpr int NSV = (HD == 128 && HV == 128) ? 1 : (HD == 64 && HV == 64) ? 2 : 3;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_DO = OFF_Q + TILE;
-  static constexpr int OFF_K = OFF_DO + TILE_V;        // [NSK]
-  static constexpr int OFF_V = OFF_K + NSK * TILE;     // [NSV]
-  static constexpr int OFF_DPART = OFF_V + NSV * TILE_V;   // [2][128] fp32 partial D of the row groups
-  static constexpr int OFF_BAR = OFF_DPART + 2 * BT * 4;
-  // q_full, q_empty, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full, s_free, dp_full[2],
-  // ds_full[2], dq_full, drain, dpart_full
-  static constexpr int NBAR = 2 + 2 * NSK + 2 * NSV + 9;
+  static constexpr int TILE_V = BT * HV * 2;  // one 128-row V, dO or O tile
+  static constexpr int SLOT = TILE > TILE_V ? TILE : TILE_V;
+  static constexpr int DPART_BYTES = 2 * 2 * BT * 4;   // [unit parity][row group][128] fp32 partial D
+  static constexpr int NSLOT_FIT = (227 * 1024 - DPART_BYTES - 256) / SLOT;
+  static constexpr int NSLOT = NSLOT_FIT < 16 ? NSLOT_FIT : 16;   // 7 at d = dv = 128
+  static constexpr int OFF_RING = 0;
+  static constexpr int OFF_DPART = OFF_RING + NSLOT * SLOT;
+  static constexpr int OFF_BAR = OFF_DPART + DPART_BYTES;
+  // full[NSLOT], empty[NSLOT], qd_ready, s_full, s_free, dp_full, ds_full, dq_full, drain, dpart_full
+  static constexpr int NBAR = 2 * NSLOT + 8;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
-  static constexpr uint32_t IDESC_S = ptx::idesc_bf16(BT, BT, false, false);
-  static constexpr uint32_t IDESC_DQ = ptx::idesc_bf16(BT, HD, false, true);
+  static constexpr uint32_t IDESC_S = ptx::idesc_bf16(BT, BT, false, false);    // S, dP (A in TMEM)
+  static constexpr uint32_t IDESC_DQ = ptx::idesc_bf16(BT, HD, false, true);    // dQ (A in TMEM, K MN-major)
+  // TMEM columns: Q and dO as packed bf16 (two elements per column), the S
+  // and dP tiles (fp32; dS is packed over the first half of each group's dP
+  // columns), the dQ accumulator
+  static constexpr uint32_t T_Q = 0, T_DO = 64, T_S = 128, T_DP = 256, T_DQ = 384;
+  static_assert(HD / 2 <= 64 && HV / 2 <= 64 && T_DQ + HD <= 512, "TMEM columns");
 };
 constexpr int DQ_THREADS = 320;
 
 // One persistent CTA per SM; a unit is one 128-row query tile of one head.
-// The row threads first form the tile's D = rowsum(dO o O) (dO from shared
-// memory, O from global memory) and -LSE * log2(e), which they use and store
-// for the dK/dV kernel that runs after this one. Then, for each key tile
-// (fixed ascending order): S = Q K^T, dP = dO V^T (both in TMEM), dS =
-// P o (dP - D) written bf16 over dP, and dQ += dS K accumulates in TMEM.
+// Per unit the row threads stage Q and dO into TMEM and form the tile's D =
+// rowsum(dO o O) and -LSE * log2(e), which they use and store for the dK/dV
+// kernel that runs after this one. Then, for each key tile (fixed ascending
+// order): S = Q K^T and dP = dO V^T (both in TMEM), dS = P o (dP - D) written
+// bf16 over dP, and dQ += dS K accumulates in TMEM. Per key tile j the MMA
+// warp issues S_{j+1}, dQ_j, dP_{j+1}: the next scores are computed while the
+// row threads turn dP_j into dS_j, and dP_{j+1} overwrites the dP tile only
+// after dQ_j has read dS_j (MMAs of one thread run in issue order).
 // Warps: 0 producer, 1 MMA, 2-5 and 6-9 two row groups; group g works on key
-// columns [64g, 64g + 64) of every query row (one thread per row each) and
-// packs its dS at columns [64g, 64g + 32) of the dP buffer.
-// TMEM: S [0, 128), dQ [128, 256), dP/dS in two buffers [256, 384) and
-// [384, 512) alternating by step, so the MMA warp computes dP of step j + 1
-// while the row threads still turn dP of step j into dS.
+// columns [64g, 64g + 64) of every query row (one thread per row each), packs
+// its dS at columns [64g, 64g + 32) of the dP tile, and stages columns
+// [g d/2, (g + 1) d/2) of Q (and of dO) into TMEM.
 // SPLIT: key ranges per unit, fp32 partial dQ (see Params).
 template <int HD, int HV, bool SPLIT>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-              const Params P) {
+              const __grid_constant__ CUtensorMap tmO, const Params P) {
   using C = CfgQ<HD, HV>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
@@ -813,44 +822,31 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     if (threadIdx.x == 0) atomicOr(P.status, ATTN_DEV_BAD_SMEM);
     return;
   }
-  uint8_t* sQ = smem + C::OFF_Q;
-  uint8_t* sdO = smem + C::OFF_DO;
-  uint8_t* sK = smem + C::OFF_K;
-  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* ring = smem + C::OFF_RING;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* q_full = bars + 0;
-  uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;               // [NSK]
-  uint64_t* k_empty = k_full + C::NSK;       // [NSK]
-  uint64_t* v_full = k_empty + C::NSK;       // [NSV]
-  uint64_t* v_empty = v_full + C::NSV;       // [NSV]
-  uint64_t* s_full = v_empty + C::NSV;
-  uint64_t* s_free = s_full + 1;
-  uint64_t* dp_full = s_full + 2;   // [2], by step parity
-  uint64_t* ds_full = s_full + 4;   // [2], by step parity
-  uint64_t* dq_full = s_full + 6;
-  uint64_t* drain = s_full + 7;
-  uint64_t* dpart_full = s_full + 8;   // both row groups have written their partial D
+  uint64_t* full = bars;                   // [NSLOT]
+  uint64_t* empty = full + C::NSLOT;       // [NSLOT]
+  uint64_t* qd_ready = empty + C::NSLOT;   // the row threads staged a unit's Q and dO (and read its O)
+  uint64_t* s_full = qd_ready + 1;
+  uint64_t* s_free = qd_ready + 2;
+  uint64_t* dp_full = qd_ready + 3;
+  uint64_t* ds_full = qd_ready + 4;
+  uint64_t* dq_full = qd_ready + 5;
+  uint64_t* drain = qd_ready + 6;
+  uint64_t* dpart_full = qd_ready + 7;     // both row groups have written a unit's partial D
   float* dpart = reinterpret_cast<float*>(smem + C::OFF_DPART);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
   if (threadIdx.x == 0) {
-    ptx::mbar_init(q_full, 1);
-    ptx::mbar_init(q_empty, 1);
-    for (int s = 0; s < C::NSK; ++s) {
-      ptx::mbar_init(k_full + s, 1);
-      ptx::mbar_init(k_empty + s, 1);
+    for (int s = 0; s < C::NSLOT; ++s) {
+      ptx::mbar_init(full + s, 1);
+      ptx::mbar_init(empty + s, 1);
     }
-    for (int s = 0; s < C::NSV; ++s) {
-      ptx::mbar_init(v_full + s, 1);
-      ptx::mbar_init(v_empty + s, 1);
-    }
+    ptx::mbar_init(qd_ready, 256);
     ptx::mbar_init(s_full, 1);
     ptx::mbar_init(s_free, 256);
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(dp_full + b, 1);
-      ptx::mbar_init(ds_full + b, 256);
-    }
+    ptx::mbar_init(dp_full, 1);
+    ptx::mbar_init(ds_full, 256);
     ptx::mbar_init(dq_full, 1);
     ptx::mbar_init(drain, 1);
     ptx::mbar_init(dpart_full, 256);
@@ -865,76 +861,53 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t T_S = 0, T_DQ = 128;
-  auto t_dp = [](uint32_t step) { return 256u + 128u * (step & 1u); };   // dP / dS buffer of a step
   const int grid = gridDim.x, cta = blockIdx.x;
   const int Tq = P.p.Tq, Tk = P.p.Tk;
-  // Key tile j of a unit is the CTA's tile number t = k_it + j (k_it runs
-  // across units); its K sits in K slot t % NSK, its V in V slot t % NSV.
-  auto kslot = [](uint32_t t) { return static_cast<int>(t % C::NSK); };
-  auto kpar = [](uint32_t t) { return (t / C::NSK) & 1u; };
-  auto vslot = [](uint32_t t) { return static_cast<int>(t % C::NSV); };
-  auto vpar = [](uint32_t t) { return (t / C::NSV) & 1u; };
+  // Ring item i (counted across units) sits in slot i % NSLOT. A unit whose
+  // first item is i0 has Q at i0, dO at i0 + 1, O at i0 + 2, and K_j, V_j of
+  // its j-th key tile at i0 + 3 + 2j and i0 + 4 + 2j.
+  auto slot = [](uint32_t i) { return static_cast<int>(i % C::NSLOT); };
+  auto par = [](uint32_t i) { return (i / C::NSLOT) & 1u; };
 
   if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
     ptx::WaitCtx w{abort_flag, P.status, 5u};
-    uint32_t u_it = 0, k_it = 0;
+    ptx::tma_prefetch_desc(&tmQ);
+    ptx::tma_prefetch_desc(&tmK);
+    ptx::tma_prefetch_desc(&tmV);
+    ptx::tma_prefetch_desc(&tmdO);
+    ptx::tma_prefetch_desc(&tmO);
+    uint32_t item = 0;
     bool ok = true;
     int bh, blk;
+    auto load = [&](const CUtensorMap* map, int boxes, uint32_t bytes, int row) {
+      const int s = slot(item);
+      if (!ptx::mbar_wait(empty + s, par(item) ^ 1u, w)) return false;
+      ptx::mbar_arrive_expect_tx(full + s, bytes);
+      for (int b = 0; b < boxes; ++b) ptx::tma_load_3d(ring + s * C::SLOT + b * BOX_BYTES, map, full + s, b * 64, row, bh);
+      ++item;
+      return true;
+    };
     for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &blk); ++round) {
       int qt, sp_, j0, nk;
       if (!dq_unit<SPLIT>(P, blk, &qt, &sp_, &j0, &nk)) continue;
-      {
-        // the next unit's O rows (its D) into L2 while this unit runs
-        int bh2, blk2;
-        if (P.order.unit(cta, grid, round + 1, &bh2, &blk2)) {
-          const int qt2 = SPLIT ? blk2 / P.dq_splits : blk2;
-          const int rows = min(BT, Tq - qt2 * BT);
-          ptx::bulk_prefetch_l2(P.O + (static_cast<size_t>(bh2) * Tq + static_cast<size_t>(qt2) * BT) * HV,
-                                static_cast<uint32_t>(rows) * HV * 2);
-        }
-      }
-      if (!(ok = ptx::mbar_wait(q_empty, (u_it & 1u) ^ 1u, w))) break;
-      // the row threads read dO from shared memory for D at their first key
-      // tile, which can come after the unit's last MMA has read Q and dO (a
-      // unit of one or two key tiles): the next unit's tiles wait for both
-      // groups' partial D of the previous unit as well
-      if (!(ok = ptx::mbar_wait(dpart_full, (u_it & 1u) ^ 1u, w))) break;
-      ptx::mbar_arrive_expect_tx(q_full, C::TILE + C::TILE_V);
-      for (int b = 0; b < C::KB; ++b) ptx::tma_load_3d(sQ + b * BOX_BYTES, &tmQ, q_full, b * 64, qt * BT, bh);
-      for (int b = 0; b < C::KBV; ++b) ptx::tma_load_3d(sdO + b * BOX_BYTES, &tmdO, q_full, b * 64, qt * BT, bh);
-      uint32_t k_issued = k_it, v_issued = k_it;   // tiles issued so far
-      for (int j = 0; ok && j < nk; ++j, ++k_it) {
-        const uint32_t t = k_it;
-        if (!(ok = ptx::mbar_wait(k_empty + kslot(t), kpar(t) ^ 1u, w))) break;
-        ptx::mbar_arrive_expect_tx(k_full + kslot(t), C::TILE);
-        for (int b = 0; b < C::KB; ++b)
-          ptx::tma_load_3d(sK + kslot(t) * C::TILE + b * BOX_BYTES, &tmK, k_full + kslot(t), b * 64, (j0 + j) * BT, bh);
-        k_issued = t + 1;
-        if (!(ok = ptx::mbar_wait(v_empty + vslot(t), vpar(t) ^ 1u, w))) break;
-        ptx::mbar_arrive_expect_tx(v_full + vslot(t), C::TILE_V);
-        for (int b = 0; b < C::KBV; ++b)
-          ptx::tma_load_3d(sV + vslot(t) * C::TILE_V + b * BOX_BYTES, &tmV, v_full + vslot(t), b * 64, (j0 + j) * BT,
-                           bh);
-        v_issued = t + 1;
-      }
-      if (!ok) {
-        // Let the copies already in flight land before the CTA exits.
-        for (uint32_t n = (k_issued > (uint32_t)C::NSK ? k_issued - C::NSK : 0u); n < k_issued; ++n)
-          ptx::mbar_wait_drain(k_full + kslot(n), kpar(n));
-        for (uint32_t n = (v_issued > (uint32_t)C::NSV ? v_issued - C::NSV : 0u); n < v_issued; ++n)
-          ptx::mbar_wait_drain(v_full + vslot(n), vpar(n));
-        ptx::mbar_wait_drain(q_full, u_it & 1u);
-        break;
-      }
-      ++u_it;
+      ok = load(&tmQ, C::KB, C::TILE, qt * BT) && load(&tmdO, C::KBV, C::TILE_V, qt * BT) &&
+           load(&tmO, C::KBV, C::TILE_V, qt * BT);
+      for (int j = 0; ok && j < nk; ++j)
+        ok = load(&tmK, C::KB, C::TILE, (j0 + j) * BT) && load(&tmV, C::KBV, C::TILE_V, (j0 + j) * BT);
+    }
+    if (!ok) {
+      // Let the copies already in flight land before the CTA exits: each of
+      // the last NSLOT items issued is the latest load of its slot.
+      for (uint32_t n = (item > static_cast<uint32_t>(C::NSLOT) ? item - C::NSLOT : 0u); n < item; ++n)
+        ptx::mbar_wait_drain(full + slot(n), par(n));
     }
   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
     // The whole warp follows the schedule and waits; the elected lane (lane 0)
     // issues the MMAs and commits (see the dK/dV kernel).
     ptx::WaitCtx w{abort_flag, P.status, 6u};
-    const uint32_t aQ = ptx::smem_u32(sQ), adO = ptx::smem_u32(sdO), aK = ptx::smem_u32(sK),
-                   aV = ptx::smem_u32(sV);
+    const uint32_t aR = ptx::smem_u32(ring);
     auto kmaj = [](uint32_t base, int kk) {
       return ptx::sdesc_advance(ptx::sdesc_sw128(base, 16, 1024), (kk >> 2) * BOX_BYTES + (kk & 3) * 32);
     };
@@ -944,89 +917,86 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     auto wait = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, w));
     };
-    uint32_t u_it = 0, k_it = 0, sp = 0;
-    bool ok = true, moved = false;
-    int bh, blk;
-    auto mma_s = [&](uint32_t t) {   // S = Q K^T with key tile t
+    auto mma_s = [&](uint32_t ik) {   // S = Q K^T: Q from TMEM (8 columns per 16 of d), K tile of item ik
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk)
-        ptx::mma_ss(tmem + T_S, kmaj(aQ, kk), kmaj(aK + kslot(t) * C::TILE, kk), C::IDESC_S, kk > 0);
+        ptx::mma_ts(tmem + C::T_S, tmem + C::T_Q + 8 * kk, kmaj(aR + slot(ik) * C::SLOT, kk), C::IDESC_S, kk > 0);
+      ptx::mma_commit(s_full);
     };
-    auto mma_dp = [&](uint32_t t, uint32_t step) {   // dP = dO V^T into the step's buffer
+    auto mma_dp = [&](uint32_t iv) {   // dP = dO V^T: dO from TMEM, V tile of item iv (read by nothing later)
 #pragma unroll
       for (int kk = 0; kk < HV / 16; ++kk)
-        ptx::mma_ss(tmem + t_dp(step), kmaj(adO, kk), kmaj(aV + vslot(t) * C::TILE_V, kk), C::IDESC_S, kk > 0);
-      ptx::mma_commit(dp_full + (step & 1u));
-      ptx::mma_commit(v_empty + vslot(t));
+        ptx::mma_ts(tmem + C::T_DP, tmem + C::T_DO + 8 * kk, kmaj(aR + slot(iv) * C::SLOT, kk), C::IDESC_S,
+                    kk > 0);
+      ptx::mma_commit(dp_full);
+      ptx::mma_commit(empty + slot(iv));
     };
+    uint32_t item = 0, u_it = 0, sp = 0;
+    bool ok = true, moved = false;
+    int bh, blk;
     for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &blk); ++round) {
       int qt, sp_, j0, nk;
       if (!dq_unit<SPLIT>(P, blk, &qt, &sp_, &j0, &nk)) continue;
-      if (!(ok = wait(q_full, u_it & 1u))) break;
+      const uint32_t i0 = item;
+      // Q and dO are in TMEM and the row threads are done with the three
+      // staging slots, which go back to the ring
+      if (!(ok = wait(qd_ready, u_it & 1u))) break;
+      if (lane == 0)
+        for (int k = 0; k < 3; ++k) ptx::mbar_arrive(empty + slot(i0 + k));
+      __syncwarp();
       // S and dP of the first key tile
-      {
-        const uint32_t t = k_it;
-        if (!(ok = wait(k_full + kslot(t), kpar(t)))) break;
-        ptx::tc_fence_after();
-        if (ptx::elect_one()) {
-          moved |= lane != 0;
-          mma_s(t);
-          ptx::mma_commit(s_full);
-        }
-        __syncwarp();
-        if (!(ok = wait(v_full + vslot(t), vpar(t)))) break;
-        ptx::tc_fence_after();
-        if (ptx::elect_one()) {
-          moved |= lane != 0;
-          mma_dp(t, sp);
-          // Q and dO are read by no later MMA of a one-tile unit: the next
-          // unit's tiles may start loading now
-          if (nk == 1) ptx::mma_commit(q_empty);
-        }
-        __syncwarp();
-        // K of the next key tile: each step waits for the K tile of the step
-        // after it while its own MMAs run
-        if (nk > 1 && !(ok = wait(k_full + kslot(t + 1), kpar(t + 1)))) break;
+      if (!(ok = wait(full + slot(i0 + 3), par(i0 + 3)))) break;
+      ptx::tc_fence_after();
+      if (ptx::elect_one()) {
+        moved |= lane != 0;
+        mma_s(i0 + 3);
       }
+      __syncwarp();
+      if (!(ok = wait(full + slot(i0 + 4), par(i0 + 4)))) break;
+      ptx::tc_fence_after();
+      if (ptx::elect_one()) {
+        moved |= lane != 0;
+        mma_dp(i0 + 4);
+      }
+      __syncwarp();
+      // K of the next key tile: each step waits for the tiles of the step
+      // after it while its own MMAs run
+      if (nk > 1 && !(ok = wait(full + slot(i0 + 5), par(i0 + 5)))) break;
       for (int j = 0; j < nk; ++j, ++sp) {
-        const uint32_t t = k_it + j, tn = t + 1;   // K of tile tn is resident
+        const uint32_t ik = i0 + 3 + 2 * j;   // K_j; V_{j+1} = ik + 3, K_{j+1} = ik + 2, K_{j+2} = ik + 4
         if (j + 1 < nk) {
-          // S of the next key tile once the row threads have read this one,
-          // then its dP into the other buffer (whose dS the previous dQ
-          // product has consumed: MMAs run in issue order)
+          // S of the next key tile once the row threads hold this one in registers
           if (!(ok = wait(s_free, sp & 1u))) break;
           ptx::tc_fence_after();
           if (ptx::elect_one()) {
             moved |= lane != 0;
-            mma_s(tn);
-            ptx::mma_commit(s_full);
-          }
-          __syncwarp();
-          if (!(ok = wait(v_full + vslot(tn), vpar(tn)))) break;
-          ptx::tc_fence_after();
-          if (ptx::elect_one()) {
-            moved |= lane != 0;
-            mma_dp(tn, sp + 1);
-            // the last S and dP of the unit are out: Q and dO are free for
-            // the next unit while the last dQ products run
-            if (j + 2 == nk) ptx::mma_commit(q_empty);
+            mma_s(ik + 2);
           }
           __syncwarp();
         }
         // dQ += dS K
-        if (!(ok = wait(ds_full + (sp & 1u), (sp >> 1) & 1u))) break;
+        if (!(ok = wait(ds_full, sp & 1u))) break;
         ptx::tc_fence_after();
         if (ptx::elect_one()) {
           moved |= lane != 0;
 #pragma unroll
           for (int kk = 0; kk < BT / 16; ++kk)
-            ptx::mma_ts(tmem + T_DQ, tmem + t_dp(sp) + packed_col(kk), mnmaj(aK + kslot(t) * C::TILE, kk),
-                        C::IDESC_DQ,
-                        (j > 0 || kk > 0) ? 1u : 0u);
-          ptx::mma_commit(k_empty + kslot(t));
+            ptx::mma_ts(tmem + C::T_DQ, tmem + C::T_DP + packed_col(kk), mnmaj(aR + slot(ik) * C::SLOT, kk),
+                        C::IDESC_DQ, (j > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_commit(empty + slot(ik));
         }
         __syncwarp();
-        if (j + 2 < nk && !(ok = wait(k_full + kslot(t + 2), kpar(t + 2)))) break;
+        if (j + 1 < nk) {
+          // dP of the next key tile, into the tile dQ_j has just been given
+          if (!(ok = wait(full + slot(ik + 3), par(ik + 3)))) break;
+          ptx::tc_fence_after();
+          if (ptx::elect_one()) {
+            moved |= lane != 0;
+            mma_dp(ik + 3);
+          }
+          __syncwarp();
+        }
+        if (j + 2 < nk && !(ok = wait(full + slot(ik + 4), par(ik + 4)))) break;
       }
       if (!ok) break;
       if (ptx::elect_one()) {
@@ -1034,7 +1004,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         ptx::mma_commit(dq_full);
       }
       __syncwarp();
-      k_it += nk;
+      item = i0 + 3 + 2 * nk;
       ++u_it;
     }
     if (!ok) {
@@ -1044,38 +1014,100 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     }
     if (__any_sync(0xffffffffu, moved) && lane == 0) atomicOr(P.status, ATTN_DEV_ISSUER);
   } else if (warp >= 2) {
+    // ------------------------------------------------------------ row groups
     const int g = (warp - 2) >> 2;          // row group: key columns [64g, 64g + 64)
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_off + T_S + 64 * g, tDQ = tmem + lane_off + T_DQ + (HD / 2) * g;
+    const uint32_t tS = tmem + lane_off + C::T_S + 64 * g, tDP = tmem + lane_off + C::T_DP + 64 * g;
+    const uint32_t tDQ = tmem + lane_off + C::T_DQ + (HD / 2) * g;
+    const uint32_t tQ = tmem + lane_off + C::T_Q + (HD / 4) * g, tDO = tmem + lane_off + C::T_DO + (HV / 4) * g;
     ptx::WaitCtx w{abort_flag, P.status, 7u + g};
     const float sc2 = P.sc2, scale = P.p.scale;
-    uint32_t u_it = 0, sp = 0;
-    bool ok = true;
-    int bh, blk;
-    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &blk); ++round) {
-      int qt, split, j0, nk;
-      if (!dq_unit<SPLIT>(P, blk, &qt, &split, &j0, &nk)) continue;
+    // Stage the unit whose first ring item is i0 (the u-th unit of this CTA):
+    // this group's half of row r of Q and of dO into TMEM, and its half of
+    // D_r = sum_c dO_rc O_rc ("attention_backprop", section "Gradient of S":
+    // ROW_SUM(dL/dO o O)) into dpart. Rows past Tq load as zeros.
+    auto stage = [&](uint32_t i0, uint32_t u) {
+      for (int k = 0; k < 3; ++k)
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(full + slot(i0 + k), par(i0 + k), w))) return false;
+      const uint8_t* sq = ring + slot(i0) * C::SLOT;
+      const uint8_t* sdo = ring + slot(i0 + 1) * C::SLOT;
+      const uint8_t* so = ring + slot(i0 + 2) * C::SLOT;
+      {
+        uint32_t v[HD / 4];
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint4 x = *reinterpret_cast<const uint4*>(sq + sw128_offset(r, (HD / 2) * g + 8 * k));
+          v[4 * k] = x.x;
+          v[4 * k + 1] = x.y;
+          v[4 * k + 2] = x.z;
+          v[4 * k + 3] = x.w;
+        }
+        if constexpr (HD == 128) ptx::tmem_st32(tQ, v); else ptx::tmem_st16(tQ, v);
+      }
+      float part = 0.f;
+      {
+        uint32_t v[HV / 4];
+#pragma unroll
+        for (int k = 0; k < HV / 16; ++k) {
+          const uint32_t off = sw128_offset(r, (HV / 2) * g + 8 * k);
+          const uint4 x = *reinterpret_cast<const uint4*>(sdo + off);
+          const uint4 o = *reinterpret_cast<const uint4*>(so + off);
+          v[4 * k] = x.x;
+          v[4 * k + 1] = x.y;
+          v[4 * k + 2] = x.z;
+          v[4 * k + 3] = x.w;
+          const __nv_bfloat162* dv = reinterpret_cast<const __nv_bfloat162*>(&x);
+          const __nv_bfloat162* ov = reinterpret_cast<const __nv_bfloat162*>(&o);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 a = __bfloat1622float2(ov[e]), b = __bfloat1622float2(dv[e]);
+            part = fmaf(a.x, b.x, part);
+            part = fmaf(a.y, b.y, part);
+          }
+        }
+        if constexpr (HV == 128) ptx::tmem_st32(tDO, v); else ptx::tmem_st16(tDO, v);
+      }
+      dpart[((u & 1u) * 2 + g) * BT + r] = part;
+      ptx::mbar_arrive(dpart_full);
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(qd_ready);
+      return true;
+    };
+    // the next unit of this CTA with at least one key tile, from round *rnd on
+    auto next_unit = [&](int* rnd, int* bh, int* qt, int* split, int* j0, int* nk) {
+      int b, bl;
+      while (P.order.unit(cta, grid, *rnd, &b, &bl)) {
+        ++*rnd;
+        if (dq_unit<SPLIT>(P, bl, qt, split, j0, nk)) {
+          *bh = b;
+          return true;
+        }
+      }
+      return false;
+    };
+    uint32_t item = 0, u_it = 0, sp = 0;
+    int round = 0, bh, qt, split, j0, nk;
+    bool have = next_unit(&round, &bh, &qt, &split, &j0, &nk);
+    bool ok = !have || stage(0u, 0u);
+    while (ok && have) {
       const int q = qt * BT + r;
       const bool q_ok = q < Tq;
-      // D_q = sum_c dO_qc O_qc ("attention_backprop", section "Gradient of
-      // S": ROW_SUM(dL/dO o O)) over this group's half of the columns, dO
-      // from the resident tile, O from global memory; padding rows get D = 0
-      // and -LSE * log2(e) = -inf, so their P and dS are 0
-      // this row's O columns come in while the first S is computed; the
-      // dot product and the exchange with the other group follow the first
-      // step's exponentials (D is first needed for the first dS)
-      uint4 o4[HV / 16];
-#pragma unroll
-      for (int k = 0; k < HV / 16; ++k) {
-        o4[k] = make_uint4(0u, 0u, 0u, 0u);
-        if (q_ok)
-          o4[k] = *reinterpret_cast<const uint4*>(P.O + (static_cast<size_t>(bh) * Tq + q) * HV + (HV / 2) * g + 8 * k);
-      }
       const float lse = q_ok ? P.LSE[static_cast<size_t>(bh) * Tq + q] : -CUDART_INF_F;
       const float nlse2 = (lse == -CUDART_INF_F) ? -CUDART_INF_F : -lse * LOG2E;
-      float dd = 0.f;
+      // D of this unit: the two groups' halves (padding rows get D = 0 and
+      // -LSE * log2(e) = -inf, so their P and dS are 0)
+      if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dpart_full, u_it & 1u, w)))) break;
+      const float* dpu = dpart + (u_it & 1u) * 2 * BT;
+      const float dd = dpu[r] + dpu[BT + r];
+      // stored for every row of the padded tile: the dK/dV kernel reads whole
+      // 128-row slices, and its padding rows must hold D = 0, -inf
+      if (g == 0 && split == 0) {   // (every split forms the same D)
+        P.D[static_cast<size_t>(bh) * P.Tq_pad + q] = dd;
+        P.NLSE2[static_cast<size_t>(bh) * P.Tq_pad + q] = nlse2;
+      }
       for (int j = 0; j < nk; ++j, ++sp) {
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(s_full, sp & 1u, w)))) break;
         ptx::tc_fence_after();
@@ -1100,31 +1132,6 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
               p[c * 32 + i + 1] = ptx::ex2(x.y);
             }
         }
-        if (j == 0) {
-          // dO of the tile is resident once q_full completed
-          if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(q_full, u_it & 1u, w)))) break;
-          float part = 0.f;
-#pragma unroll
-          for (int k = 0; k < HV / 16; ++k) {
-            const uint4 d4 = *reinterpret_cast<const uint4*>(sdO + sw128_offset(r, (HV / 2) * g + 8 * k));
-            const __nv_bfloat162* ov = reinterpret_cast<const __nv_bfloat162*>(&o4[k]);
-            const __nv_bfloat162* dv = reinterpret_cast<const __nv_bfloat162*>(&d4);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 a = __bfloat1622float2(ov[e]), b = __bfloat1622float2(dv[e]);
-              part = fmaf(a.x, b.x, part);
-              part = fmaf(a.y, b.y, part);
-            }
-          }
-          dpart[g * BT + r] = part;
-          ptx::mbar_arrive(dpart_full);
-          if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dpart_full, u_it & 1u, w)))) break;
-          dd = dpart[r] + dpart[BT + r];
-          if (g == 0 && split == 0) {   // (every split forms the same D)
-            P.D[static_cast<size_t>(bh) * P.Tq_pad + q] = dd;
-            P.NLSE2[static_cast<size_t>(bh) * P.Tq_pad + q] = nlse2;
-          }
-        }
         const int kv0 = (j0 + j) * BT + 64 * g;  // key of this thread's first column
         if (kv0 + 64 > Tk || (P.p.causal && kv0 + 63 > q)) {
           const int lim = min(Tk - kv0, P.p.causal ? q - kv0 + 1 : 64);   // columns [0, lim) allowed
@@ -1132,9 +1139,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           for (int i = 0; i < 64; ++i)
             if (i >= lim) p[i] = 0.f;
         }
-        if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dp_full + (sp & 1u), (sp >> 1) & 1u, w)))) break;
+        if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dp_full, sp & 1u, w)))) break;
         ptx::tc_fence_after();
-        const uint32_t tDP = tmem + lane_off + t_dp(sp) + 64 * g;
         uint32_t v[2][32];
 #pragma unroll
         for (int c = 0; c < 2; ++c) ptx::tmem_ld32(tDP + c * 32, v[c]);   // both in flight
@@ -1155,9 +1161,16 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         }
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(ds_full + (sp & 1u));
+        ptx::mbar_arrive(ds_full);
       }
       if (!ok) break;
+      // The next unit's Q and dO go into TMEM now: the S and dP products that
+      // read this unit's have completed (their results were consumed above),
+      // so the next unit's first S can start while this unit's epilogue runs.
+      const uint32_t i_next = item + 3 + 2 * nk;
+      int nbh = 0, nqt = 0, nsplit = 0, nj0 = 0, nnk = 0;
+      const bool have_next = next_unit(&round, &nbh, &nqt, &nsplit, &nj0, &nnk);
+      if (have_next && !(ok = stage(i_next, u_it + 1))) break;
       if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dq_full, u_it & 1u, w)))) break;
       ptx::tc_fence_after();
       // this group writes dQ columns [g HD / 2, (g + 1) HD / 2) of its row
@@ -1178,30 +1191,37 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
                               __uint_as_float(v[4 * e + 2]) * scale, __uint_as_float(v[4 * e + 3]) * scale);
           }
         }
-        ptx::tc_fence_before();
-        ++u_it;
-        continue;
-      }
-      __nv_bfloat16* row = P.dQ + (static_cast<size_t>(bh) * Tq + (q_ok ? q : 0)) * HD + (HD / 2) * g;
+      } else {
+        __nv_bfloat16* row = P.dQ + (static_cast<size_t>(bh) * Tq + (q_ok ? q : 0)) * HD + (HD / 2) * g;
 #pragma unroll
-      for (int c = 0; c < HD / 64; ++c) {
-        uint32_t v[32];
-        ptx::tmem_ld32(tDQ + c * 32, v);
-        ptx::tmem_ld_wait(v);
-        if (q_ok) {
+        for (int c = 0; c < HD / 64; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld32(tDQ + c * 32, v);
+          ptx::tmem_ld_wait(v);
+          if (q_ok) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 a;
-            a.x = ptx::pack_bf16(__uint_as_float(v[8 * e + 0]) * scale, __uint_as_float(v[8 * e + 1]) * scale);
-            a.y = ptx::pack_bf16(__uint_as_float(v[8 * e + 2]) * scale, __uint_as_float(v[8 * e + 3]) * scale);
-            a.z = ptx::pack_bf16(__uint_as_float(v[8 * e + 4]) * scale, __uint_as_float(v[8 * e + 5]) * scale);
-            a.w = ptx::pack_bf16(__uint_as_float(v[8 * e + 6]) * scale, __uint_as_float(v[8 * e + 7]) * scale);
-            reinterpret_cast<uint4*>(row + c * 32)[e] = a;
+            for (int e = 0; e < 4; ++e) {
+              uint4 a;
+              a.x = ptx::pack_bf16(__uint_as_float(v[8 * e + 0]) * scale, __uint_as_float(v[8 * e + 1]) * scale);
+              a.y = ptx::pack_bf16(__uint_as_float(v[8 * e + 2]) * scale, __uint_as_float(v[8 * e + 3]) * scale);
+              a.z = ptx::pack_bf16(__uint_as_float(v[8 * e + 4]) * scale, __uint_as_float(v[8 * e + 5]) * scale);
+              a.w = ptx::pack_bf16(__uint_as_float(v[8 * e + 6]) * scale, __uint_as_float(v[8 * e + 7]) * scale);
+              reinterpret_cast<uint4*>(row + c * 32)[e] = a;
+            }
           }
         }
       }
+      // (the next unit's first dQ product, which overwrites the accumulator,
+      // waits for this group's first dS of that unit, issued after this)
       ptx::tc_fence_before();
+      item = i_next;
       ++u_it;
+      have = have_next;
+      bh = nbh;
+      qt = nqt;
+      split = nsplit;
+      j0 = nj0;
+      nk = nnk;
     }
   }
 
@@ -1265,7 +1285,6 @@ cudaError_t launch(const LaunchBwd& a) {
   P.p = p;
   P.NLSE2 = a.NLSE2;
   P.D = a.D;
-  P.O = static_cast<const __nv_bfloat16*>(a.O);
   P.LSE = a.LSE;
   P.Tq_pad = padded_rows(p.Tq);
   P.dQacc = a.dQacc;
@@ -1291,7 +1310,7 @@ cudaError_t launch(const LaunchBwd& a) {
     auto kern = split_dq ? dq_kernel<HD, HV, true> : dq_kernel<HD, HV, false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CQ::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<grid, DQ_THREADS, CQ::SMEM, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO, P);
+    kern<<<grid, DQ_THREADS, CQ::SMEM, a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmdO, *a.tmO, P);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (main_kv) {

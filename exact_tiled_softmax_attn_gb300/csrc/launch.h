@@ -39,6 +39,7 @@ struct LaunchBwd {
   const CUtensorMap* tmK;
   const CUtensorMap* tmV;
   const CUtensorMap* tmdO;
+  const CUtensorMap* tmO;   // forward output O (bf16 deterministic dQ kernel: D of its rows)
   const CUtensorMap* tmdQacc;  // fp32 dQ accumulator, 128 x 32 boxes (bf16 atomic path only)
   const void* Q;
   const void* K;
