@@ -556,6 +556,20 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
     a.tmV = &mv;
     a.tmdO = &mdo;
     a.tmO = &mo;
+    // the CTA-pair dQ kernel (d = 128, deterministic) loads halves of tiles
+    CUtensorMap mq64, mk64, mv64, mdo64, mo64;
+    if (deterministic && d == 128) {
+      if ((s = make_map(&mq64, Q, d, Tq, static_cast<int>(bh), false, 64)) != ATTN_OK) return s;
+      if ((s = make_map(&mk64, K, d, Tk, static_cast<int>(bh), false, 64)) != ATTN_OK) return s;
+      if ((s = make_map(&mv64, V, dv, Tk, static_cast<int>(bh), false, 64)) != ATTN_OK) return s;
+      if ((s = make_map(&mdo64, dO, dv, Tq, static_cast<int>(bh), false, 64)) != ATTN_OK) return s;
+      if ((s = make_map(&mo64, O, dv, Tq, static_cast<int>(bh), false, 64)) != ATTN_OK) return s;
+      a.tmQ64 = &mq64;
+      a.tmK64 = &mk64;
+      a.tmV64 = &mv64;
+      a.tmdO64 = &mdo64;
+      a.tmO64 = &mo64;
+    }
     a.tmdQacc = nullptr;
     if (a.dQacc) {
       if ((s = make_map(&mdq, a.dQacc, d, Tq, static_cast<int>(bh), true)) != ATTN_OK) return s;

@@ -40,6 +40,12 @@ struct LaunchBwd {
   const CUtensorMap* tmV;
   const CUtensorMap* tmdO;
   const CUtensorMap* tmO;   // forward output O (bf16 deterministic dQ kernel: D of its rows)
+  // 64-row boxes of Q, K, V, dO, O (bf16 deterministic dQ on CTA pairs, d = 128)
+  const CUtensorMap* tmQ64;
+  const CUtensorMap* tmK64;
+  const CUtensorMap* tmV64;
+  const CUtensorMap* tmdO64;
+  const CUtensorMap* tmO64;
   const CUtensorMap* tmdQacc;  // fp32 dQ accumulator, 128 x 32 boxes (bf16 atomic path only)
   const void* Q;
   const void* K;
