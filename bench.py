@@ -360,7 +360,7 @@ def run_ours(args, w):
     # backward launch groups in order: preprocess (atomic dQ only for bf16),
     # dQ kernel (deterministic only; it also forms D), dK/dV kernel, dQ
     # conversion (atomic only); none with --fwd-only
-    phases = () if args.fwd_only else (1, 5, 4, 3)
+    phases = () if args.fwd_only else (1, 6 if args.dq_pairs else 5, 4, 3)
 
     def step(ev=None):
         if ev is not None:
@@ -497,7 +497,8 @@ def run_ours(args, w):
         pass
     elif det:
         kernels[f"bwd dK/dV ({tag}dkdv_kernel)"] = {"ms": kv_ms, "flop": 2 * md + 2 * mv}
-        kernels[f"bwd dQ ({tag}dq_kernel)"] = {"ms": q_ms, "flop": md, "executed_flop": 2 * md + mv}
+        kernels[f"bwd dQ ({tag}{'dq_pair_kernel' if args.dq_pairs else 'dq_kernel'})"] = \
+            {"ms": q_ms, "flop": md, "executed_flop": 2 * md + mv}
     else:
         kernels[f"bwd dK/dV + dQ atomics ({tag}dkdv_kernel)"] = {"ms": kv_ms, "flop": 3 * md + 2 * mv}
     for k, v in kernels.items():
@@ -530,6 +531,7 @@ def run_ours(args, w):
     cfg.update({"pass": "forward only" if args.fwd_only else "forward + backward",
                 "dq_mode": None if args.fwd_only else ("deterministic" if det else "atomic"),
                 "fwd_splits": n_splits, "dq_splits": None if args.fwd_only else dq_splits,
+                "dq_on_cta_pairs": bool(args.dq_pairs),
                 "fwd_tflops": F / (fwd_ms * 1e-3) / 1e12,
                 "bwd_tflops": None if args.fwd_only else Bf / (bwd_ms * 1e-3) / 1e12,
                 "fwd_bwd_frac_of_peak": (F + Bf) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12 / peak,
@@ -575,6 +577,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="c3")
     ap.add_argument("--dq-mode", choices=["deterministic", "atomic"], default="deterministic",
                     help="dQ in a separate fixed-order pass (default) or by fp32 atomics inside the dK/dV kernel")
+    ap.add_argument("--dq-pairs", action="store_true",
+                    help="time the dQ pass on CTA pairs (attn_bwd_phase phase 6; bf16, d = 128, deterministic)")
     ap.add_argument("--splitkv", type=int, default=None,
                     help="run the forward through attn_fwd_splitkv with this many key splits (0 = automatic)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

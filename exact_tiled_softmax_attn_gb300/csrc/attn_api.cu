@@ -456,8 +456,10 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
   // than 64 and 128 run on zero-padded copies (one call: no phases)
   const bool padded = dtype == ATTN_BF16 && !bf16_bwd_shape(d, dv);
   if (padded && !bf16_bwd_padded(d, dv)) return ATTN_ERR_UNSUPPORTED;
-  if (phase < 0 || phase > 5) return ATTN_ERR_INVALID_ARG;
+  if (phase < 0 || phase > 6) return ATTN_ERR_INVALID_ARG;
   if (padded && phase != 0) return ATTN_ERR_UNSUPPORTED;
+  // phase 6, the dQ pass on CTA pairs, exists for bf16 with d = 128 and deterministic dQ
+  if (phase == 6 && (dtype != ATTN_BF16 || d != 128 || deterministic != 1)) return ATTN_ERR_UNSUPPORTED;
   if (deterministic != 0 && deterministic != 1) return ATTN_ERR_INVALID_ARG;
   const size_t es = elem_size(dtype);
   const size_t bh = static_cast<size_t>(B) * H;
@@ -556,9 +558,9 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
     a.tmV = &mv;
     a.tmdO = &mdo;
     a.tmO = &mo;
-    // the CTA-pair dQ kernel (d = 128, deterministic) loads halves of tiles
+    // the CTA-pair dQ kernel (phase 6) loads halves of tiles
     CUtensorMap mq64, mk64, mv64, mdo64, mo64;
-    if (deterministic && d == 128) {
+    if (phase == 6) {
       if ((s = make_map(&mq64, Q, d, Tq, static_cast<int>(bh), false, 64)) != ATTN_OK) return s;
       if ((s = make_map(&mk64, K, d, Tk, static_cast<int>(bh), false, 64)) != ATTN_OK) return s;
       if ((s = make_map(&mv64, V, dv, Tk, static_cast<int>(bh), false, 64)) != ATTN_OK) return s;

@@ -1193,12 +1193,6 @@ __global__ void convert_dq_kernel(const float4* __restrict__ acc, uint2* __restr
   }
 }
 
-// The CTA-pair dQ kernel (dq_pair.cu) halves each SM's K and V operand
-// traffic but adds a cross-SM handshake to every key step; measured at
-// B=2 H=16 T=8192 d=128 causal it takes 0.539 ms against 0.500 ms for the
-// one-CTA kernel below, which therefore runs.
-constexpr bool kDqOnPairs = false;
-
 template <int HD, int HV>
 cudaError_t launch(const LaunchBwd& a) {
   const Problem& p = a.p;
@@ -1208,6 +1202,11 @@ cudaError_t launch(const LaunchBwd& a) {
   const bool pre = atomic && (a.phase == 0 || a.phase == 1), conv = a.phase == 0 || a.phase == 3;
   const bool main_kv = a.phase == 0 || a.phase == 2 || a.phase == 4;
   const bool main_q = a.phase == 0 || a.phase == 2 || a.phase == 5;
+  // Phase 6: the dQ pass on CTA pairs (dq_pair.cu, d = 128), in place of
+  // phase 5. It halves each SM's K and V operand traffic but adds a cross-SM
+  // handshake to every key step; at B=2 H=16 T=8192 d=128 causal it measured
+  // 0.539 ms against 0.500 ms for the one-CTA kernel, which attn_bwd runs.
+  const bool pairs_q = a.phase == 6;
   cudaError_t e = cudaSuccess;
   if (pre) {
     e = launch_bwd_preprocess(p, a.O, a.dO, a.LSE, 2, a.D, a.NLSE2, atomic ? a.dQacc : nullptr, p.d, a.num_sms,
@@ -1233,8 +1232,8 @@ cudaError_t launch(const LaunchBwd& a) {
   P.dq_splits = split_dq ? a.dq_splits : 1;
   P.dq_split_tiles = split_dq ? a.dq_split_tiles : P.n_k_tiles;
   P.dQpart = a.dQpart;
-  if (!atomic && main_q && HD == 128 && kDqOnPairs) {
-    // d = 128: query tiles in pairs on CTA pairs (dq_pair.cu)
+  if (pairs_q) {
+    if (atomic || HD != 128) return cudaErrorInvalidValue;   // (the host checks this first)
     if ((e = launch_dq_pair(a, P)) != cudaSuccess) return e;
   } else if (!atomic && main_q) {
     P.order = Order{P.n_q_tiles * P.dq_splits, heads, p.causal ? 1 : 0};

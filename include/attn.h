@@ -209,9 +209,15 @@ ATTN_API attn_status_t attn_bwd(const void* Q, const void* K, const void* V, con
  *   4  the dK/dV kernel alone (with deterministic == 0 it also accumulates dQ)
  *   5  the separate dQ kernel alone (deterministic == 1; a no-op otherwise);
  *      for bf16 it also writes the D and -LSE * log2(e) phase 4 reads
- * Calling phases 1, 2, 3 (or 1, 5, 4, 3) in order on one stream equals one
- * attn_bwd call; phase 0 is attn_bwd itself. Other values give
- * ATTN_ERR_INVALID_ARG.
+ *   6  in place of phase 5, the same dQ pass on CTA pairs: two 128-row query
+ *      tiles per cluster of two CTAs, each tensor-core product computed for
+ *      both at once with the K and V operands split between the two SMs
+ *      (bf16, d = 128, deterministic == 1 only, else ATTN_ERR_UNSUPPORTED).
+ *      Same results within rounding; attn_bwd does not use it (on GB300 at
+ *      B=2 H=16 T=8192 it is slower than phase 5).
+ * Calling phases 1, 2, 3 (or 1, 5, 4, 3, or 1, 6, 4, 3) in order on one
+ * stream equals one attn_bwd call; phase 0 is attn_bwd itself. Other values
+ * give ATTN_ERR_INVALID_ARG.
  */
 ATTN_API attn_status_t attn_bwd_phase(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
                                       const void* dO, void* dQ, void* dK, void* dV, int B, int H, int Tq, int Tk,

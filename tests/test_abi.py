@@ -161,8 +161,13 @@ def test_backward_phase_range(lib):
     args = dict(Q=0x100000, K=0x200000, V=0x300000, O=0x400000, LSE=0x500000, dO=0x600000, dQ=0x700000,
                 dK=0x800000, dV=0x900000, B=1, H=1, Tq=8, Tk=8, d=64, dv=64, scale=0.125, causal=0,
                 dtype=B.ATTN_BF16, deterministic=0, workspace=0xA00000, workspace_bytes=1 << 20)
-    for ph in (-1, 6):
+    for ph in (-1, 7):
         assert B.attn_bwd_phase(**args, phase=ph, stream=0, check=False) == B.ATTN_ERR_INVALID_ARG
+    # phase 6 (the dQ pass on CTA pairs) takes bf16, d = 128, deterministic dQ only; refused on the host
+    assert B.attn_bwd_phase(**args, phase=6, stream=0, check=False) == B.ATTN_ERR_UNSUPPORTED
+    assert B.attn_bwd_phase(**dict(args, deterministic=1), phase=6, stream=0, check=False) == B.ATTN_ERR_UNSUPPORTED
+    assert B.attn_bwd_phase(**dict(args, d=128, dv=128, dtype=B.ATTN_F32, deterministic=1), phase=6, stream=0,
+                            check=False) == B.ATTN_ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -255,5 +260,5 @@ def test_padded_bf16_backward_workspace_and_phases(lib):
     args = dict(Q=0x100000, K=0x200000, V=0x300000, O=0x400000, LSE=0x500000, dO=0x600000, dQ=0x700000,
                 dK=0x800000, dV=0x900000, B=1, H=1, Tq=8, Tk=8, d=96, dv=96, scale=0.125, causal=0,
                 dtype=B.ATTN_BF16, deterministic=1, workspace=0xA00000, workspace_bytes=1 << 20)
-    for ph in (1, 2, 3, 4, 5):
+    for ph in (1, 2, 3, 4, 5, 6):
         assert B.attn_bwd_phase(**args, phase=ph, stream=0, check=False) == B.ATTN_ERR_UNSUPPORTED

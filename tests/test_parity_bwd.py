@@ -321,3 +321,68 @@ def test_phases_equal_one_call(dt, d, Tq, Tk, deterministic):
         assert torch.equal(dq0, dq1)
     else:
         check_grad(dq1, dq0, dt, "dQ")
+
+
+# ------------------------------------------------------------------ dQ on CTA pairs (phase 6)
+
+def _backward_by_phases(x, o, lse, causal, scale, phases, dv=None):
+    B, H, Tq, d = x["Q"].shape
+    Tk = x["K"].shape[2]
+    dv = x["V"].shape[3]
+    code = pkg.ATTN_BF16
+    ws = torch.empty(max(pkg.attn_bwd_workspace_size(B, H, Tq, Tk, d, dv, code, 1), 256), dtype=torch.uint8,
+                     device=DEV)
+    g = [torch.full_like(t, float("nan")) for t in (x["Q"], x["K"], x["V"])]
+    for ph in phases:
+        pkg.attn_bwd_phase(x["Q"], x["K"], x["V"], o, lse, x["dO"], g[0], g[1], g[2], B, H, Tq, Tk, d, dv, scale,
+                           causal, code, 1, ws, ws.numel(), ph)
+    torch.cuda.synchronize()
+    return g
+
+
+PAIR_SHAPES = [  # B, H, Tq, Tk, dv: odd query-tile counts leave the last pair's second CTA without rows
+    (1, 2, 300, 300, 128),
+    (2, 1, 640, 640, 128),
+    (1, 3, 129, 513, 128),
+    (1, 1, 1000, 200, 64),
+    (1, 2, 128, 4096, 128),   # few query tiles: split dQ (partials added in split order)
+    (1, 1, 384, 1000, 64),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", PAIR_SHAPES)
+def test_bf16_dq_on_cta_pairs(shape, causal):
+    """Phases 1, 6, 4, 3 (the dQ pass on CTA pairs) against the oracle; dK and
+    dV bitwise those of attn_bwd (the same dK/dV kernel on the same D)."""
+    B, H, Tq, Tk, dv = shape
+    d = 128
+    x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, dv), seed=Tq + 3 * Tk + dv, dtype=torch.bfloat16,
+                    device=DEV)
+    scale = 1 / math.sqrt(d)
+    o, lse = pkg.forward(x["Q"], x["K"], x["V"], causal=causal, scale=scale)
+    dq, dk, dvv = _backward_by_phases(x, o, lse, causal, scale, (1, 6, 4, 3))
+    r = ref.backward(x["Q"], x["K"], x["V"], x["dO"], scale, causal)
+    check_grad(dq, r["dQ"], torch.bfloat16, "dQ")
+    check_grad(dk, r["dK"], torch.bfloat16, "dK")
+    check_grad(dvv, r["dV"], torch.bfloat16, "dV")
+    dq1, dk1, dv1 = _backward_by_phases(x, o, lse, causal, scale, (1, 5, 4, 3))
+    assert torch.equal(dk, dk1) and torch.equal(dvv, dv1)
+    check_grad(dq, dq1.double().cpu().numpy(), torch.bfloat16, "dQ vs the one-CTA pass")
+    # fixed key order: the same bits on every run
+    dq2, _, _ = _backward_by_phases(x, o, lse, causal, scale, (1, 6, 4, 3))
+    assert torch.equal(dq, dq2)
+
+
+@pytest.mark.parametrize("dt,d,det", [(torch.bfloat16, 64, 1), (torch.float32, 128, 1), (torch.bfloat16, 128, 0)])
+def test_dq_on_cta_pairs_outside_its_domain_is_refused(dt, d, det):
+    B, H, T = 1, 1, 256
+    x = make_random((B, H, T, d), (B, H, T, d), (B, H, T, d), seed=3, dtype=dt, device=DEV)
+    code = pkg.ATTN_BF16 if dt == torch.bfloat16 else pkg.ATTN_F32
+    o, lse = pkg.forward(x["Q"], x["K"], x["V"], causal=True, scale=0.1)
+    ws = torch.empty(max(pkg.attn_bwd_workspace_size(B, H, T, T, d, d, code, det), 256), dtype=torch.uint8,
+                     device=DEV)
+    g = [torch.empty_like(t) for t in (x["Q"], x["K"], x["V"])]
+    st = pkg.attn_bwd_phase(x["Q"], x["K"], x["V"], o, lse, x["dO"], g[0], g[1], g[2], B, H, T, T, d, d, 0.1, True,
+                            code, det, ws, ws.numel(), 6, check=False)
+    assert st == pkg.ATTN_ERR_UNSUPPORTED
