@@ -36,9 +36,12 @@ L2_FLUSH_BYTES = 256 << 20
 # figure counts only while these hash as they did when it was captured)
 KERNEL_SOURCES = {
     "attn_fwd_bf16_kernel": ("fwd_bf16.cu", "ptx.cuh", "common.cuh", "launch.h"),
-    "dkdv_kernel": ("bwd_bf16.cu", "ptx.cuh", "common.cuh", "launch.h"),
-    "dq_kernel": ("bwd_bf16.cu", "ptx.cuh", "common.cuh", "launch.h"),
+    "dkdv_kernel": ("bwd_bf16.cu", "bwd_common.cuh", "ptx.cuh", "common.cuh", "launch.h"),
+    "dq_kernel": ("bwd_bf16.cu", "bwd_common.cuh", "ptx.cuh", "common.cuh", "launch.h"),
     "attn_fwd_d256_kernel": ("fwd_bf16_d256.cu", "ptx.cuh", "common.cuh", "launch.h"),
+    "dq_pair_kernel": ("dq_pair.cu", "bwd_common.cuh", "ptx.cuh", "common.cuh", "launch.h"),
+    "kv256_kernel, 2 launches": ("bwd_d256.cu", "bwd_common.cuh", "ptx.cuh", "common.cuh", "launch.h"),
+    "q256_kernel": ("bwd_d256.cu", "bwd_common.cuh", "ptx.cuh", "common.cuh", "launch.h"),
 }
 
 
@@ -495,6 +498,11 @@ def run_ours(args, w):
     kernels = {fwd_name: {"ms": fwd_ms, "flop": F}}
     if args.fwd_only:
         pass
+    elif w.d > 128:
+        # rows of 256 columns: a dV kernel (S^T, dV) and a dK kernel (S^T, dP^T, dK), then a dQ kernel
+        kernels["bwd dV + dK (kv256_kernel, 2 launches)"] = {"ms": kv_ms, "flop": 2 * md + 2 * mv,
+                                                              "executed_flop": 3 * md + 2 * mv}
+        kernels["bwd dQ (q256_kernel)"] = {"ms": q_ms, "flop": md, "executed_flop": 2 * md + mv}
     elif det:
         kernels[f"bwd dK/dV ({tag}dkdv_kernel)"] = {"ms": kv_ms, "flop": 2 * md + 2 * mv}
         kernels[f"bwd dQ ({tag}{'dq_pair_kernel' if args.dq_pairs else 'dq_kernel'})"] = \
@@ -512,12 +520,12 @@ def run_ours(args, w):
             # reads O, dO, LSE; writes D and LSE*log2(e) (padded rows) and zeroes the dQ accumulator
             # atomic dQ only (bf16): the deterministic dQ kernel forms D itself
             "bwd preprocess": {"ms": pre_ms,
-                               "gbs": B * H * Tq * (2 * dv * es + 4 + 8 + (0 if det else d * 4)) / (pre_ms * 1e-3) / 1e9
-                               if (f32 or not det) else None},
+                               "gbs": B * H * Tq * (2 * dv * es + 4 + 8 + (0 if (det or w.d > 128) else d * 4)) /
+                               (pre_ms * 1e-3) / 1e9 if (f32 or not det or w.d > 128) else None},
             # atomic: fp32 accumulator -> bf16; deterministic with split dQ: the partials' sum -> bf16
             "dQ convert": {"ms": conv_ms,
                            "gbs": B * H * Tq * d * (4 * (1 if not det else dq_splits) + 2) / (conv_ms * 1e-3) / 1e9
-                           if not f32 and (not det or dq_splits > 1) else None},
+                           if not f32 and w.d <= 128 and (not det or dq_splits > 1) else None},
         })
         kernels["bwd main (all main kernels)"]["frac_of_peak"] = \
             kernels["bwd main (all main kernels)"]["tflops"] / peak
@@ -558,6 +566,8 @@ def run_ours(args, w):
         # dK/dV, convert; fp32: fwd, preprocess, dK/dV, dQ | fwd, preprocess, dK/dV
         "gpu_launches": args.steps * ((1 + (1 if n_splits > 1 else 0)) if args.fwd_only else
                                       (4 if det else 3) if f32 else
+                                      # d = 256: forward, preprocess, dQ, dV, dK kernels
+                                      (5 + (1 if n_splits > 1 else 0)) if w.d > 128 else
                                       ((3 if det else 4) + (1 if n_splits > 1 else 0) +
                                        (1 if det and dq_splits > 1 else 0))),
         "clocks": clk,
@@ -583,7 +593,7 @@ def main(argv=None):
                     help="run the forward through attn_fwd_splitkv with this many key splits (0 = automatic)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fwd-only", action="store_true",
-                    help="time the forward alone (its FLOPs only); the only pass for bf16 d = 256")
+                    help="time the forward alone (its FLOPs only)")
     ap.add_argument("--dry-run", action="store_true",
                     help="print each rank's launch plan (rank, world, device, input seed) and exit")
     argv = sys.argv[1:] if argv is None else list(argv)

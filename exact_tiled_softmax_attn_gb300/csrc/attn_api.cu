@@ -113,9 +113,14 @@ Range range(const void* p, size_t bytes) {
 // kernels run on the next tile width up (64, 128 or 256 columns), the tensor
 // maps read the missing columns of Q, K and V as zeros, which leave S and the
 // first dv columns of O unchanged, and the epilogues write dv columns. The
-// backward takes d, dv in {64, 128}.
+// backward kernels take d, dv in {64, 128}, or d = 256 with dv in {64, 128,
+// 256}; other widths run on zero-padded copies (bf16_bwd_padded).
 bool bf16_fwd_shape(int d, int dv) { return d % 8 == 0 && dv % 8 == 0 && d <= 256 && dv <= 256; }
-bool bf16_bwd_shape(int d, int dv) { return (d == 64 || d == 128) && (dv == 64 || dv == 128); }
+bool bf16_bwd_shape(int d, int dv) {
+  return ((d == 64 || d == 128) && (dv == 64 || dv == 128)) || (d == 256 && (dv == 64 || dv == 128 || dv == 256));
+}
+// the d = 256 backward (bwd_d256.cu): no fp32 dQ accumulator, no dQ splits
+bool bf16_bwd_wide(int d) { return d > 128; }
 // rows wider than 128 columns go to the d = 256 forward kernel
 bool bf16_wide(int d, int dv) { return d > 128 || dv > 128; }
 
@@ -187,17 +192,23 @@ BwdLayout bwd_layout(int B, int H, int Tq, int Tk, int d, attn_dtype_t dt, int d
   L.acc_off = 2 * part;
   const size_t acc = static_cast<size_t>(B) * H * Tq * d * sizeof(float);
   L.acc_bytes = (dt == ATTN_BF16 && !deterministic) ? acc : (L.dq_splits > 1 ? L.dq_splits * acc : 0);
+  if (dt == ATTN_BF16 && bf16_bwd_wide(d)) {
+    // the d = 256 kernels write dQ in one fixed-order pass whatever `deterministic` says
+    L.acc_bytes = 0;
+    L.dq_splits = 1;
+    L.dq_split_tiles = (Tk + 127) / 128;
+  }
   L.total = rows_pad ? L.acc_off + L.acc_bytes : 0;
   return L;
 }
 
-// bf16 backward at widths other than 64 and 128 (multiples of 8 up to 128):
-// Q, K, V, O and dO are copied into rows of the next tile width dp, dvp with
+// bf16 backward at other widths (multiples of 8 up to 256): Q, K, V, O and
+// dO are copied into rows of the next width dp, dvp the kernels take, with
 // zero columns, the backward runs on those copies, and the first d / dv
 // columns of its gradients are copied out. The zero columns add nothing to
 // S = QK^T, dP = dO V^T or D = rowsum(dO o O), so P and dS are those of the
 // unpadded problem and the gradients' first columns are its gradients.
-bool bf16_bwd_padded(int d, int dv) { return !bf16_bwd_shape(d, dv) && d <= 128 && dv <= 128; }
+bool bf16_bwd_padded(int d, int dv) { return !bf16_bwd_shape(d, dv) && bf16_fwd_shape(d, dv); }
 
 struct PadLayout {
   int dp, dvp;
@@ -208,8 +219,10 @@ struct PadLayout {
 // workspace of the backward at (dp, dvp).
 PadLayout pad_layout(int B, int H, int Tq, int Tk, int d, int dv, int deterministic) {
   PadLayout L{};
-  L.dp = d <= 64 ? 64 : 128;
-  L.dvp = dv <= 64 ? 64 : 128;
+  // rows wider than 128 columns on either side run on the d = 256 kernels
+  const bool wide = d > 128 || dv > 128;
+  L.dp = wide ? 256 : (d <= 64 ? 64 : 128);
+  L.dvp = dv <= 64 ? 64 : (dv <= 128 ? 128 : 256);
   const size_t bh = static_cast<size_t>(B) * H;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -451,9 +464,9 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
                        int phase, void* stream) {
   attn_status_t s = check_common(B, H, Tq, Tk, d, dv, scale, causal, dtype);
   if (s != ATTN_OK) return s;
-  // the tensor-core backward keeps dV and dK accumulators of d and dv columns
-  // next to two 128-column score buffers in TMEM: d, dv <= 128; widths other
-  // than 64 and 128 run on zero-padded copies (one call: no phases)
+  // the tensor-core backward kernels take d, dv in {64, 128} and d = 256 with
+  // dv in {64, 128, 256}; other widths run on zero-padded copies (one call:
+  // no phases)
   const bool padded = dtype == ATTN_BF16 && !bf16_bwd_shape(d, dv);
   if (padded && !bf16_bwd_padded(d, dv)) return ATTN_ERR_UNSUPPORTED;
   if (phase < 0 || phase > 6) return ATTN_ERR_INVALID_ARG;
@@ -558,9 +571,9 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
     a.tmV = &mv;
     a.tmdO = &mdo;
     a.tmO = &mo;
-    // the CTA-pair dQ kernel (phase 6) loads halves of tiles
+    // the CTA-pair dQ kernel (phase 6) and the d = 256 kernels load 64-row halves of tiles
     CUtensorMap mq64, mk64, mv64, mdo64, mo64;
-    if (phase == 6) {
+    if (phase == 6 || bf16_bwd_wide(d)) {
       if ((s = make_map(&mq64, Q, d, Tq, static_cast<int>(bh), false, 64)) != ATTN_OK) return s;
       if ((s = make_map(&mk64, K, d, Tk, static_cast<int>(bh), false, 64)) != ATTN_OK) return s;
       if ((s = make_map(&mv64, V, dv, Tk, static_cast<int>(bh), false, 64)) != ATTN_OK) return s;
@@ -577,7 +590,7 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
       if ((s = make_map(&mdq, a.dQacc, d, Tq, static_cast<int>(bh), true)) != ATTN_OK) return s;
       a.tmdQacc = &mdq;
     }
-    e = launch_bwd_bf16(a);
+    e = bf16_bwd_wide(d) ? launch_bwd_bf16_d256(a) : launch_bwd_bf16(a);
   }
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }

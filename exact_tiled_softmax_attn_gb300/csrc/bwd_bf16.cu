@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   auto lpar = [](uint32_t n) { return (n / C::NL) & 1u; };
 
   const int grid = gridDim.x, cta = blockIdx.x;
-  const int Tq = P.p.Tq, Tk = P.p.Tk;
+  const int Tk = P.p.Tk;
   const int wg = warp >> 2;
 
   if (wg == 0) {

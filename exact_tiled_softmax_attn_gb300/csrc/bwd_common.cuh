@@ -83,6 +83,13 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int col) {
          (col & 7) * 2;
 }
 
+// Byte offset of element (row, col) of a 64-row tile stored as 64-column
+// boxes with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw128_offset64(int row, int col) {
+  return (col >> 6) * (64 * 64 * 2) + (row >> 3) * 1024 + (row & 7) * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) +
+         (col & 7) * 2;
+}
+
 // TMEM column of k-step kk (16 query columns, 8 packed columns) of the bf16
 // P^T / dS^T operand: query columns 64h.. are packed at column 64h, where the
 // half-h group read its fp32 scores, so no group overwrites columns the other

@@ -76,13 +76,6 @@ struct CfgP {
   static_assert(NSLOT <= 32, "per-slot phase bits");
 };
 
-// Byte offset of element (row, col) of a 64-row half tile stored as 64-column
-// boxes with the 128-byte swizzle.
-__device__ __forceinline__ uint32_t sw128_offset64(int row, int col) {
-  return (col >> 6) * (64 * 64 * 2) + (row >> 3) * 1024 + (row & 7) * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) +
-         (col & 7) * 2;
-}
-
 // Pair unit `blk` of a head: query tiles 2 pq and 2 pq + 1, key split s, first
 // key tile j0 and key tile count nk (the larger of the two tiles' counts: the
 // first tile's rows mask the key tile it cannot see).

@@ -84,6 +84,10 @@ cudaError_t launch_fwd_bf16(const LaunchFwd& a);
 // tiles; tmK must be built with 128-row boxes and tmV with 64-row boxes
 cudaError_t launch_fwd_bf16_d256(const LaunchFwd& a);
 cudaError_t launch_bwd_bf16(const LaunchBwd& a);
+// d = 256 (dv 64, 128 or 256): preprocess, then a dQ kernel and a dV and a dK
+// kernel; needs the 64-row maps tmQ64, tmK64, tmV64, tmdO64 and the 128-row
+// tmV, tmdO
+cudaError_t launch_bwd_bf16_d256(const LaunchBwd& a);
 
 // O, LSE from the split-KV partials (rows of query tile qt read the splits
 // that hold at least one of its key tiles)

@@ -100,7 +100,7 @@ WORKLOADS: Dict[str, Workload] = {
     "s1": Workload("s1", 1, 8, 256, 65536, 128, 128, "bf16", False, 5),
     # V with its own head dimension (d = 64, dv = 128)
     "m1": Workload("m1", 2, 16, 4096, 4096, 64, 128, "bf16", True, 6),
-    # head size 256 (forward only on the tensor cores)
+    # head size 256 (forward and backward on the tensor cores)
     "w256": Workload("w256", 2, 16, 4096, 4096, 256, 256, "bf16", True, 7),
 }
 

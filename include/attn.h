@@ -42,11 +42,12 @@
  *              with its own head dimension); a width below 64, 128 or 256
  *              runs on the next of those tile widths with zero columns, so
  *              64, 128 and 256 are the efficient sizes. Backward (attn_bwd):
- *              d and dv multiples of 8 up to 128; widths other than 64 and
- *              128 run on zero-padded copies of the inputs held in the
- *              workspace (attn_bwd_phase takes only 64 and 128); wider bf16
- *              rows return ATTN_ERR_UNSUPPORTED (ATTN_F32 covers them). Any
- *              B, H, Tq, Tk >= 0.
+ *              d and dv multiples of 8 up to 256, independently. The
+ *              kernels take d, dv in {64, 128}, and d = 256 with dv in {64,
+ *              128, 256}; other widths run on zero-padded copies of the
+ *              inputs held in the workspace (rows wider than 128 on either
+ *              side pad d to 256), and attn_bwd_phase takes only the
+ *              kernels' own widths. Any B, H, Tq, Tk >= 0.
  * Zero-sized problems are valid: Tk == 0 gives O = 0 and LSE = -inf (a row
  * with no allowed key), and empty gradients are written as zeros.
  */
@@ -148,13 +149,13 @@ ATTN_API size_t attn_fwd_splitkv_workspace_size(int B, int H, int Tq, int Tk, in
 /*
  * Bytes of device workspace attn_bwd needs for this problem (0 is possible).
  * Holds -LSE * log2(e) and D = rowsum(dO o O), each [B*H, Tq_pad] fp32 with
- * Tq_pad = Tq rounded up to a multiple of 128, and, for bf16 with
- * deterministic == 0, the fp32 dQ accumulator [B,H,Tq,d], or, for bf16 with
+ * Tq_pad = Tq rounded up to a multiple of 128, and, for bf16 with d <= 128
+ * and deterministic == 0, the fp32 dQ accumulator [B,H,Tq,d], or, for bf16 with
  * deterministic == 1 and S = attn_bwd_dq_splits(...) > 1, S fp32 partial dQ
  * arrays [S][B,H,Tq,d]; each part starts on a 256-byte boundary. For bf16
  * widths other than 64 and 128 it first holds zero-padded bf16 copies of Q,
- * K, V, O, dO and of the three gradients, in rows of the next tile width (64
- * or 128 columns), then the workspace above for the padded widths; the
+ * K, V, O, dO and of the three gradients, in rows of the next tile width (64,
+ * 128 or 256 columns), then the workspace above for the padded widths; the
  * padded problem's dQ splits are the ones attn_bwd_dq_splits reports.
  * Returns 0 for invalid arguments as well.
  */
@@ -186,7 +187,10 @@ ATTN_API int attn_bwd_dq_splits(int B, int H, int Tq, int Tk, int d, int dv, att
  * Q and K"). `O` and `LSE` must be the outputs of attn_fwd on the same
  * inputs, scale and mask. deterministic = 1 computes dQ in a separate pass
  * that sums key tiles in a fixed order (bitwise reproducible); 0 adds each
- * key tile's share with fp32 atomics. `workspace` (256-byte aligned, at least
+ * key tile's share with fp32 atomics. For bf16 rows of 256 columns both
+ * values run the fixed-order pass: there a dQ kernel, a dV kernel and a dK
+ * kernel each hold one 256-column accumulator (tensor memory has room for
+ * one next to the score tiles), all bitwise reproducible. `workspace` (256-byte aligned, at least
  * attn_bwd_workspace_size bytes; may be NULL when that is 0) is scratch
  * owned by the caller and overwritten.
  * Errors: as attn_fwd, plus ATTN_ERR_WORKSPACE.

@@ -149,9 +149,9 @@ def _bwd(**kw):
     (dict(dQ=0x600000), B.ATTN_ERR_INVALID_ARG),          # output overlaps dO
     (dict(dO=None), B.ATTN_ERR_INVALID_ARG),
     (dict(dV=0x900008), B.ATTN_ERR_MISALIGNED),
-    (dict(d=136, dv=64), B.ATTN_ERR_UNSUPPORTED),    # the bf16 backward takes d, dv <= 128
+    (dict(d=264, dv=64), B.ATTN_ERR_UNSUPPORTED),    # the bf16 backward takes d, dv <= 256
     (dict(d=100, dv=64), B.ATTN_ERR_UNSUPPORTED),    # a multiple of 8
-    (dict(d=256, dv=256), B.ATTN_ERR_UNSUPPORTED),   # the d = 256 tensor-core path is forward only
+    (dict(d=256, dv=264), B.ATTN_ERR_UNSUPPORTED),
 ])
 def test_backward_host_validation(lib, kw, status):
     assert _bwd(**kw) == status
@@ -194,9 +194,31 @@ def test_error_text_carries_status(lib):
     assert "unsupported" in str(e.value)
 
 
-def test_d256_bf16_is_forward_only(lib):
-    assert B.attn_bwd_workspace_size(1, 1, 128, 128, 256, 256, B.ATTN_BF16, 1) == 0
-    assert B.attn_bwd_dq_splits(1, 1, 128, 128, 256, 256, B.ATTN_BF16, 1) == -1
+def test_d256_bf16_backward_workspace_and_splits(lib):
+    """d = 256: the workspace holds -LSE*log2(e) and D only (dQ is written in
+    one fixed-order pass for either value of `deterministic`, no splits); other
+    widths above 128 pad to 256 columns (and dv to 64, 128 or 256)."""
+    r256 = lambda x: (x + 255) // 256 * 256
+    B_, H, Tq, Tk = 2, 3, 300, 500
+    rows_pad = B_ * H * 384
+    for det in (0, 1):
+        for dv in (64, 128, 256):
+            assert B.attn_bwd_workspace_size(B_, H, Tq, Tk, 256, dv, B.ATTN_BF16, det) == 2 * r256(rows_pad * 4)
+            assert B.attn_bwd_dq_splits(B_, H, 128, 65536, 256, dv, B.ATTN_BF16, det) == 1
+        # d = 200, dv = 136: copies padded to 256 and 256 columns, then the d = 256 workspace
+        bh = B_ * H
+        pads = [bh * Tq * 256, bh * Tk * 256, bh * Tk * 256, bh * Tq * 256, bh * Tq * 256, bh * Tq * 256,
+                bh * Tk * 256, bh * Tk * 256]
+        assert B.attn_bwd_workspace_size(B_, H, Tq, Tk, 200, 136, B.ATTN_BF16, det) == \
+            sum(r256(2 * n) for n in pads) + 2 * r256(rows_pad * 4)
+        # d = 64, dv = 200: the value rows are wider than 128, so d pads to 256 as well
+        pads = [bh * Tq * 256, bh * Tk * 256, bh * Tk * 256, bh * Tq * 256, bh * Tq * 256, bh * Tq * 256,
+                bh * Tk * 256, bh * Tk * 256]
+        assert B.attn_bwd_workspace_size(B_, H, Tq, Tk, 64, 200, B.ATTN_BF16, det) == \
+            sum(r256(2 * n) for n in pads) + 2 * r256(rows_pad * 4)
+
+
+def test_d256_bf16_forward_splits(lib):
     # the forward splits at d = 256 as at d <= 128: 64 key tiles in 8 ranges of 8
     assert B.attn_fwd_splitkv_splits(1, 1, 128, 8192, 256, 256, B.ATTN_BF16, 8) == 8
     assert B.attn_fwd_splitkv_splits(1, 1, 128, 8192, 256, 64, B.ATTN_BF16, 100) == 64

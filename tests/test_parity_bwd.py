@@ -386,3 +386,55 @@ def test_dq_on_cta_pairs_outside_its_domain_is_refused(dt, d, det):
     st = pkg.attn_bwd_phase(x["Q"], x["K"], x["V"], o, lse, x["dO"], g[0], g[1], g[2], B, H, T, T, d, d, 0.1, True,
                             code, det, ws, ws.numel(), 6, check=False)
     assert st == pkg.ATTN_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------------ bf16 rows of 256 columns
+
+D256_SHAPES = [  # B, H, Tq, Tk, d, dv (64-row steps with ragged tails; Tq != Tk both ways)
+    (1, 2, 300, 300, 256, 256),
+    (2, 1, 129, 700, 256, 128),
+    (1, 1, 700, 129, 256, 64),
+    (1, 3, 64, 64, 256, 256),
+    (1, 1, 513, 1000, 256, 256),
+    (1, 2, 200, 300, 200, 136),   # padded to 256 / 256
+    (1, 1, 130, 250, 64, 200),    # value rows above 128: both pad to 256
+    (1, 1, 190, 190, 248, 24),    # padded to 256 / 64
+]
+
+
+@pytest.mark.parametrize("deterministic", [0, 1])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", D256_SHAPES)
+def test_bf16_d256_backward(shape, causal, deterministic):
+    B, H, Tq, Tk, d, dv = shape
+    x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, dv), seed=Tq + Tk + d + dv, dtype=torch.bfloat16,
+                    device=DEV)
+    check_all(x, causal, 1 / math.sqrt(d), torch.bfloat16, deterministic)
+
+
+def test_bf16_d256_large_logits_across_tiles():
+    B, H, T, d = 1, 1, 520, 256
+    x = make_random((B, H, T, d), (B, H, T, d), (B, H, T, d), seed=19, device="cpu")
+    sign = torch.where((torch.arange(T) // 128) % 2 == 0, 20.0, -20.0).view(1, 1, T, 1)
+    x = {k: (v * sign if k == "K" else v).to(torch.bfloat16).to(DEV) for k, v in x.items()}
+    for causal in (False, True):
+        check_all(x, causal, 1.0 / math.sqrt(d), torch.bfloat16, 1)
+
+
+def test_bf16_d256_bitwise_repeatable_and_flag_independent():
+    """Every d = 256 accumulation runs in a fixed order: the same bits on
+    every call, whichever value `deterministic` has."""
+    B, H, T, d = 1, 2, 400, 256
+    x = make_random((B, H, T, d), (B, H, T, d), (B, H, T, d), seed=23, dtype=torch.bfloat16, device=DEV)
+    a = run(x, True, 0.0625, 1)
+    b = run(x, True, 0.0625, 1)
+    c = run(x, True, 0.0625, 0)
+    for u, v, w in zip(a[2:], b[2:], c[2:]):
+        assert torch.equal(u, v) and torch.equal(u, w)
+
+
+@pytest.mark.parametrize("deterministic", [1])
+def test_bf16_w256_full_size_sampled_heads(deterministic):
+    w = WORKLOADS["w256"]
+    check_all(make_inputs(w, DEV), w.causal, w.softmax_scale, torch.bfloat16, deterministic,
+              heads=[(0, 0), (1, 15)])
