@@ -25,6 +25,7 @@ struct DeviceInfo {
   std::once_flag once;
   cudaError_t err = cudaSuccess;
   int num_sms = 0;
+  int l2_bytes = 0;
   uint32_t* status = nullptr;
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -51,6 +52,7 @@ attn_status_t device_info(DeviceInfo** out) {
   DeviceInfo& di = g_dev[dev];
   std::call_once(di.once, [&] {
     di.err = cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (di.err == cudaSuccess) di.err = cudaDeviceGetAttribute(&di.l2_bytes, cudaDevAttrL2CacheSize, dev);
     if (di.err == cudaSuccess) di.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&di.status), g_device_status);
   });
   if (di.err != cudaSuccess) return cuda_fail(di.err);
@@ -151,7 +153,7 @@ attn_status_t check_ptr(const void* p, size_t bytes, size_t align) {
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct BwdLayout {
-  size_t lse2_off, d_off, acc_off, acc_bytes, total;
+  size_t lse2_off, d_off, acc_off, acc_bytes, sched_off, total;
   int dq_splits, dq_split_tiles;   // split deterministic dQ (bf16): acc holds the partials
 };
 // The deterministic bf16 dQ kernel runs one unit per 128-row query tile; when
@@ -181,7 +183,8 @@ void dq_split_count(int B, int H, int Tq, int Tk, attn_dtype_t dt, int determini
 
 // Workspace: NLSE2 [B*H, Tq_pad] fp32 | D [B*H, Tq_pad] fp32 | (bf16 with fp32
 // dQ accumulation) dQacc [B*H*Tq, d] fp32, or (bf16 deterministic with split
-// dQ) the partials [S][B*H*Tq, d] fp32; each part 256-byte aligned.
+// dQ) the partials [S][B*H*Tq, d] fp32 | (bf16, d <= 128) 256 bytes for the
+// two unit counters of the dQ and dK/dV kernels; each part 256-byte aligned.
 BwdLayout bwd_layout(int B, int H, int Tq, int Tk, int d, attn_dtype_t dt, int deterministic) {
   BwdLayout L{};
   const size_t rows_pad = static_cast<size_t>(B) * H * padded_rows(Tq);
@@ -198,7 +201,9 @@ BwdLayout bwd_layout(int B, int H, int Tq, int Tk, int d, attn_dtype_t dt, int d
     L.dq_splits = 1;
     L.dq_split_tiles = (Tk + 127) / 128;
   }
-  L.total = rows_pad ? L.acc_off + L.acc_bytes : 0;
+  L.sched_off = round_up(L.acc_off + L.acc_bytes, 256);
+  const size_t sched = (dt == ATTN_BF16 && !bf16_bwd_wide(d)) ? 256 : 0;
+  L.total = rows_pad ? L.sched_off + sched : 0;
   return L;
 }
 
@@ -553,6 +558,10 @@ attn_status_t bwd_impl(const void* Q, const void* K, const void* V, const void* 
   a.dq_split_tiles = L.dq_split_tiles;
   a.dQpart = L.dq_splits > 1 ? acc : nullptr;
   a.deterministic = deterministic;
+  a.sched = dtype == ATTN_BF16 && !bf16_bwd_wide(d)
+                ? reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + L.sched_off)
+                : nullptr;
+  a.l2_bytes = static_cast<size_t>(di->l2_bytes);
   a.phase = phase;
   a.status = di->status;
   a.num_sms = di->num_sms;

@@ -102,9 +102,11 @@ struct CfgKV {
   // kv_full, kv_empty, q_full[NQ], q_empty[NQ], o_full[NO], o_empty[NO], l_full[NL], l_empty[NL],
   // s_full, dp_full, p_full, ds_full, dq_full, dq_free, acc_full, dv_free, stage_full, stage_free,
   // sds_free, drain, dk_free
-  static constexpr int NBAR = 2 + 2 * NQ + 2 * NO + 2 * NL + 13;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_MISC + 16;
+  // ..., unit queue full[4], empty[4]
+  static constexpr int NBAR = 2 + 2 * NQ + 2 * NO + 2 * NL + 13 + 2 * UnitQueue::N;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // TMEM address, abort word, unit queue slots
+  static constexpr int SMEM = OFF_MISC + 16 + 4 * UnitQueue::N;
+  static constexpr int UQ_READERS = 1 + 256 + 128;   // the MMA warp (once), every P/dS and epilogue thread
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16(BT, BT, false, false);
   static constexpr uint32_t IDESC_DV = ptx::idesc_bf16(BT, HV, false, true);    // dV (A in TMEM)
   static constexpr uint32_t IDESC_DK = ptx::idesc_bf16(BT, HD, false, true);    // dK (A in TMEM)
@@ -112,7 +114,9 @@ struct CfgKV {
 };
 
 
-template <int HD, int HV, bool ATOMIC_DQ>
+// DYN: units claimed at run time through the unit queue (see UnitQueue);
+// otherwise the static order, with no queue code compiled in.
+template <int HD, int HV, bool ATOMIC_DQ, bool DYN>
 __global__ void __launch_bounds__(KV_THREADS, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -156,8 +160,14 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   uint64_t* drain = s_full + 11;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
+  const UnitQueue uq{reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16), s_full + 13,
+                     s_full + 13 + UnitQueue::N};
 
   if (threadIdx.x == 0) {
+    for (int s = 0; s < UnitQueue::N; ++s) {
+      ptx::mbar_init(uq.full + s, 1);
+      ptx::mbar_init(uq.empty + s, C::UQ_READERS);
+    }
     ptx::mbar_init(kv_full, 1);
     ptx::mbar_init(kv_empty, 1);
     for (int s = 0; s < C::NQ; ++s) {
@@ -205,9 +215,13 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   auto lslot = [](uint32_t n) { return static_cast<int>(n % C::NL); };
   auto lpar = [](uint32_t n) { return (n / C::NL) & 1u; };
 
-  const int grid = gridDim.x, cta = blockIdx.x;
   const int Tk = P.p.Tk;
   const int wg = warp >> 2;
+  // the launch's units: 128-key tiles of every head, handed out at run time
+  // in head groups, the longest (causal: first) key tiles first
+  const int nb = P.n_k_tiles, nh = P.p.B * P.p.H, total = nb * nh;
+  const int cta = blockIdx.x, grid = gridDim.x;
+  auto decode = [&](int x, int* bh, int* kb) { grouped_unit(x, nb, nh, P.group, false, bh, kb); };
 
   if (wg == 0) {
     ptx::reg_release<KvRegs<ATOMIC_DQ>::CTRL>();
@@ -218,10 +232,24 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       ptx::tma_prefetch_desc(&tmK);
       ptx::tma_prefetch_desc(&tmV);
       ptx::tma_prefetch_desc(&tmdO);
-      uint32_t u_it = 0, q_it = 0, q_issued = 0, o_issued = 0, l_issued = 0;
+      uint32_t u_it = 0, q_it = 0, q_issued = 0, o_issued = 0, l_issued = 0, pu = 0;
+      int bh = 0, kb = 0;
+      // take the next unit and publish it (the one after it before this
+      // one's tiles load)
+      int x = DYN ? next_unit_index(P, pu, cta, grid, total) : 0;
       bool ok = true;
-      int bh, kb;
-      for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &kb); ++round) {
+      if constexpr (DYN) ok = uq_push(uq, pu, x, w);
+      ++pu;
+      while (ok && x < total) {
+        if constexpr (DYN) {
+          const int xn = next_unit_index(P, pu, cta, grid, total);
+          if (!(ok = uq_push(uq, pu, xn, w))) break;
+          decode(x, &bh, &kb);
+          x = xn;
+        } else if (!P.order.unit(cta, grid, static_cast<int>(pu) - 1, &bh, &kb)) {
+          break;
+        }
+        ++pu;
         int q0, nq;
         q_range(P, kb, &q0, &nq);
         if (nq == 0) continue;
@@ -290,10 +318,21 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       auto wait = [&](uint64_t* bar, uint32_t parity) {
         return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, w));
       };
-      uint32_t u_it = 0, q_it = 0, pp = 0, dqf = 0;
+      uint32_t u_it = 0, q_it = 0, pp = 0, dqf = 0, ru = 0;
       bool ok = true, moved = false;
       int bh, kb;
-      for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &kb); ++round) {
+      while (ok) {
+        if constexpr (DYN) {
+          int x;
+          if (!(ok = uq_read(uq, ru, &x, w))) break;
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(uq.empty + ru % UnitQueue::N);
+          if (x >= total) break;
+          decode(x, &bh, &kb);
+        } else if (!P.order.unit(cta, grid, static_cast<int>(ru), &bh, &kb)) {
+          break;
+        }
+        ++ru;
         int q0, nq;
         q_range(P, kb, &q0, &nq);
         if (nq == 0) continue;
@@ -418,10 +457,20 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     ptx::WaitCtx w{abort_flag, P.status, 3u};
     const float sc2 = P.sc2;
     const float2 sc2v = make_float2(sc2, sc2), neg1 = make_float2(-1.f, -1.f);
-    uint32_t q_it = 0, sp = 0;
+    uint32_t q_it = 0, sp = 0, ru = 0;
     bool ok = true;
     int bh, kb;
-    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &kb); ++round) {
+    while (ok) {
+      if constexpr (DYN) {
+        int x;
+        if (!(ok = uq_read(uq, ru, &x, w))) break;
+        ptx::mbar_arrive(uq.empty + ru % UnitQueue::N);
+        if (x >= total) break;
+        decode(x, &bh, &kb);
+      } else if (!P.order.unit(cta, grid, static_cast<int>(ru), &bh, &kb)) {
+        break;
+      }
+      ++ru;
       int q0, nq;
       q_range(P, kb, &q0, &nq);
       if (nq == 0) continue;
@@ -582,7 +631,18 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           *reinterpret_cast<uint4*>(sdS + b * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) = x;
         }
     };
-    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &kb); ++round) {
+    uint32_t ru = 0;
+    while (ok) {
+      if constexpr (DYN) {
+        int x;
+        if (!(ok = uq_read(uq, ru, &x, w))) break;
+        ptx::mbar_arrive(uq.empty + ru % UnitQueue::N);
+        if (x >= total) break;
+        decode(x, &bh, &kb);
+      } else if (!P.order.unit(cta, grid, static_cast<int>(ru), &bh, &kb)) {
+        break;
+      }
+      ++ru;
       int q0, nq;
       q_range(P, kb, &q0, &nq);
       const int key = kb * BT + r;
@@ -708,10 +768,12 @@ struct CfgQ {
   static constexpr int OFF_RING = 0;
   static constexpr int OFF_DPART = OFF_RING + NSLOT * SLOT;
   static constexpr int OFF_BAR = OFF_DPART + DPART_BYTES;
-  // full[NSLOT], empty[NSLOT], qd_ready, s_full, s_free, dp_full, ds_full, dq_full, drain, dpart_full
-  static constexpr int NBAR = 2 * NSLOT + 8;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_MISC + 16;
+  // full[NSLOT], empty[NSLOT], qd_ready, s_full, s_free, dp_full, ds_full, dq_full, drain, dpart_full,
+  // unit queue full[4], empty[4]
+  static constexpr int NBAR = 2 * NSLOT + 8 + 2 * UnitQueue::N;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // TMEM address, abort word, unit queue slots
+  static constexpr int SMEM = OFF_MISC + 16 + 4 * UnitQueue::N;
+  static constexpr int UQ_READERS = 1 + 256;   // the MMA warp (once) and every row thread
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16(BT, BT, false, false);    // S, dP (A in TMEM)
   static constexpr uint32_t IDESC_DQ = ptx::idesc_bf16(BT, HD, false, true);    // dQ (A in TMEM, K MN-major)
   // TMEM columns: Q and dO as packed bf16 (two elements per column), the S
@@ -764,10 +826,16 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   float* dpart = reinterpret_cast<float*>(smem + C::OFF_DPART);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
+  const UnitQueue uq{reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16), qd_ready + 8,
+                     qd_ready + 8 + UnitQueue::N};
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::NSLOT; ++s) {
       ptx::mbar_init(full + s, 1);
       ptx::mbar_init(empty + s, 1);
+    }
+    for (int s = 0; s < UnitQueue::N; ++s) {
+      ptx::mbar_init(uq.full + s, 1);
+      ptx::mbar_init(uq.empty + s, C::UQ_READERS);
     }
     ptx::mbar_init(qd_ready, 256);
     ptx::mbar_init(s_full, 1);
@@ -788,8 +856,12 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int grid = gridDim.x, cta = blockIdx.x;
   const int Tq = P.p.Tq, Tk = P.p.Tk;
+  // the launch's units: (query tile, key split) blocks of every head, handed
+  // out at run time in head groups, the longest (causal: last) blocks first
+  const int nb = P.n_q_tiles * P.dq_splits, nh = P.p.B * P.p.H, total = nb * nh;
+  const int cta = blockIdx.x, grid = gridDim.x;
+  auto decode = [&](int x, int* bh, int* blk) { grouped_unit(x, nb, nh, P.group, P.p.causal != 0, bh, blk); };
   // Ring item i (counted across units) sits in slot i % NSLOT. A unit whose
   // first item is i0 has Q at i0, dO at i0 + 1, O at i0 + 2, and K_j, V_j of
   // its j-th key tile at i0 + 3 + 2j and i0 + 4 + 2j.
@@ -804,9 +876,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     ptx::tma_prefetch_desc(&tmV);
     ptx::tma_prefetch_desc(&tmdO);
     ptx::tma_prefetch_desc(&tmO);
-    uint32_t item = 0;
-    bool ok = true;
-    int bh, blk;
+    uint32_t item = 0, pu = 0;
+    int bh = 0, blk = 0;
     auto load = [&](const CUtensorMap* map, int boxes, uint32_t bytes, int row) {
       const int s = slot(item);
       if (!ptx::mbar_wait(empty + s, par(item) ^ 1u, w)) return false;
@@ -815,7 +886,18 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       ++item;
       return true;
     };
-    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &blk); ++round) {
+    // take the next unit and publish it; the next one is published before
+    // this one's tiles are loaded, so that the row threads can stage it
+    // while they finish this one
+    int x = next_unit_index(P, pu, cta, grid, total);
+    bool ok = !P.dynamic || uq_push(uq, pu, x, w);
+    ++pu;
+    while (ok && x < total) {
+      const int xn = next_unit_index(P, pu, cta, grid, total);
+      if (P.dynamic && !(ok = uq_push(uq, pu, xn, w))) break;
+      ++pu;
+      decode(x, &bh, &blk);
+      x = xn;
       int qt, sp_, j0, nk;
       if (!dq_unit<SPLIT>(P, blk, &qt, &sp_, &j0, &nk)) continue;
       ok = load(&tmQ, C::KB, C::TILE, qt * BT) && load(&tmdO, C::KBV, C::TILE_V, qt * BT) &&
@@ -858,10 +940,21 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       ptx::mma_commit(dp_full);
       ptx::mma_commit(empty + slot(iv));
     };
-    uint32_t item = 0, u_it = 0, sp = 0;
+    uint32_t item = 0, u_it = 0, sp = 0, ru = 0;
     bool ok = true, moved = false;
     int bh, blk;
-    for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &blk); ++round) {
+    while (ok) {
+      int x;
+      if (P.dynamic) {
+        if (!(ok = uq_read(uq, ru, &x, w))) break;
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(uq.empty + ru % UnitQueue::N);
+      } else {
+        x = next_unit_index(P, ru, cta, grid, total);
+      }
+      ++ru;
+      if (x >= total) break;
+      decode(x, &bh, &blk);
       int qt, sp_, j0, nk;
       if (!dq_unit<SPLIT>(P, blk, &qt, &sp_, &j0, &nk)) continue;
       const uint32_t i0 = item;
@@ -1003,22 +1096,29 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       ptx::mbar_arrive(qd_ready);
       return true;
     };
-    // the next unit of this CTA with at least one key tile, from round *rnd on
-    auto next_unit = [&](int* rnd, int* bh, int* qt, int* split, int* j0, int* nk) {
-      int b, bl;
-      while (P.order.unit(cta, grid, *rnd, &b, &bl)) {
-        ++*rnd;
-        if (dq_unit<SPLIT>(P, bl, qt, split, j0, nk)) {
-          *bh = b;
-          return true;
+    // the CTA's next unit with at least one key tile: 1, or 0 at the end of
+    // the launch's units, -1 on a timeout
+    uint32_t ru = 0;
+    auto next_unit = [&](int* bh, int* qt, int* split, int* j0, int* nk) {
+      for (;;) {
+        int x, bl;
+        if (P.dynamic) {
+          if (!uq_read(uq, ru, &x, w)) return -1;
+          ptx::mbar_arrive(uq.empty + ru % UnitQueue::N);
+        } else {
+          x = next_unit_index(P, ru, cta, grid, total);
         }
+        ++ru;
+        if (x >= total) return 0;
+        decode(x, bh, &bl);
+        if (dq_unit<SPLIT>(P, bl, qt, split, j0, nk)) return 1;
       }
-      return false;
     };
     uint32_t item = 0, u_it = 0, sp = 0;
-    int round = 0, bh, qt, split, j0, nk;
-    bool have = next_unit(&round, &bh, &qt, &split, &j0, &nk);
-    bool ok = !have || stage(0u, 0u);
+    int bh, qt, split, j0, nk;
+    const int first = next_unit(&bh, &qt, &split, &j0, &nk);
+    bool have = first == 1;
+    bool ok = first >= 0 && (!have || stage(0u, 0u));
     while (ok && have) {
       const int q = qt * BT + r;
       const bool q_ok = q < Tq;
@@ -1096,7 +1196,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       // so the next unit's first S can start while this unit's epilogue runs.
       const uint32_t i_next = item + 3 + 2 * nk;
       int nbh = 0, nqt = 0, nsplit = 0, nj0 = 0, nnk = 0;
-      const bool have_next = next_unit(&round, &nbh, &nqt, &nsplit, &nj0, &nnk);
+      const int nx = next_unit(&nbh, &nqt, &nsplit, &nj0, &nnk);
+      ok = nx >= 0;
+      if (!ok) break;
+      const bool have_next = nx == 1;
       if (have_next && !(ok = stage(i_next, u_it + 1))) break;
       if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dq_full, u_it & 1u, w)))) break;
       ptx::tc_fence_after();
@@ -1229,6 +1332,27 @@ cudaError_t launch(const LaunchBwd& a) {
   P.sc2 = p.scale * LOG2E;
   const int heads = p.B * p.H;
   const bool split_dq = !atomic && a.dq_splits > 1;
+  // Unit order of the dQ and dK/dV kernels. When the tiles a kernel streams
+  // (K and V of every head for the dQ kernel, Q, dO and the LSE / D slices
+  // for the dK/dV kernel) exceed L2 twice over, the units are claimed at run
+  // time from a counter (zeroed before the launch) in head groups whose tiles
+  // fill about half of L2, so that each group's tiles are read from DRAM
+  // about once; otherwise each CTA takes its static share of all heads,
+  // heaviest first (measured on GB300, fwd+bwd: B=1 H=32 T=32768 d=128
+  // 1164-1218 -> 1280-1297 TFLOP/s with the groups, DRAM reads of the two
+  // kernels 2.1 -> 0.9 GB; B=2 H=16 T=8192 needs no groups and is unchanged;
+  // B=4 H=16 T=2048 was slower with run-time claiming, 547 -> 526).
+  P.sched = a.sched;
+  auto heads_per_group = [&](size_t per_head) {
+    if (per_head * heads <= 2 * a.l2_bytes) return heads;
+    const size_t budget = a.l2_bytes / 2;
+    size_t g = per_head ? budget / per_head : heads;
+    if (g < 1) g = 1;
+    if (g > static_cast<size_t>(heads)) g = heads;
+    return static_cast<int>(g);
+  };
+  const int group_q = heads_per_group(static_cast<size_t>(p.Tk) * (p.d + p.dv) * 2);
+  const int group_kv = heads_per_group(static_cast<size_t>(p.Tq) * (p.d + p.dv) * 2 + P.Tq_pad * 8ull);
   P.dq_splits = split_dq ? a.dq_splits : 1;
   P.dq_split_tiles = split_dq ? a.dq_split_tiles : P.n_k_tiles;
   P.dQpart = a.dQpart;
@@ -1236,9 +1360,12 @@ cudaError_t launch(const LaunchBwd& a) {
     if (atomic || HD != 128) return cudaErrorInvalidValue;   // (the host checks this first)
     if ((e = launch_dq_pair(a, P)) != cudaSuccess) return e;
   } else if (!atomic && main_q) {
-    P.order = Order{P.n_q_tiles * P.dq_splits, heads, p.causal ? 1 : 0};
     if (static_cast<long long>(P.n_q_tiles) * P.dq_splits * heads > 0x7fffffffLL) return cudaErrorInvalidValue;
     const int units = P.n_q_tiles * P.dq_splits * heads;
+    P.dynamic = group_q < heads;
+    // the static order: heaviest first over all heads (causal), head by head (no mask)
+    P.group = P.dynamic ? group_q : (p.causal ? heads : 1);
+    if (P.dynamic && (e = cudaMemsetAsync(a.sched, 0, sizeof(uint32_t), a.stream)) != cudaSuccess) return e;
     const int grid = units < a.num_sms ? units : a.num_sms;
     using CQ = CfgQ<HD, HV>;
     static_assert(CQ::SMEM <= 227 * 1024, "shared memory");
@@ -1249,12 +1376,17 @@ cudaError_t launch(const LaunchBwd& a) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (main_kv) {
-    P.order = Order{P.n_k_tiles, heads, p.causal ? 2 : 0};
+    P.order = Order{P.n_k_tiles, heads, p.causal ? 2 : 0};   // the static order
     const int units = P.n_k_tiles * heads;
+    P.sched = a.sched + 1;
+    P.dynamic = group_kv < heads;
+    P.group = P.dynamic ? group_kv : (p.causal ? heads : 1);
+    if (P.dynamic && (e = cudaMemsetAsync(P.sched, 0, sizeof(uint32_t), a.stream)) != cudaSuccess) return e;
     const int grid = units < a.num_sms ? units : a.num_sms;
     static_assert(CfgKV<HD, HV, true>::SMEM <= 227 * 1024 && CfgKV<HD, HV, false>::SMEM <= 227 * 1024,
                   "shared memory");
-    auto kern = atomic ? dkdv_kernel<HD, HV, true> : dkdv_kernel<HD, HV, false>;
+    auto kern = atomic ? (P.dynamic ? dkdv_kernel<HD, HV, true, true> : dkdv_kernel<HD, HV, true, false>)
+                       : (P.dynamic ? dkdv_kernel<HD, HV, false, true> : dkdv_kernel<HD, HV, false, false>);
     const int smem = atomic ? CfgKV<HD, HV, true>::SMEM : CfgKV<HD, HV, false>::SMEM;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;

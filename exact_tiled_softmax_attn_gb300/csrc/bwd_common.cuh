@@ -9,6 +9,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "ptx.cuh"
 
 namespace attn {
 namespace bwd {
@@ -61,7 +62,81 @@ struct Params {
   Order order;
   int n_q_tiles, n_k_tiles;
   float sc2;               // scale * log2(e)
+  // kernels whose producer hands units to the CTA's other roles (see
+  // UnitQueue): dynamic = 1 claims them at run time from the launch's unit
+  // counter `sched` (zeroed before the launch) in head groups of `group`;
+  // dynamic = 0 takes the CTA's static share (every grid-th unit, serpentine)
+  // of the same order with one group of all heads
+  uint32_t* sched;
+  int group;
+  int dynamic;
 };
+
+// The r-th unit a CTA takes: claimed from the launch's counter (dynamic), or
+// its static share of the sequence: unit r * grid + cta in even rounds and
+// r * grid + grid - 1 - cta in odd ones, so that with the heaviest units
+// first each CTA alternates between the heavy and the light end of what is
+// left. Returns the unit count once the sequence is done.
+__device__ __forceinline__ int next_unit_index(const Params& P, uint32_t r, int cta, int grid, int total) {
+  if (P.dynamic) {
+    const int x = static_cast<int>(atomicAdd(P.sched, 1u));
+    return x < total ? x : total;
+  }
+  const long long base = static_cast<long long>(r) * grid;
+  if (base >= total) return total;
+  const long long x = base + ((r & 1u) ? grid - 1 - cta : cta);
+  return x < total ? static_cast<int>(x) : total;
+}
+
+// Unit x (x < nb * nh) of a launch's sequence of units: heads in groups of
+// `group`, the groups one after another, so that the operand tiles the
+// units of a group share (K and V of a head for query-tile units, Q and dO
+// for key-tile units) stay in L2 while the group runs; within a group the
+// heaviest units first, the block index nb - 1 first when heavy_last and
+// block 0 first otherwise (equal units in either order without a mask).
+__device__ __forceinline__ void grouped_unit(int x, int nb, int nh, int group, bool heavy_last, int* bh, int* blk) {
+  const int g = x / (nb * group);
+  const int y = x - g * nb * group;
+  const int hg = min(group, nh - g * group);
+  const int b = y / hg;
+  *blk = heavy_last ? nb - 1 - b : b;
+  *bh = g * group + (y - b * hg);
+}
+
+// Units claimed at run time (Params::dynamic): the producer claims each unit
+// with an atomic add on a global counter (next_unit_index), so a CTA that
+// finishes early takes more units and the units of a head group run at about
+// the same time, and publishes its index to the CTA's other roles through a
+// ring of N slots in shared memory: slot u % N holds the CTA's u-th unit, or
+// a value >= the unit count once the sequence is done. Every role reads every
+// index in order (units without work included). With the static order each
+// role computes the same sequence itself and the ring is not used.
+struct UnitQueue {
+  static constexpr int N = 4;
+  volatile int* ids;   // [N] shared memory
+  uint64_t* full;      // [N] arrived at by the producer when it wrote the slot
+  uint64_t* empty;     // [N] arrived at once by each reader of the slot (count: all readers)
+};
+
+// Producer: publish x as the CTA's u-th unit (once every reader is done with
+// the slot's previous index). False on a timeout.
+__device__ __forceinline__ bool uq_push(const UnitQueue& q, uint32_t u, int x, const ptx::WaitCtx& w) {
+  const int s = static_cast<int>(u % UnitQueue::N);
+  if (!ptx::mbar_wait(q.empty + s, ((u / UnitQueue::N) & 1u) ^ 1u, w)) return false;
+  q.ids[s] = x;
+  ptx::mbar_arrive(q.full + s);   // (release: the index is seen by whoever acquires this phase)
+  return true;
+}
+
+// Reader (every thread of the calling warp): the CTA's u-th unit index. The
+// caller then arrives on q.empty[u % N] as its reader count says.
+__device__ __forceinline__ bool uq_read(const UnitQueue& q, uint32_t u, int* x, const ptx::WaitCtx& w) {
+  const int s = static_cast<int>(u % UnitQueue::N);
+  if (!__all_sync(0xffffffffu, ptx::mbar_wait(q.full + s, (u / UnitQueue::N) & 1u, w))) return false;
+  *x = q.ids[s];
+  return true;
+}
+
 
 // Deterministic dQ unit `blk` of a head: query tile qt, key split s, first key
 // tile j0 and key tile count nk (0 when the split lies past the tile's keys).

@@ -66,6 +66,11 @@ struct LaunchBwd {
   int dq_split_tiles;
   float* dQpart;
   int deterministic;
+  // bf16, d <= 128: two unit counters of the dQ and dK/dV kernels (zeroed
+  // before each launch), and the device's L2 size, which sets how many heads'
+  // tiles those kernels keep in flight at a time
+  uint32_t* sched;
+  size_t l2_bytes;
   int phase;                // 0 all; 1 preprocess; 2 main kernels (5 then 4); 3 dQ conversion / split reduction;
                             // 4 dK/dV kernel; 5 deterministic dQ kernel
   uint32_t* status;

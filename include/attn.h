@@ -152,7 +152,9 @@ ATTN_API size_t attn_fwd_splitkv_workspace_size(int B, int H, int Tq, int Tk, in
  * Tq_pad = Tq rounded up to a multiple of 128, and, for bf16 with d <= 128
  * and deterministic == 0, the fp32 dQ accumulator [B,H,Tq,d], or, for bf16 with
  * deterministic == 1 and S = attn_bwd_dq_splits(...) > 1, S fp32 partial dQ
- * arrays [S][B,H,Tq,d]; each part starts on a 256-byte boundary. For bf16
+ * arrays [S][B,H,Tq,d], and, for bf16 with d <= 128, 256 bytes of counters
+ * through which the dQ and dK/dV kernels hand out their work units at run
+ * time (reset by each call); each part starts on a 256-byte boundary. For bf16
  * widths other than 64 and 128 it first holds zero-padded bf16 copies of Q,
  * K, V, O, dO and of the three gradients, in rows of the next tile width (64,
  * 128 or 256 columns), then the workspace above for the padded widths; the

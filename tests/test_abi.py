@@ -116,16 +116,21 @@ def test_dq_split_rule(lib, shape, det, want):
     part = (B_ * H * ((Tq + 127) // 128 * 128) * 4 + 255) // 256 * 256
     acc = B_ * H * Tq * d * 4
     ws = B.attn_bwd_workspace_size(B_, H, Tq, Tk, d, d, B.ATTN_BF16, det)
-    assert ws == 2 * part + (acc if det == 0 else (want * acc if want > 1 else 0))
+    r256 = lambda x: (x + 255) // 256 * 256
+    # + 256 bytes for the unit counters of the bf16 dQ and dK/dV kernels
+    assert ws == r256(2 * part + (acc if det == 0 else (want * acc if want > 1 else 0))) + 256
 
 
 def test_workspace_size(lib):
     # -LSE*log2(e) and D, each [B*H, Tq rounded up to 128] fp32 and 256-byte
-    # aligned, then (bf16 with fp32 dQ accumulation) the [B*H*Tq, d] accumulator
-    part = (2 * 3 * 128 * 4 + 255) // 256 * 256
+    # aligned, then (bf16 with fp32 dQ accumulation) the [B*H*Tq, d]
+    # accumulator, then (bf16) 256 bytes of unit counters
+    r256 = lambda x: (x + 255) // 256 * 256
+    part = r256(2 * 3 * 128 * 4)
     assert B.attn_bwd_workspace_size(2, 3, 100, 50, 64, 64, B.ATTN_F32, 0) == 2 * part
-    assert B.attn_bwd_workspace_size(2, 3, 100, 50, 64, 64, B.ATTN_BF16, 1) == 2 * part
-    assert B.attn_bwd_workspace_size(2, 3, 100, 50, 64, 64, B.ATTN_BF16, 0) == 2 * part + 2 * 3 * 100 * 64 * 4
+    assert B.attn_bwd_workspace_size(2, 3, 100, 50, 64, 64, B.ATTN_BF16, 1) == 2 * part + 256
+    assert B.attn_bwd_workspace_size(2, 3, 100, 50, 64, 64, B.ATTN_BF16, 0) == \
+        r256(2 * part + 2 * 3 * 100 * 64 * 4) + 256
     assert B.attn_bwd_workspace_size(2, 3, 0, 50, 64, 64, B.ATTN_BF16, 0) == 0
     assert B.attn_bwd_workspace_size(-1, 3, 100, 50, 64, 64, B.ATTN_BF16, 0) == 0
 
