@@ -6,12 +6,23 @@
 // for fp32 inputs of any head size up to 256.
 //
 // Precision: a score q.k is accumulated in twice the fp32 precision (the
-// compensated dot product below, fp32 instructions only) and held in fp64;
-// scale * q.k and s - m are formed in fp64 before rounding to fp32 for exp.
-// Accumulating s in plain fp32 instead leaves a logit error of ~1e-5..1e-4
-// once |s| reaches the hundreds (keys scaled by +-40), which the softmax turns
-// into output errors above 1e-5. Everything after the exponent (P, sums, P V,
-// dP, dS, dQ, dK, dV) is fp32.
+// compensated dot product below) and kept as an unevaluated sum hi + lo of
+// two floats; scale * (hi + lo) - m is formed from the exact product of hi
+// and scale (one FMA gives its rounding error), so the argument of exp is
+// accurate to about one rounding of its own size even when the logits are in
+// the thousands. Accumulating s in plain fp32 instead leaves a logit error of
+// ~1e-5..1e-4 once |s| reaches the hundreds (keys scaled by +-40), which the
+// softmax turns into output errors above 1e-5. Everything after the exponent
+// (P, sums, P V, dP, dS, dQ, dK, dV) is fp32.
+//
+// Layout of the work: 256 threads per CTA as a 16 x 16 grid (ty, tx); a
+// thread owns rows ty + 16 r (r < 4) of a 64-row tile and columns tx + 16 c
+// of the tile it multiplies against, so every product is a register tile of
+// 4 x C results fed by 4 + C shared-memory loads per step of the reduction.
+// Shared-memory rows are padded to W + 1 floats (W the tile width: 64, 128 or
+// 256 columns, the smallest that holds d and dv), which keeps the 16 rows a
+// warp reads at one reduction index in 16 different banks; the columns from
+// d (or dv) to W hold zeros.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include <stdint.h>
@@ -22,181 +33,242 @@
 namespace attn {
 namespace simt {
 
-constexpr int BM = 32;          // query rows per tile
-constexpr int NT = 256;         // threads per CTA
-constexpr int MAXD = 256;       // largest supported d and dv
+constexpr int NT = 256;   // threads per CTA
+constexpr int BM = 64;    // rows of the tile a CTA owns (queries; keys in the dK/dV kernel)
 
-__device__ __forceinline__ double warp_max_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-// sum_k a_k b_k by the compensated dot product of Ogita, Rump and Oishi
-// ("Accurate Sum and Dot Product", SIAM J. Sci. Comput. 26(6), 2005,
-// algorithm Dot2): each product splits exactly into p + e with one FMA, and
-// the running sum is carried as s + c with Knuth's TwoSum, so the result is
-// as accurate as a dot product accumulated in twice the fp32 precision while
-// using only fp32 instructions (this GPU's fp64 rate is a small fraction of
+// Error-free transformations behind the compensated dot product of Ogita,
+// Rump and Oishi ("Accurate Sum and Dot Product", SIAM J. Sci. Comput. 26(6),
+// 2005, algorithm Dot2): a product splits exactly into p + e with one FMA,
+// and the running sum is carried as s + c with Knuth's TwoSum, so the result
+// is as accurate as a dot product accumulated in twice the fp32 precision,
+// with fp32 instructions only (this GPU's fp64 rate is a small fraction of
 // its fp32 rate). The _rn intrinsics keep the compiler from contracting the
-// separate roundings the method relies on into FMAs. s + c is returned in
-// fp64, where it is exact.
-__device__ __forceinline__ double dot2(const float* a, const float* b, int n) {
-  float s = 0.f, c = 0.f;
-  for (int k = 0; k < n; ++k) {
-    const float p = __fmul_rn(a[k], b[k]);
-    const float e = __fmaf_rn(a[k], b[k], -p);   // a b - p, exactly
-    const float t = __fadd_rn(s, p);
-    const float z = __fsub_rn(t, s);
-    const float err = __fadd_rn(__fsub_rn(s, __fsub_rn(t, z)), __fsub_rn(p, z));   // s + p - t, exactly
-    s = t;
-    c = __fadd_rn(c, __fadd_rn(err, e));
-  }
-  return static_cast<double>(s) + static_cast<double>(c);
+// separate roundings the method relies on into FMAs.
+__device__ __forceinline__ void dot2_step(float a, float b, float& s, float& c) {
+  const float p = __fmul_rn(a, b);
+  const float e = __fmaf_rn(a, b, -p);   // a b - p, exactly
+  const float t = __fadd_rn(s, p);
+  const float z = __fsub_rn(t, s);
+  const float err = __fadd_rn(__fsub_rn(s, __fsub_rn(t, z)), __fsub_rn(p, z));   // s + p - t, exactly
+  s = t;
+  c = __fadd_rn(c, __fadd_rn(err, e));
 }
 
-__device__ __forceinline__ float warp_sum_f(float v) {
+// scale * (hi + lo) as hi' + lo': hi' the rounded product, lo' its rounding
+// error (exact, by FMA) plus scale * lo.
+__device__ __forceinline__ void scale_pair(float hi, float lo, float scale, float& ph, float& pl) {
+  ph = __fmul_rn(hi, scale);
+  pl = __fadd_rn(__fmaf_rn(hi, scale, -ph), __fmul_rn(lo, scale));
+}
+
+// S[r][c] = sum_k A[ra + 16 r][k] B[cb + 16 c][k] over k < n, by Dot2: hi in
+// s, lo in e. A and B are shared-memory tiles with rows of `ld` floats.
+template <int C>
+__device__ __forceinline__ void dot2_tile(const float* A, const float* B, int ld, int ra, int cb, int n,
+                                          float (&s)[4][C], float (&e)[4][C]) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < C; ++c) s[r][c] = e[r][c] = 0.f;
+  const float* a0 = A + ra * ld;
+  const float* b0 = B + cb * ld;
+#pragma unroll 2
+  for (int k = 0; k < n; ++k) {
+    float a[4], b[C];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) a[r] = a0[16 * r * ld + k];
+#pragma unroll
+    for (int c = 0; c < C; ++c) b[c] = b0[16 * c * ld + k];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c = 0; c < C; ++c) dot2_step(a[r], b[c], s[r][c], e[r][c]);
+  }
+}
+
+// X[r][c] = sum_k A[ra + 16 r][k] B[cb + 16 c][k] over k < n (plain fp32).
+template <int C>
+__device__ __forceinline__ void dot_tile(const float* A, const float* B, int ld, int ra, int cb, int n,
+                                         float (&x)[4][C]) {
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < C; ++c) x[r][c] = 0.f;
+  const float* a0 = A + ra * ld;
+  const float* b0 = B + cb * ld;
+#pragma unroll 4
+  for (int k = 0; k < n; ++k) {
+    float a[4], b[C];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) a[r] = a0[16 * r * ld + k];
+#pragma unroll
+    for (int c = 0; c < C; ++c) b[c] = b0[16 * c * ld + k];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c = 0; c < C; ++c) x[r][c] = fmaf(a[r], b[c], x[r][c]);
+  }
+}
+
+// acc[r][q] += sum_k P[ra + 16 r][k] V[k][cb + 16 q] over k < n: P with rows
+// of `ldp` floats, V with rows of `ldv` floats.
+template <int R, int Q>
+__device__ __forceinline__ void acc_tile(const float* P, int ldp, const float* V, int ldv, int ra, int cb, int n,
+                                         float (&acc)[R][Q]) {
+  const float* p0 = P + ra * ldp;
+  const float* v0 = V + cb;
+#pragma unroll 4
+  for (int k = 0; k < n; ++k) {
+    float a[R], b[Q];
+#pragma unroll
+    for (int r = 0; r < R; ++r) a[r] = p0[16 * r * ldp + k];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) b[q] = v0[k * ldv + 16 * q];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int q = 0; q < Q; ++q) acc[r][q] = fmaf(a[r], b[q], acc[r][q]);
+  }
+}
+
+// Rows [r0, r0 + rows) of a [T][cols] fp32 matrix into shared memory with
+// rows of ld floats: rows at or past `valid` and columns [cols, W) as zeros.
+template <int W>
+__device__ __forceinline__ void load_tile(float* dst, int ld, const float* src, int rows, int cols, int valid) {
+  for (int e = threadIdx.x; e < rows * W; e += NT) {
+    const int r = e / W, c = e - r * W;
+    dst[r * ld + c] = (r < valid && c < cols) ? src[static_cast<size_t>(r) * cols + c] : 0.f;
+  }
+}
+
+__device__ __forceinline__ float row_max16(float v) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float row_sum16(float v) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 
-// Copy `rows` x `cols` fp32 rows from global (row stride `cols`) into shared
-// memory with row stride `ld`; rows at or beyond `valid` are zero.
-__device__ __forceinline__ void load_rows(float* dst, int ld, const float* src, int rows, int cols, int valid) {
-  for (int e = threadIdx.x; e < rows * cols; e += NT) {
-    const int r = e / cols, c = e - r * cols;
-    dst[r * ld + c] = (r < valid) ? src[static_cast<size_t>(r) * cols + c] : 0.f;
-  }
+// The tile width for head sizes d, dv: 64, 128 or 256 columns.
+__host__ __device__ inline int tile_width(int d, int dv) {
+  const int m = d > dv ? d : dv;
+  return m <= 64 ? 64 : m <= 128 ? 128 : 256;
 }
 
 // ---------------------------------------------------------------- forward
 
-template <int BN>
+// One CTA per (64-row query tile, head); key tiles of BN keys in ascending
+// order through the online softmax; O (4 x W/16 per thread) in registers.
+template <int W, int BN>
 __global__ void __launch_bounds__(NT) fwd_kernel(const float* __restrict__ Q, const float* __restrict__ K,
                                                  const float* __restrict__ V, float* __restrict__ O,
                                                  float* __restrict__ LSE, const Problem p) {
-  extern __shared__ double smem_d[];
+  constexpr int LD = W + 1, LDP = BN + 1, NC = BN / 16, NQ = W / 16;
+  extern __shared__ float smem_f[];
+  float* sQ = smem_f;           // [BM][LD]
+  float* sK = sQ + BM * LD;     // [BN][LD]
+  float* sV = sK + BN * LD;     // [BN][LD]
+  float* sP = sV + BN * LD;     // [BM][LDP]
   const int d = p.d, dv = p.dv, Tq = p.Tq, Tk = p.Tk;
-  const int ldk = d + 1;
-  double* sS = smem_d;                                  // [BM][BN+1]
-  double* sM = sS + BM * (BN + 1);                      // [BM] running max (fp64, scaled logits)
-  float* sQ = reinterpret_cast<float*>(sM + BM);        // [BM][d+1]
-  float* sK = sQ + BM * ldk;                            // [BN][d+1]
-  float* sV = sK + BN * ldk;                            // [BN][dv]
-  float* sP = sV + BN * dv;                             // [BM][BN]
-  float* sL = sP + BM * BN;                             // [BM] running sum
-  float* sC = sL + BM;                                  // [BM] per-tile correction
-
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
   const int q0 = blockIdx.x * BM;
   const size_t bh = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const double scale = p.scale;
+  const float scale = p.scale;
 
-  load_rows(sQ, ldk, Q + (bh * Tq + q0) * d, BM, d, Tq - q0);
-  if (threadIdx.x < BM) {
-    sM[threadIdx.x] = -CUDART_INF;
-    sL[threadIdx.x] = 0.f;
-  }
-  constexpr int PER = (BM * MAXD + NT - 1) / NT;   // O entries per thread
-  float acc[PER];
+  load_tile<W>(sQ, LD, Q + (bh * Tq + q0) * d, BM, d, Tq - q0);
+  float acc[4][NQ], m[4], l[4];
 #pragma unroll
-  for (int k = 0; k < PER; ++k) acc[k] = 0.f;
-
+  for (int r = 0; r < 4; ++r) {
+    m[r] = -CUDART_INF_F;
+    l[r] = 0.f;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) acc[r][q] = 0.f;
+  }
   int n_kv = (Tk + BN - 1) / BN;
   if (p.causal) n_kv = min(n_kv, (q0 + BM - 1) / BN + 1);
 
   for (int jt = 0; jt < n_kv; ++jt) {
     const int kv0 = jt * BN;
+    __syncthreads();   // the previous tile's P V is done with sK, sV, sP
+    load_tile<W>(sK, LD, K + (bh * Tk + kv0) * d, BN, d, Tk - kv0);
+    load_tile<W>(sV, LD, V + (bh * Tk + kv0) * dv, BN, dv, Tk - kv0);
     __syncthreads();
-    load_rows(sK, ldk, K + (bh * Tk + kv0) * d, BN, d, Tk - kv0);
-    load_rows(sV, dv, V + (bh * Tk + kv0) * dv, BN, dv, Tk - kv0);
-    __syncthreads();
-    // scores, compensated (twice fp32 precision) accumulation
-    for (int e = threadIdx.x; e < BM * BN; e += NT) {
-      const int i = e / BN, j = e - i * BN;
-      const int qi = q0 + i, kj = kv0 + j;
-      const double s = dot2(sQ + i * ldk, sK + j * ldk, d);
-      const bool blocked = (kj >= Tk) || (p.causal && kj > qi);
-      sS[i * (BN + 1) + j] = blocked ? -CUDART_INF : s * scale;
-    }
-    __syncthreads();
-    // online softmax step, one warp per row
-    for (int i = warp; i < BM; i += NT / 32) {
-      double mx = -CUDART_INF;
-      for (int j = lane; j < BN; j += 32) mx = fmax(mx, sS[i * (BN + 1) + j]);
-      mx = warp_max_d(mx);
-      const double m_old = sM[i];
-      const double m_new = fmax(m_old, mx);
-      const double ref = (m_new == -CUDART_INF) ? 0.0 : m_new;   // the -inf rule
+    float sh[4][NC], sl[4][NC];
+    dot2_tile<NC>(sQ, sK, LD, ty, tx, d, sh, sl);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int qi = q0 + ty + 16 * r;
+      float mx = -CUDART_INF_F;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        const int kj = kv0 + tx + 16 * c;
+        float ph, pl;
+        scale_pair(sh[r][c], sl[r][c], scale, ph, pl);
+        const bool blocked = kj >= Tk || (p.causal && kj > qi);
+        sh[r][c] = blocked ? -CUDART_INF_F : ph;
+        sl[r][c] = blocked ? 0.f : pl;
+        mx = fmaxf(mx, sh[r][c]);
+      }
+      mx = row_max16(mx);
+      const float m_new = fmaxf(m[r], mx);
+      const float ref = (m_new == -CUDART_INF_F) ? 0.f : m_new;   // the -inf rule
+      const float corr = expf(m[r] - ref);                         // 0 when m = -inf
       float sum = 0.f;
-      for (int j = lane; j < BN; j += 32) {
-        const float pj = expf(static_cast<float>(sS[i * (BN + 1) + j] - ref));
-        sP[i * BN + j] = pj;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        const float pj = expf(__fadd_rn(__fsub_rn(sh[r][c], ref), sl[r][c]));
+        sP[(ty + 16 * r) * LDP + tx + 16 * c] = pj;
         sum += pj;
       }
-      sum = warp_sum_f(sum);
-      if (lane == 0) {
-        const float corr = expf(static_cast<float>(m_old - ref));   // 0 when m_old = -inf
-        sC[i] = corr;
-        sL[i] = corr * sL[i] + sum;
-        sM[i] = m_new;
-      }
+      l[r] = fmaf(l[r], corr, row_sum16(sum));
+      m[r] = m_new;
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) acc[r][q] *= corr;
     }
     __syncthreads();
-    // acc = corr * acc + P V
-#pragma unroll
-    for (int k = 0; k < PER; ++k) {
-      const int e = threadIdx.x + k * NT;
-      if (e < BM * dv) {
-        const int i = e / dv, c = e - i * dv;
-        float a = acc[k] * sC[i];
-        const float* pr = sP + i * BN;
-        for (int j = 0; j < BN; ++j) a = fmaf(pr[j], sV[j * dv + c], a);
-        acc[k] = a;
-      }
-    }
+    // acc += P V over the tile's keys (padding keys have P = 0 and V = 0)
+    acc_tile<4, NQ>(sP, LDP, sV, LD, ty, tx, min(BN, Tk - kv0), acc);
   }
-  __syncthreads();
 #pragma unroll
-  for (int k = 0; k < PER; ++k) {
-    const int e = threadIdx.x + k * NT;
-    if (e < BM * dv) {
-      const int i = e / dv, c = e - i * dv;
-      if (q0 + i < Tq) {
-        const float l = sL[i];
-        O[(bh * Tq + q0 + i) * dv + c] = (l > 0.f) ? acc[k] / l : 0.f;
-      }
+  for (int r = 0; r < 4; ++r) {
+    const int qi = q0 + ty + 16 * r;
+    if (qi >= Tq) continue;
+    const float inv = l[r] > 0.f ? 1.0f / l[r] : 0.f;
+    float* orow = O + (bh * Tq + qi) * dv;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q)
+      if (tx + 16 * q < dv) orow[tx + 16 * q] = acc[r][q] * inv;
+    if (tx == 0) {
+      const float ref = m[r] == -CUDART_INF_F ? 0.f : m[r];
+      LSE[bh * Tq + qi] = l[r] > 0.f ? static_cast<float>(static_cast<double>(ref) + log(static_cast<double>(l[r])))
+                                     : -CUDART_INF_F;
     }
-  }
-  if (threadIdx.x < BM && q0 + threadIdx.x < Tq) {
-    const int i = threadIdx.x;
-    const float l = sL[i];
-    LSE[bh * Tq + q0 + i] = (l > 0.f) ? static_cast<float>(sM[i] + log(static_cast<double>(l))) : -CUDART_INF_F;
   }
 }
 
-template <int BN>
-size_t fwd_smem(int d, int dv) {
-  return sizeof(double) * (BM * (BN + 1) + BM) +
-         sizeof(float) * (BM * (d + 1) + BN * (d + 1) + BN * dv + BM * BN + 2 * BM);
+template <int W, int BN>
+constexpr size_t fwd_smem() {
+  return sizeof(float) * (BM * (W + 1) + 2 * BN * (W + 1) + BM * (BN + 1));
 }
 
-template <int BN>
+template <int W, int BN>
 cudaError_t fwd_launch(const LaunchFwd& a) {
-  const size_t smem = fwd_smem<BN>(a.p.d, a.p.dv);
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  constexpr size_t smem = fwd_smem<W, BN>();
+  static_assert(smem <= 227 * 1024, "shared memory");
+  cudaError_t e =
+      cudaFuncSetAttribute(fwd_kernel<W, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid((a.p.Tq + BM - 1) / BM, a.p.B * a.p.H);
-  fwd_kernel<BN><<<grid, NT, smem, a.stream>>>(static_cast<const float*>(a.Q), static_cast<const float*>(a.K),
-                                               static_cast<const float*>(a.V), static_cast<float*>(a.O),
-                                               a.LSE, a.p);
+  fwd_kernel<W, BN><<<grid, NT, smem, a.stream>>>(static_cast<const float*>(a.Q), static_cast<const float*>(a.K),
+                                                  static_cast<const float*>(a.V), static_cast<float*>(a.O), a.LSE,
+                                                  a.p);
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- backward
-
-constexpr int BNB = 32;   // keys per tile in the backward kernels
 
 struct BwdArgs {
   const float* Q;
@@ -211,218 +283,264 @@ struct BwdArgs {
   Problem p;
 };
 
-// P and dS of one (query tile, key tile) pair into shared memory.
-//   P_ij  = exp(s_ij - LSE_i)          (s_ij in fp64, blocked -> 0)
-//   dS_ij = P_ij * (dO_i . V_j - D_i)
-__device__ __forceinline__ void tile_p_ds(const float* sQ, const float* sK, const float* sV, const float* sdO,
-                                          const float* sLse, const float* sD, float* sP, float* sdS, int q0,
-                                          int kv0, const Problem& p) {
-  const int d = p.d, dv = p.dv;
-  for (int e = threadIdx.x; e < BM * BNB; e += NT) {
-    const int i = e / BNB, j = e - i * BNB;
-    const int qi = q0 + i, kj = kv0 + j;
-    const bool blocked = (qi >= p.Tq) || (kj >= p.Tk) || (p.causal && kj > qi) || (sLse[i] == -CUDART_INF_F);
-    float pij = 0.f, dsij = 0.f;
-    if (!blocked) {
-      const double s = dot2(sQ + i * (d + 1), sK + j * (d + 1), d);
-      pij = expf(static_cast<float>(s * static_cast<double>(p.scale) - static_cast<double>(sLse[i])));
-      float dp = 0.f;
-      const float* gr = sdO + i * (dv + 1);
-      const float* vr = sV + j * (dv + 1);
-      for (int c = 0; c < dv; ++c) dp = fmaf(gr[c], vr[c], dp);
-      dsij = pij * (dp - sD[i]);
-    }
-    sP[i * (BNB + 1) + j] = pij;
-    sdS[i * (BNB + 1) + j] = dsij;
-  }
+// P and dS of one score tile, for rows a + 16 r and columns b + 16 c of the
+// tile (a thread's register tile): qi, kj the global query and key of each
+// entry, lse and dd the query's LSE and D.
+//   P = exp(scale s - LSE)   (0 where blocked)
+//   dS = P (dP - D)
+__device__ __forceinline__ void p_ds(float sh, float sl, float dp, float scale, float lse, float dd, bool blocked,
+                                     float& pij, float& dsij) {
+  float ph, pl;
+  scale_pair(sh, sl, scale, ph, pl);
+  pij = blocked ? 0.f : expf(__fadd_rn(__fsub_rn(ph, lse), pl));
+  dsij = pij * (dp - dd);
 }
 
-__device__ __forceinline__ void load_qrow_stats(float* sLse, float* sD, const float* LSE, const float* D,
-                                                size_t bh, int q0, int Tq) {
-  if (threadIdx.x < BM) {
-    const int qi = q0 + threadIdx.x;
-    sLse[threadIdx.x] = qi < Tq ? LSE[bh * Tq + qi] : -CUDART_INF_F;
-    sD[threadIdx.x] = qi < Tq ? D[bh * padded_rows(Tq) + qi] : 0.f;
-  }
-}
-
-// One CTA per (key tile, head): loops over the query tiles that see the key
-// tile, accumulates dK and dV in registers, and (unless `with_dq` is 0) adds
-// this key tile's share scale * dS K into dQ with fp32 atomics.
+// One CTA per (64-key tile, head): loops over the query tiles (BQ rows each)
+// that see the key tile, computes S^T = K Q^T (Dot2) and dP^T = V dO^T for
+// the tile, and accumulates dV += P^T dO and dK += dS^T Q in registers
+// (rows of keys ty + 16 r). Unless `with_dq` is 0 it also adds this key
+// tile's share scale * dS K into dQ with fp32 atomics.
+template <int W, int BQ>
 __global__ void __launch_bounds__(NT) dkdv_kernel(const BwdArgs a, int with_dq) {
+  constexpr int LD = W + 1, LDP = BQ + 1, NC = BQ / 16, NQ = W / 16;
   extern __shared__ float smem_f[];
+  float* sK = smem_f;             // [BM][LD]
+  float* sV = sK + BM * LD;       // [BM][LD]
+  float* sQ = sV + BM * LD;       // [BQ][LD]
+  float* sdO = sQ + BQ * LD;      // [BQ][LD]
+  float* sPt = sdO + BQ * LD;     // [BM][LDP]  P^T: key rows, query columns
+  float* sdSt = sPt + BM * LDP;   // [BM][LDP]
+  float* sLse = sdSt + BM * LDP;  // [BQ]
+  float* sD = sLse + BQ;          // [BQ]
   const Problem& p = a.p;
   const int d = p.d, dv = p.dv, Tq = p.Tq, Tk = p.Tk;
-  float* sK = smem_f;                         // [BNB][d+1]
-  float* sV = sK + BNB * (d + 1);             // [BNB][dv+1]
-  float* sQ = sV + BNB * (dv + 1);            // [BM][d+1]
-  float* sdO = sQ + BM * (d + 1);             // [BM][dv+1]
-  float* sP = sdO + BM * (dv + 1);            // [BM][BNB+1]
-  float* sdS = sP + BM * (BNB + 1);           // [BM][BNB+1]
-  float* sLse = sdS + BM * (BNB + 1);         // [BM]
-  float* sD = sLse + BM;                      // [BM]
-
-  const int kv0 = blockIdx.x * BNB;
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+  const int kv0 = blockIdx.x * BM;
   const size_t bh = blockIdx.y;
-  for (int e = threadIdx.x; e < BNB * d; e += NT) {
-    const int r = e / d, c = e - r * d;
-    sK[r * (d + 1) + c] = (kv0 + r < Tk) ? a.K[(bh * Tk + kv0 + r) * d + c] : 0.f;
-  }
-  for (int e = threadIdx.x; e < BNB * dv; e += NT) {
-    const int r = e / dv, c = e - r * dv;
-    sV[r * (dv + 1) + c] = (kv0 + r < Tk) ? a.V[(bh * Tk + kv0 + r) * dv + c] : 0.f;
-  }
-  constexpr int PER = (BNB * MAXD + NT - 1) / NT;
-  float accK[PER], accV[PER];
-#pragma unroll
-  for (int k = 0; k < PER; ++k) accK[k] = accV[k] = 0.f;
+  const float scale = p.scale;
 
-  const int qt0 = p.causal ? kv0 / BM : 0;
-  const int n_qt = (Tq + BM - 1) / BM;
+  load_tile<W>(sK, LD, a.K + (bh * Tk + kv0) * d, BM, d, Tk - kv0);
+  load_tile<W>(sV, LD, a.V + (bh * Tk + kv0) * dv, BM, dv, Tk - kv0);
+  float accV[4][NQ], accK[4][NQ];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) accV[r][q] = accK[r][q] = 0.f;
+
+  const int qt0 = p.causal ? kv0 / BQ : 0;
+  const int n_qt = (Tq + BQ - 1) / BQ;
   for (int qt = qt0; qt < n_qt; ++qt) {
-    const int q0 = qt * BM;
-    __syncthreads();
-    for (int e = threadIdx.x; e < BM * d; e += NT) {
-      const int r = e / d, c = e - r * d;
-      sQ[r * (d + 1) + c] = (q0 + r < Tq) ? a.Q[(bh * Tq + q0 + r) * d + c] : 0.f;
+    const int q0 = qt * BQ;
+    __syncthreads();   // the previous step is done with sQ, sdO, sPt, sdSt
+    load_tile<W>(sQ, LD, a.Q + (bh * Tq + q0) * d, BQ, d, Tq - q0);
+    load_tile<W>(sdO, LD, a.dO + (bh * Tq + q0) * dv, BQ, dv, Tq - q0);
+    if (threadIdx.x < BQ) {
+      const int qi = q0 + threadIdx.x;
+      sLse[threadIdx.x] = qi < Tq ? a.LSE[bh * Tq + qi] : -CUDART_INF_F;
+      sD[threadIdx.x] = qi < Tq ? a.D[bh * padded_rows(Tq) + qi] : 0.f;
     }
-    for (int e = threadIdx.x; e < BM * dv; e += NT) {
-      const int r = e / dv, c = e - r * dv;
-      sdO[r * (dv + 1) + c] = (q0 + r < Tq) ? a.dO[(bh * Tq + q0 + r) * dv + c] : 0.f;
-    }
-    load_qrow_stats(sLse, sD, a.LSE, a.D, bh, q0, Tq);
     __syncthreads();
-    tile_p_ds(sQ, sK, sV, sdO, sLse, sD, sP, sdS, q0, kv0, p);
+    {
+      float sh[4][NC], sl[4][NC], dp[4][NC];
+      dot2_tile<NC>(sK, sQ, LD, ty, tx, d, sh, sl);
+      dot_tile<NC>(sV, sdO, LD, ty, tx, dv, dp);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int kj = kv0 + ty + 16 * r;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          const int i = tx + 16 * c, qi = q0 + i;
+          const float lse = sLse[i];
+          const bool blocked = qi >= Tq || kj >= Tk || (p.causal && kj > qi) || lse == -CUDART_INF_F;
+          float pij, dsij;
+          p_ds(sh[r][c], sl[r][c], dp[r][c], scale, lse, sD[i], blocked, pij, dsij);
+          sPt[(ty + 16 * r) * LDP + i] = pij;
+          sdSt[(ty + 16 * r) * LDP + i] = dsij;
+        }
+      }
+    }
     __syncthreads();
     // dV_j += sum_i P_ij dO_i ; dK_j += sum_i dS_ij Q_i
-#pragma unroll
-    for (int k = 0; k < PER; ++k) {
-      const int e = threadIdx.x + k * NT;
-      if (e < BNB * dv) {
-        const int j = e / dv, c = e - j * dv;
-        float s = accV[k];
-        for (int i = 0; i < BM; ++i) s = fmaf(sP[i * (BNB + 1) + j], sdO[i * (dv + 1) + c], s);
-        accV[k] = s;
-      }
-      if (e < BNB * d) {
-        const int j = e / d, c = e - j * d;
-        float s = accK[k];
-        for (int i = 0; i < BM; ++i) s = fmaf(sdS[i * (BNB + 1) + j], sQ[i * (d + 1) + c], s);
-        accK[k] = s;
-      }
-    }
+    const int nq = min(BQ, Tq - q0);
+    acc_tile<4, NQ>(sPt, LDP, sdO, LD, ty, tx, nq, accV);
+    acc_tile<4, NQ>(sdSt, LDP, sQ, LD, ty, tx, nq, accK);
     if (with_dq) {
-      // dQ_i += scale * sum_j dS_ij K_j
-      for (int e = threadIdx.x; e < BM * d; e += NT) {
-        const int i = e / d, c = e - i * d;
-        if (q0 + i >= Tq) continue;
-        float s = 0.f;
-        for (int j = 0; j < BNB; ++j) s = fmaf(sdS[i * (BNB + 1) + j], sK[j * (d + 1) + c], s);
-        atomicAdd(a.dQ + (bh * Tq + q0 + i) * d + c, s * p.scale);
+      // dQ_i += scale * sum_j dS_ij K_j, rows of queries ty + 16 r
+      constexpr int RQ = BQ / 16;
+      float t[RQ][NQ];
+#pragma unroll
+      for (int r = 0; r < RQ; ++r)
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) t[r][q] = 0.f;
+      // (the transposed dS: entry (query ty + 16 r, key k) sits at sdSt[k][ty + 16 r])
+      const int nk = min(BM, Tk - kv0);
+#pragma unroll 4
+      for (int k = 0; k < nk; ++k) {
+        float x[RQ], b[NQ];
+#pragma unroll
+        for (int r = 0; r < RQ; ++r) x[r] = sdSt[k * LDP + ty + 16 * r];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) b[q] = sK[k * LD + tx + 16 * q];
+#pragma unroll
+        for (int r = 0; r < RQ; ++r)
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) t[r][q] = fmaf(x[r], b[q], t[r][q]);
+      }
+#pragma unroll
+      for (int r = 0; r < RQ; ++r) {
+        const int qi = q0 + ty + 16 * r;
+        if (qi >= Tq) continue;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q)
+          if (tx + 16 * q < d) atomicAdd(a.dQ + (bh * Tq + qi) * d + tx + 16 * q, t[r][q] * scale);
       }
     }
   }
 #pragma unroll
-  for (int k = 0; k < PER; ++k) {
-    const int e = threadIdx.x + k * NT;
-    if (e < BNB * dv) {
-      const int j = e / dv, c = e - j * dv;
-      if (kv0 + j < Tk) a.dV[(bh * Tk + kv0 + j) * dv + c] = accV[k];
-    }
-    if (e < BNB * d) {
-      const int j = e / d, c = e - j * d;
-      if (kv0 + j < Tk) a.dK[(bh * Tk + kv0 + j) * d + c] = accK[k] * p.scale;
+  for (int r = 0; r < 4; ++r) {
+    const int kj = kv0 + ty + 16 * r;
+    if (kj >= Tk) continue;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      const int c = tx + 16 * q;
+      if (c < dv) a.dV[(bh * Tk + kj) * dv + c] = accV[r][q];
+      if (c < d) a.dK[(bh * Tk + kj) * d + c] = accK[r][q] * scale;
     }
   }
 }
 
-// Deterministic dQ: one CTA per (query tile, head) loops over key tiles in a
-// fixed order and writes dQ once.
+// Deterministic dQ: one CTA per (64-row query tile, head) loops over key
+// tiles of BK keys in a fixed order and writes dQ once.
+template <int W, int BK>
 __global__ void __launch_bounds__(NT) dq_kernel(const BwdArgs a) {
+  constexpr int LD = W + 1, LDS = BK + 1, NC = BK / 16, NQ = W / 16;
   extern __shared__ float smem_f[];
+  float* sQ = smem_f;             // [BM][LD]
+  float* sdO = sQ + BM * LD;      // [BM][LD]
+  float* sK = sdO + BM * LD;      // [BK][LD]
+  float* sV = sK + BK * LD;       // [BK][LD]
+  float* sdS = sV + BK * LD;      // [BM][LDS]
+  float* sLse = sdS + BM * LDS;   // [BM]
+  float* sD = sLse + BM;          // [BM]
   const Problem& p = a.p;
   const int d = p.d, dv = p.dv, Tq = p.Tq, Tk = p.Tk;
-  float* sQ = smem_f;                         // [BM][d+1]
-  float* sdO = sQ + BM * (d + 1);             // [BM][dv+1]
-  float* sK = sdO + BM * (dv + 1);            // [BNB][d+1]
-  float* sV = sK + BNB * (d + 1);             // [BNB][dv+1]
-  float* sP = sV + BNB * (dv + 1);            // [BM][BNB+1]
-  float* sdS = sP + BM * (BNB + 1);           // [BM][BNB+1]
-  float* sLse = sdS + BM * (BNB + 1);
-  float* sD = sLse + BM;
-
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
   const int q0 = blockIdx.x * BM;
   const size_t bh = blockIdx.y;
-  for (int e = threadIdx.x; e < BM * d; e += NT) {
-    const int r = e / d, c = e - r * d;
-    sQ[r * (d + 1) + c] = (q0 + r < Tq) ? a.Q[(bh * Tq + q0 + r) * d + c] : 0.f;
+  const float scale = p.scale;
+
+  load_tile<W>(sQ, LD, a.Q + (bh * Tq + q0) * d, BM, d, Tq - q0);
+  load_tile<W>(sdO, LD, a.dO + (bh * Tq + q0) * dv, BM, dv, Tq - q0);
+  if (threadIdx.x < BM) {
+    const int qi = q0 + threadIdx.x;
+    sLse[threadIdx.x] = qi < Tq ? a.LSE[bh * Tq + qi] : -CUDART_INF_F;
+    sD[threadIdx.x] = qi < Tq ? a.D[bh * padded_rows(Tq) + qi] : 0.f;
   }
-  for (int e = threadIdx.x; e < BM * dv; e += NT) {
-    const int r = e / dv, c = e - r * dv;
-    sdO[r * (dv + 1) + c] = (q0 + r < Tq) ? a.dO[(bh * Tq + q0 + r) * dv + c] : 0.f;
-  }
-  load_qrow_stats(sLse, sD, a.LSE, a.D, bh, q0, Tq);
-  constexpr int PER = (BM * MAXD + NT - 1) / NT;
-  float acc[PER];
+  float acc[4][NQ];
 #pragma unroll
-  for (int k = 0; k < PER; ++k) acc[k] = 0.f;
-  int n_kt = (Tk + BNB - 1) / BNB;
-  if (p.causal) n_kt = min(n_kt, (q0 + BM - 1) / BNB + 1);
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) acc[r][q] = 0.f;
+  int n_kt = (Tk + BK - 1) / BK;
+  if (p.causal) n_kt = min(n_kt, (q0 + BM - 1) / BK + 1);
   for (int kt = 0; kt < n_kt; ++kt) {
-    const int kv0 = kt * BNB;
+    const int kv0 = kt * BK;
+    __syncthreads();   // the previous step is done with sK, sV, sdS
+    load_tile<W>(sK, LD, a.K + (bh * Tk + kv0) * d, BK, d, Tk - kv0);
+    load_tile<W>(sV, LD, a.V + (bh * Tk + kv0) * dv, BK, dv, Tk - kv0);
     __syncthreads();
-    for (int e = threadIdx.x; e < BNB * d; e += NT) {
-      const int r = e / d, c = e - r * d;
-      sK[r * (d + 1) + c] = (kv0 + r < Tk) ? a.K[(bh * Tk + kv0 + r) * d + c] : 0.f;
-    }
-    for (int e = threadIdx.x; e < BNB * dv; e += NT) {
-      const int r = e / dv, c = e - r * dv;
-      sV[r * (dv + 1) + c] = (kv0 + r < Tk) ? a.V[(bh * Tk + kv0 + r) * dv + c] : 0.f;
-    }
-    __syncthreads();
-    tile_p_ds(sQ, sK, sV, sdO, sLse, sD, sP, sdS, q0, kv0, p);
-    __syncthreads();
+    {
+      float sh[4][NC], sl[4][NC], dp[4][NC];
+      dot2_tile<NC>(sQ, sK, LD, ty, tx, d, sh, sl);
+      dot_tile<NC>(sdO, sV, LD, ty, tx, dv, dp);
 #pragma unroll
-    for (int k = 0; k < PER; ++k) {
-      const int e = threadIdx.x + k * NT;
-      if (e < BM * d) {
-        const int i = e / d, c = e - i * d;
-        float s = acc[k];
-        for (int j = 0; j < BNB; ++j) s = fmaf(sdS[i * (BNB + 1) + j], sK[j * (d + 1) + c], s);
-        acc[k] = s;
+      for (int r = 0; r < 4; ++r) {
+        const int i = ty + 16 * r, qi = q0 + i;
+        const float lse = sLse[i], dd = sD[i];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          const int kj = kv0 + tx + 16 * c;
+          const bool blocked = qi >= Tq || kj >= Tk || (p.causal && kj > qi) || lse == -CUDART_INF_F;
+          float pij, dsij;
+          p_ds(sh[r][c], sl[r][c], dp[r][c], scale, lse, dd, blocked, pij, dsij);
+          sdS[i * LDS + tx + 16 * c] = dsij;
+        }
       }
     }
+    __syncthreads();
+    acc_tile<4, NQ>(sdS, LDS, sK, LD, ty, tx, min(BK, Tk - kv0), acc);
   }
 #pragma unroll
-  for (int k = 0; k < PER; ++k) {
-    const int e = threadIdx.x + k * NT;
-    if (e < BM * d) {
-      const int i = e / d, c = e - i * d;
-      if (q0 + i < Tq) a.dQ[(bh * Tq + q0 + i) * d + c] = acc[k] * p.scale;
-    }
+  for (int r = 0; r < 4; ++r) {
+    const int qi = q0 + ty + 16 * r;
+    if (qi >= Tq) continue;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q)
+      if (tx + 16 * q < d) a.dQ[(bh * Tq + qi) * d + tx + 16 * q] = acc[r][q] * scale;
   }
 }
 
-size_t bwd_smem(int d, int dv) {
-  return sizeof(float) * (BNB * (d + 1) + BNB * (dv + 1) + BM * (d + 1) + BM * (dv + 1) + 2 * BM * (BNB + 1) +
-                          2 * BM);
+template <int W>
+constexpr int bwd_rows() { return W > 128 ? 32 : 64; }   // queries (dK/dV) or keys (dQ) per step
+
+template <int W>
+constexpr size_t dkdv_smem() {
+  constexpr int BQ = bwd_rows<W>();
+  return sizeof(float) * (2 * BM * (W + 1) + 2 * BQ * (W + 1) + 2 * BM * (BQ + 1) + 2 * BQ);
+}
+template <int W>
+constexpr size_t dq_smem() {
+  constexpr int BK = bwd_rows<W>();
+  return sizeof(float) * (2 * BM * (W + 1) + 2 * BK * (W + 1) + BM * (BK + 1) + 2 * BM);
+}
+
+template <int W>
+cudaError_t bwd_launch(const LaunchBwd& la, const BwdArgs& b, bool kv, bool q) {
+  constexpr int R = bwd_rows<W>();
+  constexpr size_t s1 = dkdv_smem<W>(), s2 = dq_smem<W>();
+  static_assert(s1 <= 227 * 1024 && s2 <= 227 * 1024, "shared memory");
+  const Problem& p = la.p;
+  cudaError_t e;
+  if (kv && p.Tk > 0) {
+    e = cudaFuncSetAttribute(dkdv_kernel<W, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s1));
+    if (e != cudaSuccess) return e;
+    dim3 g1((p.Tk + BM - 1) / BM, p.B * p.H);
+    dkdv_kernel<W, R><<<g1, NT, s1, la.stream>>>(b, la.deterministic ? 0 : 1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (q) {
+    e = cudaFuncSetAttribute(dq_kernel<W, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s2));
+    if (e != cudaSuccess) return e;
+    dim3 g2((p.Tq + BM - 1) / BM, p.B * p.H);
+    dq_kernel<W, R><<<g2, NT, s2, la.stream>>>(b);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace simt
 
 size_t fwd_f32_smem_bytes(int block_n, int d, int dv) {
+  using namespace simt;
+  const int W = tile_width(d, dv);
   switch (block_n) {
-    case 32: return simt::fwd_smem<32>(d, dv);
-    case 128: return simt::fwd_smem<128>(d, dv);
-    default: return simt::fwd_smem<64>(d, dv);
+    case 32: return W == 64 ? fwd_smem<64, 32>() : W == 128 ? fwd_smem<128, 32>() : fwd_smem<256, 32>();
+    case 128: return W == 64 ? fwd_smem<64, 128>() : W == 128 ? fwd_smem<128, 128>() : fwd_smem<256, 128>();
+    default: return W == 64 ? fwd_smem<64, 64>() : W == 128 ? fwd_smem<128, 64>() : fwd_smem<256, 64>();
   }
 }
 
 cudaError_t launch_fwd_f32(const LaunchFwd& a) {
+  using namespace simt;
+  const int W = tile_width(a.p.d, a.p.dv);
   switch (a.block_n) {
-    case 32: return simt::fwd_launch<32>(a);
-    case 128: return simt::fwd_launch<128>(a);
-    default: return simt::fwd_launch<64>(a);
+    case 32: return W == 64 ? fwd_launch<64, 32>(a) : W == 128 ? fwd_launch<128, 32>(a) : fwd_launch<256, 32>(a);
+    case 128:
+      // a 128-key tile of rows wider than 128 columns does not fit in shared
+      // memory (the host refuses it before the launch)
+      return W == 64 ? fwd_launch<64, 128>(a) : W == 128 ? fwd_launch<128, 128>(a) : cudaErrorInvalidValue;
+    default: return W == 64 ? fwd_launch<64, 64>(a) : W == 128 ? fwd_launch<128, 64>(a) : fwd_launch<256, 64>(a);
   }
 }
 
@@ -441,23 +559,9 @@ cudaError_t launch_bwd_f32(const LaunchBwd& a) {
   simt::BwdArgs b{static_cast<const float*>(a.Q), static_cast<const float*>(a.K), static_cast<const float*>(a.V),
                   static_cast<const float*>(a.dO), a.LSE, a.D, static_cast<float*>(a.dQ),
                   static_cast<float*>(a.dK), static_cast<float*>(a.dV), p};
-  const size_t smem = simt::bwd_smem(p.d, p.dv);
-  e = cudaFuncSetAttribute(simt::dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(simt::dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  if (kv && p.Tk > 0) {
-    dim3 g1((p.Tk + simt::BNB - 1) / simt::BNB, p.B * p.H);
-    simt::dkdv_kernel<<<g1, simt::NT, smem, a.stream>>>(b, a.deterministic ? 0 : 1);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  if (q) {
-    dim3 g2((p.Tq + simt::BM - 1) / simt::BM, p.B * p.H);
-    simt::dq_kernel<<<g2, simt::NT, smem, a.stream>>>(b);
-    e = cudaGetLastError();
-  }
-  return e;
+  const int W = simt::tile_width(p.d, p.dv);
+  return W == 64 ? simt::bwd_launch<64>(a, b, kv, q)
+                 : W == 128 ? simt::bwd_launch<128>(a, b, kv, q) : simt::bwd_launch<256>(a, b, kv, q);
 }
 
 }  // namespace attn

@@ -36,7 +36,7 @@
  * Supported shapes:
  *   ATTN_F32 : 1 <= d, dv <= 256, any B, H, Tq, Tk >= 0 (attn_fwd_f32_blocked
  *              with block_n = 128 returns ATTN_ERR_UNSUPPORTED when its key
- *              tile does not fit in shared memory, above d = dv = 150 or so)
+ *              tile does not fit in shared memory: d or dv above 128)
  *   ATTN_BF16: forward (attn_fwd, attn_fwd_splitkv): d and dv multiples
  *              of 8 from 8 to 256, independently (the page's task takes V
  *              with its own head dimension); a width below 64, 128 or 256
