@@ -43,6 +43,9 @@ KERNEL_SOURCES = {
     # both launches (the dV and the dK kernel) of the phase bench.py times together
     "kv256_kernel": ("bwd_d256.cu", "bwd_common.cuh", "ptx.cuh", "common.cuh", "launch.h"),
     "q256_kernel": ("bwd_d256.cu", "bwd_common.cuh", "ptx.cuh", "common.cuh", "launch.h"),
+    "simt::fwd_kernel": ("simt_f32.cu", "common.cuh", "launch.h"),
+    "simt::dkdv_kernel": ("simt_f32.cu", "common.cuh", "launch.h"),
+    "simt::dq_kernel": ("simt_f32.cu", "common.cuh", "launch.h"),
 }
 
 
@@ -94,17 +97,18 @@ def load_peaks():
                 "source": "fallback"}
 
 
-def load_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
-    when the summary was taken on different kernel sources."""
+def load_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary, or None when there is none for that workload or it was taken on
+    different kernel sources."""
     p = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         with open(p) as f:
             for line in f:
                 parts = line.split()
-                if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel:
-                    ok = kernel in KERNEL_SOURCES and parts[1] == kernel_source_hash(kernel)
-                    return float(parts[2]) if ok else None
+                if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload:
+                    ok = kernel in KERNEL_SOURCES and parts[2] == kernel_source_hash(kernel)
+                    return float(parts[3]) if ok else None
     except OSError:
         pass
     return None
@@ -325,6 +329,7 @@ def run_ours(args, w):
     code = pkg.ATTN_BF16 if w.dtype == "bf16" else pkg.ATTN_F32
     B, H, Tq, Tk, d, dv = w.B, w.H, w.Tq, w.Tk, w.d, w.dv
     det = int(args.dq_mode == "deterministic")
+    f32 = w.dtype == "f32"
     es = 2 if w.dtype == "bf16" else 4   # bytes per input element
 
     host = make_inputs(w.with_(seed=rank_seed(w, rank)))
@@ -361,10 +366,16 @@ def run_ours(args, w):
         pkg.attn_bwd_phase(x["Q"], x["K"], x["V"], o, lse, x["dO"], dq, dk, dvv, B, H, Tq, Tk, d, dv, sc,
                            w.causal, code, det, ws, ws.numel(), ph, stream)
 
-    # backward launch groups in order: preprocess (atomic dQ only for bf16),
-    # dQ kernel (deterministic only; it also forms D), dK/dV kernel, dQ
-    # conversion (atomic only); none with --fwd-only
-    phases = () if args.fwd_only else (1, 6 if args.dq_pairs else 5, 4, 3)
+    # backward launch groups in order: preprocess, dQ kernel (deterministic
+    # only; for bf16 rows of up to 128 columns it also forms D), dK/dV kernel,
+    # dQ conversion or split-dQ reduction; none with --fwd-only. A group that
+    # launches nothing for this configuration (the library's own rule, as in
+    # attn_bwd_phase) is not called, so that no event interval of the timed
+    # step is an empty one.
+    launches = {1: f32 or not det or w.d > 128, 5: bool(det), 6: bool(det), 4: True,
+                3: not f32 and w.d <= 128 and (not det or dq_splits > 1)}
+    phases = () if args.fwd_only else tuple(ph for ph in (1, 6 if args.dq_pairs else 5, 4, 3) if launches[ph])
+    slot = {1: 1, 5: 2, 6: 2, 4: 3, 3: 4}   # per-step interval of each group: fwd, pre, q, kv, conv
 
     def step(ev=None):
         if ev is not None:
@@ -376,9 +387,6 @@ def run_ours(args, w):
             bwd_phase(ph)
             if ev is not None:
                 ev[2 + i].record(stream)
-        if ev is not None:
-            for i in range(len(phases), 4):
-                ev[2 + i].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -389,7 +397,7 @@ def run_ours(args, w):
     if clocks:
         clocks.start()
         time.sleep(0.3)
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2 + len(phases))] for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
@@ -401,7 +409,12 @@ def run_ours(args, w):
     barrier()
     if clocks:
         clocks.mark(t_wall0, t_wall1)
-    per = [[e[j].elapsed_time(e[j + 1]) for j in range(5)] for e in events]   # ms: fwd, pre, q, kv, conv
+    per = []                           # ms per step: fwd, pre, q, kv, conv (0 for a group not called)
+    for e in events:
+        row = [e[0].elapsed_time(e[1]), 0.0, 0.0, 0.0, 0.0]
+        for i, ph in enumerate(phases):
+            row[slot[ph]] = e[1 + i].elapsed_time(e[2 + i])
+        per.append(row)
     step_ms = [sum(p) for p in per]
     total_ms = reduce_max(sum(step_ms))
     fwd_ms, pre_ms, q_ms, kv_ms, conv_ms = (statistics.mean(p[j] for p in per) for j in range(5))
@@ -485,12 +498,11 @@ def run_ours(args, w):
     # kernel's own product is dQ (it recomputes S and dP, which is counted
     # under "executed").
     md, mv = w.pair_flop() * w.d, w.pair_flop() * w.dv
-    f32 = w.dtype == "f32"
     if f32:
-        # the CUDA-core path: FP32 FMA throughput (its scores accumulate in fp64)
+        # the CUDA-core path: FP32 FMA throughput (its scores accumulate compensated)
         props = torch.cuda.get_device_properties(dev)
         peak = props.multi_processor_count * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
-    tag = "simt " if f32 else ""
+    tag = "simt::" if f32 else ""
     if n_splits > 1:
         fwd_name = f"fwd split-KV, {n_splits} splits (attn_fwd_bf16_kernel + merge)"
     else:
@@ -516,26 +528,23 @@ def run_ours(args, w):
         if "executed_flop" in v:
             v["executed_tflops"] = v["executed_flop"] / (v["ms"] * 1e-3) / 1e12
     if not args.fwd_only:
-        kernels.update({
-            "bwd main (all main kernels)": {"ms": main_ms, "tflops": Bf / (main_ms * 1e-3) / 1e12},
-            # reads O, dO, LSE; writes D and LSE*log2(e) (padded rows) and zeroes the dQ accumulator
-            # atomic dQ only (bf16): the deterministic dQ kernel forms D itself
-            "bwd preprocess": {"ms": pre_ms,
-                               "gbs": B * H * Tq * (2 * dv * es + 4 + 8 + (0 if (det or w.d > 128) else d * 4)) /
-                               (pre_ms * 1e-3) / 1e9 if (f32 or not det or w.d > 128) else None},
-            # atomic: fp32 accumulator -> bf16; deterministic with split dQ: the partials' sum -> bf16
-            "dQ convert": {"ms": conv_ms,
-                           "gbs": B * H * Tq * d * (4 * (1 if not det else dq_splits) + 2) / (conv_ms * 1e-3) / 1e9
-                           if not f32 and w.d <= 128 and (not det or dq_splits > 1) else None},
-        })
+        kernels["bwd main (all main kernels)"] = {"ms": main_ms, "tflops": Bf / (main_ms * 1e-3) / 1e12}
         kernels["bwd main (all main kernels)"]["frac_of_peak"] = \
             kernels["bwd main (all main kernels)"]["tflops"] / peak
-        if kernels["bwd preprocess"]["gbs"] is not None:
-            kernels["bwd preprocess"]["frac_of_hbm"] = kernels["bwd preprocess"]["gbs"] / peaks["hbm_gbs"]
+        if launches[1]:
+            # reads O, dO, LSE; writes D and -LSE*log2(e) (padded rows); zeroes the fp32 dQ
+            # accumulator in atomic mode (bf16 rows of up to 128 columns, deterministic:
+            # the dQ kernel forms D itself and this group launches nothing)
+            gbs = B * H * Tq * (2 * dv * es + 4 + 8 + (0 if (det or w.d > 128) else d * 4)) / (pre_ms * 1e-3) / 1e9
+            kernels["bwd preprocess"] = {"ms": pre_ms, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]}
+        if launches[3]:
+            # atomic: fp32 accumulator -> bf16; deterministic with split dQ: the partials' sum -> bf16
+            kernels["dQ convert"] = {"ms": conv_ms, "gbs": B * H * Tq * d * (4 * (1 if not det else dq_splits) + 2) /
+                                     (conv_ms * 1e-3) / 1e9}
     # the dominant kernel: the longest of the single kernels
     dom = max((k for k, v in kernels.items() if "flop" in v), key=lambda k: kernels[k]["ms"])
     achieved = kernels[dom]["tflops"]
-    traffic = load_traffic(dom.split("(")[-1].rstrip(")"))
+    traffic = load_traffic(dom.split("(")[-1].rstrip(")"), args.workload)
     cfg = workload_config(w)
     cfg.update({"pass": "forward only" if args.fwd_only else "forward + backward",
                 "dq_mode": None if args.fwd_only else ("deterministic" if det else "atomic"),

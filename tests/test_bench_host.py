@@ -155,3 +155,25 @@ def test_gpus_flag_must_match_the_launcher_world_size():
 def test_rank_seeds_are_distinct():
     w = WORKLOADS["c3"]
     assert len({bench.rank_seed(w, r) for r in range(8)}) == 8 and bench.rank_seed(w, 0) == w.seed
+
+
+def test_traffic_entries_name_a_kernel_a_workload_and_a_summary():
+    # profiles/traffic.txt: kernel, workload, source hash, DRAM bytes per launch,
+    # summary file; bench.py reports a figure only for the line's own workload
+    # and only while the kernel's sources still hash the same
+    path = os.path.join(bench.ROOT, "profiles", "traffic.txt")
+    rows = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    assert rows
+    seen = set()
+    for kernel, workload, h, nbytes, summary in rows:
+        assert kernel in bench.KERNEL_SOURCES, kernel
+        assert workload in WORKLOADS, workload
+        assert (kernel, workload) not in seen
+        seen.add((kernel, workload))
+        assert len(h) == 16 and float(nbytes) > 0
+        assert os.path.isfile(os.path.join(bench.ROOT, summary)), summary
+    k, wl, h, nbytes, _ = rows[0]
+    expect = float(nbytes) if h == bench.kernel_source_hash(k) else None
+    assert bench.load_traffic(k, wl) == expect
+    other = next(n for n in WORKLOADS if (k, n) not in seen)
+    assert bench.load_traffic(k, other) is None
