@@ -506,7 +506,7 @@ def run_ours(args, w):
     if n_splits > 1:
         fwd_name = f"fwd split-KV, {n_splits} splits (attn_fwd_bf16_kernel + merge)"
     else:
-        fwd_name = "fwd (simt fwd_kernel)" if f32 else \
+        fwd_name = "fwd (simt::fwd_kernel)" if f32 else \
             "fwd (attn_fwd_d256_kernel)" if w.d > 128 else "fwd (attn_fwd_bf16_kernel)"
     kernels = {fwd_name: {"ms": fwd_ms, "flop": F}}
     if args.fwd_only:

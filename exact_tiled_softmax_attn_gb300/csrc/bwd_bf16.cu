@@ -1339,9 +1339,10 @@ cudaError_t launch(const LaunchBwd& a) {
   // fill about half of L2, so that each group's tiles are read from DRAM
   // about once; otherwise each CTA takes its static share of all heads,
   // heaviest first (measured on GB300, fwd+bwd: B=1 H=32 T=32768 d=128
-  // 1164-1218 -> 1280-1297 TFLOP/s with the groups, DRAM reads of the two
-  // kernels 2.1 -> 0.9 GB; B=2 H=16 T=8192 needs no groups and is unchanged;
-  // B=4 H=16 T=2048 was slower with run-time claiming, 547 -> 526).
+  // 1164-1218 -> 1280-1297 TFLOP/s with the groups, DRAM reads per launch of
+  // the dQ kernel 38.7 -> 2.0 GB and of the dK/dV kernel 24.2 -> 1.1 GB;
+  // B=2 H=16 T=8192 needs no groups and is unchanged; B=4 H=16 T=2048 was
+  // slower with run-time claiming, 547 -> 526).
   P.sched = a.sched;
   auto heads_per_group = [&](size_t per_head) {
     if (per_head * heads <= 2 * a.l2_bytes) return heads;
