@@ -481,23 +481,30 @@ __global__ void __launch_bounds__(NT) dq_kernel(const BwdArgs a) {
   }
 }
 
+// Queries per step of the dK/dV kernel and keys per step of the dQ kernel.
+// The dQ kernel takes 32-key steps from W = 128 on: its shared memory then
+// fits two CTAs per SM (measured on GB300 at B=2 H=8 Tq=1000 Tk=4000
+// d=128: 5.14 -> 4.60 ms), where 32-query steps made the dK/dV kernel
+// slower (5.20 -> 5.57 ms) and W = 64 problems gain nothing.
 template <int W>
-constexpr int bwd_rows() { return W > 128 ? 32 : 64; }   // queries (dK/dV) or keys (dQ) per step
+constexpr int dkdv_rows() { return W > 128 ? 32 : 64; }
+template <int W>
+constexpr int dq_rows() { return W >= 128 ? 32 : 64; }
 
 template <int W>
 constexpr size_t dkdv_smem() {
-  constexpr int BQ = bwd_rows<W>();
+  constexpr int BQ = dkdv_rows<W>();
   return sizeof(float) * (2 * BM * (W + 1) + 2 * BQ * (W + 1) + 2 * BM * (BQ + 1) + 2 * BQ);
 }
 template <int W>
 constexpr size_t dq_smem() {
-  constexpr int BK = bwd_rows<W>();
+  constexpr int BK = dq_rows<W>();
   return sizeof(float) * (2 * BM * (W + 1) + 2 * BK * (W + 1) + BM * (BK + 1) + 2 * BM);
 }
 
 template <int W>
 cudaError_t bwd_launch(const LaunchBwd& la, const BwdArgs& b, bool kv, bool q) {
-  constexpr int R = bwd_rows<W>();
+  constexpr int R = dkdv_rows<W>(), RK = dq_rows<W>();
   constexpr size_t s1 = dkdv_smem<W>(), s2 = dq_smem<W>();
   static_assert(s1 <= 227 * 1024 && s2 <= 227 * 1024, "shared memory");
   const Problem& p = la.p;
@@ -510,10 +517,10 @@ cudaError_t bwd_launch(const LaunchBwd& la, const BwdArgs& b, bool kv, bool q) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (q) {
-    e = cudaFuncSetAttribute(dq_kernel<W, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s2));
+    e = cudaFuncSetAttribute(dq_kernel<W, RK>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s2));
     if (e != cudaSuccess) return e;
     dim3 g2((p.Tq + BM - 1) / BM, p.B * p.H);
-    dq_kernel<W, R><<<g2, NT, s2, la.stream>>>(b);
+    dq_kernel<W, RK><<<g2, NT, s2, la.stream>>>(b);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
