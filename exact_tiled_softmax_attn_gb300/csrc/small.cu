@@ -41,8 +41,8 @@ __device__ __forceinline__ float dot16(const uint4& a, const uint4& b, const flo
 // stored log-sum-exp in log2 units into [B*H, Tq_pad] arrays whose padding
 // rows hold D = 0 and NLSE2 = -inf (so exp2(s + NLSE2) = 0 there). The backward
 // fetches a 128-row slice of each with one bulk copy. Each group of LPR lanes
-// reads one row with 16-byte loads; rows are walked grid-stride. Optionally
-// zeroes the matching row of an fp32 accumulator.
+// reads a row with 16-byte loads, two rows at a time; rows are walked
+// grid-stride. Optionally zeroes the matching row of an fp32 accumulator.
 template <typename T>
 __global__ void __launch_bounds__(NT) preprocess_vec(const T* __restrict__ O, const T* __restrict__ dO,
                                                       const float* __restrict__ LSE, float* __restrict__ D,
@@ -55,28 +55,40 @@ __global__ void __launch_bounds__(NT) preprocess_vec(const T* __restrict__ O, co
   const int sub = lane / lpr, c = lane - sub * lpr;
   const long long warp_id = (static_cast<long long>(blockIdx.x) * NT + threadIdx.x) >> 5;
   const long long n_warps = (static_cast<long long>(gridDim.x) * NT) >> 5;
-  for (long long r0 = warp_id * rows_per_warp; r0 < rows_pad; r0 += n_warps * rows_per_warp) {
-    const long long rp = r0 + sub;
-    const long long bh = rp / Tq_pad;
-    const int q = static_cast<int>(rp - bh * Tq_pad);
-    const long long r = bh * Tq + q;                           // unpadded row
-    const bool inside = (sub < rows_per_warp) && (rp < rows_pad);
-    const bool real = inside && q < Tq;
-    float s = 0.f;
-    if (real) {
-      const uint4 a = reinterpret_cast<const uint4*>(O + r * dv)[c];
-      const uint4 b = reinterpret_cast<const uint4*>(dO + r * dv)[c];
-      s = dot16(a, b, static_cast<const T*>(nullptr));
+  const long long step = n_warps * rows_per_warp;
+  // two rows per lane group in flight: both rows' loads (O, dO chunks and
+  // the LSE) are issued before either is reduced
+  for (long long r0 = warp_id * rows_per_warp; r0 < rows_pad; r0 += 2 * step) {
+    long long rp[2], r[2];
+    bool inside[2], real[2];
+    float lse[2], s[2];
+    uint4 a[2], b[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      rp[u] = r0 + u * step + sub;
+      const long long bh = rp[u] / Tq_pad;
+      const int q = static_cast<int>(rp[u] - bh * Tq_pad);
+      r[u] = bh * Tq + q;                                      // unpadded row
+      inside[u] = (sub < rows_per_warp) && (rp[u] < rows_pad);
+      real[u] = inside[u] && q < Tq;
+      lse[u] = (real[u] && c == 0) ? LSE[r[u]] : -CUDART_INF_F;
+      if (real[u]) {
+        a[u] = reinterpret_cast<const uint4*>(O + r[u] * dv)[c];
+        b[u] = reinterpret_cast<const uint4*>(dO + r[u] * dv)[c];
+      }
     }
-    for (int o = lpr >> 1; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (inside && c == 0) {
-      D[rp] = s;
-      const float lse = real ? LSE[r] : -CUDART_INF_F;
-      NLSE2[rp] = (lse == -CUDART_INF_F) ? -CUDART_INF_F : -lse * 1.4426950408889634f;
-    }
-    if (real && zero_rows) {
-      float4* z = reinterpret_cast<float4*>(zero_rows + r * zero_cols);
-      for (int k = c; k < zero_cols / 4; k += lpr) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      s[u] = real[u] ? dot16(a[u], b[u], static_cast<const T*>(nullptr)) : 0.f;
+      for (int o = lpr >> 1; o > 0; o >>= 1) s[u] += __shfl_xor_sync(0xffffffffu, s[u], o);
+      if (inside[u] && c == 0) {
+        D[rp[u]] = s[u];
+        NLSE2[rp[u]] = (lse[u] == -CUDART_INF_F) ? -CUDART_INF_F : -lse[u] * 1.4426950408889634f;
+      }
+      if (real[u] && zero_rows) {
+        float4* z = reinterpret_cast<float4*>(zero_rows + r[u] * zero_cols);
+        for (int k = c; k < zero_cols / 4; k += lpr) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
   }
 }
@@ -93,13 +105,13 @@ __global__ void __launch_bounds__(NT) preprocess_f32(const float* __restrict__ O
     const long long bh = rp / Tq_pad;
     const int q = static_cast<int>(rp - bh * Tq_pad);
     const long long r = bh * Tq + q;
+    const float lse = (q < Tq && lane == 0) ? LSE[r] : -CUDART_INF_F;   // with the row loads
     float s = 0.f;
     if (q < Tq)
       for (int c = lane; c < dv; c += 32) s = fmaf(O[r * dv + c], dO[r * dv + c], s);
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (lane == 0) {
       D[rp] = s;
-      const float lse = q < Tq ? LSE[r] : -CUDART_INF_F;
       NLSE2[rp] = (lse == -CUDART_INF_F) ? -CUDART_INF_F : -lse * 1.4426950408889634f;
     }
     if (zero_rows && q < Tq)
