@@ -39,6 +39,7 @@ KERNEL_SOURCES = {
     "dkdv_kernel": ("bwd_bf16.cu", "bwd_common.cuh", "ptx.cuh", "common.cuh", "launch.h"),
     "dq_kernel": ("bwd_bf16.cu", "bwd_common.cuh", "ptx.cuh", "common.cuh", "launch.h"),
     "attn_fwd_d256_kernel": ("fwd_bf16_d256.cu", "ptx.cuh", "common.cuh", "launch.h"),
+    "attn_fwd_d256_pair_kernel": ("fwd_d256_pair.cu", "ptx.cuh", "common.cuh", "launch.h"),
     "dq_pair_kernel": ("dq_pair.cu", "bwd_common.cuh", "ptx.cuh", "common.cuh", "launch.h"),
     # both launches (the dV and the dK kernel) of the phase bench.py times together
     "kv256_kernel": ("bwd_d256.cu", "bwd_common.cuh", "ptx.cuh", "common.cuh", "launch.h"),
@@ -507,7 +508,8 @@ def run_ours(args, w):
         fwd_name = f"fwd split-KV, {n_splits} splits (attn_fwd_bf16_kernel + merge)"
     else:
         fwd_name = "fwd (simt::fwd_kernel)" if f32 else \
-            "fwd (attn_fwd_d256_kernel)" if w.d > 128 else "fwd (attn_fwd_bf16_kernel)"
+            ("fwd (attn_fwd_d256_pair_kernel)" if w.dv > 64 else "fwd (attn_fwd_d256_kernel)") if w.d > 128 else \
+            "fwd (attn_fwd_bf16_kernel)"
     kernels = {fwd_name: {"ms": fwd_ms, "flop": F}}
     if args.fwd_only:
         pass

@@ -358,17 +358,22 @@ attn_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, flo
   if (dtype == ATTN_F32) {
     e = launch_fwd_f32(a);
   } else {
-    // the wide-row forward loads V by 64-key halves of its 128-key tiles
+    // Rows wider than 128 columns: on CTA pairs (each CTA loads 64-key
+    // halves of K and 128-key tiles of half of V's columns) unless the keys
+    // are split or V is 64 columns wide; otherwise the one-CTA kernel, which
+    // loads V by 64-key halves of its 128-key tiles.
     const bool wide = bf16_wide(d, dv);
-    const unsigned v_rows = wide ? 64u : 128u;
+    const bool pair = wide && n_splits == 1 && dv > 64;
+    const unsigned k_rows = pair ? 64u : 128u;
+    const unsigned v_rows = wide && !pair ? 64u : 128u;
     CUtensorMap mq, mk, mv;
     if ((s = make_map(&mq, Q, d, Tq, static_cast<int>(bh))) != ATTN_OK) return s;
-    if ((s = make_map(&mk, K, d, Tk, static_cast<int>(bh))) != ATTN_OK) return s;
+    if ((s = make_map(&mk, K, d, Tk, static_cast<int>(bh), false, k_rows)) != ATTN_OK) return s;
     if ((s = make_map(&mv, V, dv, Tk, static_cast<int>(bh), false, v_rows)) != ATTN_OK) return s;
     a.tmQ = &mq;
     a.tmK = &mk;
     a.tmV = &mv;
-    e = wide ? launch_fwd_bf16_d256(a) : launch_fwd_bf16(a);
+    e = pair ? launch_fwd_bf16_d256_pair(a) : wide ? launch_fwd_bf16_d256(a) : launch_fwd_bf16(a);
     if (e == cudaSuccess && n_splits > 1)
       e = launch_splitkv_merge(p, a.Opart, a.LSEpart, n_splits, split_tiles, O, LSE, di->num_sms, st);
   }

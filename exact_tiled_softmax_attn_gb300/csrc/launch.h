@@ -88,6 +88,10 @@ cudaError_t launch_fwd_bf16(const LaunchFwd& a);
 // d = 256 (dv 64, 128 or 256): one 128-row query tile per unit, 128-key
 // tiles; tmK must be built with 128-row boxes and tmV with 64-row boxes
 cudaError_t launch_fwd_bf16_d256(const LaunchFwd& a);
+// The same on CTA pairs (two 128-row query tiles per cluster of two CTAs;
+// dv above 64, no key split): tmQ with 128-row boxes, tmK with 64-row boxes,
+// tmV with 128-row boxes
+cudaError_t launch_fwd_bf16_d256_pair(const LaunchFwd& a);
 cudaError_t launch_bwd_bf16(const LaunchBwd& a);
 // d = 256 (dv 64, 128 or 256): preprocess, then a dQ kernel and a dV and a dK
 // kernel; needs the 64-row maps tmQ64, tmK64, tmV64, tmdO64 and the 128-row
