@@ -37,6 +37,18 @@
 namespace attn {
 namespace fwd256p {
 
+// D[tmem, both CTAs] (+)= A[smem, each CTA its own rows] * B[smem, split by N]
+// (the shared-memory-A form of ptx::mma_ts_pair)
+__device__ __forceinline__ void mma_ss_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 constexpr int BM = 128;                  // query rows per CTA
 constexpr int BN = 128;                  // keys per tile
 constexpr int HD = 256;                  // Q / K tile width
@@ -216,7 +228,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint64_t b0 = ptx::sdesc_sw128(sKVa + sl * C::SLOT, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk)
-        ptx::mma_ss_pair(d, ptx::sdesc_advance(a0, (kk >> 2) * QBOX + (kk & 3) * 32),
+        mma_ss_pair(d, ptx::sdesc_advance(a0, (kk >> 2) * QBOX + (kk & 3) * 32),
                          ptx::sdesc_advance(b0, (kk >> 2) * KBOX + (kk & 3) * 32), C::IDESC_S, kk > 0 ? 1u : 0u);
     };
     // O (+)= P_g V_g: 8 k-steps over the tile's 128 keys, B = this CTA's
