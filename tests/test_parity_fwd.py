@@ -105,8 +105,9 @@ MIXED_DV_SHAPES = [  # B, H, Tq, Tk, d, dv
 ]
 
 
-D256_SHAPES = [  # B, H, Tq, Tk, dv: d = 256 (one query tile per unit, 128-key tiles)
-    (1, 2, 300, 257, 256),
+D256_SHAPES = [  # B, H, Tq, Tk, dv: d = 256, 128-key tiles; dv > 64 on CTA pairs (two query tiles per unit)
+    (1, 2, 300, 257, 256),    # three query tiles: the second pair's second CTA has no rows
+    (1, 3, 77, 300, 256),     # one query tile: no pair has a second tile
     (2, 1, 129, 700, 128),
     (1, 1, 1, 1, 64),
     (1, 2, 512, 512, 256),
