@@ -367,13 +367,13 @@ def run_ours(args, w):
         pkg.attn_bwd_phase(x["Q"], x["K"], x["V"], o, lse, x["dO"], dq, dk, dvv, B, H, Tq, Tk, d, dv, sc,
                            w.causal, code, det, ws, ws.numel(), ph, stream)
 
-    # backward launch groups in order: preprocess, dQ kernel (deterministic
-    # only; for bf16 rows of up to 128 columns it also forms D), dK/dV kernel,
+    # backward launch groups in order: preprocess, dQ kernel (deterministic,
+    # or any bf16 rows wider than 128 columns; for bf16 it also forms D), dK/dV kernel,
     # dQ conversion or split-dQ reduction; none with --fwd-only. A group that
     # launches nothing for this configuration (the library's own rule, as in
     # attn_bwd_phase) is not called, so that no event interval of the timed
     # step is an empty one.
-    launches = {1: f32 or not det or w.d > 128, 5: bool(det), 6: bool(det), 4: True,
+    launches = {1: f32 or (not det and w.d <= 128), 5: bool(det) or w.d > 128, 6: bool(det), 4: True,
                 3: not f32 and w.d <= 128 and (not det or dq_splits > 1)}
     phases = () if args.fwd_only else tuple(ph for ph in (1, 6 if args.dq_pairs else 5, 4, 3) if launches[ph])
     slot = {1: 1, 5: 2, 6: 2, 4: 3, 3: 4}   # per-step interval of each group: fwd, pre, q, kv, conv
@@ -578,8 +578,8 @@ def run_ours(args, w):
         # dK/dV, convert; fp32: fwd, preprocess, dK/dV, dQ | fwd, preprocess, dK/dV
         "gpu_launches": args.steps * ((1 + (1 if n_splits > 1 else 0)) if args.fwd_only else
                                       (4 if det else 3) if f32 else
-                                      # d = 256: forward, preprocess, dQ, dV, dK kernels
-                                      (5 + (1 if n_splits > 1 else 0)) if w.d > 128 else
+                                      # d = 256: forward, dQ (it forms D), dV, dK kernels
+                                      (4 + (1 if n_splits > 1 else 0)) if w.d > 128 else
                                       ((3 if det else 4) + (1 if n_splits > 1 else 0) +
                                        (1 if det and dq_splits > 1 else 0))),
         "clocks": clk,

@@ -5,13 +5,14 @@
 // stored log-sum-exp ("The Hidden Recurrence in Softmax Attention", section
 // "Flash Attention Backward Pass"):
 //   P = exp(scale Q K^T - LSE), dV = P^T dO, dP = dO V^T, dS = P o (dP - D),
-//   dK = scale dS^T Q, dQ = scale dS K,  D = rowsum(dO o O) (preprocess kernel).
+//   dK = scale dS^T Q, dQ = scale dS K,  D = rowsum(dO o O) (formed by the dQ kernel).
 // With rows of 256 columns the dK and dV accumulators of one 128-key tile
 // fill tensor memory's 512 columns on their own, so the work is split into
 // three kernels, each of which holds one accumulator next to its score tiles:
 //   kv256_kernel<DV, 0>  per 128-key tile: S^T = K Q^T, P^T, dV += P^T dO
 //   kv256_kernel<DV, 1>  per 128-key tile: S^T, dP^T = V dO^T, dS^T, dK += dS^T Q
-//   q256_kernel<DV>      per 128-row query tile: S = Q K^T, dP = dO V^T, dS, dQ += dS K
+//   q256_kernel<DV>      per 128-row query tile: D, then S = Q K^T, dP = dO V^T, dS, dQ += dS K
+// The dQ kernel runs first and stores D and -LSE log2(e) for the other two.
 // The key-tile kernels walk the query rows in steps of 64 and the query-tile
 // kernel the keys in steps of 64, so that the 256-column accumulator, the
 // 128 columns of the resident operand (K or Q as packed bf16, the A operand
@@ -543,14 +544,16 @@ __global__ void __launch_bounds__(THREADS, 1)
 template <int DV>
 struct CfgQ {
   static constexpr int DORES = BT * DV * 2;   // dO of the unit (A operand of dP), 128-row boxes
-  static constexpr int NSLOT_FIT = (227 * 1024 - DORES - 512) / SLOT;
+  static constexpr int DPART_BYTES = 2 * 2 * BT * 4;   // [unit parity][row group][128] fp32 partial D
+  static constexpr int NSLOT_FIT = (227 * 1024 - DORES - DPART_BYTES - 512) / SLOT;
   static constexpr int NSLOT = NSLOT_FIT < 16 ? NSLOT_FIT : 16;
   static constexpr int OFF_DO = 0;
   static constexpr int OFF_RING = OFF_DO + DORES;
-  static constexpr int OFF_BAR = OFF_RING + NSLOT * SLOT;
+  static constexpr int OFF_DPART = OFF_RING + NSLOT * SLOT;
+  static constexpr int OFF_BAR = OFF_DPART + DPART_BYTES;
   // full[NSLOT], empty[NSLOT], q_ready, do_full, do_empty, s_full, s_free, dp_full, ds_full, dq_full,
-  // dq_free, drain
-  static constexpr int NBAR = 2 * NSLOT + 10;
+  // dq_free, drain, dpart_full
+  static constexpr int NBAR = 2 * NSLOT + 11;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16;
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16(BT, NS, false, false);   // S, dP: N = 64 keys
@@ -572,7 +575,7 @@ template <int DV>
 __global__ void __launch_bounds__(THREADS, 1)
     q256_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant__ CUtensorMap tmK64,
                 const __grid_constant__ CUtensorMap tmV64, const __grid_constant__ CUtensorMap tmdO,
-                const Params P) {
+                const __grid_constant__ CUtensorMap tmO64, const Params P) {
   using C = CfgQ<DV>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
@@ -596,6 +599,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* dq_full = q_ready + 7;
   uint64_t* dq_free = q_ready + 8;        // the epilogue has read the dQ accumulator
   uint64_t* drain = q_ready + 9;
+  uint64_t* dpart_full = q_ready + 10;    // both row groups wrote a unit's partial D
+  float* dpart = reinterpret_cast<float*>(smem + C::OFF_DPART);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
   if (threadIdx.x == 0) {
@@ -605,7 +610,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     ptx::mbar_init(q_ready, 256);
     ptx::mbar_init(do_full, 1);
-    ptx::mbar_init(do_empty, 1);
+    // the unit's last dP product has read dO, and the row threads have formed D from it
+    ptx::mbar_init(do_empty, 2);
     ptx::mbar_init(s_full, 1);
     ptx::mbar_init(s_free, 256);
     ptx::mbar_init(dp_full, 1);
@@ -613,6 +619,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     ptx::mbar_init(dq_full, 1);
     ptx::mbar_init(dq_free, 256);
     ptx::mbar_init(drain, 1);
+    ptx::mbar_init(dpart_full, 256);
     *abort_flag = 0u;
     ptx::fence_mbar_init();
   }
@@ -626,8 +633,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const int grid = gridDim.x, cta = blockIdx.x;
   const int Tq = P.p.Tq, Tk = P.p.Tk;
-  // Ring items: per unit the halves of its Q tile at i0, i0 + 1, then per key
-  // step s the 64 rows of K at i0 + 2 + 2s and of V at i0 + 3 + 2s.
+  // Ring items: per unit the halves of its Q tile at i0, i0 + 1 and of its O
+  // tile at i0 + 2, i0 + 3, then per key step s the 64 rows of K at
+  // i0 + 4 + 2s and of V at i0 + 5 + 2s.
   auto slot = [](uint32_t i) { return static_cast<int>(i % C::NSLOT); };
   auto par = [](uint32_t i) { return (i / C::NSLOT) & 1u; };
 
@@ -638,6 +646,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     ptx::tma_prefetch_desc(&tmK64);
     ptx::tma_prefetch_desc(&tmV64);
     ptx::tma_prefetch_desc(&tmdO);
+    ptx::tma_prefetch_desc(&tmO64);
     uint32_t item = 0, u_it = 0, d_issued = 0;
     bool ok = true;
     int bh, qt;
@@ -652,9 +661,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int round = 0; ok && P.order.unit(cta, grid, round, &bh, &qt); ++round) {
       const int ns = q_steps(P, qt);
       if (ns == 0) continue;
-      ok = load(&tmQ64, HD / 64, 64 * HD * 2, qt * BT) && load(&tmQ64, HD / 64, 64 * HD * 2, qt * BT + 64);
+      ok = load(&tmQ64, HD / 64, 64 * HD * 2, qt * BT) && load(&tmQ64, HD / 64, 64 * HD * 2, qt * BT + 64) &&
+           load(&tmO64, DV / 64, 64 * DV * 2, qt * BT) && load(&tmO64, DV / 64, 64 * DV * 2, qt * BT + 64);
       if (!ok) break;
-      // dO of the unit, once the previous unit's last dP product has read it
+      // dO of the unit, once the previous unit's last dP product and D have read it
       if (!(ok = ptx::mbar_wait(do_empty, (u_it & 1u) ^ 1u, w))) break;
       ptx::mbar_arrive_expect_tx(do_full, BT * DV * 2);
       for (int b = 0; b < DV / 64; ++b) ptx::tma_load_3d(sdO + b * BOX128, &tmdO, do_full, b * 64, qt * BT, bh);
@@ -703,23 +713,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         ptx::mbar_arrive(empty + slot(i0 + 1));
       }
       __syncwarp();
-      if (!(ok = wait(full + slot(i0 + 2), par(i0 + 2)))) break;
+      if (!(ok = wait(full + slot(i0 + 4), par(i0 + 4)))) break;
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
         moved |= lane != 0;
-        mma_s(i0 + 2);
+        mma_s(i0 + 4);
       }
       __syncwarp();
       if (!(ok = wait(do_full, u_it & 1u))) break;
-      if (!(ok = wait(full + slot(i0 + 3), par(i0 + 3)))) break;
+      if (!(ok = wait(full + slot(i0 + 5), par(i0 + 5)))) break;
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
         moved |= lane != 0;
-        mma_dp(i0 + 3, ns == 1);
+        mma_dp(i0 + 5, ns == 1);
       }
       __syncwarp();
       for (int s = 0; ok && s < ns; ++s, ++gs) {
-        const uint32_t ik = i0 + 2 + 2 * s;   // K_s; K_{s+1} = ik + 2, V_{s+1} = ik + 3
+        const uint32_t ik = i0 + 4 + 2 * s;   // K_s; K_{s+1} = ik + 2, V_{s+1} = ik + 3
         if (s + 1 < ns) {
           if (!(ok = wait(s_free, gs & 1u))) break;
           if (!(ok = wait(full + slot(ik + 2), par(ik + 2)))) break;
@@ -760,7 +770,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         ptx::mma_commit(dq_full);
       }
       __syncwarp();
-      item = i0 + 2 + 2 * ns;
+      item = i0 + 4 + 2 * ns;
       ++u_it;
     }
     if (!ok) {
@@ -789,9 +799,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t i0 = item;
       const int q = qt * BT + r;
       const bool q_ok = q < Tq;
-      // -LSE*log2(e) and D of this row (the preprocess kernel wrote them; -inf and 0 past Tq)
-      const float nlse2 = P.NLSE2[static_cast<size_t>(bh) * P.Tq_pad + q];
-      const float dd = P.D[static_cast<size_t>(bh) * P.Tq_pad + q];
+      // -LSE*log2(e) of this row (-inf past Tq and for rows without keys)
+      const float lse = q_ok ? P.LSE[static_cast<size_t>(bh) * Tq + q] : -CUDART_INF_F;
+      const float nlse2 = lse == -CUDART_INF_F ? -CUDART_INF_F : -lse * LOG2E;
       // stage this group's half of Q row r (d columns [128g, 128g + 128)) into TMEM
       for (int h = 0; h < 2; ++h)
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(full + slot(i0 + h), par(i0 + h), w)))) break;
@@ -816,6 +826,51 @@ __global__ void __launch_bounds__(THREADS, 1)
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       ptx::mbar_arrive(q_ready);
+      // D = rowsum(dO o O) of this row ("attention_backprop", section
+      // "Gradient of S"): this group's half of the dv columns from the
+      // resident dO and the unit's O items, the two halves added through
+      // shared memory (rows past Tq load as zeros, so their D is 0). Group 0
+      // stores D and -LSE*log2(e) into the padded arrays the dV and dK
+      // kernels read after this kernel.
+      float dd;
+      {
+        if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(do_full, u_it & 1u, w)))) break;
+        for (int h = 0; h < 2; ++h)
+          if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(full + slot(i0 + 2 + h), par(i0 + 2 + h), w)))) break;
+        if (!ok) break;
+        const uint8_t* so = ring + slot(i0 + 2 + (r >> 6)) * SLOT;
+        const int rl = r & 63;
+        float part = 0.f;
+#pragma unroll
+        for (int k = 0; k < DV / 16; ++k) {
+          const int c = (DV / 2) * g + 8 * k;
+          const uint4 x = *reinterpret_cast<const uint4*>(sdO + bwd::sw128_offset(r, c));
+          const uint4 o = *reinterpret_cast<const uint4*>(so + bwd::sw128_offset64(rl, c));
+          const __nv_bfloat162* dv2 = reinterpret_cast<const __nv_bfloat162*>(&x);
+          const __nv_bfloat162* ov2 = reinterpret_cast<const __nv_bfloat162*>(&o);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 a = __bfloat1622float2(ov2[e]), b = __bfloat1622float2(dv2[e]);
+            part = fmaf(a.x, b.x, part);
+            part = fmaf(a.y, b.y, part);
+          }
+        }
+        float* dpu = dpart + (u_it & 1u) * 2 * BT;
+        dpu[g * BT + r] = part;
+        ptx::mbar_arrive(dpart_full);
+        if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(dpart_full, u_it & 1u, w)))) break;
+        dd = dpu[r] + dpu[BT + r];
+        if (g == 0) {   // every row of the padded tile: the dV and dK kernels read whole slices
+          P.D[static_cast<size_t>(bh) * P.Tq_pad + q] = dd;
+          P.NLSE2[static_cast<size_t>(bh) * P.Tq_pad + q] = nlse2;
+        }
+        if (threadIdx.x == 64) {
+          // every row thread has read the O items and dO for D
+          ptx::mbar_arrive(empty + slot(i0 + 2));
+          ptx::mbar_arrive(empty + slot(i0 + 3));
+          ptx::mbar_arrive(do_empty);
+        }
+      }
       for (int s = 0; s < ns; ++s, ++gs) {
         if (!(ok = __all_sync(0xffffffffu, ptx::mbar_wait(s_full, gs & 1u, w)))) break;
         ptx::tc_fence_after();
@@ -878,7 +933,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(dq_free);
-      item = i0 + 2 + 2 * ns;
+      item = i0 + 4 + 2 * ns;
       ++u_it;
     }
   }
@@ -910,7 +965,7 @@ cudaError_t launch_t(const LaunchBwd& a, Params P) {
     const int grid = units < a.num_sms ? static_cast<int>(units) : a.num_sms;
     auto kq = q256_kernel<DV>;
     if ((e = prep(kq, CfgQ<DV>::SMEM)) != cudaSuccess) return e;
-    kq<<<grid, THREADS, CfgQ<DV>::SMEM, a.stream>>>(*a.tmQ64, *a.tmK64, *a.tmV64, *a.tmdO, P);
+    kq<<<grid, THREADS, CfgQ<DV>::SMEM, a.stream>>>(*a.tmQ64, *a.tmK64, *a.tmV64, *a.tmdO, *a.tmO64, P);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (all || a.phase == 4) {
@@ -931,16 +986,11 @@ cudaError_t launch_t(const LaunchBwd& a, Params P) {
 
 }  // namespace bwd256
 
-// The bf16 backward for d = 256 (dv 64, 128 or 256): the preprocess (phase 1:
-// D and -LSE * log2(e)), the dQ kernel (phase 5), the dV and dK kernels
-// (phase 4); dQ is written directly (no conversion phase).
+// The bf16 backward for d = 256 (dv 64, 128 or 256): the dQ kernel (phase 5),
+// which also forms D and -LSE * log2(e), then the dV and dK kernels (phase 4);
+// dQ is written directly (no conversion phase) and phase 1 launches nothing.
 cudaError_t launch_bwd_bf16_d256(const LaunchBwd& a) {
   const Problem& p = a.p;
-  cudaError_t e;
-  if (a.phase == 0 || a.phase == 1) {
-    e = launch_bwd_preprocess(p, a.O, a.dO, a.LSE, 2, a.D, a.NLSE2, nullptr, 0, a.num_sms, a.stream);
-    if (e != cudaSuccess) return e;
-  }
   bwd::Params P{};
   P.p = p;
   P.NLSE2 = a.NLSE2;

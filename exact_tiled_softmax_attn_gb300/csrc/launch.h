@@ -93,9 +93,9 @@ cudaError_t launch_fwd_bf16_d256(const LaunchFwd& a);
 // tmV with 128-row boxes
 cudaError_t launch_fwd_bf16_d256_pair(const LaunchFwd& a);
 cudaError_t launch_bwd_bf16(const LaunchBwd& a);
-// d = 256 (dv 64, 128 or 256): preprocess, then a dQ kernel and a dV and a dK
-// kernel; needs the 64-row maps tmQ64, tmK64, tmV64, tmdO64 and the 128-row
-// tmV, tmdO
+// d = 256 (dv 64, 128 or 256): a dQ kernel (which also forms D), then a dV
+// and a dK kernel; needs the 64-row maps tmQ64, tmK64, tmV64, tmdO64, tmO64
+// and the 128-row tmV, tmdO
 cudaError_t launch_bwd_bf16_d256(const LaunchBwd& a);
 
 // O, LSE from the split-KV partials (rows of query tile qt read the splits

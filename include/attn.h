@@ -207,14 +207,17 @@ ATTN_API attn_status_t attn_bwd(const void* Q, const void* K, const void* V, con
  * arguments as attn_bwd plus `phase`:
  *   1  preprocess: D = rowsum(dO o O) and -LSE * log2(e) (and zeroing of the
  *      fp32 dQ accumulator when deterministic == 0); a no-op for bf16 with
- *      deterministic == 1, where the dQ kernel forms D itself
+ *      deterministic == 1 and for bf16 rows wider than 128 columns, where
+ *      the dQ kernel forms D itself
  *   2  main kernels: phases 5 and 4 in this order
  *   3  dQ conversion from the fp32 accumulator (bf16 with deterministic
  *      == 0), or the in-order sum of the split dQ partials (bf16 with
  *      deterministic == 1 and attn_bwd_dq_splits(...) > 1); a no-op otherwise
- *   4  the dK/dV kernel alone (with deterministic == 0 it also accumulates dQ)
- *   5  the separate dQ kernel alone (deterministic == 1; a no-op otherwise);
- *      for bf16 it also writes the D and -LSE * log2(e) phase 4 reads
+ *   4  the dK/dV kernel alone (with deterministic == 0 it also accumulates dQ;
+ *      bf16 rows wider than 128 columns: the dV and the dK kernel)
+ *   5  the separate dQ kernel alone (deterministic == 1, or bf16 rows wider
+ *      than 128 columns; a no-op otherwise); for bf16 it also writes the D
+ *      and -LSE * log2(e) phase 4 reads
  *   6  in place of phase 5, the same dQ pass on CTA pairs: two 128-row query
  *      tiles per cluster of two CTAs, each tensor-core product computed for
  *      both at once with the K and V operands split between the two SMs

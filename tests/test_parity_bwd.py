@@ -296,7 +296,8 @@ def test_bf16_inputs_unchanged():
 
 
 @pytest.mark.parametrize("dt,d,Tq,Tk", [(torch.float32, 64, 515, 515), (torch.bfloat16, 128, 515, 515),
-                                        (torch.bfloat16, 128, 128, 4096)])   # the last: split dQ when deterministic
+                                        (torch.bfloat16, 128, 128, 4096),    # split dQ when deterministic
+                                        (torch.bfloat16, 256, 300, 333)])    # rows of 256: D formed in phase 5
 @pytest.mark.parametrize("deterministic", [0, 1])
 def test_phases_equal_one_call(dt, d, Tq, Tk, deterministic):
     # preprocess, dQ kernel, dK/dV kernel, dQ conversion / split reduction
