@@ -300,9 +300,11 @@ __device__ __forceinline__ void p_ds(float sh, float sl, float dp, float scale, 
 // that see the key tile, computes S^T = K Q^T (Dot2) and dP^T = V dO^T for
 // the tile, and accumulates dV += P^T dO and dK += dS^T Q in registers
 // (rows of keys ty + 16 r). Unless `with_dq` is 0 it also adds this key
-// tile's share scale * dS K into dQ with fp32 atomics.
-template <int W, int BQ>
-__global__ void __launch_bounds__(NT) dkdv_kernel(const BwdArgs a, int with_dq) {
+// tile's share scale * dS K into dQ with fp32 atomics. ONE_BUF: P^T and
+// dS^T take turns in one shared buffer (P^T for the dV product, then dS^T
+// over it), so that two CTAs fit per SM.
+template <int W, int BQ, bool ONE_BUF>
+__global__ void __launch_bounds__(NT, (ONE_BUF || W == 64) ? 2 : 1) dkdv_kernel(const BwdArgs a, int with_dq) {
   constexpr int LD = W + 1, LDP = BQ + 1, NC = BQ / 16, NQ = W / 16;
   extern __shared__ float smem_f[];
   float* sK = smem_f;             // [BM][LD]
@@ -310,7 +312,7 @@ __global__ void __launch_bounds__(NT) dkdv_kernel(const BwdArgs a, int with_dq) 
   float* sQ = sV + BM * LD;       // [BQ][LD]
   float* sdO = sQ + BQ * LD;      // [BQ][LD]
   float* sPt = sdO + BQ * LD;     // [BM][LDP]  P^T: key rows, query columns
-  float* sdSt = sPt + BM * LDP;   // [BM][LDP]
+  float* sdSt = ONE_BUF ? sPt : sPt + BM * LDP;   // [BM][LDP]
   float* sLse = sdSt + BM * LDP;  // [BQ]
   float* sD = sLse + BQ;          // [BQ]
   const Problem& p = a.p;
@@ -341,6 +343,7 @@ __global__ void __launch_bounds__(NT) dkdv_kernel(const BwdArgs a, int with_dq) 
       sD[threadIdx.x] = qi < Tq ? a.D[bh * padded_rows(Tq) + qi] : 0.f;
     }
     __syncthreads();
+    float ds_keep[4][NC];   // ONE_BUF: dS^T waits in registers until the dV product is done with P^T
     {
       float sh[4][NC], sl[4][NC], dp[4][NC];
       dot2_tile<NC>(sK, sQ, LD, ty, tx, d, sh, sl);
@@ -356,7 +359,10 @@ __global__ void __launch_bounds__(NT) dkdv_kernel(const BwdArgs a, int with_dq) 
           float pij, dsij;
           p_ds(sh[r][c], sl[r][c], dp[r][c], scale, lse, sD[i], blocked, pij, dsij);
           sPt[(ty + 16 * r) * LDP + i] = pij;
-          sdSt[(ty + 16 * r) * LDP + i] = dsij;
+          if constexpr (ONE_BUF)
+            ds_keep[r][c] = dsij;
+          else
+            sdSt[(ty + 16 * r) * LDP + i] = dsij;
         }
       }
     }
@@ -364,6 +370,14 @@ __global__ void __launch_bounds__(NT) dkdv_kernel(const BwdArgs a, int with_dq) 
     // dV_j += sum_i P_ij dO_i ; dK_j += sum_i dS_ij Q_i
     const int nq = min(BQ, Tq - q0);
     acc_tile<4, NQ>(sPt, LDP, sdO, LD, ty, tx, nq, accV);
+    if constexpr (ONE_BUF) {
+      __syncthreads();   // every thread is done reading P^T
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < NC; ++c) sdSt[(ty + 16 * r) * LDP + tx + 16 * c] = ds_keep[r][c];
+      __syncthreads();
+    }
     acc_tile<4, NQ>(sdSt, LDP, sQ, LD, ty, tx, nq, accK);
     if (with_dq) {
       // dQ_i += scale * sum_j dS_ij K_j, rows of queries ty + 16 r
@@ -487,14 +501,17 @@ __global__ void __launch_bounds__(NT) dq_kernel(const BwdArgs a) {
 // d=128: 5.14 -> 4.60 ms), where 32-query steps made the dK/dV kernel
 // slower (5.20 -> 5.57 ms) and W = 64 problems gain nothing.
 template <int W>
-constexpr int dkdv_rows() { return W > 128 ? 32 : 64; }
+constexpr int dkdv_rows() { return W >= 128 ? 32 : 64; }
+// one buffer for P^T and dS^T at W = 128: two CTAs per SM
+template <int W>
+constexpr bool dkdv_one_buf() { return W == 128; }
 template <int W>
 constexpr int dq_rows() { return W >= 128 ? 32 : 64; }
 
 template <int W>
 constexpr size_t dkdv_smem() {
   constexpr int BQ = dkdv_rows<W>();
-  return sizeof(float) * (2 * BM * (W + 1) + 2 * BQ * (W + 1) + 2 * BM * (BQ + 1) + 2 * BQ);
+  return sizeof(float) * (2 * BM * (W + 1) + 2 * BQ * (W + 1) + (dkdv_one_buf<W>() ? 1 : 2) * BM * (BQ + 1) + 2 * BQ);
 }
 template <int W>
 constexpr size_t dq_smem() {
@@ -510,10 +527,12 @@ cudaError_t bwd_launch(const LaunchBwd& la, const BwdArgs& b, bool kv, bool q) {
   const Problem& p = la.p;
   cudaError_t e;
   if (kv && p.Tk > 0) {
-    e = cudaFuncSetAttribute(dkdv_kernel<W, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s1));
+    constexpr bool OB = dkdv_one_buf<W>();
+    e = cudaFuncSetAttribute(dkdv_kernel<W, R, OB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(s1));
     if (e != cudaSuccess) return e;
     dim3 g1((p.Tk + BM - 1) / BM, p.B * p.H);
-    dkdv_kernel<W, R><<<g1, NT, s1, la.stream>>>(b, la.deterministic ? 0 : 1);
+    dkdv_kernel<W, R, OB><<<g1, NT, s1, la.stream>>>(b, la.deterministic ? 0 : 1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (q) {
