@@ -502,7 +502,7 @@ def run_ours(args, w):
     # under "executed").
     md, mv = w.pair_flop() * w.d, w.pair_flop() * w.dv
     if f32:
-        # the CUDA-core path: FP32 FMA throughput (its scores accumulate compensated)
+        # the CUDA-core path: FP32 FMA throughput (its scores are formed beyond fp32 precision)
         props = torch.cuda.get_device_properties(dev)
         peak = props.multi_processor_count * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
     tag = "simt::" if f32 else ""

@@ -78,7 +78,7 @@ struct LaunchBwd {
   cudaStream_t stream;
 };
 
-// fp32 (SIMT, compensated score accumulation); d, dv <= 256
+// fp32 (SIMT; scores as float pairs from split rows or a compensated dot); d, dv <= 256
 cudaError_t launch_fwd_f32(const LaunchFwd& a);
 size_t fwd_f32_smem_bytes(int block_n, int d, int dv);   // dynamic shared memory of one forward CTA
 cudaError_t launch_bwd_f32(const LaunchBwd& a);

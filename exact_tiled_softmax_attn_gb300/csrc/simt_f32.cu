@@ -5,15 +5,22 @@
 // sections "Gradient of V and P", "Gradient of S", "Gradient of Q and K"),
 // for fp32 inputs of any head size up to 256.
 //
-// Precision: a score q.k is accumulated in twice the fp32 precision (the
-// compensated dot product below) and kept as an unevaluated sum hi + lo of
-// two floats; scale * (hi + lo) - m is formed from the exact product of hi
-// and scale (one FMA gives its rounding error), so the argument of exp is
-// accurate to about one rounding of its own size even when the logits are in
-// the thousands. Accumulating s in plain fp32 instead leaves a logit error of
+// Precision: a score q.k is formed well beyond fp32 precision and kept as an
+// unevaluated sum hi + lo of two floats; scale * (hi + lo) - m is formed from
+// the exact product of hi and scale (one FMA gives its rounding error), so
+// the argument of exp stays accurate even when the logits are in the
+// thousands. Accumulating s in plain fp32 instead leaves a logit error of
 // ~1e-5..1e-4 once |s| reaches the hundreds (keys scaled by +-40), which the
 // softmax turns into output errors above 1e-5. Everything after the exponent
-// (P, sums, P V, dP, dS, dQ, dK, dV) is fp32.
+// (P, sums, P V, dP, dS, dQ, dK, dV) is fp32. Two ways of forming the score
+// pair, chosen per kernel by whether its tiles fit in shared memory:
+//  - split rows (rows up to 128 columns): every q and k row is split
+//    exactly into a coarse part on a power-of-two grid set by the row's
+//    largest entry plus a remainder; the coarse products then sum exactly in
+//    fp32, and only the small cross terms round (3 FMAs per multiply-add);
+//  - the compensated dot product Dot2 (10 FP32 instructions per
+//    multiply-add) where the extra split rows do not fit (256 columns, and
+//    128-key forward tiles of 128-column rows).
 //
 // Layout of the work: 256 threads per CTA as a 16 x 16 grid (ty, tx); a
 // thread owns rows ty + 16 r (r < 4) of a 64-row tile and columns tx + 16 c
@@ -59,6 +66,114 @@ __device__ __forceinline__ void dot2_step(float a, float b, float& s, float& c) 
 __device__ __forceinline__ void scale_pair(float hi, float lo, float scale, float& ph, float& pl) {
   ph = __fmul_rn(hi, scale);
   pl = __fadd_rn(__fmaf_rn(hi, scale, -ph), __fmul_rn(lo, scale));
+}
+
+// Exact split of a row x into x = hi + lo (the error-free splitting of
+// Ozaki, Ogita, Oishi and Rump, "Error-free transformations of matrix
+// multiplication by using fast routines of matrix multiplication and its
+// applications", Numer. Algorithms 59, 2012, restated for rows of at most
+// 256 entries). With E the exponent of the row's largest |x| (2^E <= max
+// |x| < 2^(E+1)) and u = 2^(E-7), hi = rint(x / u) u is an integer multiple
+// n u with |n| <= 256, and lo = x - hi, |lo| <= u / 2, is exact in fp32.
+// For two split rows q, k of n <= 256 entries every partial sum of
+// hq_i hk_i is an integer multiple of uq uk below 2^24 of them in magnitude,
+// so the fp32 sum of the coarse products is exact (as long as uq uk does not
+// underflow, i.e. outside rows whose largest entries multiply to below
+// ~2^-120); q.k = sum hq hk + sum (hq lk + lq k) with only the second sum,
+// whose terms are 2^-8 of the scale of q.k, rounded.
+// u and 1/u for a row whose largest |x| is m (>= 0): powers of two, both
+// normal (rows below 2^-119 take u = 2^-126; inf and NaN are not split).
+__device__ __forceinline__ void split_grid(float m, float& u, float& inv) {
+  int eb = static_cast<int>((__float_as_uint(m) >> 23) & 0xffu);   // E + 127
+  eb = min(max(eb, 8), 254);
+  u = __uint_as_float(static_cast<uint32_t>(eb - 7) << 23);     // 2^(E - 7)
+  inv = __uint_as_float(static_cast<uint32_t>(261 - eb) << 23);  // 2^(7 - E)
+}
+
+// Rows [0, ROWS) of a [T][cols] fp32 block (src at its first row) split
+// as above into shared memory with rows of ld floats: hi to xh, lo to xl and,
+// if xf is not null, x itself to xf; rows at or past `valid` and columns
+// [cols, W) as zeros. Warp w takes rows w, w + 8, ...; all of a warp's loads
+// are issued before its first row maximum.
+template <int W, int ROWS>
+__device__ __forceinline__ void load_split(float* xf, float* xh, float* xl, int ld, const float* src, int cols,
+                                           int valid) {
+  constexpr int NW = NT / 32, PER = W / 32, RW = ROWS / NW;
+  static_assert(ROWS % NW == 0, "rows per warp");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float v[RW][PER];
+#pragma unroll
+  for (int i = 0; i < RW; ++i) {
+    const int r = warp + NW * i;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int c = lane + 32 * j;
+      v[i][j] = (r < valid && c < cols) ? src[static_cast<size_t>(r) * cols + c] : 0.f;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < RW; ++i) {
+    const int r = warp + NW * i;
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) m = fmaxf(m, fabsf(v[i][j]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float u, inv;
+    split_grid(m, u, inv);
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int c = lane + 32 * j;
+      const float hi = __fmul_rn(rintf(__fmul_rn(v[i][j], inv)), u);
+      xh[r * ld + c] = hi;
+      xl[r * ld + c] = __fsub_rn(v[i][j], hi);
+      if (xf != nullptr) xf[r * ld + c] = v[i][j];
+    }
+  }
+}
+
+// S[r][c] = sum_k A[ra + 16 r][k] B[cb + 16 c][k] over k < n from split
+// rows, as s (the exact sum of the coarse products) + e (the cross terms):
+// Ah, Al the A rows' parts, Bh, Bl the B rows'. FULL_A: e sums Al Bh + A Bl
+// (A the unsplit A rows; B unused), else Ah Bl + Al B (A unused).
+template <int C, bool FULL_A>
+__device__ __forceinline__ void split_tile(const float* A, const float* Ah, const float* Al, const float* B,
+                                           const float* Bh, const float* Bl, int ld, int ra, int cb, int n,
+                                           float (&s)[4][C], float (&e)[4][C]) {
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < C; ++c) s[r][c] = e[r][c] = 0.f;
+  const int ao = ra * ld, bo = cb * ld;
+#pragma unroll 2
+  for (int k = 0; k < n; ++k) {
+    float ah[4], al[4], af[4], bh[C], bl[C], bf[C];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      ah[r] = Ah[ao + 16 * r * ld + k];
+      al[r] = Al[ao + 16 * r * ld + k];
+      if constexpr (FULL_A) af[r] = A[ao + 16 * r * ld + k];
+    }
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+      bh[c] = Bh[bo + 16 * c * ld + k];
+      bl[c] = Bl[bo + 16 * c * ld + k];
+      if constexpr (!FULL_A) bf[c] = B[bo + 16 * c * ld + k];
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c = 0; c < C; ++c) {
+        s[r][c] = __fmaf_rn(ah[r], bh[c], s[r][c]);   // exact
+        if constexpr (FULL_A) {
+          e[r][c] = __fmaf_rn(al[r], bh[c], e[r][c]);
+          e[r][c] = __fmaf_rn(af[r], bl[c], e[r][c]);
+        } else {
+          e[r][c] = __fmaf_rn(ah[r], bl[c], e[r][c]);
+          e[r][c] = __fmaf_rn(al[r], bf[c], e[r][c]);
+        }
+      }
+  }
 }
 
 // S[r][c] = sum_k A[ra + 16 r][k] B[cb + 16 c][k] over k < n, by Dot2: hi in
@@ -162,23 +277,30 @@ __host__ __device__ inline int tile_width(int d, int dv) {
 
 // One CTA per (64-row query tile, head); key tiles of BN keys in ascending
 // order through the online softmax; O (4 x W/16 per thread) in registers.
-template <int W, int BN>
+// SPLIT: scores from split rows (Q whole and split, K split), else by Dot2.
+template <int W, int BN, bool SPLIT>
 __global__ void __launch_bounds__(NT) fwd_kernel(const float* __restrict__ Q, const float* __restrict__ K,
                                                  const float* __restrict__ V, float* __restrict__ O,
                                                  float* __restrict__ LSE, const Problem p) {
   constexpr int LD = W + 1, LDP = BN + 1, NC = BN / 16, NQ = W / 16;
   extern __shared__ float smem_f[];
-  float* sQ = smem_f;           // [BM][LD]
-  float* sK = sQ + BM * LD;     // [BN][LD]
-  float* sV = sK + BN * LD;     // [BN][LD]
-  float* sP = sV + BN * LD;     // [BM][LDP]
+  float* sQ = smem_f;                              // [BM][LD]
+  float* sQh = sQ + BM * LD;                       // split: [BM][LD] coarse parts of Q, then remainders
+  float* sQl = sQh + BM * LD;
+  float* sK = sQ + (SPLIT ? 3 : 1) * BM * LD;      // [BN][LD] K (split: its coarse parts, then remainders)
+  float* sKl = sK + BN * LD;
+  float* sV = sK + (SPLIT ? 2 : 1) * BN * LD;      // [BN][LD]
+  float* sP = sV + BN * LD;                        // [BM][LDP]
   const int d = p.d, dv = p.dv, Tq = p.Tq, Tk = p.Tk;
   const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
   const int q0 = blockIdx.x * BM;
   const size_t bh = blockIdx.y;
   const float scale = p.scale;
 
-  load_tile<W>(sQ, LD, Q + (bh * Tq + q0) * d, BM, d, Tq - q0);
+  if constexpr (SPLIT)
+    load_split<W, BM>(sQ, sQh, sQl, LD, Q + (bh * Tq + q0) * d, d, Tq - q0);
+  else
+    load_tile<W>(sQ, LD, Q + (bh * Tq + q0) * d, BM, d, Tq - q0);
   float acc[4][NQ], m[4], l[4];
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
@@ -193,11 +315,17 @@ __global__ void __launch_bounds__(NT) fwd_kernel(const float* __restrict__ Q, co
   for (int jt = 0; jt < n_kv; ++jt) {
     const int kv0 = jt * BN;
     __syncthreads();   // the previous tile's P V is done with sK, sV, sP
-    load_tile<W>(sK, LD, K + (bh * Tk + kv0) * d, BN, d, Tk - kv0);
+    if constexpr (SPLIT)
+      load_split<W, BN>(nullptr, sK, sKl, LD, K + (bh * Tk + kv0) * d, d, Tk - kv0);
+    else
+      load_tile<W>(sK, LD, K + (bh * Tk + kv0) * d, BN, d, Tk - kv0);
     load_tile<W>(sV, LD, V + (bh * Tk + kv0) * dv, BN, dv, Tk - kv0);
     __syncthreads();
     float sh[4][NC], sl[4][NC];
-    dot2_tile<NC>(sQ, sK, LD, ty, tx, d, sh, sl);
+    if constexpr (SPLIT)
+      split_tile<NC, true>(sQ, sQh, sQl, nullptr, sK, sKl, LD, ty, tx, d, sh, sl);
+    else
+      dot2_tile<NC>(sQ, sK, LD, ty, tx, d, sh, sl);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int qi = q0 + ty + 16 * r;
@@ -249,20 +377,28 @@ __global__ void __launch_bounds__(NT) fwd_kernel(const float* __restrict__ Q, co
   }
 }
 
-template <int W, int BN>
-constexpr size_t fwd_smem() {
-  return sizeof(float) * (BM * (W + 1) + 2 * BN * (W + 1) + BM * (BN + 1));
+constexpr size_t kSmemMax = 227 * 1024;
+
+template <int W, int BN, bool SPLIT>
+constexpr size_t fwd_smem_of() {
+  return sizeof(float) * ((SPLIT ? 3 : 1) * BM * (W + 1) + (SPLIT ? 3 : 2) * BN * (W + 1) + BM * (BN + 1));
 }
+// split rows wherever their tiles fit
+template <int W, int BN>
+constexpr bool fwd_split() { return fwd_smem_of<W, BN, true>() <= kSmemMax; }
+template <int W, int BN>
+constexpr size_t fwd_smem() { return fwd_smem_of<W, BN, fwd_split<W, BN>()>(); }
 
 template <int W, int BN>
 cudaError_t fwd_launch(const LaunchFwd& a) {
+  constexpr bool SP = fwd_split<W, BN>();
   constexpr size_t smem = fwd_smem<W, BN>();
-  static_assert(smem <= 227 * 1024, "shared memory");
-  cudaError_t e =
-      cudaFuncSetAttribute(fwd_kernel<W, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  static_assert(smem <= kSmemMax, "shared memory");
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<W, BN, SP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid((a.p.Tq + BM - 1) / BM, a.p.B * a.p.H);
-  fwd_kernel<W, BN><<<grid, NT, smem, a.stream>>>(static_cast<const float*>(a.Q), static_cast<const float*>(a.K),
+  fwd_kernel<W, BN, SP><<<grid, NT, smem, a.stream>>>(static_cast<const float*>(a.Q), static_cast<const float*>(a.K),
                                                   static_cast<const float*>(a.V), static_cast<float*>(a.O), a.LSE,
                                                   a.p);
   return cudaGetLastError();
@@ -297,20 +433,25 @@ __device__ __forceinline__ void p_ds(float sh, float sl, float dp, float scale, 
 }
 
 // One CTA per (64-key tile, head): loops over the query tiles (BQ rows each)
-// that see the key tile, computes S^T = K Q^T (Dot2) and dP^T = V dO^T for
+// that see the key tile, computes S^T = K Q^T and dP^T = V dO^T for
 // the tile, and accumulates dV += P^T dO and dK += dS^T Q in registers
 // (rows of keys ty + 16 r). Unless `with_dq` is 0 it also adds this key
 // tile's share scale * dS K into dQ with fp32 atomics. ONE_BUF: P^T and
 // dS^T take turns in one shared buffer (P^T for the dV product, then dS^T
-// over it), so that two CTAs fit per SM.
-template <int W, int BQ, bool ONE_BUF>
-__global__ void __launch_bounds__(NT, (ONE_BUF || W == 64) ? 2 : 1) dkdv_kernel(const BwdArgs a, int with_dq) {
+// over it), so that two CTAs fit per SM. SPLIT: scores from split rows (K
+// split, Q whole and split), else by Dot2.
+template <int W, int BQ, bool ONE_BUF, bool SPLIT>
+__global__ void __launch_bounds__(NT, (!SPLIT && (ONE_BUF || W == 64)) ? 2 : 1)
+    dkdv_kernel(const BwdArgs a, int with_dq) {
   constexpr int LD = W + 1, LDP = BQ + 1, NC = BQ / 16, NQ = W / 16;
   extern __shared__ float smem_f[];
-  float* sK = smem_f;             // [BM][LD]
-  float* sV = sK + BM * LD;       // [BM][LD]
-  float* sQ = sV + BM * LD;       // [BQ][LD]
-  float* sdO = sQ + BQ * LD;      // [BQ][LD]
+  float* sK = smem_f;                            // [BM][LD] K (split: its coarse parts, then remainders)
+  float* sKl = sK + BM * LD;
+  float* sV = sK + (SPLIT ? 2 : 1) * BM * LD;    // [BM][LD]
+  float* sQ = sV + BM * LD;                      // [BQ][LD] (split: then Q's coarse parts and remainders)
+  float* sQh = sQ + BQ * LD;
+  float* sQl = sQh + BQ * LD;
+  float* sdO = sQ + (SPLIT ? 3 : 1) * BQ * LD;   // [BQ][LD]
   float* sPt = sdO + BQ * LD;     // [BM][LDP]  P^T: key rows, query columns
   float* sdSt = ONE_BUF ? sPt : sPt + BM * LDP;   // [BM][LDP]
   float* sLse = sdSt + BM * LDP;  // [BQ]
@@ -322,7 +463,10 @@ __global__ void __launch_bounds__(NT, (ONE_BUF || W == 64) ? 2 : 1) dkdv_kernel(
   const size_t bh = blockIdx.y;
   const float scale = p.scale;
 
-  load_tile<W>(sK, LD, a.K + (bh * Tk + kv0) * d, BM, d, Tk - kv0);
+  if constexpr (SPLIT)
+    load_split<W, BM>(nullptr, sK, sKl, LD, a.K + (bh * Tk + kv0) * d, d, Tk - kv0);
+  else
+    load_tile<W>(sK, LD, a.K + (bh * Tk + kv0) * d, BM, d, Tk - kv0);
   load_tile<W>(sV, LD, a.V + (bh * Tk + kv0) * dv, BM, dv, Tk - kv0);
   float accV[4][NQ], accK[4][NQ];
 #pragma unroll
@@ -335,7 +479,10 @@ __global__ void __launch_bounds__(NT, (ONE_BUF || W == 64) ? 2 : 1) dkdv_kernel(
   for (int qt = qt0; qt < n_qt; ++qt) {
     const int q0 = qt * BQ;
     __syncthreads();   // the previous step is done with sQ, sdO, sPt, sdSt
-    load_tile<W>(sQ, LD, a.Q + (bh * Tq + q0) * d, BQ, d, Tq - q0);
+    if constexpr (SPLIT)
+      load_split<W, BQ>(sQ, sQh, sQl, LD, a.Q + (bh * Tq + q0) * d, d, Tq - q0);
+    else
+      load_tile<W>(sQ, LD, a.Q + (bh * Tq + q0) * d, BQ, d, Tq - q0);
     load_tile<W>(sdO, LD, a.dO + (bh * Tq + q0) * dv, BQ, dv, Tq - q0);
     if (threadIdx.x < BQ) {
       const int qi = q0 + threadIdx.x;
@@ -346,7 +493,10 @@ __global__ void __launch_bounds__(NT, (ONE_BUF || W == 64) ? 2 : 1) dkdv_kernel(
     float ds_keep[4][NC];   // ONE_BUF: dS^T waits in registers until the dV product is done with P^T
     {
       float sh[4][NC], sl[4][NC], dp[4][NC];
-      dot2_tile<NC>(sK, sQ, LD, ty, tx, d, sh, sl);
+      if constexpr (SPLIT)
+        split_tile<NC, false>(nullptr, sK, sKl, sQ, sQh, sQl, LD, ty, tx, d, sh, sl);
+      else
+        dot2_tile<NC>(sK, sQ, LD, ty, tx, d, sh, sl);
       dot_tile<NC>(sV, sdO, LD, ty, tx, dv, dp);
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
@@ -395,7 +545,8 @@ __global__ void __launch_bounds__(NT, (ONE_BUF || W == 64) ? 2 : 1) dkdv_kernel(
 #pragma unroll
         for (int r = 0; r < RQ; ++r) x[r] = sdSt[k * LDP + ty + 16 * r];
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) b[q] = sK[k * LD + tx + 16 * q];
+        for (int q = 0; q < NQ; ++q)   // (split: K = coarse part + remainder, exactly)
+          b[q] = SPLIT ? __fadd_rn(sK[k * LD + tx + 16 * q], sKl[k * LD + tx + 16 * q]) : sK[k * LD + tx + 16 * q];
 #pragma unroll
         for (int r = 0; r < RQ; ++r)
 #pragma unroll
@@ -425,15 +576,19 @@ __global__ void __launch_bounds__(NT, (ONE_BUF || W == 64) ? 2 : 1) dkdv_kernel(
 }
 
 // Deterministic dQ: one CTA per (64-row query tile, head) loops over key
-// tiles of BK keys in a fixed order and writes dQ once.
-template <int W, int BK>
+// tiles of BK keys in a fixed order and writes dQ once. SPLIT: scores from
+// split rows (Q split, K whole and split), else by Dot2.
+template <int W, int BK, bool SPLIT>
 __global__ void __launch_bounds__(NT) dq_kernel(const BwdArgs a) {
   constexpr int LD = W + 1, LDS = BK + 1, NC = BK / 16, NQ = W / 16;
   extern __shared__ float smem_f[];
-  float* sQ = smem_f;             // [BM][LD]
-  float* sdO = sQ + BM * LD;      // [BM][LD]
-  float* sK = sdO + BM * LD;      // [BK][LD]
-  float* sV = sK + BK * LD;       // [BK][LD]
+  float* sQ = smem_f;                            // [BM][LD] Q (split: its coarse parts, then remainders)
+  float* sQl = sQ + BM * LD;
+  float* sdO = sQ + (SPLIT ? 2 : 1) * BM * LD;   // [BM][LD]
+  float* sK = sdO + BM * LD;                     // [BK][LD] (split: then K's coarse parts and remainders)
+  float* sKh = sK + BK * LD;
+  float* sKl = sKh + BK * LD;
+  float* sV = sK + (SPLIT ? 3 : 1) * BK * LD;    // [BK][LD]
   float* sdS = sV + BK * LD;      // [BM][LDS]
   float* sLse = sdS + BM * LDS;   // [BM]
   float* sD = sLse + BM;          // [BM]
@@ -444,7 +599,10 @@ __global__ void __launch_bounds__(NT) dq_kernel(const BwdArgs a) {
   const size_t bh = blockIdx.y;
   const float scale = p.scale;
 
-  load_tile<W>(sQ, LD, a.Q + (bh * Tq + q0) * d, BM, d, Tq - q0);
+  if constexpr (SPLIT)
+    load_split<W, BM>(nullptr, sQ, sQl, LD, a.Q + (bh * Tq + q0) * d, d, Tq - q0);
+  else
+    load_tile<W>(sQ, LD, a.Q + (bh * Tq + q0) * d, BM, d, Tq - q0);
   load_tile<W>(sdO, LD, a.dO + (bh * Tq + q0) * dv, BM, dv, Tq - q0);
   if (threadIdx.x < BM) {
     const int qi = q0 + threadIdx.x;
@@ -461,12 +619,18 @@ __global__ void __launch_bounds__(NT) dq_kernel(const BwdArgs a) {
   for (int kt = 0; kt < n_kt; ++kt) {
     const int kv0 = kt * BK;
     __syncthreads();   // the previous step is done with sK, sV, sdS
-    load_tile<W>(sK, LD, a.K + (bh * Tk + kv0) * d, BK, d, Tk - kv0);
+    if constexpr (SPLIT)
+      load_split<W, BK>(sK, sKh, sKl, LD, a.K + (bh * Tk + kv0) * d, d, Tk - kv0);
+    else
+      load_tile<W>(sK, LD, a.K + (bh * Tk + kv0) * d, BK, d, Tk - kv0);
     load_tile<W>(sV, LD, a.V + (bh * Tk + kv0) * dv, BK, dv, Tk - kv0);
     __syncthreads();
     {
       float sh[4][NC], sl[4][NC], dp[4][NC];
-      dot2_tile<NC>(sQ, sK, LD, ty, tx, d, sh, sl);
+      if constexpr (SPLIT)
+        split_tile<NC, false>(nullptr, sQ, sQl, sK, sKh, sKl, LD, ty, tx, d, sh, sl);
+      else
+        dot2_tile<NC>(sQ, sK, LD, ty, tx, d, sh, sl);
       dot_tile<NC>(sdO, sV, LD, ty, tx, dv, dp);
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
@@ -502,44 +666,57 @@ __global__ void __launch_bounds__(NT) dq_kernel(const BwdArgs a) {
 // slower (5.20 -> 5.57 ms) and W = 64 problems gain nothing.
 template <int W>
 constexpr int dkdv_rows() { return W >= 128 ? 32 : 64; }
-// one buffer for P^T and dS^T at W = 128: two CTAs per SM
-template <int W>
-constexpr bool dkdv_one_buf() { return W == 128; }
 template <int W>
 constexpr int dq_rows() { return W >= 128 ? 32 : 64; }
 
-template <int W>
-constexpr size_t dkdv_smem() {
+template <int W, bool SPLIT, bool ONE_BUF>
+constexpr size_t dkdv_smem_of() {
   constexpr int BQ = dkdv_rows<W>();
-  return sizeof(float) * (2 * BM * (W + 1) + 2 * BQ * (W + 1) + (dkdv_one_buf<W>() ? 1 : 2) * BM * (BQ + 1) + 2 * BQ);
+  return sizeof(float) * ((SPLIT ? 3 : 2) * BM * (W + 1) + (SPLIT ? 4 : 2) * BQ * (W + 1) +
+                          (ONE_BUF ? 1 : 2) * BM * (BQ + 1) + 2 * BQ);
+}
+// split rows wherever their tiles fit
+template <int W>
+constexpr bool dkdv_split() { return dkdv_smem_of<W, true, false>() <= kSmemMax; }
+// one buffer for P^T and dS^T at W = 128 with Dot2 scores: two CTAs per SM
+template <int W>
+constexpr bool dkdv_one_buf() { return W == 128 && !dkdv_split<W>(); }
+template <int W>
+constexpr size_t dkdv_smem() { return dkdv_smem_of<W, dkdv_split<W>(), dkdv_one_buf<W>()>(); }
+
+template <int W, bool SPLIT>
+constexpr size_t dq_smem_of() {
+  constexpr int BK = dq_rows<W>();
+  return sizeof(float) * ((SPLIT ? 3 : 2) * BM * (W + 1) + (SPLIT ? 4 : 2) * BK * (W + 1) + BM * (BK + 1) + 2 * BM);
 }
 template <int W>
-constexpr size_t dq_smem() {
-  constexpr int BK = dq_rows<W>();
-  return sizeof(float) * (2 * BM * (W + 1) + 2 * BK * (W + 1) + BM * (BK + 1) + 2 * BM);
-}
+constexpr bool dq_split() { return dq_smem_of<W, true>() <= kSmemMax; }
+template <int W>
+constexpr size_t dq_smem() { return dq_smem_of<W, dq_split<W>()>(); }
 
 template <int W>
 cudaError_t bwd_launch(const LaunchBwd& la, const BwdArgs& b, bool kv, bool q) {
   constexpr int R = dkdv_rows<W>(), RK = dq_rows<W>();
   constexpr size_t s1 = dkdv_smem<W>(), s2 = dq_smem<W>();
-  static_assert(s1 <= 227 * 1024 && s2 <= 227 * 1024, "shared memory");
+  static_assert(s1 <= kSmemMax && s2 <= kSmemMax, "shared memory");
   const Problem& p = la.p;
   cudaError_t e;
   if (kv && p.Tk > 0) {
-    constexpr bool OB = dkdv_one_buf<W>();
-    e = cudaFuncSetAttribute(dkdv_kernel<W, R, OB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    constexpr bool OB = dkdv_one_buf<W>(), SP = dkdv_split<W>();
+    e = cudaFuncSetAttribute(dkdv_kernel<W, R, OB, SP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(s1));
     if (e != cudaSuccess) return e;
     dim3 g1((p.Tk + BM - 1) / BM, p.B * p.H);
-    dkdv_kernel<W, R, OB><<<g1, NT, s1, la.stream>>>(b, la.deterministic ? 0 : 1);
+    dkdv_kernel<W, R, OB, SP><<<g1, NT, s1, la.stream>>>(b, la.deterministic ? 0 : 1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (q) {
-    e = cudaFuncSetAttribute(dq_kernel<W, RK>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s2));
+    constexpr bool SP = dq_split<W>();
+    e = cudaFuncSetAttribute(dq_kernel<W, RK, SP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(s2));
     if (e != cudaSuccess) return e;
     dim3 g2((p.Tq + BM - 1) / BM, p.B * p.H);
-    dq_kernel<W, RK><<<g2, NT, s2, la.stream>>>(b);
+    dq_kernel<W, RK, SP><<<g2, NT, s2, la.stream>>>(b);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -71,6 +71,71 @@ def test_f32_c4_full_size(name, deterministic):
     check_all(make_inputs(w, DEV), w.causal, w.softmax_scale, torch.float32, deterministic)
 
 
+def _split_edge_rows(rng, n, d, scaled=False):
+    """n fp32 rows of d entries from patterns aimed at the exact row split of
+    the fp32 score products: zero rows; one entry of 3 among entries 2^20
+    smaller; every entry on a rounding tie of the split grid; subnormal rows;
+    a largest entry that is an exact power of two, with entries of +-that
+    size; a largest entry that rounds to the end of the grid (256 steps);
+    plain normals; with `scaled`, also normals scaled by 40. (With the dense
+    +-2 rows those give logits in the thousands, where an fp32 backward with
+    exact logits already misses the 1e-4 gradient bound: the backward cases
+    leave them to the c4 workloads.)"""
+    x = rng.standard_normal((n, d)).astype(np.float32)
+    for i, kind in enumerate(rng.integers(0, 8 if scaled else 7, n)):
+        if kind == 0:
+            x[i] = 0.0
+        elif kind == 1:
+            x[i] *= np.float32(2.0 ** -20)
+            x[i, rng.integers(d)] = 3.0
+        elif kind == 2:
+            x[i] = (rng.integers(-255, 255, d) + 0.5) / 128.0   # largest entry in [1, 2): grid step 2^-7
+            x[i, 0] = 1.0
+        elif kind == 3:
+            x[i] = (x[i].astype(np.float64) * 1e-40).astype(np.float32)
+        elif kind == 4:
+            x[i] = np.where(rng.random(d) < 0.5, -2.0, 2.0) * (rng.random(d) < 0.7)
+            x[i, 0] = 2.0
+        elif kind == 5:
+            x[i] = rng.uniform(-1.0, 1.0, d)
+            x[i, 0] = np.float32(1.9999999)
+        elif kind == 7:
+            x[i] *= 40.0
+    return x
+
+
+@pytest.mark.parametrize("deterministic", [0, 1])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d,dv", [(64, 64), (128, 128), (120, 72)])
+def test_f32_split_edge_rows(d, dv, causal, deterministic):
+    B, H, Tq, Tk = 1, 2, 77, 150
+    rng = np.random.default_rng(1000 + d + dv)
+    Q = _split_edge_rows(rng, B * H * Tq, d).reshape(B, H, Tq, d)
+    K = _split_edge_rows(rng, B * H * Tk, d).reshape(B, H, Tk, d)
+    V = rng.standard_normal((B, H, Tk, dv)).astype(np.float32)
+    dO = rng.standard_normal((B, H, Tq, dv)).astype(np.float32)
+    x = {k: torch.from_numpy(v).to(DEV) for k, v in (("Q", Q), ("K", K), ("V", V), ("dO", dO))}
+    check_all(x, causal, 1 / math.sqrt(d), torch.float32, deterministic)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d,dv", [(64, 64), (128, 128), (120, 72)])
+def test_f32_split_edge_rows_forward_large_logits(d, dv, causal):
+    B, H, Tq, Tk = 1, 2, 77, 150
+    rng = np.random.default_rng(2000 + d + dv)
+    Q = _split_edge_rows(rng, B * H * Tq, d, scaled=True).reshape(B, H, Tq, d)
+    K = _split_edge_rows(rng, B * H * Tk, d, scaled=True).reshape(B, H, Tk, d)
+    V = rng.standard_normal((B, H, Tk, dv)).astype(np.float32)
+    x = {k: torch.from_numpy(v).to(DEV) for k, v in (("Q", Q), ("K", K), ("V", V))}
+    scale = 1 / math.sqrt(d)
+    o, lse = pkg.forward(x["Q"], x["K"], x["V"], causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    O, L = ref.forward(x["Q"], x["K"], x["V"], scale, causal)
+    assert np.abs(np.asarray(L)[np.isfinite(L)]).max() > 1000   # logits in the thousands
+    check_o(o, O, torch.float32)
+    check_lse(lse, L, torch.float32)
+
+
 def test_f32_deterministic_is_bitwise_repeatable():
     w = WORKLOADS["c1_causal"]
     x = make_inputs(w.with_(H=3, Tq=300, Tk=300), DEV)
