@@ -23,13 +23,16 @@
 //    128-key forward tiles of 128-column rows).
 //
 // Layout of the work: 256 threads per CTA as a 16 x 16 grid (ty, tx); a
-// thread owns rows ty + 16 r (r < 4) of a 64-row tile and columns tx + 16 c
-// of the tile it multiplies against, so every product is a register tile of
-// 4 x C results fed by 4 + C shared-memory loads per step of the reduction.
-// Shared-memory rows are padded to W + 1 floats (W the tile width: 64, 128 or
-// 256 columns, the smallest that holds d and dv), which keeps the 16 rows a
-// warp reads at one reduction index in 16 different banks; the columns from
-// d (or dv) to W hold zeros.
+// thread owns rows ty + 16 r (r < 4) of a 64-row tile and, in a score-shaped
+// product, rows tx + 16 c of the tile it multiplies against (in a P V-shaped
+// product, columns acc_col(tx, q) of the right-hand tile), so every product
+// is a register tile of 4 x C results fed by 128-bit shared-memory loads,
+// each carrying four steps of the reduction. Shared-memory rows are padded to
+// W + 4 floats (W the tile width: 64, 128 or 256 columns, the smallest that
+// holds d and dv): 16-byte aligned, and 8 consecutive rows start in 8
+// different groups of four banks, so a warp's 128-bit loads of 16 rows take
+// the two wavefronts their 256 bytes need. Columns from d (or dv) to W hold
+// zeros.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include <stdint.h>
@@ -132,6 +135,15 @@ __device__ __forceinline__ void load_split(float* xf, float* xh, float* xl, int 
   }
 }
 
+// Element i (0..3) of a float4; i is a constant once the loops are unrolled.
+__device__ __forceinline__ float el(const float4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+// The reduction products below read 4 consecutive reduction indices per
+// 128-bit shared-memory load, over ceil(n / 4) * 4 indices: tiles are
+// zero-filled to their width W (a multiple of 4), so the extra indices add 0.
+// Each accumulator still takes its terms in ascending index order.
+
 // S[r][c] = sum_k A[ra + 16 r][k] B[cb + 16 c][k] over k < n from split
 // rows, as s (the exact sum of the coarse products) + e (the cross terms):
 // Ah, Al the A rows' parts, Bh, Bl the B rows'. FULL_A: e sums Al Bh + A Bl
@@ -144,35 +156,36 @@ __device__ __forceinline__ void split_tile(const float* A, const float* Ah, cons
   for (int r = 0; r < 4; ++r)
 #pragma unroll
     for (int c = 0; c < C; ++c) s[r][c] = e[r][c] = 0.f;
-  const int ao = ra * ld, bo = cb * ld;
-#pragma unroll 2
-  for (int k = 0; k < n; ++k) {
-    float ah[4], al[4], af[4], bh[C], bl[C], bf[C];
+  const int ao = ra * ld, bo = cb * ld, n4 = (n + 3) >> 2;
+  for (int k = 0; k < 4 * n4; k += 4) {
+    float4 ah[4], al[4], af[4], bh[C], bl[C], bf[C];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      ah[r] = Ah[ao + 16 * r * ld + k];
-      al[r] = Al[ao + 16 * r * ld + k];
-      if constexpr (FULL_A) af[r] = A[ao + 16 * r * ld + k];
+      ah[r] = ld4(Ah + ao + 16 * r * ld + k);
+      al[r] = ld4(Al + ao + 16 * r * ld + k);
+      if constexpr (FULL_A) af[r] = ld4(A + ao + 16 * r * ld + k);
     }
 #pragma unroll
     for (int c = 0; c < C; ++c) {
-      bh[c] = Bh[bo + 16 * c * ld + k];
-      bl[c] = Bl[bo + 16 * c * ld + k];
-      if constexpr (!FULL_A) bf[c] = B[bo + 16 * c * ld + k];
+      bh[c] = ld4(Bh + bo + 16 * c * ld + k);
+      bl[c] = ld4(Bl + bo + 16 * c * ld + k);
+      if constexpr (!FULL_A) bf[c] = ld4(B + bo + 16 * c * ld + k);
     }
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int c = 0; c < C; ++c) {
-        s[r][c] = __fmaf_rn(ah[r], bh[c], s[r][c]);   // exact
-        if constexpr (FULL_A) {
-          e[r][c] = __fmaf_rn(al[r], bh[c], e[r][c]);
-          e[r][c] = __fmaf_rn(af[r], bl[c], e[r][c]);
-        } else {
-          e[r][c] = __fmaf_rn(ah[r], bl[c], e[r][c]);
-          e[r][c] = __fmaf_rn(al[r], bf[c], e[r][c]);
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+          s[r][c] = __fmaf_rn(el(ah[r], i), el(bh[c], i), s[r][c]);   // exact
+          if constexpr (FULL_A) {
+            e[r][c] = __fmaf_rn(el(al[r], i), el(bh[c], i), e[r][c]);
+            e[r][c] = __fmaf_rn(el(af[r], i), el(bl[c], i), e[r][c]);
+          } else {
+            e[r][c] = __fmaf_rn(el(ah[r], i), el(bl[c], i), e[r][c]);
+            e[r][c] = __fmaf_rn(el(al[r], i), el(bf[c], i), e[r][c]);
+          }
         }
-      }
   }
 }
 
@@ -187,17 +200,19 @@ __device__ __forceinline__ void dot2_tile(const float* A, const float* B, int ld
     for (int c = 0; c < C; ++c) s[r][c] = e[r][c] = 0.f;
   const float* a0 = A + ra * ld;
   const float* b0 = B + cb * ld;
-#pragma unroll 2
-  for (int k = 0; k < n; ++k) {
-    float a[4], b[C];
+  const int n4 = (n + 3) >> 2;
+  for (int k = 0; k < 4 * n4; k += 4) {
+    float4 a[4], b[C];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) a[r] = a0[16 * r * ld + k];
+    for (int r = 0; r < 4; ++r) a[r] = ld4(a0 + 16 * r * ld + k);
 #pragma unroll
-    for (int c = 0; c < C; ++c) b[c] = b0[16 * c * ld + k];
+    for (int c = 0; c < C; ++c) b[c] = ld4(b0 + 16 * c * ld + k);
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int c = 0; c < C; ++c) dot2_step(a[r], b[c], s[r][c], e[r][c]);
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < C; ++c) dot2_step(el(a[r], i), el(b[c], i), s[r][c], e[r][c]);
   }
 }
 
@@ -211,38 +226,52 @@ __device__ __forceinline__ void dot_tile(const float* A, const float* B, int ld,
     for (int c = 0; c < C; ++c) x[r][c] = 0.f;
   const float* a0 = A + ra * ld;
   const float* b0 = B + cb * ld;
-#pragma unroll 4
-  for (int k = 0; k < n; ++k) {
-    float a[4], b[C];
+  const int n4 = (n + 3) >> 2;
+#pragma unroll 2
+  for (int k = 0; k < 4 * n4; k += 4) {
+    float4 a[4], b[C];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) a[r] = a0[16 * r * ld + k];
+    for (int r = 0; r < 4; ++r) a[r] = ld4(a0 + 16 * r * ld + k);
 #pragma unroll
-    for (int c = 0; c < C; ++c) b[c] = b0[16 * c * ld + k];
+    for (int c = 0; c < C; ++c) b[c] = ld4(b0 + 16 * c * ld + k);
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int c = 0; c < C; ++c) x[r][c] = fmaf(a[r], b[c], x[r][c]);
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < C; ++c) x[r][c] = fmaf(el(a[r], i), el(b[c], i), x[r][c]);
   }
 }
 
-// acc[r][q] += sum_k P[ra + 16 r][k] V[k][cb + 16 q] over k < n: P with rows
-// of `ldp` floats, V with rows of `ldv` floats.
+// Column of the tile width held by a thread's q-th accumulator in the
+// products below: four adjacent columns in every 64, so that a row of the
+// right-hand tile is read with one 128-bit load per 64 columns.
+__device__ __forceinline__ int acc_col(int tx, int q) { return 64 * (q >> 2) + 4 * tx + (q & 3); }
+
+// acc[r][q] += sum_k P[ra + 16 r][k] V[k][acc_col(tx, q)] over k < n: P
+// with rows of `ldp` floats, V with rows of `ldv` floats.
 template <int R, int Q>
-__device__ __forceinline__ void acc_tile(const float* P, int ldp, const float* V, int ldv, int ra, int cb, int n,
+__device__ __forceinline__ void acc_tile(const float* P, int ldp, const float* V, int ldv, int ra, int tx, int n,
                                          float (&acc)[R][Q]) {
+  static_assert(Q % 4 == 0, "four columns per load");
   const float* p0 = P + ra * ldp;
-  const float* v0 = V + cb;
-#pragma unroll 4
-  for (int k = 0; k < n; ++k) {
-    float a[R], b[Q];
+  const float* v0 = V + 4 * tx;
+  const int n4 = (n + 3) >> 2;
+#pragma unroll 2
+  for (int k = 0; k < 4 * n4; k += 4) {
+    float4 a[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) a[r] = p0[16 * r * ldp + k];
+    for (int r = 0; r < R; ++r) a[r] = ld4(p0 + 16 * r * ldp + k);
 #pragma unroll
-    for (int q = 0; q < Q; ++q) b[q] = v0[k * ldv + 16 * q];
+    for (int i = 0; i < 4; ++i) {
+      float4 b[Q / 4];
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+      for (int g = 0; g < Q / 4; ++g) b[g] = ld4(v0 + (k + i) * ldv + 64 * g);
 #pragma unroll
-      for (int q = 0; q < Q; ++q) acc[r][q] = fmaf(a[r], b[q], acc[r][q]);
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int q = 0; q < Q; ++q) acc[r][q] = fmaf(el(a[r], i), el(b[q >> 2], q & 3), acc[r][q]);
+    }
   }
 }
 
@@ -282,8 +311,8 @@ template <int W, int BN, bool SPLIT>
 __global__ void __launch_bounds__(NT) fwd_kernel(const float* __restrict__ Q, const float* __restrict__ K,
                                                  const float* __restrict__ V, float* __restrict__ O,
                                                  float* __restrict__ LSE, const Problem p) {
-  constexpr int LD = W + 1, LDP = BN + 1, NC = BN / 16, NQ = W / 16;
-  extern __shared__ float smem_f[];
+  constexpr int LD = W + 4, LDP = BN + 4, NC = BN / 16, NQ = W / 16;
+  extern __shared__ __align__(16) float smem_f[];
   float* sQ = smem_f;                              // [BM][LD]
   float* sQh = sQ + BM * LD;                       // split: [BM][LD] coarse parts of Q, then remainders
   float* sQl = sQh + BM * LD;
@@ -368,7 +397,7 @@ __global__ void __launch_bounds__(NT) fwd_kernel(const float* __restrict__ Q, co
     float* orow = O + (bh * Tq + qi) * dv;
 #pragma unroll
     for (int q = 0; q < NQ; ++q)
-      if (tx + 16 * q < dv) orow[tx + 16 * q] = acc[r][q] * inv;
+      if (acc_col(tx, q) < dv) orow[acc_col(tx, q)] = acc[r][q] * inv;
     if (tx == 0) {
       const float ref = m[r] == -CUDART_INF_F ? 0.f : m[r];
       LSE[bh * Tq + qi] = l[r] > 0.f ? static_cast<float>(static_cast<double>(ref) + log(static_cast<double>(l[r])))
@@ -381,7 +410,7 @@ constexpr size_t kSmemMax = 227 * 1024;
 
 template <int W, int BN, bool SPLIT>
 constexpr size_t fwd_smem_of() {
-  return sizeof(float) * ((SPLIT ? 3 : 1) * BM * (W + 1) + (SPLIT ? 3 : 2) * BN * (W + 1) + BM * (BN + 1));
+  return sizeof(float) * ((SPLIT ? 3 : 1) * BM * (W + 4) + (SPLIT ? 3 : 2) * BN * (W + 4) + BM * (BN + 4));
 }
 // split rows wherever their tiles fit
 template <int W, int BN>
@@ -443,8 +472,8 @@ __device__ __forceinline__ void p_ds(float sh, float sl, float dp, float scale, 
 template <int W, int BQ, bool ONE_BUF, bool SPLIT>
 __global__ void __launch_bounds__(NT, (!SPLIT && (ONE_BUF || W == 64)) ? 2 : 1)
     dkdv_kernel(const BwdArgs a, int with_dq) {
-  constexpr int LD = W + 1, LDP = BQ + 1, NC = BQ / 16, NQ = W / 16;
-  extern __shared__ float smem_f[];
+  constexpr int LD = W + 4, LDP = BQ + 4, NC = BQ / 16, NQ = W / 16;
+  extern __shared__ __align__(16) float smem_f[];
   float* sK = smem_f;                            // [BM][LD] K (split: its coarse parts, then remainders)
   float* sKl = sK + BM * LD;
   float* sV = sK + (SPLIT ? 2 : 1) * BM * LD;    // [BM][LD]
@@ -541,16 +570,23 @@ __global__ void __launch_bounds__(NT, (!SPLIT && (ONE_BUF || W == 64)) ? 2 : 1)
       const int nk = min(BM, Tk - kv0);
 #pragma unroll 4
       for (int k = 0; k < nk; ++k) {
-        float x[RQ], b[NQ];
+        float x[RQ];
+        float4 b[NQ / 4];
 #pragma unroll
         for (int r = 0; r < RQ; ++r) x[r] = sdSt[k * LDP + ty + 16 * r];
 #pragma unroll
-        for (int q = 0; q < NQ; ++q)   // (split: K = coarse part + remainder, exactly)
-          b[q] = SPLIT ? __fadd_rn(sK[k * LD + tx + 16 * q], sKl[k * LD + tx + 16 * q]) : sK[k * LD + tx + 16 * q];
+        for (int g = 0; g < NQ / 4; ++g) {
+          b[g] = ld4(sK + k * LD + 64 * g + 4 * tx);
+          if constexpr (SPLIT) {   // K = coarse part + remainder, exactly
+            const float4 l = ld4(sKl + k * LD + 64 * g + 4 * tx);
+            b[g] = make_float4(__fadd_rn(b[g].x, l.x), __fadd_rn(b[g].y, l.y), __fadd_rn(b[g].z, l.z),
+                               __fadd_rn(b[g].w, l.w));
+          }
+        }
 #pragma unroll
         for (int r = 0; r < RQ; ++r)
 #pragma unroll
-          for (int q = 0; q < NQ; ++q) t[r][q] = fmaf(x[r], b[q], t[r][q]);
+          for (int q = 0; q < NQ; ++q) t[r][q] = fmaf(x[r], el(b[q >> 2], q & 3), t[r][q]);
       }
 #pragma unroll
       for (int r = 0; r < RQ; ++r) {
@@ -558,7 +594,7 @@ __global__ void __launch_bounds__(NT, (!SPLIT && (ONE_BUF || W == 64)) ? 2 : 1)
         if (qi >= Tq) continue;
 #pragma unroll
         for (int q = 0; q < NQ; ++q)
-          if (tx + 16 * q < d) atomicAdd(a.dQ + (bh * Tq + qi) * d + tx + 16 * q, t[r][q] * scale);
+          if (acc_col(tx, q) < d) atomicAdd(a.dQ + (bh * Tq + qi) * d + acc_col(tx, q), t[r][q] * scale);
       }
     }
   }
@@ -568,7 +604,7 @@ __global__ void __launch_bounds__(NT, (!SPLIT && (ONE_BUF || W == 64)) ? 2 : 1)
     if (kj >= Tk) continue;
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
-      const int c = tx + 16 * q;
+      const int c = acc_col(tx, q);
       if (c < dv) a.dV[(bh * Tk + kj) * dv + c] = accV[r][q];
       if (c < d) a.dK[(bh * Tk + kj) * d + c] = accK[r][q] * scale;
     }
@@ -580,8 +616,8 @@ __global__ void __launch_bounds__(NT, (!SPLIT && (ONE_BUF || W == 64)) ? 2 : 1)
 // split rows (Q split, K whole and split), else by Dot2.
 template <int W, int BK, bool SPLIT>
 __global__ void __launch_bounds__(NT) dq_kernel(const BwdArgs a) {
-  constexpr int LD = W + 1, LDS = BK + 1, NC = BK / 16, NQ = W / 16;
-  extern __shared__ float smem_f[];
+  constexpr int LD = W + 4, LDS = BK + 4, NC = BK / 16, NQ = W / 16;
+  extern __shared__ __align__(16) float smem_f[];
   float* sQ = smem_f;                            // [BM][LD] Q (split: its coarse parts, then remainders)
   float* sQl = sQ + BM * LD;
   float* sdO = sQ + (SPLIT ? 2 : 1) * BM * LD;   // [BM][LD]
@@ -655,7 +691,7 @@ __global__ void __launch_bounds__(NT) dq_kernel(const BwdArgs a) {
     if (qi >= Tq) continue;
 #pragma unroll
     for (int q = 0; q < NQ; ++q)
-      if (tx + 16 * q < d) a.dQ[(bh * Tq + qi) * d + tx + 16 * q] = acc[r][q] * scale;
+      if (acc_col(tx, q) < d) a.dQ[(bh * Tq + qi) * d + acc_col(tx, q)] = acc[r][q] * scale;
   }
 }
 
@@ -672,8 +708,8 @@ constexpr int dq_rows() { return W >= 128 ? 32 : 64; }
 template <int W, bool SPLIT, bool ONE_BUF>
 constexpr size_t dkdv_smem_of() {
   constexpr int BQ = dkdv_rows<W>();
-  return sizeof(float) * ((SPLIT ? 3 : 2) * BM * (W + 1) + (SPLIT ? 4 : 2) * BQ * (W + 1) +
-                          (ONE_BUF ? 1 : 2) * BM * (BQ + 1) + 2 * BQ);
+  return sizeof(float) * ((SPLIT ? 3 : 2) * BM * (W + 4) + (SPLIT ? 4 : 2) * BQ * (W + 4) +
+                          (ONE_BUF ? 1 : 2) * BM * (BQ + 4) + 2 * BQ);
 }
 // split rows wherever their tiles fit
 template <int W>
@@ -687,7 +723,7 @@ constexpr size_t dkdv_smem() { return dkdv_smem_of<W, dkdv_split<W>(), dkdv_one_
 template <int W, bool SPLIT>
 constexpr size_t dq_smem_of() {
   constexpr int BK = dq_rows<W>();
-  return sizeof(float) * ((SPLIT ? 3 : 2) * BM * (W + 1) + (SPLIT ? 4 : 2) * BK * (W + 1) + BM * (BK + 1) + 2 * BM);
+  return sizeof(float) * ((SPLIT ? 3 : 2) * BM * (W + 4) + (SPLIT ? 4 : 2) * BK * (W + 4) + BM * (BK + 4) + 2 * BM);
 }
 template <int W>
 constexpr bool dq_split() { return dq_smem_of<W, true>() <= kSmemMax; }
