@@ -157,6 +157,7 @@ __device__ __forceinline__ void split_tile(const float* A, const float* Ah, cons
 #pragma unroll
     for (int c = 0; c < C; ++c) s[r][c] = e[r][c] = 0.f;
   const int ao = ra * ld, bo = cb * ld, n4 = (n + 3) >> 2;
+#pragma unroll 2
   for (int k = 0; k < 4 * n4; k += 4) {
     float4 ah[4], al[4], af[4], bh[C], bl[C], bf[C];
 #pragma unroll
