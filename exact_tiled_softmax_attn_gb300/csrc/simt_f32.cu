@@ -93,46 +93,71 @@ __device__ __forceinline__ void split_grid(float m, float& u, float& inv) {
   inv = __uint_as_float(static_cast<uint32_t>(261 - eb) << 23);  // 2^(7 - E)
 }
 
-// Rows [0, ROWS) of a [T][cols] fp32 block (src at its first row) split
-// as above into shared memory with rows of ld floats: hi to xh, lo to xl and,
-// if xf is not null, x itself to xf; rows at or past `valid` and columns
-// [cols, W) as zeros. Warp w takes rows w, w + 8, ...; all of a warp's loads
-// are issued before its first row maximum.
+// ROWS rows of W columns on their way from global to shared memory, held in
+// registers: warp w holds rows w, w + 8, ..., lane l columns l, l + 32, ...
+// Loading and storing are separate steps, so that a tile's loads can be in
+// flight while the CTA still computes on the previous tile.
+template <int W, int ROWS>
+struct RowRegs {
+  static constexpr int NW = NT / 32, PER = W / 32, RW = ROWS / NW;
+  static_assert(ROWS % NW == 0, "rows per warp");
+  float v[RW][PER];
+
+  // Rows [0, ROWS) of a [T][cols] fp32 block (src at its first row); rows at
+  // or past `valid` and columns [cols, W) read as zeros.
+  __device__ __forceinline__ void load(const float* src, int cols, int valid) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < RW; ++i) {
+      const int r = warp + NW * i;
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        const int c = lane + 32 * j;
+        v[i][j] = (r < valid && c < cols) ? src[static_cast<size_t>(r) * cols + c] : 0.f;
+      }
+    }
+  }
+  // To shared memory with rows of ld floats.
+  __device__ __forceinline__ void store(float* dst, int ld) const {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < RW; ++i)
+#pragma unroll
+      for (int j = 0; j < PER; ++j) dst[(warp + NW * i) * ld + lane + 32 * j] = v[i][j];
+  }
+  // Each row split as above: hi to xh, lo to xl and, if xf is not null, x
+  // itself to xf (shared memory, rows of ld floats).
+  __device__ __forceinline__ void split(float* xf, float* xh, float* xl, int ld) const {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < RW; ++i) {
+      const int r = warp + NW * i;
+      float m = 0.f;
+#pragma unroll
+      for (int j = 0; j < PER; ++j) m = fmaxf(m, fabsf(v[i][j]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      float u, inv;
+      split_grid(m, u, inv);
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        const int c = lane + 32 * j;
+        const float hi = __fmul_rn(rintf(__fmul_rn(v[i][j], inv)), u);
+        xh[r * ld + c] = hi;
+        xl[r * ld + c] = __fsub_rn(v[i][j], hi);
+        if (xf != nullptr) xf[r * ld + c] = v[i][j];
+      }
+    }
+  }
+};
+
+// Rows [0, ROWS) of a block loaded and split into shared memory at once.
 template <int W, int ROWS>
 __device__ __forceinline__ void load_split(float* xf, float* xh, float* xl, int ld, const float* src, int cols,
                                            int valid) {
-  constexpr int NW = NT / 32, PER = W / 32, RW = ROWS / NW;
-  static_assert(ROWS % NW == 0, "rows per warp");
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float v[RW][PER];
-#pragma unroll
-  for (int i = 0; i < RW; ++i) {
-    const int r = warp + NW * i;
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int c = lane + 32 * j;
-      v[i][j] = (r < valid && c < cols) ? src[static_cast<size_t>(r) * cols + c] : 0.f;
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < RW; ++i) {
-    const int r = warp + NW * i;
-    float m = 0.f;
-#pragma unroll
-    for (int j = 0; j < PER; ++j) m = fmaxf(m, fabsf(v[i][j]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float u, inv;
-    split_grid(m, u, inv);
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int c = lane + 32 * j;
-      const float hi = __fmul_rn(rintf(__fmul_rn(v[i][j], inv)), u);
-      xh[r * ld + c] = hi;
-      xl[r * ld + c] = __fsub_rn(v[i][j], hi);
-      if (xf != nullptr) xf[r * ld + c] = v[i][j];
-    }
-  }
+  RowRegs<W, ROWS> x;
+  x.load(src, cols, valid);
+  x.split(xf, xh, xl, ld);
 }
 
 // Element i (0..3) of a float4; i is a constant once the loops are unrolled.
@@ -342,14 +367,23 @@ __global__ void __launch_bounds__(NT) fwd_kernel(const float* __restrict__ Q, co
   int n_kv = (Tk + BN - 1) / BN;
   if (p.causal) n_kv = min(n_kv, (q0 + BM - 1) / BN + 1);
 
+  // split rows: a key tile's K and V rows load into registers while the
+  // previous tile's P V product runs
+  RowRegs<W, BN> kr, vr;
+  if constexpr (SPLIT) {
+    kr.load(K + bh * Tk * d, d, Tk);
+    vr.load(V + bh * Tk * dv, dv, Tk);
+  }
   for (int jt = 0; jt < n_kv; ++jt) {
     const int kv0 = jt * BN;
     __syncthreads();   // the previous tile's P V is done with sK, sV, sP
-    if constexpr (SPLIT)
-      load_split<W, BN>(nullptr, sK, sKl, LD, K + (bh * Tk + kv0) * d, d, Tk - kv0);
-    else
+    if constexpr (SPLIT) {
+      kr.split(nullptr, sK, sKl, LD);
+      vr.store(sV, LD);
+    } else {
       load_tile<W>(sK, LD, K + (bh * Tk + kv0) * d, BN, d, Tk - kv0);
-    load_tile<W>(sV, LD, V + (bh * Tk + kv0) * dv, BN, dv, Tk - kv0);
+      load_tile<W>(sV, LD, V + (bh * Tk + kv0) * dv, BN, dv, Tk - kv0);
+    }
     __syncthreads();
     float sh[4][NC], sl[4][NC];
     if constexpr (SPLIT)
@@ -387,6 +421,12 @@ __global__ void __launch_bounds__(NT) fwd_kernel(const float* __restrict__ Q, co
       for (int q = 0; q < NQ; ++q) acc[r][q] *= corr;
     }
     __syncthreads();
+    if constexpr (SPLIT) {
+      if (jt + 1 < n_kv) {
+        kr.load(K + (bh * Tk + kv0 + BN) * d, d, Tk - kv0 - BN);
+        vr.load(V + (bh * Tk + kv0 + BN) * dv, dv, Tk - kv0 - BN);
+      }
+    }
     // acc += P V over the tile's keys (padding keys have P = 0 and V = 0)
     acc_tile<4, NQ>(sP, LDP, sV, LD, ty, tx, min(BN, Tk - kv0), acc);
   }
@@ -506,18 +546,38 @@ __global__ void __launch_bounds__(NT, (!SPLIT && (ONE_BUF || W == 64)) ? 2 : 1)
 
   const int qt0 = p.causal ? kv0 / BQ : 0;
   const int n_qt = (Tq + BQ - 1) / BQ;
+  // split rows: a query step's Q and dO rows (and its LSE and D) load into
+  // registers while the previous step's dV and dK products run
+  RowRegs<W, BQ> qr, dor;
+  float lse_n = -CUDART_INF_F, d_n = 0.f;
+  auto load_step = [&](int q0) {
+    qr.load(a.Q + (bh * Tq + q0) * d, d, Tq - q0);
+    dor.load(a.dO + (bh * Tq + q0) * dv, dv, Tq - q0);
+    if (threadIdx.x < BQ) {
+      const int qi = q0 + threadIdx.x;
+      lse_n = qi < Tq ? a.LSE[bh * Tq + qi] : -CUDART_INF_F;
+      d_n = qi < Tq ? a.D[bh * padded_rows(Tq) + qi] : 0.f;
+    }
+  };
+  if constexpr (SPLIT) load_step(qt0 * BQ);
   for (int qt = qt0; qt < n_qt; ++qt) {
     const int q0 = qt * BQ;
     __syncthreads();   // the previous step is done with sQ, sdO, sPt, sdSt
-    if constexpr (SPLIT)
-      load_split<W, BQ>(sQ, sQh, sQl, LD, a.Q + (bh * Tq + q0) * d, d, Tq - q0);
-    else
+    if constexpr (SPLIT) {
+      qr.split(sQ, sQh, sQl, LD);
+      dor.store(sdO, LD);
+      if (threadIdx.x < BQ) {
+        sLse[threadIdx.x] = lse_n;
+        sD[threadIdx.x] = d_n;
+      }
+    } else {
       load_tile<W>(sQ, LD, a.Q + (bh * Tq + q0) * d, BQ, d, Tq - q0);
-    load_tile<W>(sdO, LD, a.dO + (bh * Tq + q0) * dv, BQ, dv, Tq - q0);
-    if (threadIdx.x < BQ) {
-      const int qi = q0 + threadIdx.x;
-      sLse[threadIdx.x] = qi < Tq ? a.LSE[bh * Tq + qi] : -CUDART_INF_F;
-      sD[threadIdx.x] = qi < Tq ? a.D[bh * padded_rows(Tq) + qi] : 0.f;
+      load_tile<W>(sdO, LD, a.dO + (bh * Tq + q0) * dv, BQ, dv, Tq - q0);
+      if (threadIdx.x < BQ) {
+        const int qi = q0 + threadIdx.x;
+        sLse[threadIdx.x] = qi < Tq ? a.LSE[bh * Tq + qi] : -CUDART_INF_F;
+        sD[threadIdx.x] = qi < Tq ? a.D[bh * padded_rows(Tq) + qi] : 0.f;
+      }
     }
     __syncthreads();
     float ds_keep[4][NC];   // ONE_BUF: dS^T waits in registers until the dV product is done with P^T
@@ -547,6 +607,9 @@ __global__ void __launch_bounds__(NT, (!SPLIT && (ONE_BUF || W == 64)) ? 2 : 1)
       }
     }
     __syncthreads();
+    if constexpr (SPLIT) {
+      if (qt + 1 < n_qt) load_step(q0 + BQ);
+    }
     // dV_j += sum_i P_ij dO_i ; dK_j += sum_i dS_ij Q_i
     const int nq = min(BQ, Tq - q0);
     acc_tile<4, NQ>(sPt, LDP, sdO, LD, ty, tx, nq, accV);
@@ -653,14 +716,23 @@ __global__ void __launch_bounds__(NT) dq_kernel(const BwdArgs a) {
     for (int q = 0; q < NQ; ++q) acc[r][q] = 0.f;
   int n_kt = (Tk + BK - 1) / BK;
   if (p.causal) n_kt = min(n_kt, (q0 + BM - 1) / BK + 1);
+  // split rows: a key step's K and V rows load into registers while the
+  // previous step's dQ product runs
+  RowRegs<W, BK> kr, vr;
+  if constexpr (SPLIT) {
+    kr.load(a.K + bh * Tk * d, d, Tk);
+    vr.load(a.V + bh * Tk * dv, dv, Tk);
+  }
   for (int kt = 0; kt < n_kt; ++kt) {
     const int kv0 = kt * BK;
     __syncthreads();   // the previous step is done with sK, sV, sdS
-    if constexpr (SPLIT)
-      load_split<W, BK>(sK, sKh, sKl, LD, a.K + (bh * Tk + kv0) * d, d, Tk - kv0);
-    else
+    if constexpr (SPLIT) {
+      kr.split(sK, sKh, sKl, LD);
+      vr.store(sV, LD);
+    } else {
       load_tile<W>(sK, LD, a.K + (bh * Tk + kv0) * d, BK, d, Tk - kv0);
-    load_tile<W>(sV, LD, a.V + (bh * Tk + kv0) * dv, BK, dv, Tk - kv0);
+      load_tile<W>(sV, LD, a.V + (bh * Tk + kv0) * dv, BK, dv, Tk - kv0);
+    }
     __syncthreads();
     {
       float sh[4][NC], sl[4][NC], dp[4][NC];
@@ -684,6 +756,12 @@ __global__ void __launch_bounds__(NT) dq_kernel(const BwdArgs a) {
       }
     }
     __syncthreads();
+    if constexpr (SPLIT) {
+      if (kt + 1 < n_kt) {
+        kr.load(a.K + (bh * Tk + kv0 + BK) * d, d, Tk - kv0 - BK);
+        vr.load(a.V + (bh * Tk + kv0 + BK) * dv, dv, Tk - kv0 - BK);
+      }
+    }
     acc_tile<4, NQ>(sdS, LDS, sK, LD, ty, tx, min(BK, Tk - kv0), acc);
   }
 #pragma unroll
