@@ -215,6 +215,49 @@ __device__ __forceinline__ void split_tile(const float* A, const float* Ah, cons
   }
 }
 
+// split_tile<C, false> and dot_tile<C> of two row sets in one reduction
+// loop (both products reduce over n): S from the split rows Ah, Al / B, Bh,
+// Bl and X[r][c] = sum_k D[ra + 16 r][k] E[cb + 16 c][k].
+template <int C>
+__device__ __forceinline__ void split_dot_tile(const float* Ah, const float* Al, const float* B, const float* Bh,
+                                               const float* Bl, const float* D, const float* E, int ld, int ra,
+                                               int cb, int n, float (&s)[4][C], float (&e)[4][C],
+                                               float (&x)[4][C]) {
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < C; ++c) s[r][c] = e[r][c] = x[r][c] = 0.f;
+  const int ao = ra * ld, bo = cb * ld, n4 = (n + 3) >> 2;
+#pragma unroll 2
+  for (int k = 0; k < 4 * n4; k += 4) {
+    float4 ah[4], al[4], ad[4], bh[C], bl[C], bf[C], be[C];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      ah[r] = ld4(Ah + ao + 16 * r * ld + k);
+      al[r] = ld4(Al + ao + 16 * r * ld + k);
+      ad[r] = ld4(D + ao + 16 * r * ld + k);
+    }
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+      bh[c] = ld4(Bh + bo + 16 * c * ld + k);
+      bl[c] = ld4(Bl + bo + 16 * c * ld + k);
+      bf[c] = ld4(B + bo + 16 * c * ld + k);
+      be[c] = ld4(E + bo + 16 * c * ld + k);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+          s[r][c] = __fmaf_rn(el(ah[r], i), el(bh[c], i), s[r][c]);   // exact
+          e[r][c] = __fmaf_rn(el(ah[r], i), el(bl[c], i), e[r][c]);
+          e[r][c] = __fmaf_rn(el(al[r], i), el(bf[c], i), e[r][c]);
+          x[r][c] = fmaf(el(ad[r], i), el(be[c], i), x[r][c]);
+        }
+  }
+}
+
 // S[r][c] = sum_k A[ra + 16 r][k] B[cb + 16 c][k] over k < n, by Dot2: hi in
 // s, lo in e. A and B are shared-memory tiles with rows of `ld` floats.
 template <int C>
@@ -506,13 +549,10 @@ __device__ __forceinline__ void p_ds(float sh, float sl, float dp, float scale, 
 // that see the key tile, computes S^T = K Q^T and dP^T = V dO^T for
 // the tile, and accumulates dV += P^T dO and dK += dS^T Q in registers
 // (rows of keys ty + 16 r). Unless `with_dq` is 0 it also adds this key
-// tile's share scale * dS K into dQ with fp32 atomics. ONE_BUF: P^T and
-// dS^T take turns in one shared buffer (P^T for the dV product, then dS^T
-// over it), so that two CTAs fit per SM. SPLIT: scores from split rows (K
-// split, Q whole and split), else by Dot2.
-template <int W, int BQ, bool ONE_BUF, bool SPLIT>
-__global__ void __launch_bounds__(NT, (!SPLIT && (ONE_BUF || W == 64)) ? 2 : 1)
-    dkdv_kernel(const BwdArgs a, int with_dq) {
+// tile's share scale * dS K into dQ with fp32 atomics. SPLIT: scores from
+// split rows (K split, Q whole and split), else by Dot2.
+template <int W, int BQ, bool SPLIT>
+__global__ void __launch_bounds__(NT, 1) dkdv_kernel(const BwdArgs a, int with_dq) {
   constexpr int LD = W + 4, LDP = BQ + 4, NC = BQ / 16, NQ = W / 16;
   extern __shared__ __align__(16) float smem_f[];
   float* sK = smem_f;                            // [BM][LD] K (split: its coarse parts, then remainders)
@@ -523,7 +563,7 @@ __global__ void __launch_bounds__(NT, (!SPLIT && (ONE_BUF || W == 64)) ? 2 : 1)
   float* sQl = sQh + BQ * LD;
   float* sdO = sQ + (SPLIT ? 3 : 1) * BQ * LD;   // [BQ][LD]
   float* sPt = sdO + BQ * LD;     // [BM][LDP]  P^T: key rows, query columns
-  float* sdSt = ONE_BUF ? sPt : sPt + BM * LDP;   // [BM][LDP]
+  float* sdSt = sPt + BM * LDP;                  // [BM][LDP]
   float* sLse = sdSt + BM * LDP;  // [BQ]
   float* sD = sLse + BQ;          // [BQ]
   const Problem& p = a.p;
@@ -580,14 +620,21 @@ __global__ void __launch_bounds__(NT, (!SPLIT && (ONE_BUF || W == 64)) ? 2 : 1)
       }
     }
     __syncthreads();
-    float ds_keep[4][NC];   // ONE_BUF: dS^T waits in registers until the dV product is done with P^T
     {
       float sh[4][NC], sl[4][NC], dp[4][NC];
-      if constexpr (SPLIT)
-        split_tile<NC, false>(nullptr, sK, sKl, sQ, sQh, sQl, LD, ty, tx, d, sh, sl);
-      else
+      if constexpr (SPLIT) {
+        // one loop for both products where it measured faster (128-column
+        // rows; 64-column rows, which fit 64-query steps, were slower so)
+        if (W >= 128 && d == dv) {
+          split_dot_tile<NC>(sK, sKl, sQ, sQh, sQl, sV, sdO, LD, ty, tx, d, sh, sl, dp);
+        } else {
+          split_tile<NC, false>(nullptr, sK, sKl, sQ, sQh, sQl, LD, ty, tx, d, sh, sl);
+          dot_tile<NC>(sV, sdO, LD, ty, tx, dv, dp);
+        }
+      } else {
         dot2_tile<NC>(sK, sQ, LD, ty, tx, d, sh, sl);
-      dot_tile<NC>(sV, sdO, LD, ty, tx, dv, dp);
+        dot_tile<NC>(sV, sdO, LD, ty, tx, dv, dp);
+      }
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int kj = kv0 + ty + 16 * r;
@@ -599,10 +646,7 @@ __global__ void __launch_bounds__(NT, (!SPLIT && (ONE_BUF || W == 64)) ? 2 : 1)
           float pij, dsij;
           p_ds(sh[r][c], sl[r][c], dp[r][c], scale, lse, sD[i], blocked, pij, dsij);
           sPt[(ty + 16 * r) * LDP + i] = pij;
-          if constexpr (ONE_BUF)
-            ds_keep[r][c] = dsij;
-          else
-            sdSt[(ty + 16 * r) * LDP + i] = dsij;
+          sdSt[(ty + 16 * r) * LDP + i] = dsij;
         }
       }
     }
@@ -613,14 +657,6 @@ __global__ void __launch_bounds__(NT, (!SPLIT && (ONE_BUF || W == 64)) ? 2 : 1)
     // dV_j += sum_i P_ij dO_i ; dK_j += sum_i dS_ij Q_i
     const int nq = min(BQ, Tq - q0);
     acc_tile<4, NQ>(sPt, LDP, sdO, LD, ty, tx, nq, accV);
-    if constexpr (ONE_BUF) {
-      __syncthreads();   // every thread is done reading P^T
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int c = 0; c < NC; ++c) sdSt[(ty + 16 * r) * LDP + tx + 16 * c] = ds_keep[r][c];
-      __syncthreads();
-    }
     acc_tile<4, NQ>(sdSt, LDP, sQ, LD, ty, tx, nq, accK);
     if (with_dq) {
       // dQ_i += scale * sum_j dS_ij K_j, rows of queries ty + 16 r
@@ -736,11 +772,17 @@ __global__ void __launch_bounds__(NT) dq_kernel(const BwdArgs a) {
     __syncthreads();
     {
       float sh[4][NC], sl[4][NC], dp[4][NC];
-      if constexpr (SPLIT)
-        split_tile<NC, false>(nullptr, sQ, sQl, sK, sKh, sKl, LD, ty, tx, d, sh, sl);
-      else
+      if constexpr (SPLIT) {
+        if (d == dv) {
+          split_dot_tile<NC>(sQ, sQl, sK, sKh, sKl, sdO, sV, LD, ty, tx, d, sh, sl, dp);
+        } else {
+          split_tile<NC, false>(nullptr, sQ, sQl, sK, sKh, sKl, LD, ty, tx, d, sh, sl);
+          dot_tile<NC>(sdO, sV, LD, ty, tx, dv, dp);
+        }
+      } else {
         dot2_tile<NC>(sQ, sK, LD, ty, tx, d, sh, sl);
-      dot_tile<NC>(sdO, sV, LD, ty, tx, dv, dp);
+        dot_tile<NC>(sdO, sV, LD, ty, tx, dv, dp);
+      }
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int i = ty + 16 * r, qi = q0 + i;
@@ -774,30 +816,24 @@ __global__ void __launch_bounds__(NT) dq_kernel(const BwdArgs a) {
   }
 }
 
-// Queries per step of the dK/dV kernel and keys per step of the dQ kernel.
-// The dQ kernel takes 32-key steps from W = 128 on: its shared memory then
-// fits two CTAs per SM (measured on GB300 at B=2 H=8 Tq=1000 Tk=4000
-// d=128: 5.14 -> 4.60 ms), where 32-query steps made the dK/dV kernel
-// slower (5.20 -> 5.57 ms) and W = 64 problems gain nothing.
+// Queries per step of the dK/dV kernel and keys per step of the dQ kernel:
+// 32 from W = 128 on, 64 at W = 64, so that the split tiles fit in shared
+// memory (one CTA per SM).
 template <int W>
 constexpr int dkdv_rows() { return W >= 128 ? 32 : 64; }
 template <int W>
 constexpr int dq_rows() { return W >= 128 ? 32 : 64; }
 
-template <int W, bool SPLIT, bool ONE_BUF>
+template <int W, bool SPLIT>
 constexpr size_t dkdv_smem_of() {
   constexpr int BQ = dkdv_rows<W>();
-  return sizeof(float) * ((SPLIT ? 3 : 2) * BM * (W + 4) + (SPLIT ? 4 : 2) * BQ * (W + 4) +
-                          (ONE_BUF ? 1 : 2) * BM * (BQ + 4) + 2 * BQ);
+  return sizeof(float) * ((SPLIT ? 3 : 2) * BM * (W + 4) + (SPLIT ? 4 : 2) * BQ * (W + 4) + 2 * BM * (BQ + 4) + 2 * BQ);
 }
 // split rows wherever their tiles fit
 template <int W>
-constexpr bool dkdv_split() { return dkdv_smem_of<W, true, false>() <= kSmemMax; }
-// one buffer for P^T and dS^T at W = 128 with Dot2 scores: two CTAs per SM
+constexpr bool dkdv_split() { return dkdv_smem_of<W, true>() <= kSmemMax; }
 template <int W>
-constexpr bool dkdv_one_buf() { return W == 128 && !dkdv_split<W>(); }
-template <int W>
-constexpr size_t dkdv_smem() { return dkdv_smem_of<W, dkdv_split<W>(), dkdv_one_buf<W>()>(); }
+constexpr size_t dkdv_smem() { return dkdv_smem_of<W, dkdv_split<W>()>(); }
 
 template <int W, bool SPLIT>
 constexpr size_t dq_smem_of() {
@@ -811,18 +847,18 @@ constexpr size_t dq_smem() { return dq_smem_of<W, dq_split<W>()>(); }
 
 template <int W>
 cudaError_t bwd_launch(const LaunchBwd& la, const BwdArgs& b, bool kv, bool q) {
-  constexpr int R = dkdv_rows<W>(), RK = dq_rows<W>();
+  constexpr int RQ = dkdv_rows<W>(), RK = dq_rows<W>();
   constexpr size_t s1 = dkdv_smem<W>(), s2 = dq_smem<W>();
   static_assert(s1 <= kSmemMax && s2 <= kSmemMax, "shared memory");
   const Problem& p = la.p;
   cudaError_t e;
   if (kv && p.Tk > 0) {
-    constexpr bool OB = dkdv_one_buf<W>(), SP = dkdv_split<W>();
-    e = cudaFuncSetAttribute(dkdv_kernel<W, R, OB, SP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    constexpr bool SP = dkdv_split<W>();
+    e = cudaFuncSetAttribute(dkdv_kernel<W, RQ, SP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(s1));
     if (e != cudaSuccess) return e;
     dim3 g1((p.Tk + BM - 1) / BM, p.B * p.H);
-    dkdv_kernel<W, R, OB, SP><<<g1, NT, s1, la.stream>>>(b, la.deterministic ? 0 : 1);
+    dkdv_kernel<W, RQ, SP><<<g1, NT, s1, la.stream>>>(b, la.deterministic ? 0 : 1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (q) {
