@@ -486,6 +486,9 @@ def run_ours(args, w):
     e2e_total = e2e_run(e2e_steps)
     e2e_total = reduce_max(e2e_total)
     e2e_value = world * e2e_steps * (F + Bf) / (e2e_total * 1e-3) / 1e12
+    link = copy_link(dev_in[0], pinned, dev_out[0], host_out[0], s_in, s_out, h2d, d2h)
+    # a step can take no less than the longer of its kernels and its copies
+    link["bound_value"] = world * (F + Bf) / (max(total_ms / args.steps, link["concurrent_ms"]) * 1e-3) / 1e12
     if clocks:
         clk = clocks.stop()
     if world > 1:
@@ -575,7 +578,8 @@ def run_ours(args, w):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps,
                 "pipeline": "two buffer sets; step i+1 host-to-device and step i-1 device-to-host copies "
-                            "overlap step i's kernels on separate streams"},
+                            "overlap step i's kernels on separate streams",
+                "link": link},
         # bf16: fwd (+ split-KV merge), dQ (+ split reduction), dK/dV | fwd (+ merge), preprocess,
         # dK/dV, convert; fp32: fwd, preprocess, dK/dV, dQ | fwd, preprocess, dK/dV
         "gpu_launches": args.steps * ((1 + (1 if n_splits > 1 else 0)) if args.fwd_only else
@@ -590,6 +594,39 @@ def run_ours(args, w):
         line["cpu_baseline"] = cpu_baseline(w, host, fwd_only=args.fwd_only)
     print(json.dumps(line), flush=True)
     return 0
+
+
+def copy_link(dev_in, pinned, dev_out, host_out, s_in, s_out, h2d, d2h, reps=3):
+    """One step's copies alone (outside every timed region): host-to-device,
+    device-to-host, and both at once, each on its own stream as in the
+    end-to-end pipeline. Returns GB/s per direction and the concurrent time."""
+    import torch
+
+    def run(do_in, do_out):
+        ev = []
+        for _ in range(reps):
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(torch.cuda.current_stream())
+            s_in.wait_stream(torch.cuda.current_stream())
+            s_out.wait_stream(torch.cuda.current_stream())
+            if do_in:
+                with torch.cuda.stream(s_in):
+                    for k in dev_in:
+                        dev_in[k].copy_(pinned[k], non_blocking=True)
+            if do_out:
+                with torch.cuda.stream(s_out):
+                    for n in host_out:
+                        host_out[n].copy_(dev_out[n], non_blocking=True)
+            torch.cuda.current_stream().wait_stream(s_in)
+            torch.cuda.current_stream().wait_stream(s_out)
+            t1.record(torch.cuda.current_stream())
+            ev.append((t0, t1))
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+    t_in, t_out, t_both = run(True, False), run(False, True), run(True, True)
+    return {"h2d_gbs": h2d / (t_in * 1e-3) / 1e9, "d2h_gbs": d2h / (t_out * 1e-3) / 1e9,
+            "concurrent_ms": t_both, "note": "one step's copies alone on this box; bound_value: the metric at "
+            "max(kernel time, concurrent copy time) per step"}
 
 
 def main(argv=None):

@@ -177,3 +177,37 @@ def test_traffic_entries_name_a_kernel_a_workload_and_a_summary():
     assert bench.load_traffic(k, wl) == expect
     other = next(n for n in WORKLOADS if (k, n) not in seen)
     assert bench.load_traffic(k, other) is None
+
+
+def test_bench_functions_use_only_bound_names():
+    """Every name a bench.py function reads is bound in that function (an
+    argument, an assignment, a local import, a nested def) or at module level:
+    torch is imported inside the functions that need it, so a helper that
+    forgets its own import would fail only on the GPU machine."""
+    import ast
+    import builtins
+
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "bench.py")).read()
+    tree = ast.parse(src)
+    module = set(dir(builtins)) | {"__file__", "__name__"}
+    for node in tree.body:
+        if isinstance(node, (ast.Import, ast.ImportFrom)):
+            module |= {(a.asname or a.name).split(".")[0] for a in node.names}
+        elif isinstance(node, (ast.FunctionDef, ast.ClassDef)):
+            module.add(node.name)
+        elif isinstance(node, (ast.Assign, ast.AnnAssign)):
+            for t in (node.targets if isinstance(node, ast.Assign) else [node.target]):
+                module |= {n.id for n in ast.walk(t) if isinstance(n, ast.Name)}
+    for fn in (n for n in tree.body if isinstance(n, ast.FunctionDef)):
+        bound = set()
+        for n in ast.walk(fn):
+            if isinstance(n, (ast.Import, ast.ImportFrom)):
+                bound |= {(a.asname or a.name).split(".")[0] for a in n.names}
+            elif isinstance(n, ast.Name) and isinstance(n.ctx, ast.Store):
+                bound.add(n.id)
+            elif isinstance(n, ast.arg):
+                bound.add(n.arg)
+            elif isinstance(n, ast.FunctionDef):
+                bound.add(n.name)
+        used = {n.id for n in ast.walk(fn) if isinstance(n, ast.Name) and isinstance(n.ctx, ast.Load)}
+        assert not (used - bound - module), f"{fn.name} reads unbound names {sorted(used - bound - module)}"
