@@ -169,18 +169,76 @@ __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast
 // zero-filled to their width W (a multiple of 4), so the extra indices add 0.
 // Each accumulator still takes its terms in ascending index order.
 
+// a * b + c in each of two fp32 lanes, one instruction (sm_100 and later);
+// each lane rounded as the scalar FMA
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 r;
+  asm("{\n\t.reg .b64 x, y, z, w;\n\t"
+      "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\tmov.b64 z, {%6, %7};\n\t"
+      "fma.rn.f32x2 w, x, y, z;\n\tmov.b64 {%0, %1}, w;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return r;
+}
+// elements (2h, 2h + 1) of a float4
+__device__ __forceinline__ float2 pair(const float4& v, int h) { return h == 0 ? make_float2(v.x, v.y) : make_float2(v.z, v.w); }
+
 // S[r][c] = sum_k A[ra + 16 r][k] B[cb + 16 c][k] over k < n from split
 // rows, as s (the exact sum of the coarse products) + e (the cross terms):
 // Ah, Al the A rows' parts, Bh, Bl the B rows'. FULL_A: e sums Al Bh + A Bl
 // (A the unsplit A rows; B unused), else Ah Bl + Al B (A unused).
+// Up to 4 columns per thread two-lane FMAs carry the even and the odd
+// reduction indices in separate partial sums, added at the end (the coarse
+// sums stay exact: any subset of the coarse products sums exactly); wider
+// tiles (128-key forward tiles of 64-column rows) would not fit the doubled
+// accumulators in registers and take one FMA per term.
 template <int C, bool FULL_A>
 __device__ __forceinline__ void split_tile(const float* A, const float* Ah, const float* Al, const float* B,
                                            const float* Bh, const float* Bl, int ld, int ra, int cb, int n,
                                            float (&s)[4][C], float (&e)[4][C]) {
+  if constexpr (C > 4) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c = 0; c < C; ++c) s[r][c] = e[r][c] = 0.f;
+    const int ao = ra * ld, bo = cb * ld, n4 = (n + 3) >> 2;
+    for (int k = 0; k < 4 * n4; k += 4) {
+      float4 ah[4], al[4], af[4], bh[C], bl[C], bf[C];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        ah[r] = ld4(Ah + ao + 16 * r * ld + k);
+        al[r] = ld4(Al + ao + 16 * r * ld + k);
+        if constexpr (FULL_A) af[r] = ld4(A + ao + 16 * r * ld + k);
+      }
+#pragma unroll
+      for (int c = 0; c < C; ++c) {
+        bh[c] = ld4(Bh + bo + 16 * c * ld + k);
+        bl[c] = ld4(Bl + bo + 16 * c * ld + k);
+        if constexpr (!FULL_A) bf[c] = ld4(B + bo + 16 * c * ld + k);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int c = 0; c < C; ++c) {
+            s[r][c] = __fmaf_rn(el(ah[r], i), el(bh[c], i), s[r][c]);   // exact
+            if constexpr (FULL_A) {
+              e[r][c] = __fmaf_rn(el(al[r], i), el(bh[c], i), e[r][c]);
+              e[r][c] = __fmaf_rn(el(af[r], i), el(bl[c], i), e[r][c]);
+            } else {
+              e[r][c] = __fmaf_rn(el(ah[r], i), el(bl[c], i), e[r][c]);
+              e[r][c] = __fmaf_rn(el(al[r], i), el(bf[c], i), e[r][c]);
+            }
+          }
+    }
+    return;
+  }
+  float2 s2[4][C], e2[4][C];
 #pragma unroll
   for (int r = 0; r < 4; ++r)
 #pragma unroll
-    for (int c = 0; c < C; ++c) s[r][c] = e[r][c] = 0.f;
+    for (int c = 0; c < C; ++c) s2[r][c] = e2[r][c] = make_float2(0.f, 0.f);
   const int ao = ra * ld, bo = cb * ld, n4 = (n + 3) >> 2;
 #pragma unroll 2
   for (int k = 0; k < 4 * n4; k += 4) {
@@ -198,35 +256,46 @@ __device__ __forceinline__ void split_tile(const float* A, const float* Ah, cons
       if constexpr (!FULL_A) bf[c] = ld4(B + bo + 16 * c * ld + k);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
       for (int r = 0; r < 4; ++r)
 #pragma unroll
         for (int c = 0; c < C; ++c) {
-          s[r][c] = __fmaf_rn(el(ah[r], i), el(bh[c], i), s[r][c]);   // exact
+          s2[r][c] = fma2(pair(ah[r], h), pair(bh[c], h), s2[r][c]);   // exact
           if constexpr (FULL_A) {
-            e[r][c] = __fmaf_rn(el(al[r], i), el(bh[c], i), e[r][c]);
-            e[r][c] = __fmaf_rn(el(af[r], i), el(bl[c], i), e[r][c]);
+            e2[r][c] = fma2(pair(al[r], h), pair(bh[c], h), e2[r][c]);
+            e2[r][c] = fma2(pair(af[r], h), pair(bl[c], h), e2[r][c]);
           } else {
-            e[r][c] = __fmaf_rn(el(ah[r], i), el(bl[c], i), e[r][c]);
-            e[r][c] = __fmaf_rn(el(al[r], i), el(bf[c], i), e[r][c]);
+            e2[r][c] = fma2(pair(ah[r], h), pair(bl[c], h), e2[r][c]);
+            e2[r][c] = fma2(pair(al[r], h), pair(bf[c], h), e2[r][c]);
           }
         }
   }
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+      s[r][c] = __fadd_rn(s2[r][c].x, s2[r][c].y);
+      e[r][c] = __fadd_rn(e2[r][c].x, e2[r][c].y);
+    }
 }
 
 // split_tile<C, false> and dot_tile<C> of two row sets in one reduction
 // loop (both products reduce over n): S from the split rows Ah, Al / B, Bh,
-// Bl and X[r][c] = sum_k D[ra + 16 r][k] E[cb + 16 c][k].
+// Bl and X[r][c] = sum_k D[ra + 16 r][k] E[cb + 16 c][k]. Two-lane FMAs
+// carry the even and the odd reduction indices in separate partial sums,
+// added at the end (the coarse sums stay exact: any subset of the coarse
+// products sums exactly).
 template <int C>
 __device__ __forceinline__ void split_dot_tile(const float* Ah, const float* Al, const float* B, const float* Bh,
                                                const float* Bl, const float* D, const float* E, int ld, int ra,
                                                int cb, int n, float (&s)[4][C], float (&e)[4][C],
                                                float (&x)[4][C]) {
+  float2 s2[4][C], e2[4][C], x2[4][C];
 #pragma unroll
   for (int r = 0; r < 4; ++r)
 #pragma unroll
-    for (int c = 0; c < C; ++c) s[r][c] = e[r][c] = x[r][c] = 0.f;
+    for (int c = 0; c < C; ++c) s2[r][c] = e2[r][c] = x2[r][c] = make_float2(0.f, 0.f);
   const int ao = ra * ld, bo = cb * ld, n4 = (n + 3) >> 2;
 #pragma unroll 2
   for (int k = 0; k < 4 * n4; k += 4) {
@@ -245,17 +314,25 @@ __device__ __forceinline__ void split_dot_tile(const float* Ah, const float* Al,
       be[c] = ld4(E + bo + 16 * c * ld + k);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
       for (int r = 0; r < 4; ++r)
 #pragma unroll
         for (int c = 0; c < C; ++c) {
-          s[r][c] = __fmaf_rn(el(ah[r], i), el(bh[c], i), s[r][c]);   // exact
-          e[r][c] = __fmaf_rn(el(ah[r], i), el(bl[c], i), e[r][c]);
-          e[r][c] = __fmaf_rn(el(al[r], i), el(bf[c], i), e[r][c]);
-          x[r][c] = fmaf(el(ad[r], i), el(be[c], i), x[r][c]);
+          s2[r][c] = fma2(pair(ah[r], h), pair(bh[c], h), s2[r][c]);   // exact
+          e2[r][c] = fma2(pair(ah[r], h), pair(bl[c], h), e2[r][c]);
+          e2[r][c] = fma2(pair(al[r], h), pair(bf[c], h), e2[r][c]);
+          x2[r][c] = fma2(pair(ad[r], h), pair(be[c], h), x2[r][c]);
         }
   }
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+      s[r][c] = __fadd_rn(s2[r][c].x, s2[r][c].y);
+      e[r][c] = __fadd_rn(e2[r][c].x, e2[r][c].y);
+      x[r][c] = __fadd_rn(x2[r][c].x, x2[r][c].y);
+    }
 }
 
 // S[r][c] = sum_k A[ra + 16 r][k] B[cb + 16 c][k] over k < n, by Dot2: hi in
@@ -337,9 +414,17 @@ __device__ __forceinline__ void acc_tile(const float* P, int ldp, const float* V
 #pragma unroll
       for (int g = 0; g < Q / 4; ++g) b[g] = ld4(v0 + (k + i) * ldv + 64 * g);
 #pragma unroll
-      for (int r = 0; r < R; ++r)
+      for (int r = 0; r < R; ++r) {
+        const float2 ar = make_float2(el(a[r], i), el(a[r], i));
 #pragma unroll
-        for (int q = 0; q < Q; ++q) acc[r][q] = fmaf(el(a[r], i), el(b[q >> 2], q & 3), acc[r][q]);
+        for (int g = 0; g < Q / 4; ++g)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {   // columns 4g + 2h, 4g + 2h + 1: two lanes of one FMA
+            const float2 t = fma2(ar, pair(b[g], h), make_float2(acc[r][4 * g + 2 * h], acc[r][4 * g + 2 * h + 1]));
+            acc[r][4 * g + 2 * h] = t.x;
+            acc[r][4 * g + 2 * h + 1] = t.y;
+          }
+      }
     }
   }
 }
@@ -377,7 +462,7 @@ __host__ __device__ inline int tile_width(int d, int dv) {
 // order through the online softmax; O (4 x W/16 per thread) in registers.
 // SPLIT: scores from split rows (Q whole and split, K split), else by Dot2.
 template <int W, int BN, bool SPLIT>
-__global__ void __launch_bounds__(NT) fwd_kernel(const float* __restrict__ Q, const float* __restrict__ K,
+__global__ void __launch_bounds__(NT, 1) fwd_kernel(const float* __restrict__ Q, const float* __restrict__ K,
                                                  const float* __restrict__ V, float* __restrict__ O,
                                                  float* __restrict__ LSE, const Problem p) {
   constexpr int LD = W + 4, LDP = BN + 4, NC = BN / 16, NQ = W / 16;
@@ -715,7 +800,7 @@ __global__ void __launch_bounds__(NT, 1) dkdv_kernel(const BwdArgs a, int with_d
 // tiles of BK keys in a fixed order and writes dQ once. SPLIT: scores from
 // split rows (Q split, K whole and split), else by Dot2.
 template <int W, int BK, bool SPLIT>
-__global__ void __launch_bounds__(NT) dq_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(NT, 1) dq_kernel(const BwdArgs a) {
   constexpr int LD = W + 4, LDS = BK + 4, NC = BK / 16, NQ = W / 16;
   extern __shared__ __align__(16) float smem_f[];
   float* sQ = smem_f;                            // [BM][LD] Q (split: its coarse parts, then remainders)
