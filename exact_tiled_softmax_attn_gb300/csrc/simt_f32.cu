@@ -32,7 +32,10 @@
 // holds d and dv): 16-byte aligned, and 8 consecutive rows start in 8
 // different groups of four banks, so a warp's 128-bit loads of 16 rows take
 // the two wavefronts their 256 bytes need. Columns from d (or dv) to W hold
-// zeros.
+// zeros. The products issue two-lane FMAs (fma.rn.f32x2) where their
+// accumulators fit in registers. Each kernel runs one CTA per SM (its split
+// tiles take most of the shared memory); a step's streamed tile loads into
+// registers while the previous step's P V-shaped products run.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include <stdint.h>
@@ -167,7 +170,8 @@ __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast
 // The reduction products below read 4 consecutive reduction indices per
 // 128-bit shared-memory load, over ceil(n / 4) * 4 indices: tiles are
 // zero-filled to their width W (a multiple of 4), so the extra indices add 0.
-// Each accumulator still takes its terms in ascending index order.
+// Each accumulator (each lane of a two-lane one) takes its terms in
+// ascending index order, so every result is the same from run to run.
 
 // a * b + c in each of two fp32 lanes, one instruction (sm_100 and later);
 // each lane rounded as the scalar FMA
@@ -395,7 +399,8 @@ __device__ __forceinline__ void dot_tile(const float* A, const float* B, int ld,
 __device__ __forceinline__ int acc_col(int tx, int q) { return 64 * (q >> 2) + 4 * tx + (q & 3); }
 
 // acc[r][q] += sum_k P[ra + 16 r][k] V[k][acc_col(tx, q)] over k < n: P
-// with rows of `ldp` floats, V with rows of `ldv` floats.
+// with rows of `ldp` floats, V with rows of `ldv` floats. Two adjacent
+// columns share one two-lane FMA, P's element broadcast to both lanes.
 template <int R, int Q>
 __device__ __forceinline__ void acc_tile(const float* P, int ldp, const float* V, int ldv, int ra, int tx, int n,
                                          float (&acc)[R][Q]) {
