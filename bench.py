@@ -510,7 +510,7 @@ def run_ours(args, w):
         peak = props.multi_processor_count * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
     tag = "simt::" if f32 else ""
     if n_splits > 1:
-        fwd_name = f"fwd split-KV, {n_splits} splits (attn_fwd_bf16_kernel + merge)"
+        fwd_name = f"fwd split-KV, {n_splits} splits ({'simt::fwd_kernel' if f32 else 'attn_fwd_bf16_kernel'} + merge)"
     else:
         fwd_name = "fwd (simt::fwd_kernel)" if f32 else \
             ("fwd (attn_fwd_d256_pair_kernel)" if w.dv > 64 else "fwd (attn_fwd_d256_kernel)") if w.d > 128 else \
@@ -583,7 +583,7 @@ def run_ours(args, w):
         # bf16: fwd (+ split-KV merge), dQ (+ split reduction), dK/dV | fwd (+ merge), preprocess,
         # dK/dV, convert; fp32: fwd, preprocess, dK/dV, dQ | fwd, preprocess, dK/dV
         "gpu_launches": args.steps * ((1 + (1 if n_splits > 1 else 0)) if args.fwd_only else
-                                      (4 if det else 3) if f32 else
+                                      (4 if det else 3) + (1 if n_splits > 1 else 0) if f32 else
                                       # d = 256: forward, dQ (it forms D), dV, dK kernels
                                       (4 + (1 if n_splits > 1 else 0)) if w.d > 128 else
                                       ((3 if det else 4) + (1 if n_splits > 1 else 0) +

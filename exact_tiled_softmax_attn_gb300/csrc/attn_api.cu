@@ -248,23 +248,40 @@ PadLayout pad_layout(int B, int H, int Tq, int Tk, int d, int dv, int determinis
   return L;
 }
 
-// Split-KV forward: effective number of key splits for a request (0 = pick
-// one so that the forward's units times the splits fill the SMs once, with
-// at least two key tiles per split), clamped to [1, min(key tiles, 64)]; the
-// key tiles per split go to *split_tiles. fp32 problems never split. A unit
-// is a pair of 128-row query tiles for rows of up to 128 columns and one
-// query tile for wider rows; key tiles are 128 keys for both.
+// Split-KV forward: effective number of key splits for a request, clamped to
+// [1, min(key tiles, 64)]; the key tiles per split go to *split_tiles. A
+// bf16 unit is a pair of 128-row query tiles for rows of up to 128 columns
+// and one query tile for wider rows, with 128-key tiles; an fp32 unit is one
+// 64-row query tile, with 64-key tiles (one CTA per SM either way). Request
+// 0 picks the count: the time of S splits is taken as the waves of units * S
+// CTAs over the SMs times the key tiles of a split, and S is the smallest
+// count within 5 % of the best (at least two key tiles per split). A bf16
+// problem with at least as many units as SMs does not split: its persistent
+// forward spreads the units over the SMs itself.
 int splitkv_count(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dt, int req, int num_sms,
                   int* split_tiles) {
-  const int rows_per_unit = bf16_wide(d, dv) ? 128 : 256;
-  const int nkb = (Tk + 127) / 128;
+  const bool f32 = dt == ATTN_F32;
+  const int tile = f32 ? kF32SplitTile : 128;
+  const int rows_per_unit = f32 ? kF32SplitTile : bf16_wide(d, dv) ? 128 : 256;
+  const int nkb = (Tk + tile - 1) / tile;
   int S = req;
-  if (dt != ATTN_BF16 || nkb <= 1 || B == 0 || H == 0 || Tq == 0) {
+  if (nkb <= 1 || B == 0 || H == 0 || Tq == 0) {
     S = 1;
   } else if (req == 0) {
     const long long units = static_cast<long long>(B) * H * ((Tq + rows_per_unit - 1) / rows_per_unit);
-    S = units >= num_sms ? 1 : static_cast<int>((num_sms + units - 1) / units);
-    S = S < nkb / 2 ? S : (nkb / 2 > 1 ? nkb / 2 : 1);
+    if ((!f32 && units >= num_sms) || num_sms <= 0) {
+      S = 1;
+    } else {
+      const int smax = nkb / 2 < 64 ? (nkb / 2 > 1 ? nkb / 2 : 1) : 64;
+      auto cost = [&](int s) {   // waves x key tiles per split, in units of one key tile's work
+        const long long cs = (nkb + s - 1) / s, se = (nkb + cs - 1) / cs;
+        return static_cast<double>((units * se + num_sms - 1) / num_sms) * static_cast<double>(cs);
+      };
+      double best = cost(1);
+      for (int s = 2; s <= smax; ++s) best = cost(s) < best ? cost(s) : best;
+      S = 1;
+      while (S < smax && cost(S) > 1.05 * best) ++S;
+    }
   }
   if (S > nkb) S = nkb;
   if (S > 64) S = 64;
@@ -278,13 +295,15 @@ struct SplitLayout {
   size_t lse_off, total;
 };
 // Workspace of the split-KV forward: Opart [S][B*H*Tq][dv] fp32 | LSEpart
-// [S][B*H*Tq] fp32, each part 256-byte aligned; nothing when S = 1.
-SplitLayout split_layout(int B, int H, int Tq, int dv, int S) {
+// [S][B*H*Tq] (fp32 for bf16 problems, fp64 for fp32 ones), each part
+// 256-byte aligned; nothing when S = 1.
+SplitLayout split_layout(int B, int H, int Tq, int dv, int S, attn_dtype_t dt) {
   SplitLayout L{};
   if (S <= 1) return L;
   const size_t rows = static_cast<size_t>(B) * H * Tq;
+  const size_t lse_bytes = dt == ATTN_F32 ? sizeof(double) : sizeof(float);
   L.lse_off = round_up(static_cast<size_t>(S) * rows * dv * sizeof(float), 256);
-  L.total = L.lse_off + round_up(static_cast<size_t>(S) * rows * sizeof(float), 256);
+  L.total = L.lse_off + round_up(static_cast<size_t>(S) * rows * lse_bytes, 256);
   return L;
 }
 
@@ -294,7 +313,6 @@ attn_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, flo
   attn_status_t s = check_common(B, H, Tq, Tk, d, dv, scale, causal, dtype);
   if (s != ATTN_OK) return s;
   if (split_req < 0) return ATTN_ERR_INVALID_ARG;
-  if (dtype == ATTN_F32 && split_req > 1) return ATTN_ERR_UNSUPPORTED;
   // the CUDA-core forward keeps a key tile of K and V rows in shared memory:
   // with d or dv above 128 a 128-key tile does not fit
   if (dtype == ATTN_F32 && fwd_f32_smem_bytes(block_n, d, dv) > 227 * 1024) return ATTN_ERR_UNSUPPORTED;
@@ -317,9 +335,9 @@ attn_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, flo
   DeviceInfo* di = nullptr;
   if (split_req != 1) {
     // only the automatic choice needs the device (its SM count)
-    if (split_req == 0 && dtype == ATTN_BF16 && (s = device_info(&di)) != ATTN_OK) return s;
+    if (split_req == 0 && (s = device_info(&di)) != ATTN_OK) return s;
     n_splits = splitkv_count(B, H, Tq, Tk, d, dv, dtype, split_req, di ? di->num_sms : 0, &split_tiles);
-    SL = split_layout(B, H, Tq, dv, n_splits);
+    SL = split_layout(B, H, Tq, dv, n_splits, dtype);
     if (SL.total > 0) {
       if (workspace == nullptr || workspace_bytes < SL.total || reinterpret_cast<uintptr_t>(workspace) % 256)
         return ATTN_ERR_WORKSPACE;
@@ -351,12 +369,19 @@ attn_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, flo
   a.split_tiles = split_tiles;
   if (n_splits > 1) {
     a.Opart = static_cast<float*>(workspace);
-    a.LSEpart = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + SL.lse_off);
+    uint8_t* lse_part = static_cast<uint8_t*>(workspace) + SL.lse_off;
+    if (dtype == ATTN_F32)
+      a.LSEpart64 = reinterpret_cast<double*>(lse_part);
+    else
+      a.LSEpart = reinterpret_cast<float*>(lse_part);
   }
   a.stream = st;
   cudaError_t e;
   if (dtype == ATTN_F32) {
     e = launch_fwd_f32(a);
+    if (e == cudaSuccess && n_splits > 1)
+      e = launch_splitkv_merge_f32(p, a.Opart, a.LSEpart64, n_splits, split_tiles, kF32SplitTile,
+                                   static_cast<float*>(O), LSE, di->num_sms, st);
   } else {
     // Rows wider than 128 columns: on CTA pairs (each CTA loads 64-key
     // halves of K and 128-key tiles of half of V's columns) unless the keys
@@ -412,9 +437,8 @@ attn_status_t attn_fwd(const void* Q, const void* K, const void* V, void* O, flo
 
 int attn_fwd_splitkv_splits(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype, int num_splits) {
   if (check_common(B, H, Tq, Tk, d, dv, 1.0f, 0, dtype) != ATTN_OK || num_splits < 0) return -1;
-  if (dtype == ATTN_F32 && num_splits > 1) return -1;
   int num_sms = 0;
-  if (num_splits == 0 && dtype == ATTN_BF16) {
+  if (num_splits == 0) {
     DeviceInfo* di;
     if (device_info(&di) != ATTN_OK) return -1;
     num_sms = di->num_sms;
@@ -427,7 +451,7 @@ size_t attn_fwd_splitkv_workspace_size(int B, int H, int Tq, int Tk, int d, int 
                                        int num_splits) {
   const int S = attn_fwd_splitkv_splits(B, H, Tq, Tk, d, dv, dtype, num_splits);
   if (S < 1) return 0;
-  return split_layout(B, H, Tq, dv, S).total;
+  return split_layout(B, H, Tq, dv, S, dtype).total;
 }
 
 attn_status_t attn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,

@@ -30,6 +30,7 @@ struct LaunchFwd {
   int split_tiles;
   float* Opart;
   float* LSEpart;
+  double* LSEpart64;        // fp32 path: the split log-sum-exps in fp64 (instead of LSEpart)
   cudaStream_t stream;
 };
 
@@ -102,6 +103,14 @@ cudaError_t launch_bwd_bf16_d256(const LaunchBwd& a);
 // that hold at least one of its key tiles)
 cudaError_t launch_splitkv_merge(const Problem& p, const float* Opart, const float* LSEpart, int n_splits,
                                  int split_tiles, void* O, float* LSE, int num_sms, cudaStream_t s);
+// The same for the fp32 forward's key ranges (fp32 O, fp64 partial
+// log-sum-exps; `tile` rows per query tile and keys per key tile of that
+// forward)
+cudaError_t launch_splitkv_merge_f32(const Problem& p, const float* Opart, const double* LSEpart, int n_splits,
+                                     int split_tiles, int tile, float* O, float* LSE, int num_sms, cudaStream_t s);
+// Rows of the fp32 forward's query tiles and keys of its key tiles when its
+// keys are split into ranges (attn_fwd_splitkv)
+constexpr int kF32SplitTile = 64;
 
 // shared small kernels
 cudaError_t launch_fill_empty_fwd(const Problem& p, void* O, float* LSE, int elem_bytes, cudaStream_t s);

@@ -463,13 +463,27 @@ __host__ __device__ inline int tile_width(int d, int dv) {
 
 // ---------------------------------------------------------------- forward
 
-// One CTA per (64-row query tile, head); key tiles of BN keys in ascending
-// order through the online softmax; O (4 x W/16 per thread) in registers.
-// SPLIT: scores from split rows (Q whole and split, K split), else by Dot2.
+// Key ranges of the split-KV forward: range z of a query tile holds its key
+// tiles [z * tiles, (z + 1) * tiles); with n > 1 each (query tile, range)
+// writes its own normalized O_z = A_z / l_z and LSE_z to Opart [n][B*H*Tq][dv]
+// and LSEpart [n][B*H*Tq] (rows with no allowed key in the range: 0 and
+// -inf), for the merge kernel. LSE_z stays in fp64: at logits in the
+// thousands an fp32 LSE_z is off by up to 1e-4, and the merge weights
+// exp(LSE_z - max) would carry that into O.
+struct KeyRanges {
+  int n, tiles;
+  float* Opart;
+  double* LSEpart;
+};
+
+// One CTA per (64-row query tile, head, key range); key tiles of BN keys in
+// ascending order through the online softmax; O (4 x W/16 per thread) in
+// registers. SPLIT: scores from split rows (Q whole and split, K split),
+// else by Dot2.
 template <int W, int BN, bool SPLIT>
 __global__ void __launch_bounds__(NT, 1) fwd_kernel(const float* __restrict__ Q, const float* __restrict__ K,
                                                  const float* __restrict__ V, float* __restrict__ O,
-                                                 float* __restrict__ LSE, const Problem p) {
+                                                 float* __restrict__ LSE, const Problem p, const KeyRanges ranges) {
   constexpr int LD = W + 4, LDP = BN + 4, NC = BN / 16, NQ = W / 16;
   extern __shared__ __align__(16) float smem_f[];
   float* sQ = smem_f;                              // [BM][LD]
@@ -484,6 +498,12 @@ __global__ void __launch_bounds__(NT, 1) fwd_kernel(const float* __restrict__ Q,
   const int q0 = blockIdx.x * BM;
   const size_t bh = blockIdx.y;
   const float scale = p.scale;
+  int n_kv = (Tk + BN - 1) / BN;
+  if (p.causal) n_kv = min(n_kv, (q0 + BM - 1) / BN + 1);
+  // this CTA's key tiles [j0, j1): a range past the causal limit has none
+  // (the merge does not read it)
+  const int j0 = blockIdx.z * ranges.tiles, j1 = ranges.n > 1 ? min(n_kv, j0 + ranges.tiles) : n_kv;
+  if (j0 >= j1 && ranges.n > 1) return;
 
   if constexpr (SPLIT)
     load_split<W, BM>(sQ, sQh, sQl, LD, Q + (bh * Tq + q0) * d, d, Tq - q0);
@@ -497,17 +517,15 @@ __global__ void __launch_bounds__(NT, 1) fwd_kernel(const float* __restrict__ Q,
 #pragma unroll
     for (int q = 0; q < NQ; ++q) acc[r][q] = 0.f;
   }
-  int n_kv = (Tk + BN - 1) / BN;
-  if (p.causal) n_kv = min(n_kv, (q0 + BM - 1) / BN + 1);
 
   // split rows: a key tile's K and V rows load into registers while the
   // previous tile's P V product runs
   RowRegs<W, BN> kr, vr;
   if constexpr (SPLIT) {
-    kr.load(K + bh * Tk * d, d, Tk);
-    vr.load(V + bh * Tk * dv, dv, Tk);
+    kr.load(K + (bh * Tk + j0 * BN) * d, d, Tk - j0 * BN);
+    vr.load(V + (bh * Tk + j0 * BN) * dv, dv, Tk - j0 * BN);
   }
-  for (int jt = 0; jt < n_kv; ++jt) {
+  for (int jt = j0; jt < j1; ++jt) {
     const int kv0 = jt * BN;
     __syncthreads();   // the previous tile's P V is done with sK, sV, sP
     if constexpr (SPLIT) {
@@ -555,7 +573,7 @@ __global__ void __launch_bounds__(NT, 1) fwd_kernel(const float* __restrict__ Q,
     }
     __syncthreads();
     if constexpr (SPLIT) {
-      if (jt + 1 < n_kv) {
+      if (jt + 1 < j1) {
         kr.load(K + (bh * Tk + kv0 + BN) * d, d, Tk - kv0 - BN);
         vr.load(V + (bh * Tk + kv0 + BN) * dv, dv, Tk - kv0 - BN);
       }
@@ -563,19 +581,25 @@ __global__ void __launch_bounds__(NT, 1) fwd_kernel(const float* __restrict__ Q,
     // acc += P V over the tile's keys (padding keys have P = 0 and V = 0)
     acc_tile<4, NQ>(sP, LDP, sV, LD, ty, tx, min(BN, Tk - kv0), acc);
   }
+  // with key ranges, this range's partial state goes to the workspace
+  const size_t rows = static_cast<size_t>(p.B) * p.H * Tq;
+  float* Oout = ranges.n > 1 ? ranges.Opart + blockIdx.z * rows * dv : O;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int qi = q0 + ty + 16 * r;
     if (qi >= Tq) continue;
     const float inv = l[r] > 0.f ? 1.0f / l[r] : 0.f;
-    float* orow = O + (bh * Tq + qi) * dv;
+    float* orow = Oout + (bh * Tq + qi) * dv;
 #pragma unroll
     for (int q = 0; q < NQ; ++q)
       if (acc_col(tx, q) < dv) orow[acc_col(tx, q)] = acc[r][q] * inv;
     if (tx == 0) {
       const float ref = m[r] == -CUDART_INF_F ? 0.f : m[r];
-      LSE[bh * Tq + qi] = l[r] > 0.f ? static_cast<float>(static_cast<double>(ref) + log(static_cast<double>(l[r])))
-                                     : -CUDART_INF_F;
+      const double lse = l[r] > 0.f ? static_cast<double>(ref) + log(static_cast<double>(l[r])) : -CUDART_INF;
+      if (ranges.n > 1)
+        ranges.LSEpart[blockIdx.z * rows + bh * Tq + qi] = lse;
+      else
+        LSE[bh * Tq + qi] = static_cast<float>(lse);
     }
   }
 }
@@ -600,10 +624,12 @@ cudaError_t fwd_launch(const LaunchFwd& a) {
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<W, BN, SP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid((a.p.Tq + BM - 1) / BM, a.p.B * a.p.H);
+  const int n_ranges = a.n_splits > 1 ? a.n_splits : 1;
+  dim3 grid((a.p.Tq + BM - 1) / BM, a.p.B * a.p.H, n_ranges);
+  const KeyRanges kr{n_ranges, a.split_tiles, a.Opart, a.LSEpart64};
   fwd_kernel<W, BN, SP><<<grid, NT, smem, a.stream>>>(static_cast<const float*>(a.Q), static_cast<const float*>(a.K),
                                                   static_cast<const float*>(a.V), static_cast<float*>(a.O), a.LSE,
-                                                  a.p);
+                                                  a.p, kr);
   return cudaGetLastError();
 }
 
@@ -977,7 +1003,9 @@ size_t fwd_f32_smem_bytes(int block_n, int d, int dv) {
 
 cudaError_t launch_fwd_f32(const LaunchFwd& a) {
   using namespace simt;
+  static_assert(BM == kF32SplitTile, "key ranges count 64-row query tiles and 64-key tiles");
   const int W = tile_width(a.p.d, a.p.dv);
+  if (a.n_splits > 1 && a.block_n != kF32SplitTile) return cudaErrorInvalidValue;
   switch (a.block_n) {
     case 32: return W == 64 ? fwd_launch<64, 32>(a) : W == 128 ? fwd_launch<128, 32>(a) : fwd_launch<256, 32>(a);
     case 128:

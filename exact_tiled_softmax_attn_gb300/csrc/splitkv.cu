@@ -91,7 +91,70 @@ __global__ void __launch_bounds__(NT) merge_kernel(const float* __restrict__ Opa
   }
 }
 
+// The same merge for fp32 outputs (the CUDA-core forward's key ranges): one
+// warp per output row, lane c handling columns c, c + 32, ... (any dv up to
+// 256, rows with no alignment beyond 4 bytes). The partial log-sum-exps are
+// fp64 and the weights are formed in fp64 (at logits in the thousands an
+// fp32 LSE_s is off by up to 1e-4). `tile`: rows per query tile and keys per
+// key tile of the forward that wrote the partials.
+__global__ void __launch_bounds__(NT) merge_f32_kernel(const float* __restrict__ Opart,
+                                                       const double* __restrict__ LSEpart, float* __restrict__ O,
+                                                       float* __restrict__ LSE, long long rows, int Tq, int dv,
+                                                       int n_splits, int split_tiles, int n_kv_tiles, int tile,
+                                                       int causal) {
+  const int lane = threadIdx.x & 31;
+  const long long warp_id = (static_cast<long long>(blockIdx.x) * NT + threadIdx.x) >> 5;
+  const long long n_warps = (static_cast<long long>(gridDim.x) * NT) >> 5;
+  for (long long r = warp_id; r < rows; r += n_warps) {
+    const int q = static_cast<int>(r % Tq);
+    // the ranges the forward ran for this row's query tile (key tiles up to
+    // the diagonal tile under the causal mask)
+    const int qt = q / tile;
+    const int nt = causal ? min(qt + 1, n_kv_tiles) : n_kv_tiles;
+    const int ns = min(n_splits, (nt + split_tiles - 1) / split_tiles);
+    double mx = -CUDART_INF;
+    for (int s = 0; s < ns; ++s) mx = fmax(mx, LSEpart[static_cast<long long>(s) * rows + r]);
+    float acc[8];
+#pragma unroll
+    for (int h = 0; h < 8; ++h) acc[h] = 0.f;
+    float lse = -CUDART_INF_F;
+    if (mx != -CUDART_INF) {
+      double wsum = 0.0;
+      for (int s = 0; s < ns; ++s) {
+        const double w = exp(LSEpart[static_cast<long long>(s) * rows + r] - mx);   // 0: no allowed key
+        const float wgt = static_cast<float>(w);
+        wsum += w;
+        const float* orow = Opart + (static_cast<long long>(s) * rows + r) * dv;
+#pragma unroll
+        for (int h = 0; h < 8; ++h)
+          if (lane + 32 * h < dv) acc[h] = fmaf(wgt, orow[lane + 32 * h], acc[h]);
+      }
+      const float inv = static_cast<float>(1.0 / wsum);
+#pragma unroll
+      for (int h = 0; h < 8; ++h) acc[h] *= inv;
+      lse = static_cast<float>(mx + log(wsum));
+    }
+#pragma unroll
+    for (int h = 0; h < 8; ++h)
+      if (lane + 32 * h < dv) O[r * dv + lane + 32 * h] = acc[h];
+    if (lane == 0) LSE[r] = lse;
+  }
+}
+
 }  // namespace splitkv
+
+cudaError_t launch_splitkv_merge_f32(const Problem& p, const float* Opart, const double* LSEpart, int n_splits,
+                                     int split_tiles, int tile, float* O, float* LSE, int num_sms, cudaStream_t s) {
+  const long long rows = static_cast<long long>(p.B) * p.H * p.Tq;
+  if (rows == 0) return cudaSuccess;
+  if (p.dv > 256 || n_splits < 1 || n_splits > splitkv::kMaxSplits || split_tiles < 1 || tile < 1)
+    return cudaErrorInvalidValue;
+  const long long want = (rows + splitkv::NT / 32 - 1) / (splitkv::NT / 32);
+  const int grid = static_cast<int>(want < num_sms * 16LL ? want : num_sms * 16LL);
+  splitkv::merge_f32_kernel<<<grid, splitkv::NT, 0, s>>>(Opart, LSEpart, O, LSE, rows, p.Tq, p.dv, n_splits,
+                                                         split_tiles, (p.Tk + tile - 1) / tile, tile, p.causal);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_splitkv_merge(const Problem& p, const float* Opart, const float* LSEpart, int n_splits,
                                  int split_tiles, void* O, float* LSE, int num_sms, cudaStream_t s) {

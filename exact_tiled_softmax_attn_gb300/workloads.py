@@ -23,6 +23,7 @@ c4     B2  H8  Tq=1000 Tk=4000 d=dv=128             f32    none    1/sqrt(128) 3
 c5     B1  H32 Tq=Tk=32768 d=dv=128                 bf16   causal  1/sqrt(128) 4
 s1     B1  H8  Tq=256 Tk=65536 d=dv=128             bf16   none    1/sqrt(128) 5
        (few query tiles, many keys: the split-KV forward's case)
+s1f    the same shape and seed                      f32    none    1/sqrt(128) 5
 m1     B2  H16 Tq=Tk=4096  d=64 dv=128              bf16   causal  1/sqrt(64)  6
 =====  ===========================================  =====  ======  ==========  ====
 
@@ -98,6 +99,8 @@ WORKLOADS: Dict[str, Workload] = {
     # few query tiles against many keys (8 query-tile pairs for 152 SMs): the
     # split-KV forward's case
     "s1": Workload("s1", 1, 8, 256, 65536, 128, 128, "bf16", False, 5),
+    # the same in fp32 (32 query tiles of 64 rows: the fp32 split-KV forward's case)
+    "s1f": Workload("s1f", 1, 8, 256, 65536, 128, 128, "f32", False, 5),
     # V with its own head dimension (d = 64, dv = 128)
     "m1": Workload("m1", 2, 16, 4096, 4096, 64, 128, "bf16", True, 6),
     # head size 256 (forward and backward on the tensor cores)

@@ -104,8 +104,10 @@ ATTN_API attn_status_t attn_fwd_f32_blocked(const float* Q, const float* K, cons
 
 /*
  * Split-KV forward for problems with few query tiles per SM (small B*H*Tq,
- * long Tk): the key tiles of every pair of 128-row query tiles are divided
- * into S contiguous ranges ("splits") that run as separate work units; each
+ * long Tk): the key tiles of every query-tile unit (bf16: a pair of 128-row
+ * query tiles, one tile for d = 256, 128-key tiles; fp32: one 64-row query
+ * tile, 64-key tiles) are divided into S contiguous ranges ("splits") that
+ * run as separate work units; each
  * writes its partial softmax state for its keys (O_s = A_s / l_s and LSE_s,
  * fp32) to `workspace`, and a merge kernel combines the splits with the
  * associative rescale of the running max, sum and accumulator ("The Hidden
@@ -114,17 +116,18 @@ ATTN_API attn_status_t attn_fwd_f32_blocked(const float* Q, const float* K, cons
  *   M = max_s LSE_s, w_s = exp(LSE_s - M), O = sum_s w_s O_s / sum_s w_s,
  *   LSE = M + log sum_s w_s.
  * Same inputs, outputs, layout and mask as attn_fwd; O and LSE agree with
- * attn_fwd up to fp32 rounding order. num_splits = 0 picks S so that the
- * forward's units (pairs of 128-row query tiles; single query tiles for
- * d = 256) times S fill the SMs about once (at least two key tiles per
- * split); num_splits >= 1 asks for that many, clamped to the number of
- * 128-key tiles and 64. S = 1 is attn_fwd itself (no workspace). bf16 only
- * for S > 1: an fp32 problem with num_splits > 1 returns ATTN_ERR_UNSUPPORTED
- * (num_splits 0 or 1 runs the fp32 attn_fwd). `workspace` (256-byte aligned,
- * at least attn_fwd_splitkv_workspace_size bytes, not overlapping any other
- * argument; may be NULL when that is 0) holds Opart [S][B*H*Tq][dv] then
- * LSEpart [S][B*H*Tq], both fp32; else ATTN_ERR_WORKSPACE. Other errors as
- * attn_fwd; asynchronous on `stream`.
+ * attn_fwd up to fp32 rounding order. num_splits = 0 picks S from the
+ * current device's SM count: the smallest S whose time (the waves of units
+ * x S work units over the SMs, times the key tiles of a split) is within 5 %
+ * of the best, at least two key tiles per split; a bf16 problem with at
+ * least as many units as SMs keeps S = 1. num_splits >= 1 asks for that
+ * many, clamped to the number of key tiles and 64. S = 1 is attn_fwd itself (no workspace). `workspace`
+ * (256-byte aligned, at least attn_fwd_splitkv_workspace_size bytes, not
+ * overlapping any other argument; may be NULL when that is 0) holds Opart
+ * [S][B*H*Tq][dv] fp32 then LSEpart [S][B*H*Tq] (fp32 for bf16 problems;
+ * fp64 for fp32 ones, whose merge weights exp(LSE_s - max) must keep fp32
+ * accuracy at logits in the thousands); else ATTN_ERR_WORKSPACE. Other
+ * errors as attn_fwd; asynchronous on `stream`.
  */
 ATTN_API attn_status_t attn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
                                         int H, int Tq, int Tk, int d, int dv, float scale, int causal,

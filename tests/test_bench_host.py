@@ -50,7 +50,7 @@ def test_reduce_max_without_process_group_is_identity():
     assert bench.reduce_max(3.5) == 3.5
 
 
-@pytest.mark.parametrize("name", ["c1", "c1_causal", "c2", "c3", "c4", "c5", "s1", "m1", "w256"])
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
 def test_row_flops_sum_to_the_workload_count(name):
     w = WORKLOADS[name]
     one_head = (w.fwd_flop() + w.bwd_flop()) / (w.B * w.H)

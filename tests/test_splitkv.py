@@ -2,12 +2,12 @@
 parity of the split forward with the float64 oracle and with the plain
 forward on the GPU.
 
-The split forward divides each query-tile pair's key tiles into ranges whose
-partial softmax states are merged by the associative rescale of "The Hidden
-Recurrence in Softmax Attention", section "Chunk-wise Mode with Online Softmax
-Re-scale"; its result is the same attention ("Tiled attention with an online
-softmax", section "Task"), so the oracle and the tolerances are those of the
-bf16 forward.
+The split forward divides each query tile's (bf16: each query-tile pair's)
+key tiles into ranges whose partial softmax states are merged by the
+associative rescale of "The Hidden Recurrence in Softmax Attention", section
+"Chunk-wise Mode with Online Softmax Re-scale"; its result is the same
+attention ("Tiled attention with an online softmax", section "Task"), so the
+oracle and the tolerances are those of the plain forward of each dtype.
 """
 import math
 
@@ -38,8 +38,12 @@ def test_split_counts(Tk, req, want):
 
 def test_split_count_invalid_and_fp32():
     assert B.attn_fwd_splitkv_splits(1, 1, 128, 1024, 128, 128, B.ATTN_BF16, -1) == -1
-    assert B.attn_fwd_splitkv_splits(1, 1, 128, 1024, 128, 128, B.ATTN_F32, 2) == -1
-    assert B.attn_fwd_splitkv_splits(1, 1, 128, 1024, 128, 128, B.ATTN_F32, 0) == 1
+    # fp32 counts 64-key tiles: 1024 keys are 16 tiles
+    assert B.attn_fwd_splitkv_splits(1, 1, 128, 1024, 128, 128, B.ATTN_F32, 2) == 2
+    assert B.attn_fwd_splitkv_splits(1, 1, 128, 1024, 128, 128, B.ATTN_F32, 5) == 4   # ranges of 4 tiles
+    assert B.attn_fwd_splitkv_splits(1, 1, 128, 1024, 128, 128, B.ATTN_F32, 100) == 16
+    assert B.attn_fwd_splitkv_splits(1, 1, 128, 64, 128, 128, B.ATTN_F32, 4) == 1     # one key tile
+    assert B.attn_fwd_splitkv_splits(1, 1, 128, 1024, 300, 128, B.ATTN_F32, 2) == -1  # beyond 256 columns
     assert B.attn_fwd_splitkv_splits(1, 1, 128, 1024, 100, 100, B.ATTN_BF16, 2) == -1
     # padded widths split like the tile width they run on
     assert B.attn_fwd_splitkv_splits(1, 1, 128, 1024, 96, 40, B.ATTN_BF16, 2) == 2
@@ -54,11 +58,15 @@ def test_workspace_size_formula():
     assert B.attn_fwd_splitkv_workspace_size(Bn, H, Tq, Tk, d, d, B.ATTN_BF16, 3) == \
         r256(S * rows * d * 4) + r256(S * rows * 4)
     assert B.attn_fwd_splitkv_workspace_size(Bn, H, Tq, Tk, d, d, B.ATTN_BF16, 1) == 0
+    S = B.attn_fwd_splitkv_splits(Bn, H, Tq, Tk, 7, 13, B.ATTN_F32, 5)
+    # fp32: the partial log-sum-exps are fp64
+    assert S == 4 and B.attn_fwd_splitkv_workspace_size(Bn, H, Tq, Tk, 7, 13, B.ATTN_F32, 5) == \
+        r256(S * rows * 13 * 4) + r256(S * rows * 8)
 
 
 @pytest.mark.parametrize("kw,status", [
     (dict(num_splits=-1), B.ATTN_ERR_INVALID_ARG),
-    (dict(dtype=B.ATTN_F32, num_splits=2), B.ATTN_ERR_UNSUPPORTED),
+    (dict(dtype=B.ATTN_F32, num_splits=2, workspace_bytes=1024), B.ATTN_ERR_WORKSPACE),
     (dict(workspace=0, workspace_bytes=0), B.ATTN_ERR_WORKSPACE),
     (dict(workspace_bytes=1024), B.ATTN_ERR_WORKSPACE),
     (dict(workspace=0x9000010), B.ATTN_ERR_WORKSPACE),                  # misaligned
@@ -156,16 +164,57 @@ def test_splitkv_d256(shape, causal):
     assert (o.float() - o1.float()).abs().max().item() <= 2.0 ** -7 * max(1.0, o1.float().abs().max().item())
 
 
+F32_SHAPES = [  # B, H, Tq, Tk, d, dv, num_splits
+    (1, 2, 70, 300, 48, 40, 2),
+    (1, 2, 70, 300, 48, 40, 0),      # automatic: few query tiles, so it splits
+    (1, 1, 128, 4000, 128, 128, 0),
+    (2, 3, 1, 5000, 64, 64, 7),      # one query row per head
+    (1, 1, 200, 1000, 7, 13, 5),     # odd widths
+    (1, 2, 300, 700, 128, 128, 64),  # clamped to the key tiles
+    (1, 1, 1000, 300, 200, 136, 3),  # Tq > Tk; rows above 128 columns (compensated scores)
+    (1, 1, 100, 64, 64, 64, 4),      # one key tile: no split
+]
+
+
 @pytest.mark.gpu
-def test_splitkv_fp32_runs_the_plain_forward():
-    """fp32 never splits: num_splits 0 or 1 gives exactly attn_fwd's result."""
-    x = make_random((1, 2, 70, d := 48), (1, 2, 300, d), (1, 2, 300, 40), seed=5, dtype=torch.float32, device="cuda")
-    o1, l1 = B.forward(x["Q"], x["K"], x["V"], causal=True, scale=0.2)
-    for ns in (0, 1):
-        assert B.attn_fwd_splitkv_splits(1, 2, 70, 300, d, 40, B.ATTN_F32, ns) == 1
-        o, l = B.forward(x["Q"], x["K"], x["V"], causal=True, scale=0.2, num_splits=ns)
-        torch.cuda.synchronize()
-        assert torch.equal(o, o1) and torch.equal(l, l1)
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", F32_SHAPES)
+def test_splitkv_fp32_matches_oracle(shape, causal):
+    """fp32 split-KV forward (64-row query tiles, 64-key tiles, ranges merged
+    in fp32): the oracle at the fp32 bounds, and the plain fp32 forward up to
+    fp32 rounding order."""
+    Bn, H, Tq, Tk, d, dv, ns = shape
+    x = make_random((Bn, H, Tq, d), (Bn, H, Tk, d), (Bn, H, Tk, dv), seed=Tq + 3 * Tk + d, dtype=torch.float32,
+                    device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    o, lse = B.forward(x["Q"], x["K"], x["V"], causal=causal, scale=scale, num_splits=ns)
+    torch.cuda.synchronize()
+    assert B.attn_device_status() == B.ATTN_OK
+    O, L = ref.forward(x["Q"], x["K"], x["V"], scale, causal)
+    check_o(o, O, torch.float32)
+    check_lse(lse, L, torch.float32)
+    o1, lse1 = B.forward(x["Q"], x["K"], x["V"], causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert (lse - lse1).abs().max().item() <= 1e-5 * max(1.0, lse1.abs().max().item())
+    assert (o - o1).abs().max().item() <= 1e-5 * max(1.0, o1.abs().max().item())
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("scale", [1.0 / math.sqrt(128), 1.0])
+def test_splitkv_fp32_banded_keys(scale):
+    """The c4 key bands (rows of K scaled by +-40 in alternating 128-key
+    bands; logits beyond 1000 at scale 1) through the fp32 split forward: the
+    merge weights exp(LSE_s - max) span many orders of magnitude."""
+    from exact_tiled_softmax_attn_gb300.workloads import band_signs
+    Bn, H, Tq, Tk, d = 1, 2, 100, 4000, 128
+    x = make_random((Bn, H, Tq, d), (Bn, H, Tk, d), (Bn, H, Tk, d), seed=41, dtype=torch.float32, device="cpu")
+    x["K"] = x["K"] * (40.0 * band_signs(Tk)).view(1, 1, Tk, 1)
+    xg = {k: v.cuda() for k, v in x.items()}
+    o, lse = B.forward(xg["Q"], xg["K"], xg["V"], causal=False, scale=scale, num_splits=6)
+    torch.cuda.synchronize()
+    O, L = ref.forward(x["Q"], x["K"], x["V"], scale, False)
+    check_o(o, O, torch.float32)
+    check_lse(lse, L, torch.float32)
 
 
 @pytest.mark.gpu
