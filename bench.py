@@ -374,7 +374,7 @@ def run_ours(args, w):
     # attn_bwd_phase) is not called, so that no event interval of the timed
     # step is an empty one.
     launches = {1: f32 or (not det and w.d <= 128), 5: bool(det) or w.d > 128, 6: bool(det), 4: True,
-                3: not f32 and w.d <= 128 and (not det or dq_splits > 1)}
+                3: (not f32 and w.d <= 128 and (not det or dq_splits > 1)) or (f32 and bool(det) and dq_splits > 1)}
     phases = () if args.fwd_only else tuple(ph for ph in (1, 6 if args.dq_pairs else 5, 4, 3) if launches[ph])
     slot = {1: 1, 5: 2, 6: 2, 4: 3, 3: 4}   # per-step interval of each group: fwd, pre, q, kv, conv
 
@@ -545,9 +545,10 @@ def run_ours(args, w):
             gbs = B * H * Tq * (2 * dv * es + 4 + 8 + (0 if (det or w.d > 128) else d * 4)) / (pre_ms * 1e-3) / 1e9
             kernels["bwd preprocess"] = {"ms": pre_ms, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]}
         if launches[3]:
-            # atomic: fp32 accumulator -> bf16; deterministic with split dQ: the partials' sum -> bf16
-            kernels["dQ convert"] = {"ms": conv_ms, "gbs": B * H * Tq * d * (4 * (1 if not det else dq_splits) + 2) /
-                                     (conv_ms * 1e-3) / 1e9}
+            # atomic: fp32 accumulator -> bf16; deterministic with split dQ: the partials' sum -> dQ
+            # (bf16, or fp32 for the fp32 path)
+            kernels["dQ convert"] = {"ms": conv_ms, "gbs": B * H * Tq * d * (4 * (1 if not det else dq_splits) +
+                                                                           (4 if f32 else 2)) / (conv_ms * 1e-3) / 1e9}
     # the dominant kernel: the longest of the single kernels
     dom = max((k for k, v in kernels.items() if "flop" in v), key=lambda k: kernels[k]["ms"])
     achieved = kernels[dom]["tflops"]
@@ -583,7 +584,8 @@ def run_ours(args, w):
         # bf16: fwd (+ split-KV merge), dQ (+ split reduction), dK/dV | fwd (+ merge), preprocess,
         # dK/dV, convert; fp32: fwd, preprocess, dK/dV, dQ | fwd, preprocess, dK/dV
         "gpu_launches": args.steps * ((1 + (1 if n_splits > 1 else 0)) if args.fwd_only else
-                                      (4 if det else 3) + (1 if n_splits > 1 else 0) if f32 else
+                                      (4 if det else 3) + (1 if n_splits > 1 else 0) +
+                                      (1 if det and dq_splits > 1 else 0) if f32 else
                                       # d = 256: forward, dQ (it forms D), dV, dK kernels
                                       (4 + (1 if n_splits > 1 else 0)) if w.d > 128 else
                                       ((3 if det else 4) + (1 if n_splits > 1 else 0) +

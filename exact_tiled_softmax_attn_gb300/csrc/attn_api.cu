@@ -152,6 +152,25 @@ attn_status_t check_ptr(const void* p, size_t bytes, size_t align) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Key splits for `units` work units of nkb key tiles each, one CTA per unit
+// and key range on `slots` SMs: the time of S splits is taken as the waves of
+// units * S CTAs times the key tiles of a split, and the result is the
+// smallest S within 5 % of the best, with at least two key tiles per split
+// and at most 64 splits.
+int wave_splits(long long units, int nkb, int slots) {
+  if (units <= 0 || slots <= 0 || nkb < 4) return 1;
+  const int smax = nkb / 2 < 64 ? nkb / 2 : 64;
+  auto cost = [&](int s) {   // waves x key tiles per split
+    const long long cs = (nkb + s - 1) / s, se = (nkb + cs - 1) / cs;
+    return static_cast<double>((units * se + slots - 1) / slots) * static_cast<double>(cs);
+  };
+  double best = cost(1);
+  for (int s = 2; s <= smax; ++s) best = cost(s) < best ? cost(s) : best;
+  int S = 1;
+  while (S < smax && cost(S) > 1.05 * best) ++S;
+  return S;
+}
+
 struct BwdLayout {
   size_t lse2_off, d_off, acc_off, acc_bytes, sched_off, total;
   int dq_splits, dq_split_tiles;   // split deterministic dQ (bf16): acc holds the partials
@@ -162,8 +181,19 @@ struct BwdLayout {
 // split into ranges so that at most 152 units run (one wave), each with at
 // least 4 key tiles; at most 64 splits. A rule of the shapes only, so the workspace size
 // needs no device.
+// The fp32 dQ kernel (one CTA per 64-row query tile) splits its units over
+// ranges of 64-key tiles by the wave model of wave_splits on 152 SMs, also a
+// rule of the shapes only.
 constexpr int kDqSplitTargetUnits = 152;
 void dq_split_count(int B, int H, int Tq, int Tk, attn_dtype_t dt, int deterministic, int* S, int* cs) {
+  if (dt == ATTN_F32) {
+    const long long units = static_cast<long long>(B) * H * ((Tq + kF32SplitTile - 1) / kF32SplitTile);
+    const int nkt = (Tk + kF32SplitTile - 1) / kF32SplitTile;
+    const int want = deterministic ? wave_splits(units, nkt, kDqSplitTargetUnits) : 1;
+    *cs = want > 1 ? (nkt + want - 1) / want : nkt;
+    *S = want > 1 ? (nkt + *cs - 1) / *cs : 1;
+    return;
+  }
   const long long units = static_cast<long long>(B) * H * ((Tq + 127) / 128);
   const int nkt = (Tk + 127) / 128;
   *S = 1;
@@ -269,19 +299,7 @@ int splitkv_count(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dt, 
     S = 1;
   } else if (req == 0) {
     const long long units = static_cast<long long>(B) * H * ((Tq + rows_per_unit - 1) / rows_per_unit);
-    if ((!f32 && units >= num_sms) || num_sms <= 0) {
-      S = 1;
-    } else {
-      const int smax = nkb / 2 < 64 ? (nkb / 2 > 1 ? nkb / 2 : 1) : 64;
-      auto cost = [&](int s) {   // waves x key tiles per split, in units of one key tile's work
-        const long long cs = (nkb + s - 1) / s, se = (nkb + cs - 1) / cs;
-        return static_cast<double>((units * se + num_sms - 1) / num_sms) * static_cast<double>(cs);
-      };
-      double best = cost(1);
-      for (int s = 2; s <= smax; ++s) best = cost(s) < best ? cost(s) : best;
-      S = 1;
-      while (S < smax && cost(S) > 1.05 * best) ++S;
-    }
+    S = (!f32 && units >= num_sms) ? 1 : wave_splits(units, nkb, num_sms);
   }
   if (S > nkb) S = nkb;
   if (S > 64) S = 64;

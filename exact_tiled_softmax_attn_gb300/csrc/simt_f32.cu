@@ -646,6 +646,10 @@ struct BwdArgs {
   float* dK;
   float* dV;
   Problem p;
+  // deterministic dQ over key ranges: count, 64-key tiles per range, partials
+  int dq_splits;
+  int dq_split_tiles;
+  float* dQpart;
 };
 
 // P and dS of one score tile, for rows a + 16 r and columns b + 16 c of the
@@ -827,9 +831,14 @@ __global__ void __launch_bounds__(NT, 1) dkdv_kernel(const BwdArgs a, int with_d
   }
 }
 
-// Deterministic dQ: one CTA per (64-row query tile, head) loops over key
-// tiles of BK keys in a fixed order and writes dQ once. SPLIT: scores from
-// split rows (Q split, K whole and split), else by Dot2.
+// Deterministic dQ: one CTA per (64-row query tile, head, key range) loops
+// over its key steps of BK keys in a fixed order and writes dQ once. With
+// several ranges (a.dq_splits > 1; ranges of a.dq_split_tiles 64-key tiles)
+// each writes scale * (its partial dQ) in fp32 to a.dQpart
+// [ranges][B*H*Tq][d], and reduce_dq_kernel adds them in range order; a
+// range past the causal limit of its query tile returns at once (the
+// reduction does not read it). SPLIT: scores from split rows (Q split, K
+// whole and split), else by Dot2.
 template <int W, int BK, bool SPLIT>
 __global__ void __launch_bounds__(NT, 1) dq_kernel(const BwdArgs a) {
   constexpr int LD = W + 4, LDS = BK + 4, NC = BK / 16, NQ = W / 16;
@@ -850,6 +859,13 @@ __global__ void __launch_bounds__(NT, 1) dq_kernel(const BwdArgs a) {
   const int q0 = blockIdx.x * BM;
   const size_t bh = blockIdx.y;
   const float scale = p.scale;
+  int n_kt = (Tk + BK - 1) / BK;
+  if (p.causal) n_kt = min(n_kt, (q0 + BM - 1) / BK + 1);
+  // this CTA's key steps [k0, k1)
+  const int steps_per_range = a.dq_split_tiles * (kF32SplitTile / BK);
+  const int k0 = a.dq_splits > 1 ? blockIdx.z * steps_per_range : 0;
+  const int k1 = a.dq_splits > 1 ? min(n_kt, k0 + steps_per_range) : n_kt;
+  if (k0 >= k1 && a.dq_splits > 1) return;
 
   if constexpr (SPLIT)
     load_split<W, BM>(nullptr, sQ, sQl, LD, a.Q + (bh * Tq + q0) * d, d, Tq - q0);
@@ -866,16 +882,14 @@ __global__ void __launch_bounds__(NT, 1) dq_kernel(const BwdArgs a) {
   for (int r = 0; r < 4; ++r)
 #pragma unroll
     for (int q = 0; q < NQ; ++q) acc[r][q] = 0.f;
-  int n_kt = (Tk + BK - 1) / BK;
-  if (p.causal) n_kt = min(n_kt, (q0 + BM - 1) / BK + 1);
   // split rows: a key step's K and V rows load into registers while the
   // previous step's dQ product runs
   RowRegs<W, BK> kr, vr;
   if constexpr (SPLIT) {
-    kr.load(a.K + bh * Tk * d, d, Tk);
-    vr.load(a.V + bh * Tk * dv, dv, Tk);
+    kr.load(a.K + (bh * Tk + k0 * BK) * d, d, Tk - k0 * BK);
+    vr.load(a.V + (bh * Tk + k0 * BK) * dv, dv, Tk - k0 * BK);
   }
-  for (int kt = 0; kt < n_kt; ++kt) {
+  for (int kt = k0; kt < k1; ++kt) {
     const int kv0 = kt * BK;
     __syncthreads();   // the previous step is done with sK, sV, sdS
     if constexpr (SPLIT) {
@@ -915,20 +929,39 @@ __global__ void __launch_bounds__(NT, 1) dq_kernel(const BwdArgs a) {
     }
     __syncthreads();
     if constexpr (SPLIT) {
-      if (kt + 1 < n_kt) {
+      if (kt + 1 < k1) {
         kr.load(a.K + (bh * Tk + kv0 + BK) * d, d, Tk - kv0 - BK);
         vr.load(a.V + (bh * Tk + kv0 + BK) * dv, dv, Tk - kv0 - BK);
       }
     }
     acc_tile<4, NQ>(sdS, LDS, sK, LD, ty, tx, min(BK, Tk - kv0), acc);
   }
+  float* out = a.dq_splits > 1 ? a.dQpart + blockIdx.z * static_cast<size_t>(p.B) * p.H * Tq * d : a.dQ;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int qi = q0 + ty + 16 * r;
     if (qi >= Tq) continue;
 #pragma unroll
     for (int q = 0; q < NQ; ++q)
-      if (acc_col(tx, q) < d) a.dQ[(bh * Tq + qi) * d + acc_col(tx, q)] = acc[r][q] * scale;
+      if (acc_col(tx, q) < d) out[(bh * Tq + qi) * d + acc_col(tx, q)] = acc[r][q] * scale;
+  }
+}
+
+// dQ = the sum of the dQ kernel's partials (already scaled) in range order,
+// over the ranges that hold key tiles of the row's query tile: one thread per
+// element (any d).
+__global__ void __launch_bounds__(256) reduce_dq_kernel(const float* __restrict__ part, float* __restrict__ out,
+                                                        long long rows, int Tq, int d, int n_ranges,
+                                                        int range_tiles, int n_k_tiles, int causal) {
+  const long long n = rows * d;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int qt = static_cast<int>((i / d) % Tq) / kF32SplitTile;
+    const int nt = causal ? min(qt + 1, n_k_tiles) : n_k_tiles;
+    const int ns = min(n_ranges, (nt + range_tiles - 1) / range_tiles);
+    float acc = 0.f;
+    for (int s = 0; s < ns; ++s) acc += part[static_cast<long long>(s) * n + i];
+    out[i] = acc;
   }
 }
 
@@ -962,7 +995,7 @@ template <int W>
 constexpr size_t dq_smem() { return dq_smem_of<W, dq_split<W>()>(); }
 
 template <int W>
-cudaError_t bwd_launch(const LaunchBwd& la, const BwdArgs& b, bool kv, bool q) {
+cudaError_t bwd_launch(const LaunchBwd& la, const BwdArgs& b, bool kv, bool q, bool red) {
   constexpr int RQ = dkdv_rows<W>(), RK = dq_rows<W>();
   constexpr size_t s1 = dkdv_smem<W>(), s2 = dq_smem<W>();
   static_assert(s1 <= kSmemMax && s2 <= kSmemMax, "shared memory");
@@ -982,8 +1015,15 @@ cudaError_t bwd_launch(const LaunchBwd& la, const BwdArgs& b, bool kv, bool q) {
     e = cudaFuncSetAttribute(dq_kernel<W, RK, SP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(s2));
     if (e != cudaSuccess) return e;
-    dim3 g2((p.Tq + BM - 1) / BM, p.B * p.H);
+    dim3 g2((p.Tq + BM - 1) / BM, p.B * p.H, b.dq_splits > 1 ? b.dq_splits : 1);
     dq_kernel<W, RK, SP><<<g2, NT, s2, la.stream>>>(b);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (red && b.dq_splits > 1) {
+    const long long rows = static_cast<long long>(p.B) * p.H * p.Tq;
+    reduce_dq_kernel<<<la.num_sms * 8, 256, 0, la.stream>>>(
+        b.dQpart, b.dQ, rows, p.Tq, p.d, b.dq_splits, b.dq_split_tiles,
+        (p.Tk + kF32SplitTile - 1) / kF32SplitTile, p.causal);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -1027,13 +1067,17 @@ cudaError_t launch_bwd_f32(const LaunchBwd& a) {
   }
   const bool kv = a.phase == 0 || a.phase == 2 || a.phase == 4;
   const bool q = a.deterministic && (a.phase == 0 || a.phase == 2 || a.phase == 5);
-  if (!kv && !q) return cudaSuccess;
+  // the sum of the dQ kernel's range partials (phase 3, as for bf16)
+  const bool red = a.deterministic && a.dq_splits > 1 && (a.phase == 0 || a.phase == 3);
+  if (!kv && !q && !red) return cudaSuccess;
+  if ((q || red) && a.dq_splits > 1 && a.dQpart == nullptr) return cudaErrorInvalidValue;
   simt::BwdArgs b{static_cast<const float*>(a.Q), static_cast<const float*>(a.K), static_cast<const float*>(a.V),
                   static_cast<const float*>(a.dO), a.LSE, a.D, static_cast<float*>(a.dQ),
-                  static_cast<float*>(a.dK), static_cast<float*>(a.dV), p};
+                  static_cast<float*>(a.dK), static_cast<float*>(a.dV), p,
+                  a.deterministic ? a.dq_splits : 1, a.dq_split_tiles, a.dQpart};
   const int W = simt::tile_width(p.d, p.dv);
-  return W == 64 ? simt::bwd_launch<64>(a, b, kv, q)
-                 : W == 128 ? simt::bwd_launch<128>(a, b, kv, q) : simt::bwd_launch<256>(a, b, kv, q);
+  return W == 64 ? simt::bwd_launch<64>(a, b, kv, q, red)
+                 : W == 128 ? simt::bwd_launch<128>(a, b, kv, q, red) : simt::bwd_launch<256>(a, b, kv, q, red);
 }
 
 }  // namespace attn

@@ -153,9 +153,9 @@ ATTN_API size_t attn_fwd_splitkv_workspace_size(int B, int H, int Tq, int Tk, in
  * Bytes of device workspace attn_bwd needs for this problem (0 is possible).
  * Holds -LSE * log2(e) and D = rowsum(dO o O), each [B*H, Tq_pad] fp32 with
  * Tq_pad = Tq rounded up to a multiple of 128, and, for bf16 with d <= 128
- * and deterministic == 0, the fp32 dQ accumulator [B,H,Tq,d], or, for bf16 with
- * deterministic == 1 and S = attn_bwd_dq_splits(...) > 1, S fp32 partial dQ
- * arrays [S][B,H,Tq,d], and, for bf16 with d <= 128, 256 bytes of counters
+ * and deterministic == 0, the fp32 dQ accumulator [B,H,Tq,d], or, with
+ * deterministic == 1 and S = attn_bwd_dq_splits(...) > 1 (either dtype), S
+ * fp32 partial dQ arrays [S][B,H,Tq,d], and, for bf16 with d <= 128, 256 bytes of counters
  * through which the dQ and dK/dV kernels hand out their work units at run
  * time (reset by each call); each part starts on a 256-byte boundary. For bf16
  * widths other than 64 and 128 it first holds zero-padded bf16 copies of Q,
@@ -168,16 +168,19 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int d, int
                                int deterministic);
 
 /*
- * Number of key splits S the deterministic bf16 backward uses for dQ (1 when
- * it does not split; -1 for invalid arguments). The dQ kernel runs one unit
- * per 128-row query tile; when there are fewer such units than 76 (half of a
- * GB300's 152 SMs) and at least 8 key tiles, each query tile's keys are cut
- * into S ranges (at most 152 units in all, at least 4 key tiles each, S <= 64)
- * whose partial dQ go to the workspace and are then added in split order, so
- * the result stays bitwise reproducible. A rule of the shapes only, so that
- * the workspace size needs no device: the 152 is GB300's SM count, and on a
- * device with another SM count the split stays correct but fills the SMs
- * less evenly.
+ * Number of key splits S the deterministic backward uses for dQ (1 when it
+ * does not split; -1 for invalid arguments). Each query tile's keys are cut
+ * into S ranges whose partial dQ go to the workspace and are then added in
+ * split order, so the result stays bitwise reproducible. bf16: the dQ kernel
+ * runs one unit per 128-row query tile; when there are fewer such units than
+ * 76 (half of a GB300's 152 SMs) and at least 8 key tiles, S ranges of at
+ * least 4 key tiles each, at most 152 units in all, S <= 64. fp32: one unit
+ * per 64-row query tile and ranges of 64-key tiles; S is the smallest count
+ * whose time (the waves of units x S on 152 SMs, times the key tiles of a
+ * range) is within 5 % of the best, at least two key tiles per range, S <=
+ * 64. Rules of the shapes only, so that the workspace size needs no device:
+ * the 152 is GB300's SM count, and on a device with another SM count the
+ * split stays correct but fills the SMs less evenly.
  */
 ATTN_API int attn_bwd_dq_splits(int B, int H, int Tq, int Tk, int d, int dv, attn_dtype_t dtype,
                                 int deterministic);

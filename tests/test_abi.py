@@ -112,13 +112,33 @@ def test_blocked_forward_validates_block(lib):
 def test_dq_split_rule(lib, shape, det, want):
     B_, H, Tq, Tk, d = shape
     assert B.attn_bwd_dq_splits(B_, H, Tq, Tk, d, d, B.ATTN_BF16, det) == want
-    assert B.attn_bwd_dq_splits(B_, H, Tq, Tk, d, d, B.ATTN_F32, det) == 1
     part = (B_ * H * ((Tq + 127) // 128 * 128) * 4 + 255) // 256 * 256
     acc = B_ * H * Tq * d * 4
     ws = B.attn_bwd_workspace_size(B_, H, Tq, Tk, d, d, B.ATTN_BF16, det)
     r256 = lambda x: (x + 255) // 256 * 256
     # + 256 bytes for the unit counters of the bf16 dQ and dK/dV kernels
     assert ws == r256(2 * part + (acc if det == 0 else (want * acc if want > 1 else 0))) + 256
+
+
+@pytest.mark.parametrize("shape,det,want", [
+    ((2, 8, 1000, 4000, 128), 1, 4),     # c4: 256 query tiles of 64 rows, 63 key tiles of 64 -> ranges of 16
+    ((2, 8, 1000, 4000, 128), 0, 1),     # atomic dQ never splits
+    ((1, 8, 256, 65536, 128), 1, 14),    # 32 query tiles: 14 ranges of 74 key tiles, three waves of 448 CTAs
+    ((1, 1, 128, 200, 64), 1, 2),        # 4 key tiles: two ranges of 2
+    ((1, 1, 128, 192, 64), 1, 1),        # 3 key tiles: too few to split
+    ((2, 16, 8192, 8192, 128), 1, 1),    # 4096 query tiles fill the SMs
+])
+def test_dq_split_rule_fp32(lib, shape, det, want):
+    """The fp32 dQ kernel splits its 64-row query tiles over ranges of
+    64-key tiles: the smallest count whose waves of units x ranges on 152 SMs,
+    times the key tiles of a range, come within 5 % of the best count."""
+    B_, H, Tq, Tk, d = shape
+    S = B.attn_bwd_dq_splits(B_, H, Tq, Tk, d, d, B.ATTN_F32, det)
+    assert S == want
+    r256 = lambda x: (x + 255) // 256 * 256
+    part = r256(B_ * H * ((Tq + 127) // 128 * 128) * 4)
+    partials = B_ * H * Tq * d * 4 * S if S > 1 else 0
+    assert B.attn_bwd_workspace_size(B_, H, Tq, Tk, d, d, B.ATTN_F32, det) == 2 * part + partials
 
 
 def test_workspace_size(lib):

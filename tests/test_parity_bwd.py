@@ -281,6 +281,35 @@ def test_bf16_split_dq_deterministic(shape, causal):
     assert (dq1.float() - dqa.float()).norm() <= 1e-2 * dqa.float().norm() + 1e-5
 
 
+F32_SPLIT_DQ_SHAPES = [  # B, H, Tq, Tk, d, dv: few 64-row query tiles, many 64-key tiles
+    (1, 1, 1, 5000, 128, 128),     # one query row
+    (1, 2, 128, 4096, 128, 128),
+    (1, 1, 256, 3000, 64, 64),     # 64-key steps (rows of 64 columns)
+    (2, 1, 200, 2500, 40, 24),     # odd widths
+    (1, 1, 1300, 1100, 128, 128),  # Tq > Tk: causal query tiles see 1 ... all 18 key tiles
+    (1, 1, 100, 900, 200, 136),    # rows above 128 columns (compensated scores)
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", F32_SPLIT_DQ_SHAPES)
+def test_f32_split_dq_deterministic(shape, causal):
+    """The fp32 deterministic backward with dQ split over ranges of 64-key
+    tiles (partials added in range order): parity with the oracle at the fp32
+    bounds, bitwise equal across two runs, and equal to the atomic mode up to
+    fp32 rounding order."""
+    B, H, Tq, Tk, d, dv = shape
+    assert pkg.attn_bwd_dq_splits(B, H, Tq, Tk, d, dv, pkg.ATTN_F32, 1) > 1
+    x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, dv), seed=Tq + Tk + d, device=DEV)
+    scale = 1 / math.sqrt(d)
+    check_all(x, causal, scale, torch.float32, 1)
+    _, _, dq1, dk1, dv1 = run(x, causal, scale, 1)
+    _, _, dq2, dk2, dv2 = run(x, causal, scale, 1)
+    assert torch.equal(dq1, dq2) and torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    _, _, dqa, _, _ = run(x, causal, scale, 0)
+    assert (dq1 - dqa).abs().max().item() <= 1e-5 * max(dqa.abs().max().item(), 1e-30) + 1e-7
+
+
 @pytest.mark.parametrize("deterministic", [0, 1])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("shape", [(20, 16, 130, 128), (40, 8, 256, 64), (75, 4, 70, 128), (3, 100, 1, 64)])
