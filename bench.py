@@ -44,9 +44,9 @@ KERNEL_SOURCES = {
     # both launches (the dV and the dK kernel) of the phase bench.py times together
     "kv256_kernel": ("bwd_d256.cu", "bwd_common.cuh", "ptx.cuh", "common.cuh", "launch.h"),
     "q256_kernel": ("bwd_d256.cu", "bwd_common.cuh", "ptx.cuh", "common.cuh", "launch.h"),
-    "simt::fwd_kernel": ("simt_f32.cu", "common.cuh", "launch.h"),
-    "simt::dkdv_kernel": ("simt_f32.cu", "common.cuh", "launch.h"),
-    "simt::dq_kernel": ("simt_f32.cu", "common.cuh", "launch.h"),
+    "simt::fwd_kernel": ("simt_f32.cu", "simt.h", "common.cuh", "launch.h"),
+    "simt::dkdv_kernel": ("simt_f32.cu", "simt.h", "common.cuh", "launch.h"),
+    "simt::dq_kernel": ("simt_f32.cu", "simt.h", "common.cuh", "launch.h"),
 }
 
 

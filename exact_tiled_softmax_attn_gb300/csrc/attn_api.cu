@@ -11,6 +11,7 @@
 #include "attn.h"
 #include "common.cuh"
 #include "launch.h"
+#include "simt.h"
 #include "ptx.cuh"
 
 namespace attn {
@@ -387,19 +388,16 @@ attn_status_t fwd_impl(const void* Q, const void* K, const void* V, void* O, flo
   a.split_tiles = split_tiles;
   if (n_splits > 1) {
     a.Opart = static_cast<float*>(workspace);
-    uint8_t* lse_part = static_cast<uint8_t*>(workspace) + SL.lse_off;
-    if (dtype == ATTN_F32)
-      a.LSEpart64 = reinterpret_cast<double*>(lse_part);
-    else
-      a.LSEpart = reinterpret_cast<float*>(lse_part);
+    // fp32 problems: fp64 log-sum-exps (the fp32 kernels cast the pointer back)
+    a.LSEpart = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + SL.lse_off);
   }
   a.stream = st;
   cudaError_t e;
   if (dtype == ATTN_F32) {
     e = launch_fwd_f32(a);
     if (e == cudaSuccess && n_splits > 1)
-      e = launch_splitkv_merge_f32(p, a.Opart, a.LSEpart64, n_splits, split_tiles, kF32SplitTile,
-                                   static_cast<float*>(O), LSE, di->num_sms, st);
+      e = launch_splitkv_merge_f32(p, a.Opart, reinterpret_cast<const double*>(a.LSEpart), n_splits, split_tiles,
+                                   kF32SplitTile, static_cast<float*>(O), LSE, di->num_sms, st);
   } else {
     // Rows wider than 128 columns: on CTA pairs (each CTA loads 64-key
     // halves of K and 128-key tiles of half of V's columns) unless the keys

@@ -29,8 +29,7 @@ struct LaunchFwd {
   int n_splits;
   int split_tiles;
   float* Opart;
-  float* LSEpart;
-  double* LSEpart64;        // fp32 path: the split log-sum-exps in fp64 (instead of LSEpart)
+  float* LSEpart;           // fp32 path: points at fp64 log-sum-exps (cast back to double*)
   cudaStream_t stream;
 };
 
@@ -108,9 +107,6 @@ cudaError_t launch_splitkv_merge(const Problem& p, const float* Opart, const flo
 // forward)
 cudaError_t launch_splitkv_merge_f32(const Problem& p, const float* Opart, const double* LSEpart, int n_splits,
                                      int split_tiles, int tile, float* O, float* LSE, int num_sms, cudaStream_t s);
-// Rows of the fp32 forward's query tiles and keys of its key tiles when its
-// keys are split into ranges (attn_fwd_splitkv)
-constexpr int kF32SplitTile = 64;
 
 // shared small kernels
 cudaError_t launch_fill_empty_fwd(const Problem& p, void* O, float* LSE, int elem_bytes, cudaStream_t s);

@@ -42,6 +42,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "simt.h"
 
 namespace attn {
 namespace simt {
@@ -626,7 +627,8 @@ cudaError_t fwd_launch(const LaunchFwd& a) {
   if (e != cudaSuccess) return e;
   const int n_ranges = a.n_splits > 1 ? a.n_splits : 1;
   dim3 grid((a.p.Tq + BM - 1) / BM, a.p.B * a.p.H, n_ranges);
-  const KeyRanges kr{n_ranges, a.split_tiles, a.Opart, a.LSEpart64};
+  // (fp32 problems: the split log-sum-exps are fp64, LSEpart points at them)
+  const KeyRanges kr{n_ranges, a.split_tiles, a.Opart, reinterpret_cast<double*>(a.LSEpart)};
   fwd_kernel<W, BN, SP><<<grid, NT, smem, a.stream>>>(static_cast<const float*>(a.Q), static_cast<const float*>(a.K),
                                                   static_cast<const float*>(a.V), static_cast<float*>(a.O), a.LSE,
                                                   a.p, kr);
