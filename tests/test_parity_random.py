@@ -2,8 +2,11 @@
 problems: shapes, widths, masks, scales and dQ modes drawn together, so that
 combinations the hand-picked cases do not list are checked as well. Examples
 are the CTA-pair forward with a ragged last key tile, padded widths with
-split dQ, and Tq != Tk under the causal mask. The draw is fixed by the seed,
-and every case is small enough for the oracle to finish in about a second."""
+split dQ, and Tq != Tk under the causal mask. Each case also draws whether
+the forward runs through the split-KV forward (automatic or a fixed count
+of key ranges), from a stream of its own so that the problems themselves
+stay the same. The draw is fixed by the seed, and every case is small
+enough for the oracle to finish in about a second."""
 import math
 
 import numpy as np
@@ -31,6 +34,7 @@ def _width(rng, bf16):
 
 def _cases(n=24, seed=20261203):
     rng = np.random.default_rng(seed)
+    rng_split = np.random.default_rng(seed + 1)
     out = []
     for _ in range(n):
         bf16 = rng.random() < 0.8
@@ -43,7 +47,10 @@ def _cases(n=24, seed=20261203):
         causal = bool(rng.random() < 0.5)
         det = int(rng.random() < 0.6)
         scale = float(rng.uniform(0.5, 2.0) / math.sqrt(d))
-        out.append((B, H, Tq, Tk, d, dv, "bf16" if bf16 else "f32", causal, det, scale))
+        # forward: plain (None), split-KV with the automatic count (0), or 2 .. 9 key ranges
+        pick = int(rng_split.integers(0, 3))
+        splits = None if pick == 0 else 0 if pick == 1 else int(rng_split.integers(2, 10))
+        out.append((B, H, Tq, Tk, d, dv, "bf16" if bf16 else "f32", causal, det, scale, splits))
     return out
 
 
@@ -59,11 +66,11 @@ def _lib():
 
 @pytest.mark.parametrize("case", CASES, ids=[f"case{i}" for i in range(len(CASES))])
 def test_random_problem(case):
-    B, H, Tq, Tk, d, dv, dts, causal, det, scale = case
+    B, H, Tq, Tk, d, dv, dts, causal, det, scale, splits = case
     dt = torch.bfloat16 if dts == "bf16" else torch.float32
     x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, dv), seed=Tq * 7 + Tk * 3 + d + dv, dtype=dt,
                     device=DEV)
-    o, lse = pkg.forward(x["Q"], x["K"], x["V"], causal=causal, scale=scale)
+    o, lse = pkg.forward(x["Q"], x["K"], x["V"], causal=causal, scale=scale, num_splits=splits)
     dq, dk, dvv = pkg.backward(x["Q"], x["K"], x["V"], o, lse, x["dO"], causal=causal, scale=scale,
                                deterministic=det)
     torch.cuda.synchronize()
