@@ -83,8 +83,9 @@ __device__ __forceinline__ void scale_pair(float hi, float lo, float scale, floa
 // |x| < 2^(E+1)) and u = 2^(E-7), hi = rint(x / u) u is an integer multiple
 // n u with |n| <= 256, and lo = x - hi, |lo| <= u / 2, is exact in fp32.
 // For two split rows q, k of n <= 256 entries every partial sum of
-// hq_i hk_i is an integer multiple of uq uk below 2^24 of them in magnitude,
-// so the fp32 sum of the coarse products is exact (as long as uq uk does not
+// hq_i hk_i (over any subset of i) is an integer multiple of uq uk of at
+// most 2^24 of them in magnitude, so the fp32 sum of the coarse products is
+// exact in any order and grouping (as long as uq uk does not
 // underflow, i.e. outside rows whose largest entries multiply to below
 // ~2^-120); q.k = sum hq hk + sum (hq lk + lq k) with only the second sum,
 // whose terms are 2^-8 of the scale of q.k, rounded.
