@@ -345,20 +345,26 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream()
     sc = w.softmax_scale
 
-    # forward: attn_fwd, or with --splitkv the split-KV forward (key ranges
-    # as separate work units, then the merge kernel)
+    # forward: attn_fwd, or the split-KV forward (key ranges as separate work
+    # units, then the merge kernel). --splitkv N takes the split-KV forward
+    # with N splits (0: the library's automatic count) and --splitkv -1 takes
+    # attn_fwd; by default the split-KV forward runs where the automatic count
+    # is above 1 (few query tiles against many keys) and attn_fwd elsewhere.
+    splitkv = args.splitkv
+    if splitkv is None:
+        splitkv = 0 if pkg.attn_fwd_splitkv_splits(B, H, Tq, Tk, d, dv, code, 0) > 1 else -1
     n_splits = 1
-    if args.splitkv is not None:
-        n_splits = pkg.attn_fwd_splitkv_splits(B, H, Tq, Tk, d, dv, code, args.splitkv)
-        sk_bytes = pkg.attn_fwd_splitkv_workspace_size(B, H, Tq, Tk, d, dv, code, args.splitkv)
+    if splitkv >= 0:
+        n_splits = pkg.attn_fwd_splitkv_splits(B, H, Tq, Tk, d, dv, code, splitkv)
+        sk_bytes = pkg.attn_fwd_splitkv_workspace_size(B, H, Tq, Tk, d, dv, code, splitkv)
         sk_ws = torch.empty(max(sk_bytes, 256), dtype=torch.uint8, device=dev)
 
     def fwd_call(xi, oi, li, st):
-        if args.splitkv is None:
+        if splitkv < 0:
             pkg.attn_fwd(xi["Q"], xi["K"], xi["V"], oi, li, B, H, Tq, Tk, d, dv, sc, w.causal, code, st)
         else:
             pkg.attn_fwd_splitkv(xi["Q"], xi["K"], xi["V"], oi, li, B, H, Tq, Tk, d, dv, sc, w.causal, code,
-                                 args.splitkv, sk_ws, sk_ws.numel(), st)
+                                 splitkv, sk_ws, sk_ws.numel(), st)
 
     def fwd():
         fwd_call(x, o, lse, stream)
@@ -643,7 +649,8 @@ def main(argv=None):
     ap.add_argument("--dq-pairs", action="store_true",
                     help="time the dQ pass on CTA pairs (attn_bwd_phase phase 6; bf16, d = 128, deterministic)")
     ap.add_argument("--splitkv", type=int, default=None,
-                    help="run the forward through attn_fwd_splitkv with this many key splits (0 = automatic)")
+                    help="forward through attn_fwd_splitkv with this many key splits (0 = automatic) or, with -1, "
+                         "through attn_fwd; default: attn_fwd_splitkv where the automatic count is above 1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fwd-only", action="store_true",
                     help="time the forward alone (its FLOPs only)")
