@@ -668,12 +668,19 @@ __device__ __forceinline__ void p_ds(float sh, float sl, float dp, float scale, 
   dsij = pij * (dp - dd);
 }
 
+// Four fp32 atomic adds to consecutive addresses in one instruction (sm_90+;
+// the address 16-byte aligned).
+__device__ __forceinline__ void red_add4(float* g, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(g), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
 // One CTA per (64-key tile, head): loops over the query tiles (BQ rows each)
 // that see the key tile, computes S^T = K Q^T and dP^T = V dO^T for
 // the tile, and accumulates dV += P^T dO and dK += dS^T Q in registers
 // (rows of keys ty + 16 r). Unless `with_dq` is 0 it also adds this key
 // tile's share scale * dS K into dQ with fp32 atomics. SPLIT: scores from
-// split rows (K split, Q whole and split), else by Dot2.
+// split rows (K split, Q whole and split), else by Dot2; with `with_dq` the
+// split rows' K is also summed back into a whole copy for the dQ product.
 template <int W, int BQ, bool SPLIT>
 __global__ void __launch_bounds__(NT, 1) dkdv_kernel(const BwdArgs a, int with_dq) {
   constexpr int LD = W + 4, LDP = BQ + 4, NC = BQ / 16, NQ = W / 16;
@@ -689,6 +696,7 @@ __global__ void __launch_bounds__(NT, 1) dkdv_kernel(const BwdArgs a, int with_d
   float* sdSt = sPt + BM * LDP;                  // [BM][LDP]
   float* sLse = sdSt + BM * LDP;  // [BQ]
   float* sD = sLse + BQ;          // [BQ]
+  float* sKf = sD + BQ;           // [BM][LD] split rows: K whole (coarse part + remainder), for the dQ product
   const Problem& p = a.p;
   const int d = p.d, dv = p.dv, Tq = p.Tq, Tk = p.Tk;
   const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
@@ -696,8 +704,13 @@ __global__ void __launch_bounds__(NT, 1) dkdv_kernel(const BwdArgs a, int with_d
   const size_t bh = blockIdx.y;
   const float scale = p.scale;
 
-  if constexpr (SPLIT)
+  if constexpr (SPLIT) {
     load_split<W, BM>(nullptr, sK, sKl, LD, a.K + (bh * Tk + kv0) * d, d, Tk - kv0);
+    if (with_dq) {
+      __syncthreads();
+      for (int e = threadIdx.x; e < BM * LD; e += NT) sKf[e] = __fadd_rn(sK[e], sKl[e]);   // exact
+    }
+  }
   else
     load_tile<W>(sK, LD, a.K + (bh * Tk + kv0) * d, BM, d, Tk - kv0);
   load_tile<W>(sV, LD, a.V + (bh * Tk + kv0) * dv, BM, dv, Tk - kv0);
@@ -782,42 +795,56 @@ __global__ void __launch_bounds__(NT, 1) dkdv_kernel(const BwdArgs a, int with_d
     acc_tile<4, NQ>(sPt, LDP, sdO, LD, ty, tx, nq, accV);
     acc_tile<4, NQ>(sdSt, LDP, sQ, LD, ty, tx, nq, accK);
     if (with_dq) {
-      // dQ_i += scale * sum_j dS_ij K_j, rows of queries ty + 16 r
+      // dQ_i += scale * sum_j dS_ij K_j, rows of queries ty + 16 r: two
+      // adjacent columns per two-lane FMA with dS_ij broadcast to both lanes
+      // (the transposed dS: entry (query ty + 16 r, key k) sits at
+      // sdSt[k][ty + 16 r]); each row's four adjacent columns 64 g + 4 tx ..
+      // go out in one vector reduction where the rows are 16-byte aligned
       constexpr int RQ = BQ / 16;
+      const float* kf = SPLIT ? sKf : sK;
       float t[RQ][NQ];
 #pragma unroll
       for (int r = 0; r < RQ; ++r)
 #pragma unroll
         for (int q = 0; q < NQ; ++q) t[r][q] = 0.f;
-      // (the transposed dS: entry (query ty + 16 r, key k) sits at sdSt[k][ty + 16 r])
       const int nk = min(BM, Tk - kv0);
 #pragma unroll 4
       for (int k = 0; k < nk; ++k) {
-        float x[RQ];
         float4 b[NQ / 4];
 #pragma unroll
-        for (int r = 0; r < RQ; ++r) x[r] = sdSt[k * LDP + ty + 16 * r];
+        for (int g = 0; g < NQ / 4; ++g) b[g] = ld4(kf + k * LD + 64 * g + 4 * tx);
 #pragma unroll
-        for (int g = 0; g < NQ / 4; ++g) {
-          b[g] = ld4(sK + k * LD + 64 * g + 4 * tx);
-          if constexpr (SPLIT) {   // K = coarse part + remainder, exactly
-            const float4 l = ld4(sKl + k * LD + 64 * g + 4 * tx);
-            b[g] = make_float4(__fadd_rn(b[g].x, l.x), __fadd_rn(b[g].y, l.y), __fadd_rn(b[g].z, l.z),
-                               __fadd_rn(b[g].w, l.w));
-          }
+        for (int r = 0; r < RQ; ++r) {
+          const float x = sdSt[k * LDP + ty + 16 * r];
+          const float2 xr = make_float2(x, x);
+#pragma unroll
+          for (int g = 0; g < NQ / 4; ++g)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float2 u = fma2(xr, pair(b[g], h), make_float2(t[r][4 * g + 2 * h], t[r][4 * g + 2 * h + 1]));
+              t[r][4 * g + 2 * h] = u.x;
+              t[r][4 * g + 2 * h + 1] = u.y;
+            }
         }
-#pragma unroll
-        for (int r = 0; r < RQ; ++r)
-#pragma unroll
-          for (int q = 0; q < NQ; ++q) t[r][q] = fmaf(x[r], el(b[q >> 2], q & 3), t[r][q]);
       }
+      const bool vec = (d & 3) == 0 && (reinterpret_cast<uintptr_t>(a.dQ) & 15u) == 0;
 #pragma unroll
       for (int r = 0; r < RQ; ++r) {
         const int qi = q0 + ty + 16 * r;
         if (qi >= Tq) continue;
+        float* row = a.dQ + (bh * Tq + qi) * d;
 #pragma unroll
-        for (int q = 0; q < NQ; ++q)
-          if (acc_col(tx, q) < d) atomicAdd(a.dQ + (bh * Tq + qi) * d + acc_col(tx, q), t[r][q] * scale);
+        for (int g = 0; g < NQ / 4; ++g) {
+          const int c = 64 * g + 4 * tx;
+          if (vec && c + 3 < d) {
+            red_add4(row + c, t[r][4 * g] * scale, t[r][4 * g + 1] * scale, t[r][4 * g + 2] * scale,
+                     t[r][4 * g + 3] * scale);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (c + e < d) atomicAdd(row + c + e, t[r][4 * g + e] * scale);
+          }
+        }
       }
     }
   }
@@ -979,7 +1006,8 @@ constexpr int dq_rows() { return W >= 128 ? 32 : 64; }
 template <int W, bool SPLIT>
 constexpr size_t dkdv_smem_of() {
   constexpr int BQ = dkdv_rows<W>();
-  return sizeof(float) * ((SPLIT ? 3 : 2) * BM * (W + 4) + (SPLIT ? 4 : 2) * BQ * (W + 4) + 2 * BM * (BQ + 4) + 2 * BQ);
+  // (split rows: one more [BM][W + 4] tile, the whole K for the atomic dQ product)
+  return sizeof(float) * ((SPLIT ? 4 : 2) * BM * (W + 4) + (SPLIT ? 4 : 2) * BQ * (W + 4) + 2 * BM * (BQ + 4) + 2 * BQ);
 }
 // split rows wherever their tiles fit
 template <int W>
