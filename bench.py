@@ -47,6 +47,9 @@ KERNEL_SOURCES = {
     "simt::fwd_kernel": ("simt_f32.cu", "simt.h", "common.cuh", "launch.h"),
     "simt::dkdv_kernel": ("simt_f32.cu", "simt.h", "common.cuh", "launch.h"),
     "simt::dq_kernel": ("simt_f32.cu", "simt.h", "common.cuh", "launch.h"),
+    # the dK/dV kernel with the dQ share and its reductions (atomic dQ mode)
+    "dkdv_kernel@atomic": ("bwd_bf16.cu", "bwd_common.cuh", "ptx.cuh", "common.cuh", "launch.h"),
+    "simt::dkdv_kernel@atomic": ("simt_f32.cu", "simt.h", "common.cuh", "launch.h"),
 }
 
 
@@ -558,7 +561,9 @@ def run_ours(args, w):
     # the dominant kernel: the longest of the single kernels
     dom = max((k for k, v in kernels.items() if "flop" in v), key=lambda k: kernels[k]["ms"])
     achieved = kernels[dom]["tflops"]
-    traffic = load_traffic(dom.split("(")[-1].rstrip(")"), args.workload)
+    # (atomic dQ mode: the dK/dV kernel with its dQ reductions has lines of its own)
+    dom_kernel = dom.split("(")[-1].rstrip(")")
+    traffic = load_traffic(dom_kernel + ("@atomic" if not det and "dkdv" in dom_kernel else ""), args.workload)
     cfg = workload_config(w)
     cfg.update({"pass": "forward only" if args.fwd_only else "forward + backward",
                 "dq_mode": None if args.fwd_only else ("deterministic" if det else "atomic"),

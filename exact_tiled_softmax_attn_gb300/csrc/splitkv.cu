@@ -94,9 +94,14 @@ __global__ void __launch_bounds__(NT) merge_kernel(const float* __restrict__ Opa
 // The same merge for fp32 outputs (the CUDA-core forward's key ranges): one
 // warp per output row, lane c handling columns c, c + 32, ... (any dv up to
 // 256, rows with no alignment beyond 4 bytes). The partial log-sum-exps are
-// fp64 and the weights are formed in fp64 (at logits in the thousands an
-// fp32 LSE_s is off by up to 1e-4). `tile`: rows per query tile and keys per
-// key tile of the forward that wrote the partials.
+// fp64: at logits in the thousands an fp32 LSE_s is off by up to 1e-4. Lane
+// s holds split s's (and split s + 32's): the maximum M is taken over the
+// warp in fp64 and each weight exp(LSE_s - M) from the fp64 difference
+// rounded to fp32, whose error (|LSE_s - M| * 2^-24) matters only where the
+// weight does not vanish. The weights and their sum are fp32 from there on,
+// and every lane forms the same sum (a butterfly of commutative adds).
+// `tile`: rows per query tile and keys per key tile of the forward that
+// wrote the partials.
 __global__ void __launch_bounds__(NT) merge_f32_kernel(const float* __restrict__ Opart,
                                                        const double* __restrict__ LSEpart, float* __restrict__ O,
                                                        float* __restrict__ LSE, long long rows, int Tq, int dv,
@@ -111,28 +116,34 @@ __global__ void __launch_bounds__(NT) merge_f32_kernel(const float* __restrict__
     // the diagonal tile under the causal mask)
     const int qt = q / tile;
     const int nt = causal ? min(qt + 1, n_kv_tiles) : n_kv_tiles;
-    const int ns = min(n_splits, (nt + split_tiles - 1) / split_tiles);
-    double mx = -CUDART_INF;
-    for (int s = 0; s < ns; ++s) mx = fmax(mx, LSEpart[static_cast<long long>(s) * rows + r]);
+    const int ns = min(n_splits, (nt + split_tiles - 1) / split_tiles);   // <= 64
+    const double l0 = lane < ns ? LSEpart[static_cast<long long>(lane) * rows + r] : -CUDART_INF;
+    const double l1 = lane + 32 < ns ? LSEpart[static_cast<long long>(lane + 32) * rows + r] : -CUDART_INF;
+    double mx = fmax(l0, l1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     float acc[8];
 #pragma unroll
     for (int h = 0; h < 8; ++h) acc[h] = 0.f;
     float lse = -CUDART_INF_F;
     if (mx != -CUDART_INF) {
-      double wsum = 0.0;
+      // 0 for a split with no allowed key (LSE_s = -inf)
+      const float w0 = expf(static_cast<float>(l0 - mx));
+      const float w1 = expf(static_cast<float>(l1 - mx));
+      float wsum = w0 + w1;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
       for (int s = 0; s < ns; ++s) {
-        const double w = exp(LSEpart[static_cast<long long>(s) * rows + r] - mx);   // 0: no allowed key
-        const float wgt = static_cast<float>(w);
-        wsum += w;
+        const float wgt = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
         const float* orow = Opart + (static_cast<long long>(s) * rows + r) * dv;
 #pragma unroll
         for (int h = 0; h < 8; ++h)
           if (lane + 32 * h < dv) acc[h] = fmaf(wgt, orow[lane + 32 * h], acc[h]);
       }
-      const float inv = static_cast<float>(1.0 / wsum);
+      const float inv = 1.0f / wsum;
 #pragma unroll
       for (int h = 0; h < 8; ++h) acc[h] *= inv;
-      lse = static_cast<float>(mx + log(wsum));
+      lse = static_cast<float>(mx + static_cast<double>(logf(wsum)));
     }
 #pragma unroll
     for (int h = 0; h < 8; ++h)
