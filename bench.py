@@ -50,6 +50,8 @@ KERNEL_SOURCES = {
     # the dK/dV kernel with the dQ share and its reductions (atomic dQ mode)
     "dkdv_kernel@atomic": ("bwd_bf16.cu", "bwd_common.cuh", "ptx.cuh", "common.cuh", "launch.h"),
     "simt::dkdv_kernel@atomic": ("simt_f32.cu", "simt.h", "common.cuh", "launch.h"),
+    # the fp32 dK/dV kernel that also writes the key tiles' dQ partials (deterministic, no dQ kernel)
+    "simt::dkdv_kernel@dqpart": ("simt_f32.cu", "simt.h", "common.cuh", "launch.h"),
 }
 
 
@@ -382,7 +384,11 @@ def run_ours(args, w):
     # launches nothing for this configuration (the library's own rule, as in
     # attn_bwd_phase) is not called, so that no event interval of the timed
     # step is an empty one.
-    launches = {1: f32 or (not det and w.d <= 128), 5: bool(det) or w.d > 128, 6: bool(det), 4: True,
+    # fp32 deterministic with few key tiles: the dK/dV kernel writes one dQ
+    # partial per 64-key tile and no dQ kernel runs (the library reports one
+    # split per key tile then; its dQ kernel's own splits are never that many)
+    f32_fused = f32 and bool(det) and dq_splits == -(-Tk // 64)
+    launches = {1: f32 or (not det and w.d <= 128), 5: (bool(det) and not f32_fused) or w.d > 128, 6: bool(det), 4: True,
                 3: (not f32 and w.d <= 128 and (not det or dq_splits > 1)) or (f32 and bool(det) and dq_splits > 1)}
     phases = () if args.fwd_only else tuple(ph for ph in (1, 6 if args.dq_pairs else 5, 4, 3) if launches[ph])
     slot = {1: 1, 5: 2, 6: 2, 4: 3, 3: 4}   # per-step interval of each group: fwd, pre, q, kv, conv
@@ -532,6 +538,8 @@ def run_ours(args, w):
         kernels["bwd dV + dK (kv256_kernel)"] = {"ms": kv_ms, "flop": 2 * md + 2 * mv,
                                                  "executed_flop": 3 * md + 2 * mv, "launches": 2}
         kernels["bwd dQ (q256_kernel)"] = {"ms": q_ms, "flop": md, "executed_flop": 2 * md + mv}
+    elif f32_fused:
+        kernels["bwd dK/dV + dQ partials (simt::dkdv_kernel)"] = {"ms": kv_ms, "flop": 3 * md + 2 * mv}
     elif det:
         kernels[f"bwd dK/dV ({tag}dkdv_kernel)"] = {"ms": kv_ms, "flop": 2 * md + 2 * mv}
         kernels[f"bwd dQ ({tag}{'dq_pair_kernel' if args.dq_pairs else 'dq_kernel'})"] = \
@@ -561,9 +569,10 @@ def run_ours(args, w):
     # the dominant kernel: the longest of the single kernels
     dom = max((k for k, v in kernels.items() if "flop" in v), key=lambda k: kernels[k]["ms"])
     achieved = kernels[dom]["tflops"]
-    # (atomic dQ mode: the dK/dV kernel with its dQ reductions has lines of its own)
+    # (atomic dQ mode, and the fp32 dK/dV kernel with dQ partials: lines of their own)
     dom_kernel = dom.split("(")[-1].rstrip(")")
-    traffic = load_traffic(dom_kernel + ("@atomic" if not det and "dkdv" in dom_kernel else ""), args.workload)
+    suffix = "" if "dkdv" not in dom_kernel else "@atomic" if not det else "@dqpart" if f32_fused else ""
+    traffic = load_traffic(dom_kernel + suffix, args.workload)
     cfg = workload_config(w)
     cfg.update({"pass": "forward only" if args.fwd_only else "forward + backward",
                 "dq_mode": None if args.fwd_only else ("deterministic" if det else "atomic"),
@@ -595,7 +604,7 @@ def run_ours(args, w):
         # bf16: fwd (+ split-KV merge), dQ (+ split reduction), dK/dV | fwd (+ merge), preprocess,
         # dK/dV, convert; fp32: fwd, preprocess, dK/dV, dQ | fwd, preprocess, dK/dV
         "gpu_launches": args.steps * ((1 + (1 if n_splits > 1 else 0)) if args.fwd_only else
-                                      (4 if det else 3) + (1 if n_splits > 1 else 0) +
+                                      (4 if det and not f32_fused else 3) + (1 if n_splits > 1 else 0) +
                                       (1 if det and dq_splits > 1 else 0) if f32 else
                                       # d = 256: forward, dQ (it forms D), dV, dK kernels
                                       (4 + (1 if n_splits > 1 else 0)) if w.d > 128 else

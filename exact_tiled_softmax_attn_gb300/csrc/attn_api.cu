@@ -182,14 +182,22 @@ struct BwdLayout {
 // split into ranges so that at most 152 units run (one wave), each with at
 // least 4 key tiles; at most 64 splits. A rule of the shapes only, so the workspace size
 // needs no device.
-// The fp32 dQ kernel (one CTA per 64-row query tile) splits its units over
+// fp32: with at most 64 key tiles of 64 keys and 1 GiB of partials
+// (f32_fused_dq) every key tile is a range of its own, whose partial dQ the
+// dK/dV kernel writes; otherwise
+// the fp32 dQ kernel (one CTA per 64-row query tile) splits its units over
 // ranges of 64-key tiles by the wave model of wave_splits on 152 SMs, also a
 // rule of the shapes only.
 constexpr int kDqSplitTargetUnits = 152;
-void dq_split_count(int B, int H, int Tq, int Tk, attn_dtype_t dt, int deterministic, int* S, int* cs) {
+void dq_split_count(int B, int H, int Tq, int Tk, int d, attn_dtype_t dt, int deterministic, int* S, int* cs) {
   if (dt == ATTN_F32) {
     const long long units = static_cast<long long>(B) * H * ((Tq + kF32SplitTile - 1) / kF32SplitTile);
     const int nkt = (Tk + kF32SplitTile - 1) / kF32SplitTile;
+    if (deterministic && f32_fused_dq(B, H, Tq, Tk, d)) {
+      *S = nkt;
+      *cs = 1;
+      return;
+    }
     const int want = deterministic ? wave_splits(units, nkt, kDqSplitTargetUnits) : 1;
     *cs = want > 1 ? (nkt + want - 1) / want : nkt;
     *S = want > 1 ? (nkt + *cs - 1) / *cs : 1;
@@ -220,7 +228,7 @@ BwdLayout bwd_layout(int B, int H, int Tq, int Tk, int d, attn_dtype_t dt, int d
   BwdLayout L{};
   const size_t rows_pad = static_cast<size_t>(B) * H * padded_rows(Tq);
   const size_t part = round_up(rows_pad * sizeof(float), 256);
-  dq_split_count(B, H, Tq, Tk, dt, deterministic, &L.dq_splits, &L.dq_split_tiles);
+  dq_split_count(B, H, Tq, Tk, d, dt, deterministic, &L.dq_splits, &L.dq_split_tiles);
   L.lse2_off = 0;
   L.d_off = part;
   L.acc_off = 2 * part;

@@ -677,10 +677,12 @@ __device__ __forceinline__ void red_add4(float* g, float a, float b, float c, fl
 // One CTA per (64-key tile, head): loops over the query tiles (BQ rows each)
 // that see the key tile, computes S^T = K Q^T and dP^T = V dO^T for
 // the tile, and accumulates dV += P^T dO and dK += dS^T Q in registers
-// (rows of keys ty + 16 r). Unless `with_dq` is 0 it also adds this key
-// tile's share scale * dS K into dQ with fp32 atomics. SPLIT: scores from
-// split rows (K split, Q whole and split), else by Dot2; with `with_dq` the
-// split rows' K is also summed back into a whole copy for the dQ product.
+// (rows of keys ty + 16 r). With `with_dq` it also forms this key tile's
+// share scale * dS K of dQ: 1 adds it into dQ with fp32 atomics, 2 stores it
+// into the key tile's own partial array a.dQpart[key tile] (dQ itself when
+// there is one key tile), whose sum in key-tile order is dQ. SPLIT: scores
+// from split rows (K split, Q whole and split), else by Dot2; with `with_dq`
+// the split rows' K is also summed back into a whole copy for the dQ product.
 template <int W, int BQ, bool SPLIT>
 __global__ void __launch_bounds__(NT, 1) dkdv_kernel(const BwdArgs a, int with_dq) {
   constexpr int LD = W + 4, LDP = BQ + 4, NC = BQ / 16, NQ = W / 16;
@@ -827,22 +829,34 @@ __global__ void __launch_bounds__(NT, 1) dkdv_kernel(const BwdArgs a, int with_d
             }
         }
       }
-      const bool vec = (d & 3) == 0 && (reinterpret_cast<uintptr_t>(a.dQ) & 15u) == 0;
+      float* dst = with_dq == 1 || a.dq_splits <= 1
+                       ? a.dQ
+                       : a.dQpart + static_cast<size_t>(blockIdx.x) * p.B * p.H * Tq * d;
+      const bool vec = (d & 3) == 0 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
 #pragma unroll
       for (int r = 0; r < RQ; ++r) {
         const int qi = q0 + ty + 16 * r;
         if (qi >= Tq) continue;
-        float* row = a.dQ + (bh * Tq + qi) * d;
+        float* row = dst + (bh * Tq + qi) * d;
 #pragma unroll
         for (int g = 0; g < NQ / 4; ++g) {
           const int c = 64 * g + 4 * tx;
+          const float4 v = make_float4(t[r][4 * g] * scale, t[r][4 * g + 1] * scale, t[r][4 * g + 2] * scale,
+                                       t[r][4 * g + 3] * scale);
           if (vec && c + 3 < d) {
-            red_add4(row + c, t[r][4 * g] * scale, t[r][4 * g + 1] * scale, t[r][4 * g + 2] * scale,
-                     t[r][4 * g + 3] * scale);
+            if (with_dq == 1)
+              red_add4(row + c, v.x, v.y, v.z, v.w);
+            else
+              *reinterpret_cast<float4*>(row + c) = v;
           } else {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              if (c + e < d) atomicAdd(row + c + e, t[r][4 * g + e] * scale);
+              if (c + e < d) {
+                if (with_dq == 1)
+                  atomicAdd(row + c + e, el(v, e));
+                else
+                  row[c + e] = el(v, e);
+              }
           }
         }
       }
@@ -1038,7 +1052,7 @@ cudaError_t bwd_launch(const LaunchBwd& la, const BwdArgs& b, bool kv, bool q, b
                              static_cast<int>(s1));
     if (e != cudaSuccess) return e;
     dim3 g1((p.Tk + BM - 1) / BM, p.B * p.H);
-    dkdv_kernel<W, RQ, SP><<<g1, NT, s1, la.stream>>>(b, la.deterministic ? 0 : 1);
+    dkdv_kernel<W, RQ, SP><<<g1, NT, s1, la.stream>>>(b, !la.deterministic ? 1 : f32_fused_dq(p.B, p.H, p.Tq, p.Tk, p.d) ? 2 : 0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (q) {
@@ -1097,11 +1111,12 @@ cudaError_t launch_bwd_f32(const LaunchBwd& a) {
     if (e != cudaSuccess) return e;
   }
   const bool kv = a.phase == 0 || a.phase == 2 || a.phase == 4;
-  const bool q = a.deterministic && (a.phase == 0 || a.phase == 2 || a.phase == 5);
-  // the sum of the dQ kernel's range partials (phase 3, as for bf16)
+  // (no dQ kernel where the dK/dV kernel writes the key tiles' partials)
+  const bool q = a.deterministic && !f32_fused_dq(p.B, p.H, p.Tq, p.Tk, p.d) && (a.phase == 0 || a.phase == 2 || a.phase == 5);
+  // the sum of the range partials (phase 3, as for bf16)
   const bool red = a.deterministic && a.dq_splits > 1 && (a.phase == 0 || a.phase == 3);
   if (!kv && !q && !red) return cudaSuccess;
-  if ((q || red) && a.dq_splits > 1 && a.dQpart == nullptr) return cudaErrorInvalidValue;
+  if ((q || red || (kv && a.deterministic)) && a.dq_splits > 1 && a.dQpart == nullptr) return cudaErrorInvalidValue;
   simt::BwdArgs b{static_cast<const float*>(a.Q), static_cast<const float*>(a.K), static_cast<const float*>(a.V),
                   static_cast<const float*>(a.dO), a.LSE, a.D, static_cast<float*>(a.dQ),
                   static_cast<float*>(a.dK), static_cast<float*>(a.dV), p,

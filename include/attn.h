@@ -174,8 +174,12 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int d, int
  * split order, so the result stays bitwise reproducible. bf16: the dQ kernel
  * runs one unit per 128-row query tile; when there are fewer such units than
  * 76 (half of a GB300's 152 SMs) and at least 8 key tiles, S ranges of at
- * least 4 key tiles each, at most 152 units in all, S <= 64. fp32: one unit
- * per 64-row query tile and ranges of 64-key tiles; S is the smallest count
+ * least 4 key tiles each, at most 152 units in all, S <= 64. fp32: with at
+ * most 64 key tiles of 64 keys and at most 1 GiB of partials (S x B*H*Tq*d*4
+ * bytes), every key tile is a range of its own (S = the number of key tiles):
+ * the dK/dV kernel writes each key tile's partial dQ (with one key tile, dQ
+ * itself) and no separate dQ pass runs. Otherwise the dQ pass runs one unit
+ * per 64-row query tile over ranges of 64-key tiles; S is the smallest count
  * whose time (the waves of units x S on 152 SMs, times the key tiles of a
  * range) is within 5 % of the best, at least two key tiles per range, S <=
  * 64. Rules of the shapes only, so that the workspace size needs no device:

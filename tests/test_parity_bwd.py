@@ -282,12 +282,16 @@ def test_bf16_split_dq_deterministic(shape, causal):
 
 
 F32_SPLIT_DQ_SHAPES = [  # B, H, Tq, Tk, d, dv: few 64-row query tiles, many 64-key tiles
+    # more than 64 key tiles: the dQ kernel over key ranges
     (1, 1, 1, 5000, 128, 128),     # one query row
+    (1, 2, 128, 8192, 128, 128),
+    (1, 1, 200, 6000, 64, 64),     # 64-key steps (rows of 64 columns)
+    # at most 64 key tiles: the dK/dV kernel writes one partial per key tile
     (1, 2, 128, 4096, 128, 128),
     (1, 1, 256, 3000, 64, 64),     # 64-key steps (rows of 64 columns)
-    (2, 1, 200, 2500, 40, 24),     # odd widths
+    (2, 1, 200, 2500, 40, 24),     # odd widths (scalar partial stores)
     (1, 1, 1300, 1100, 128, 128),  # Tq > Tk: causal query tiles see 1 ... all 18 key tiles
-    (1, 1, 100, 900, 200, 136),    # rows above 128 columns (compensated scores)
+    (1, 1, 100, 900, 200, 136),    # rows above 128 columns (compensated scores, K whole in shared memory)
 ]
 
 
@@ -295,9 +299,10 @@ F32_SPLIT_DQ_SHAPES = [  # B, H, Tq, Tk, d, dv: few 64-row query tiles, many 64-
 @pytest.mark.parametrize("shape", F32_SPLIT_DQ_SHAPES)
 def test_f32_split_dq_deterministic(shape, causal):
     """The fp32 deterministic backward with dQ split over ranges of 64-key
-    tiles (partials added in range order): parity with the oracle at the fp32
-    bounds, bitwise equal across two runs, and equal to the atomic mode up to
-    fp32 rounding order."""
+    tiles (partials added in range order), from the dQ kernel or, with at
+    most 64 key tiles, from the dK/dV kernel (a range per key tile): parity
+    with the oracle at the fp32 bounds, bitwise equal across two runs, and
+    equal to the atomic mode up to fp32 rounding order."""
     B, H, Tq, Tk, d, dv = shape
     assert pkg.attn_bwd_dq_splits(B, H, Tq, Tk, d, dv, pkg.ATTN_F32, 1) > 1
     x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, dv), seed=Tq + Tk + d, device=DEV)
