@@ -182,9 +182,8 @@ struct BwdLayout {
 // split into ranges so that at most 152 units run (one wave), each with at
 // least 4 key tiles; at most 64 splits. A rule of the shapes only, so the workspace size
 // needs no device.
-// fp32: with at most 64 key tiles of 64 keys and 1 GiB of partials
-// (f32_fused_dq) every key tile is a range of its own, whose partial dQ the
-// dK/dV kernel writes; otherwise
+// fp32: with at most 1 GiB of partials (f32_fused_dq) every 64-key tile is
+// a range of its own, whose partial dQ the dK/dV kernel writes; otherwise
 // the fp32 dQ kernel (one CTA per 64-row query tile) splits its units over
 // ranges of 64-key tiles by the wave model of wave_splits on 152 SMs, also a
 // rule of the shapes only.

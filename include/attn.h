@@ -175,8 +175,8 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int H, int Tq, int Tk, int d, int
  * runs one unit per 128-row query tile; when there are fewer such units than
  * 76 (half of a GB300's 152 SMs) and at least 8 key tiles, S ranges of at
  * least 4 key tiles each, at most 152 units in all, S <= 64. fp32: with at
- * most 64 key tiles of 64 keys and at most 1 GiB of partials (S x B*H*Tq*d*4
- * bytes), every key tile is a range of its own (S = the number of key tiles):
+ * most 1 GiB of partials (S x B*H*Tq*d*4 bytes for S the number of 64-key
+ * tiles), every key tile is a range of its own (S = the number of key tiles):
  * the dK/dV kernel writes each key tile's partial dQ (with one key tile, dQ
  * itself) and no separate dQ pass runs. Otherwise the dQ pass runs one unit
  * per 64-row query tile over ranges of 64-key tiles; S is the smallest count

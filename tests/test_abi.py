@@ -123,18 +123,19 @@ def test_dq_split_rule(lib, shape, det, want):
 @pytest.mark.parametrize("shape,det,want", [
     ((2, 8, 1000, 4000, 128), 1, 63),    # c4: 63 key tiles, 516 MB of partials: one per key tile (dK/dV kernel)
     ((2, 8, 1000, 4000, 128), 0, 1),     # atomic dQ never splits
-    ((1, 8, 256, 65536, 128), 1, 14),    # 1024 key tiles: the dQ kernel, 14 ranges of 74 key tiles (three waves)
+    ((1, 8, 256, 65536, 128), 1, 1024),  # s1f: 1024 key tiles, exactly 1 GiB of partials
     ((1, 1, 128, 200, 64), 1, 4),        # 4 key tiles: one partial each
     ((1, 1, 128, 192, 64), 1, 3),
     ((1, 1, 100, 50, 64), 1, 1),         # one key tile: the dK/dV kernel writes dQ itself
-    ((2, 16, 8192, 8192, 128), 1, 1),    # 128 key tiles, 4096 query tiles fill the SMs: the dQ kernel, unsplit
-    ((4, 16, 8192, 4096, 128), 1, 1),    # 64 key tiles but 17 GB of partials: the dQ kernel, unsplit
-    ((1, 2, 128, 8192, 128), 1, 32),     # 128 key tiles, 4 query tiles: the dQ kernel, 32 ranges of 4
+    ((1, 2, 128, 8192, 128), 1, 128),
+    ((2, 16, 8192, 8192, 128), 1, 1),    # 16 GiB of partials: the dQ kernel; 4096 query tiles fill the SMs
+    ((4, 16, 8192, 4096, 128), 1, 1),
+    ((1, 8, 512, 65536, 128), 1, 7),     # 2 GiB of partials, 64 query tiles: the dQ kernel, 7 ranges
 ])
 def test_dq_split_rule_fp32(lib, shape, det, want):
-    """fp32 deterministic dQ. With at most 64 key tiles of 64 keys and at
-    most 1 GiB of partials, every key tile is its own range: the dK/dV kernel
-    writes its partial dQ, and the partials are added in key-tile order.
+    """fp32 deterministic dQ. With at most 1 GiB of partials (one per 64-key
+    tile), every key tile is its own range: the dK/dV kernel writes its
+    partial dQ, and the partials are added in key-tile order.
     Otherwise the dQ kernel splits its 64-row query tiles over ranges of
     64-key tiles: the smallest count whose waves of units x ranges on 152
     SMs, times the key tiles of a range, come within 5 % of the best count."""

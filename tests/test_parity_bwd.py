@@ -281,13 +281,9 @@ def test_bf16_split_dq_deterministic(shape, causal):
     assert (dq1.float() - dqa.float()).norm() <= 1e-2 * dqa.float().norm() + 1e-5
 
 
-F32_SPLIT_DQ_SHAPES = [  # B, H, Tq, Tk, d, dv: few 64-row query tiles, many 64-key tiles
-    # more than 64 key tiles: the dQ kernel over key ranges
-    (1, 1, 1, 5000, 128, 128),     # one query row
-    (1, 2, 128, 8192, 128, 128),
-    (1, 1, 200, 6000, 64, 64),     # 64-key steps (rows of 64 columns)
-    # at most 64 key tiles: the dK/dV kernel writes one partial per key tile
-    (1, 2, 128, 4096, 128, 128),
+F32_SPLIT_DQ_SHAPES = [  # B, H, Tq, Tk, d, dv: a dQ partial per 64-key tile from the dK/dV kernel
+    (1, 1, 1, 5000, 128, 128),     # one query row, 79 key tiles
+    (1, 2, 128, 8192, 128, 128),   # 128 key tiles
     (1, 1, 256, 3000, 64, 64),     # 64-key steps (rows of 64 columns)
     (2, 1, 200, 2500, 40, 24),     # odd widths (scalar partial stores)
     (1, 1, 1300, 1100, 128, 128),  # Tq > Tk: causal query tiles see 1 ... all 18 key tiles
@@ -298,11 +294,10 @@ F32_SPLIT_DQ_SHAPES = [  # B, H, Tq, Tk, d, dv: few 64-row query tiles, many 64-
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("shape", F32_SPLIT_DQ_SHAPES)
 def test_f32_split_dq_deterministic(shape, causal):
-    """The fp32 deterministic backward with dQ split over ranges of 64-key
-    tiles (partials added in range order), from the dQ kernel or, with at
-    most 64 key tiles, from the dK/dV kernel (a range per key tile): parity
-    with the oracle at the fp32 bounds, bitwise equal across two runs, and
-    equal to the atomic mode up to fp32 rounding order."""
+    """The fp32 deterministic backward with a dQ partial per 64-key tile,
+    written by the dK/dV kernel and added in key-tile order: parity with the
+    oracle at the fp32 bounds, bitwise equal across two runs, and equal to the
+    atomic mode up to fp32 rounding order."""
     B, H, Tq, Tk, d, dv = shape
     assert pkg.attn_bwd_dq_splits(B, H, Tq, Tk, d, dv, pkg.ATTN_F32, 1) > 1
     x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, dv), seed=Tq + Tk + d, device=DEV)
@@ -312,6 +307,29 @@ def test_f32_split_dq_deterministic(shape, causal):
     _, _, dq2, dk2, dv2 = run(x, causal, scale, 1)
     assert torch.equal(dq1, dq2) and torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
     _, _, dqa, _, _ = run(x, causal, scale, 0)
+    assert (dq1 - dqa).abs().max().item() <= 1e-5 * max(dqa.abs().max().item(), 1e-30) + 1e-7
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_f32_dq_kernel_ranges_above_the_partials_cap(causal):
+    """Above 1 GiB of per-key-tile partials the fp32 deterministic backward
+    runs the dQ kernel over key ranges (7 ranges of 147 key tiles here, 2 GiB
+    of partials otherwise). The shape is too large for the oracle, so the
+    path is held to the ones the oracle pins: bitwise equal across two runs,
+    dK and dV bitwise equal to the atomic mode's (the same dK/dV kernel and
+    order), dQ equal to the atomic mode's up to fp32 rounding order. The dQ
+    kernel's ranges themselves met the oracle before the partials moved into
+    the dK/dV kernel, and their code has not changed since."""
+    B, H, Tq, Tk, d = 1, 8, 512, 65536, 128
+    assert pkg.attn_bwd_dq_splits(B, H, Tq, Tk, d, d, pkg.ATTN_F32, 1) == 7
+    x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, d), seed=11 + causal, device=DEV)
+    scale = 1 / math.sqrt(d)
+    _, _, dq1, dk1, dv1 = run(x, causal, scale, 1)
+    _, _, dq2, dk2, dv2 = run(x, causal, scale, 1)
+    assert torch.equal(dq1, dq2) and torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    _, _, dqa, dka, dva = run(x, causal, scale, 0)
+    assert torch.equal(dk1, dka) and torch.equal(dv1, dva)
+    assert torch.isfinite(dq1).all()
     assert (dq1 - dqa).abs().max().item() <= 1e-5 * max(dqa.abs().max().item(), 1e-30) + 1e-7
 
 
