@@ -305,6 +305,15 @@ def run_reference(args, w):
     return 0
 
 
+def f32_dq_partials(f32: bool, det: bool, Tk: int, dq_splits: int) -> bool:
+    """True where the fp32 deterministic backward runs no dQ kernel: its
+    dK/dV kernel writes one dQ partial per 64-key tile (or dQ itself, with one
+    key tile), and the library reports one split per key tile. The dQ
+    kernel's own key ranges hold at least two key tiles each, so they never
+    reach that count."""
+    return bool(f32 and det and dq_splits == -(-Tk // 64))
+
+
 def workload_config(w):
     return {"workload": f"{w.name}: B={w.B} H={w.H} Tq={w.Tq} Tk={w.Tk} d={w.d} dv={w.dv} {w.dtype} "
                         f"{'causal' if w.causal else 'no mask'}, scale={w.softmax_scale:.6g}",
@@ -384,10 +393,7 @@ def run_ours(args, w):
     # launches nothing for this configuration (the library's own rule, as in
     # attn_bwd_phase) is not called, so that no event interval of the timed
     # step is an empty one.
-    # fp32 deterministic with few key tiles: the dK/dV kernel writes one dQ
-    # partial per 64-key tile and no dQ kernel runs (the library reports one
-    # split per key tile then; its dQ kernel's own splits are never that many)
-    f32_fused = f32 and bool(det) and dq_splits == -(-Tk // 64)
+    f32_fused = f32_dq_partials(f32, bool(det), Tk, dq_splits)
     launches = {1: f32 or (not det and w.d <= 128), 5: (bool(det) and not f32_fused) or w.d > 128, 6: bool(det), 4: True,
                 3: (not f32 and w.d <= 128 and (not det or dq_splits > 1)) or (f32 and bool(det) and dq_splits > 1)}
     phases = () if args.fwd_only else tuple(ph for ph in (1, 6 if args.dq_pairs else 5, 4, 3) if launches[ph])

@@ -211,3 +211,23 @@ def test_bench_functions_use_only_bound_names():
                 bound.add(n.name)
         used = {n.id for n in ast.walk(fn) if isinstance(n, ast.Name) and isinstance(n.ctx, ast.Load)}
         assert not (used - bound - module), f"{fn.name} reads unbound names {sorted(used - bound - module)}"
+
+
+@pytest.mark.parametrize("name", ["c1", "c1_causal", "c4", "c4_scale1", "s1f"])
+def test_f32_dq_partials_matches_the_library_rule(name):
+    """bench.py's reading of the library's split count (one split per
+    64-key tile means the dK/dV kernel writes the dQ partials and no dQ
+    kernel runs) agrees with the rule the library states: at most 1 GiB of
+    partials, one fp32 [B,H,Tq,d] array per key tile."""
+    from exact_tiled_softmax_attn_gb300 import binding as Bn
+    from exact_tiled_softmax_attn_gb300 import build as build_mod
+    build_mod.build()   # host-side calls only: no device is touched
+    w = WORKLOADS[name]
+    for det in (0, 1):
+        S = Bn.attn_bwd_dq_splits(w.B, w.H, w.Tq, w.Tk, w.d, w.dv, Bn.ATTN_F32, det)
+        n_kt = -(-w.Tk // 64)
+        want = bool(det) and (n_kt == 1 or n_kt * w.B * w.H * w.Tq * w.d * 4 <= 2 ** 30)
+        assert bench.f32_dq_partials(True, bool(det), w.Tk, S) == want
+    # above the cap the dQ kernel's ranges hold at least two key tiles each
+    S = Bn.attn_bwd_dq_splits(1, 8, 512, 65536, 128, 128, Bn.ATTN_F32, 1)
+    assert S > 1 and not bench.f32_dq_partials(True, True, 65536, S)
