@@ -699,6 +699,7 @@ __global__ void __launch_bounds__(NT, 1) dkdv_kernel(const BwdArgs a, int with_d
   float* sLse = sdSt + BM * LDP;  // [BQ]
   float* sD = sLse + BQ;          // [BQ]
   float* sKf = sD + BQ;           // [BM][LD] split rows: K whole (coarse part + remainder), for the dQ product
+  float* sdS = sKf + (SPLIT ? BM * LD : 0);   // [BQ][BM + 4] dS with query rows, for the dQ product
   const Problem& p = a.p;
   const int d = p.d, dv = p.dv, Tq = p.Tq, Tk = p.Tk;
   const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
@@ -785,6 +786,7 @@ __global__ void __launch_bounds__(NT, 1) dkdv_kernel(const BwdArgs a, int with_d
           p_ds(sh[r][c], sl[r][c], dp[r][c], scale, lse, sD[i], blocked, pij, dsij);
           sPt[(ty + 16 * r) * LDP + i] = pij;
           sdSt[(ty + 16 * r) * LDP + i] = dsij;
+          if (with_dq) sdS[i * (BM + 4) + ty + 16 * r] = dsij;
         }
       }
     }
@@ -797,11 +799,8 @@ __global__ void __launch_bounds__(NT, 1) dkdv_kernel(const BwdArgs a, int with_d
     acc_tile<4, NQ>(sPt, LDP, sdO, LD, ty, tx, nq, accV);
     acc_tile<4, NQ>(sdSt, LDP, sQ, LD, ty, tx, nq, accK);
     if (with_dq) {
-      // dQ_i += scale * sum_j dS_ij K_j, rows of queries ty + 16 r: two
-      // adjacent columns per two-lane FMA with dS_ij broadcast to both lanes
-      // (the transposed dS: entry (query ty + 16 r, key k) sits at
-      // sdSt[k][ty + 16 r]); each row's four adjacent columns 64 g + 4 tx ..
-      // go out in one vector reduction where the rows are 16-byte aligned
+      // dQ_i += scale * sum_j dS_ij K_j, rows of queries ty + 16 r: a P V-shaped
+      // product of the query-major dS tile and the whole K tile
       constexpr int RQ = BQ / 16;
       const float* kf = SPLIT ? sKf : sK;
       float t[RQ][NQ];
@@ -809,26 +808,7 @@ __global__ void __launch_bounds__(NT, 1) dkdv_kernel(const BwdArgs a, int with_d
       for (int r = 0; r < RQ; ++r)
 #pragma unroll
         for (int q = 0; q < NQ; ++q) t[r][q] = 0.f;
-      const int nk = min(BM, Tk - kv0);
-#pragma unroll 4
-      for (int k = 0; k < nk; ++k) {
-        float4 b[NQ / 4];
-#pragma unroll
-        for (int g = 0; g < NQ / 4; ++g) b[g] = ld4(kf + k * LD + 64 * g + 4 * tx);
-#pragma unroll
-        for (int r = 0; r < RQ; ++r) {
-          const float x = sdSt[k * LDP + ty + 16 * r];
-          const float2 xr = make_float2(x, x);
-#pragma unroll
-          for (int g = 0; g < NQ / 4; ++g)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const float2 u = fma2(xr, pair(b[g], h), make_float2(t[r][4 * g + 2 * h], t[r][4 * g + 2 * h + 1]));
-              t[r][4 * g + 2 * h] = u.x;
-              t[r][4 * g + 2 * h + 1] = u.y;
-            }
-        }
-      }
+      acc_tile<RQ, NQ>(sdS, BM + 4, kf, LD, ty, tx, min(BM, Tk - kv0), t);
       float* dst = with_dq == 1 || a.dq_splits <= 1
                        ? a.dQ
                        : a.dQpart + static_cast<size_t>(blockIdx.x) * p.B * p.H * Tq * d;
@@ -1021,7 +1001,8 @@ template <int W, bool SPLIT>
 constexpr size_t dkdv_smem_of() {
   constexpr int BQ = dkdv_rows<W>();
   // (split rows: one more [BM][W + 4] tile, the whole K for the atomic dQ product)
-  return sizeof(float) * ((SPLIT ? 4 : 2) * BM * (W + 4) + (SPLIT ? 4 : 2) * BQ * (W + 4) + 2 * BM * (BQ + 4) + 2 * BQ);
+  return sizeof(float) * ((SPLIT ? 4 : 2) * BM * (W + 4) + (SPLIT ? 4 : 2) * BQ * (W + 4) + 2 * BM * (BQ + 4) + 2 * BQ +
+                          BQ * (BM + 4));
 }
 // split rows wherever their tiles fit
 template <int W>
