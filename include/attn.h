@@ -197,9 +197,12 @@ ATTN_API int attn_bwd_dq_splits(int B, int H, int Tq, int Tk, int d, int dv, att
  * D = rowsum(dO o O), and accumulates the per-tile gradient terms of
  * "attention_backprop" (sections "Gradient of V and P" through "Gradient of
  * Q and K"). `O` and `LSE` must be the outputs of attn_fwd on the same
- * inputs, scale and mask. deterministic = 1 computes dQ in a separate pass
- * that sums key tiles in a fixed order (bitwise reproducible); 0 adds each
- * key tile's share with fp32 atomics. For bf16 rows of 256 columns both
+ * inputs, scale and mask. deterministic = 1 sums the key tiles' shares of
+ * dQ in a fixed order (bitwise reproducible): bf16 in a separate dQ pass;
+ * fp32 from one partial per 64-key tile that the dK/dV pass writes, added in
+ * key-tile order, or, above 1 GiB of such partials, in a separate dQ pass
+ * (attn_bwd_dq_splits). 0 adds each key tile's share with fp32 atomics. For
+ * bf16 rows of 256 columns both
  * values run the fixed-order pass: there a dQ kernel, a dV kernel and a dK
  * kernel each hold one 256-column accumulator (tensor memory has room for
  * one next to the score tiles), all bitwise reproducible. `workspace` (256-byte aligned, at least
