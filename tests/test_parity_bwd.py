@@ -52,7 +52,8 @@ def test_f32_c1(name, deterministic):
 
 
 F32_SHAPES = [(1, 1, 1, 1, 1, 1), (2, 3, 77, 133, 40, 24), (1, 2, 200, 65, 128, 128), (1, 1, 33, 300, 7, 128),
-              (1, 2, 100, 150, 256, 256), (1, 1, 70, 90, 200, 136)]   # head sizes above 128
+              (1, 2, 100, 150, 256, 256), (1, 1, 70, 90, 200, 136),   # head sizes above 128
+              (2, 3, 150, 64, 128, 128)]   # one 64-key tile: the deterministic dK/dV kernel writes dQ itself
 
 
 @pytest.mark.parametrize("deterministic", [0, 1])
