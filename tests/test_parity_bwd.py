@@ -297,8 +297,9 @@ F32_SPLIT_DQ_SHAPES = [  # B, H, Tq, Tk, d, dv: a dQ partial per 64-key tile fro
 def test_f32_split_dq_deterministic(shape, causal):
     """The fp32 deterministic backward with a dQ partial per 64-key tile,
     written by the dK/dV kernel and added in key-tile order: parity with the
-    oracle at the fp32 bounds, bitwise equal across two runs, and equal to the
-    atomic mode up to fp32 rounding order."""
+    oracle at the fp32 bounds, bitwise equal across two runs, dK and dV
+    bitwise equal to the atomic mode's (the same kernel; only where the dQ
+    share goes differs), and dQ equal to it up to fp32 rounding order."""
     B, H, Tq, Tk, d, dv = shape
     assert pkg.attn_bwd_dq_splits(B, H, Tq, Tk, d, dv, pkg.ATTN_F32, 1) > 1
     x = make_random((B, H, Tq, d), (B, H, Tk, d), (B, H, Tk, dv), seed=Tq + Tk + d, device=DEV)
@@ -307,7 +308,8 @@ def test_f32_split_dq_deterministic(shape, causal):
     _, _, dq1, dk1, dv1 = run(x, causal, scale, 1)
     _, _, dq2, dk2, dv2 = run(x, causal, scale, 1)
     assert torch.equal(dq1, dq2) and torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
-    _, _, dqa, _, _ = run(x, causal, scale, 0)
+    _, _, dqa, dka, dva = run(x, causal, scale, 0)
+    assert torch.equal(dk1, dka) and torch.equal(dv1, dva)
     assert (dq1 - dqa).abs().max().item() <= 1e-5 * max(dqa.abs().max().item(), 1e-30) + 1e-7
 
 
