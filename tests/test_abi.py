@@ -148,6 +148,17 @@ def test_dq_split_rule_fp32(lib, shape, det, want):
     assert B.attn_bwd_workspace_size(B_, H, Tq, Tk, d, d, B.ATTN_F32, det) == 2 * part + partials
 
 
+def test_noalloc_refuses_fp32_partials_beyond_its_buffer(lib):
+    """The fp32 deterministic backward of c4 keeps 63 dQ partials (516 MB) in
+    its workspace, beyond the no-allocation entry point's fixed 64 MiB: it
+    refuses the call on the host, before any device work, as it does for any
+    problem beyond its buffer."""
+    args = (0x100000, 0x200000, 0x300000, 0x400000, 0x500000, 0x600000, 0x700000, 0x800000, 0x900000,
+            2, 8, 1000, 4000, 128, 128, 0.088, 0, B.ATTN_F32)
+    assert B.attn_bwd_workspace_size(2, 8, 1000, 4000, 128, 128, B.ATTN_F32, 1) > B.ATTN_NOALLOC_SCRATCH_BYTES
+    assert B.attn_bwd_noalloc(*args, 1, stream=0, check=False) == B.ATTN_ERR_WORKSPACE
+
+
 def test_workspace_size(lib):
     # -LSE*log2(e) and D, each [B*H, Tq rounded up to 128] fp32 and 256-byte
     # aligned, then (bf16 with fp32 dQ accumulation) the [B*H*Tq, d]
